@@ -1,0 +1,337 @@
+/*
+ * ssm_oracle.c -- plain, sequential fp64 CPU oracle for the selective-scan
+ * (S6) forward pass in its three forms: one direction, Vision Mamba's
+ * bidirectional v1/v2 (flip-add), and VMamba's SS2D four-way cross-scan.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file; only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg do.  It shares no source with the CUDA library.
+ *
+ * Every time-indexed step is written out the way the pages state it: no
+ * blocking, no fusion, no reordering.  Flips and cross-scan orders are
+ * materialised as explicit copies, exactly as the pages' Python does.
+ *
+ * Sources (page title, section):
+ *  - S6 recurrence h_t = A h_{t-1} + B x_t, y_t = C h_t + D x_t:
+ *    "状态空间模型如何重塑视觉序列处理" (Vision Mamba overview), section
+ *    "选择性扫描机制的计算效率优势".  Its operators are stripped in the text;
+ *    the discretisation taken is zero-order hold for A (Abar = exp(delta*A))
+ *    and Euler for B (Bbar = delta*B), the standard Mamba reading.
+ *  - delta = softplus(dt_proj(x)), bias inside the softplus:
+ *    "VMamba的SS2D模块详解", section 3.1 (动态参数生成);
+ *    "Vision Mamba实战", section 4 (数值稳定性).
+ *  - A = -exp(A_log): "VMamba的SS2D模块详解", section 3.2.
+ *  - Tensor shapes A/A_b [d_inner,d_state], B/C [batch,d_state,seq_len],
+ *    D/D_b [d_inner]: "Vision Mamba实战", section 1 (parameter table).
+ *  - bidirectional scan (flip inputs, scan with A_b, flip back, add):
+ *    "Vision Mamba实战", section 2.2 (bidirectional_scan).
+ *  - v1 shares everything except A/A_b; v2 has an independent second set:
+ *    "从Transformer到Mamba", section 2.1; "Vision Mamba实战", section 1.
+ *  - averaged fusion (out_f + flip(out_b)) / 2 for v2, plain sum as the other
+ *    fusion: "从Transformer到Mamba", sections 2.2 and 4.3.
+ *  - gate y * act(z) with act = SiLU: "VMamba的SS2D模块详解", section 2.1.
+ *  - cross-scan [flatten, transpose-flatten, flip, flip(transpose-flatten)]
+ *    of X in R^{B x D x H x W}: "VMamba的SS2D模块详解", section 2.2.
+ *
+ * Readings where the pages are silent: h_0 = 0 in every direction; the
+ * backward branch reverses every time-indexed input (u, delta, B, C) although
+ * the printed bidirectional_scan only shows x and delta being flipped; the
+ * SS2D cross-merge is the plain sum of the four directions mapped back to
+ * H x W, followed by the gate; softplus is log(1 + e^x) with no threshold.
+ *
+ * Layouts (row-major, contiguous):
+ *   u, delta, z, y       [B, D, L]          (bidirectional: original order)
+ *   A, A_b               [D, N]
+ *   Bm, Cm (and _b)      [B, N, L]
+ *   Dskip, D_b, bias     [D]
+ *   SS2D: x, z, y        [B, D, H, W];  delta [B, K, D, L];  A [K, D, N];
+ *         Bm, Cm [B, K, N, L] in each direction's scan order;
+ *         Dskip, bias [K, D].
+ * Nullable: Dskip/D_b (-> 0), z (-> no gate), bias (-> 0), u_b (-> u).
+ * All functions return 0 on success and -1 on a bad argument or failed
+ * allocation.
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* softplus(x) = log(1 + e^x).  Both branches are the same function, written
+ * so that exp never overflows. */
+static double softplus(double x)
+{
+    if (x > 0.0)
+        return x + log1p(exp(-x));
+    return log1p(exp(x));
+}
+
+/* gate: y * silu(z) = y * z * sigmoid(z) */
+static double gate(double y, double z)
+{
+    return y * (z / (1.0 + exp(-z)));
+}
+
+/*
+ * One direction over one sequence, in the order the arrays are given.
+ *   delta_t = softplus(dt_t + bias)            (or dt_t + bias)
+ *   h_t[n]  = exp(delta_t * A[n]) * h_{t-1}[n] + delta_t * B[n][t] * u_t
+ *   y_t     = sum_n C[n][t] * h_t[n] + Dd * u_t
+ * Bm and Cm are [N][L] for this sequence.  h is caller scratch of N doubles.
+ */
+static void scan_sequence(int L, int N, const double *u, const double *dt,
+                          const double *A, const double *Bm, const double *Cm,
+                          double Dd, double bias, int delta_softplus,
+                          double *y, double *h)
+{
+    for (int n = 0; n < N; ++n)
+        h[n] = 0.0;
+    for (int t = 0; t < L; ++t) {
+        double delta = dt[t] + bias;
+        if (delta_softplus)
+            delta = softplus(delta);
+        double acc = 0.0;
+        for (int n = 0; n < N; ++n) {
+            double dA = exp(delta * A[n]);
+            double dBu = delta * Bm[(size_t)n * L + t] * u[t];
+            h[n] = dA * h[n] + dBu;
+            acc += Cm[(size_t)n * L + t] * h[n];
+        }
+        y[t] = acc + Dd * u[t];
+    }
+}
+
+/* Copy of a length-L sequence in reverse order (torch.flip on the last dim). */
+static void flip_copy(int L, const double *src, double *dst)
+{
+    for (int t = 0; t < L; ++t)
+        dst[t] = src[L - 1 - t];
+}
+
+/* [N][L] block with every row reversed in time. */
+static void flip_rows_copy(int N, int L, const double *src, double *dst)
+{
+    for (int n = 0; n < N; ++n)
+        flip_copy(L, src + (size_t)n * L, dst + (size_t)n * L);
+}
+
+int oracle_selective_scan(int B, int D, int L, int N,
+                          const double *u, const double *delta,
+                          const double *A, const double *Bm, const double *Cm,
+                          const double *Dskip, const double *z,
+                          const double *delta_bias, int delta_softplus,
+                          double *y)
+{
+    if (B < 0 || D < 0 || L < 0 || N <= 0 || !u || !delta || !A || !Bm || !Cm || !y)
+        return -1;
+    double *h = (double *)malloc(sizeof(double) * (size_t)N);
+    if (!h)
+        return -1;
+    for (int b = 0; b < B; ++b) {
+        for (int d = 0; d < D; ++d) {
+            size_t row = ((size_t)b * D + d) * (size_t)L;
+            scan_sequence(L, N, u + row, delta + row, A + (size_t)d * N,
+                          Bm + (size_t)b * N * L, Cm + (size_t)b * N * L,
+                          Dskip ? Dskip[d] : 0.0,
+                          delta_bias ? delta_bias[d] : 0.0, delta_softplus,
+                          y + row, h);
+            if (z)
+                for (int t = 0; t < L; ++t)
+                    y[row + t] = gate(y[row + t], z[row + t]);
+        }
+    }
+    free(h);
+    return 0;
+}
+
+/*
+ * Bidirectional scan, general form covering v1 and v2.  The forward branch
+ * scans (u, delta, A, Bm, Cm, Dskip, bias) as given.  The backward branch
+ * builds flipped copies of (u_b, delta_b, Bm_b, Cm_b), scans them with
+ * (A_b, D_b, bias_b), and flips its output back.  Then
+ *   y_t = out_scale * (y_f[t] + y_b[t]),   then the gate.
+ */
+static int bidirectional(int B, int D, int L, int N,
+                         const double *u, const double *u_b,
+                         const double *delta, const double *delta_b,
+                         const double *A, const double *A_b,
+                         const double *Bm, const double *Cm,
+                         const double *Bm_b, const double *Cm_b,
+                         const double *Dskip, const double *D_b,
+                         const double *z, const double *bias,
+                         const double *bias_b, int delta_softplus,
+                         double out_scale, double *y)
+{
+    size_t Ls = (size_t)(L > 0 ? L : 1);
+    size_t NL = (size_t)N * Ls;
+    double *h = (double *)malloc(sizeof(double) * (size_t)N);
+    double *yf = (double *)malloc(sizeof(double) * Ls);
+    double *yb = (double *)malloc(sizeof(double) * Ls);
+    double *uf = (double *)malloc(sizeof(double) * Ls);
+    double *df = (double *)malloc(sizeof(double) * Ls);
+    double *Bf = (double *)malloc(sizeof(double) * NL);
+    double *Cf = (double *)malloc(sizeof(double) * NL);
+    int rc = 0;
+    if (!h || !yf || !yb || !uf || !df || !Bf || !Cf) {
+        rc = -1;
+        goto done;
+    }
+    for (int b = 0; b < B; ++b) {
+        /* the backward branch's B and C, reversed in time */
+        flip_rows_copy(N, L, Bm_b + (size_t)b * N * L, Bf);
+        flip_rows_copy(N, L, Cm_b + (size_t)b * N * L, Cf);
+        for (int d = 0; d < D; ++d) {
+            size_t row = ((size_t)b * D + d) * (size_t)L;
+            /* forward branch */
+            scan_sequence(L, N, u + row, delta + row, A + (size_t)d * N,
+                          Bm + (size_t)b * N * L, Cm + (size_t)b * N * L,
+                          Dskip ? Dskip[d] : 0.0, bias ? bias[d] : 0.0,
+                          delta_softplus, yf, h);
+            /* backward branch: x.flip(-1), delta.flip(-1), scan with A_b */
+            flip_copy(L, u_b + row, uf);
+            flip_copy(L, delta_b + row, df);
+            scan_sequence(L, N, uf, df, A_b + (size_t)d * N, Bf, Cf,
+                          D_b ? D_b[d] : 0.0, bias_b ? bias_b[d] : 0.0,
+                          delta_softplus, yb, h);
+            /* flip the backward output back and fuse */
+            for (int t = 0; t < L; ++t) {
+                double v = out_scale * (yf[t] + yb[L - 1 - t]);
+                y[row + t] = z ? gate(v, z[row + t]) : v;
+            }
+        }
+    }
+done:
+    free(h);
+    free(yf);
+    free(yb);
+    free(uf);
+    free(df);
+    free(Bf);
+    free(Cf);
+    return rc;
+}
+
+/* v1: only A and A_b differ; delta, B, C, D and the bias are shared. */
+int oracle_bimamba_v1(int B, int D, int L, int N,
+                      const double *u, const double *delta,
+                      const double *A, const double *A_b,
+                      const double *Bm, const double *Cm,
+                      const double *Dskip, const double *z,
+                      const double *delta_bias, int delta_softplus,
+                      double out_scale, double *y)
+{
+    if (B < 0 || D < 0 || L < 0 || N <= 0 || !u || !delta || !A || !A_b || !Bm ||
+        !Cm || !y)
+        return -1;
+    return bidirectional(B, D, L, N, u, u, delta, delta, A, A_b, Bm, Cm, Bm, Cm,
+                         Dskip, Dskip, z, delta_bias, delta_bias,
+                         delta_softplus, out_scale, y);
+}
+
+/* v2: an independent backward set.  u_b == NULL means the backward branch
+ * scans the same u. */
+int oracle_bimamba_v2(int B, int D, int L, int N,
+                      const double *u, const double *u_b,
+                      const double *delta, const double *delta_b,
+                      const double *A, const double *A_b,
+                      const double *Bm, const double *Cm,
+                      const double *Bm_b, const double *Cm_b,
+                      const double *Dskip, const double *D_b,
+                      const double *z, const double *delta_bias,
+                      const double *delta_bias_b, int delta_softplus,
+                      double out_scale, double *y)
+{
+    if (B < 0 || D < 0 || L < 0 || N <= 0 || !u || !delta || !delta_b || !A ||
+        !A_b || !Bm || !Cm || !Bm_b || !Cm_b || !y)
+        return -1;
+    return bidirectional(B, D, L, N, u, u_b ? u_b : u, delta, delta_b, A, A_b,
+                         Bm, Cm, Bm_b, Cm_b, Dskip, D_b, z, delta_bias,
+                         delta_bias_b, delta_softplus, out_scale, y);
+}
+
+/*
+ * SS2D cross-scan order: the spatial index (h*W + w) visited at scan step t
+ * of direction k, for an H x W map (L = H*W):
+ *   k=0  X.flatten(2,3)                 row-major:    (t / W, t % W)
+ *   k=1  X.transpose(2,3).flatten(2,3)  column-major: (t % H, t / H)
+ *   k=2  flip of k=0                    k=0 at L-1-t
+ *   k=3  flip of k=1                    k=1 at L-1-t
+ * Returns -1 for an out-of-range argument.
+ */
+long oracle_cross_scan_index(int H, int W, int k, long t)
+{
+    long L = (long)H * (long)W;
+    if (H <= 0 || W <= 0 || t < 0 || t >= L || k < 0 || k > 3)
+        return -1;
+    long s = (k >= 2) ? (L - 1 - t) : t;
+    long hh, ww;
+    if (k == 0 || k == 2) {
+        hh = s / W;
+        ww = s % W;
+    } else {
+        hh = s % H;
+        ww = s / H;
+    }
+    return hh * W + ww;
+}
+
+/*
+ * SS2D with K = 4 directions.  For every (b, d): build xs_k (the image read in
+ * direction k's order), scan it with direction k's (delta_k, A_k, B_k, C_k,
+ * D_k, bias_k), scatter the result back to H x W and sum over k; then gate.
+ */
+int oracle_ss2d(int B, int D, int H, int W, int N, int K,
+                const double *x, const double *delta, const double *A,
+                const double *Bm, const double *Cm, const double *Dskip,
+                const double *z, const double *delta_bias, int delta_softplus,
+                double *y)
+{
+    if (B < 0 || D < 0 || H <= 0 || W <= 0 || N <= 0 || K != 4 || !x || !delta ||
+        !A || !Bm || !Cm || !y)
+        return -1;
+    int L = H * W;
+    long *order = (long *)malloc(sizeof(long) * (size_t)K * (size_t)L);
+    double *h = (double *)malloc(sizeof(double) * (size_t)N);
+    double *xs = (double *)malloc(sizeof(double) * (size_t)L);
+    double *ys = (double *)malloc(sizeof(double) * (size_t)L);
+    double *acc = (double *)malloc(sizeof(double) * (size_t)L);
+    int rc = 0;
+    if (!order || !h || !xs || !ys || !acc) {
+        rc = -1;
+        goto done;
+    }
+    for (int k = 0; k < K; ++k)
+        for (int t = 0; t < L; ++t)
+            order[(size_t)k * L + t] = oracle_cross_scan_index(H, W, k, t);
+    for (int b = 0; b < B; ++b) {
+        for (int d = 0; d < D; ++d) {
+            const double *img = x + ((size_t)b * D + d) * (size_t)L;
+            for (int p = 0; p < L; ++p)
+                acc[p] = 0.0;
+            for (int k = 0; k < K; ++k) {
+                const long *ord = order + (size_t)k * L;
+                for (int t = 0; t < L; ++t)
+                    xs[t] = img[ord[t]];
+                size_t drow = (((size_t)b * K + k) * D + d) * (size_t)L;
+                size_t bc = ((size_t)b * K + k) * (size_t)N * L;
+                size_t kd = (size_t)k * D + d;
+                scan_sequence(L, N, xs, delta + drow, A + kd * N, Bm + bc, Cm + bc,
+                              Dskip ? Dskip[kd] : 0.0,
+                              delta_bias ? delta_bias[kd] : 0.0, delta_softplus,
+                              ys, h);
+                /* cross-merge: back to H x W, summed over directions */
+                for (int t = 0; t < L; ++t)
+                    acc[ord[t]] += ys[t];
+            }
+            double *out = y + ((size_t)b * D + d) * (size_t)L;
+            const double *zz = z ? z + ((size_t)b * D + d) * (size_t)L : NULL;
+            for (int p = 0; p < L; ++p)
+                out[p] = zz ? gate(acc[p], zz[p]) : acc[p];
+        }
+    }
+done:
+    free(order);
+    free(h);
+    free(xs);
+    free(ys);
+    free(acc);
+    return rc;
+}
