@@ -1,0 +1,373 @@
+"""Benchmark of the selective-scan forward pass on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+A step is one full pass of the hot path (one call of the operation) over the
+workload's synthetic inputs, already resident in HBM.  The default workload
+is the Vim-S 1248x1248 bidirectional v2 scan: batch 8, d_inner 768,
+d_state 16, L = 78*78 + 1 = 6085, bf16 I/O with fp32 state.
+
+One JSON line is printed by rank 0.  `value` is the algorithmic HBM
+throughput (every I/O tensor read once, y written once) of the whole job in
+GB/s; `elem_updates_per_s` counts (direction, batch, channel, state, step)
+recurrence updates.  Inputs are larger than L2, so no flush is needed between
+steps.  Under torchrun every rank runs its own replica with its own seed
+(rows are independent: weak scaling, no collective on the data path).
+
+`--impl reference` times the fp64 CPU oracle (the reference of this
+repository) on a bounded sample of whole rows of the same workload, on the
+host cores, and prints the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "vim_s_1248_bimamba_v2"
+METRIC = "bi-dir selective-scan HBM GB/s (% of peak) and elem-updates/s, Vim-S 1248²"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), float(d.get("sm_max_mhz", 2032.0)), "measured"
+    return 6400.0, 2032.0, "fallback"
+
+
+# ---------------------------------------------------------------- GPU arm
+def launches_per_step(op):
+    return 2 if op == "ss2d" else 1
+
+
+def call(ssm, spec, g, ws, out):
+    sp = spec.delta_softplus
+    if spec.op == "single":
+        return ssm.selective_scan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"],
+                                      g["delta_bias"], sp, out=out, workspace=ws)
+    if spec.op == "v1":
+        return ssm.bimamba_scan_fwd_v1(g["u"], g["delta"], g["A"], g["A_b"], g["B"], g["C"],
+                                       g["D"], g["z"], g["delta_bias"], sp, g["out_scale"],
+                                       out=out, workspace=ws)
+    if spec.op == "v2":
+        return ssm.bimamba_scan_fwd_v2(g["u"], g["delta"], g["delta_b"], g["A"], g["A_b"], g["B"],
+                                       g["C"], g["B_b"], g["C_b"], g["D"], g["D_b"], g["z"],
+                                       g["delta_bias"], g["delta_bias_b"], g["u_b"], sp,
+                                       g["out_scale"], out=out, workspace=ws)
+    return ssm.ss2d_scan_fwd(g["x"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"],
+                             g["delta_bias"], sp, out=out, workspace=ws)
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        # "under load": samples at the upper half of the observed power range
+        if pw:
+            thr = min(pw) + 0.5 * (max(pw) - min(pw))
+            loaded = [num(r[1]) for r in rows if num(r[3]) is not None and num(r[3]) >= thr
+                      and num(r[1]) is not None]
+        else:
+            loaded = sm
+        return {"sm_mhz": statistics.median(loaded or sm), "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from selective_state_space_111_b300 import build
+    build.build()
+    import selective_state_space_111_b300 as ssm
+    from selective_state_space_111_b300.synth import WORKLOADS, make_inputs, seed_for
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    spec = WORKLOADS[args.workload]
+    t = make_inputs(spec, seed_for(args.workload) + rank)
+    g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in t.items()}
+    L = spec.seq_len
+    ws_n = ssm.workspace_bytes(spec.op, g["u" if spec.op != "ss2d" else "x"].dtype, spec.B,
+                               spec.D, L, spec.N, spec.K)
+    ws = torch.empty(max(ws_n, 1), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(g["x"] if spec.op == "ss2d" else g["u"])
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    for _ in range(args.warmup):
+        call(ssm, spec, g, ws, out)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(stream)
+    for i in range(args.steps):
+        call(ssm, spec, g, ws, out)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+
+    # e2e: host (pinned) inputs -> device -> the public API -> result to host
+    e2e = None
+    if not args.no_e2e:
+        host = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in t.items()}
+        h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        h2d = sum(v.numel() * v.element_size() for v in host.values() if isinstance(v, torch.Tensor))
+        d2h = h_out.numel() * h_out.element_size()
+        n_e2e = max(1, min(args.steps, 20))
+
+        def e2e_step():
+            gg = {k: (v.to(dev, non_blocking=True) if isinstance(v, torch.Tensor) else v)
+                  for k, v in host.items()}
+            y = call(ssm, spec, gg, ws, None)
+            h_out.copy_(y, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / n_e2e
+        if world > 1:
+            tt = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_ms = float(tt.item())
+        e2e = {"value": round(spec.algorithmic_bytes() * world / (e2e_ms * 1e-3) / 1e9, 3),
+               "unit": "GB/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": round(e2e_ms, 4)}
+
+    if rank == 0:
+        ms = total_ms / args.steps
+        hbm_peak, sm_max, peak_kind = peaks()
+        gbps = spec.algorithmic_bytes() * world / (ms * 1e-3) / 1e9
+        ups = spec.updates() * world / (ms * 1e-3)
+        # dominant kernel: the per-launch average over the timed region
+        kern_ms = statistics.mean(per) / launches_per_step(spec.op)
+        upd_launch = spec.updates() / launches_per_step(spec.op)
+        alu_peak = 148 * 128 * sm_max * 1e6 / 1e12          # FP32-pipe Tops/s
+        alu_ach = 4 * upd_launch / (kern_ms * 1e-3) / 1e12
+        line = {
+            "metric": METRIC,
+            "value": round(gbps, 2),
+            "unit": "GB/s",
+            "pct_of_hbm_peak": round(100 * gbps / hbm_peak, 2),
+            "elem_updates_per_s": float("%.4g" % ups),
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms, 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16" if spec.io == "bf16" else "f32",
+            "data": "synthetic (seeded; shapes and distributions of the pages' workloads)",
+            "config": {"workload": args.workload, "op": spec.op, "batch": spec.B,
+                       "d_inner": spec.D, "d_state": spec.N, "seq_len": L,
+                       "l2": "inputs larger than L2 (no flush)",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": {"bound": "alu", "achieved": round(alu_ach, 3), "peak": round(alu_peak, 2),
+                         "unit": "Tops/s (FP32 pipe, 4 ops per update)",
+                         "frac": round(alu_ach / alu_peak, 4), "traffic": args.traffic,
+                         "hbm_frac": round(spec.algorithmic_bytes() / (kern_ms * 1e-3) / 1e9
+                                           / hbm_peak, 4),
+                         "hbm_peak_gbs": hbm_peak, "peak_kind": peak_kind},
+            "gpu_launches": launches_per_step(spec.op) * args.steps,
+            "clocks": clocks,
+        }
+        if e2e:
+            line["e2e"] = e2e
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(spec, args.workload, args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- CPU oracle
+def cpu_baseline(spec, name, seconds):
+    """The fp64 oracle, as it stands, over a bounded sample of whole rows of
+    the workload, rows spread over the host cores (one oracle call per row)."""
+    import numpy as np
+
+    import oracle
+    from selective_state_space_111_b300.synth import make_inputs, seed_for
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from cases import row_slice, run_oracle
+
+    cores = len(os.sched_getaffinity(0))
+    t = make_inputs(spec, seed_for(name))
+    oracle.build()
+    rng = np.random.default_rng(0)
+    rows = [(int(rng.integers(spec.B)), int(rng.integers(spec.D))) for _ in range(100000)]
+    slices = {}
+    done = [0]
+    lock = threading.Lock()
+    deadline = time.perf_counter() + seconds
+
+    def worker(k):
+        i = k
+        while time.perf_counter() < deadline and i < len(rows):
+            b, d = rows[i]
+            run_oracle(spec, row_slice(spec, t, b, d))
+            with lock:
+                done[0] += 1
+            i += cores
+        return
+
+    t0 = time.perf_counter()
+    th = [threading.Thread(target=worker, args=(k,)) for k in range(cores)]
+    for x in th:
+        x.start()
+    for x in th:
+        x.join()
+    el = time.perf_counter() - t0
+    per_row_updates = spec.updates() // (spec.B * spec.D)
+    per_row_bytes = spec.algorithmic_bytes() / (spec.B * spec.D)
+    ups = done[0] * per_row_updates / el
+    del slices
+    return {"value": round(done[0] * per_row_bytes / el / 1e9, 6), "unit": "GB/s",
+            "elem_updates_per_s": float("%.4g" % ups), "cores": cores, "kind": "oracle",
+            "sample": "%d whole rows (both directions, L=%d) of %s in %.1f s, one row per "
+                      "oracle call, %d threads" % (done[0], spec.seq_len, name, el, cores)}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from selective_state_space_111_b300.synth import WORKLOADS
+    spec = WORKLOADS[args.workload]
+    vals = []
+    t_all = time.perf_counter()
+    per_step = max(2.0, args.cpu_seconds / max(1, args.steps))
+    for i in range(args.warmup + args.steps):
+        cb = cpu_baseline(spec, args.workload, per_step if i >= args.warmup else 1.0)
+        if i >= args.warmup:
+            vals.append(cb)
+    v = statistics.mean(c["value"] for c in vals)
+    ups = statistics.mean(c["elem_updates_per_s"] for c in vals)
+    ms = spec.algorithmic_bytes() / (v * 1e9) * 1e3 if v > 0 else None
+    line = {"metric": METRIC, "value": v, "unit": "GB/s", "impl": "reference",
+            "elem_updates_per_s": ups, "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": args.workload, "op": spec.op, "batch": spec.B,
+                       "d_inner": spec.D, "d_state": spec.N, "seq_len": spec.seq_len},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "kind": "oracle",
+                             "cores": vals[0]["cores"], "sample": vals[-1]["sample"]},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": round(time.perf_counter() - t_all, 1)}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch of the dominant kernel from an ncu capture")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,170 @@
+/*
+ * ssm_scan.h -- C ABI of the B300 (sm_103a) selective-scan library.
+ *
+ * The library computes the Mamba selective scan (S6) forward pass in three
+ * forms: one direction, Vision Mamba's bidirectional v1/v2 with flip-add
+ * fusion, and VMamba's SS2D four-way cross-scan with cross-merge.  Every step
+ * runs in the library's own CUDA kernels; there is no host fallback.
+ *
+ * Per (batch b, channel d, state n) and time t, with h_{-1} = 0:
+ *   delta_t = softplus(dt_t + delta_bias[d])   (dt_t + delta_bias[d] if
+ *                                               delta_softplus == 0)
+ *   h_t[n]  = exp(delta_t * A[d,n]) * h_{t-1}[n] + delta_t * B[n,t] * u_t
+ *   y_t     = sum_n C[n,t] * h_t[n] + Dskip[d] * u_t
+ * and the output is gated, y_t * silu(z_t), when z is given.
+ * Sources: the S6 equations in "状态空间模型如何重塑视觉序列处理" (Vision Mamba
+ * overview), section "选择性扫描机制的计算效率优势" (discretisation read as
+ * exp(delta*A) for A and delta*B for B); delta = softplus(dt_proj(x)) and
+ * A = -exp(A_log) in "VMamba的SS2D模块详解", sections 3.1 and 3.2; the
+ * tensor shapes in "Vision Mamba实战", section 1.
+ *
+ * Common conventions
+ *  - All tensor pointers are DEVICE pointers to contiguous, caller-owned
+ *    memory.  I/O tensors (u, delta, B, C, z, y and the per-branch copies)
+ *    use the dtype `dt` (fp32 or bf16); A, Dskip and delta_bias are fp32.
+ *  - Every I/O tensor must start on a 16-byte boundary (as cudaMalloc and
+ *    PyTorch allocations do); the fp32 parameters on a 4-byte boundary.
+ *  - Optional pointers may be NULL: Dskip -> 0, z -> no gate,
+ *    delta_bias -> 0 (and u_b -> u for v2).
+ *  - `y` must not alias any input.  State and arithmetic are fp32; bf16
+ *    outputs are rounded to nearest even.
+ *  - `workspace` is device memory of at least ssm_workspace_bytes(...)
+ *    bytes for the same arguments (NULL is fine when that is 0).  Its
+ *    contents need no initialisation and are garbage afterwards.  Two calls
+ *    in flight at once must not share a workspace.
+ *  - Calls are asynchronous on `stream` (0 = the legacy default stream).
+ *    The library allocates nothing and keeps no global state.
+ *  - Errors: SSM_ERR_INVALID_ARG for a bad size, NULL required pointer or
+ *    misaligned pointer; SSM_ERR_UNSUPPORTED for N > 16, K != 4 or sizes
+ *    beyond the 32-bit index range; SSM_ERR_WORKSPACE when ws_bytes is too
+ *    small; SSM_ERR_CUDA when a launch fails (cudaGetLastError is consumed).
+ *    Every check happens before any launch: an error means nothing ran.
+ *  - A call with B == 0, D == 0 or L == 0 is valid and launches nothing.
+ */
+#ifndef SSM_SCAN_H
+#define SSM_SCAN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SSM_API __attribute__((visibility("default")))
+#else
+#define SSM_API
+#endif
+
+typedef struct CUstream_st *ssm_stream_t; /* same type as cudaStream_t */
+
+typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
+
+typedef enum {
+    SSM_OK = 0,
+    SSM_ERR_INVALID_ARG = 1,
+    SSM_ERR_UNSUPPORTED = 2,
+    SSM_ERR_CUDA = 3,
+    SSM_ERR_WORKSPACE = 4
+} ssm_status;
+
+typedef enum {
+    SSM_OP_SELECTIVE_SCAN = 0,
+    SSM_OP_BIMAMBA_V1 = 1,
+    SSM_OP_BIMAMBA_V2 = 2,
+    SSM_OP_SS2D = 3
+} ssm_op;
+
+/*
+ * One direction.
+ *   u, delta, z, y : [B, D, L]      A : [D, N]      Bm, Cm : [B, N, L]
+ *   Dskip, delta_bias : [D]
+ */
+SSM_API ssm_status selective_scan_fwd(ssm_dtype dt, int B, int D, int L, int N,
+                              const void *u, const void *delta, const float *A,
+                              const void *Bm, const void *Cm,
+                              const float *Dskip, const void *z,
+                              const float *delta_bias, int delta_softplus,
+                              void *y, void *workspace, size_t ws_bytes,
+                              ssm_stream_t stream);
+
+/*
+ * BiMamba v1 ("从Transformer到Mamba" section 2.1; "Vision Mamba实战"
+ * sections 1 and 2.2): delta, B, C, Dskip and delta_bias are shared by the
+ * two branches; only A (forward) and A_b (backward) differ.  The backward
+ * branch scans the sequence reversed in time, and its output is flipped
+ * back before the fusion
+ *   y_t = out_scale * (y_fwd[t] + y_bwd[t]),   then the gate.
+ * (out_scale = 1 is the plain flip-add of the pages; 0.5 averages.)
+ * Every tensor is in ORIGINAL token order; the kernel reads the backward
+ * branch reversed.  Shapes as selective_scan_fwd, A_b : [D, N].
+ */
+SSM_API ssm_status bimamba_scan_fwd_v1(ssm_dtype dt, int B, int D, int L, int N,
+                               const void *u, const void *delta,
+                               const float *A, const float *A_b,
+                               const void *Bm, const void *Cm,
+                               const float *Dskip, const void *z,
+                               const float *delta_bias, int delta_softplus,
+                               float out_scale, void *y, void *workspace,
+                               size_t ws_bytes, ssm_stream_t stream);
+
+/*
+ * BiMamba v2 ("从Transformer到Mamba" sections 2.1, 2.2 and 4.3): the
+ * backward branch has its own delta_b, A_b, Bm_b, Cm_b, D_b and
+ * delta_bias_b (and u_b when its input differs; NULL means it scans u).
+ * Fusion as v1; the pages' v2 averages, i.e. out_scale = 0.5.  All tensors
+ * in ORIGINAL token order.  Shapes as v1; delta_b, u_b : [B, D, L];
+ * Bm_b, Cm_b : [B, N, L]; D_b, delta_bias_b : [D].
+ */
+SSM_API ssm_status bimamba_scan_fwd_v2(ssm_dtype dt, int B, int D, int L, int N,
+                               const void *u, const void *u_b,
+                               const void *delta, const void *delta_b,
+                               const float *A, const float *A_b,
+                               const void *Bm, const void *Cm,
+                               const void *Bm_b, const void *Cm_b,
+                               const float *Dskip, const float *D_b,
+                               const void *z, const float *delta_bias,
+                               const float *delta_bias_b, int delta_softplus,
+                               float out_scale, void *y, void *workspace,
+                               size_t ws_bytes, ssm_stream_t stream);
+
+/*
+ * VMamba SS2D ("VMamba的SS2D模块详解" sections 2.1, 2.2 and 3.1), K = 4.
+ * Direction k scans the H x W map in order
+ *   k=0 row-major, k=1 column-major, k=2 row-major reversed,
+ *   k=3 column-major reversed,
+ * with its own delta_k, A_k, B_k, C_k, D_k and delta_bias_k.  The four
+ * outputs are mapped back to H x W and summed (cross-merge), then gated.
+ *   x, z, y : [B, D, H, W] (spatial)
+ *   delta : [B, K, D, L] and Bm, Cm : [B, K, N, L] in each direction's SCAN
+ *           order (L = H*W), as per-direction projections emit them
+ *   A : [K, D, N];  Dskip, delta_bias : [K, D]
+ * Cross-scan and cross-merge are folded into the kernels' addressing.
+ */
+SSM_API ssm_status ss2d_scan_fwd(ssm_dtype dt, int B, int D, int H, int W, int N,
+                         int K, const void *x, const void *delta,
+                         const float *A, const void *Bm, const void *Cm,
+                         const float *Dskip, const void *z,
+                         const float *delta_bias, int delta_softplus, void *y,
+                         void *workspace, size_t ws_bytes,
+                         ssm_stream_t stream);
+
+/*
+ * Workspace bytes the call with these sizes needs (0 when none).
+ * `L_or_HW` is L, or H*W for SS2D; K is ignored except for SS2D.
+ * Returns (size_t)-1 for invalid sizes.
+ */
+SSM_API size_t ssm_workspace_bytes(ssm_op op, ssm_dtype dt, int B, int D,
+                           int L_or_HW, int N, int K);
+
+/* Static description of a status code (never NULL). */
+SSM_API const char *ssm_status_string(ssm_status s);
+
+/* Library version, "major.minor.patch". */
+SSM_API const char *ssm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_SCAN_H */

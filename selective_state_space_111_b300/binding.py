@@ -1,0 +1,198 @@
+"""Thin Python binding of the C ABI in include/ssm_scan.h (ctypes).
+
+Argument marshalling only: every function checks that the tensors are CUDA,
+contiguous and of the right dtype, passes their device pointers and the
+current CUDA stream to the library, and raises SsmError on a non-zero status.
+PyTorch supplies the device memory (outputs and workspace) and the stream.
+All arithmetic runs in the library's kernels; if the library is missing this
+module fails to import.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libssm_scan.so")
+
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(
+        "libssm_scan.so not found next to %s; build it with "
+        "`python -m selective_state_space_111_b300.build`" % __file__)
+
+_lib = ctypes.CDLL(_LIB_PATH)
+
+SSM_F32, SSM_BF16 = 0, 1
+OPS = {"single": 0, "v1": 1, "v2": 2, "ss2d": 3}
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA launch error",
+           4: "workspace"}
+
+_vp, _fp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_lib.selective_scan_fwd.argtypes = [_i] * 5 + [_vp] * 8 + [_i, _vp, _vp, _sz, _vp]
+_lib.bimamba_scan_fwd_v1.argtypes = [_i] * 5 + [_vp] * 9 + [_i, _f, _vp, _vp, _sz, _vp]
+_lib.bimamba_scan_fwd_v2.argtypes = [_i] * 5 + [_vp] * 15 + [_i, _f, _vp, _vp, _sz, _vp]
+_lib.ss2d_scan_fwd.argtypes = [_i] * 7 + [_vp] * 8 + [_i, _vp, _vp, _sz, _vp]
+_lib.ssm_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
+_lib.ssm_workspace_bytes.restype = _sz
+_lib.ssm_status_string.argtypes = [_i]
+_lib.ssm_status_string.restype = ctypes.c_char_p
+_lib.ssm_version.restype = ctypes.c_char_p
+for _fn in (_lib.selective_scan_fwd, _lib.bimamba_scan_fwd_v1, _lib.bimamba_scan_fwd_v2,
+            _lib.ss2d_scan_fwd):
+    _fn.restype = _i
+
+
+class SsmError(RuntimeError):
+    def __init__(self, status, where):
+        msg = _lib.ssm_status_string(status).decode()
+        super().__init__("%s: %s (status %d)" % (where, msg, status))
+        self.status = status
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """The loaded ctypes library (for callers that pass raw pointers)."""
+    return _lib
+
+
+def version() -> str:
+    return _lib.ssm_version().decode()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SSM_F32
+    if t.dtype == torch.bfloat16:
+        return SSM_BF16
+    raise TypeError("I/O tensors must be float32 or bfloat16, got %s" % t.dtype)
+
+
+def _io(t, io_dtype, name, shape=None, optional=False):
+    if t is None:
+        if optional:
+            return None
+        raise ValueError("%s is required" % name)
+    if not t.is_cuda or not t.is_contiguous() or t.dtype != io_dtype:
+        raise ValueError("%s must be a contiguous CUDA %s tensor" % (name, io_dtype))
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s: expected shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+    return t.data_ptr()
+
+
+def _par(t, name, shape=None, optional=False):
+    return _io(t, torch.float32, name, shape, optional)
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def workspace_bytes(op: str, dtype: torch.dtype, B: int, D: int, L: int, N: int, K: int = 4) -> int:
+    code = SSM_F32 if dtype == torch.float32 else SSM_BF16
+    n = _lib.ssm_workspace_bytes(OPS[op], code, B, D, L, N, K)
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("invalid sizes")
+    return int(n)
+
+
+def _workspace(op, dtype, B, D, L, N, device, workspace, K=4):
+    need = workspace_bytes(op, dtype, B, D, L, N, K)
+    if need == 0:
+        return None, 0
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    if not workspace.is_cuda or workspace.numel() * workspace.element_size() < need:
+        raise ValueError("workspace must be a CUDA tensor of at least %d bytes" % need)
+    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
+
+def _check(status, where):
+    if status != 0:
+        raise SsmError(status, where)
+
+
+def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None,
+                       delta_softplus=True, out=None, workspace=None, stream=None):
+    """One direction.  u, delta, z: [Bt, Dc, L]; A: [Dc, N] fp32; B, C: [Bt, N, L];
+    D, delta_bias: [Dc] fp32.  Returns y [Bt, Dc, L]."""
+    io = u.dtype
+    Bt, Dc, L = u.shape
+    N = A.shape[1]
+    y = torch.empty_like(u) if out is None else out
+    args = [_io(u, io, "u"), _io(delta, io, "delta", (Bt, Dc, L)), _par(A, "A", (Dc, N)),
+            _io(B, io, "B", (Bt, N, L)), _io(C, io, "C", (Bt, N, L)),
+            _par(D, "D", (Dc,), True), _io(z, io, "z", (Bt, Dc, L), True),
+            _par(delta_bias, "delta_bias", (Dc,), True)]
+    wp, wn = _workspace("single", io, Bt, Dc, L, N, u.device, workspace)
+    _check(_lib.selective_scan_fwd(_dtype_code(u), Bt, Dc, L, N, *args, int(bool(delta_softplus)),
+                                   _io(y, io, "out", (Bt, Dc, L)), wp, wn, _stream(stream)),
+           "selective_scan_fwd")
+    return y
+
+
+def bimamba_scan_fwd_v1(u, delta, A, A_b, B, C, D=None, z=None, delta_bias=None,
+                        delta_softplus=True, out_scale=1.0, out=None, workspace=None,
+                        stream=None):
+    """BiMamba v1: shared delta/B/C/D/bias, separate A and A_b.  Original order."""
+    io = u.dtype
+    Bt, Dc, L = u.shape
+    N = A.shape[1]
+    y = torch.empty_like(u) if out is None else out
+    args = [_io(u, io, "u"), _io(delta, io, "delta", (Bt, Dc, L)), _par(A, "A", (Dc, N)),
+            _par(A_b, "A_b", (Dc, N)), _io(B, io, "B", (Bt, N, L)), _io(C, io, "C", (Bt, N, L)),
+            _par(D, "D", (Dc,), True), _io(z, io, "z", (Bt, Dc, L), True),
+            _par(delta_bias, "delta_bias", (Dc,), True)]
+    wp, wn = _workspace("v1", io, Bt, Dc, L, N, u.device, workspace)
+    _check(_lib.bimamba_scan_fwd_v1(_dtype_code(u), Bt, Dc, L, N, *args, int(bool(delta_softplus)),
+                                    float(out_scale), _io(y, io, "out", (Bt, Dc, L)), wp, wn,
+                                    _stream(stream)), "bimamba_scan_fwd_v1")
+    return y
+
+
+def bimamba_scan_fwd_v2(u, delta, delta_b, A, A_b, B, C, B_b, C_b, D=None, D_b=None, z=None,
+                        delta_bias=None, delta_bias_b=None, u_b=None, delta_softplus=True,
+                        out_scale=0.5, out=None, workspace=None, stream=None):
+    """BiMamba v2: independent backward set.  Original token order."""
+    io = u.dtype
+    Bt, Dc, L = u.shape
+    N = A.shape[1]
+    y = torch.empty_like(u) if out is None else out
+    sh, shn = (Bt, Dc, L), (Bt, N, L)
+    args = [_io(u, io, "u"), _io(u_b, io, "u_b", sh, True), _io(delta, io, "delta", sh),
+            _io(delta_b, io, "delta_b", sh), _par(A, "A", (Dc, N)), _par(A_b, "A_b", (Dc, N)),
+            _io(B, io, "B", shn), _io(C, io, "C", shn), _io(B_b, io, "B_b", shn),
+            _io(C_b, io, "C_b", shn), _par(D, "D", (Dc,), True), _par(D_b, "D_b", (Dc,), True),
+            _io(z, io, "z", sh, True), _par(delta_bias, "delta_bias", (Dc,), True),
+            _par(delta_bias_b, "delta_bias_b", (Dc,), True)]
+    wp, wn = _workspace("v2", io, Bt, Dc, L, N, u.device, workspace)
+    _check(_lib.bimamba_scan_fwd_v2(_dtype_code(u), Bt, Dc, L, N, *args, int(bool(delta_softplus)),
+                                    float(out_scale), _io(y, io, "out", sh), wp, wn,
+                                    _stream(stream)), "bimamba_scan_fwd_v2")
+    return y
+
+
+def ss2d_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+                  out=None, workspace=None, stream=None):
+    """SS2D, K=4.  x, z: [Bt, Dc, H, W]; delta: [Bt, 4, Dc, H*W] and B, C: [Bt, 4, N, H*W]
+    in each direction's scan order; A: [4, Dc, N]; D, delta_bias: [4, Dc]."""
+    io = x.dtype
+    Bt, Dc, H, W = x.shape
+    K = 4
+    L = H * W
+    N = A.shape[2]
+    y = torch.empty_like(x) if out is None else out
+    args = [_io(x, io, "x"), _io(delta, io, "delta", (Bt, K, Dc, L)), _par(A, "A", (K, Dc, N)),
+            _io(B, io, "B", (Bt, K, N, L)), _io(C, io, "C", (Bt, K, N, L)),
+            _par(D, "D", (K, Dc), True), _io(z, io, "z", (Bt, Dc, H, W), True),
+            _par(delta_bias, "delta_bias", (K, Dc), True)]
+    wp, wn = _workspace("ss2d", io, Bt, Dc, L, N, x.device, workspace, K)
+    _check(_lib.ss2d_scan_fwd(_dtype_code(x), Bt, Dc, H, W, N, K, *args, int(bool(delta_softplus)),
+                              _io(y, io, "out", (Bt, Dc, H, W)), wp, wn, _stream(stream)),
+           "ss2d_scan_fwd")
+    return y

@@ -1,0 +1,52 @@
+"""Builds the CUDA library libssm_scan.so in-tree (sm_103a only).
+
+    python -m selective_state_space_111_b300.build
+
+nvcc compiles csrc/ssm_scan_api.cu (which includes the kernel header) into a
+shared library with the CUDA runtime linked statically, so the .so loads on a
+machine without a GPU as well (for symbol checks) and needs nothing from the
+environment at run time beyond the NVIDIA driver.
+"""
+import os
+import subprocess
+import sys
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+LIB = os.path.join(HERE, "libssm_scan.so")
+SOURCES = [os.path.join(HERE, "csrc", "ssm_scan_api.cu")]
+DEPS = SOURCES + [os.path.join(HERE, "csrc", "scan_kernel.cuh"),
+                  os.path.join(ROOT, "include", "ssm_scan.h")]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def nvcc():
+    cand = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
+    return cand if os.path.exists(cand) else "nvcc"
+
+
+def needs_build():
+    if not os.path.exists(LIB):
+        return True
+    t = os.path.getmtime(LIB)
+    return any(os.path.getmtime(p) > t for p in DEPS)
+
+
+def build(force=False, verbose=False, extra=()):
+    if not force and not needs_build():
+        return LIB
+    tmp = LIB + ".tmp%d" % os.getpid()
+    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
+           "-Xcompiler", "-fvisibility=hidden", "-cudart", "static",
+           "-I", os.path.join(ROOT, "include"), "-o", tmp, *SOURCES, *extra]
+    if verbose:
+        cmd.insert(1, "-Xptxas=-v")
+        print(" ".join(cmd))
+    subprocess.check_call(cmd)
+    os.replace(tmp, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    build(force="--force" in sys.argv, verbose="-v" in sys.argv)
+    print(LIB)

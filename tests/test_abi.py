@@ -1,0 +1,94 @@
+"""The C ABI: the library loads, exports every function include/ssm_scan.h
+declares, and rejects bad arguments before touching the GPU.  CPU only: no
+call here reaches a kernel launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssm_scan.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from selective_state_space_111_b300 import build
+    build.build()
+    from selective_state_space_111_b300 import binding
+    return binding.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    return re.findall(r"SSM_API\s+[\w\s\*]+?\b(\w+)\s*\(", src)
+
+
+def test_header_declares_the_operations():
+    names = set(declared_functions())
+    assert {"selective_scan_fwd", "bimamba_scan_fwd_v1", "bimamba_scan_fwd_v2", "ss2d_scan_fwd",
+            "ssm_workspace_bytes", "ssm_status_string", "ssm_version"} <= names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    for code in range(5):
+        assert lib.ssm_status_string(code)
+    assert re.match(rb"^\d+\.\d+\.\d+$", lib.ssm_version())
+
+
+def test_workspace_bytes(lib):
+    ws = lib.ssm_workspace_bytes
+    assert ws(0, 1, 8, 768, 6085, 16, 4) == 0                      # single: none
+    assert ws(2, 1, 8, 768, 6085, 16, 4) == 8 * 768 * 6085 * 4     # v2: fp32 per position
+    assert ws(1, 1, 2, 1536, 4096, 16, 4) == 2 * 1536 * 4096 * 4
+    assert ws(2, 1, 4, 8, 20, 16, 4) == 0                          # one chunk: in shared memory
+    assert ws(3, 1, 32, 192, 3136, 16, 4) == 32 * 192 * 3136 * 4   # SS2D: the pair sum
+    assert ws(3, 1, 32, 192, 3136, 16, 2) == ctypes.c_size_t(-1).value
+    assert ws(0, 7, 1, 1, 1, 16, 4) == ctypes.c_size_t(-1).value   # bad dtype
+
+
+FAKE = 0x10000   # 16-byte aligned, never dereferenced: every call below fails validation
+
+
+def single(lib, *, dt=1, B=1, D=1, L=8, N=16, u=FAKE, delta=FAKE, A=FAKE, Bm=FAKE, Cm=FAKE,
+           Ds=None, z=None, bias=None, y=FAKE):
+    return lib.selective_scan_fwd(dt, B, D, L, N, u, delta, A, Bm, Cm, Ds, z, bias, 1, y,
+                                  None, 0, None)
+
+
+def test_invalid_arguments_are_rejected_before_launch(lib):
+    assert single(lib, N=17) == 2                   # N > 16: unsupported
+    assert single(lib, N=0) == 1
+    assert single(lib, L=-1) == 1
+    assert single(lib, dt=5) == 1
+    assert single(lib, u=None) == 1                 # required pointer
+    assert single(lib, u=FAKE + 2) == 1             # misaligned I/O tensor
+    assert single(lib, A=FAKE + 2) == 1             # misaligned fp32 parameter
+    assert single(lib, y=None) == 1
+
+
+def test_empty_problems_launch_nothing(lib):
+    assert single(lib, B=0) == 0
+    assert single(lib, D=0) == 0
+    assert single(lib, L=0) == 0
+
+
+def test_bidirectional_workspace_is_checked(lib):
+    args = [1, 2, 16, 100, 16] + [FAKE] * 4 + [FAKE, FAKE] + [FAKE] * 4 + [None, None, None,
+                                                                           None, None]
+    # v2 with a multi-chunk L and no workspace
+    st = lib.bimamba_scan_fwd_v2(*args, 1, ctypes.c_float(0.5), FAKE, None, 0, None)
+    assert st == 4
+    st = lib.bimamba_scan_fwd_v2(*args, 1, ctypes.c_float(0.5), FAKE, FAKE, 16, None)
+    assert st == 4
+
+
+def test_ss2d_requires_four_directions(lib):
+    st = lib.ss2d_scan_fwd(1, 1, 1, 4, 4, 16, 2, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None,
+                           1, FAKE, FAKE, 1 << 20, None)
+    assert st == 2

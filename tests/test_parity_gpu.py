@@ -1,0 +1,163 @@
+"""GPU parity: the CUDA library against the fp64 oracle, element by element,
+on the same seeded inputs (tolerance |gpu - oracle| <= tol * (1 + |oracle|),
+tol = 1e-4 for fp32 I/O and 1e-2 for bf16 I/O)."""
+import numpy as np
+import pytest
+import torch
+
+from cases import TOL, max_scaled_err, row_slice, run_gpu, run_oracle
+from selective_state_space_111_b300.synth import WORKLOADS, Spec, make_inputs, seed_for
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from selective_state_space_111_b300 import build
+    build.build()
+
+
+def check(spec, seed, ref=None):
+    t = make_inputs(spec, seed)
+    y = run_gpu(spec, t)
+    torch.cuda.synchronize()
+    if ref is None:
+        ref = run_oracle(spec, t)
+    err = max_scaled_err(y, ref)
+    assert np.isfinite(err) and err <= TOL[spec.io], "%s: max scaled error %.3g" % (spec, err)
+    return y, err
+
+
+# ------------------------------------------------------------ small shapes
+# L spans: shorter than a chunk, one chunk, chunk +- 1, several chunks with a
+# ragged tail; D spans partial CTAs; N < 16 exercises the state mask.
+SHAPES = [(1, 1, 1, 16), (2, 3, 5, 16), (1, 17, 31, 16), (2, 16, 32, 16), (1, 5, 33, 16),
+          (3, 20, 97, 16), (2, 40, 197, 16), (1, 9, 64, 7), (2, 4, 129, 1), (1, 33, 300, 16)]
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", SHAPES)
+def test_single(io, shape):
+    B, D, L, N = shape
+    check(Spec("single", io, B=B, D=D, L=L, N=N, perturb=True), 1000 + L)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", SHAPES)
+def test_v1(io, shape):
+    B, D, L, N = shape
+    check(Spec("v1", io, B=B, D=D, L=L, N=N, perturb=True, a_b_noise=0.1, out_scale=1.0), 2000 + L)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("shared_u", [True, False])
+def test_v2(io, shape, shared_u):
+    B, D, L, N = shape
+    check(Spec("v2", io, B=B, D=D, L=L, N=N, perturb=True, shared_u=shared_u, out_scale=0.5),
+          3000 + L)
+
+
+SS2D_SHAPES = [(1, 1, 1, 1), (1, 2, 2, 3), (2, 3, 5, 7), (1, 17, 8, 8), (2, 5, 3, 11),
+               (1, 4, 11, 3), (1, 16, 14, 14), (1, 3, 56, 56)]
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", SS2D_SHAPES)
+def test_ss2d(io, shape):
+    B, D, H, W = shape
+    check(Spec("ss2d", io, B=B, D=D, H=H, W=W, perturb=True), 4000 + H * W)
+
+
+# ------------------------------------------------------------ options
+@pytest.mark.parametrize("op", ["single", "v1", "v2", "ss2d"])
+def test_optional_inputs_absent(op):
+    # no gate, no skip, no bias, no softplus (delta used as given)
+    kw = dict(H=5, W=6) if op == "ss2d" else dict(L=77)
+    spec = Spec(op, "f32", B=2, D=18, gate=False, delta_softplus=False, **kw)
+    t = make_inputs(spec, 77)
+    t["delta"] = t["delta"].abs() * 0.05           # keep delta positive
+    if op == "v2":
+        t["delta_b"] = t["delta_b"].abs() * 0.05
+    for k in ("D", "D_b", "delta_bias", "delta_bias_b"):
+        if k in t:
+            t[k] = None
+    y = run_gpu(spec, t)
+    ref = run_oracle(spec, t)
+    assert max_scaled_err(y, ref) <= TOL["f32"]
+
+
+def test_deterministic_and_workspace_contents_irrelevant():
+    spec = Spec("v2", "bf16", B=2, D=24, L=150, perturb=True, out_scale=0.5)
+    t = make_inputs(spec, 5)
+    from selective_state_space_111_b300 import workspace_bytes
+    n = workspace_bytes("v2", torch.bfloat16, 2, 24, 150, 16)
+    ws1 = torch.full((n,), 0xFF, dtype=torch.uint8, device="cuda")   # NaN patterns
+    ws2 = torch.zeros((n,), dtype=torch.uint8, device="cuda")
+    y1 = run_gpu(spec, t, workspace=ws1)
+    y2 = run_gpu(spec, t, workspace=ws2)
+    assert torch.equal(y1, y2)
+
+
+def test_length_one_branches_agree():
+    # With L = 1 and identical parameter sets the two branches coincide, so
+    # v2 with out_scale 0.5 equals the single-direction scan.
+    spec = Spec("v2", "f32", B=2, D=8, L=1, out_scale=0.5)
+    t = make_inputs(spec, 9)
+    for a, b in (("delta_b", "delta"), ("A_b", "A"), ("B_b", "B"), ("C_b", "C"), ("D_b", "D"),
+                 ("delta_bias_b", "delta_bias")):
+        t[a] = t[b].clone()
+    y2 = run_gpu(spec, t)
+    ys = run_gpu(Spec("single", "f32", B=2, D=8, L=1), t)
+    assert torch.allclose(y2, ys, rtol=1e-6, atol=1e-6)
+
+
+# ------------------------------------------------------------ the pages' workloads
+def _sampled_rows(spec, seed, nrows):
+    """Full-size launch; the oracle recomputes a seeded sample of whole rows."""
+    t = make_inputs(spec, seed)
+    y = run_gpu(spec, t).cpu()
+    rng = np.random.default_rng(seed)
+    rows = {(0, 0), (spec.B - 1, spec.D - 1)}
+    while len(rows) < nrows:
+        rows.add((int(rng.integers(spec.B)), int(rng.integers(spec.D))))
+    worst = 0.0
+    for b, d in sorted(rows):
+        ref = run_oracle(spec, row_slice(spec, t, b, d))
+        worst = max(worst, max_scaled_err(y[b:b + 1, d:d + 1], ref))
+    assert worst <= TOL[spec.io], "%s: worst sampled row error %.3g" % (spec.name, worst)
+    return worst
+
+
+def test_workload_vim_ti_224_single_f32_full():
+    name = "vim_ti_224_single_f32"
+    check(WORKLOADS[name], seed_for(name))
+
+
+def test_workload_vim_ti_224_bimamba_v2():
+    name = "vim_ti_224_bimamba_v2"
+    _sampled_rows(WORKLOADS[name], seed_for(name), 64)
+
+
+def test_workload_vim_s_1248_bimamba_v2():
+    name = "vim_s_1248_bimamba_v2"
+    _sampled_rows(WORKLOADS[name], seed_for(name), 64)
+
+
+def test_workload_vmamba_56x56_ss2d():
+    name = "vmamba_56x56_ss2d"
+    _sampled_rows(WORKLOADS[name], seed_for(name), 48)
+
+
+@pytest.mark.parametrize("L", [4096, 16384, 65536])
+def test_workload_bimamba_v1_long(L):
+    name = "bimamba_v1_L%d" % L
+    _sampled_rows(WORKLOADS[name], seed_for(name), 16 if L > 16384 else 32)
+
+
+@pytest.mark.slow
+def test_workload_bimamba_v1_L262144():
+    name = "bimamba_v1_L262144"
+    _sampled_rows(WORKLOADS[name], seed_for(name), 8)
