@@ -33,11 +33,14 @@
  *    contents need no initialisation and are garbage afterwards.  Two calls
  *    in flight at once must not share a workspace.
  *  - Calls are asynchronous on `stream` (0 = the legacy default stream).
- *    The library allocates nothing and keeps no global state.
+ *    The library allocates nothing and keeps no global state, except the
+ *    fixed scratch array that bimamba_scan_fwd_v2_noalloc uses.
  *  - Errors: SSM_ERR_INVALID_ARG for a bad size, NULL required pointer or
  *    misaligned pointer; SSM_ERR_UNSUPPORTED for N > 16, K != 4 or sizes
  *    beyond the 32-bit index range; SSM_ERR_WORKSPACE when ws_bytes is too
- *    small; SSM_ERR_CUDA when a launch fails (cudaGetLastError is consumed).
+ *    small; SSM_ERR_CUDA when a launch fails (cudaGetLastError is consumed);
+ *    SSM_ERR_SCRATCH_LIMIT when a problem is too large for the fixed scratch
+ *    of bimamba_scan_fwd_v2_noalloc.
  *    Every check happens before any launch: an error means nothing ran.
  *  - A call with B == 0, D == 0 or L == 0 is valid and launches nothing.
  */
@@ -65,7 +68,8 @@ typedef enum {
     SSM_ERR_INVALID_ARG = 1,
     SSM_ERR_UNSUPPORTED = 2,
     SSM_ERR_CUDA = 3,
-    SSM_ERR_WORKSPACE = 4
+    SSM_ERR_WORKSPACE = 4,
+    SSM_ERR_SCRATCH_LIMIT = 5
 } ssm_status;
 
 typedef enum {
@@ -156,6 +160,42 @@ SSM_API ssm_status ss2d_scan_fwd(ssm_dtype dt, int B, int D, int H, int W, int N
  */
 SSM_API size_t ssm_workspace_bytes(ssm_op op, ssm_dtype dt, int B, int D,
                            int L_or_HW, int N, int K);
+
+/*
+ * Allocation-free variant of bimamba_scan_fwd_v2.  The pages have no
+ * counterpart for this entry point: it exists for callers that cannot
+ * allocate device memory themselves, for example a plugin inside a host
+ * framework that owns the device allocator and hands its plugins only their
+ * input and output buffers, or real-time code that must not call cudaMalloc
+ * (which can synchronise the device) once it is running.
+ *
+ * Arguments, layouts, results and errors are those of bimamba_scan_fwd_v2,
+ * without `workspace` / `ws_bytes`.  Instead of a caller workspace, the call
+ * uses a scratch array of SSM_STATIC_SCRATCH_BYTES bytes that the library
+ * declares as a file-scope __device__ array, so every GPU that loads the
+ * library holds those bytes until the process exits.
+ *  - Problems whose workspace (ssm_workspace_bytes(SSM_OP_BIMAMBA_V2, ...))
+ *    exceeds SSM_STATIC_SCRATCH_BYTES return SSM_ERR_SCRATCH_LIMIT before
+ *    anything runs; B * D * L <= 16 Mi positions always fits.
+ *  - The first call on a device (the one current on the calling thread,
+ *    which must be the device `stream` belongs to) looks up the array's
+ *    device address, once; make that first call before any stream capture.
+ *  - The call allocates nothing, on the host or the device.
+ *  - Every call on a device shares the one array, and the array keeps the
+ *    previous call's contents.  The kernel writes each scratch slot before
+ *    it reads it, so nothing needs clearing between calls; but calls whose
+ *    executions overlap on the GPU (different streams, or different host
+ *    threads) race on the array and give wrong results.  Serialise them.
+ */
+#define SSM_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
+
+SSM_API ssm_status bimamba_scan_fwd_v2_noalloc(
+    ssm_dtype dt, int B, int D, int L, int N, const void *u, const void *u_b,
+    const void *delta, const void *delta_b, const float *A, const float *A_b,
+    const void *Bm, const void *Cm, const void *Bm_b, const void *Cm_b,
+    const float *Dskip, const float *D_b, const void *z,
+    const float *delta_bias, const float *delta_bias_b, int delta_softplus,
+    float out_scale, void *y, ssm_stream_t stream);
 
 /* Static description of a status code (never NULL). */
 SSM_API const char *ssm_status_string(ssm_status s);

@@ -8,7 +8,8 @@ imported without it.  Touching any operation when the library is missing
 raises immediately: there is no fallback.
 """
 _OPS = ("selective_scan_fwd", "bimamba_scan_fwd_v1", "bimamba_scan_fwd_v2",
-        "ss2d_scan_fwd", "workspace_bytes", "library_path", "SsmError", "version")
+        "bimamba_scan_fwd_v2_noalloc", "ss2d_scan_fwd", "workspace_bytes", "library_path",
+        "SsmError", "version")
 
 
 def __getattr__(name):

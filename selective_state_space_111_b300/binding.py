@@ -27,20 +27,21 @@ _lib = ctypes.CDLL(_LIB_PATH)
 SSM_F32, SSM_BF16 = 0, 1
 OPS = {"single": 0, "v1": 1, "v2": 2, "ss2d": 3}
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA launch error",
-           4: "workspace"}
+           4: "workspace", 5: "scratch limit"}
 
 _vp, _fp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 _lib.selective_scan_fwd.argtypes = [_i] * 5 + [_vp] * 8 + [_i, _vp, _vp, _sz, _vp]
 _lib.bimamba_scan_fwd_v1.argtypes = [_i] * 5 + [_vp] * 9 + [_i, _f, _vp, _vp, _sz, _vp]
 _lib.bimamba_scan_fwd_v2.argtypes = [_i] * 5 + [_vp] * 15 + [_i, _f, _vp, _vp, _sz, _vp]
 _lib.ss2d_scan_fwd.argtypes = [_i] * 7 + [_vp] * 8 + [_i, _vp, _vp, _sz, _vp]
+_lib.bimamba_scan_fwd_v2_noalloc.argtypes = [_i] * 5 + [_vp] * 15 + [_i, _f, _vp, _vp]
 _lib.ssm_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
 _lib.ssm_workspace_bytes.restype = _sz
 _lib.ssm_status_string.argtypes = [_i]
 _lib.ssm_status_string.restype = ctypes.c_char_p
 _lib.ssm_version.restype = ctypes.c_char_p
 for _fn in (_lib.selective_scan_fwd, _lib.bimamba_scan_fwd_v1, _lib.bimamba_scan_fwd_v2,
-            _lib.ss2d_scan_fwd):
+            _lib.ss2d_scan_fwd, _lib.bimamba_scan_fwd_v2_noalloc):
     _fn.restype = _i
 
 
@@ -195,4 +196,29 @@ def ss2d_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_soft
     _check(_lib.ss2d_scan_fwd(_dtype_code(x), Bt, Dc, H, W, N, K, *args, int(bool(delta_softplus)),
                               _io(y, io, "out", (Bt, Dc, H, W)), wp, wn, _stream(stream)),
            "ss2d_scan_fwd")
+    return y
+
+
+def bimamba_scan_fwd_v2_noalloc(u, delta, delta_b, A, A_b, B, C, B_b, C_b, D=None, D_b=None,
+                                z=None, delta_bias=None, delta_bias_b=None, u_b=None,
+                                delta_softplus=True, out_scale=0.5, out=None, stream=None):
+    """BiMamba v2 through the allocation-free entry point: the library's fixed
+    scratch array replaces the workspace, so only `out` (if not given) is
+    allocated here, by PyTorch.  Raises SsmError (status 5) when the problem
+    needs more scratch than the array holds."""
+    io = u.dtype
+    Bt, Dc, L = u.shape
+    N = A.shape[1]
+    y = torch.empty_like(u) if out is None else out
+    sh, shn = (Bt, Dc, L), (Bt, N, L)
+    args = [_io(u, io, "u"), _io(u_b, io, "u_b", sh, True), _io(delta, io, "delta", sh),
+            _io(delta_b, io, "delta_b", sh), _par(A, "A", (Dc, N)), _par(A_b, "A_b", (Dc, N)),
+            _io(B, io, "B", shn), _io(C, io, "C", shn), _io(B_b, io, "B_b", shn),
+            _io(C_b, io, "C_b", shn), _par(D, "D", (Dc,), True), _par(D_b, "D_b", (Dc,), True),
+            _io(z, io, "z", sh, True), _par(delta_bias, "delta_bias", (Dc,), True),
+            _par(delta_bias_b, "delta_bias_b", (Dc,), True)]
+    _check(_lib.bimamba_scan_fwd_v2_noalloc(_dtype_code(u), Bt, Dc, L, N, *args,
+                                            int(bool(delta_softplus)), float(out_scale),
+                                            _io(y, io, "out", sh), _stream(stream)),
+           "bimamba_scan_fwd_v2_noalloc")
     return y

@@ -2,11 +2,14 @@
 //
 // Each entry point validates its arguments on the host, fills the kernel's
 // parameter block and launches the scan kernel(s) on the caller's stream.
-// Nothing is allocated and no state is kept between calls.
+// Nothing is allocated.  The one piece of state kept between calls is the
+// fixed scratch array of the allocation-free entry point and its per-device
+// address.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "scan_kernel.cuh"
 #include "ssm_scan.h"
@@ -139,6 +142,36 @@ ssm_status bidirectional(ssm_dtype dt, int B, int D, int L, int N, const void *u
     return dispatch<2, ssm::MAP_ROW, ssm::MODE_FINAL>(dt, P, stream);
 }
 
+// ---- fixed scratch of the allocation-free entry point
+// The array lives in the library's device image; in host code its name is
+// only a host-side stand-in, so the kernel is given the device address that
+// cudaGetSymbolAddress reports for the current device (looked up once per
+// device, on that device's first call).
+constexpr int kMaxDevices = 256;
+__device__ __align__(256) unsigned char g_static_scratch[SSM_STATIC_SCRATCH_BYTES];
+std::mutex g_scratch_mutex;
+void *g_scratch_addr[kMaxDevices];
+
+ssm_status static_scratch(void **out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SSM_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return SSM_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (g_scratch_addr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return SSM_ERR_CUDA;
+        }
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return SSM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -199,6 +232,25 @@ ssm_status bimamba_scan_fwd_v2(ssm_dtype dt, int B, int D, int L, int N, const v
     return bidirectional(dt, B, D, L, N, u, u_b, delta, delta_b, A, A_b, Bm, Cm, Bm_b, Cm_b,
                          Dskip, D_b, z, delta_bias, delta_bias_b, delta_softplus, out_scale, y,
                          workspace, ws_bytes, (cudaStream_t)stream);
+}
+
+ssm_status bimamba_scan_fwd_v2_noalloc(ssm_dtype dt, int B, int D, int L, int N,
+                                       const void *u, const void *u_b, const void *delta,
+                                       const void *delta_b, const float *A, const float *A_b,
+                                       const void *Bm, const void *Cm, const void *Bm_b,
+                                       const void *Cm_b, const float *Dskip, const float *D_b,
+                                       const void *z, const float *delta_bias,
+                                       const float *delta_bias_b, int delta_softplus,
+                                       float out_scale, void *y, ssm_stream_t stream) {
+    ssm_status s = check_common(dt, B, D, L, N);
+    if (s != SSM_OK) return s;
+    if (bidir_ws(B, D, L) > SSM_STATIC_SCRATCH_BYTES) return SSM_ERR_SCRATCH_LIMIT;
+    void *scratch = nullptr;
+    s = static_scratch(&scratch);
+    if (s != SSM_OK) return s;
+    return bidirectional(dt, B, D, L, N, u, u_b, delta, delta_b, A, A_b, Bm, Cm, Bm_b, Cm_b,
+                         Dskip, D_b, z, delta_bias, delta_bias_b, delta_softplus, out_scale, y,
+                         scratch, SSM_STATIC_SCRATCH_BYTES, (cudaStream_t)stream);
 }
 
 ssm_status ss2d_scan_fwd(ssm_dtype dt, int B, int D, int H, int W, int N, int K,
@@ -276,6 +328,8 @@ const char *ssm_status_string(ssm_status s) {
     case SSM_ERR_UNSUPPORTED: return "unsupported size or option";
     case SSM_ERR_CUDA: return "CUDA launch error";
     case SSM_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case SSM_ERR_SCRATCH_LIMIT:
+        return "problem needs more scratch than the library's fixed 64 MiB array";
     }
     return "unknown status";
 }
