@@ -50,7 +50,32 @@ def peaks():
 
 # ---------------------------------------------------------------- GPU arm
 def launches_per_step(op):
-    return 2 if op == "ss2d" else 1
+    """Kernels one call launches: B/C packing (one per B/C set), the
+    transposes of SS2D, and the scan kernel(s)."""
+    return {"single": 2, "v1": 2, "v2": 3, "ss2d": 5}[op]
+
+
+def scan_sources_sha():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("bidir_kernel.cuh", "scan_ops.cuh"):
+        with open(os.path.join(ROOT, "selective_state_space_111_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload):
+    """DRAM bytes per launch of the scan kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "scan_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        d = json.load(fh)
+    ent = d.get(workload)
+    if not ent or ent.get("src_sha") != scan_sources_sha():
+        return None
+    return ent.get("dram_bytes_per_launch")
 
 
 def call(ssm, spec, g, ws, out):
@@ -175,15 +200,23 @@ def run_ours(args):
     barrier()
     torch.cuda.synchronize()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    # the scan kernel's own launches, bracketed by the library's profiling hook
+    kb = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ke = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for e in kb + ke:
+        e.record(stream)                  # creates the CUDA events
+    torch.cuda.synchronize()
     ev[0].record(stream)
     for i in range(args.steps):
+        ssm.set_profile_events(kb[i], ke[i])
         call(ssm, spec, g, ws, out)
         ev[i + 1].record(stream)
+    ssm.set_profile_events(None, None)
     torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
     clocks = sampler.stop()
-    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    kern = [kb[i].elapsed_time(ke[i]) for i in range(args.steps)]
     total_ms = ev[0].elapsed_time(ev[-1])
     if world > 1:
         tt = torch.tensor([total_ms], device=dev)
@@ -229,11 +262,14 @@ def run_ours(args):
         hbm_peak, sm_max, peak_kind = peaks()
         gbps = spec.algorithmic_bytes() * world / (ms * 1e-3) / 1e9
         ups = spec.updates() * world / (ms * 1e-3)
-        # dominant kernel: the per-launch average over the timed region
-        kern_ms = statistics.mean(per) / launches_per_step(spec.op)
-        upd_launch = spec.updates() / launches_per_step(spec.op)
-        alu_peak = 148 * 128 * sm_max * 1e6 / 1e12          # FP32-pipe Tops/s
-        alu_ach = 4 * upd_launch / (kern_ms * 1e-3) / 1e12
+        # dominant kernel: the scan kernel's average launch over the timed region
+        kern_ms = statistics.mean(kern)
+        scans = 2 if spec.op == "ss2d" else 1          # the hook brackets the last one
+        upd_launch = spec.updates() / scans
+        # ALU roof: 128 fp32 lanes per SM and 4 fp32 operations per element
+        # update (equal to the MUFU ex2 roof: 32 per SM per clock, one each)
+        alu_peak = 148 * 32 * sm_max * 1e6 / 1e9          # Gupd/s
+        alu_ach = upd_launch / (kern_ms * 1e-3) / 1e9
         line = {
             "metric": METRIC,
             "value": round(gbps, 2),
@@ -253,12 +289,16 @@ def run_ours(args):
                        "d_inner": spec.D, "d_state": spec.N, "seq_len": L,
                        "l2": "inputs larger than L2 (no flush)",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
-            "roofline": {"bound": "alu", "achieved": round(alu_ach, 3), "peak": round(alu_peak, 2),
-                         "unit": "Tops/s (FP32 pipe, 4 ops per update)",
-                         "frac": round(alu_ach / alu_peak, 4), "traffic": args.traffic,
-                         "hbm_frac": round(spec.algorithmic_bytes() / (kern_ms * 1e-3) / 1e9
-                                           / hbm_peak, 4),
-                         "hbm_peak_gbs": hbm_peak, "peak_kind": peak_kind},
+            "roofline": {"bound": "alu", "achieved": round(alu_ach, 2), "peak": round(alu_peak, 1),
+                         "unit": "Gupd/s", "frac": round(alu_ach / alu_peak, 4),
+                         "traffic": (args.traffic if args.traffic is not None
+                                     else measured_traffic(args.workload)),
+                         "kernel": "bidir_scan_kernel", "kernel_ms": round(kern_ms, 5),
+                         "peak_basis": "148 SMs x 128 fp32 lanes x %.0f MHz / 4 fp32 ops per "
+                                       "update (recipe unit counts and max clock)" % sm_max,
+                         "hbm_gbs_kernel": round(spec.algorithmic_bytes() / scans
+                                                 / (kern_ms * 1e-3) / 1e9, 1),
+                         "hbm_peak_gbs": hbm_peak, "hbm_peak_kind": peak_kind},
             "gpu_launches": launches_per_step(spec.op) * args.steps,
             "clocks": clocks,
         }

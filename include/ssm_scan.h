@@ -29,9 +29,13 @@
  *  - `y` must not alias any input.  State and arithmetic are fp32; bf16
  *    outputs are rounded to nearest even.
  *  - `workspace` is device memory of at least ssm_workspace_bytes(...)
- *    bytes for the same arguments (NULL is fine when that is 0).  Its
- *    contents need no initialisation and are garbage afterwards.  Two calls
- *    in flight at once must not share a workspace.
+ *    bytes for the same arguments, 16-byte aligned (NULL is fine when that
+ *    is 0).  It holds a status word, the B and C tensors repacked per
+ *    position for the kernels, and (bidirectional forms) the fp32 outputs
+ *    of the branch that reaches a position first.  Its contents need no
+ *    initialisation and are garbage afterwards, except the status word read
+ *    by ssm_get_status.  Two calls in flight at once must not share a
+ *    workspace.
  *  - Calls are asynchronous on `stream` (0 = the legacy default stream).
  *    The library allocates nothing and keeps no global state, except the
  *    fixed scratch array that bimamba_scan_fwd_v2_noalloc uses.
@@ -40,7 +44,10 @@
  *    beyond the 32-bit index range; SSM_ERR_WORKSPACE when ws_bytes is too
  *    small; SSM_ERR_CUDA when a launch fails (cudaGetLastError is consumed);
  *    SSM_ERR_SCRATCH_LIMIT when a problem is too large for the fixed scratch
- *    of bimamba_scan_fwd_v2_noalloc.
+ *    of bimamba_scan_fwd_v2_noalloc;
+ *    SSM_ERR_TIMEOUT (through ssm_get_status, after the call's kernels ran)
+ *    when a kernel's bounded wait for its own bulk copies ran out; its
+ *    output is then incomplete.
  *    Every check happens before any launch: an error means nothing ran.
  *  - A call with B == 0, D == 0 or L == 0 is valid and launches nothing.
  */
@@ -69,7 +76,8 @@ typedef enum {
     SSM_ERR_UNSUPPORTED = 2,
     SSM_ERR_CUDA = 3,
     SSM_ERR_WORKSPACE = 4,
-    SSM_ERR_SCRATCH_LIMIT = 5
+    SSM_ERR_SCRATCH_LIMIT = 5,
+    SSM_ERR_TIMEOUT = 6
 } ssm_status;
 
 typedef enum {
@@ -154,6 +162,16 @@ SSM_API ssm_status ss2d_scan_fwd(ssm_dtype dt, int B, int D, int H, int W, int N
                          ssm_stream_t stream);
 
 /*
+ * Status of the last call that used `workspace`, once the work queued on
+ * `stream` before this call has finished (the call synchronises `stream`):
+ * *out = SSM_OK, or SSM_ERR_TIMEOUT when a kernel gave up a bounded wait.
+ * For selective_scan_fwd and bimamba_scan_fwd_v1/_v2 only.  Returns
+ * SSM_ERR_CUDA if the copy of the status word fails.
+ */
+SSM_API ssm_status ssm_get_status(const void *workspace, ssm_stream_t stream,
+                                  ssm_status *out);
+
+/*
  * Workspace bytes the call with these sizes needs (0 when none).
  * `L_or_HW` is L, or H*W for SS2D; K is ignored except for SS2D.
  * Returns (size_t)-1 for invalid sizes.
@@ -176,7 +194,7 @@ SSM_API size_t ssm_workspace_bytes(ssm_op op, ssm_dtype dt, int B, int D,
  * library holds those bytes until the process exits.
  *  - Problems whose workspace (ssm_workspace_bytes(SSM_OP_BIMAMBA_V2, ...))
  *    exceeds SSM_STATIC_SCRATCH_BYTES return SSM_ERR_SCRATCH_LIMIT before
- *    anything runs; B * D * L <= 16 Mi positions always fits.
+ *    anything runs.
  *  - The first call on a device (the one current on the calling thread,
  *    which must be the device `stream` belongs to) looks up the array's
  *    device address, once; make that first call before any stream capture.
@@ -199,6 +217,16 @@ SSM_API ssm_status bimamba_scan_fwd_v2_noalloc(
 
 /* Static description of a status code (never NULL). */
 SSM_API const char *ssm_status_string(ssm_status s);
+
+/*
+ * Profiling hook.  `begin` and `end` are cudaEvent_t handles (or both NULL
+ * to switch the hook off).  While set, every call made on this host thread
+ * records `begin` immediately before and `end` immediately after its scan
+ * kernel on the call's stream -- for ss2d_scan_fwd the row-pair scan, the
+ * last of its two -- so that cudaEventElapsedTime gives that kernel's
+ * duration.  The events stay owned by the caller.
+ */
+SSM_API void ssm_set_profile_events(void *begin, void *end);
 
 /* Library version, "major.minor.patch". */
 SSM_API const char *ssm_version(void);

@@ -27,7 +27,7 @@ _lib = ctypes.CDLL(_LIB_PATH)
 SSM_F32, SSM_BF16 = 0, 1
 OPS = {"single": 0, "v1": 1, "v2": 2, "ss2d": 3}
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA launch error",
-           4: "workspace", 5: "scratch limit"}
+           4: "workspace", 5: "scratch limit", 6: "timeout"}
 
 _vp, _fp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 _lib.selective_scan_fwd.argtypes = [_i] * 5 + [_vp] * 8 + [_i, _vp, _vp, _sz, _vp]
@@ -37,9 +37,13 @@ _lib.ss2d_scan_fwd.argtypes = [_i] * 7 + [_vp] * 8 + [_i, _vp, _vp, _sz, _vp]
 _lib.bimamba_scan_fwd_v2_noalloc.argtypes = [_i] * 5 + [_vp] * 15 + [_i, _f, _vp, _vp]
 _lib.ssm_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
 _lib.ssm_workspace_bytes.restype = _sz
+_lib.ssm_get_status.argtypes = [_vp, _vp, ctypes.POINTER(_i)]
+_lib.ssm_get_status.restype = _i
 _lib.ssm_status_string.argtypes = [_i]
 _lib.ssm_status_string.restype = ctypes.c_char_p
 _lib.ssm_version.restype = ctypes.c_char_p
+_lib.ssm_set_profile_events.argtypes = [_vp, _vp]
+_lib.ssm_set_profile_events.restype = None
 for _fn in (_lib.selective_scan_fwd, _lib.bimamba_scan_fwd_v1, _lib.bimamba_scan_fwd_v2,
             _lib.ss2d_scan_fwd, _lib.bimamba_scan_fwd_v2_noalloc):
     _fn.restype = _i
@@ -111,6 +115,25 @@ def _workspace(op, dtype, B, D, L, N, device, workspace, K=4):
     if not workspace.is_cuda or workspace.numel() * workspace.element_size() < need:
         raise ValueError("workspace must be a CUDA tensor of at least %d bytes" % need)
     return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
+
+def set_profile_events(begin=None, end=None) -> None:
+    """Record `begin` / `end` (torch.cuda.Event, already created by a first
+    record) around the scan kernel of every later call on this thread;
+    None switches the hook off."""
+    if begin is None or end is None:
+        _lib.ssm_set_profile_events(None, None)
+        return
+    _lib.ssm_set_profile_events(ctypes.c_void_p(begin.cuda_event), ctypes.c_void_p(end.cuda_event))
+
+
+def get_status(workspace, stream=None) -> int:
+    """Status word of the last call that used `workspace` (0 = ok, 6 = a
+    kernel's bounded wait ran out); synchronises the stream."""
+    out = _i(0)
+    _check(_lib.ssm_get_status(workspace.data_ptr(), _stream(stream), ctypes.byref(out)),
+           "ssm_get_status")
+    return out.value
 
 
 def _check(status, where):

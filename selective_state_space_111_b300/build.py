@@ -15,7 +15,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libssm_scan.so")
 SOURCES = [os.path.join(HERE, "csrc", "ssm_scan_api.cu")]
-DEPS = SOURCES + [os.path.join(HERE, "csrc", "scan_kernel.cuh"),
+DEPS = SOURCES + [os.path.join(HERE, "csrc", f) for f in
+                  ("bidir_kernel.cuh", "scan_ops.cuh")] + [
                   os.path.join(ROOT, "include", "ssm_scan.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

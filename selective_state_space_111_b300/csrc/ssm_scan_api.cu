@@ -11,57 +11,15 @@
 #include <cstdint>
 #include <mutex>
 
-#include "scan_kernel.cuh"
+#include "bidir_kernel.cuh"
 #include "ssm_scan.h"
 
 namespace {
 
-using ssm::KParams;
-using ssm::DirArgs;
-
-constexpr int kChunk = 32;      // time steps per chunk (T)
-constexpr int kRows = 16;       // channels per CTA (G)
-
 bool aligned(const void *p, unsigned a) { return ((uintptr_t)p % a) == 0; }
 
-// 2^31 - 1 bounds every per-dimension index the kernel forms in 32 bits.
+// 2^31 - 1 bounds every per-dimension index the kernels form in 32 bits.
 bool fits(long long v) { return v >= 0 && v <= 0x7fffffffLL; }
-
-int chunks_of(int L) { return (L + kChunk - 1) / kChunk; }
-
-template <typename IO, int S, int NDIR, int MAP, int MODE>
-ssm_status launch(const KParams &P, cudaStream_t stream) {
-    using SM = ssm::Smem<IO, S, NDIR, kRows, kChunk>;
-    constexpr int NT = NDIR * kRows * (ssm::kMaxN / S);
-    auto *kern = &ssm::scan_kernel<IO, S, NDIR, kRows, kChunk, MAP, MODE>;
-    // Raising the dynamic shared-memory limit is cheap and idempotent.
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::bytes) !=
-        cudaSuccess) {
-        cudaGetLastError();
-        return SSM_ERR_CUDA;
-    }
-    dim3 grid((P.D + kRows - 1) / kRows, P.B);
-    kern<<<grid, NT, SM::bytes, stream>>>(P);
-    return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
-}
-
-// Pick the states-per-lane variant: 4 states per lane (more threads) unless
-// the problem has enough rows to keep every SM busy with 8 per lane.
-int pick_S(long long rows, int ndir) {
-    const long long lanes8 = rows * ndir * 2;     // threads at S = 8
-    return lanes8 >= 148LL * 384 ? 8 : 4;
-}
-
-template <int NDIR, int MAP, int MODE>
-ssm_status dispatch(ssm_dtype dt, const KParams &P, cudaStream_t st) {
-    const int S = pick_S((long long)P.B * P.D, NDIR);
-    if (dt == SSM_F32) {
-        return S == 8 ? launch<float, 8, NDIR, MAP, MODE>(P, st)
-                      : launch<float, 4, NDIR, MAP, MODE>(P, st);
-    }
-    return S == 8 ? launch<__nv_bfloat16, 8, NDIR, MAP, MODE>(P, st)
-                  : launch<__nv_bfloat16, 4, NDIR, MAP, MODE>(P, st);
-}
 
 ssm_status check_common(ssm_dtype dt, int B, int D, int L, int N) {
     if (dt != SSM_F32 && dt != SSM_BF16) return SSM_ERR_INVALID_ARG;
@@ -77,38 +35,121 @@ bool opt_io_ok(const void *p) { return p == nullptr || aligned(p, 16); }
 bool f32_ok(const float *p) { return p != nullptr && aligned(p, 4); }
 bool opt_f32_ok(const float *p) { return p == nullptr || aligned(p, 4); }
 
-size_t bidir_ws(int B, int D, int L) {
-    return chunks_of(L) > 1 ? (size_t)B * D * L * sizeof(float) : 0;
+// ---- single / bidirectional path (bidir_kernel.cuh)
+// Workspace: [256-byte header: status word][packed B/C of the forward
+// branch][packed B/C of the backward branch (v2)][fp32 stash W (two
+// branches, more than one chunk)].  Every region starts on 128 bytes.
+constexpr size_t kHeaderBytes = 256;
+#ifndef SSM_BI_S
+#define SSM_BI_S 8
+#endif
+#ifndef SSM_BI_G2
+#define SSM_BI_G2 8
+#endif
+#ifndef SSM_BI_G1
+#define SSM_BI_G1 16
+#endif
+constexpr int kBiT = 32;                   // positions per chunk
+constexpr int kBiS = SSM_BI_S;             // states per lane
+constexpr int kBiG2 = SSM_BI_G2;           // channels per CTA, two branches
+constexpr int kBiG1 = SSM_BI_G1;           // channels per CTA, one branch
+
+int bi_chunks(int L) { return (L + kBiT - 1) / kBiT; }
+size_t bc_bytes(int B, int L) { return (size_t)B * L * ssm::kBC * sizeof(float); }
+
+struct BiWs {
+    size_t bc0, bc1, w, total;
+};
+// bc_sets: 1 (single, v1) or 2 (v2); stash only with two branches.
+BiWs bi_ws(int bc_sets, int ndir, int B, int D, int L) {
+    BiWs w;
+    size_t off = kHeaderBytes;
+    w.bc0 = off;
+    off += bc_bytes(B, L);
+    w.bc1 = w.bc0;
+    if (bc_sets == 2) {
+        w.bc1 = off;
+        off += bc_bytes(B, L);
+    }
+    w.w = 0;
+    if (ndir == 2 && bi_chunks(L) > 1) {
+        w.w = off;
+        off += (size_t)B * D * L * sizeof(float);
+    }
+    w.total = off;
+    return w;
 }
 
-void fill_dir(DirArgs &a, const void *dt, long long dt_off, long long dt_bs, long long dt_total,
-              const void *Bm, const void *Cm, long long bc_off, long long bc_bs,
-              long long bc_total, const float *A, const float *Dskip, const float *bias,
-              const void *u, int stream_rev) {
-    a.dt = dt;
-    a.dt_off = dt_off;
-    a.dt_bs = dt_bs;
-    a.dt_total = dt_total;
-    a.Bm = Bm;
-    a.Cm = Cm;
-    a.bc_off = bc_off;
-    a.bc_bs = bc_bs;
-    a.bc_total = bc_total;
-    a.A = A;
-    a.Dskip = Dskip;
-    a.bias = bias;
-    a.u = u;
-    a.stream_rev = stream_rev;
+template <typename IO>
+ssm_status launch_pack(const void *Bm, const void *Cm, float *out, int B, int N, int L,
+                       unsigned *status, cudaStream_t st, int K = 1) {
+    dim3 grid((L + 63) / 64, B, K);
+    ssm::pack_bc_kernel<IO><<<grid, 256, 0, st>>>((const IO *)Bm, (const IO *)Cm, out, N, L,
+                                                  status);
+    return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
-// Shared body of v1 / v2 (v1 passes the forward tensors for both branches).
+// Profiling hook (ssm_set_profile_events): events recorded around the last
+// scan-kernel launch of each call made on this host thread.
+thread_local cudaEvent_t t_prof_begin = nullptr, t_prof_end = nullptr;
+
+template <typename IO, int S, int NDIR, int G, int OUT = ssm::OUT_Y>
+ssm_status launch_bidir(const ssm::BiParams &P, cudaStream_t st, bool last = true) {
+    using LY = ssm::BiLayout<IO, S, NDIR, G, kBiT>;
+    auto *kern = &ssm::bidir_scan_kernel<IO, S, NDIR, G, kBiT, OUT>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::bytes) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return SSM_ERR_CUDA;
+    }
+    // every bulk copy starts at base + a multiple of 16 bytes from these
+    // bases, so they must all be 16-byte aligned (checked, never assumed)
+    for (int d = 0; d < NDIR; ++d) {
+        if (!aligned(P.br[d].dt, 16) || !aligned(P.br[d].u, 16) || !aligned(P.br[d].bc, 16))
+            return SSM_ERR_INVALID_ARG;
+    }
+    if (!aligned(P.z, 16) || !aligned(P.W, 16) || !aligned(P.acc_in, 16))
+        return SSM_ERR_INVALID_ARG;
+    dim3 grid((P.D + G - 1) / G, P.B);
+    const bool prof = last && t_prof_begin != nullptr && t_prof_end != nullptr;
+    if (prof && cudaEventRecord(t_prof_begin, st) != cudaSuccess) {
+        cudaGetLastError();
+        return SSM_ERR_CUDA;
+    }
+    kern<<<grid, LY::NT, LY::bytes, st>>>(P);
+    if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
+    if (prof && cudaEventRecord(t_prof_end, st) != cudaSuccess) {
+        cudaGetLastError();
+        return SSM_ERR_CUDA;
+    }
+    return SSM_OK;
+}
+
+// Packs B/C (one or two sets), then runs the scan kernel.
+template <typename IO, int NDIR>
+ssm_status run_bidir(ssm::BiParams P, const void *Bm, const void *Cm, const void *Bm_b,
+                     const void *Cm_b, bool two_sets, cudaStream_t st) {
+    ssm_status s = launch_pack<IO>(Bm, Cm, const_cast<float *>(P.br[0].bc), P.B, P.N, P.L,
+                                   P.status, st);
+    if (s != SSM_OK) return s;
+    if (two_sets) {
+        s = launch_pack<IO>(Bm_b, Cm_b, const_cast<float *>(P.br[1].bc), P.B, P.N, P.L,
+                            nullptr, st);
+        if (s != SSM_OK) return s;
+    }
+    if (NDIR == 2) return launch_bidir<IO, kBiS, 2, kBiG2>(P, st);
+    return launch_bidir<IO, kBiS, 1, kBiG1>(P, st);
+}
+
+// Shared body of v1 / v2 (v1 passes the forward tensors for both branches
+// and a single B/C set).
 ssm_status bidirectional(ssm_dtype dt, int B, int D, int L, int N, const void *u,
                          const void *u_b, const void *delta, const void *delta_b,
                          const float *A, const float *A_b, const void *Bm, const void *Cm,
                          const void *Bm_b, const void *Cm_b, const float *Dskip,
                          const float *D_b, const void *z, const float *bias,
                          const float *bias_b, int delta_softplus, float out_scale, void *y,
-                         void *ws, size_t ws_bytes, cudaStream_t stream) {
+                         void *ws, size_t ws_bytes, bool two_sets, cudaStream_t stream) {
     ssm_status s = check_common(dt, B, D, L, N);
     if (s != SSM_OK) return s;
     if (!io_ok(u) || !opt_io_ok(u_b) || !io_ok(delta) || !io_ok(delta_b) || !io_ok(Bm) ||
@@ -116,30 +157,124 @@ ssm_status bidirectional(ssm_dtype dt, int B, int D, int L, int N, const void *u
         !f32_ok(A) || !f32_ok(A_b) || !opt_f32_ok(Dskip) || !opt_f32_ok(D_b) ||
         !opt_f32_ok(bias) || !opt_f32_ok(bias_b))
         return SSM_ERR_INVALID_ARG;
-    const size_t need = bidir_ws(B, D, L);
-    if (need > 0 && (ws == nullptr || ws_bytes < need || !aligned(ws, 16)))
-        return SSM_ERR_WORKSPACE;
     if ((long long)B * D * L == 0) return SSM_OK;
-    const long long tot = (long long)B * D * L, bct = (long long)B * N * L;
-    KParams P{};
-    fill_dir(P.dir[0], delta, 0, (long long)D * L, tot, Bm, Cm, 0, (long long)N * L, bct, A,
-             Dskip, bias, u, 0);
-    fill_dir(P.dir[1], delta_b, 0, (long long)D * L, tot, Bm_b, Cm_b, 0, (long long)N * L, bct,
-             A_b, D_b, bias_b, u_b ? u_b : u, 0);
+    const BiWs lay = bi_ws(two_sets ? 2 : 1, 2, B, D, L);
+    if (ws == nullptr || ws_bytes < lay.total || !aligned(ws, 16)) return SSM_ERR_WORKSPACE;
+    char *wsb = (char *)ws;
+    ssm::BiParams P{};
+    const long long DL = (long long)D * L, tot = (long long)B * D * L;
+    P.br[0] = {delta, u, (const float *)(wsb + lay.bc0), A, Dskip, bias, 0, DL, tot, 0};
+    P.br[1] = {delta_b, u_b ? u_b : u, (const float *)(wsb + lay.bc1), A_b, D_b, bias_b,
+               0, DL, tot, 0};
     P.z = z;
     P.y = y;
-    P.W = (float *)ws;
-    P.u_total = tot;
+    P.W = lay.w ? (float *)(wsb + lay.w) : nullptr;
+    P.status = (unsigned *)wsb;
+    P.total = (long long)B * D * L;
     P.B = B;
     P.D = D;
     P.L = L;
     P.N = N;
-    P.H = 1;
-    P.Wd = L;
-    P.nchunks = chunks_of(L);
+    P.nchunks = bi_chunks(L);
     P.delta_softplus = delta_softplus ? 1 : 0;
     P.out_scale = out_scale;
-    return dispatch<2, ssm::MAP_ROW, ssm::MODE_FINAL>(dt, P, stream);
+    if (dt == SSM_F32) return run_bidir<float, 2>(P, Bm, Cm, Bm_b, Cm_b, two_sets, stream);
+    return run_bidir<__nv_bfloat16, 2>(P, Bm, Cm, Bm_b, Cm_b, two_sets, stream);
+}
+
+// ---- SS2D (VMamba cross-scan / cross-merge)
+// Directions 0/2 walk the map row-major forward/backward and 1/3 walk it
+// column-major forward/backward; each direction's delta and B/C are in its
+// own scan order.  The column pair runs on the map transposed per channel
+// (x^T), so both pairs are contiguous sequences of L = H * W positions:
+//   1. pack B/C of the four directions;          2. x^T = transpose(x);
+//   3. column pair (1, 3) on x^T -> Wt = y1 + y3 (fp32, column-major);
+//   4. Wa = transpose(Wt);
+//   5. row pair (0, 2) on x: y = gate(y0 + y2 + Wa, z).
+// Workspace: [header][packed B/C, 4 directions][x^T][R1][R2] where R1 is
+// the column pair's stash and then Wa, and R2 is Wt and then the row pair's
+// stash.
+struct SsWs {
+    size_t bc, xt, r1, r2, total;
+};
+size_t round128(size_t v) { return (v + 127) & ~(size_t)127; }
+SsWs ss2d_ws(ssm_dtype dt, int B, int D, int L) {
+    const size_t es = dt == SSM_F32 ? 4 : 2;
+    const size_t n = (size_t)B * D * L;
+    SsWs w;
+    w.bc = kHeaderBytes;
+    w.xt = w.bc + 4 * bc_bytes(B, L);
+    w.r1 = w.xt + round128(n * es);
+    w.r2 = w.r1 + round128(n * 4);
+    w.total = w.r2 + round128(n * 4);
+    return w;
+}
+
+template <typename E>
+ssm_status launch_transpose(const E *in, E *out, int maps, int R, int C, cudaStream_t st) {
+    dim3 grid((C + 31) / 32, (R + 31) / 32, maps < 65535 ? maps : 65535);
+    ssm::transpose_maps_kernel<E><<<grid, 256, 0, st>>>(in, out, maps, R, C);
+    return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+template <typename IO>
+ssm_status ss2d_run(int B, int D, int H, int W, int N, const void *x, const void *delta,
+                    const float *A, const void *Bm, const void *Cm, const float *Dskip,
+                    const void *z, const float *bias, int delta_softplus, void *y, char *wsb,
+                    const SsWs &lay, cudaStream_t st) {
+    const int L = H * W;
+    const long long DL = (long long)D * L, n = (long long)B * D * L;
+    float *bcK = (float *)(wsb + lay.bc);
+    IO *xt = (IO *)(wsb + lay.xt);
+    float *r1 = (float *)(wsb + lay.r1), *r2 = (float *)(wsb + lay.r2);
+    unsigned *status = (unsigned *)wsb;
+    ssm_status s = launch_pack<IO>(Bm, Cm, bcK, B, N, L, status, st, 4);
+    if (s != SSM_OK) return s;
+    s = launch_transpose<IO>((const IO *)x, xt, B * D, H, W, st);
+    if (s != SSM_OK) return s;
+    auto branch = [&](int k, const void *u, int rev) {
+        ssm::BiBranch br;
+        br.dt = delta;
+        br.dt_off = k * DL;
+        br.u = u;
+        br.bc = bcK + (long long)k * B * L * ssm::kBC;
+        br.A = A + (long long)k * D * N;
+        br.Dskip = Dskip ? Dskip + (long long)k * D : nullptr;
+        br.bias = bias ? bias + (long long)k * D : nullptr;
+        br.dt_bstride = 4 * DL;
+        br.dt_total = 4 * n;
+        br.stream_rev = rev;
+        return br;
+    };
+    ssm::BiParams P{};
+    P.status = status;
+    P.total = n;
+    P.B = B;
+    P.D = D;
+    P.L = L;
+    P.N = N;
+    P.nchunks = bi_chunks(L);
+    P.delta_softplus = delta_softplus ? 1 : 0;
+    P.out_scale = 1.f;
+    // column pair on x^T: the fused sum goes to Wt (R2), stash in R1
+    P.br[0] = branch(1, xt, 0);
+    P.br[1] = branch(3, xt, 1);
+    P.W = r1;
+    P.acc_out = r2;
+    s = launch_bidir<IO, kBiS, 2, kBiG2, ssm::OUT_ACC>(P, st, false);
+    if (s != SSM_OK) return s;
+    // Wa (R1) = Wt (R2) transposed back to H x W
+    s = launch_transpose<float>(r2, r1, B * D, W, H, st);
+    if (s != SSM_OK) return s;
+    // row pair on x: y = gate(y0 + y2 + Wa), stash in R2
+    P.br[0] = branch(0, x, 0);
+    P.br[1] = branch(2, x, 1);
+    P.z = z;
+    P.y = y;
+    P.W = r2;
+    P.acc_in = r1;
+    P.acc_out = nullptr;
+    return launch_bidir<IO, kBiS, 2, kBiG2, ssm::OUT_ADD_Y>(P, st);
 }
 
 // ---- fixed scratch of the allocation-free entry point
@@ -181,33 +316,35 @@ ssm_status selective_scan_fwd(ssm_dtype dt, int B, int D, int L, int N, const vo
                               const void *Cm, const float *Dskip, const void *z,
                               const float *delta_bias, int delta_softplus, void *y,
                               void *workspace, size_t ws_bytes, ssm_stream_t stream) {
-    (void)workspace;
-    (void)ws_bytes;
     ssm_status s = check_common(dt, B, D, L, N);
     if (s != SSM_OK) return s;
     if (!io_ok(u) || !io_ok(delta) || !io_ok(Bm) || !io_ok(Cm) || !opt_io_ok(z) ||
         !io_ok(y) || !f32_ok(A) || !opt_f32_ok(Dskip) || !opt_f32_ok(delta_bias))
         return SSM_ERR_INVALID_ARG;
     if ((long long)B * D * L == 0) return SSM_OK;
-    const long long tot = (long long)B * D * L, bct = (long long)B * N * L;
-    KParams P{};
-    fill_dir(P.dir[0], delta, 0, (long long)D * L, tot, Bm, Cm, 0, (long long)N * L, bct, A,
-             Dskip, delta_bias, u, 0);
-    P.dir[1] = P.dir[0];
+    const BiWs lay = bi_ws(1, 1, B, D, L);
+    if (workspace == nullptr || ws_bytes < lay.total || !aligned(workspace, 16))
+        return SSM_ERR_WORKSPACE;
+    char *wsb = (char *)workspace;
+    ssm::BiParams P{};
+    P.br[0] = {delta, u, (const float *)(wsb + lay.bc0), A, Dskip, delta_bias, 0,
+               (long long)D * L, (long long)B * D * L, 0};
+    P.br[1] = P.br[0];
     P.z = z;
     P.y = y;
     P.W = nullptr;
-    P.u_total = tot;
+    P.status = (unsigned *)wsb;
+    P.total = (long long)B * D * L;
     P.B = B;
     P.D = D;
     P.L = L;
     P.N = N;
-    P.H = 1;
-    P.Wd = L;
-    P.nchunks = chunks_of(L);
+    P.nchunks = bi_chunks(L);
     P.delta_softplus = delta_softplus ? 1 : 0;
     P.out_scale = 1.f;
-    return dispatch<1, ssm::MAP_ROW, ssm::MODE_FINAL>(dt, P, (cudaStream_t)stream);
+    cudaStream_t st = (cudaStream_t)stream;
+    if (dt == SSM_F32) return run_bidir<float, 1>(P, Bm, Cm, Bm, Cm, false, st);
+    return run_bidir<__nv_bfloat16, 1>(P, Bm, Cm, Bm, Cm, false, st);
 }
 
 ssm_status bimamba_scan_fwd_v1(ssm_dtype dt, int B, int D, int L, int N, const void *u,
@@ -218,7 +355,7 @@ ssm_status bimamba_scan_fwd_v1(ssm_dtype dt, int B, int D, int L, int N, const v
                                ssm_stream_t stream) {
     return bidirectional(dt, B, D, L, N, u, nullptr, delta, delta, A, A_b, Bm, Cm, Bm, Cm,
                          Dskip, Dskip, z, delta_bias, delta_bias, delta_softplus, out_scale, y,
-                         workspace, ws_bytes, (cudaStream_t)stream);
+                         workspace, ws_bytes, false, (cudaStream_t)stream);
 }
 
 ssm_status bimamba_scan_fwd_v2(ssm_dtype dt, int B, int D, int L, int N, const void *u,
@@ -231,7 +368,7 @@ ssm_status bimamba_scan_fwd_v2(ssm_dtype dt, int B, int D, int L, int N, const v
                                size_t ws_bytes, ssm_stream_t stream) {
     return bidirectional(dt, B, D, L, N, u, u_b, delta, delta_b, A, A_b, Bm, Cm, Bm_b, Cm_b,
                          Dskip, D_b, z, delta_bias, delta_bias_b, delta_softplus, out_scale, y,
-                         workspace, ws_bytes, (cudaStream_t)stream);
+                         workspace, ws_bytes, true, (cudaStream_t)stream);
 }
 
 ssm_status bimamba_scan_fwd_v2_noalloc(ssm_dtype dt, int B, int D, int L, int N,
@@ -244,13 +381,13 @@ ssm_status bimamba_scan_fwd_v2_noalloc(ssm_dtype dt, int B, int D, int L, int N,
                                        float out_scale, void *y, ssm_stream_t stream) {
     ssm_status s = check_common(dt, B, D, L, N);
     if (s != SSM_OK) return s;
-    if (bidir_ws(B, D, L) > SSM_STATIC_SCRATCH_BYTES) return SSM_ERR_SCRATCH_LIMIT;
+    if (bi_ws(2, 2, B, D, L).total > SSM_STATIC_SCRATCH_BYTES) return SSM_ERR_SCRATCH_LIMIT;
     void *scratch = nullptr;
     s = static_scratch(&scratch);
     if (s != SSM_OK) return s;
     return bidirectional(dt, B, D, L, N, u, u_b, delta, delta_b, A, A_b, Bm, Cm, Bm_b, Cm_b,
                          Dskip, D_b, z, delta_bias, delta_bias_b, delta_softplus, out_scale, y,
-                         scratch, SSM_STATIC_SCRATCH_BYTES, (cudaStream_t)stream);
+                         scratch, SSM_STATIC_SCRATCH_BYTES, true, (cudaStream_t)stream);
 }
 
 ssm_status ss2d_scan_fwd(ssm_dtype dt, int B, int D, int H, int W, int N, int K,
@@ -268,40 +405,17 @@ ssm_status ss2d_scan_fwd(ssm_dtype dt, int B, int D, int H, int W, int N, int K,
     if (!io_ok(x) || !io_ok(delta) || !io_ok(Bm) || !io_ok(Cm) || !opt_io_ok(z) ||
         !io_ok(y) || !f32_ok(A) || !opt_f32_ok(Dskip) || !opt_f32_ok(delta_bias))
         return SSM_ERR_INVALID_ARG;
-    const size_t need = ssm_workspace_bytes(SSM_OP_SS2D, dt, B, D, L, N, K);
-    if (need > 0 && (workspace == nullptr || ws_bytes < need || !aligned(workspace, 16)))
-        return SSM_ERR_WORKSPACE;
     if ((long long)B * D * L == 0) return SSM_OK;
-    const long long DL = (long long)D * L, NL = (long long)N * L;
-    const long long dtot = (long long)B * K * DL, bct = (long long)B * K * NL;
-    auto dir = [&](DirArgs &a, int k, int stream_rev) {
-        fill_dir(a, delta, k * DL, K * DL, dtot, Bm, Cm, k * NL, K * NL, bct,
-                 A + (long long)k * D * N, Dskip ? Dskip + (long long)k * D : nullptr,
-                 delta_bias ? delta_bias + (long long)k * D : nullptr, x, stream_rev);
-    };
-    KParams P{};
-    P.z = z;
-    P.y = y;
-    P.W = (float *)workspace;
-    P.u_total = (long long)B * DL;
-    P.B = B;
-    P.D = D;
-    P.L = L;
-    P.N = N;
-    P.H = H;
-    P.Wd = W;
-    P.nchunks = chunks_of(L);
-    P.delta_softplus = delta_softplus ? 1 : 0;
-    P.out_scale = 1.f;
-    // Row-major pair: directions 0 (forward) and 2 (reversed), fused sum to W.
-    dir(P.dir[0], 0, 0);
-    dir(P.dir[1], 2, 1);
-    s = dispatch<2, ssm::MAP_ROW, ssm::MODE_ACCOUT>(dt, P, (cudaStream_t)stream);
-    if (s != SSM_OK) return s;
-    // Column-major pair: directions 1 and 3; adds W, gates and stores y.
-    dir(P.dir[0], 1, 0);
-    dir(P.dir[1], 3, 1);
-    return dispatch<2, ssm::MAP_COL, ssm::MODE_ACCIN>(dt, P, (cudaStream_t)stream);
+    const SsWs lay = ss2d_ws(dt, B, D, L);
+    if (workspace == nullptr || ws_bytes < lay.total || !aligned(workspace, 16))
+        return SSM_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    return dt == SSM_F32 ? ss2d_run<float>(B, D, H, W, N, x, delta, A, Bm, Cm, Dskip, z,
+                                           delta_bias, delta_softplus, y, (char *)workspace,
+                                           lay, st)
+                         : ss2d_run<__nv_bfloat16>(B, D, H, W, N, x, delta, A, Bm, Cm, Dskip, z,
+                                                   delta_bias, delta_softplus, y,
+                                                   (char *)workspace, lay, st);
 }
 
 size_t ssm_workspace_bytes(ssm_op op, ssm_dtype dt, int B, int D, int L_or_HW, int N, int K) {
@@ -310,15 +424,29 @@ size_t ssm_workspace_bytes(ssm_op op, ssm_dtype dt, int B, int D, int L_or_HW, i
     if (B < 0 || D < 0 || L_or_HW < 0) return (size_t)-1;
     switch (op) {
     case SSM_OP_SELECTIVE_SCAN:
-        return 0;
+        return bi_ws(1, 1, B, D, L_or_HW).total;
     case SSM_OP_BIMAMBA_V1:
+        return bi_ws(1, 2, B, D, L_or_HW).total;
     case SSM_OP_BIMAMBA_V2:
-        return bidir_ws(B, D, L_or_HW);
+        return bi_ws(2, 2, B, D, L_or_HW).total;
     case SSM_OP_SS2D:
         if (K != 4) return (size_t)-1;
-        return (size_t)B * D * L_or_HW * sizeof(float);
+        return ss2d_ws(dt, B, D, L_or_HW).total;
     }
     return (size_t)-1;
+}
+
+ssm_status ssm_get_status(const void *workspace, ssm_stream_t stream, ssm_status *out) {
+    if (workspace == nullptr || out == nullptr) return SSM_ERR_INVALID_ARG;
+    unsigned word = 0;
+    if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost,
+                        (cudaStream_t)stream) != cudaSuccess ||
+        cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) {
+        cudaGetLastError();
+        return SSM_ERR_CUDA;
+    }
+    *out = word ? SSM_ERR_TIMEOUT : SSM_OK;
+    return SSM_OK;
 }
 
 const char *ssm_status_string(ssm_status s) {
@@ -328,12 +456,18 @@ const char *ssm_status_string(ssm_status s) {
     case SSM_ERR_UNSUPPORTED: return "unsupported size or option";
     case SSM_ERR_CUDA: return "CUDA launch error";
     case SSM_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case SSM_ERR_TIMEOUT: return "a kernel's bounded wait for its own copies ran out";
     case SSM_ERR_SCRATCH_LIMIT:
         return "problem needs more scratch than the library's fixed 64 MiB array";
     }
     return "unknown status";
 }
 
-const char *ssm_version(void) { return "0.1.0"; }
+void ssm_set_profile_events(void *begin, void *end) {
+    t_prof_begin = (cudaEvent_t)begin;
+    t_prof_end = (cudaEvent_t)end;
+}
+
+const char *ssm_version(void) { return "0.2.0"; }
 
 }  // extern "C"

@@ -27,7 +27,7 @@ def declared_functions():
 def test_header_declares_the_operations():
     names = set(declared_functions())
     assert {"selective_scan_fwd", "bimamba_scan_fwd_v1", "bimamba_scan_fwd_v2", "ss2d_scan_fwd",
-            "ssm_workspace_bytes", "ssm_status_string", "ssm_version"} <= names
+            "ssm_workspace_bytes", "ssm_get_status", "ssm_status_string", "ssm_version"} <= names
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -36,18 +36,20 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    for code in range(5):
+    for code in range(7):
         assert lib.ssm_status_string(code)
     assert re.match(rb"^\d+\.\d+\.\d+$", lib.ssm_version())
 
 
 def test_workspace_bytes(lib):
     ws = lib.ssm_workspace_bytes
-    assert ws(0, 1, 8, 768, 6085, 16, 4) == 0                      # single: none
-    assert ws(2, 1, 8, 768, 6085, 16, 4) == 8 * 768 * 6085 * 4     # v2: fp32 per position
-    assert ws(1, 1, 2, 1536, 4096, 16, 4) == 2 * 1536 * 4096 * 4
-    assert ws(2, 1, 4, 8, 20, 16, 4) == 0                          # one chunk: in shared memory
-    assert ws(3, 1, 32, 192, 3136, 16, 4) == 32 * 192 * 3136 * 4   # SS2D: the pair sum
+    hdr, bc = 256, 32 * 4          # status header; packed B/C: 32 fp32 per (batch, position)
+    assert ws(0, 1, 8, 768, 6085, 16, 4) == hdr + 8 * 6085 * bc            # single
+    assert ws(2, 1, 8, 768, 6085, 16, 4) == hdr + 2 * 8 * 6085 * bc + 8 * 768 * 6085 * 4
+    assert ws(1, 1, 2, 1536, 4096, 16, 4) == hdr + 2 * 4096 * bc + 2 * 1536 * 4096 * 4
+    assert ws(2, 1, 4, 8, 20, 16, 4) == hdr + 2 * 4 * 20 * bc     # one chunk: no stash
+    n = 32 * 192 * 3136                                           # SS2D: B/C of 4 directions,
+    assert ws(3, 1, 32, 192, 3136, 16, 4) == hdr + 4 * 32 * 3136 * bc + 2 * n + 2 * 4 * n  # x^T, 2 fp32
     assert ws(3, 1, 32, 192, 3136, 16, 2) == ctypes.c_size_t(-1).value
     assert ws(0, 7, 1, 1, 1, 16, 4) == ctypes.c_size_t(-1).value   # bad dtype
 

@@ -74,7 +74,7 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(lib, io):
         spec = Spec("v2", io, B=B, D=D, L=L, perturb=True, shared_u=(k == 0), out_scale=0.5)
         g = to_dev(make_inputs(spec, 7100 + k))
         y_ref = torch.empty_like(g["u"])
-        need = B * D * L * 4
+        need = lib.ssm_workspace_bytes(2, 0 if io == "f32" else 1, B, D, L, 16, 4)
         ws = torch.empty(need, dtype=torch.uint8, device="cuda")
         assert _call_workspace(lib, g, y_ref, ws, stream) == 0
         y = torch.full_like(g["u"], float("nan"))
@@ -90,7 +90,7 @@ FAKE = 0x10000   # 16-byte aligned, never dereferenced: the call is refused firs
 
 
 def test_noalloc_refuses_problems_beyond_its_scratch(lib):
-    # B * D * L * 4 bytes of scratch: one position beyond 64 MiB.
+    # the stash alone (B * D * L fp32) is beyond 64 MiB
     B, D, L = 1, 1, SCRATCH_BYTES // 4 + 1
     st = lib.bimamba_scan_fwd_v2_noalloc(1, B, D, L, 16, FAKE, None, FAKE, FAKE, FAKE, FAKE,
                                          FAKE, FAKE, FAKE, FAKE, None, None, None, None, None,
