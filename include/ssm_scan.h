@@ -228,6 +228,16 @@ SSM_API const char *ssm_status_string(ssm_status s);
  */
 SSM_API void ssm_set_profile_events(void *begin, void *end);
 
+/*
+ * Test hook for the failure path.  The next scan-kernel launch made on this
+ * host thread never issues the bulk copy of B/C for chunk `chunk` (>= 0), so
+ * the scan's bounded wait for it runs out after about two seconds; the kernel
+ * then stops, sets the status word and leaves its output incomplete, and
+ * ssm_get_status reports SSM_ERR_TIMEOUT.  Nothing faults or hangs.  The
+ * hook applies to one launch only; -1 clears it.
+ */
+SSM_API void ssm_test_withhold_copy(int chunk);
+
 /* Library version, "major.minor.patch". */
 SSM_API const char *ssm_version(void);
 

@@ -42,6 +42,8 @@ _lib.ssm_get_status.restype = _i
 _lib.ssm_status_string.argtypes = [_i]
 _lib.ssm_status_string.restype = ctypes.c_char_p
 _lib.ssm_version.restype = ctypes.c_char_p
+_lib.ssm_test_withhold_copy.argtypes = [_i]
+_lib.ssm_test_withhold_copy.restype = None
 _lib.ssm_set_profile_events.argtypes = [_vp, _vp]
 _lib.ssm_set_profile_events.restype = None
 for _fn in (_lib.selective_scan_fwd, _lib.bimamba_scan_fwd_v1, _lib.bimamba_scan_fwd_v2,

@@ -97,6 +97,7 @@ struct BiParams {
     int nchunks;
     int delta_softplus;
     float out_scale;
+    int withhold_bc;       // test hook: chunk whose B/C copy is never issued (-1: none)
 };
 
 // ------------------------------------------------------------------ pack
@@ -154,40 +155,45 @@ transpose_maps_kernel(const E *__restrict__ in, E *__restrict__ out, int maps, i
 }
 
 // ------------------------------------------------------------------ layout
-template <typename IO, int S, int NDIR, int G, int T>
-struct BiLayout {
+// One CTA = R channels of one batch element x NDIR branches, in warps with
+// three roles linked by full/empty mbarrier rings (T = 32 positions per
+// chunk, one lane per position in the prep and epilogue roles):
+//   scan warps  (NSW)  lane = (branch, channel, state group)
+//   prep warps  (NPW)  16 rows each: delta and w = delta*u from dt, u
+//   epi warps   (NEW)  16 rows each (both branches of 16/NDIR channels):
+//                      readout sums, D*u, fusion, gate, stores; lane 0 of
+//                      the first epilogue warp also issues the B/C copies
+template <typename IO, int S, int NDIR, int R>
+struct WsLayout {
+    static constexpr int T = 32;
     static constexpr int LPR = kMaxN / S;
-    static constexpr int NT = NDIR * G * LPR;
-    static constexpr int VEC = 16 / (int)sizeof(IO);       // elements per 16 B
-    static constexpr int NRAW = 3;                         // raw ring depth
-    static constexpr int NBC = 2;                          // B/C ring depth
-    static constexpr int RC = T + 2 * VEC;                 // raw row capacity
-    static constexpr int RAW_ROW = RC * (int)sizeof(IO);   // bytes
-    static constexpr int RAW_DIR = 3 * G * RAW_ROW;        // dt[G], u[G], z[G]
-    static constexpr int RAW_STAGE = NDIR * RAW_DIR;
-    static constexpr int W_CAP = T + 8;                    // fp32 covering capacity
-    static constexpr int W_ROW = W_CAP * 4;
+    static constexpr int ROWS = NDIR * R;                   // (branch, channel) rows
+    static constexpr int NSW = ROWS * LPR / 32;
+    static constexpr int NPW = ROWS / 16;
+    static constexpr int NEW = ROWS / 16;
+    static constexpr int CPE = 16 / NDIR;                   // channels per epilogue warp
+    static constexpr int NT = (NSW + NPW + NEW) * 32;
+    static constexpr int NBC = 2;                           // B/C ring
     static constexpr int BC_DIR = T * kBC * 4;
     static constexpr int BC_STAGE = NDIR * BC_DIR;
-    static constexpr int DW_ROW = T * 16 + 16;             // float4 per step, padded
-    static constexpr int YP_ROW = (T * LPR + LPR) * 4;     // padded: banks spread
+    static constexpr int DW_ROW = T * 16 + 16;              // float4 per step, padded
+    static constexpr int DW_STAGE = ROWS * DW_ROW;
+    static constexpr int YP_ROW = (T * LPR + LPR) * 4;      // padded: banks spread
+    static constexpr int YP_STAGE = ROWS * YP_ROW;
+    static constexpr int off_bc = 0;                        // 128-byte aligned
+    static constexpr int off_dw = off_bc + NBC * BC_STAGE;
+    static constexpr int off_yp = off_dw + 2 * DW_STAGE;
+    static constexpr int off_bar = (off_yp + 2 * YP_STAGE + 7) & ~7;
+    // bc_full[NBC], dw_full[2], dw_empty[2], yp_full[2], yp_empty[2]
+    static constexpr int NBAR = NBC + 8;
+    static constexpr int off_flag = off_bar + NBAR * 8;
+    static constexpr int bytes = off_flag + 16;
 
-    static constexpr int off_bc = 0;                       // 128-byte aligned
-    static constexpr int off_raw = off_bc + NBC * BC_STAGE;
-    static constexpr int off_w = off_raw + NRAW * RAW_STAGE;
-    static constexpr int off_dw = off_w + 2 * NDIR * G * W_ROW;   // stash, acc_in
-    static constexpr int off_yp = off_dw + NDIR * G * DW_ROW;
-    static constexpr int off_bar = (off_yp + NDIR * G * YP_ROW + 7) & ~7;
-    static constexpr int bytes = off_bar + (NBC + NRAW + 1) * 8;
-
-    static_assert(T % 8 == 0 && T % VEC == 0, "T must be a multiple of 8");
-    static_assert(RAW_ROW % 16 == 0 && W_ROW % 16 == 0 && DW_ROW % 16 == 0, "alignment");
     static_assert(S == 4 || S == 8 || S == 16, "S must be 4, 8 or 16");
-    static_assert(NT % 32 == 0, "a CTA must be whole warps");
-
-    __device__ static IO *raw(char *sm, int stage, int d, int k, int r) {
-        return (IO *)(sm + off_raw + stage * RAW_STAGE + d * RAW_DIR + (k * G + r) * RAW_ROW);
-    }
+    static_assert((ROWS * LPR) % 32 == 0 && ROWS % 16 == 0, "whole warps per role");
+    static_assert(R % 16 == 0, "each prep warp takes 16 channels of one branch");
+    // registers per thread so that 3 CTAs fit the 64 K register file
+    static constexpr int MAX_REGS = (65536 / (3 * NT)) / 8 * 8 > 255 ? 255 : (65536 / (3 * NT)) / 8 * 8;
 };
 
 // Positions [lo, lo + len) of branch d at chunk c (both branches have the
@@ -203,369 +209,362 @@ __device__ __forceinline__ void chunk_geom(int c, int d, int L, int T, int &lo, 
     }
 }
 
-// Stage elements [a, e) of the row that starts at element `rowbase` of a
-// global array of `total` elements into dst_row, so that element a + q lands
-// at dst_row[(rowbase + a) % VEC + q]: one bulk copy of the whole 16-byte
-// vectors covering the range (announced on `bar` first), and element-wise
-// copies for a last vector of the array that is not whole.
-template <typename E>
-__device__ __forceinline__ void stage_bulk(E *dst_row, const E *src, long long rowbase, int a,
-                                           int e, long long total, uint64_t *bar) {
-    constexpr int VEC = 16 / (int)sizeof(E);
-    if (e <= a) return;
-    const long long e0 = rowbase + a, e1 = rowbase + e;
-    const long long v0 = e0 / VEC;
-    const long long v1 = (e1 + VEC - 1) / VEC;
-    const long long vfull = total / VEC;
-    const long long vb = v1 < vfull ? v1 : vfull;
-    if (vb > v0) {
-        const unsigned bytes = (unsigned)((vb - v0) * 16);
-        mbar_expect_tx(bar, bytes);
-        bulk_g2s(dst_row, src + v0 * VEC, bytes, bar);
-    }
-    for (long long x = (vb > v0 ? vb : v0) * VEC; x < e1; ++x) dst_row[x - v0 * VEC] = src[x];
-}
-
 // ------------------------------------------------------------------ kernel
-template <typename IO, int S, int NDIR, int G, int T, int OUT>
-__global__ void __launch_bounds__(BiLayout<IO, S, NDIR, G, T>::NT)
+template <typename IO, int S, int NDIR, int R, int OUT>
+__global__ void __maxnreg__((WsLayout<IO, S, NDIR, R>::MAX_REGS))
 bidir_scan_kernel(const BiParams P) {
-    using LY = BiLayout<IO, S, NDIR, G, T>;
+    using LY = WsLayout<IO, S, NDIR, R>;
+    constexpr int T = LY::T;
     constexpr int LPR = LY::LPR;
-    constexpr int NT = LY::NT;
-    constexpr int NW = NT / 32;
-    constexpr int VEC = LY::VEC;
+    constexpr int NSW = LY::NSW, NPW = LY::NPW;
     constexpr int NP = S / 2;                  // packed state pairs per lane
-    constexpr int U = 4;                       // scan unroll (steps)
-    constexpr bool USE_W = NDIR == 2 || OUT == OUT_ADD_Y;
+    constexpr int UB = 4;                      // scan block (steps)
 
     extern __shared__ __align__(128) char sm[];
-    uint64_t *bc_bar = (uint64_t *)(sm + LY::off_bar);     // [NBC], one arrival
-    uint64_t *raw_bar = bc_bar + LY::NBC;                    // [NRAW], NT arrivals
-    uint64_t *w_bar = raw_bar + LY::NRAW;                    // [1], NT arrivals
+    uint64_t *bar = (uint64_t *)(sm + LY::off_bar);
+    uint64_t *bc_full = bar;                   // count 1 (+ transaction bytes)
+    uint64_t *dw_full = bar + LY::NBC;         // count NPW*32
+    uint64_t *dw_empty = dw_full + 2;          // count NSW*32
+    uint64_t *yp_full = dw_empty + 2;          // count NSW*32
+    uint64_t *yp_empty = yp_full + 2;          // count NEW*32
+    volatile int *abort_flag = (volatile int *)(sm + LY::off_flag);
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const int b = blockIdx.y;
-    const int d0 = blockIdx.x * G;
-    const int L = P.L, D = P.D, N = P.N;
+    const int d0 = blockIdx.x * R;
+    const int L = P.L, D = P.D;
+    const int nch = P.nchunks;
     const long long bD = (long long)b * D;
-
-    // ---- scan role of this lane
-    const int s_dir = tid / (G * LPR);
-    const int s_row = (tid / LPR) % G;
-    const int s_sg = tid % LPR;
-    const int s_ch = d0 + s_row;
-    f2 A2[NP], h[NP];
-    {
-        const float *A = P.br[s_dir].A;
-#pragma unroll
-        for (int q = 0; q < NP; ++q) {
-            const int n0 = s_sg * S + 2 * q;
-            const bool ok = s_ch < D;
-            const float a0 = (ok && n0 < N) ? A[(long long)s_ch * N + n0] * kLog2e : 0.f;
-            const float a1 = (ok && n0 + 1 < N) ? A[(long long)s_ch * N + n0 + 1] * kLog2e : 0.f;
-            A2[q] = pk(a0, a1);
-            h[q] = pk(0.f, 0.f);
-        }
-    }
 
     if (tid == 0) {
 #pragma unroll
-        for (int s = 0; s < LY::NBC; ++s) mbar_init(&bc_bar[s], 1);
+        for (int s = 0; s < LY::NBC; ++s) mbar_init(&bc_full[s], 1);
 #pragma unroll
-        for (int s = 0; s < LY::NRAW; ++s) mbar_init(&raw_bar[s], NT);
-        mbar_init(w_bar, NT);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&dw_full[s], NPW * 32);
+            mbar_init(&dw_empty[s], NSW * 32);
+            mbar_init(&yp_full[s], NSW * 32);
+            mbar_init(&yp_empty[s], LY::NEW * 32);
+        }
+        *abort_flag = 0;
         fence_barrier_init();
     }
     __syncthreads();
 
-    // ---- chunk sub-ranges (positions)
-    // first stream index (dt, B/C) of branch d at chunk c
+    // a bounded wait that ran out: every role stops at its next check
+    auto give_up = [&]() {
+        *abort_flag = 1;
+        if (P.status != nullptr) atomicOr(P.status, 1u);
+    };
+    auto wait = [&](uint64_t *bar_, int parity) -> bool {
+        if (mbar_wait_bounded(bar_, (unsigned)parity)) return true;
+        give_up();
+        return false;
+    };
     auto stream_lo = [&](int c, int d, int lo) { return P.br[d].stream_rev ? c * T : lo; };
-    // positions branch d finalises at chunk c
-    auto final_range = [&](int c, int d, int lo, int len, int &a, int &e) {
-        a = lo;
-        e = lo + len;
-        if (NDIR == 2) {
-            if (d == 0) a = max(lo, L - (c + 1) * T);
-            else e = min(lo + len, c * T);
-        }
-    };
-    // positions whose other branch reached them at an earlier chunk
-    auto stash_range = [&](int c, int d, int lo, int len, int &a, int &e) {
-        a = lo;
-        e = lo + len;
-        if (d == 0) a = max(lo, L - c * T);
-        else e = min(lo + len, c * T);
-    };
 
-    // ---- staging: bulk copies (TMA) completing on mbarriers
-    auto issue_bc = [&](int c) {
-        if (tid != 0 || c >= P.nchunks) return;
-        const int st = c % LY::NBC;
-        int lo, len;
-        chunk_geom(c, 0, L, T, lo, len);
-        mbar_arrive_expect_tx(&bc_bar[st], (unsigned)(NDIR * len * kBC * 4));
-#pragma unroll
-        for (int d = 0; d < NDIR; ++d) {
-            chunk_geom(c, d, L, T, lo, len);
-            bulk_g2s(sm + LY::off_bc + st * LY::BC_STAGE + d * LY::BC_DIR,
-                     P.br[d].bc + ((long long)b * L + stream_lo(c, d, lo)) * kBC,
-                     (unsigned)(len * kBC * 4), &bc_bar[st]);
-        }
-    };
-    // dt, u and z rows of chunk c: one segment per (branch, tensor, channel)
-    auto issue_raw = [&](int c) {
-        if (c >= P.nchunks) return;
-        const int st = c % LY::NRAW;
-        uint64_t *bar = &raw_bar[st];
-        for (int sg = tid; sg < NDIR * 3 * G; sg += NT) {
-            const int r = sg % G;
-            const int k = (sg / G) % 3;
-            const int d = sg / (3 * G);
-            const int ch = d0 + r;
-            if (ch >= D) continue;
-            int lo, len, a, e;
-            chunk_geom(c, d, L, T, lo, len);
-            const BiBranch &br = P.br[d];
-            if (k == 0) {
-                a = stream_lo(c, d, lo);
-                stage_bulk<IO>(LY::raw(sm, st, d, 0, r), (const IO *)br.dt,
-                               br.dt_off + b * br.dt_bstride + (long long)ch * L, a, a + len,
-                               br.dt_total, bar);
-            } else if (k == 1) {
-                stage_bulk<IO>(LY::raw(sm, st, d, 1, r), (const IO *)br.u, (bD + ch) * L, lo,
-                               lo + len, P.total, bar);
-            } else if (OUT != OUT_ACC && P.z != nullptr) {
-                final_range(c, d, lo, len, a, e);
-                stage_bulk<IO>(LY::raw(sm, st, d, 2, r), (const IO *)P.z, (bD + ch) * L, a, e,
-                               P.total, bar);
-            }
-        }
-        mbar_arrive(bar);
-    };
-    // fp32 rows of chunk c: the stash W over the second-arrival range and,
-    // for OUT_ADD_Y, acc_in over the final range
-    auto issue_w = [&](int c) {
-        if constexpr (!USE_W) return;
-        if (c >= P.nchunks) return;
-        for (int sg = tid; sg < 2 * NDIR * G; sg += NT) {
-            const int r = sg % G;
-            const int d = (sg / G) % NDIR;
-            const int which = sg / (G * NDIR);
-            const int ch = d0 + r;
-            if (ch >= D) continue;
-            int lo, len, a, e;
-            chunk_geom(c, d, L, T, lo, len);
-            float *dst = (float *)(sm + LY::off_w + ((which * NDIR + d) * G + r) * LY::W_ROW);
-            if (which == 0) {
-                if (NDIR == 1) continue;
-                stash_range(c, d, lo, len, a, e);
-                stage_bulk<float>(dst, P.W, (bD + ch) * L, a, e, P.total, w_bar);
-            } else if (OUT == OUT_ADD_Y) {
-                final_range(c, d, lo, len, a, e);
-                stage_bulk<float>(dst, P.acc_in, (bD + ch) * L, a, e, P.total, w_bar);
-            }
-        }
-        mbar_arrive(w_bar);
-    };
-
-    // ---- prep: (delta, delta, w, w) per (branch, channel, walk step);
-    // one warp per (branch, channel) row, one lane per position
-    auto prep = [&](int c) {
-        const int st = c % LY::NRAW;
-        for (int row = warp; row < NDIR * G; row += NW) {
-            const int d = row / G, r = row % G;
-            const int ch = d0 + r;
-            int lo, len;
-            chunk_geom(c, d, L, T, lo, len);
-            float4 *dwr = (float4 *)(sm + LY::off_dw + row * LY::DW_ROW);
-            if (ch >= D) {
-                for (int q = lane; q < len; q += 32) dwr[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-                continue;
-            }
-            const BiBranch &br = P.br[d];
-            const float bias = br.bias ? br.bias[ch] : 0.f;
-            const bool srev = br.stream_rev != 0;
-            const IO *rdt = LY::raw(sm, st, d, 0, r) +
-                            (int)((br.dt_off + b * br.dt_bstride + (long long)ch * L +
-                                   stream_lo(c, d, lo)) & (VEC - 1));
-            const IO *ru = LY::raw(sm, st, d, 1, r) + (int)(((bD + ch) * L + lo) & (VEC - 1));
-            for (int q = lane; q < len; q += 32) {
-                const int j = d ? len - 1 - q : q;
-                const float x = to_f32(rdt[srev ? j : q]) + bias;
-                const float dl = P.delta_softplus ? softplus_f<IO>(x) : x;
-                const float w = dl * to_f32(ru[q]);
-                dwr[j] = make_float4(dl, dl, w, w);
-            }
-        }
-    };
-
-    // ---- scan of one chunk by this lane
-    auto scan = [&](int c) -> bool {
-        const int stb = c % LY::NBC;
-        const bool ok = mbar_wait_bounded(&bc_bar[stb], (unsigned)((c / LY::NBC) & 1));
-        int lo, len;
-        chunk_geom(c, s_dir, L, T, lo, len);
-        const char *dwp = sm + LY::off_dw + (s_dir * G + s_row) * LY::DW_ROW;
-        const float *bcp = (const float *)(sm + LY::off_bc + stb * LY::BC_STAGE +
-                                           s_dir * LY::BC_DIR) + s_sg * S;
-        int bstep = kBC;
-        if (s_dir == 1 && !P.br[1].stream_rev) {   // backward walk over a
-            bcp += (len - 1) * kBC;                 // position-ordered stream
-            bstep = -kBC;
-        }
-        float *ypp = (float *)(sm + LY::off_yp + (s_dir * G + s_row) * LY::YP_ROW) + s_sg;
-        auto step = [&](int j) {
-            const float4 v = *(const float4 *)(dwp + j * 16);
-            const f2 dd = pk(v.x, v.y), ww = pk(v.z, v.w);
-            const float *bj = bcp + j * bstep;
-            f2 bq[NP], cq[NP];
-#pragma unroll
-            for (int k = 0; k < S / 4; ++k) {
-                const float4 vb = *(const float4 *)(bj + 4 * k);
-                const float4 vc = *(const float4 *)(bj + kMaxN + 4 * k);
-                bq[2 * k] = pk(vb.x, vb.y);
-                bq[2 * k + 1] = pk(vb.z, vb.w);
-                cq[2 * k] = pk(vc.x, vc.y);
-                cq[2 * k + 1] = pk(vc.z, vc.w);
-            }
-            f2 y2;
+    if (warp < NSW) {
+        // ================================================================ scan
+        const int s_dir = tid / (R * LPR);
+        const int s_row = (tid / LPR) % R;
+        const int s_sg = tid % LPR;
+        const int s_ch = d0 + s_row;
+        const int N = P.N;
+        f2 A2[NP], h[NP];
+        {
+            const float *A = P.br[s_dir].A;
 #pragma unroll
             for (int q = 0; q < NP; ++q) {
-                float a0, a1;
-                upk(mul2(dd, A2[q]), a0, a1);
-                const f2 e = pk(ex2_approx(a0), ex2_approx(a1));
-                h[q] = fma2(e, h[q], mul2(bq[q], ww));
-                y2 = (q == 0) ? mul2(cq[q], h[q]) : fma2(cq[q], h[q], y2);
+                const int n0 = s_sg * S + 2 * q;
+                const bool ok = s_ch < D;
+                const float a0 = (ok && n0 < N) ? A[(long long)s_ch * N + n0] * kLog2e : 0.f;
+                const float a1 = (ok && n0 + 1 < N) ? A[(long long)s_ch * N + n0 + 1] * kLog2e : 0.f;
+                A2[q] = pk(a0, a1);
+                h[q] = pk(0.f, 0.f);
             }
-            float ylo, yhi;
-            upk(y2, ylo, yhi);
-            ypp[j * LPR] = ylo + yhi;
-        };
-        int j = 0;
-        for (; j + U <= len; j += U) {
+        }
+        const bool walk_down = s_dir == 1 && !P.br[1].stream_rev;
+        for (int c = 0; c < nch; ++c) {
+            const int s2 = c & 1, sb = c % LY::NBC;
+            if (*abort_flag || !wait(&dw_full[s2], (c >> 1) & 1) ||
+                !wait(&bc_full[sb], (c / LY::NBC) & 1) || !wait(&yp_empty[s2], ((c >> 1) & 1) ^ 1))
+                return;
+            int lo, len;
+            chunk_geom(c, s_dir, L, T, lo, len);
+            const char *dwp = sm + LY::off_dw + s2 * LY::DW_STAGE + (s_dir * R + s_row) * LY::DW_ROW;
+            const float *bcp = (const float *)(sm + LY::off_bc + sb * LY::BC_STAGE +
+                                               s_dir * LY::BC_DIR) + s_sg * S;
+            int bstep = kBC;
+            if (walk_down) {                   // backward walk over a position-ordered stream
+                bcp += (len - 1) * kBC;
+                bstep = -kBC;
+            }
+            float *ypp = (float *)(sm + LY::off_yp + s2 * LY::YP_STAGE +
+                                   (s_dir * R + s_row) * LY::YP_ROW) + s_sg;
+            // UB steps at a time, in three passes so that independent work
+            // is adjacent for the scheduler: (1) every shared-memory load of
+            // the block; (2) every decay e = 2^(delta*A*log2e) (MUFU) and
+            // input B*w of the block -- independent of the state; (3) the
+            // state recurrences and readouts, then the partial stores.
+            auto block = [&](int j0) {
+                float4 dv[UB], bv[UB][S / 4], cv[UB][S / 4];
 #pragma unroll
-            for (int jj = 0; jj < U; ++jj) step(j + jj);
+                for (int jj = 0; jj < UB; ++jj) {
+                    dv[jj] = *(const float4 *)(dwp + (j0 + jj) * 16);
+                    const float *bj = bcp + (j0 + jj) * bstep;
+#pragma unroll
+                    for (int k = 0; k < S / 4; ++k) {
+                        bv[jj][k] = *(const float4 *)(bj + 4 * k);
+                        cv[jj][k] = *(const float4 *)(bj + kMaxN + 4 * k);
+                    }
+                }
+                f2 e[UB][NP], bw[UB][NP];
+#pragma unroll
+                for (int jj = 0; jj < UB; ++jj) {
+                    const f2 dd = pk(dv[jj].x, dv[jj].y), ww = pk(dv[jj].z, dv[jj].w);
+#pragma unroll
+                    for (int q = 0; q < NP; ++q) {
+                        const float4 &vb = bv[jj][q / 2];
+                        const f2 bq = (q & 1) ? pk(vb.z, vb.w) : pk(vb.x, vb.y);
+                        float a0, a1;
+                        upk(mul2(dd, A2[q]), a0, a1);
+                        e[jj][q] = pk(ex2_approx(a0), ex2_approx(a1));
+                        bw[jj][q] = mul2(bq, ww);
+                    }
+                }
+                float ys[UB];
+#pragma unroll
+                for (int jj = 0; jj < UB; ++jj) {
+                    f2 y2;
+#pragma unroll
+                    for (int q = 0; q < NP; ++q) {
+                        const float4 &vc = cv[jj][q / 2];
+                        const f2 cq = (q & 1) ? pk(vc.z, vc.w) : pk(vc.x, vc.y);
+                        h[q] = fma2(e[jj][q], h[q], bw[jj][q]);
+                        y2 = (q == 0) ? mul2(cq, h[q]) : fma2(cq, h[q], y2);
+                    }
+                    float ylo, yhi;
+                    upk(y2, ylo, yhi);
+                    ys[jj] = ylo + yhi;
+                }
+#pragma unroll
+                for (int jj = 0; jj < UB; ++jj) ypp[(j0 + jj) * LPR] = ys[jj];
+            };
+            // one step (the chunk's tail)
+            auto step = [&](int j) {
+                const float4 v = *(const float4 *)(dwp + j * 16);
+                const f2 dd = pk(v.x, v.y), ww = pk(v.z, v.w);
+                const float *bj = bcp + j * bstep;
+                f2 y2;
+#pragma unroll
+                for (int q = 0; q < NP; ++q) {
+                    const float2 vb = *(const float2 *)(bj + 2 * q);
+                    const float2 vc = *(const float2 *)(bj + kMaxN + 2 * q);
+                    float a0, a1;
+                    upk(mul2(dd, A2[q]), a0, a1);
+                    const f2 ee = pk(ex2_approx(a0), ex2_approx(a1));
+                    h[q] = fma2(ee, h[q], mul2(pk(vb.x, vb.y), ww));
+                    y2 = (q == 0) ? mul2(pk(vc.x, vc.y), h[q]) : fma2(pk(vc.x, vc.y), h[q], y2);
+                }
+                float ylo, yhi;
+                upk(y2, ylo, yhi);
+                ypp[j * LPR] = ylo + yhi;
+            };
+            int j = 0;
+            for (; j + UB <= len; j += UB) block(j);
+            for (; j < len; ++j) step(j);
+            mbar_arrive(&dw_empty[s2]);
+            mbar_arrive(&yp_full[s2]);
         }
-        for (; j < len; ++j) step(j);
-        return ok;
-    };
-
-    // sum of the LPR partial readouts at walk step j of a row
-    auto ypsum = [&](const float *yrow, int j) -> float {
-        const float *ps = yrow + j * LPR;
-        if constexpr (LPR == 4) {
-            const float4 v = *(const float4 *)ps;
-            return (v.x + v.y) + (v.z + v.w);
-        } else if constexpr (LPR == 2) {
-            const float2 v = *(const float2 *)ps;
-            return v.x + v.y;
-        } else {
-            return ps[0];
+    } else if (warp < NSW + NPW) {
+        // ================================================================ prep
+        // 16 rows of one branch; lane = walk step j of the chunk
+        const int pw = warp - NSW;
+        const int d = (pw * 16) / R;
+        const int r0 = (pw * 16) % R;
+        const BiBranch &br = P.br[d];
+        const IO *dtp = (const IO *)br.dt;
+        const IO *up = (const IO *)br.u;
+        const bool srev = br.stream_rev != 0;
+        float bias[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int ch = d0 + r0 + i;
+            bias[i] = (ch < D && br.bias) ? br.bias[ch] : 0.f;
         }
-    };
-
-    // ---- epilogue of one chunk; one warp per (branch, channel) row
-    auto epilogue = [&](int c) {
-        const int st = c % LY::NRAW;
-        int lo0, len, lo1 = 0;
-        chunk_geom(c, 0, L, T, lo0, len);
-        if (NDIR == 2) chunk_geom(c, 1, L, T, lo1, len);
-        for (int row = warp; row < NDIR * G; row += NW) {
-            const int d = row / G, r = row % G;
-            const int ch = d0 + r;
-            if (ch >= D) continue;
-            const long long rowbase = (bD + ch) * L;
-            const int lo = d ? lo1 : lo0;
-            const BiBranch &br = P.br[d];
-            const float dsk = br.Dskip ? br.Dskip[ch] : 0.f;
-            const float *yown = (const float *)(sm + LY::off_yp + row * LY::YP_ROW);
-            const IO *ru = LY::raw(sm, st, d, 1, r) + (int)((rowbase + lo) & (VEC - 1)) ;
-            int fa, fe, wa, we;
-            final_range(c, d, lo, len, fa, fe);
-            stash_range(c, d, lo, len, wa, we);
-            const IO *rz = LY::raw(sm, st, d, 2, r) + (int)((rowbase + fa) & (VEC - 1));
-            const float *wst = (const float *)(sm + LY::off_w + row * LY::W_ROW) +
-                               (int)((rowbase + wa) & 3);
-            const float *acc = (const float *)(sm + LY::off_w + (NDIR * G + row) * LY::W_ROW) +
-                               (int)((rowbase + fa) & 3);
-            // the backward branch's row, for positions both reach in this chunk
-            const float *yoth = (const float *)(sm + LY::off_yp + ((NDIR - 1) * G + r) * LY::YP_ROW);
-            const float dsko = (NDIR == 2 && P.br[NDIR - 1].Dskip) ? P.br[NDIR - 1].Dskip[ch] : 0.f;
-            const IO *ruo = LY::raw(sm, st, NDIR - 1, 1, r) + (int)((rowbase + lo1) & (VEC - 1));
-            for (int q = lane; q < len; q += 32) {
-                const int p = lo + q;
-                // 0: first arrival (stash), 1: second arrival (stash holds
-                // the other branch), 2: both in this chunk, 3: left to branch 0
-                int cls = 1;
-                if (NDIR == 2) {
-                    if (d == 0) cls = (p < L - (c + 1) * T) ? 0 : (p >= L - c * T ? 1 : 2);
-                    else cls = (p >= (c + 1) * T) ? 0 : (p < c * T ? 1 : 3);
-                }
-                if (cls == 3) continue;
-                const int j = d ? len - 1 - q : q;
-                const float yv = fmaf(dsk, to_f32(ru[q]), ypsum(yown, j));
-                if (NDIR == 2 && cls == 0) {
-                    P.W[rowbase + p] = yv;
-                    continue;
-                }
-                float v = yv;
-                if (NDIR == 2) {
-                    const float other =
-                        cls == 1 ? wst[p - wa]
-                                 : fmaf(dsko, to_f32(ruo[p - lo1]), ypsum(yoth, L - 1 - p - c * T));
-                    v = P.out_scale * (yv + other);
-                }
-                if (OUT == OUT_ACC) {
-                    P.acc_out[rowbase + p] = v;
-                    continue;
-                }
-                if (OUT == OUT_ADD_Y) v += acc[p - fa];
-                if (P.z) v *= silu_f<IO>(to_f32(rz[p - fa]));
-                ((IO *)P.y)[rowbase + p] = from_f32<IO>(v);
+        const long long dt0 = br.dt_off + b * br.dt_bstride + (long long)(d0 + r0) * L;
+        const long long u0 = (bD + d0 + r0) * L;
+        const int nrow = min(16, D - (d0 + r0));            // valid rows of this warp
+        for (int c = 0; c < nch; ++c) {
+            const int s2 = c & 1;
+            int lo, len;
+            chunk_geom(c, d, L, T, lo, len);
+            const int j = lane;
+            const bool act = j < len;
+            const int p = d ? lo + len - 1 - j : lo + j;        // position of walk step j
+            const int si = srev ? stream_lo(c, d, lo) + j : p;  // dt stream index
+            // all loads of the chunk first (coalesced: 32 consecutive
+            // elements of each row), then the arithmetic
+            IO xdt[16], xu[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const bool ok = act && i < nrow;
+                xdt[i] = ok ? dtp[dt0 + (long long)i * L + si] : from_f32<IO>(0.f);
+                xu[i] = ok ? up[u0 + (long long)i * L + p] : from_f32<IO>(0.f);
             }
+            if (*abort_flag || !wait(&dw_empty[s2], ((c >> 1) & 1) ^ 1)) return;
+            float4 *dw = (float4 *)(sm + LY::off_dw + s2 * LY::DW_STAGE);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float x = to_f32(xdt[i]) + bias[i];
+                const float dl = P.delta_softplus ? softplus_f<IO>(x) : x;
+                const float w = dl * to_f32(xu[i]);
+                const float4 v = i < nrow ? make_float4(dl, dl, w, w)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+                if (act) dw[(d * R + r0 + i) * (LY::DW_ROW / 16) + j] = v;
+            }
+            mbar_arrive(&dw_full[s2]);
         }
-        // the stash stores must precede the bulk copies that read them back
-        if (NDIR == 2) fence_proxy_async_global();
-    };
-
-    // ---- pipeline.  Ring depths: raw 3 (issued two chunks ahead), B/C 2,
-    // fp32 rows 1 (issued after the previous chunk's epilogue).
-    bool ok = true;
-    issue_bc(0);
-    issue_bc(1);
-    issue_raw(0);
-    issue_raw(1);
-    issue_raw(2);
-    issue_w(0);
-    ok &= mbar_wait_bounded(&raw_bar[0], 0u);
-    prep(0);
-    __syncthreads();
-    for (int c = 0; c < P.nchunks; ++c) {
-        ok &= scan(c);
-        if (c + 1 < P.nchunks)
-            ok &= mbar_wait_bounded(&raw_bar[(c + 1) % LY::NRAW], (unsigned)(((c + 1) / LY::NRAW) & 1));
-        if (USE_W) ok &= mbar_wait_bounded(w_bar, (unsigned)(c & 1));
-        if (__syncthreads_or(!ok)) {
-            // a bulk copy did not land in time: report, drain what was
-            // issued (bounded), leave
-            if (tid == 0 && P.status != nullptr) atomicOr(P.status, 1u);
-            const int last_raw = min(c + 2, P.nchunks - 1);
-            for (int k = max(0, last_raw - LY::NRAW + 1); k <= last_raw; ++k)
-                mbar_wait_bounded(&raw_bar[k % LY::NRAW], (unsigned)((k / LY::NRAW) & 1));
-            const int last_bc = min(c + 1, P.nchunks - 1);
-            for (int k = max(0, last_bc - LY::NBC + 1); k <= last_bc; ++k)
-                mbar_wait_bounded(&bc_bar[k % LY::NBC], (unsigned)((k / LY::NBC) & 1));
-            if (USE_W) mbar_wait_bounded(w_bar, (unsigned)(c & 1));
-            return;
+    } else {
+        // ================================================================ epilogue
+        // both branches of CPE channels; lane = position offset q in the chunk
+        constexpr int CPE = LY::CPE;
+        const int ew = warp - NSW - NPW;
+        const int c0 = ew * CPE;                               // first channel (in CTA)
+        float dsk[NDIR][CPE];
+        long long rowb[CPE];
+#pragma unroll
+        for (int i = 0; i < CPE; ++i) {
+            const int ch = d0 + c0 + i;
+            const bool ok = ch < D;
+            rowb[i] = ok ? (bD + ch) * L : -1;
+#pragma unroll
+            for (int d = 0; d < NDIR; ++d)
+                dsk[d][i] = (ok && P.br[d].Dskip) ? P.br[d].Dskip[ch] : 0.f;
         }
-        epilogue(c);
-        if (c + 1 < P.nchunks) prep(c + 1);
-        __syncthreads();
-        issue_bc(c + 2);
-        issue_w(c + 1);
-        issue_raw(c + 3);
+        auto issue_bc = [&](int c) {
+            if (c >= nch || c == P.withhold_bc) return;
+            const int st = c % LY::NBC;
+            int lo, len;
+            chunk_geom(c, 0, L, T, lo, len);
+            mbar_arrive_expect_tx(&bc_full[st], (unsigned)(NDIR * len * kBC * 4));
+#pragma unroll
+            for (int d = 0; d < NDIR; ++d) {
+                chunk_geom(c, d, L, T, lo, len);
+                bulk_g2s(sm + LY::off_bc + st * LY::BC_STAGE + d * LY::BC_DIR,
+                         P.br[d].bc + ((long long)b * L + stream_lo(c, d, lo)) * kBC,
+                         (unsigned)(len * kBC * 4), &bc_full[st]);
+            }
+        };
+        const bool producer = ew == 0 && lane == 0;
+        if (producer) {
+            issue_bc(0);
+            issue_bc(1);
+        }
+        int issued = 2;
+        for (int c = 0; c < nch; ++c) {
+            const int s2 = c & 1;
+            int lo0, len, lo1 = 0;
+            chunk_geom(c, 0, L, T, lo0, len);
+            if (NDIR == 2) chunk_geom(c, 1, L, T, lo1, len);
+            const int q = lane;
+            const bool act = q < len;
+            // loads first: u (for D*u), z, stash, acc_in of this lane's
+            // positions; independent of the scan, so they overlap its wait
+            float uu[NDIR][CPE], zz[NDIR][CPE], ws[NDIR][CPE], ai[NDIR][CPE];
+            int cls[NDIR];
+#pragma unroll
+            for (int d = 0; d < NDIR; ++d) {
+                const int p = (d ? lo1 : lo0) + q;
+                // 0: first arrival (stash), 1: second arrival (the stash holds
+                // the other branch), 2: both in this chunk, 3: left to branch 0
+                int k = 1;
+                if (NDIR == 2) {
+                    if (d == 0) k = (p < L - (c + 1) * T) ? 0 : (p >= L - c * T ? 1 : 2);
+                    else k = (p >= (c + 1) * T) ? 0 : (p < c * T ? 1 : 3);
+                }
+                cls[d] = k;
+                const IO *up = (const IO *)P.br[d].u;
+#pragma unroll
+                for (int i = 0; i < CPE; ++i) {
+                    const bool ok = act && rowb[i] >= 0;
+                    const long long o = rowb[i] + p;
+                    uu[d][i] = (ok && k != 3) ? to_f32(up[o]) : 0.f;
+                    const bool fin = ok && (k == 1 || k == 2);
+                    zz[d][i] = (fin && P.z && OUT != OUT_ACC) ? to_f32(((const IO *)P.z)[o]) : 0.f;
+                    ws[d][i] = (NDIR == 2 && ok && k == 1) ? P.W[o] : 0.f;
+                    ai[d][i] = (OUT == OUT_ADD_Y && fin) ? P.acc_in[o] : 0.f;
+                }
+            }
+            if (*abort_flag || !wait(&yp_full[s2], (c >> 1) & 1)) {
+                // the producer waits (bounded) for the B/C copies it issued
+                if (producer)
+                    for (int k = c; k < min(c + LY::NBC, nch); ++k)
+                        if (k != P.withhold_bc)
+                            mbar_wait_bounded(&bc_full[k % LY::NBC], (unsigned)((k / LY::NBC) & 1));
+                return;
+            }
+            // scan(c) is done: its B/C stage is free for chunk c + NBC
+            if (producer && issued < nch) {
+                issue_bc(c + LY::NBC);
+                ++issued;
+            }
+            const float *yp = (const float *)(sm + LY::off_yp + s2 * LY::YP_STAGE);
+            auto ypsum = [&](int row, int jj) -> float {
+                const float *ps = yp + row * (LY::YP_ROW / 4) + jj * LPR;
+                if constexpr (LPR == 4) {
+                    const float4 v = *(const float4 *)ps;
+                    return (v.x + v.y) + (v.z + v.w);
+                } else if constexpr (LPR == 2) {
+                    const float2 v = *(const float2 *)ps;
+                    return v.x + v.y;
+                } else {
+                    return ps[0];
+                }
+            };
+#pragma unroll
+            for (int d = 0; d < NDIR; ++d) {
+                const int lo = d ? lo1 : lo0;
+                const int p = lo + q;
+                const int k = cls[d];
+                const int jw = d ? len - 1 - q : q;            // walk step of p
+#pragma unroll
+                for (int i = 0; i < CPE; ++i) {
+                    if (!act || rowb[i] < 0 || k == 3) continue;
+                    const int row = d * R + c0 + i;
+                    const float yv = fmaf(dsk[d][i], uu[d][i], ypsum(row, jw));
+                    const long long o = rowb[i] + p;
+                    if (NDIR == 2 && k == 0) {
+                        P.W[o] = yv;
+                        continue;
+                    }
+                    float v = yv;
+                    if (NDIR == 2) {
+                        float other;
+                        if (k == 1) {
+                            other = ws[d][i];
+                        } else {                                // both here (d == 0)
+                            const int jb = L - 1 - p - c * T;   // backward walk step of p
+                            const IO *ub = (const IO *)P.br[NDIR - 1].u;
+                            other = fmaf(dsk[NDIR - 1][i], to_f32(ub[o]),
+                                         ypsum((NDIR - 1) * R + c0 + i, jb));
+                        }
+                        v = P.out_scale * (yv + other);
+                    }
+                    if (OUT == OUT_ACC) {
+                        P.acc_out[o] = v;
+                        continue;
+                    }
+                    if (OUT == OUT_ADD_Y) v += ai[d][i];
+                    if (P.z) v *= silu_f<IO>(zz[d][i]);
+                    ((IO *)P.y)[o] = from_f32<IO>(v);
+                }
+            }
+            mbar_arrive(&yp_empty[s2]);
+            // stash stores of this chunk must be visible to this warp's loads
+            // of the next chunk
+            __syncwarp();
+        }
     }
 }
 

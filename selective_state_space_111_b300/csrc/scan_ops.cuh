@@ -140,15 +140,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait for the phase with parity `parity` to complete.  Returns
-// false when the iteration limit is reached (the caller reports a timeout;
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Bounded wait for the phase with parity `parity` to complete: try_wait
+// suspends the thread in hardware until the phase completes or a short
+// system time limit passes, and the loop gives up after about two seconds
+// of wall time.  Returns false on giving up (the caller reports a timeout;
 // nothing in this library waits forever).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, unsigned parity) {
-    for (int it = 0; it < (1 << 22); ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (it > 64) __nanosleep(128);
+        if (global_ns() - t0 > 2000000000ull) return false;
     }
-    return false;
 }
 // Global -> shared bulk copy of `bytes` (multiple of 16; both addresses
 // 16-byte aligned), completing on `bar` as transaction bytes.

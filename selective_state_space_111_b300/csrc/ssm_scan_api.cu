@@ -44,10 +44,10 @@ constexpr size_t kHeaderBytes = 256;
 #define SSM_BI_S 8
 #endif
 #ifndef SSM_BI_G2
-#define SSM_BI_G2 8
+#define SSM_BI_G2 16
 #endif
 #ifndef SSM_BI_G1
-#define SSM_BI_G1 16
+#define SSM_BI_G1 32
 #endif
 constexpr int kBiT = 32;                   // positions per chunk
 constexpr int kBiS = SSM_BI_S;             // states per lane
@@ -92,11 +92,14 @@ ssm_status launch_pack(const void *Bm, const void *Cm, float *out, int B, int N,
 // Profiling hook (ssm_set_profile_events): events recorded around the last
 // scan-kernel launch of each call made on this host thread.
 thread_local cudaEvent_t t_prof_begin = nullptr, t_prof_end = nullptr;
+// Test hook (ssm_test_withhold_copy): chunk whose B/C copy the next call on
+// this host thread withholds, to exercise the bounded waits.
+thread_local int t_withhold = -1;
 
 template <typename IO, int S, int NDIR, int G, int OUT = ssm::OUT_Y>
 ssm_status launch_bidir(const ssm::BiParams &P, cudaStream_t st, bool last = true) {
-    using LY = ssm::BiLayout<IO, S, NDIR, G, kBiT>;
-    auto *kern = &ssm::bidir_scan_kernel<IO, S, NDIR, G, kBiT, OUT>;
+    using LY = ssm::WsLayout<IO, S, NDIR, G>;
+    auto *kern = &ssm::bidir_scan_kernel<IO, S, NDIR, G, OUT>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::bytes) !=
         cudaSuccess) {
         cudaGetLastError();
@@ -112,11 +115,14 @@ ssm_status launch_bidir(const ssm::BiParams &P, cudaStream_t st, bool last = tru
         return SSM_ERR_INVALID_ARG;
     dim3 grid((P.D + G - 1) / G, P.B);
     const bool prof = last && t_prof_begin != nullptr && t_prof_end != nullptr;
+    ssm::BiParams Q = P;
+    Q.withhold_bc = t_withhold;
+    t_withhold = -1;
     if (prof && cudaEventRecord(t_prof_begin, st) != cudaSuccess) {
         cudaGetLastError();
         return SSM_ERR_CUDA;
     }
-    kern<<<grid, LY::NT, LY::bytes, st>>>(P);
+    kern<<<grid, LY::NT, LY::bytes, st>>>(Q);
     if (cudaGetLastError() != cudaSuccess) return SSM_ERR_CUDA;
     if (prof && cudaEventRecord(t_prof_end, st) != cudaSuccess) {
         cudaGetLastError();
@@ -462,6 +468,8 @@ const char *ssm_status_string(ssm_status s) {
     }
     return "unknown status";
 }
+
+void ssm_test_withhold_copy(int chunk) { t_withhold = chunk; }
 
 void ssm_set_profile_events(void *begin, void *end) {
     t_prof_begin = (cudaEvent_t)begin;
