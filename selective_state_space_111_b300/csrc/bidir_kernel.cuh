@@ -61,6 +61,10 @@ namespace ssm {
 
 constexpr int kBC = 2 * kMaxN;   // floats per position in the packed B/C stream
 
+#ifndef SSM_SCAN_BLOCK
+#define SSM_SCAN_BLOCK 4         // scan steps per block (loads, then ex2, then recurrences)
+#endif
+
 struct BiBranch {
     const void *dt;        // delta tensor (I/O dtype, 16-byte aligned); row
                            // (b, d) of this branch starts at element
@@ -180,14 +184,17 @@ struct WsLayout {
     static constexpr int DW_STAGE = ROWS * DW_ROW;
     static constexpr int YP_ROW = (T * LPR + LPR) * 4;      // padded: banks spread
     static constexpr int YP_STAGE = ROWS * YP_ROW;
+    static constexpr int U_STAGE = ROWS * T * (int)sizeof(IO);   // u in walk order
     static constexpr int off_bc = 0;                        // 128-byte aligned
     static constexpr int off_dw = off_bc + NBC * BC_STAGE;
     static constexpr int off_yp = off_dw + 2 * DW_STAGE;
-    static constexpr int off_bar = (off_yp + 2 * YP_STAGE + 7) & ~7;
+    static constexpr int off_u = off_yp + 2 * YP_STAGE;
+    static constexpr int off_bar = (off_u + 2 * U_STAGE + 7) & ~7;
     // bc_full[NBC], dw_full[2], dw_empty[2], yp_full[2], yp_empty[2]
     static constexpr int NBAR = NBC + 8;
     static constexpr int off_flag = off_bar + NBAR * 8;
-    static constexpr int bytes = off_flag + 16;
+    static constexpr int off_tab = off_flag + 16;             // D per (branch, channel)
+    static constexpr int bytes = off_tab + ROWS * 4;
 
     static_assert(S == 4 || S == 8 || S == 16, "S must be 4, 8 or 16");
     static_assert((ROWS * LPR) % 32 == 0 && ROWS % 16 == 0, "whole warps per role");
@@ -218,13 +225,13 @@ bidir_scan_kernel(const BiParams P) {
     constexpr int LPR = LY::LPR;
     constexpr int NSW = LY::NSW, NPW = LY::NPW;
     constexpr int NP = S / 2;                  // packed state pairs per lane
-    constexpr int UB = 4;                      // scan block (steps)
+    constexpr int UB = SSM_SCAN_BLOCK;         // scan block (steps)
 
     extern __shared__ __align__(128) char sm[];
     uint64_t *bar = (uint64_t *)(sm + LY::off_bar);
     uint64_t *bc_full = bar;                   // count 1 (+ transaction bytes)
     uint64_t *dw_full = bar + LY::NBC;         // count NPW*32
-    uint64_t *dw_empty = dw_full + 2;          // count NSW*32
+    uint64_t *dw_empty = dw_full + 2;          // count NEW*32
     uint64_t *yp_full = dw_empty + 2;          // count NSW*32
     uint64_t *yp_empty = yp_full + 2;          // count NEW*32
     volatile int *abort_flag = (volatile int *)(sm + LY::off_flag);
@@ -242,7 +249,7 @@ bidir_scan_kernel(const BiParams P) {
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
             mbar_init(&dw_full[s], NPW * 32);
-            mbar_init(&dw_empty[s], NSW * 32);
+            mbar_init(&dw_empty[s], LY::NEW * 32);   // released by the epilogue (u stage)
             mbar_init(&yp_full[s], NSW * 32);
             mbar_init(&yp_empty[s], LY::NEW * 32);
         }
@@ -373,7 +380,6 @@ bidir_scan_kernel(const BiParams P) {
             int j = 0;
             for (; j + UB <= len; j += UB) block(j);
             for (; j < len; ++j) step(j);
-            mbar_arrive(&dw_empty[s2]);
             mbar_arrive(&yp_full[s2]);
         }
     } else if (warp < NSW + NPW) {
@@ -409,19 +415,27 @@ bidir_scan_kernel(const BiParams P) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const bool ok = act && i < nrow;
-                xdt[i] = ok ? dtp[dt0 + (long long)i * L + si] : from_f32<IO>(0.f);
-                xu[i] = ok ? up[u0 + (long long)i * L + p] : from_f32<IO>(0.f);
+                xdt[i] = ok ? __ldg(dtp + dt0 + (long long)i * L + si) : from_f32<IO>(0.f);
+                xu[i] = ok ? __ldg(up + u0 + (long long)i * L + p) : from_f32<IO>(0.f);
             }
             if (*abort_flag || !wait(&dw_empty[s2], ((c >> 1) & 1) ^ 1)) return;
             float4 *dw = (float4 *)(sm + LY::off_dw + s2 * LY::DW_STAGE);
+            float dlv[16], wv[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const float x = to_f32(xdt[i]) + bias[i];
                 const float dl = P.delta_softplus ? softplus_f<IO>(x) : x;
-                const float w = dl * to_f32(xu[i]);
-                const float4 v = i < nrow ? make_float4(dl, dl, w, w)
-                                          : make_float4(0.f, 0.f, 0.f, 0.f);
-                if (act) dw[(d * R + r0 + i) * (LY::DW_ROW / 16) + j] = v;
+                dlv[i] = i < nrow ? dl : 0.f;
+                wv[i] = i < nrow ? dl * to_f32(xu[i]) : 0.f;
+            }
+            if (act) {
+                IO *us = (IO *)(sm + LY::off_u + s2 * LY::U_STAGE);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    dw[(d * R + r0 + i) * (LY::DW_ROW / 16) + j] =
+                        make_float4(dlv[i], dlv[i], wv[i], wv[i]);
+                    us[(d * R + r0 + i) * T + j] = xu[i];
+                }
             }
             mbar_arrive(&dw_full[s2]);
         }
@@ -431,17 +445,15 @@ bidir_scan_kernel(const BiParams P) {
         constexpr int CPE = LY::CPE;
         const int ew = warp - NSW - NPW;
         const int c0 = ew * CPE;                               // first channel (in CTA)
-        float dsk[NDIR][CPE];
-        long long rowb[CPE];
-#pragma unroll
-        for (int i = 0; i < CPE; ++i) {
-            const int ch = d0 + c0 + i;
-            const bool ok = ch < D;
-            rowb[i] = ok ? (bD + ch) * L : -1;
-#pragma unroll
-            for (int d = 0; d < NDIR; ++d)
-                dsk[d][i] = (ok && P.br[d].Dskip) ? P.br[d].Dskip[ch] : 0.f;
+        // per-channel constants in shared memory (this warp's channels)
+        float *dsk_tab = (float *)(sm + LY::off_tab) + ew * NDIR * CPE;   // [NDIR][CPE]
+        if (lane < NDIR * CPE) {
+            const int d = lane / CPE, ch = d0 + c0 + lane % CPE;
+            dsk_tab[lane] = (ch < D && P.br[d].Dskip) ? P.br[d].Dskip[ch] : 0.f;
         }
+        __syncwarp();
+        const long long rowb0 = (bD + d0 + c0) * L;          // channel c0's row
+        const int nch_ok = min(CPE, D - (d0 + c0));           // valid channels
         auto issue_bc = [&](int c) {
             if (c >= nch || c == P.withhold_bc) return;
             const int st = c % LY::NBC;
@@ -461,41 +473,49 @@ bidir_scan_kernel(const BiParams P) {
             issue_bc(0);
             issue_bc(1);
         }
-        int issued = 2;
+        const int q = lane;
+        // classes of this lane's position in branch d at chunk c:
+        // 0 first arrival (stash), 1 second arrival (the stash holds the other
+        // branch), 2 both in this chunk, 3 left to branch 0
+        auto classify = [&](int c, int d, int p) -> int {
+            if (NDIR == 1) return 1;
+            if (d == 0) return (p < L - (c + 1) * T) ? 0 : (p >= L - c * T ? 1 : 2);
+            return (p >= (c + 1) * T) ? 0 : (p < c * T ? 1 : 3);
+        };
+        // z, the stash and acc_in of the positions a lane finalises at chunk
+        // c, fetched one chunk ahead (raw values, converted at use, all in
+        // flight together).  u comes from the prep warps through shared
+        // memory (its stage is released by this role).
+        IO zr[NDIR][CPE];
+        float wr[NDIR][CPE], ar[NDIR][CPE];
+        auto prefetch = [&](int c) {
+            int lo0, len, lo1 = 0;
+            chunk_geom(c, 0, L, T, lo0, len);
+            if (NDIR == 2) chunk_geom(c, 1, L, T, lo1, len);
+            const bool act = q < len;
+#pragma unroll
+            for (int d = 0; d < NDIR; ++d) {
+                const int p = (d ? lo1 : lo0) + q;
+                const int k = classify(c, d, p);
+                const bool fin = act && (k == 1 || k == 2);
+#pragma unroll
+                for (int i = 0; i < CPE; ++i) {
+                    const bool ok = fin && i < nch_ok;
+                    const long long o = rowb0 + (long long)i * L + p;
+                    zr[d][i] = (ok && OUT != OUT_ACC && P.z != nullptr)
+                                   ? __ldg((const IO *)P.z + o) : from_f32<IO>(0.f);
+                    wr[d][i] = (NDIR == 2 && ok && k == 1) ? P.W[o] : 0.f;
+                    ar[d][i] = (OUT == OUT_ADD_Y && ok) ? __ldg(P.acc_in + o) : 0.f;
+                }
+            }
+        };
+        prefetch(0);
         for (int c = 0; c < nch; ++c) {
             const int s2 = c & 1;
             int lo0, len, lo1 = 0;
             chunk_geom(c, 0, L, T, lo0, len);
             if (NDIR == 2) chunk_geom(c, 1, L, T, lo1, len);
-            const int q = lane;
             const bool act = q < len;
-            // loads first: u (for D*u), z, stash, acc_in of this lane's
-            // positions; independent of the scan, so they overlap its wait
-            float uu[NDIR][CPE], zz[NDIR][CPE], ws[NDIR][CPE], ai[NDIR][CPE];
-            int cls[NDIR];
-#pragma unroll
-            for (int d = 0; d < NDIR; ++d) {
-                const int p = (d ? lo1 : lo0) + q;
-                // 0: first arrival (stash), 1: second arrival (the stash holds
-                // the other branch), 2: both in this chunk, 3: left to branch 0
-                int k = 1;
-                if (NDIR == 2) {
-                    if (d == 0) k = (p < L - (c + 1) * T) ? 0 : (p >= L - c * T ? 1 : 2);
-                    else k = (p >= (c + 1) * T) ? 0 : (p < c * T ? 1 : 3);
-                }
-                cls[d] = k;
-                const IO *up = (const IO *)P.br[d].u;
-#pragma unroll
-                for (int i = 0; i < CPE; ++i) {
-                    const bool ok = act && rowb[i] >= 0;
-                    const long long o = rowb[i] + p;
-                    uu[d][i] = (ok && k != 3) ? to_f32(up[o]) : 0.f;
-                    const bool fin = ok && (k == 1 || k == 2);
-                    zz[d][i] = (fin && P.z && OUT != OUT_ACC) ? to_f32(((const IO *)P.z)[o]) : 0.f;
-                    ws[d][i] = (NDIR == 2 && ok && k == 1) ? P.W[o] : 0.f;
-                    ai[d][i] = (OUT == OUT_ADD_Y && fin) ? P.acc_in[o] : 0.f;
-                }
-            }
             if (*abort_flag || !wait(&yp_full[s2], (c >> 1) & 1)) {
                 // the producer waits (bounded) for the B/C copies it issued
                 if (producer)
@@ -505,11 +525,9 @@ bidir_scan_kernel(const BiParams P) {
                 return;
             }
             // scan(c) is done: its B/C stage is free for chunk c + NBC
-            if (producer && issued < nch) {
-                issue_bc(c + LY::NBC);
-                ++issued;
-            }
+            if (producer) issue_bc(c + LY::NBC);
             const float *yp = (const float *)(sm + LY::off_yp + s2 * LY::YP_STAGE);
+            const IO *us = (const IO *)(sm + LY::off_u + s2 * LY::U_STAGE);
             auto ypsum = [&](int row, int jj) -> float {
                 const float *ps = yp + row * (LY::YP_ROW / 4) + jj * LPR;
                 if constexpr (LPR == 4) {
@@ -522,48 +540,58 @@ bidir_scan_kernel(const BiParams P) {
                     return ps[0];
                 }
             };
+            // every item's value first (straight-line code, items overlap),
+            // then the stores
+            float vv[NDIR][CPE];     // the stash value (first arrival) or the output
 #pragma unroll
             for (int d = 0; d < NDIR; ++d) {
                 const int lo = d ? lo1 : lo0;
                 const int p = lo + q;
-                const int k = cls[d];
-                const int jw = d ? len - 1 - q : q;            // walk step of p
+                const int k = classify(c, d, p);
+                const int jw = act ? (d ? len - 1 - q : q) : 0;     // walk step of p
+                const int jb = (NDIR == 2 && k == 2) ? L - 1 - p - c * T : 0;
 #pragma unroll
                 for (int i = 0; i < CPE; ++i) {
-                    if (!act || rowb[i] < 0 || k == 3) continue;
                     const int row = d * R + c0 + i;
-                    const float yv = fmaf(dsk[d][i], uu[d][i], ypsum(row, jw));
-                    const long long o = rowb[i] + p;
-                    if (NDIR == 2 && k == 0) {
-                        P.W[o] = yv;
-                        continue;
-                    }
-                    float v = yv;
+                    // this branch's output at p, with its D*u term
+                    const float own = fmaf(dsk_tab[d * CPE + i], to_f32(us[row * T + jw]),
+                                           ypsum(row, jw));
+                    float v = own;
                     if (NDIR == 2) {
-                        float other;
-                        if (k == 1) {
-                            other = ws[d][i];
-                        } else {                                // both here (d == 0)
-                            const int jb = L - 1 - p - c * T;   // backward walk step of p
-                            const IO *ub = (const IO *)P.br[NDIR - 1].u;
-                            other = fmaf(dsk[NDIR - 1][i], to_f32(ub[o]),
-                                         ypsum((NDIR - 1) * R + c0 + i, jb));
-                        }
-                        v = P.out_scale * (yv + other);
+                        const int rb = (NDIR - 1) * R + c0 + i;     // backward row
+                        const float same = fmaf(dsk_tab[(NDIR - 1) * CPE + i],
+                                                to_f32(us[rb * T + jb]), ypsum(rb, jb));
+                        v = k == 0 ? own : P.out_scale * (own + (k == 1 ? wr[d][i] : same));
                     }
-                    if (OUT == OUT_ACC) {
-                        P.acc_out[o] = v;
-                        continue;
+                    if (OUT == OUT_ADD_Y) v += ar[d][i];
+                    if (OUT != OUT_ACC && P.z && !(NDIR == 2 && k == 0))
+                        v *= silu_f<IO>(to_f32(zr[d][i]));
+                    vv[d][i] = v;
+                }
+            }
+            // the u stage (and the step inputs) of chunk c are no longer needed
+            mbar_arrive(&dw_empty[s2]);
+#pragma unroll
+            for (int d = 0; d < NDIR; ++d) {
+                const int p = (d ? lo1 : lo0) + q;
+                const int k = classify(c, d, p);
+#pragma unroll
+                for (int i = 0; i < CPE; ++i) {
+                    const bool live = act && i < nch_ok && k != 3;
+                    const long long o = rowb0 + (long long)i * L + p;
+                    if (NDIR == 2 && live && k == 0) P.W[o] = vv[d][i];
+                    const bool fin = live && (NDIR == 1 || k != 0);
+                    if (fin) {
+                        if (OUT == OUT_ACC) P.acc_out[o] = vv[d][i];
+                        else ((IO *)P.y)[o] = from_f32<IO>(vv[d][i]);
                     }
-                    if (OUT == OUT_ADD_Y) v += ai[d][i];
-                    if (P.z) v *= silu_f<IO>(zz[d][i]);
-                    ((IO *)P.y)[o] = from_f32<IO>(v);
                 }
             }
             mbar_arrive(&yp_empty[s2]);
-            // stash stores of this chunk must be visible to this warp's loads
-            // of the next chunk
+            // the stash stores of this chunk must precede this warp's loads
+            // of the next one
             __syncwarp();
+            if (c + 1 < nch) prefetch(c + 1);
         }
     }
 }

@@ -100,8 +100,13 @@ template <typename IO, int S, int NDIR, int G, int OUT = ssm::OUT_Y>
 ssm_status launch_bidir(const ssm::BiParams &P, cudaStream_t st, bool last = true) {
     using LY = ssm::WsLayout<IO, S, NDIR, G>;
     auto *kern = &ssm::bidir_scan_kernel<IO, S, NDIR, G, OUT>;
+    // Raising the dynamic shared-memory limit and asking for the largest
+    // shared-memory carveout are cheap and idempotent; without the carveout
+    // the driver may pick one that fits fewer CTAs per SM.
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::bytes) !=
-        cudaSuccess) {
+            cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess) {
         cudaGetLastError();
         return SSM_ERR_CUDA;
     }
