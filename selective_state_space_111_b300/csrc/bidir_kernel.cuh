@@ -199,8 +199,10 @@ struct WsLayout {
     static_assert(S == 4 || S == 8 || S == 16, "S must be 4, 8 or 16");
     static_assert((ROWS * LPR) % 32 == 0 && ROWS % 16 == 0, "whole warps per role");
     static_assert(R % 16 == 0, "each prep warp takes 16 channels of one branch");
-    // registers per thread so that 3 CTAs fit the 64 K register file
-    static constexpr int MAX_REGS = (65536 / (3 * NT)) / 8 * 8 > 255 ? 255 : (65536 / (3 * NT)) / 8 * 8;
+    // registers per thread so that 3 CTAs fit: each of the 4 schedulers of
+    // an SM has its own 16 K registers and holds up to ceil(3 NT / 128) warps
+    static constexpr int WPS = (3 * NT / 32 + 3) / 4;
+    static constexpr int MAX_REGS = (16384 / (32 * WPS)) / 8 * 8 > 255 ? 255 : (16384 / (32 * WPS)) / 8 * 8;
 };
 
 // Positions [lo, lo + len) of branch d at chunk c (both branches have the
