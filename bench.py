@@ -78,6 +78,31 @@ def measured_traffic(workload):
     return ent.get("dram_bytes_per_launch")
 
 
+# ---------------------------------------------------------------- ranks
+def rank_env():
+    """(world, rank, local_rank) from the torchrun environment (1, 0, 0 alone)."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_seed(workload, rank):
+    """Each replica draws its own inputs: the workload's seed plus the rank."""
+    from selective_state_space_111_b300.synth import seed_for
+    return seed_for(workload) + rank
+
+
+def max_over_ranks(value, world, device=None):
+    """The slowest rank's time (the job's time): an all-reduce MAX of one
+    float (a no-op alone).  Replicas share nothing else."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def call(ssm, spec, g, ws, out):
     sp = spec.delta_softplus
     if spec.op == "single":
@@ -168,18 +193,16 @@ def run_ours(args):
     from selective_state_space_111_b300 import build
     build.build()
     import selective_state_space_111_b300 as ssm
-    from selective_state_space_111_b300.synth import WORKLOADS, make_inputs, seed_for
+    from selective_state_space_111_b300.synth import WORKLOADS, make_inputs
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_env()
     if world > 1:
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
     spec = WORKLOADS[args.workload]
-    t = make_inputs(spec, seed_for(args.workload) + rank)
+    t = make_inputs(spec, rank_seed(args.workload, rank))
     g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in t.items()}
     L = spec.seq_len
     ws_n = ssm.workspace_bytes(spec.op, g["u" if spec.op != "ss2d" else "x"].dtype, spec.B,
@@ -218,10 +241,7 @@ def run_ours(args):
     clocks = sampler.stop()
     kern = [kb[i].elapsed_time(ke[i]) for i in range(args.steps)]
     total_ms = ev[0].elapsed_time(ev[-1])
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
 
     # e2e: host (pinned) inputs -> device -> the public API -> result to host
     e2e = None
@@ -249,10 +269,7 @@ def run_ours(args):
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / n_e2e
-        if world > 1:
-            tt = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e_ms = float(tt.item())
+        e2e_ms = max_over_ranks(e2e_ms, world, dev)
         e2e = {"value": round(spec.algorithmic_bytes() * world / (e2e_ms * 1e-3) / 1e9, 3),
                "unit": "GB/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": round(e2e_ms, 4)}

@@ -188,13 +188,14 @@ struct WsLayout {
     static constexpr int off_bc = 0;                        // 128-byte aligned
     static constexpr int off_dw = off_bc + NBC * BC_STAGE;
     static constexpr int off_yp = off_dw + 2 * DW_STAGE;
+    static constexpr int NU = 4;                            // u ring (prep -> epilogue)
     static constexpr int off_u = off_yp + 2 * YP_STAGE;
-    static constexpr int off_bar = (off_u + 2 * U_STAGE + 7) & ~7;
-    // bc_full[NBC], dw_full[2], dw_empty[2], yp_full[2], yp_empty[2]
-    static constexpr int NBAR = NBC + 8;
+    static constexpr int off_bar = (off_u + NU * U_STAGE + 7) & ~7;
+    // bc_full[NBC], dw_full[2], dw_empty[2], yp_full[2], yp_empty[2], u_empty[NU]
+    static constexpr int NBAR = NBC + 8 + NU;
     static constexpr int off_flag = off_bar + NBAR * 8;
-    static constexpr int off_tab = off_flag + 16;             // D per (branch, channel)
-    static constexpr int bytes = off_tab + ROWS * 4;
+    static constexpr int off_tab = off_flag + 16;             // D and bias per row
+    static constexpr int bytes = off_tab + 2 * ROWS * 4;     // D, then bias
 
     static_assert(S == 4 || S == 8 || S == 16, "S must be 4, 8 or 16");
     static_assert((ROWS * LPR) % 32 == 0 && ROWS % 16 == 0, "whole warps per role");
@@ -233,9 +234,10 @@ bidir_scan_kernel(const BiParams P) {
     uint64_t *bar = (uint64_t *)(sm + LY::off_bar);
     uint64_t *bc_full = bar;                   // count 1 (+ transaction bytes)
     uint64_t *dw_full = bar + LY::NBC;         // count NPW*32
-    uint64_t *dw_empty = dw_full + 2;          // count NEW*32
+    uint64_t *dw_empty = dw_full + 2;          // count NSW*32
     uint64_t *yp_full = dw_empty + 2;          // count NSW*32
     uint64_t *yp_empty = yp_full + 2;          // count NEW*32
+    uint64_t *u_empty = yp_empty + 2;          // count NEW*32 (u ring, NU deep)
     volatile int *abort_flag = (volatile int *)(sm + LY::off_flag);
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
@@ -251,10 +253,12 @@ bidir_scan_kernel(const BiParams P) {
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
             mbar_init(&dw_full[s], NPW * 32);
-            mbar_init(&dw_empty[s], LY::NEW * 32);   // released by the epilogue (u stage)
+            mbar_init(&dw_empty[s], NSW * 32);
             mbar_init(&yp_full[s], NSW * 32);
             mbar_init(&yp_empty[s], LY::NEW * 32);
         }
+#pragma unroll
+        for (int s = 0; s < LY::NU; ++s) mbar_init(&u_empty[s], LY::NEW * 32);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -341,19 +345,31 @@ bidir_scan_kernel(const BiParams P) {
                         bw[jj][q] = mul2(bq, ww);
                     }
                 }
-                float ys[UB];
+                // recurrences in state-pair-major order (the independent h
+                // chains sit next to each other) with two readout
+                // accumulators per step, so no chain is longer than UB
+                f2 ya[UB], yb[UB];
 #pragma unroll
                 for (int jj = 0; jj < UB; ++jj) {
-                    f2 y2;
+                    ya[jj] = pk(0.f, 0.f);
+                    yb[jj] = pk(0.f, 0.f);
+                }
 #pragma unroll
-                    for (int q = 0; q < NP; ++q) {
+                for (int q = 0; q < NP; ++q) {
+#pragma unroll
+                    for (int jj = 0; jj < UB; ++jj) {
                         const float4 &vc = cv[jj][q / 2];
                         const f2 cq = (q & 1) ? pk(vc.z, vc.w) : pk(vc.x, vc.y);
                         h[q] = fma2(e[jj][q], h[q], bw[jj][q]);
-                        y2 = (q == 0) ? mul2(cq, h[q]) : fma2(cq, h[q], y2);
+                        if (q & 1) yb[jj] = fma2(cq, h[q], yb[jj]);
+                        else ya[jj] = fma2(cq, h[q], ya[jj]);
                     }
+                }
+                float ys[UB];
+#pragma unroll
+                for (int jj = 0; jj < UB; ++jj) {
                     float ylo, yhi;
-                    upk(y2, ylo, yhi);
+                    upk(add2(ya[jj], yb[jj]), ylo, yhi);
                     ys[jj] = ylo + yhi;
                 }
 #pragma unroll
@@ -382,6 +398,7 @@ bidir_scan_kernel(const BiParams P) {
             int j = 0;
             for (; j + UB <= len; j += UB) block(j);
             for (; j < len; ++j) step(j);
+            mbar_arrive(&dw_empty[s2]);
             mbar_arrive(&yp_full[s2]);
         }
     } else if (warp < NSW + NPW) {
@@ -394,49 +411,64 @@ bidir_scan_kernel(const BiParams P) {
         const IO *dtp = (const IO *)br.dt;
         const IO *up = (const IO *)br.u;
         const bool srev = br.stream_rev != 0;
-        float bias[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int ch = d0 + r0 + i;
-            bias[i] = (ch < D && br.bias) ? br.bias[ch] : 0.f;
+        // this warp's 16 biases in shared memory
+        float *bias_tab = (float *)(sm + LY::off_tab) + LY::ROWS + pw * 16;
+        if (lane < 16) {
+            const int ch = d0 + r0 + lane;
+            bias_tab[lane] = (ch < D && br.bias) ? br.bias[ch] : 0.f;
         }
+        __syncwarp();
         const long long dt0 = br.dt_off + b * br.dt_bstride + (long long)(d0 + r0) * L;
         const long long u0 = (bD + d0 + r0) * L;
         const int nrow = min(16, D - (d0 + r0));            // valid rows of this warp
-        for (int c = 0; c < nch; ++c) {
-            const int s2 = c & 1;
+        // dt and u of chunk c for this lane's walk step, all 32 loads in
+        // flight together; fetched one chunk ahead of their use
+        IO xdt[16], xu[16];
+        auto fetch = [&](int c) {
             int lo, len;
             chunk_geom(c, d, L, T, lo, len);
             const int j = lane;
             const bool act = j < len;
             const int p = d ? lo + len - 1 - j : lo + j;        // position of walk step j
             const int si = srev ? stream_lo(c, d, lo) + j : p;  // dt stream index
-            // all loads of the chunk first (coalesced: 32 consecutive
-            // elements of each row), then the arithmetic
-            IO xdt[16], xu[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const bool ok = act && i < nrow;
                 xdt[i] = ok ? __ldg(dtp + dt0 + (long long)i * L + si) : from_f32<IO>(0.f);
                 xu[i] = ok ? __ldg(up + u0 + (long long)i * L + p) : from_f32<IO>(0.f);
             }
-            if (*abort_flag || !wait(&dw_empty[s2], ((c >> 1) & 1) ^ 1)) return;
-            float4 *dw = (float4 *)(sm + LY::off_dw + s2 * LY::DW_STAGE);
-            float dlv[16], wv[16];
+        };
+        fetch(0);
+        for (int c = 0; c < nch; ++c) {
+            const int s2 = c & 1;
+            int lo, len;
+            chunk_geom(c, d, L, T, lo, len);
+            const int j = lane;
+            const bool act = j < len;
+            IO cdt[16], cu[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                const float x = to_f32(xdt[i]) + bias[i];
-                const float dl = P.delta_softplus ? softplus_f<IO>(x) : x;
-                dlv[i] = i < nrow ? dl : 0.f;
-                wv[i] = i < nrow ? dl * to_f32(xu[i]) : 0.f;
+                cdt[i] = xdt[i];
+                cu[i] = xu[i];
             }
-            if (act) {
-                IO *us = (IO *)(sm + LY::off_u + s2 * LY::U_STAGE);
+            if (c + 1 < nch) fetch(c + 1);
+            const int su = c % LY::NU;
+            if (*abort_flag || !wait(&dw_empty[s2], ((c >> 1) & 1) ^ 1) ||
+                !wait(&u_empty[su], ((c / LY::NU) & 1) ^ 1))
+                return;
+            // shared-memory stores only: they cannot alias the global loads
+            // in flight, so each row is computed and stored in turn
+            float4 *dw = (float4 *)(sm + LY::off_dw + s2 * LY::DW_STAGE);
+            IO *us = (IO *)(sm + LY::off_u + su * LY::U_STAGE);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    dw[(d * R + r0 + i) * (LY::DW_ROW / 16) + j] =
-                        make_float4(dlv[i], dlv[i], wv[i], wv[i]);
-                    us[(d * R + r0 + i) * T + j] = xu[i];
+            for (int i = 0; i < 16; ++i) {
+                const float x = to_f32(cdt[i]) + bias_tab[i];
+                float dl = P.delta_softplus ? softplus_f<IO>(x) : x;
+                dl = i < nrow ? dl : 0.f;
+                const float w = dl * to_f32(cu[i]);
+                if (act) {
+                    dw[(d * R + r0 + i) * (LY::DW_ROW / 16) + j] = make_float4(dl, dl, w, w);
+                    us[(d * R + r0 + i) * T + j] = cu[i];
                 }
             }
             mbar_arrive(&dw_full[s2]);
@@ -529,7 +561,7 @@ bidir_scan_kernel(const BiParams P) {
             // scan(c) is done: its B/C stage is free for chunk c + NBC
             if (producer) issue_bc(c + LY::NBC);
             const float *yp = (const float *)(sm + LY::off_yp + s2 * LY::YP_STAGE);
-            const IO *us = (const IO *)(sm + LY::off_u + s2 * LY::U_STAGE);
+            const IO *us = (const IO *)(sm + LY::off_u + (c % LY::NU) * LY::U_STAGE);
             auto ypsum = [&](int row, int jj) -> float {
                 const float *ps = yp + row * (LY::YP_ROW / 4) + jj * LPR;
                 if constexpr (LPR == 4) {
@@ -545,45 +577,71 @@ bidir_scan_kernel(const BiParams P) {
             // every item's value first (straight-line code, items overlap),
             // then the stores
             float vv[NDIR][CPE];     // the stash value (first arrival) or the output
+            int kk[NDIR];
 #pragma unroll
             for (int d = 0; d < NDIR; ++d) {
                 const int lo = d ? lo1 : lo0;
                 const int p = lo + q;
                 const int k = classify(c, d, p);
+                kk[d] = k;
                 const int jw = act ? (d ? len - 1 - q : q) : 0;     // walk step of p
-                const int jb = (NDIR == 2 && k == 2) ? L - 1 - p - c * T : 0;
+                // this branch's rows at walk step jw
+                const float *ypd = yp + (d * R + c0) * (LY::YP_ROW / 4) + jw * LPR;
+                const IO *usd = us + (d * R + c0) * T + jw;
+                float own[CPE];
 #pragma unroll
                 for (int i = 0; i < CPE; ++i) {
-                    const int row = d * R + c0 + i;
-                    // this branch's output at p, with its D*u term
-                    const float own = fmaf(dsk_tab[d * CPE + i], to_f32(us[row * T + jw]),
-                                           ypsum(row, jw));
-                    float v = own;
-                    if (NDIR == 2) {
-                        const int rb = (NDIR - 1) * R + c0 + i;     // backward row
-                        const float same = fmaf(dsk_tab[(NDIR - 1) * CPE + i],
-                                                to_f32(us[rb * T + jb]), ypsum(rb, jb));
-                        v = k == 0 ? own : P.out_scale * (own + (k == 1 ? wr[d][i] : same));
+                    const float *ps = ypd + i * (LY::YP_ROW / 4);
+                    float part;
+                    if constexpr (LPR == 4) {
+                        const float4 v = *(const float4 *)ps;
+                        part = (v.x + v.y) + (v.z + v.w);
+                    } else if constexpr (LPR == 2) {
+                        const float2 v = *(const float2 *)ps;
+                        part = v.x + v.y;
+                    } else {
+                        part = ps[0];
                     }
+                    own[i] = fmaf(dsk_tab[d * CPE + i], to_f32(usd[i * T]), part);
+                }
+                if (NDIR == 2 && d == 0 && __any_sync(0xffffffffu, k == 2)) {
+                    // both branches reach p in this chunk (the middle of the
+                    // sequence): the backward branch's output from its rows
+                    const int jb = k == 2 ? L - 1 - p - c * T : 0;
+                    const int rb0 = (NDIR - 1) * R + c0;
+#pragma unroll
+                    for (int i = 0; i < CPE; ++i) {
+                        if (k == 2)
+                            wr[d][i] = fmaf(dsk_tab[(NDIR - 1) * CPE + i],
+                                            to_f32(us[(rb0 + i) * T + jb]),
+                                            ypsum(rb0 + i, jb));
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < CPE; ++i) {
+                    float v = own[i];
+                    if (NDIR == 2) v = k == 0 ? v : P.out_scale * (v + wr[d][i]);
                     if (OUT == OUT_ADD_Y) v += ar[d][i];
                     if (OUT != OUT_ACC && P.z && !(NDIR == 2 && k == 0))
                         v *= silu_f<IO>(to_f32(zr[d][i]));
                     vv[d][i] = v;
                 }
             }
-            // the u stage (and the step inputs) of chunk c are no longer needed
-            mbar_arrive(&dw_empty[s2]);
+            // the u stage of chunk c is no longer needed
+            mbar_arrive(&u_empty[c % LY::NU]);
 #pragma unroll
             for (int d = 0; d < NDIR; ++d) {
                 const int p = (d ? lo1 : lo0) + q;
-                const int k = classify(c, d, p);
+                const int k = kk[d];
+                const bool live = act && k != 3;
+                const bool fin = live && (NDIR == 1 || k != 0);
+                const long long o0 = rowb0 + p;
 #pragma unroll
                 for (int i = 0; i < CPE; ++i) {
-                    const bool live = act && i < nch_ok && k != 3;
-                    const long long o = rowb0 + (long long)i * L + p;
-                    if (NDIR == 2 && live && k == 0) P.W[o] = vv[d][i];
-                    const bool fin = live && (NDIR == 1 || k != 0);
-                    if (fin) {
+                    const bool ok = i < nch_ok;
+                    const long long o = o0 + (long long)i * L;
+                    if (NDIR == 2 && ok && live && k == 0) P.W[o] = vv[d][i];
+                    if (ok && fin) {
                         if (OUT == OUT_ACC) P.acc_out[o] = vv[d][i];
                         else ((IO *)P.y)[o] = from_f32<IO>(vv[d][i]);
                     }
