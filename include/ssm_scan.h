@@ -22,8 +22,9 @@
  *  - All tensor pointers are DEVICE pointers to contiguous, caller-owned
  *    memory.  I/O tensors (u, delta, B, C, z, y and the per-branch copies)
  *    use the dtype `dt` (fp32 or bf16); A, Dskip and delta_bias are fp32.
- *  - Every I/O tensor must start on a 16-byte boundary (as cudaMalloc and
- *    PyTorch allocations do); the fp32 parameters on a 4-byte boundary.
+ *  - Every pointer must be aligned to its element type (2 bytes for bf16,
+ *    4 for fp32); I/O tensors may start anywhere else, e.g. at an offset
+ *    into a larger buffer.  Only the workspace needs 16 bytes.
  *  - Optional pointers may be NULL: Dskip -> 0, z -> no gate,
  *    delta_bias -> 0 (and u_b -> u for v2).
  *  - `y` must not alias any input.  State and arithmetic are fp32; bf16

@@ -15,35 +15,30 @@
 // y_t * silu(z_t) ("VMamba的SS2D模块详解" section 2.1).
 //
 // The path is bound by the arithmetic of the recurrence (per element update
-// four fp32 operations and one MUFU ex2; see the roofline in the design
-// notes), so the kernel is organised to spend its issue slots there:
+// four fp32 operations and one MUFU ex2), so the kernel is organised to
+// spend its issue slots there:
 //
 //   pack_bc_kernel  B and C ([B, N, L], I/O dtype) are converted once per
 //                   batch element into a packed fp32 stream BC[b][t][32] =
 //                   (B_0..B_15, C_0..C_15) -- 128 bytes per position, so one
-//                   chunk of positions is one contiguous, aligned range.
+//                   chunk of positions is one contiguous, aligned range that
+//                   a single bulk copy (cp.async.bulk) moves to shared memory.
 //   bidir_scan_kernel
-//     CTA    = G channels of one batch element x NDIR branches.
-//     lane   = (branch, channel, state group): S of the 16 states of one
-//              channel; LPR = 16 / S lanes share a channel.  The states are
-//              packed fp32 pairs updated with the f32x2 MUL/FMA forms.
-//     time   = chunks of T positions.  Everything a chunk reads arrives by
-//              bulk copies (TMA, cp.async.bulk) completing on mbarriers:
-//              per branch one copy of the packed B/C range (2-deep ring),
-//              one per dt / u / z row segment (3-deep ring, issued two
-//              chunks ahead) and one per fp32 stash / accumulator segment.
-//              Rows of odd length do not start on 16 bytes, so a segment
-//              copies the whole 16-byte vectors covering it; TMA tensor
-//              maps cannot describe such rows (their stride must be a
-//              multiple of 16 bytes).
-//     phases = prep  (delta, w = delta * u) once per (branch, channel, step);
-//              scan  T steps per lane; the lane's partial readout per step
-//                    goes to shared memory;
-//              epilogue sums the partials, adds D*u, fuses the branches,
-//                    gates and stores.
-//              prep and epilogue run one warp per (branch, channel) row and
-//              one lane per position, so row constants are warp-uniform and
-//              global stores are coalesced.
+//     CTA  = R channels of one batch element x NDIR branches, T = 32
+//            positions per chunk, in three warp roles linked by full/empty
+//            mbarrier rings:
+//     scan warps      lane = (branch, channel, group of S states); the states
+//                     are packed fp32 pairs (f32x2 MUL/FMA); per step the
+//                     lane's partial readout goes to shared memory;
+//     prep warps      lane = walk step; dt and u are read element by element
+//                     (32 consecutive positions per row, coalesced) one chunk
+//                     ahead; delta = softplus(dt + bias) and w = delta * u
+//                     are computed once per (branch, channel, step);
+//     epilogue warps  lane = position; sum the partial readouts, add D * u,
+//                     fuse the branches, gate and store (coalesced); one lane
+//                     issues the B/C bulk copies.
+//     Every wait is bounded in time; on expiry the kernel sets the status
+//     word and all roles stop.
 //
 // Flip-add without flipped copies.  At chunk c the forward branch covers
 // positions [cT, cT+T) and the backward branch [L-cT-T, L-cT) (clipped),
@@ -66,7 +61,7 @@ constexpr int kBC = 2 * kMaxN;   // floats per position in the packed B/C stream
 #endif
 
 struct BiBranch {
-    const void *dt;        // delta tensor (I/O dtype, 16-byte aligned); row
+    const void *dt;        // delta tensor (I/O dtype); row
                            // (b, d) of this branch starts at element
                            // dt_off + b * dt_bstride + d * L
     const void *u;         // [B, D, L] I/O dtype, position order
@@ -76,7 +71,6 @@ struct BiBranch {
     const float *bias;     // [D] or null
     long long dt_off;      // elements to this branch's first row
     long long dt_bstride;  // elements between batch elements of dt
-    long long dt_total;    // elements in the whole dt tensor (tail guard)
     int stream_rev;        // backward branch only: dt and B/C are stored in
                            // walk order (index L-1-p for position p)
 };
@@ -96,7 +90,6 @@ struct BiParams {
     float *acc_out;        // [B, D, L] fp32 (OUT_ACC)
     float *W;              // [B, D, L] fp32 stash (two branches, several chunks)
     unsigned *status;      // device status word, or null
-    long long total;       // B * D * L
     int B, D, L, N;
     int nchunks;
     int delta_softplus;
@@ -408,8 +401,6 @@ bidir_scan_kernel(const BiParams P) {
         const int d = (pw * 16) / R;
         const int r0 = (pw * 16) % R;
         const BiBranch &br = P.br[d];
-        const IO *dtp = (const IO *)br.dt;
-        const IO *up = (const IO *)br.u;
         const bool srev = br.stream_rev != 0;
         // this warp's 16 biases in shared memory
         float *bias_tab = (float *)(sm + LY::off_tab) + LY::ROWS + pw * 16;
@@ -418,8 +409,10 @@ bidir_scan_kernel(const BiParams P) {
             bias_tab[lane] = (ch < D && br.bias) ? br.bias[ch] : 0.f;
         }
         __syncwarp();
-        const long long dt0 = br.dt_off + b * br.dt_bstride + (long long)(d0 + r0) * L;
-        const long long u0 = (bD + d0 + r0) * L;
+        // first row of this warp in dt and u; row i is i * L further on
+        // (offsets within the rows stay below D * L < 2^31)
+        const IO *dtb = (const IO *)br.dt + br.dt_off + b * br.dt_bstride + (long long)(d0 + r0) * L;
+        const IO *ub = (const IO *)br.u + (bD + d0 + r0) * L;
         const int nrow = min(16, D - (d0 + r0));            // valid rows of this warp
         // dt and u of chunk c for this lane's walk step, all 32 loads in
         // flight together; fetched one chunk ahead of their use
@@ -428,14 +421,38 @@ bidir_scan_kernel(const BiParams P) {
             int lo, len;
             chunk_geom(c, d, L, T, lo, len);
             const int j = lane;
-            const bool act = j < len;
             const int p = d ? lo + len - 1 - j : lo + j;        // position of walk step j
-            const int si = srev ? stream_lo(c, d, lo) + j : p;  // dt stream index
+            const int si = srev ? c * T + j : p;                // dt stream index
+            if (len == T && nrow == 16) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    xdt[i] = __ldg(dtb + (i * L + si));
+                    xu[i] = __ldg(ub + (i * L + p));
+                }
+            } else {
+                const bool act = j < len;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const bool ok = act && i < nrow;
+                    xdt[i] = ok ? __ldg(dtb + (i * L + si)) : from_f32<IO>(0.f);
+                    xu[i] = ok ? __ldg(ub + (i * L + p)) : from_f32<IO>(0.f);
+                }
+            }
+        };
+        // delta and w of 16 rows to shared memory; SP: softplus, FULL: a
+        // whole chunk of 16 valid rows (no per-row predicates)
+        auto emit = [&](auto SP, auto FULL, const IO *cdt, const IO *cu, float4 *dwl, IO *usl,
+                        bool act) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                const bool ok = act && i < nrow;
-                xdt[i] = ok ? __ldg(dtp + dt0 + (long long)i * L + si) : from_f32<IO>(0.f);
-                xu[i] = ok ? __ldg(up + u0 + (long long)i * L + p) : from_f32<IO>(0.f);
+                const float x = to_f32(cdt[i]) + bias_tab[i];
+                float dl = decltype(SP)::value ? softplus_f<IO>(x) : x;
+                if (!decltype(FULL)::value) dl = i < nrow ? dl : 0.f;
+                const float w = dl * to_f32(cu[i]);
+                if (decltype(FULL)::value || act) {
+                    dwl[i * (LY::DW_ROW / 16)] = make_float4(dl, dl, w, w);
+                    usl[i * T] = cu[i];
+                }
             }
         };
         fetch(0);
@@ -458,18 +475,16 @@ bidir_scan_kernel(const BiParams P) {
                 return;
             // shared-memory stores only: they cannot alias the global loads
             // in flight, so each row is computed and stored in turn
-            float4 *dw = (float4 *)(sm + LY::off_dw + s2 * LY::DW_STAGE);
-            IO *us = (IO *)(sm + LY::off_u + su * LY::U_STAGE);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float x = to_f32(cdt[i]) + bias_tab[i];
-                float dl = P.delta_softplus ? softplus_f<IO>(x) : x;
-                dl = i < nrow ? dl : 0.f;
-                const float w = dl * to_f32(cu[i]);
-                if (act) {
-                    dw[(d * R + r0 + i) * (LY::DW_ROW / 16) + j] = make_float4(dl, dl, w, w);
-                    us[(d * R + r0 + i) * T + j] = cu[i];
-                }
+            float4 *dwl = (float4 *)(sm + LY::off_dw + s2 * LY::DW_STAGE) +
+                          (d * R + r0) * (LY::DW_ROW / 16) + j;
+            IO *usl = (IO *)(sm + LY::off_u + su * LY::U_STAGE) + (d * R + r0) * T + j;
+            const bool full = len == T && nrow == 16;
+            if (P.delta_softplus) {
+                if (full) emit(BoolC<true>(), BoolC<true>(), cdt, cu, dwl, usl, act);
+                else emit(BoolC<true>(), BoolC<false>(), cdt, cu, dwl, usl, act);
+            } else {
+                if (full) emit(BoolC<false>(), BoolC<true>(), cdt, cu, dwl, usl, act);
+                else emit(BoolC<false>(), BoolC<false>(), cdt, cu, dwl, usl, act);
             }
             mbar_arrive(&dw_full[s2]);
         }
@@ -486,7 +501,14 @@ bidir_scan_kernel(const BiParams P) {
             dsk_tab[lane] = (ch < D && P.br[d].Dskip) ? P.br[d].Dskip[ch] : 0.f;
         }
         __syncwarp();
-        const long long rowb0 = (bD + d0 + c0) * L;          // channel c0's row
+        // channel c0's row in each [B, D, L] tensor; channel c0 + i is i * L
+        // further on (offsets within the rows stay below D * L < 2^31)
+        const long long rowb0 = (bD + d0 + c0) * L;
+        const IO *zrow = P.z ? (const IO *)P.z + rowb0 : nullptr;
+        float *Wrow = P.W ? P.W + rowb0 : nullptr;
+        IO *yrow = P.y ? (IO *)P.y + rowb0 : nullptr;
+        float *aorow = P.acc_out ? P.acc_out + rowb0 : nullptr;
+        const float *airow = P.acc_in ? P.acc_in + rowb0 : nullptr;
         const int nch_ok = min(CPE, D - (d0 + c0));           // valid channels
         auto issue_bc = [&](int c) {
             if (c >= nch || c == P.withhold_bc) return;
@@ -516,32 +538,48 @@ bidir_scan_kernel(const BiParams P) {
             if (d == 0) return (p < L - (c + 1) * T) ? 0 : (p >= L - c * T ? 1 : 2);
             return (p >= (c + 1) * T) ? 0 : (p < c * T ? 1 : 3);
         };
+        // the same for a whole chunk (both branches): 0 every position is a
+        // first arrival, 1 every position is finalised here, 2 the middle of
+        // the sequence (classes mixed)
+        auto kind = [&](int c) -> int {
+            if (NDIR == 1) return 1;
+            if ((2LL * c + 2) * T <= L) return 0;
+            if (2LL * c * T >= L) return 1;
+            return 2;
+        };
         // z, the stash and acc_in of the positions a lane finalises at chunk
         // c, fetched one chunk ahead (raw values, converted at use, all in
         // flight together).  u comes from the prep warps through shared
         // memory (its stage is released by this role).
         IO zr[NDIR][CPE];
         float wr[NDIR][CPE], ar[NDIR][CPE];
-        auto prefetch = [&](int c) {
-            int lo0, len, lo1 = 0;
-            chunk_geom(c, 0, L, T, lo0, len);
-            if (NDIR == 2) chunk_geom(c, 1, L, T, lo1, len);
+        auto load_items = [&](auto FULL, int c, int kd, int lo0, int lo1, int len) {
             const bool act = q < len;
 #pragma unroll
             for (int d = 0; d < NDIR; ++d) {
                 const int p = (d ? lo1 : lo0) + q;
-                const int k = classify(c, d, p);
-                const bool fin = act && (k == 1 || k == 2);
+                const int k = kd == 1 ? 1 : classify(c, d, p);
+                const bool fin = decltype(FULL)::value || (act && (k == 1 || k == 2));
+                const bool stash = NDIR == 2 && (decltype(FULL)::value || k == 1);
 #pragma unroll
                 for (int i = 0; i < CPE; ++i) {
-                    const bool ok = fin && i < nch_ok;
-                    const long long o = rowb0 + (long long)i * L + p;
-                    zr[d][i] = (ok && OUT != OUT_ACC && P.z != nullptr)
-                                   ? __ldg((const IO *)P.z + o) : from_f32<IO>(0.f);
-                    wr[d][i] = (NDIR == 2 && ok && k == 1) ? P.W[o] : 0.f;
-                    ar[d][i] = (OUT == OUT_ADD_Y && ok) ? __ldg(P.acc_in + o) : 0.f;
+                    const bool ok = fin && (decltype(FULL)::value || i < nch_ok);
+                    const int o = i * L + p;
+                    zr[d][i] = (ok && OUT != OUT_ACC && zrow != nullptr) ? __ldg(zrow + o)
+                                                                          : from_f32<IO>(0.f);
+                    wr[d][i] = (ok && stash) ? Wrow[o] : 0.f;
+                    ar[d][i] = (OUT == OUT_ADD_Y && ok) ? __ldg(airow + o) : 0.f;
                 }
             }
+        };
+        auto prefetch = [&](int c) {
+            const int kd = kind(c);
+            if (kd == 0) return;                    // nothing to read back
+            int lo0, len, lo1 = 0;
+            chunk_geom(c, 0, L, T, lo0, len);
+            if (NDIR == 2) chunk_geom(c, 1, L, T, lo1, len);
+            if (kd == 1 && len == T && nch_ok == CPE) load_items(BoolC<true>(), c, kd, lo0, lo1, len);
+            else load_items(BoolC<false>(), c, kd, lo0, lo1, len);
         };
         prefetch(0);
         for (int c = 0; c < nch; ++c) {
@@ -574,76 +612,104 @@ bidir_scan_kernel(const BiParams P) {
                     return ps[0];
                 }
             };
-            // every item's value first (straight-line code, items overlap),
-            // then the stores
+            // output of branch d, channel c0 + i at walk step jw, with D * u
+            auto own = [&](int d, int i, int jw) -> float {
+                const int row = d * R + c0 + i;
+                return fmaf(dsk_tab[d * CPE + i], to_f32(us[row * T + jw]), ypsum(row, jw));
+            };
+            const int kd = kind(c);
             float vv[NDIR][CPE];     // the stash value (first arrival) or the output
-            int kk[NDIR];
+            if (kd == 0) {
+                // every position is a first arrival (so the chunk is full):
+                // both branches leave their outputs in the stash
 #pragma unroll
-            for (int d = 0; d < NDIR; ++d) {
-                const int lo = d ? lo1 : lo0;
-                const int p = lo + q;
-                const int k = classify(c, d, p);
-                kk[d] = k;
-                const int jw = act ? (d ? len - 1 - q : q) : 0;     // walk step of p
-                // this branch's rows at walk step jw
-                const float *ypd = yp + (d * R + c0) * (LY::YP_ROW / 4) + jw * LPR;
-                const IO *usd = us + (d * R + c0) * T + jw;
-                float own[CPE];
+                for (int d = 0; d < NDIR; ++d)
 #pragma unroll
-                for (int i = 0; i < CPE; ++i) {
-                    const float *ps = ypd + i * (LY::YP_ROW / 4);
-                    float part;
-                    if constexpr (LPR == 4) {
-                        const float4 v = *(const float4 *)ps;
-                        part = (v.x + v.y) + (v.z + v.w);
-                    } else if constexpr (LPR == 2) {
-                        const float2 v = *(const float2 *)ps;
-                        part = v.x + v.y;
-                    } else {
-                        part = ps[0];
-                    }
-                    own[i] = fmaf(dsk_tab[d * CPE + i], to_f32(usd[i * T]), part);
+                    for (int i = 0; i < CPE; ++i) vv[d][i] = own(d, i, d ? T - 1 - q : q);
+                mbar_arrive(&u_empty[c % LY::NU]);
+#pragma unroll
+                for (int d = 0; d < NDIR; ++d) {
+                    const int p = (d ? lo1 : lo0) + q;
+#pragma unroll
+                    for (int i = 0; i < CPE; ++i)
+                        if (i < nch_ok) Wrow[i * L + p] = vv[d][i];
                 }
-                if (NDIR == 2 && d == 0 && __any_sync(0xffffffffu, k == 2)) {
-                    // both branches reach p in this chunk (the middle of the
-                    // sequence): the backward branch's output from its rows
-                    const int jb = k == 2 ? L - 1 - p - c * T : 0;
-                    const int rb0 = (NDIR - 1) * R + c0;
+            } else if (kd == 1) {
+                // every position is finalised here (single direction, or
+                // the other branch's output is in the stash)
+                const bool gate = OUT != OUT_ACC && zrow != nullptr;
+#pragma unroll
+                for (int d = 0; d < NDIR; ++d) {
+                    const int jw = act ? (d ? len - 1 - q : q) : 0;
 #pragma unroll
                     for (int i = 0; i < CPE; ++i) {
-                        if (k == 2)
-                            wr[d][i] = fmaf(dsk_tab[(NDIR - 1) * CPE + i],
-                                            to_f32(us[(rb0 + i) * T + jb]),
-                                            ypsum(rb0 + i, jb));
+                        float v = own(d, i, jw);
+                        if (NDIR == 2) v = P.out_scale * (v + wr[d][i]);
+                        if (OUT == OUT_ADD_Y) v += ar[d][i];
+                        if (gate) v *= silu_f<IO>(to_f32(zr[d][i]));
+                        vv[d][i] = v;
                     }
                 }
+                mbar_arrive(&u_empty[c % LY::NU]);
+                const bool full = len == T && nch_ok == CPE;
 #pragma unroll
-                for (int i = 0; i < CPE; ++i) {
-                    float v = own[i];
-                    if (NDIR == 2) v = k == 0 ? v : P.out_scale * (v + wr[d][i]);
-                    if (OUT == OUT_ADD_Y) v += ar[d][i];
-                    if (OUT != OUT_ACC && P.z && !(NDIR == 2 && k == 0))
-                        v *= silu_f<IO>(to_f32(zr[d][i]));
-                    vv[d][i] = v;
+                for (int d = 0; d < NDIR; ++d) {
+                    const int p = (d ? lo1 : lo0) + q;
+#pragma unroll
+                    for (int i = 0; i < CPE; ++i) {
+                        if (full || (act && i < nch_ok)) {
+                            if (OUT == OUT_ACC) aorow[i * L + p] = vv[d][i];
+                            else yrow[i * L + p] = from_f32<IO>(vv[d][i]);
+                        }
+                    }
                 }
-            }
-            // the u stage of chunk c is no longer needed
-            mbar_arrive(&u_empty[c % LY::NU]);
+            } else {
+                // the middle of the sequence: classes differ between lanes
+                int kk[NDIR];
 #pragma unroll
-            for (int d = 0; d < NDIR; ++d) {
-                const int p = (d ? lo1 : lo0) + q;
-                const int k = kk[d];
-                const bool live = act && k != 3;
-                const bool fin = live && (NDIR == 1 || k != 0);
-                const long long o0 = rowb0 + p;
+                for (int d = 0; d < NDIR; ++d) {
+                    const int lo = d ? lo1 : lo0;
+                    const int p = lo + q;
+                    const int k = classify(c, d, p);
+                    kk[d] = k;
+                    const int jw = act ? (d ? len - 1 - q : q) : 0;     // walk step of p
+                    float ow[CPE];
 #pragma unroll
-                for (int i = 0; i < CPE; ++i) {
-                    const bool ok = i < nch_ok;
-                    const long long o = o0 + (long long)i * L;
-                    if (NDIR == 2 && ok && live && k == 0) P.W[o] = vv[d][i];
-                    if (ok && fin) {
-                        if (OUT == OUT_ACC) P.acc_out[o] = vv[d][i];
-                        else ((IO *)P.y)[o] = from_f32<IO>(vv[d][i]);
+                    for (int i = 0; i < CPE; ++i) ow[i] = own(d, i, jw);
+                    if (NDIR == 2 && d == 0 && __any_sync(0xffffffffu, k == 2)) {
+                        // both branches reach p in this chunk: the backward
+                        // branch's output from its rows
+                        const int jb = k == 2 ? L - 1 - p - c * T : 0;
+#pragma unroll
+                        for (int i = 0; i < CPE; ++i)
+                            if (k == 2) wr[d][i] = own(NDIR - 1, i, jb);
+                    }
+#pragma unroll
+                    for (int i = 0; i < CPE; ++i) {
+                        float v = ow[i];
+                        if (NDIR == 2) v = k == 0 ? v : P.out_scale * (v + wr[d][i]);
+                        if (OUT == OUT_ADD_Y) v += ar[d][i];
+                        if (OUT != OUT_ACC && zrow != nullptr && !(NDIR == 2 && k == 0))
+                            v *= silu_f<IO>(to_f32(zr[d][i]));
+                        vv[d][i] = v;
+                    }
+                }
+                mbar_arrive(&u_empty[c % LY::NU]);
+#pragma unroll
+                for (int d = 0; d < NDIR; ++d) {
+                    const int p = (d ? lo1 : lo0) + q;
+                    const int k = kk[d];
+                    const bool live = act && k != 3;
+                    const bool fin = live && (NDIR == 1 || k != 0);
+#pragma unroll
+                    for (int i = 0; i < CPE; ++i) {
+                        const bool ok = i < nch_ok;
+                        const int o = i * L + p;
+                        if (NDIR == 2 && ok && live && k == 0) Wrow[o] = vv[d][i];
+                        if (ok && fin) {
+                            if (OUT == OUT_ACC) aorow[o] = vv[d][i];
+                            else yrow[o] = from_f32<IO>(vv[d][i]);
+                        }
                     }
                 }
             }

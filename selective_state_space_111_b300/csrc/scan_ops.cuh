@@ -17,6 +17,11 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 typedef unsigned long long f2;  // two fp32 in one 64-bit register pair
 
+// compile-time flag passed to generic lambdas (selects a specialised body)
+template <bool V> struct BoolC {
+    static constexpr bool value = V;
+};
+
 __device__ __forceinline__ f2 pk(float a, float b) {
     f2 r;
     asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));

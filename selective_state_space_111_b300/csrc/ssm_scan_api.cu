@@ -30,8 +30,11 @@ ssm_status check_common(ssm_dtype dt, int B, int D, int L, int N) {
     return SSM_OK;
 }
 
-bool io_ok(const void *p) { return p != nullptr && aligned(p, 16); }
-bool opt_io_ok(const void *p) { return p == nullptr || aligned(p, 16); }
+// I/O tensors are read and written element by element, so they need only
+// their element's alignment; the bulk copies read the workspace alone.
+unsigned io_align(ssm_dtype dt) { return dt == SSM_F32 ? 4u : 2u; }
+bool io_ok(ssm_dtype dt, const void *p) { return p != nullptr && aligned(p, io_align(dt)); }
+bool opt_io_ok(ssm_dtype dt, const void *p) { return p == nullptr || aligned(p, io_align(dt)); }
 bool f32_ok(const float *p) { return p != nullptr && aligned(p, 4); }
 bool opt_f32_ok(const float *p) { return p == nullptr || aligned(p, 4); }
 
@@ -110,14 +113,11 @@ ssm_status launch_bidir(const ssm::BiParams &P, cudaStream_t st, bool last = tru
         cudaGetLastError();
         return SSM_ERR_CUDA;
     }
-    // every bulk copy starts at base + a multiple of 16 bytes from these
-    // bases, so they must all be 16-byte aligned (checked, never assumed)
-    for (int d = 0; d < NDIR; ++d) {
-        if (!aligned(P.br[d].dt, 16) || !aligned(P.br[d].u, 16) || !aligned(P.br[d].bc, 16))
-            return SSM_ERR_INVALID_ARG;
-    }
-    if (!aligned(P.z, 16) || !aligned(P.W, 16) || !aligned(P.acc_in, 16))
-        return SSM_ERR_INVALID_ARG;
+    // the packed B/C chunks are bulk copies from base + a multiple of 128
+    // bytes, so their bases must be 16-byte aligned (checked, never assumed);
+    // every other tensor is accessed element by element
+    for (int d = 0; d < NDIR; ++d)
+        if (!aligned(P.br[d].bc, 16)) return SSM_ERR_INVALID_ARG;
     dim3 grid((P.D + G - 1) / G, P.B);
     const bool prof = last && t_prof_begin != nullptr && t_prof_end != nullptr;
     ssm::BiParams Q = P;
@@ -163,8 +163,9 @@ ssm_status bidirectional(ssm_dtype dt, int B, int D, int L, int N, const void *u
                          void *ws, size_t ws_bytes, bool two_sets, cudaStream_t stream) {
     ssm_status s = check_common(dt, B, D, L, N);
     if (s != SSM_OK) return s;
-    if (!io_ok(u) || !opt_io_ok(u_b) || !io_ok(delta) || !io_ok(delta_b) || !io_ok(Bm) ||
-        !io_ok(Cm) || !io_ok(Bm_b) || !io_ok(Cm_b) || !opt_io_ok(z) || !io_ok(y) ||
+    if (!io_ok(dt, u) || !opt_io_ok(dt, u_b) || !io_ok(dt, delta) || !io_ok(dt, delta_b) ||
+        !io_ok(dt, Bm) || !io_ok(dt, Cm) || !io_ok(dt, Bm_b) || !io_ok(dt, Cm_b) ||
+        !opt_io_ok(dt, z) || !io_ok(dt, y) ||
         !f32_ok(A) || !f32_ok(A_b) || !opt_f32_ok(Dskip) || !opt_f32_ok(D_b) ||
         !opt_f32_ok(bias) || !opt_f32_ok(bias_b))
         return SSM_ERR_INVALID_ARG;
@@ -173,15 +174,14 @@ ssm_status bidirectional(ssm_dtype dt, int B, int D, int L, int N, const void *u
     if (ws == nullptr || ws_bytes < lay.total || !aligned(ws, 16)) return SSM_ERR_WORKSPACE;
     char *wsb = (char *)ws;
     ssm::BiParams P{};
-    const long long DL = (long long)D * L, tot = (long long)B * D * L;
-    P.br[0] = {delta, u, (const float *)(wsb + lay.bc0), A, Dskip, bias, 0, DL, tot, 0};
+    const long long DL = (long long)D * L;
+    P.br[0] = {delta, u, (const float *)(wsb + lay.bc0), A, Dskip, bias, 0, DL, 0};
     P.br[1] = {delta_b, u_b ? u_b : u, (const float *)(wsb + lay.bc1), A_b, D_b, bias_b,
-               0, DL, tot, 0};
+               0, DL, 0};
     P.z = z;
     P.y = y;
     P.W = lay.w ? (float *)(wsb + lay.w) : nullptr;
     P.status = (unsigned *)wsb;
-    P.total = (long long)B * D * L;
     P.B = B;
     P.D = D;
     P.L = L;
@@ -234,7 +234,7 @@ ssm_status ss2d_run(int B, int D, int H, int W, int N, const void *x, const void
                     const void *z, const float *bias, int delta_softplus, void *y, char *wsb,
                     const SsWs &lay, cudaStream_t st) {
     const int L = H * W;
-    const long long DL = (long long)D * L, n = (long long)B * D * L;
+    const long long DL = (long long)D * L;
     float *bcK = (float *)(wsb + lay.bc);
     IO *xt = (IO *)(wsb + lay.xt);
     float *r1 = (float *)(wsb + lay.r1), *r2 = (float *)(wsb + lay.r2);
@@ -253,13 +253,11 @@ ssm_status ss2d_run(int B, int D, int H, int W, int N, const void *x, const void
         br.Dskip = Dskip ? Dskip + (long long)k * D : nullptr;
         br.bias = bias ? bias + (long long)k * D : nullptr;
         br.dt_bstride = 4 * DL;
-        br.dt_total = 4 * n;
         br.stream_rev = rev;
         return br;
     };
     ssm::BiParams P{};
     P.status = status;
-    P.total = n;
     P.B = B;
     P.D = D;
     P.L = L;
@@ -329,8 +327,9 @@ ssm_status selective_scan_fwd(ssm_dtype dt, int B, int D, int L, int N, const vo
                               void *workspace, size_t ws_bytes, ssm_stream_t stream) {
     ssm_status s = check_common(dt, B, D, L, N);
     if (s != SSM_OK) return s;
-    if (!io_ok(u) || !io_ok(delta) || !io_ok(Bm) || !io_ok(Cm) || !opt_io_ok(z) ||
-        !io_ok(y) || !f32_ok(A) || !opt_f32_ok(Dskip) || !opt_f32_ok(delta_bias))
+    if (!io_ok(dt, u) || !io_ok(dt, delta) || !io_ok(dt, Bm) || !io_ok(dt, Cm) ||
+        !opt_io_ok(dt, z) || !io_ok(dt, y) || !f32_ok(A) || !opt_f32_ok(Dskip) ||
+        !opt_f32_ok(delta_bias))
         return SSM_ERR_INVALID_ARG;
     if ((long long)B * D * L == 0) return SSM_OK;
     const BiWs lay = bi_ws(1, 1, B, D, L);
@@ -339,13 +338,12 @@ ssm_status selective_scan_fwd(ssm_dtype dt, int B, int D, int L, int N, const vo
     char *wsb = (char *)workspace;
     ssm::BiParams P{};
     P.br[0] = {delta, u, (const float *)(wsb + lay.bc0), A, Dskip, delta_bias, 0,
-               (long long)D * L, (long long)B * D * L, 0};
+               (long long)D * L, 0};
     P.br[1] = P.br[0];
     P.z = z;
     P.y = y;
     P.W = nullptr;
     P.status = (unsigned *)wsb;
-    P.total = (long long)B * D * L;
     P.B = B;
     P.D = D;
     P.L = L;
@@ -413,8 +411,9 @@ ssm_status ss2d_scan_fwd(ssm_dtype dt, int B, int D, int H, int W, int N, int K,
     ssm_status s = check_common(dt, B, D, L, N);
     if (s != SSM_OK) return s;
     if (!fits((long long)K * D * L) || !fits((long long)K * N * L)) return SSM_ERR_UNSUPPORTED;
-    if (!io_ok(x) || !io_ok(delta) || !io_ok(Bm) || !io_ok(Cm) || !opt_io_ok(z) ||
-        !io_ok(y) || !f32_ok(A) || !opt_f32_ok(Dskip) || !opt_f32_ok(delta_bias))
+    if (!io_ok(dt, x) || !io_ok(dt, delta) || !io_ok(dt, Bm) || !io_ok(dt, Cm) ||
+        !opt_io_ok(dt, z) || !io_ok(dt, y) || !f32_ok(A) || !opt_f32_ok(Dskip) ||
+        !opt_f32_ok(delta_bias))
         return SSM_ERR_INVALID_ARG;
     if ((long long)B * D * L == 0) return SSM_OK;
     const SsWs lay = ss2d_ws(dt, B, D, L);

@@ -14,25 +14,27 @@ def to_dev(t):
     return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in t.items()}
 
 
-def run_gpu(spec, t, workspace=None):
+def run_gpu(spec, t, workspace=None, dev=None, out=None):
+    """Runs the library on the host inputs `t` (copied to the GPU), or on
+    the device tensors `dev` when given; `out` is an optional output."""
     import selective_state_space_111_b300 as ssm
 
-    g = to_dev(t)
+    g = to_dev(t) if dev is None else dev
     sp = spec.delta_softplus
+    kw = dict(workspace=workspace, out=out)
     if spec.op == "single":
         return ssm.selective_scan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"],
-                                      g["delta_bias"], sp, workspace=workspace)
+                                      g["delta_bias"], sp, **kw)
     if spec.op == "v1":
         return ssm.bimamba_scan_fwd_v1(g["u"], g["delta"], g["A"], g["A_b"], g["B"], g["C"],
-                                       g["D"], g["z"], g["delta_bias"], sp, g["out_scale"],
-                                       workspace=workspace)
+                                       g["D"], g["z"], g["delta_bias"], sp, g["out_scale"], **kw)
     if spec.op == "v2":
         return ssm.bimamba_scan_fwd_v2(g["u"], g["delta"], g["delta_b"], g["A"], g["A_b"], g["B"],
                                        g["C"], g["B_b"], g["C_b"], g["D"], g["D_b"], g["z"],
                                        g["delta_bias"], g["delta_bias_b"], g["u_b"], sp,
-                                       g["out_scale"], workspace=workspace)
+                                       g["out_scale"], **kw)
     return ssm.ss2d_scan_fwd(g["x"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"],
-                             g["delta_bias"], sp, workspace=workspace)
+                             g["delta_bias"], sp, **kw)
 
 
 def run_oracle(spec, t):

@@ -69,7 +69,8 @@ def test_invalid_arguments_are_rejected_before_launch(lib):
     assert single(lib, L=-1) == 1
     assert single(lib, dt=5) == 1
     assert single(lib, u=None) == 1                 # required pointer
-    assert single(lib, u=FAKE + 2) == 1             # misaligned I/O tensor
+    assert single(lib, u=FAKE + 1) == 1             # bf16 I/O tensor off its 2-byte grid
+    assert single(lib, dt=0, u=FAKE + 2) == 1       # fp32 I/O tensor off its 4-byte grid
     assert single(lib, A=FAKE + 2) == 1             # misaligned fp32 parameter
     assert single(lib, y=None) == 1
 

@@ -114,6 +114,34 @@ def test_length_one_branches_agree():
     assert torch.allclose(y2, ys, rtol=1e-6, atol=1e-6)
 
 
+def _at_offset(v, k):
+    """A contiguous device copy of `v` that starts k elements into a larger
+    buffer (so off every vector boundary for odd k)."""
+    buf = torch.zeros(v.numel() + k, dtype=v.dtype, device="cuda")
+    w = buf[k:].view(v.shape)
+    w.copy_(v)
+    return w
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("op", ["single", "v1", "v2", "ss2d"])
+def test_unaligned_io_tensors(op, io):
+    # every I/O tensor and the output start one element past a 16-byte
+    # boundary; rows of odd length then start anywhere
+    kw = dict(H=7, W=9) if op == "ss2d" else dict(L=101)
+    spec = Spec(op, io, B=2, D=19, perturb=True, out_scale=0.5 if op == "v2" else 1.0, **kw)
+    t = make_inputs(spec, 31)
+    g = {k: (_at_offset(v.cuda(), 1) if isinstance(v, torch.Tensor) else v)
+         for k, v in t.items()}
+    shape = t["x" if op == "ss2d" else "u"].shape
+    out = _at_offset(torch.zeros(shape, dtype=g["delta"].dtype, device="cuda"), 1)
+    y = run_gpu(spec, t, dev=g, out=out)
+    torch.cuda.synchronize()
+    assert y.data_ptr() % 16 != 0 and g["delta"].data_ptr() % 16 != 0
+    err = max_scaled_err(y, run_oracle(spec, t))
+    assert err <= TOL[io], err
+
+
 # ------------------------------------------------------------ the pages' workloads
 def _sampled_rows(spec, seed, nrows):
     """Full-size launch; the oracle recomputes a seeded sample of whole rows."""
