@@ -415,7 +415,8 @@ bidir_scan_kernel(const BiParams P) {
         const IO *ub = (const IO *)br.u + (bD + d0 + r0) * L;
         const int nrow = min(16, D - (d0 + r0));            // valid rows of this warp
         // dt and u of chunk c for this lane's walk step, all 32 loads in
-        // flight together; fetched one chunk ahead of their use
+        // flight together; fetched one chunk ahead of their use (their
+        // latency hides behind this role's wait for a free stage)
         IO xdt[16], xu[16];
         auto fetch = [&](int c) {
             int lo, len;
@@ -462,13 +463,6 @@ bidir_scan_kernel(const BiParams P) {
             chunk_geom(c, d, L, T, lo, len);
             const int j = lane;
             const bool act = j < len;
-            IO cdt[16], cu[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                cdt[i] = xdt[i];
-                cu[i] = xu[i];
-            }
-            if (c + 1 < nch) fetch(c + 1);
             const int su = c % LY::NU;
             if (*abort_flag || !wait(&dw_empty[s2], ((c >> 1) & 1) ^ 1) ||
                 !wait(&u_empty[su], ((c / LY::NU) & 1) ^ 1))
@@ -480,13 +474,14 @@ bidir_scan_kernel(const BiParams P) {
             IO *usl = (IO *)(sm + LY::off_u + su * LY::U_STAGE) + (d * R + r0) * T + j;
             const bool full = len == T && nrow == 16;
             if (P.delta_softplus) {
-                if (full) emit(BoolC<true>(), BoolC<true>(), cdt, cu, dwl, usl, act);
-                else emit(BoolC<true>(), BoolC<false>(), cdt, cu, dwl, usl, act);
+                if (full) emit(BoolC<true>(), BoolC<true>(), xdt, xu, dwl, usl, act);
+                else emit(BoolC<true>(), BoolC<false>(), xdt, xu, dwl, usl, act);
             } else {
-                if (full) emit(BoolC<false>(), BoolC<true>(), cdt, cu, dwl, usl, act);
-                else emit(BoolC<false>(), BoolC<false>(), cdt, cu, dwl, usl, act);
+                if (full) emit(BoolC<false>(), BoolC<true>(), xdt, xu, dwl, usl, act);
+                else emit(BoolC<false>(), BoolC<false>(), xdt, xu, dwl, usl, act);
             }
             mbar_arrive(&dw_full[s2]);
+            if (c + 1 < nch) fetch(c + 1);
         }
     } else {
         // ================================================================ epilogue
@@ -618,53 +613,44 @@ bidir_scan_kernel(const BiParams P) {
                 return fmaf(dsk_tab[d * CPE + i], to_f32(us[row * T + jw]), ypsum(row, jw));
             };
             const int kd = kind(c);
-            float vv[NDIR][CPE];     // the stash value (first arrival) or the output
+            // each item is stored as soon as it is formed (few registers);
+            // the u stage is released after the chunk's last read of it
             if (kd == 0) {
                 // every position is a first arrival (so the chunk is full):
                 // both branches leave their outputs in the stash
-#pragma unroll
-                for (int d = 0; d < NDIR; ++d)
-#pragma unroll
-                    for (int i = 0; i < CPE; ++i) vv[d][i] = own(d, i, d ? T - 1 - q : q);
-                mbar_arrive(&u_empty[c % LY::NU]);
 #pragma unroll
                 for (int d = 0; d < NDIR; ++d) {
                     const int p = (d ? lo1 : lo0) + q;
 #pragma unroll
                     for (int i = 0; i < CPE; ++i)
-                        if (i < nch_ok) Wrow[i * L + p] = vv[d][i];
+                        if (i < nch_ok) Wrow[i * L + p] = own(d, i, d ? T - 1 - q : q);
                 }
+                mbar_arrive(&u_empty[c % LY::NU]);
             } else if (kd == 1) {
                 // every position is finalised here (single direction, or
                 // the other branch's output is in the stash)
                 const bool gate = OUT != OUT_ACC && zrow != nullptr;
+                const bool full = len == T && nch_ok == CPE;
 #pragma unroll
                 for (int d = 0; d < NDIR; ++d) {
                     const int jw = act ? (d ? len - 1 - q : q) : 0;
+                    const int p = (d ? lo1 : lo0) + q;
 #pragma unroll
                     for (int i = 0; i < CPE; ++i) {
                         float v = own(d, i, jw);
                         if (NDIR == 2) v = P.out_scale * (v + wr[d][i]);
                         if (OUT == OUT_ADD_Y) v += ar[d][i];
                         if (gate) v *= silu_f<IO>(to_f32(zr[d][i]));
-                        vv[d][i] = v;
-                    }
-                }
-                mbar_arrive(&u_empty[c % LY::NU]);
-                const bool full = len == T && nch_ok == CPE;
-#pragma unroll
-                for (int d = 0; d < NDIR; ++d) {
-                    const int p = (d ? lo1 : lo0) + q;
-#pragma unroll
-                    for (int i = 0; i < CPE; ++i) {
                         if (full || (act && i < nch_ok)) {
-                            if (OUT == OUT_ACC) aorow[i * L + p] = vv[d][i];
-                            else yrow[i * L + p] = from_f32<IO>(vv[d][i]);
+                            if (OUT == OUT_ACC) aorow[i * L + p] = v;
+                            else yrow[i * L + p] = from_f32<IO>(v);
                         }
                     }
                 }
+                mbar_arrive(&u_empty[c % LY::NU]);
             } else {
                 // the middle of the sequence: classes differ between lanes
+                float vv[NDIR][CPE];     // the stash value (first arrival) or the output
                 int kk[NDIR];
 #pragma unroll
                 for (int d = 0; d < NDIR; ++d) {
