@@ -230,6 +230,17 @@ SSM_API const char *ssm_status_string(ssm_status s);
 SSM_API void ssm_set_profile_events(void *begin, void *end);
 
 /*
+ * Tuning override for the two-branch kernels (v1, v2 and both SS2D passes).
+ * A CTA takes `channels` channels of one batch element, both branches:
+ * 16, or 8 (about half the shared memory, so more CTAs fit an SM).  With 0,
+ * the default, each call picks the one that leaves fewer (branch, channel)
+ * rows on the busiest SM for its B and D -- 8 for small B * D, where CTAs of
+ * 16 channels leave SMs idle.  Applies to later calls on this host thread;
+ * any other value is treated as 0.  Results do not depend on it.
+ */
+SSM_API void ssm_set_cta_channels(int channels);
+
+/*
  * Test hook for the failure path.  The next scan-kernel launch made on this
  * host thread never issues the bulk copy of B/C for chunk `chunk` (>= 0), so
  * the scan's bounded wait for it runs out after about two seconds; the kernel

@@ -44,6 +44,8 @@ _lib.ssm_status_string.restype = ctypes.c_char_p
 _lib.ssm_version.restype = ctypes.c_char_p
 _lib.ssm_test_withhold_copy.argtypes = [_i]
 _lib.ssm_test_withhold_copy.restype = None
+_lib.ssm_set_cta_channels.argtypes = [_i]
+_lib.ssm_set_cta_channels.restype = None
 _lib.ssm_set_profile_events.argtypes = [_vp, _vp]
 _lib.ssm_set_profile_events.restype = None
 for _fn in (_lib.selective_scan_fwd, _lib.bimamba_scan_fwd_v1, _lib.bimamba_scan_fwd_v2,
@@ -127,6 +129,12 @@ def set_profile_events(begin=None, end=None) -> None:
         _lib.ssm_set_profile_events(None, None)
         return
     _lib.ssm_set_profile_events(ctypes.c_void_p(begin.cuda_event), ctypes.c_void_p(end.cuda_event))
+
+
+def set_cta_channels(channels: int = 0) -> None:
+    """Channels per CTA of the two-branch kernels for later calls on this
+    thread: 8, 16, or 0 for the automatic choice."""
+    _lib.ssm_set_cta_channels(int(channels))
 
 
 def get_status(workspace, stream=None) -> int:

@@ -181,7 +181,7 @@ struct WsLayout {
     static constexpr int off_bc = 0;                        // 128-byte aligned
     static constexpr int off_dw = off_bc + NBC * BC_STAGE;
     static constexpr int off_yp = off_dw + 2 * DW_STAGE;
-    static constexpr int NU = 4;                            // u ring (prep -> epilogue)
+    static constexpr int NU = R < 16 ? 2 : 4;               // u ring (prep -> epilogue)
     static constexpr int off_u = off_yp + 2 * YP_STAGE;
     static constexpr int off_bar = (off_u + NU * U_STAGE + 7) & ~7;
     // bc_full[NBC], dw_full[2], dw_empty[2], yp_full[2], yp_empty[2], u_empty[NU]
@@ -192,10 +192,15 @@ struct WsLayout {
 
     static_assert(S == 4 || S == 8 || S == 16, "S must be 4, 8 or 16");
     static_assert((ROWS * LPR) % 32 == 0 && ROWS % 16 == 0, "whole warps per role");
-    static_assert(R % 16 == 0, "each prep warp takes 16 channels of one branch");
-    // registers per thread so that 3 CTAs fit: each of the 4 schedulers of
-    // an SM has its own 16 K registers and holds up to ceil(3 NT / 128) warps
-    static constexpr int WPS = (3 * NT / 32 + 3) / 4;
+    static_assert(R % 16 == 0 || (R == 8 && NDIR == 2),
+                  "a prep warp takes 16 channels of one branch, or 8 of each");
+    // CTAs per SM that the shared memory allows (228 KB per SM, 1 KB
+    // reserved per CTA), and registers per thread so that they all fit:
+    // each of the 4 schedulers of an SM has its own 16 K registers and holds
+    // up to ceil(CPS * NT / 128) warps
+    static constexpr int CPS_SMEM = 233472 / (bytes + 1024);
+    static constexpr int CPS = CPS_SMEM < 64 * 32 / NT ? CPS_SMEM : 64 * 32 / NT;
+    static constexpr int WPS = (CPS * NT / 32 + 3) / 4;
     static constexpr int MAX_REGS = (16384 / (32 * WPS)) / 8 * 8 > 255 ? 255 : (16384 / (32 * WPS)) / 8 * 8;
 };
 
@@ -397,46 +402,67 @@ bidir_scan_kernel(const BiParams P) {
     } else if (warp < NSW + NPW) {
         // ================================================================ prep
         // 16 rows of one branch; lane = walk step j of the chunk
+        // rows pw*16 .. pw*16+15 of the (branch, channel) row space, in NG
+        // groups of GR channels of one branch (NG = 2 when R = 8)
+        constexpr int GR = R < 16 ? R : 16;
+        constexpr int NG = 16 / GR;
         const int pw = warp - NSW;
-        const int d = (pw * 16) / R;
-        const int r0 = (pw * 16) % R;
-        const BiBranch &br = P.br[d];
-        const bool srev = br.stream_rev != 0;
+        int gd[NG], gn[NG];
+        bool gsrev[NG];
+        const IO *gdt[NG], *gu[NG];
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+            const int row = pw * 16 + g * GR;
+            const int d = row / R, r0 = row % R;
+            const BiBranch &br = P.br[d];
+            gd[g] = d;
+            gsrev[g] = br.stream_rev != 0;
+            gn[g] = min(GR, D - (d0 + r0));                  // valid channels
+            // first row of the group in dt and u; row i is i * L further on
+            // (offsets within the rows stay below D * L < 2^31)
+            gdt[g] = (const IO *)br.dt + br.dt_off + b * br.dt_bstride + (long long)(d0 + r0) * L;
+            gu[g] = (const IO *)br.u + (bD + d0 + r0) * L;
+        }
         // this warp's 16 biases in shared memory
         float *bias_tab = (float *)(sm + LY::off_tab) + LY::ROWS + pw * 16;
         if (lane < 16) {
-            const int ch = d0 + r0 + lane;
-            bias_tab[lane] = (ch < D && br.bias) ? br.bias[ch] : 0.f;
+            const int row = pw * 16 + lane;
+            const int d = row / R, ch = d0 + row % R;
+            bias_tab[lane] = (ch < D && P.br[d].bias) ? P.br[d].bias[ch] : 0.f;
         }
         __syncwarp();
-        // first row of this warp in dt and u; row i is i * L further on
-        // (offsets within the rows stay below D * L < 2^31)
-        const IO *dtb = (const IO *)br.dt + br.dt_off + b * br.dt_bstride + (long long)(d0 + r0) * L;
-        const IO *ub = (const IO *)br.u + (bD + d0 + r0) * L;
-        const int nrow = min(16, D - (d0 + r0));            // valid rows of this warp
+        bool all_rows = true;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) all_rows = all_rows && gn[g] == GR;
         // dt and u of chunk c for this lane's walk step, all 32 loads in
         // flight together; fetched one chunk ahead of their use (their
         // latency hides behind this role's wait for a free stage)
         IO xdt[16], xu[16];
         auto fetch = [&](int c) {
-            int lo, len;
-            chunk_geom(c, d, L, T, lo, len);
             const int j = lane;
-            const int p = d ? lo + len - 1 - j : lo + j;        // position of walk step j
-            const int si = srev ? c * T + j : p;                // dt stream index
-            if (len == T && nrow == 16) {
+            int p[NG], si[NG], len = 0;
+#pragma unroll
+            for (int g = 0; g < NG; ++g) {
+                int lo;
+                chunk_geom(c, gd[g], L, T, lo, len);
+                p[g] = gd[g] ? lo + len - 1 - j : lo + j;        // position of walk step j
+                si[g] = gsrev[g] ? c * T + j : p[g];              // dt stream index
+            }
+            if (len == T && all_rows) {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    xdt[i] = __ldg(dtb + (i * L + si));
-                    xu[i] = __ldg(ub + (i * L + p));
+                    const int g = i / GR, ii = i % GR;
+                    xdt[i] = __ldg(gdt[g] + (ii * L + si[g]));
+                    xu[i] = __ldg(gu[g] + (ii * L + p[g]));
                 }
             } else {
                 const bool act = j < len;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const bool ok = act && i < nrow;
-                    xdt[i] = ok ? __ldg(dtb + (i * L + si)) : from_f32<IO>(0.f);
-                    xu[i] = ok ? __ldg(ub + (i * L + p)) : from_f32<IO>(0.f);
+                    const int g = i / GR, ii = i % GR;
+                    const bool ok = act && ii < gn[g];
+                    xdt[i] = ok ? __ldg(gdt[g] + (ii * L + si[g])) : from_f32<IO>(0.f);
+                    xu[i] = ok ? __ldg(gu[g] + (ii * L + p[g])) : from_f32<IO>(0.f);
                 }
             }
         };
@@ -448,7 +474,7 @@ bidir_scan_kernel(const BiParams P) {
             for (int i = 0; i < 16; ++i) {
                 const float x = to_f32(cdt[i]) + bias_tab[i];
                 float dl = decltype(SP)::value ? softplus_f<IO>(x) : x;
-                if (!decltype(FULL)::value) dl = i < nrow ? dl : 0.f;
+                if (!decltype(FULL)::value) dl = (i % GR) < gn[i / GR] ? dl : 0.f;
                 const float w = dl * to_f32(cu[i]);
                 if (decltype(FULL)::value || act) {
                     dwl[i * (LY::DW_ROW / 16)] = make_float4(dl, dl, w, w);
@@ -460,7 +486,7 @@ bidir_scan_kernel(const BiParams P) {
         for (int c = 0; c < nch; ++c) {
             const int s2 = c & 1;
             int lo, len;
-            chunk_geom(c, d, L, T, lo, len);
+            chunk_geom(c, 0, L, T, lo, len);
             const int j = lane;
             const bool act = j < len;
             const int su = c % LY::NU;
@@ -470,9 +496,9 @@ bidir_scan_kernel(const BiParams P) {
             // shared-memory stores only: they cannot alias the global loads
             // in flight, so each row is computed and stored in turn
             float4 *dwl = (float4 *)(sm + LY::off_dw + s2 * LY::DW_STAGE) +
-                          (d * R + r0) * (LY::DW_ROW / 16) + j;
-            IO *usl = (IO *)(sm + LY::off_u + su * LY::U_STAGE) + (d * R + r0) * T + j;
-            const bool full = len == T && nrow == 16;
+                          (pw * 16) * (LY::DW_ROW / 16) + j;
+            IO *usl = (IO *)(sm + LY::off_u + su * LY::U_STAGE) + (pw * 16) * T + j;
+            const bool full = len == T && all_rows;
             if (P.delta_softplus) {
                 if (full) emit(BoolC<true>(), BoolC<true>(), xdt, xu, dwl, usl, act);
                 else emit(BoolC<true>(), BoolC<false>(), xdt, xu, dwl, usl, act);

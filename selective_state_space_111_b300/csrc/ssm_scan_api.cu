@@ -95,6 +95,8 @@ ssm_status launch_pack(const void *Bm, const void *Cm, float *out, int B, int N,
 // Profiling hook (ssm_set_profile_events): events recorded around the last
 // scan-kernel launch of each call made on this host thread.
 thread_local cudaEvent_t t_prof_begin = nullptr, t_prof_end = nullptr;
+// Override of the two-branch CTA shape (ssm_set_cta_channels): 0, 8 or 16.
+thread_local int t_cta_channels = 0;
 // Test hook (ssm_test_withhold_copy): chunk whose B/C copy the next call on
 // this host thread withholds, to exercise the bounded waits.
 thread_local int t_withhold = -1;
@@ -136,6 +138,38 @@ ssm_status launch_bidir(const ssm::BiParams &P, cudaStream_t st, bool last = tru
     return SSM_OK;
 }
 
+// Channels per CTA of the two-branch kernel: 16, or 8 when that leaves
+// fewer (branch, channel) rows on the busiest SM -- small B * D, where CTAs
+// of 16 channels leave SMs idle.  An SM holds LY::CPS CTAs at a time; a
+// busier SM runs them in waves.
+template <typename IO, int G>
+long long busiest_sm_rows(int B, int D, int nsm) {
+    constexpr int cps = ssm::WsLayout<IO, kBiS, 2, G>::CPS;
+    const long long ctas = (long long)((D + G - 1) / G) * B;
+    const long long per = (ctas + nsm - 1) / nsm;
+    const long long slots = per <= cps ? per : (per + cps - 1) / cps * cps;
+    return slots * G;
+}
+template <typename IO>
+bool narrow_ctas(int B, int D) {
+    int dev = 0, nsm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        nsm <= 0) {
+        cudaGetLastError();
+        return false;
+    }
+    return busiest_sm_rows<IO, 8>(B, D, nsm) < busiest_sm_rows<IO, kBiG2>(B, D, nsm);
+}
+template <typename IO, int OUT = ssm::OUT_Y>
+ssm_status launch_two_branch(const ssm::BiParams &P, cudaStream_t st, bool last = true) {
+    const bool narrow = t_cta_channels == 8 ? true
+                        : t_cta_channels == 16 ? false
+                                               : narrow_ctas<IO>(P.B, P.D);
+    if (narrow) return launch_bidir<IO, kBiS, 2, 8, OUT>(P, st, last);
+    return launch_bidir<IO, kBiS, 2, kBiG2, OUT>(P, st, last);
+}
+
 // Packs B/C (one or two sets), then runs the scan kernel.
 template <typename IO, int NDIR>
 ssm_status run_bidir(ssm::BiParams P, const void *Bm, const void *Cm, const void *Bm_b,
@@ -148,7 +182,7 @@ ssm_status run_bidir(ssm::BiParams P, const void *Bm, const void *Cm, const void
                             nullptr, st);
         if (s != SSM_OK) return s;
     }
-    if (NDIR == 2) return launch_bidir<IO, kBiS, 2, kBiG2>(P, st);
+    if (NDIR == 2) return launch_two_branch<IO>(P, st);
     return launch_bidir<IO, kBiS, 1, kBiG1>(P, st);
 }
 
@@ -270,7 +304,7 @@ ssm_status ss2d_run(int B, int D, int H, int W, int N, const void *x, const void
     P.br[1] = branch(3, xt, 1);
     P.W = r1;
     P.acc_out = r2;
-    s = launch_bidir<IO, kBiS, 2, kBiG2, ssm::OUT_ACC>(P, st, false);
+    s = launch_two_branch<IO, ssm::OUT_ACC>(P, st, false);
     if (s != SSM_OK) return s;
     // Wa (R1) = Wt (R2) transposed back to H x W
     s = launch_transpose<float>(r2, r1, B * D, W, H, st);
@@ -283,7 +317,7 @@ ssm_status ss2d_run(int B, int D, int H, int W, int N, const void *x, const void
     P.W = r2;
     P.acc_in = r1;
     P.acc_out = nullptr;
-    return launch_bidir<IO, kBiS, 2, kBiG2, ssm::OUT_ADD_Y>(P, st);
+    return launch_two_branch<IO, ssm::OUT_ADD_Y>(P, st);
 }
 
 // ---- fixed scratch of the allocation-free entry point
@@ -474,6 +508,10 @@ const char *ssm_status_string(ssm_status s) {
 }
 
 void ssm_test_withhold_copy(int chunk) { t_withhold = chunk; }
+
+void ssm_set_cta_channels(int channels) {
+    t_cta_channels = (channels == 8 || channels == 16) ? channels : 0;
+}
 
 void ssm_set_profile_events(void *begin, void *end) {
     t_prof_begin = (cudaEvent_t)begin;

@@ -44,9 +44,18 @@ def test_single(io, shape):
     check(Spec("single", io, B=B, D=D, L=L, N=N, perturb=True), 1000 + L)
 
 
+@pytest.fixture(params=[8, 16], ids=["cta8", "cta16"])
+def cta(request):
+    """Both CTA shapes of the two-branch kernels (8 or 16 channels)."""
+    import selective_state_space_111_b300 as ssm
+    ssm.set_cta_channels(request.param)
+    yield request.param
+    ssm.set_cta_channels(0)
+
+
 @pytest.mark.parametrize("io", ["f32", "bf16"])
 @pytest.mark.parametrize("shape", SHAPES)
-def test_v1(io, shape):
+def test_v1(io, shape, cta):
     B, D, L, N = shape
     check(Spec("v1", io, B=B, D=D, L=L, N=N, perturb=True, a_b_noise=0.1, out_scale=1.0), 2000 + L)
 
@@ -54,7 +63,7 @@ def test_v1(io, shape):
 @pytest.mark.parametrize("io", ["f32", "bf16"])
 @pytest.mark.parametrize("shape", SHAPES)
 @pytest.mark.parametrize("shared_u", [True, False])
-def test_v2(io, shape, shared_u):
+def test_v2(io, shape, shared_u, cta):
     B, D, L, N = shape
     check(Spec("v2", io, B=B, D=D, L=L, N=N, perturb=True, shared_u=shared_u, out_scale=0.5),
           3000 + L)
@@ -66,7 +75,7 @@ SS2D_SHAPES = [(1, 1, 1, 1), (1, 2, 2, 3), (2, 3, 5, 7), (1, 17, 8, 8), (2, 5, 3
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
 @pytest.mark.parametrize("shape", SS2D_SHAPES)
-def test_ss2d(io, shape):
+def test_ss2d(io, shape, cta):
     B, D, H, W = shape
     check(Spec("ss2d", io, B=B, D=D, H=H, W=W, perturb=True), 4000 + H * W)
 
@@ -101,6 +110,23 @@ def test_deterministic_and_workspace_contents_irrelevant():
     assert torch.equal(y1, y2)
 
 
+@pytest.mark.parametrize("op", ["v1", "v2", "ss2d"])
+def test_cta_shape_does_not_change_results(op):
+    # the two CTA shapes run the same arithmetic per row: identical bits
+    import selective_state_space_111_b300 as ssm
+    kw = dict(H=9, W=13) if op == "ss2d" else dict(L=300)
+    spec = Spec(op, "bf16", B=3, D=40, perturb=True, out_scale=0.5 if op == "v2" else 1.0, **kw)
+    t = make_inputs(spec, 12)
+    try:
+        ssm.set_cta_channels(8)
+        y8 = run_gpu(spec, t)
+        ssm.set_cta_channels(16)
+        y16 = run_gpu(spec, t)
+    finally:
+        ssm.set_cta_channels(0)
+    assert torch.equal(y8, y16)
+
+
 def test_length_one_branches_agree():
     # With L = 1 and identical parameter sets the two branches coincide, so
     # v2 with out_scale 0.5 equals the single-direction scan.
@@ -125,7 +151,7 @@ def _at_offset(v, k):
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
 @pytest.mark.parametrize("op", ["single", "v1", "v2", "ss2d"])
-def test_unaligned_io_tensors(op, io):
+def test_unaligned_io_tensors(op, io, cta):
     # every I/O tensor and the output start one element past a 16-byte
     # boundary; rows of odd length then start anywhere
     kw = dict(H=7, W=9) if op == "ss2d" else dict(L=101)
