@@ -19,7 +19,18 @@ Functions mirror the C ABI's operations:
   ss2d(x, delta, A, B, C, D=None, z=None, delta_bias=None,
        delta_softplus=True)                                           -> y
   cross_scan_index(H, W, k)                   -> int64 array of length H*W
-Shapes are the ones documented in ``ssm_oracle.c``.
+and the backward pass of each form (gradients of sum(g * out) for the
+incoming output gradient g), returning a dict of gradient arrays:
+  selective_scan_bwd(g, ...same inputs...)    -> du, ddelta, dA, dB, dC, dD, dz, ddelta_bias
+  bimamba_v1_bwd(g, ...)                      -> du, ddelta, dA, dA_b, dB, dC, dD, dz,
+                                                 ddelta_bias
+  bimamba_v2_bwd(g, ...)                      -> du, (du_b), ddelta, ddelta_b, dA, dA_b,
+                                                 dB, dC, dB_b, dC_b, dD, dD_b, dz,
+                                                 ddelta_bias, ddelta_bias_b
+  ss2d_bwd(g, ...)                            -> dx, ddelta, dA, dB, dC, dD, dz,
+                                                 ddelta_bias
+Shapes are the ones documented in ``ssm_oracle.c``; a gradient has its
+input's shape.
 """
 from __future__ import annotations
 
@@ -60,10 +71,17 @@ def _load():
             lib.oracle_bimamba_v1.argtypes = [i, i, i, i] + [_dp] * 9 + [i, d, _dp]
             lib.oracle_bimamba_v2.argtypes = [i, i, i, i] + [_dp] * 15 + [i, d, _dp]
             lib.oracle_ss2d.argtypes = [i, i, i, i, i, i] + [_dp] * 8 + [i, _dp]
+            lib.oracle_selective_scan_bwd.argtypes = [i, i, i, i] + [_dp] * 8 + [i] + [_dp] * 9
+            lib.oracle_bimamba_v1_bwd.argtypes = [i, i, i, i] + [_dp] * 9 + [i, d] + [_dp] * 10
+            lib.oracle_bimamba_v2_bwd.argtypes = ([i, i, i, i] + [_dp] * 15 + [i, d] +
+                                                  [_dp] * 16)
+            lib.oracle_ss2d_bwd.argtypes = [i, i, i, i, i, i] + [_dp] * 8 + [i] + [_dp] * 9
             lib.oracle_cross_scan_index.argtypes = [i, i, i, ctypes.c_long]
             lib.oracle_cross_scan_index.restype = ctypes.c_long
             for f in (lib.oracle_selective_scan, lib.oracle_bimamba_v1,
-                      lib.oracle_bimamba_v2, lib.oracle_ss2d):
+                      lib.oracle_bimamba_v2, lib.oracle_ss2d, lib.oracle_selective_scan_bwd,
+                      lib.oracle_bimamba_v1_bwd, lib.oracle_bimamba_v2_bwd,
+                      lib.oracle_ss2d_bwd):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -162,3 +180,92 @@ def cross_scan_index(H, W, k):
     if (out < 0).any():
         raise ValueError("bad cross-scan arguments")
     return out
+
+
+# ---------------------------------------------------------------- backward
+def _out(shape, present=True):
+    return np.empty(shape, np.float64) if present else None
+
+
+def selective_scan_bwd(g, u, delta, A, B, C, D=None, z=None, delta_bias=None,
+                       delta_softplus=True):
+    u = _f64(u)
+    Bn, Dn, L = u.shape
+    N = np.shape(A)[1]
+    a = [u, _f64(delta, (Bn, Dn, L)), _f64(A, (Dn, N)), _f64(B, (Bn, N, L)),
+         _f64(C, (Bn, N, L)), _f64(D, (Dn,)), _f64(z, (Bn, Dn, L)),
+         _f64(delta_bias, (Dn,))]
+    r = {"du": _out((Bn, Dn, L)), "ddelta": _out((Bn, Dn, L)), "dA": _out((Dn, N)),
+         "dB": _out((Bn, N, L)), "dC": _out((Bn, N, L)), "dD": _out((Dn,), D is not None),
+         "dz": _out((Bn, Dn, L), z is not None),
+         "ddelta_bias": _out((Dn,), delta_bias is not None)}
+    _check(_load().oracle_selective_scan_bwd(
+        Bn, Dn, L, N, *map(_ptr, a), int(bool(delta_softplus)), _ptr(_f64(g, (Bn, Dn, L))),
+        *[_ptr(r[k]) for k in ("du", "ddelta", "dA", "dB", "dC", "dD", "dz", "ddelta_bias")]),
+        "selective_scan_bwd")
+    return {k: v for k, v in r.items() if v is not None}
+
+
+def bimamba_v1_bwd(g, u, delta, A, A_b, B, C, D=None, z=None, delta_bias=None,
+                   delta_softplus=True, out_scale=1.0):
+    u = _f64(u)
+    Bn, Dn, L = u.shape
+    N = np.shape(A)[1]
+    a = [u, _f64(delta, (Bn, Dn, L)), _f64(A, (Dn, N)), _f64(A_b, (Dn, N)),
+         _f64(B, (Bn, N, L)), _f64(C, (Bn, N, L)), _f64(D, (Dn,)),
+         _f64(z, (Bn, Dn, L)), _f64(delta_bias, (Dn,))]
+    keys = ("du", "ddelta", "dA", "dA_b", "dB", "dC", "dD", "dz", "ddelta_bias")
+    r = {"du": _out((Bn, Dn, L)), "ddelta": _out((Bn, Dn, L)), "dA": _out((Dn, N)),
+         "dA_b": _out((Dn, N)), "dB": _out((Bn, N, L)), "dC": _out((Bn, N, L)),
+         "dD": _out((Dn,), D is not None), "dz": _out((Bn, Dn, L), z is not None),
+         "ddelta_bias": _out((Dn,), delta_bias is not None)}
+    _check(_load().oracle_bimamba_v1_bwd(
+        Bn, Dn, L, N, *map(_ptr, a), int(bool(delta_softplus)), float(out_scale),
+        _ptr(_f64(g, (Bn, Dn, L))), *[_ptr(r[k]) for k in keys]), "bimamba_v1_bwd")
+    return {k: v for k, v in r.items() if v is not None}
+
+
+def bimamba_v2_bwd(g, u, delta, delta_b, A, A_b, B, C, B_b, C_b, D=None, D_b=None,
+                   z=None, delta_bias=None, delta_bias_b=None, u_b=None,
+                   delta_softplus=True, out_scale=0.5):
+    u = _f64(u)
+    Bn, Dn, L = u.shape
+    N = np.shape(A)[1]
+    a = [u, _f64(u_b, (Bn, Dn, L)), _f64(delta, (Bn, Dn, L)),
+         _f64(delta_b, (Bn, Dn, L)), _f64(A, (Dn, N)), _f64(A_b, (Dn, N)),
+         _f64(B, (Bn, N, L)), _f64(C, (Bn, N, L)), _f64(B_b, (Bn, N, L)),
+         _f64(C_b, (Bn, N, L)), _f64(D, (Dn,)), _f64(D_b, (Dn,)),
+         _f64(z, (Bn, Dn, L)), _f64(delta_bias, (Dn,)), _f64(delta_bias_b, (Dn,))]
+    keys = ("du", "du_b", "ddelta", "ddelta_b", "dA", "dA_b", "dB", "dC", "dB_b", "dC_b",
+            "dD", "dD_b", "dz", "ddelta_bias", "ddelta_bias_b")
+    sh, shn = (Bn, Dn, L), (Bn, N, L)
+    r = {"du": _out(sh), "du_b": _out(sh, u_b is not None), "ddelta": _out(sh),
+         "ddelta_b": _out(sh), "dA": _out((Dn, N)), "dA_b": _out((Dn, N)),
+         "dB": _out(shn), "dC": _out(shn), "dB_b": _out(shn), "dC_b": _out(shn),
+         "dD": _out((Dn,), D is not None), "dD_b": _out((Dn,), D_b is not None),
+         "dz": _out(sh, z is not None), "ddelta_bias": _out((Dn,), delta_bias is not None),
+         "ddelta_bias_b": _out((Dn,), delta_bias_b is not None)}
+    _check(_load().oracle_bimamba_v2_bwd(
+        Bn, Dn, L, N, *map(_ptr, a), int(bool(delta_softplus)), float(out_scale),
+        _ptr(_f64(g, sh)), *[_ptr(r[k]) for k in keys]), "bimamba_v2_bwd")
+    return {k: v for k, v in r.items() if v is not None}
+
+
+def ss2d_bwd(g, x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True):
+    x = _f64(x)
+    Bn, Dn, H, W = x.shape
+    K = 4
+    L = H * W
+    N = np.shape(A)[2]
+    a = [x, _f64(delta, (Bn, K, Dn, L)), _f64(A, (K, Dn, N)),
+         _f64(B, (Bn, K, N, L)), _f64(C, (Bn, K, N, L)), _f64(D, (K, Dn)),
+         _f64(z, (Bn, Dn, H, W)), _f64(delta_bias, (K, Dn))]
+    keys = ("dx", "ddelta", "dA", "dB", "dC", "dD", "dz", "ddelta_bias")
+    r = {"dx": _out((Bn, Dn, H, W)), "ddelta": _out((Bn, K, Dn, L)), "dA": _out((K, Dn, N)),
+         "dB": _out((Bn, K, N, L)), "dC": _out((Bn, K, N, L)),
+         "dD": _out((K, Dn), D is not None), "dz": _out((Bn, Dn, H, W), z is not None),
+         "ddelta_bias": _out((K, Dn), delta_bias is not None)}
+    _check(_load().oracle_ss2d_bwd(
+        Bn, Dn, H, W, N, K, *map(_ptr, a), int(bool(delta_softplus)),
+        _ptr(_f64(g, (Bn, Dn, H, W))), *[_ptr(r[k]) for k in keys]), "ss2d_bwd")
+    return {k: v for k, v in r.items() if v is not None}

@@ -335,3 +335,475 @@ done:
     free(acc);
     return rc;
 }
+
+/* ======================================================================
+ * Backward pass (gradients), fp64.
+ *
+ * For a loss  sum_t g[t] * out[t]  (g = the incoming gradient of the
+ * output), the gradients of every input follow from the chain rule applied
+ * to the forward steps above, in reverse order.  Per direction, with
+ * a_t[n] = exp(delta_t * A[n]) and G_t[n] = dLoss/dh_t[n]:
+ *   G_t      = gy_t * C_t + a_{t+1} * G_{t+1}          (G_L = 0)
+ *   dC_t     = gy_t * h_t            dD += gy_t * u_t
+ *   dB_t     = G_t * delta_t * u_t   du_t = gy_t * D + sum_n G_t delta_t B_t
+ *   dA      += G_t * h_{t-1} * a_t * delta_t
+ *   ddelta_t = sum_n G_t * (h_{t-1} * a_t * A + B_t * u_t)
+ *   ddt_t    = ddelta_t * sigmoid(dt_t + bias)   (softplus'; or ddelta_t)
+ *   dbias   += ddt_t
+ * and the gate out = y * silu(z) gives gy = g * silu(z),
+ * dz = g * y * silu'(z) with silu'(z) = s (1 + z (1 - s)), s = sigmoid(z).
+ * Bidirectional and SS2D compose exactly as their forward passes do: the
+ * backward branch / direction k runs on the same flipped or cross-scanned
+ * copies, and its sequence gradients are flipped or scattered back.
+ * All gradient outputs are overwritten (zeroed first); NULL outputs are
+ * skipped.  Parameter gradients (dA, dD, dbias, and dB/dC over channels)
+ * are summed over every row that uses the parameter.
+ * ====================================================================== */
+
+static double sigmoid(double x)
+{
+    if (x >= 0.0)
+        return 1.0 / (1.0 + exp(-x));
+    double e = exp(x);
+    return e / (1.0 + e);
+}
+
+/* derivative of silu(z) = z * sigmoid(z) */
+static double dsilu(double z)
+{
+    double s = sigmoid(z);
+    return s * (1.0 + z * (1.0 - s));
+}
+
+static void zero(double *p, size_t n)
+{
+    if (p)
+        memset(p, 0, sizeof(double) * n);
+}
+
+/*
+ * Gradients of one direction over one sequence (arguments as scan_sequence;
+ * gy = dLoss/dy before any gate).  Accumulates into du[L], ddt[L], dA[N],
+ * dBm[N][L], dCm[N][L], *dD and *dbias.  hs: scratch of (L+1)*N doubles for
+ * h_{-1} = 0, h_0 .. h_{L-1}; G: scratch of N doubles.
+ */
+static void scan_sequence_bwd(int L, int N, const double *u, const double *dt,
+                              const double *A, const double *Bm, const double *Cm,
+                              double Dd, double bias, int delta_softplus,
+                              const double *gy, double *du, double *ddt, double *dA,
+                              double *dBm, double *dCm, double *dD, double *dbias,
+                              double *hs, double *G)
+{
+    /* forward, keeping every state */
+    for (int n = 0; n < N; ++n)
+        hs[n] = 0.0;
+    for (int t = 0; t < L; ++t) {
+        double delta = dt[t] + bias;
+        if (delta_softplus)
+            delta = softplus(delta);
+        for (int n = 0; n < N; ++n)
+            hs[(size_t)(t + 1) * N + n] =
+                exp(delta * A[n]) * hs[(size_t)t * N + n] +
+                delta * Bm[(size_t)n * L + t] * u[t];
+    }
+    /* reverse sweep; G[n] holds a_{t+1} * G_{t+1} on entry to step t */
+    for (int n = 0; n < N; ++n)
+        G[n] = 0.0;
+    for (int t = L - 1; t >= 0; --t) {
+        double x = dt[t] + bias;
+        double delta = delta_softplus ? softplus(x) : x;
+        *dD += gy[t] * u[t];
+        du[t] += gy[t] * Dd;
+        double ddelta = 0.0;
+        for (int n = 0; n < N; ++n) {
+            double a = exp(delta * A[n]);
+            double ht = hs[(size_t)(t + 1) * N + n];
+            double hp = hs[(size_t)t * N + n];
+            double b = Bm[(size_t)n * L + t];
+            double g = gy[t] * Cm[(size_t)n * L + t] + G[n];
+            dCm[(size_t)n * L + t] += gy[t] * ht;
+            dBm[(size_t)n * L + t] += g * delta * u[t];
+            du[t] += g * delta * b;
+            dA[n] += g * hp * a * delta;
+            ddelta += g * (hp * a * A[n] + b * u[t]);
+            G[n] = a * g;
+        }
+        double dx = delta_softplus ? ddelta * sigmoid(x) : ddelta;
+        ddt[t] += dx;
+        *dbias += dx;
+    }
+}
+
+/* Gate backward for one sequence: gy = g * silu(z), dz = g * y * silu'(z)
+ * (z == NULL: gy = g). */
+static void gate_bwd(int L, const double *g, const double *y, const double *z,
+                     double *gy, double *dz)
+{
+    for (int t = 0; t < L; ++t) {
+        if (z) {
+            gy[t] = g[t] * (z[t] / (1.0 + exp(-z[t])));
+            if (dz)
+                dz[t] = g[t] * y[t] * dsilu(z[t]);
+        } else {
+            gy[t] = g[t];
+        }
+    }
+}
+
+int oracle_selective_scan_bwd(int B, int D, int L, int N,
+                              const double *u, const double *delta,
+                              const double *A, const double *Bm, const double *Cm,
+                              const double *Dskip, const double *z,
+                              const double *delta_bias, int delta_softplus,
+                              const double *gout,
+                              double *du, double *ddelta, double *dA, double *dBm,
+                              double *dCm, double *dD, double *dz, double *dbias)
+{
+    if (B < 0 || D < 0 || L < 0 || N <= 0 || !u || !delta || !A || !Bm || !Cm ||
+        !gout || !du || !ddelta || !dA || !dBm || !dCm)
+        return -1;
+    size_t Ls = (size_t)(L > 0 ? L : 1);
+    double *h = (double *)malloc(sizeof(double) * (size_t)N);
+    double *G = (double *)malloc(sizeof(double) * (size_t)N);
+    double *hs = (double *)malloc(sizeof(double) * (Ls + 1) * (size_t)N);
+    double *y = (double *)malloc(sizeof(double) * Ls);
+    double *gy = (double *)malloc(sizeof(double) * Ls);
+    int rc = 0;
+    if (!h || !G || !hs || !y || !gy) {
+        rc = -1;
+        goto done;
+    }
+    zero(du, (size_t)B * D * L);
+    zero(ddelta, (size_t)B * D * L);
+    zero(dA, (size_t)D * N);
+    zero(dBm, (size_t)B * N * L);
+    zero(dCm, (size_t)B * N * L);
+    zero(dD, (size_t)D);
+    zero(dz, (size_t)B * D * L);
+    zero(dbias, (size_t)D);
+    for (int b = 0; b < B; ++b) {
+        for (int d = 0; d < D; ++d) {
+            size_t row = ((size_t)b * D + d) * (size_t)L;
+            double Dd = Dskip ? Dskip[d] : 0.0, bias = delta_bias ? delta_bias[d] : 0.0;
+            double sD = 0.0, sb = 0.0;
+            scan_sequence(L, N, u + row, delta + row, A + (size_t)d * N,
+                          Bm + (size_t)b * N * L, Cm + (size_t)b * N * L, Dd, bias,
+                          delta_softplus, y, h);
+            gate_bwd(L, gout + row, y, z ? z + row : NULL, gy, dz ? dz + row : NULL);
+            scan_sequence_bwd(L, N, u + row, delta + row, A + (size_t)d * N,
+                              Bm + (size_t)b * N * L, Cm + (size_t)b * N * L, Dd, bias,
+                              delta_softplus, gy, du + row, ddelta + row,
+                              dA + (size_t)d * N, dBm + (size_t)b * N * L,
+                              dCm + (size_t)b * N * L, &sD, &sb, hs, G);
+            if (dD)
+                dD[d] += sD;
+            if (dbias)
+                dbias[d] += sb;
+        }
+    }
+done:
+    free(h);
+    free(G);
+    free(hs);
+    free(y);
+    free(gy);
+    return rc;
+}
+
+/*
+ * Bidirectional backward, general form (v1 and v2).  Outputs of the
+ * backward branch's set (du_b, ddelta_b, dA_b, dBm_b, dCm_b, dD_b,
+ * dbias_b) may alias the forward set's arrays when the parameter is shared
+ * (v1; v2 with a shared u): the two branches' gradients are then summed.
+ */
+static int bidirectional_bwd(int B, int D, int L, int N,
+                             const double *u, const double *u_b,
+                             const double *delta, const double *delta_b,
+                             const double *A, const double *A_b,
+                             const double *Bm, const double *Cm,
+                             const double *Bm_b, const double *Cm_b,
+                             const double *Dskip, const double *D_b,
+                             const double *z, const double *bias,
+                             const double *bias_b, int delta_softplus,
+                             double out_scale, const double *gout,
+                             double *du, double *du_b, double *ddelta, double *ddelta_b,
+                             double *dA, double *dA_b, double *dBm, double *dCm,
+                             double *dBm_b, double *dCm_b, double *dD, double *dD_b,
+                             double *dz, double *dbias, double *dbias_b)
+{
+    size_t Ls = (size_t)(L > 0 ? L : 1);
+    size_t NL = (size_t)N * Ls;
+    double *h = (double *)malloc(sizeof(double) * (size_t)N);
+    double *G = (double *)malloc(sizeof(double) * (size_t)N);
+    double *hs = (double *)malloc(sizeof(double) * (Ls + 1) * (size_t)N);
+    double *yf = (double *)malloc(sizeof(double) * Ls);
+    double *yb = (double *)malloc(sizeof(double) * Ls);
+    double *yv = (double *)malloc(sizeof(double) * Ls);
+    double *gy = (double *)malloc(sizeof(double) * Ls);
+    double *gf = (double *)malloc(sizeof(double) * Ls);
+    double *gb = (double *)malloc(sizeof(double) * Ls);
+    double *uf = (double *)malloc(sizeof(double) * Ls);
+    double *df = (double *)malloc(sizeof(double) * Ls);
+    double *Bf = (double *)malloc(sizeof(double) * NL);
+    double *Cf = (double *)malloc(sizeof(double) * NL);
+    double *duf = (double *)malloc(sizeof(double) * Ls);
+    double *ddf = (double *)malloc(sizeof(double) * Ls);
+    double *dBf = (double *)malloc(sizeof(double) * NL);
+    double *dCf = (double *)malloc(sizeof(double) * NL);
+    int rc = 0;
+    if (!h || !G || !hs || !yf || !yb || !yv || !gy || !gf || !gb || !uf || !df || !Bf ||
+        !Cf || !duf || !ddf || !dBf || !dCf) {
+        rc = -1;
+        goto done;
+    }
+    /* zero every distinct output once (aliases are zeroed twice: harmless) */
+    zero(du, (size_t)B * D * L);
+    zero(du_b, (size_t)B * D * L);
+    zero(ddelta, (size_t)B * D * L);
+    zero(ddelta_b, (size_t)B * D * L);
+    zero(dA, (size_t)D * N);
+    zero(dA_b, (size_t)D * N);
+    zero(dBm, (size_t)B * N * L);
+    zero(dCm, (size_t)B * N * L);
+    zero(dBm_b, (size_t)B * N * L);
+    zero(dCm_b, (size_t)B * N * L);
+    zero(dD, (size_t)D);
+    zero(dD_b, (size_t)D);
+    zero(dz, (size_t)B * D * L);
+    zero(dbias, (size_t)D);
+    zero(dbias_b, (size_t)D);
+    for (int b = 0; b < B; ++b) {
+        flip_rows_copy(N, L, Bm_b + (size_t)b * N * L, Bf);
+        flip_rows_copy(N, L, Cm_b + (size_t)b * N * L, Cf);
+        /* the backward branch's dB/dC of this batch element, in its own
+         * (flipped) order, summed over channels */
+        zero(dBf, NL);
+        zero(dCf, NL);
+        for (int d = 0; d < D; ++d) {
+            size_t row = ((size_t)b * D + d) * (size_t)L;
+            double Df = Dskip ? Dskip[d] : 0.0, Dbk = D_b ? D_b[d] : 0.0;
+            double bf = bias ? bias[d] : 0.0, bb = bias_b ? bias_b[d] : 0.0;
+            /* forward pass of both branches, fused and gated as before */
+            scan_sequence(L, N, u + row, delta + row, A + (size_t)d * N,
+                          Bm + (size_t)b * N * L, Cm + (size_t)b * N * L, Df, bf,
+                          delta_softplus, yf, h);
+            flip_copy(L, u_b + row, uf);
+            flip_copy(L, delta_b + row, df);
+            scan_sequence(L, N, uf, df, A_b + (size_t)d * N, Bf, Cf, Dbk, bb,
+                          delta_softplus, yb, h);
+            for (int t = 0; t < L; ++t)
+                yv[t] = out_scale * (yf[t] + yb[L - 1 - t]);
+            gate_bwd(L, gout + row, yv, z ? z + row : NULL, gy, dz ? dz + row : NULL);
+            /* y = out_scale * (y_f + flip(y_b)) */
+            for (int t = 0; t < L; ++t) {
+                gf[t] = out_scale * gy[t];
+                gb[t] = out_scale * gy[L - 1 - t];
+            }
+            double sD = 0.0, sb = 0.0;
+            scan_sequence_bwd(L, N, u + row, delta + row, A + (size_t)d * N,
+                              Bm + (size_t)b * N * L, Cm + (size_t)b * N * L, Df, bf,
+                              delta_softplus, gf, du + row, ddelta + row,
+                              dA + (size_t)d * N, dBm + (size_t)b * N * L,
+                              dCm + (size_t)b * N * L, &sD, &sb, hs, G);
+            if (dD)
+                dD[d] += sD;
+            if (dbias)
+                dbias[d] += sb;
+            /* backward branch on the flipped copies; flip its gradients back */
+            zero(duf, Ls);
+            zero(ddf, Ls);
+            sD = 0.0;
+            sb = 0.0;
+            scan_sequence_bwd(L, N, uf, df, A_b + (size_t)d * N, Bf, Cf, Dbk, bb,
+                              delta_softplus, gb, duf, ddf, dA_b + (size_t)d * N, dBf,
+                              dCf, &sD, &sb, hs, G);
+            for (int t = 0; t < L; ++t) {
+                du_b[row + t] += duf[L - 1 - t];
+                ddelta_b[row + t] += ddf[L - 1 - t];
+            }
+            if (dD_b)
+                dD_b[d] += sD;
+            if (dbias_b)
+                dbias_b[d] += sb;
+        }
+        for (int n = 0; n < N; ++n)
+            for (int t = 0; t < L; ++t) {
+                dBm_b[((size_t)b * N + n) * L + t] += dBf[(size_t)n * L + (L - 1 - t)];
+                dCm_b[((size_t)b * N + n) * L + t] += dCf[(size_t)n * L + (L - 1 - t)];
+            }
+    }
+done:
+    free(h);
+    free(G);
+    free(hs);
+    free(yf);
+    free(yb);
+    free(yv);
+    free(gy);
+    free(gf);
+    free(gb);
+    free(uf);
+    free(df);
+    free(Bf);
+    free(Cf);
+    free(duf);
+    free(ddf);
+    free(dBf);
+    free(dCf);
+    return rc;
+}
+
+/* v1 backward: delta, B, C, D and the bias are shared by both branches, so
+ * their gradients sum the two branches'; dA and dA_b are separate. */
+int oracle_bimamba_v1_bwd(int B, int D, int L, int N,
+                          const double *u, const double *delta,
+                          const double *A, const double *A_b,
+                          const double *Bm, const double *Cm,
+                          const double *Dskip, const double *z,
+                          const double *delta_bias, int delta_softplus,
+                          double out_scale, const double *gout,
+                          double *du, double *ddelta, double *dA, double *dA_b,
+                          double *dBm, double *dCm, double *dD, double *dz,
+                          double *dbias)
+{
+    if (B < 0 || D < 0 || L < 0 || N <= 0 || !u || !delta || !A || !A_b || !Bm ||
+        !Cm || !gout || !du || !ddelta || !dA || !dA_b || !dBm || !dCm)
+        return -1;
+    return bidirectional_bwd(B, D, L, N, u, u, delta, delta, A, A_b, Bm, Cm, Bm, Cm,
+                             Dskip, Dskip, z, delta_bias, delta_bias, delta_softplus,
+                             out_scale, gout, du, du, ddelta, ddelta, dA, dA_b, dBm,
+                             dCm, dBm, dCm, dD, dD, dz, dbias, dbias);
+}
+
+/* v2 backward: an independent backward set.  u_b == NULL (shared u): the
+ * gradient of u sums both branches and du_b is not written. */
+int oracle_bimamba_v2_bwd(int B, int D, int L, int N,
+                          const double *u, const double *u_b,
+                          const double *delta, const double *delta_b,
+                          const double *A, const double *A_b,
+                          const double *Bm, const double *Cm,
+                          const double *Bm_b, const double *Cm_b,
+                          const double *Dskip, const double *D_b,
+                          const double *z, const double *delta_bias,
+                          const double *delta_bias_b, int delta_softplus,
+                          double out_scale, const double *gout,
+                          double *du, double *du_b, double *ddelta, double *ddelta_b,
+                          double *dA, double *dA_b, double *dBm, double *dCm,
+                          double *dBm_b, double *dCm_b, double *dD, double *dD_b,
+                          double *dz, double *dbias, double *dbias_b)
+{
+    if (B < 0 || D < 0 || L < 0 || N <= 0 || !u || !delta || !delta_b || !A ||
+        !A_b || !Bm || !Cm || !Bm_b || !Cm_b || !gout || !du || !ddelta ||
+        !ddelta_b || !dA || !dA_b || !dBm || !dCm || !dBm_b || !dCm_b ||
+        (u_b && !du_b))
+        return -1;
+    return bidirectional_bwd(B, D, L, N, u, u_b ? u_b : u, delta, delta_b, A, A_b,
+                             Bm, Cm, Bm_b, Cm_b, Dskip, D_b, z, delta_bias,
+                             delta_bias_b, delta_softplus, out_scale, gout, du,
+                             u_b ? du_b : du, ddelta, ddelta_b, dA, dA_b, dBm, dCm,
+                             dBm_b, dCm_b, dD, dD_b, dz, dbias, dbias_b);
+}
+
+/*
+ * SS2D backward: per (b, d) the four directions read the image in their
+ * scan orders, so the gradient of x gathers each direction's sequence
+ * gradient back through the same order; delta_k, B_k and C_k are in scan
+ * order already.  Layouts as oracle_ss2d; dA [K,D,N], dD and dbias [K,D].
+ */
+int oracle_ss2d_bwd(int B, int D, int H, int W, int N, int K,
+                    const double *x, const double *delta, const double *A,
+                    const double *Bm, const double *Cm, const double *Dskip,
+                    const double *z, const double *delta_bias, int delta_softplus,
+                    const double *gout, double *dx, double *ddelta, double *dA,
+                    double *dBm, double *dCm, double *dD, double *dz, double *dbias)
+{
+    if (B < 0 || D < 0 || H <= 0 || W <= 0 || N <= 0 || K != 4 || !x || !delta ||
+        !A || !Bm || !Cm || !gout || !dx || !ddelta || !dA || !dBm || !dCm)
+        return -1;
+    int L = H * W;
+    long *order = (long *)malloc(sizeof(long) * (size_t)K * (size_t)L);
+    double *h = (double *)malloc(sizeof(double) * (size_t)N);
+    double *G = (double *)malloc(sizeof(double) * (size_t)N);
+    double *hs = (double *)malloc(sizeof(double) * ((size_t)L + 1) * (size_t)N);
+    double *xs = (double *)malloc(sizeof(double) * (size_t)L);
+    double *ys = (double *)malloc(sizeof(double) * (size_t)L);
+    double *acc = (double *)malloc(sizeof(double) * (size_t)L);
+    double *gy = (double *)malloc(sizeof(double) * (size_t)L);
+    double *gs = (double *)malloc(sizeof(double) * (size_t)L);
+    double *dxs = (double *)malloc(sizeof(double) * (size_t)L);
+    int rc = 0;
+    if (!order || !h || !G || !hs || !xs || !ys || !acc || !gy || !gs || !dxs) {
+        rc = -1;
+        goto done;
+    }
+    zero(dx, (size_t)B * D * L);
+    zero(ddelta, (size_t)B * K * D * L);
+    zero(dA, (size_t)K * D * N);
+    zero(dBm, (size_t)B * K * N * L);
+    zero(dCm, (size_t)B * K * N * L);
+    zero(dD, (size_t)K * D);
+    zero(dz, (size_t)B * D * L);
+    zero(dbias, (size_t)K * D);
+    for (int k = 0; k < K; ++k)
+        for (int t = 0; t < L; ++t)
+            order[(size_t)k * L + t] = oracle_cross_scan_index(H, W, k, t);
+    for (int b = 0; b < B; ++b) {
+        for (int d = 0; d < D; ++d) {
+            const double *img = x + ((size_t)b * D + d) * (size_t)L;
+            /* forward: the merged output before the gate */
+            for (int p = 0; p < L; ++p)
+                acc[p] = 0.0;
+            for (int k = 0; k < K; ++k) {
+                const long *ord = order + (size_t)k * L;
+                for (int t = 0; t < L; ++t)
+                    xs[t] = img[ord[t]];
+                size_t drow = (((size_t)b * K + k) * D + d) * (size_t)L;
+                size_t bc = ((size_t)b * K + k) * (size_t)N * L;
+                size_t kd = (size_t)k * D + d;
+                scan_sequence(L, N, xs, delta + drow, A + kd * N, Bm + bc, Cm + bc,
+                              Dskip ? Dskip[kd] : 0.0,
+                              delta_bias ? delta_bias[kd] : 0.0, delta_softplus, ys, h);
+                for (int t = 0; t < L; ++t)
+                    acc[ord[t]] += ys[t];
+            }
+            size_t prow = ((size_t)b * D + d) * (size_t)L;
+            gate_bwd(L, gout + prow, acc, z ? z + prow : NULL, gy, dz ? dz + prow : NULL);
+            /* each direction: gradient in its scan order, scattered back */
+            for (int k = 0; k < K; ++k) {
+                const long *ord = order + (size_t)k * L;
+                for (int t = 0; t < L; ++t) {
+                    xs[t] = img[ord[t]];
+                    gs[t] = gy[ord[t]];
+                    dxs[t] = 0.0;
+                }
+                size_t drow = (((size_t)b * K + k) * D + d) * (size_t)L;
+                size_t bc = ((size_t)b * K + k) * (size_t)N * L;
+                size_t kd = (size_t)k * D + d;
+                double sD = 0.0, sb = 0.0;
+                scan_sequence_bwd(L, N, xs, delta + drow, A + kd * N, Bm + bc, Cm + bc,
+                                  Dskip ? Dskip[kd] : 0.0,
+                                  delta_bias ? delta_bias[kd] : 0.0, delta_softplus, gs,
+                                  dxs, ddelta + drow, dA + kd * N, dBm + bc, dCm + bc,
+                                  &sD, &sb, hs, G);
+                for (int t = 0; t < L; ++t)
+                    dx[prow + ord[t]] += dxs[t];
+                if (dD)
+                    dD[kd] += sD;
+                if (dbias)
+                    dbias[kd] += sb;
+            }
+        }
+    }
+done:
+    free(order);
+    free(h);
+    free(G);
+    free(hs);
+    free(xs);
+    free(ys);
+    free(acc);
+    free(gy);
+    free(gs);
+    free(dxs);
+    return rc;
+}
