@@ -229,6 +229,81 @@ SSM_API const char *ssm_status_string(ssm_status s);
  */
 SSM_API void ssm_set_profile_events(void *begin, void *end);
 
+/* ---------------------------------------------------------------------------
+ * Backward pass.  Gradients of the loss sum(dout * out) for the output `out`
+ * of the matching forward call with the same arguments: the adjoint of the
+ * recurrence above (G_t = gy_t C_t + exp(delta_{t+1} A) G_{t+1}, then dC, dB,
+ * du, dA, ddelta from G and the states), of the softplus, the gate, the
+ * flip-add and the cross-merge.  The pages discuss training through the
+ * scan and checking its gradients ("Vision Mamba实战", section 4;
+ * "从Transformer到Mamba", section 4.2) but print no backward formula; this
+ * is the exact derivative of the forward definition.
+ *
+ * Gradient outputs are device buffers with their input's shape: du, ddelta,
+ * dB, dC, dz (and the _b and dx variants) in the I/O dtype; dA, dD and
+ * ddelta_bias fp32.  Every output is overwritten.  dz is required when z is
+ * given (ignored otherwise); dD is written only when Dskip is given;
+ * ddelta_bias (and the _b variants) may be NULL.  Parameter gradients sum
+ * over every batch element and position (and, for v1, both branches);
+ * partial sums are reduced in a fixed order, so results are deterministic.
+ * `workspace`: at least ssm_bwd_workspace_bytes(...) bytes, 16-byte
+ * aligned, contents irrelevant.  State and arithmetic are fp32.  Errors as
+ * for the forward calls; SSM_ERR_WORKSPACE when it is too small.
+ * ------------------------------------------------------------------------- */
+SSM_API ssm_status selective_scan_bwd(ssm_dtype dt, int B, int D, int L, int N,
+                         const void *u, const void *delta, const float *A,
+                         const void *Bm, const void *Cm, const float *Dskip,
+                         const void *z, const float *delta_bias,
+                         int delta_softplus, const void *dout, void *du,
+                         void *ddelta, float *dA, void *dB, void *dC, float *dD,
+                         void *dz, float *ddelta_bias, void *workspace,
+                         size_t ws_bytes, ssm_stream_t stream);
+
+/* v1: delta, B, C, Dskip and delta_bias are shared by both branches, so their
+ * gradients sum both; dA and dA_b belong to A and A_b. */
+SSM_API ssm_status bimamba_scan_bwd_v1(ssm_dtype dt, int B, int D, int L, int N,
+                         const void *u, const void *delta, const float *A,
+                         const float *A_b, const void *Bm, const void *Cm,
+                         const float *Dskip, const void *z,
+                         const float *delta_bias, int delta_softplus,
+                         float out_scale, const void *dout, void *du,
+                         void *ddelta, float *dA, float *dA_b, void *dB, void *dC,
+                         float *dD, void *dz, float *ddelta_bias,
+                         void *workspace, size_t ws_bytes, ssm_stream_t stream);
+
+/* v2: one gradient per tensor of each set.  u_b == NULL (shared u): du sums
+ * both branches and du_b is ignored; otherwise du_b is required. */
+SSM_API ssm_status bimamba_scan_bwd_v2(ssm_dtype dt, int B, int D, int L, int N,
+                         const void *u, const void *u_b, const void *delta,
+                         const void *delta_b, const float *A, const float *A_b,
+                         const void *Bm, const void *Cm, const void *Bm_b,
+                         const void *Cm_b, const float *Dskip, const float *D_b,
+                         const void *z, const float *delta_bias,
+                         const float *delta_bias_b, int delta_softplus,
+                         float out_scale, const void *dout, void *du, void *du_b,
+                         void *ddelta, void *ddelta_b, float *dA, float *dA_b,
+                         void *dB, void *dC, void *dB_b, void *dC_b, float *dD,
+                         float *dD_b, void *dz, float *ddelta_bias,
+                         float *ddelta_bias_b, void *workspace, size_t ws_bytes,
+                         ssm_stream_t stream);
+
+/* SS2D, K = 4: dx [B,D,H,W]; ddelta [B,4,D,L], dB/dC [B,4,N,L] in each
+ * direction's scan order; dA [4,D,N]; dD and ddelta_bias [4,D]. */
+SSM_API ssm_status ss2d_scan_bwd(ssm_dtype dt, int B, int D, int H, int W, int N,
+                         int K, const void *x, const void *delta, const float *A,
+                         const void *Bm, const void *Cm, const float *Dskip,
+                         const void *z, const float *delta_bias,
+                         int delta_softplus, const void *dout, void *dx,
+                         void *ddelta, float *dA, void *dB, void *dC, float *dD,
+                         void *dz, float *ddelta_bias, void *workspace,
+                         size_t ws_bytes, ssm_stream_t stream);
+
+/* Workspace bytes of the backward call with these sizes (0 when B*D*L is 0;
+ * (size_t)-1 for invalid sizes).  separate_u_b: v2 called with u_b != NULL. */
+SSM_API size_t ssm_bwd_workspace_bytes(ssm_op op, ssm_dtype dt, int B, int D,
+                                       int L_or_HW, int N, int K,
+                                       int separate_u_b);
+
 /*
  * Tuning override for the two-branch kernels (v1, v2 and both SS2D passes).
  * A CTA takes `channels` channels of one batch element, both branches:

@@ -48,8 +48,17 @@ _lib.ssm_set_cta_channels.argtypes = [_i]
 _lib.ssm_set_cta_channels.restype = None
 _lib.ssm_set_profile_events.argtypes = [_vp, _vp]
 _lib.ssm_set_profile_events.restype = None
+_lib.selective_scan_bwd.argtypes = [_i] * 5 + [_vp] * 8 + [_i] + [_vp] * 10 + [_sz, _vp]
+_lib.bimamba_scan_bwd_v1.argtypes = ([_i] * 5 + [_vp] * 9 + [_i, _f] + [_vp] * 11 +
+                                     [_sz, _vp])
+_lib.bimamba_scan_bwd_v2.argtypes = ([_i] * 5 + [_vp] * 15 + [_i, _f] + [_vp] * 17 +
+                                     [_sz, _vp])
+_lib.ss2d_scan_bwd.argtypes = [_i] * 7 + [_vp] * 8 + [_i] + [_vp] * 10 + [_sz, _vp]
+_lib.ssm_bwd_workspace_bytes.argtypes = [_i] * 8
+_lib.ssm_bwd_workspace_bytes.restype = _sz
 for _fn in (_lib.selective_scan_fwd, _lib.bimamba_scan_fwd_v1, _lib.bimamba_scan_fwd_v2,
-            _lib.ss2d_scan_fwd, _lib.bimamba_scan_fwd_v2_noalloc):
+            _lib.ss2d_scan_fwd, _lib.bimamba_scan_fwd_v2_noalloc, _lib.selective_scan_bwd,
+            _lib.bimamba_scan_bwd_v1, _lib.bimamba_scan_bwd_v2, _lib.ss2d_scan_bwd):
     _fn.restype = _i
 
 
@@ -255,3 +264,167 @@ def bimamba_scan_fwd_v2_noalloc(u, delta, delta_b, A, A_b, B, C, B_b, C_b, D=Non
                                             _io(y, io, "out", sh), _stream(stream)),
            "bimamba_scan_fwd_v2_noalloc")
     return y
+
+
+# ---------------------------------------------------------------- backward
+def bwd_workspace_bytes(op: str, dtype: torch.dtype, B: int, D: int, L: int, N: int,
+                        K: int = 4, separate_u_b: bool = False) -> int:
+    code = SSM_F32 if dtype == torch.float32 else SSM_BF16
+    n = _lib.ssm_bwd_workspace_bytes(OPS[op], code, B, D, L, N, K, int(bool(separate_u_b)))
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("invalid sizes")
+    return int(n)
+
+
+def _bwd_workspace(op, dtype, B, D, L, N, device, workspace, K=4, separate_u_b=False):
+    need = bwd_workspace_bytes(op, dtype, B, D, L, N, K, separate_u_b)
+    if need == 0:
+        return None, 0
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    if not workspace.is_cuda or workspace.numel() * workspace.element_size() < need:
+        raise ValueError("workspace must be a CUDA tensor of at least %d bytes" % need)
+    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
+
+def _ptr_or_none(t):
+    return None if t is None else t.data_ptr()
+
+
+def selective_scan_bwd(dout, u, delta, A, B, C, D=None, z=None, delta_bias=None,
+                       delta_softplus=True, workspace=None, stream=None):
+    """Gradients of sum(dout * selective_scan_fwd(...)).  Returns a dict:
+    du, ddelta, dA, dB, dC, and dD / dz / ddelta_bias for the inputs given."""
+    io = u.dtype
+    Bt, Dc, L = u.shape
+    N = A.shape[1]
+    sh, shn = (Bt, Dc, L), (Bt, N, L)
+    g = {"du": torch.empty_like(u), "ddelta": torch.empty_like(u),
+         "dA": torch.empty_like(A), "dB": torch.empty(shn, dtype=io, device=u.device),
+         "dC": torch.empty(shn, dtype=io, device=u.device)}
+    if D is not None:
+        g["dD"] = torch.empty_like(D)
+    if z is not None:
+        g["dz"] = torch.empty_like(u)
+    if delta_bias is not None:
+        g["ddelta_bias"] = torch.empty_like(delta_bias)
+    args = [_io(u, io, "u"), _io(delta, io, "delta", sh), _par(A, "A", (Dc, N)),
+            _io(B, io, "B", shn), _io(C, io, "C", shn), _par(D, "D", (Dc,), True),
+            _io(z, io, "z", sh, True), _par(delta_bias, "delta_bias", (Dc,), True)]
+    outs = [g["du"], g["ddelta"], g["dA"], g["dB"], g["dC"], g.get("dD"), g.get("dz"),
+            g.get("ddelta_bias")]
+    wp, wn = _bwd_workspace("single", io, Bt, Dc, L, N, u.device, workspace)
+    _check(_lib.selective_scan_bwd(_dtype_code(u), Bt, Dc, L, N, *args,
+                                   int(bool(delta_softplus)), _io(dout, io, "dout", sh),
+                                   *map(_ptr_or_none, outs), wp, wn, _stream(stream)),
+           "selective_scan_bwd")
+    return g
+
+
+def bimamba_scan_bwd_v1(dout, u, delta, A, A_b, B, C, D=None, z=None, delta_bias=None,
+                        delta_softplus=True, out_scale=1.0, workspace=None, stream=None):
+    """Gradients of sum(dout * bimamba_scan_fwd_v1(...)): du, ddelta, dA, dA_b,
+    dB, dC, and dD / dz / ddelta_bias for the inputs given."""
+    io = u.dtype
+    Bt, Dc, L = u.shape
+    N = A.shape[1]
+    sh, shn = (Bt, Dc, L), (Bt, N, L)
+    g = {"du": torch.empty_like(u), "ddelta": torch.empty_like(u),
+         "dA": torch.empty_like(A), "dA_b": torch.empty_like(A_b),
+         "dB": torch.empty(shn, dtype=io, device=u.device),
+         "dC": torch.empty(shn, dtype=io, device=u.device)}
+    if D is not None:
+        g["dD"] = torch.empty_like(D)
+    if z is not None:
+        g["dz"] = torch.empty_like(u)
+    if delta_bias is not None:
+        g["ddelta_bias"] = torch.empty_like(delta_bias)
+    args = [_io(u, io, "u"), _io(delta, io, "delta", sh), _par(A, "A", (Dc, N)),
+            _par(A_b, "A_b", (Dc, N)), _io(B, io, "B", shn), _io(C, io, "C", shn),
+            _par(D, "D", (Dc,), True), _io(z, io, "z", sh, True),
+            _par(delta_bias, "delta_bias", (Dc,), True)]
+    outs = [g["du"], g["ddelta"], g["dA"], g["dA_b"], g["dB"], g["dC"], g.get("dD"),
+            g.get("dz"), g.get("ddelta_bias")]
+    wp, wn = _bwd_workspace("v1", io, Bt, Dc, L, N, u.device, workspace)
+    _check(_lib.bimamba_scan_bwd_v1(_dtype_code(u), Bt, Dc, L, N, *args,
+                                    int(bool(delta_softplus)), float(out_scale),
+                                    _io(dout, io, "dout", sh), *map(_ptr_or_none, outs),
+                                    wp, wn, _stream(stream)), "bimamba_scan_bwd_v1")
+    return g
+
+
+def bimamba_scan_bwd_v2(dout, u, delta, delta_b, A, A_b, B, C, B_b, C_b, D=None, D_b=None,
+                        z=None, delta_bias=None, delta_bias_b=None, u_b=None,
+                        delta_softplus=True, out_scale=0.5, workspace=None, stream=None):
+    """Gradients of sum(dout * bimamba_scan_fwd_v2(...)): one per input given
+    (du_b only with u_b)."""
+    io = u.dtype
+    Bt, Dc, L = u.shape
+    N = A.shape[1]
+    sh, shn = (Bt, Dc, L), (Bt, N, L)
+    dev = u.device
+    g = {"du": torch.empty_like(u), "ddelta": torch.empty_like(u),
+         "ddelta_b": torch.empty_like(u), "dA": torch.empty_like(A),
+         "dA_b": torch.empty_like(A_b)}
+    for k in ("dB", "dC", "dB_b", "dC_b"):
+        g[k] = torch.empty(shn, dtype=io, device=dev)
+    if u_b is not None:
+        g["du_b"] = torch.empty_like(u)
+    if D is not None:
+        g["dD"] = torch.empty_like(D)
+    if D_b is not None:
+        g["dD_b"] = torch.empty_like(D_b)
+    if z is not None:
+        g["dz"] = torch.empty_like(u)
+    if delta_bias is not None:
+        g["ddelta_bias"] = torch.empty_like(delta_bias)
+    if delta_bias_b is not None:
+        g["ddelta_bias_b"] = torch.empty_like(delta_bias_b)
+    args = [_io(u, io, "u"), _io(u_b, io, "u_b", sh, True), _io(delta, io, "delta", sh),
+            _io(delta_b, io, "delta_b", sh), _par(A, "A", (Dc, N)), _par(A_b, "A_b", (Dc, N)),
+            _io(B, io, "B", shn), _io(C, io, "C", shn), _io(B_b, io, "B_b", shn),
+            _io(C_b, io, "C_b", shn), _par(D, "D", (Dc,), True), _par(D_b, "D_b", (Dc,), True),
+            _io(z, io, "z", sh, True), _par(delta_bias, "delta_bias", (Dc,), True),
+            _par(delta_bias_b, "delta_bias_b", (Dc,), True)]
+    outs = [g["du"], g.get("du_b"), g["ddelta"], g["ddelta_b"], g["dA"], g["dA_b"], g["dB"],
+            g["dC"], g["dB_b"], g["dC_b"], g.get("dD"), g.get("dD_b"), g.get("dz"),
+            g.get("ddelta_bias"), g.get("ddelta_bias_b")]
+    wp, wn = _bwd_workspace("v2", io, Bt, Dc, L, N, dev, workspace,
+                            separate_u_b=u_b is not None)
+    _check(_lib.bimamba_scan_bwd_v2(_dtype_code(u), Bt, Dc, L, N, *args,
+                                    int(bool(delta_softplus)), float(out_scale),
+                                    _io(dout, io, "dout", sh), *map(_ptr_or_none, outs),
+                                    wp, wn, _stream(stream)), "bimamba_scan_bwd_v2")
+    return g
+
+
+def ss2d_scan_bwd(dout, x, delta, A, B, C, D=None, z=None, delta_bias=None,
+                  delta_softplus=True, workspace=None, stream=None):
+    """Gradients of sum(dout * ss2d_scan_fwd(...)): dx, ddelta, dA, dB, dC, and
+    dD / dz / ddelta_bias for the inputs given."""
+    io = x.dtype
+    Bt, Dc, H, W = x.shape
+    K = 4
+    L = H * W
+    N = A.shape[2]
+    dev = x.device
+    g = {"dx": torch.empty_like(x), "ddelta": torch.empty_like(delta),
+         "dA": torch.empty_like(A), "dB": torch.empty_like(B), "dC": torch.empty_like(C)}
+    if D is not None:
+        g["dD"] = torch.empty_like(D)
+    if z is not None:
+        g["dz"] = torch.empty_like(x)
+    if delta_bias is not None:
+        g["ddelta_bias"] = torch.empty_like(delta_bias)
+    args = [_io(x, io, "x"), _io(delta, io, "delta", (Bt, K, Dc, L)), _par(A, "A", (K, Dc, N)),
+            _io(B, io, "B", (Bt, K, N, L)), _io(C, io, "C", (Bt, K, N, L)),
+            _par(D, "D", (K, Dc), True), _io(z, io, "z", (Bt, Dc, H, W), True),
+            _par(delta_bias, "delta_bias", (K, Dc), True)]
+    outs = [g["dx"], g["ddelta"], g["dA"], g["dB"], g["dC"], g.get("dD"), g.get("dz"),
+            g.get("ddelta_bias")]
+    wp, wn = _bwd_workspace("ss2d", io, Bt, Dc, L, N, dev, workspace, K)
+    _check(_lib.ss2d_scan_bwd(_dtype_code(x), Bt, Dc, H, W, N, K, *args,
+                              int(bool(delta_softplus)), _io(dout, io, "dout", (Bt, Dc, H, W)),
+                              *map(_ptr_or_none, outs), wp, wn, _stream(stream)),
+           "ss2d_scan_bwd")
+    return g

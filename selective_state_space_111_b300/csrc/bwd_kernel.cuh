@@ -1,0 +1,322 @@
+// bwd_kernel.cuh -- backward pass of the selective scan (S6), sm_103a.
+//
+// Gradients of a loss sum_t g_t * out_t for the three forms.  Per direction,
+// with a_t[n] = exp(delta_t * A[n]) and G_t[n] = dLoss/dh_t[n] (the adjoint
+// of the forward recurrence of "状态空间模型如何重塑视觉序列处理", section
+// "选择性扫描机制的计算效率优势", read with exp(delta*A) and delta*B):
+//   G_t      = gy_t * C_t + a_{t+1} * G_{t+1}                (G_L = 0)
+//   dC_t     = gy_t * h_t,       dB_t = G_t * delta_t * u_t
+//   du_t     = gy_t * D + sum_n G_t * delta_t * B_t
+//   dA      += G_t * h_{t-1} * a_t * delta_t
+//   ddelta_t = sum_n G_t * (h_{t-1} * a_t * A + B_t * u_t)
+//   ddt_t    = ddelta_t * sigmoid(dt_t + bias)   (softplus' ; or ddelta_t)
+// gy is the gradient of the direction's own output y (before the gate; the
+// gate, the flip-add and the cross-merge are undone by the callers).
+//
+//   scan_bwd_kernel   CTA = 16 channels of one batch element, one direction;
+//                     lane = (channel, state).  Pass 1 runs the recurrence
+//                     forward and stores the state at every chunk start
+//                     (chunks of T = 32 steps).  Pass 2 walks the chunks
+//                     backwards: it recomputes the chunk's states in
+//                     registers from the stored start, then runs the adjoint
+//                     recurrence step by step.  Per-position gradients (du,
+//                     ddelta) are summed over the 16 states by shuffles; dB
+//                     and dC (summed over channels) go through shared memory
+//                     into one fp32 partial per CTA, reduced afterwards in a
+//                     fixed order, so results are deterministic.
+//   gate_bwd_kernel   gy = g * silu(z), dz = g * y * silu'(z).
+//   reduce kernels    partial sums -> dA, dD, dbias (fp32), dB, dC (I/O dtype).
+#pragma once
+
+#include "scan_ops.cuh"
+
+namespace ssm {
+namespace bwd {
+
+constexpr int T = 32;            // steps per chunk
+constexpr int CH = 16;           // channels per CTA
+constexpr int NT = CH * kMaxN;   // threads: lane = (channel, state)
+constexpr int NWARP = NT / 32;
+
+// One direction of one form.  Walk step w (0..L-1) is position
+// p = rev ? L-1-w : w of the position-ordered tensors (u, G, du); dt and
+// B/C are read at stream index s = stream_rev ? w : p.
+struct Pass {
+    const void *dt;            // delta: row (b, d) at dt_off + b * dt_bstride + d * L
+    long long dt_off, dt_bstride;
+    const void *u;             // [B, D, L], position order
+    const void *Bm, *Cm;       // row (b, n) at bc_off + b * bc_bstride + n * L
+    long long bc_off, bc_bstride;
+    const float *A;            // [D, N]
+    const float *Dskip;        // [D] or null
+    const float *bias;         // [D] or null
+    const float *G;            // dLoss/dy (fp32 [B, D, L], position order)
+    float gscale;              // this direction's share of G (out_scale)
+    int rev, stream_rev;
+    float *du;                 // fp32 [B, D, L], position order, accumulated
+    float *ddt;                // fp32, indexed like dt, accumulated
+    float *pdB, *pdC;          // this pass's partials [ncg][B][L][16] (stream index)
+    float *pdA;                // [B][D][16]
+    float *pdD, *pdbias;       // [B][D]
+    float *hc;                 // chunk-start states [B][D][nch][16]
+};
+
+struct Params {
+    Pass ps;
+    int B, D, L, N, nch;
+    int delta_softplus;
+};
+
+__device__ __forceinline__ float sigmoid_f(float x) {
+    return 1.f / (1.f + expf(-x));
+}
+constexpr int kDynBytes = 2 * NWARP * T * kMaxN * (int)sizeof(float);
+
+template <typename IO>
+__global__ void __launch_bounds__(NT)
+scan_bwd_kernel(const Params P) {
+    __shared__ float sD[CH][T + 1], sS[CH][T + 1], sU[CH][T + 1], sG[CH][T + 1];
+    __shared__ float sB[T][kMaxN + 1], sC[T][kMaxN + 1];
+    __shared__ float sDu[CH][T + 1], sDd[CH][T + 1];
+    // per-warp dB, dC partials of a chunk (dynamic: kDynBytes)
+    extern __shared__ float dyn[];
+    float (*sPB)[T][kMaxN] = reinterpret_cast<float (*)[T][kMaxN]>(dyn);
+    float (*sPC)[T][kMaxN] = reinterpret_cast<float (*)[T][kMaxN]>(dyn + NWARP * T * kMaxN);
+
+    const Pass &ps = P.ps;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int ch = tid / kMaxN, n = tid % kMaxN;
+    const int b = blockIdx.y, d0 = blockIdx.x * CH, d = d0 + ch;
+    const int L = P.L, D = P.D, N = P.N, nch = P.nch;
+    const bool cvalid = d < D, valid = cvalid && n < N;
+    const float A2 = valid ? ps.A[(long long)d * N + n] * kLog2e : 0.f;
+    const float Av = valid ? ps.A[(long long)d * N + n] : 0.f;
+    const float Dd = (cvalid && ps.Dskip) ? ps.Dskip[d] : 0.f;
+    const IO *dtp = (const IO *)ps.dt + ps.dt_off + b * ps.dt_bstride;
+    const IO *bp = (const IO *)ps.Bm + ps.bc_off + b * ps.bc_bstride;
+    const IO *cp = (const IO *)ps.Cm + ps.bc_off + b * ps.bc_bstride;
+    const IO *up = (const IO *)ps.u;
+    float *hcp = ps.hc + (((long long)b * D + d) * nch) * kMaxN + n;
+
+    auto pos = [&](int w) { return ps.rev ? L - 1 - w : w; };
+    auto sidx = [&](int w) { return ps.stream_rev ? w : pos(w); };
+    // chunk c of every input into shared memory (zeros beyond L and D)
+    auto stage = [&](int c, bool full) {
+        for (int i = tid; i < CH * T; i += NT) {
+            const int cc = i / T, j = i % T, w = c * T + j, dd = d0 + cc;
+            float dl = 0.f, sg = 1.f, uu = 0.f, gg = 0.f;
+            if (w < L && dd < D) {
+                const float x = to_f32(dtp[(long long)dd * L + sidx(w)]) +
+                                (ps.bias ? ps.bias[dd] : 0.f);
+                if (P.delta_softplus) {
+                    dl = x > 20.f ? x : log1pf(expf(x));
+                    sg = sigmoid_f(x);
+                } else {
+                    dl = x;
+                }
+                uu = to_f32(up[((long long)b * D + dd) * L + pos(w)]);
+                if (full) gg = ps.gscale * ps.G[((long long)b * D + dd) * L + pos(w)];
+            }
+            sD[cc][j] = dl;
+            sS[cc][j] = sg;
+            sU[cc][j] = uu;
+            sG[cc][j] = gg;
+        }
+        for (int i = tid; i < kMaxN * T; i += NT) {
+            const int nn = i / T, j = i % T, w = c * T + j;
+            const bool ok = w < L && nn < N;
+            const long long o = (long long)nn * L + (ok ? sidx(w) : 0);
+            sB[j][nn] = ok ? to_f32(bp[o]) : 0.f;
+            if (full) sC[j][nn] = ok ? to_f32(cp[o]) : 0.f;
+        }
+    };
+
+    // ---- pass 1: states at the chunk starts
+    float h = 0.f;
+    for (int c = 0; c < nch; ++c) {
+        if (cvalid) hcp[(long long)c * kMaxN] = h;
+        stage(c, false);
+        __syncthreads();
+        const int len = min(T, L - c * T);
+        for (int j = 0; j < len; ++j) {
+            const float dl = sD[ch][j];
+            h = fmaf(ex2_approx(dl * A2), h, dl * sB[j][n] * sU[ch][j]);
+        }
+        __syncthreads();
+    }
+
+    // ---- pass 2: adjoint, chunks in reverse
+    float Gc = 0.f, dA = 0.f, dDs = 0.f, dbs = 0.f;
+    for (int c = nch - 1; c >= 0; --c) {
+        stage(c, true);
+        __syncthreads();
+        const int len = min(T, L - c * T);
+        const float h0 = cvalid ? hcp[(long long)c * kMaxN] : 0.f;
+        float hr[T];
+        {
+            float hh = h0;
+#pragma unroll
+            for (int j = 0; j < T; ++j) {
+                if (j < len) {
+                    const float dl = sD[ch][j];
+                    hh = fmaf(ex2_approx(dl * A2), hh, dl * sB[j][n] * sU[ch][j]);
+                }
+                hr[j] = hh;
+            }
+        }
+#pragma unroll
+        for (int j = T - 1; j >= 0; --j) {
+            if (j < len) {
+                const float dl = sD[ch][j], uu = sU[ch][j], gy = sG[ch][j];
+                const float bb = sB[j][n], cc = sC[j][n];
+                const float a = ex2_approx(dl * A2);
+                const float hp = j > 0 ? hr[j - 1] : h0;
+                const float g = fmaf(gy, cc, Gc);
+                float dCp = gy * hr[j];
+                float dBp = g * dl * uu;
+                float dup = g * dl * bb;
+                float ddp = g * fmaf(hp * a, Av, bb * uu);
+                dA = fmaf(g * hp * a, dl, dA);
+                Gc = a * g;
+                // sums over the 16 states of the channel
+#pragma unroll
+                for (int o = kMaxN / 2; o >= 1; o >>= 1) {
+                    dup += __shfl_xor_sync(0xffffffffu, dup, o);
+                    ddp += __shfl_xor_sync(0xffffffffu, ddp, o);
+                }
+                // sums over the warp's two channels
+                dBp += __shfl_xor_sync(0xffffffffu, dBp, 16);
+                dCp += __shfl_xor_sync(0xffffffffu, dCp, 16);
+                if (n == 0) {
+                    sDu[ch][j] = fmaf(gy, Dd, dup);
+                    sDd[ch][j] = ddp;
+                    dDs = fmaf(gy, uu, dDs);
+                    dbs += P.delta_softplus ? ddp * sS[ch][j] : ddp;
+                }
+                if (lane < 16) {
+                    sPB[warp][j][n] = dBp;
+                    sPC[warp][j][n] = dCp;
+                }
+            }
+        }
+        __syncthreads();
+        // per-position gradients, accumulated (several directions may add)
+        for (int i = tid; i < CH * T; i += NT) {
+            const int cc = i / T, j = i % T, w = c * T + j, dd = d0 + cc;
+            if (w < L && dd < D) {
+                const long long prow = ((long long)b * D + dd) * L;
+                ps.du[prow + pos(w)] += sDu[cc][j];
+                const float gx = P.delta_softplus ? sDd[cc][j] * sS[cc][j] : sDd[cc][j];
+                ps.ddt[ps.dt_off + b * ps.dt_bstride + (long long)dd * L + sidx(w)] += gx;
+            }
+        }
+        // dB, dC partial of this CTA: sum over its warps
+        for (int i = tid; i < T * kMaxN; i += NT) {
+            const int j = i / kMaxN, nn = i % kMaxN, w = c * T + j;
+            if (w < L) {
+                float sb = 0.f, sc = 0.f;
+#pragma unroll
+                for (int k = 0; k < NWARP; ++k) {
+                    sb += sPB[k][j][nn];
+                    sc += sPC[k][j][nn];
+                }
+                const long long o = (((long long)blockIdx.x * P.B + b) * L + sidx(w)) * kMaxN + nn;
+                ps.pdB[o] = sb;
+                ps.pdC[o] = sc;
+            }
+        }
+        __syncthreads();
+    }
+    if (cvalid) {
+        ps.pdA[((long long)b * D + d) * kMaxN + n] = dA;
+        if (n == 0) {
+            ps.pdD[(long long)b * D + d] = dDs;
+            ps.pdbias[(long long)b * D + d] = dbs;
+        }
+    }
+}
+
+// gy = g * silu(z) (fp32), dz = g * y * silu'(z) (I/O dtype); z == null: gy = g
+template <typename IO>
+__global__ void gate_bwd_kernel(const IO *__restrict__ g, const IO *__restrict__ z,
+                                const IO *__restrict__ y, float *__restrict__ gy,
+                                IO *__restrict__ dz, long long n) {
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x) {
+        const float gv = to_f32(g[i]);
+        if (z) {
+            const float zv = to_f32(z[i]), s = sigmoid_f(zv);
+            gy[i] = gv * zv * s;
+            if (dz) dz[i] = from_f32<IO>(gv * to_f32(y[i]) * s * (1.f + zv * (1.f - s)));
+        } else {
+            gy[i] = gv;
+        }
+    }
+}
+
+// out[m][c][r] = in[m][r][c] for maps of R x C (fp32 or I/O), optionally
+// added to a second map: out = add + transpose(in)
+template <typename E>
+__global__ void transpose_kernel(const E *__restrict__ in, E *__restrict__ out, int maps, int R,
+                                 int C) {
+    __shared__ E tile[32][33];
+    const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    for (int m = blockIdx.z; m < maps; m += gridDim.z) {
+        const E *src = in + (long long)m * R * C;
+        E *dst = out + (long long)m * R * C;
+        for (int i = ty; i < 32; i += 8) {
+            const int r = r0 + i, c = c0 + tx;
+            if (r < R && c < C) tile[i][tx] = src[(long long)r * C + c];
+        }
+        __syncthreads();
+        for (int i = ty; i < 32; i += 8) {
+            const int c = c0 + i, r = r0 + tx;
+            if (r < R && c < C) dst[(long long)c * R + r] = tile[tx][i];
+        }
+        __syncthreads();
+    }
+}
+
+// out (I/O) = a [+ b] elementwise, fp32 inputs
+template <typename IO>
+__global__ void convert_kernel(const float *__restrict__ a, const float *__restrict__ b,
+                               IO *__restrict__ out, long long n) {
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x)
+        out[i] = from_f32<IO>(b ? a[i] + b[i] : a[i]);
+}
+
+// dB[b][n][s] (I/O, at out + b * out_bstride) = sum over the nslot partials
+// [slot][B][L][16] (slot-major, fixed order)
+template <typename IO>
+__global__ void reduce_bc_kernel(const float *__restrict__ part, int nslot, int B, int L, int N,
+                                 IO *__restrict__ out, long long out_bstride) {
+    const long long total = (long long)B * L * N;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int nn = (int)(i % N);
+        const long long bs = i / N;                  // b * L + s
+        const int s = (int)(bs % L), b = (int)(bs / L);
+        float acc = 0.f;
+        for (int k = 0; k < nslot; ++k) acc += part[((long long)k * B * L + bs) * kMaxN + nn];
+        out[b * out_bstride + (long long)nn * L + s] = from_f32<IO>(acc);
+    }
+}
+
+// out[i] = sum over the nslot partials [slot][B][cols] of column i (fixed
+// order): dA (cols = D * 16, written [D][N]), dD and dbias (cols = D)
+__global__ void reduce_param_kernel(const float *__restrict__ part, int nslot, int B, int D,
+                                    int N, int per_state, float *__restrict__ out) {
+    const int cols = per_state ? D * kMaxN : D;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < cols; i += gridDim.x * blockDim.x) {
+        if (per_state && i % kMaxN >= N) continue;
+        float acc = 0.f;
+        for (int k = 0; k < nslot; ++k)
+            for (int b = 0; b < B; ++b) acc += part[((long long)k * B + b) * cols + i];
+        out[per_state ? (i / kMaxN) * N + i % kMaxN : i] = acc;
+    }
+}
+
+}  // namespace bwd
+}  // namespace ssm

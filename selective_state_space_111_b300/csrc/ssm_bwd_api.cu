@@ -1,0 +1,530 @@
+// ssm_bwd_api.cu -- the backward entry points declared in include/ssm_scan.h.
+//
+// Each call: (1) recomputes the pre-gate output y with the forward entry
+// point (only when z is given), (2) gy = dout * silu(z) and dz, (3) one
+// scan_bwd_kernel launch per direction, which accumulates the per-position
+// gradients in fp32 and leaves per-CTA partial sums of the parameter
+// gradients, (4) fixed-order reductions of the partials and conversion to
+// the output dtypes.  Nothing is allocated; everything lives in the
+// caller's workspace (ssm_bwd_workspace_bytes).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "bwd_kernel.cuh"
+#include "ssm_scan.h"
+
+namespace {
+
+using ssm::bwd::Pass;
+
+bool aligned(const void *p, unsigned a) { return ((uintptr_t)p % a) == 0; }
+bool fits(long long v) { return v >= 0 && v <= 0x7fffffffLL; }
+unsigned esz(ssm_dtype dt) { return dt == SSM_F32 ? 4u : 2u; }
+bool io_ok(ssm_dtype dt, const void *p) { return p != nullptr && aligned(p, esz(dt)); }
+bool opt_io(ssm_dtype dt, const void *p) { return p == nullptr || aligned(p, esz(dt)); }
+bool f32_ok(const float *p) { return p != nullptr && aligned(p, 4); }
+bool opt_f32(const float *p) { return p == nullptr || aligned(p, 4); }
+
+ssm_status check_sizes(ssm_dtype dt, int B, int D, int L, int N) {
+    if (dt != SSM_F32 && dt != SSM_BF16) return SSM_ERR_INVALID_ARG;
+    if (B < 0 || D < 0 || L < 0 || N <= 0) return SSM_ERR_INVALID_ARG;
+    if (N > ssm::kMaxN) return SSM_ERR_UNSUPPORTED;
+    if (B > 65535) return SSM_ERR_UNSUPPORTED;
+    if (!fits((long long)D * L) || !fits((long long)N * L)) return SSM_ERR_UNSUPPORTED;
+    return SSM_OK;
+}
+
+size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+// Workspace of one backward call; every region starts on 256 bytes.
+struct BwdWs {
+    size_t fwd, ypre, G, GT, xT, dxT, du, du_b, ddt, hc, pdB, pdC, pdA, pdD, pdbias, total;
+    size_t fwd_bytes;
+};
+// op: 0 single, 1 v1, 2 v2 (u_b given: separate du_b), 3 SS2D
+BwdWs bwd_ws(int op, ssm_dtype dt, int B, int D, int L, int N, bool sep_ub) {
+    const size_t n = (size_t)B * D * L;
+    const int npass = op == 0 ? 1 : op == 3 ? 4 : 2;
+    const int ncg = (D + ssm::bwd::CH - 1) / ssm::bwd::CH;
+    const int nch = (L + ssm::bwd::T - 1) / ssm::bwd::T;
+    BwdWs w{};
+    size_t off = 256;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off += up256(bytes);
+        return o;
+    };
+    const ssm_op fop = op == 0 ? SSM_OP_SELECTIVE_SCAN
+                       : op == 1 ? SSM_OP_BIMAMBA_V1
+                       : op == 2 ? SSM_OP_BIMAMBA_V2
+                                 : SSM_OP_SS2D;
+    w.fwd_bytes = ssm_workspace_bytes(fop, dt, B, D, L, N, 4);
+    w.fwd = take(w.fwd_bytes);
+    w.ypre = take(n * esz(dt));
+    w.G = take(n * 4);
+    w.GT = op == 3 ? take(n * 4) : 0;
+    w.xT = op == 3 ? take(n * esz(dt)) : 0;
+    w.dxT = op == 3 ? take(n * 4) : 0;
+    w.du = take(n * 4);
+    w.du_b = (op == 2 && sep_ub) ? take(n * 4) : 0;
+    w.ddt = take(n * 4 * (op == 2 ? 2 : op == 3 ? 4 : 1));
+    w.hc = take((size_t)B * D * nch * ssm::kMaxN * 4);
+    const size_t part = (size_t)npass * ncg * B * L * ssm::kMaxN * 4;
+    w.pdB = take(part);
+    w.pdC = take(part);
+    w.pdA = take((size_t)npass * B * D * ssm::kMaxN * 4);
+    w.pdD = take((size_t)npass * B * D * 4);
+    w.pdbias = take((size_t)npass * B * D * 4);
+    w.total = off;
+    return w;
+}
+
+int grid1d(long long n) {
+    long long g = (n + 255) / 256;
+    return (int)(g < 1 ? 1 : g > 148 * 16 ? 148 * 16 : g);
+}
+
+ssm_status last_error() {
+    return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+// One scan_bwd_kernel launch (grid: channel groups x batch).
+template <typename IO>
+ssm_status launch_pass(const Pass &ps, int B, int D, int L, int N, int sp, cudaStream_t st) {
+    ssm::bwd::Params P;
+    P.ps = ps;
+    P.B = B;
+    P.D = D;
+    P.L = L;
+    P.N = N;
+    P.nch = (L + ssm::bwd::T - 1) / ssm::bwd::T;
+    P.delta_softplus = sp ? 1 : 0;
+    dim3 grid((D + ssm::bwd::CH - 1) / ssm::bwd::CH, B);
+    auto *kern = &ssm::bwd::scan_bwd_kernel<IO>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             ssm::bwd::kDynBytes) != cudaSuccess) {
+        cudaGetLastError();
+        return SSM_ERR_CUDA;
+    }
+    kern<<<grid, ssm::bwd::NT, ssm::bwd::kDynBytes, st>>>(P);
+    return last_error();
+}
+
+template <typename IO>
+ssm_status gate_bwd(const void *g, const void *z, const void *y, float *G, void *dz, long long n,
+                    cudaStream_t st) {
+    ssm::bwd::gate_bwd_kernel<IO><<<grid1d(n), 256, 0, st>>>(
+        (const IO *)g, (const IO *)z, (const IO *)y, G, (IO *)dz, n);
+    return last_error();
+}
+
+template <typename E>
+ssm_status transpose(const E *in, E *out, int maps, int R, int C, cudaStream_t st) {
+    dim3 grid((C + 31) / 32, (R + 31) / 32, maps < 65535 ? maps : 65535);
+    ssm::bwd::transpose_kernel<E><<<grid, 256, 0, st>>>(in, out, maps, R, C);
+    return last_error();
+}
+
+template <typename IO>
+ssm_status convert(const float *a, const float *b, void *out, long long n, cudaStream_t st) {
+    ssm::bwd::convert_kernel<IO><<<grid1d(n), 256, 0, st>>>(a, b, (IO *)out, n);
+    return last_error();
+}
+
+template <typename IO>
+ssm_status reduce_bc(const float *part, int nslot, int B, int L, int N, void *out,
+                     long long out_bstride, cudaStream_t st) {
+    ssm::bwd::reduce_bc_kernel<IO><<<grid1d((long long)B * L * N), 256, 0, st>>>(
+        part, nslot, B, L, N, (IO *)out, out_bstride);
+    return last_error();
+}
+
+ssm_status reduce_param(const float *part, int nslot, int B, int D, int N, bool per_state,
+                        float *out, cudaStream_t st) {
+    if (out == nullptr) return SSM_OK;
+    const int cols = per_state ? D * ssm::kMaxN : D;
+    ssm::bwd::reduce_param_kernel<<<grid1d(cols), 256, 0, st>>>(part, nslot, B, D, N,
+                                                                per_state ? 1 : 0, out);
+    return last_error();
+}
+
+#define TRY(x)                              \
+    do {                                    \
+        const ssm_status s_ = (x);          \
+        if (s_ != SSM_OK) return s_;        \
+    } while (0)
+
+// The common tail: partials of pass p live at slot offset p * ncg.
+struct Parts {
+    const float *pdB, *pdC, *pdA, *pdD, *pdbias;
+    int ncg, B, D, L, N;
+    const float *dB_slot(int p) const { return pdB + (size_t)p * ncg * B * L * ssm::kMaxN; }
+    const float *dC_slot(int p) const { return pdC + (size_t)p * ncg * B * L * ssm::kMaxN; }
+    const float *dA_slot(int p) const { return pdA + (size_t)p * B * D * ssm::kMaxN; }
+    const float *dD_slot(int p) const { return pdD + (size_t)p * B * D; }
+    const float *db_slot(int p) const { return pdbias + (size_t)p * B * D; }
+};
+
+Parts parts_of(char *ws, const BwdWs &w, int B, int D, int L, int N) {
+    Parts q;
+    q.pdB = (const float *)(ws + w.pdB);
+    q.pdC = (const float *)(ws + w.pdC);
+    q.pdA = (const float *)(ws + w.pdA);
+    q.pdD = (const float *)(ws + w.pdD);
+    q.pdbias = (const float *)(ws + w.pdbias);
+    q.ncg = (D + ssm::bwd::CH - 1) / ssm::bwd::CH;
+    q.B = B;
+    q.D = D;
+    q.L = L;
+    q.N = N;
+    return q;
+}
+
+// Pass p's parameter and scratch pointers into the workspace.
+Pass base_pass(char *ws, const BwdWs &w, int p, int B, int D, int L) {
+    Pass ps{};
+    const int ncg = (D + ssm::bwd::CH - 1) / ssm::bwd::CH;
+    ps.pdB = (float *)(ws + w.pdB) + (size_t)p * ncg * B * L * ssm::kMaxN;
+    ps.pdC = (float *)(ws + w.pdC) + (size_t)p * ncg * B * L * ssm::kMaxN;
+    ps.pdA = (float *)(ws + w.pdA) + (size_t)p * B * D * ssm::kMaxN;
+    ps.pdD = (float *)(ws + w.pdD) + (size_t)p * B * D;
+    ps.pdbias = (float *)(ws + w.pdbias) + (size_t)p * B * D;
+    ps.hc = (float *)(ws + w.hc);
+    ps.G = (const float *)(ws + w.G);
+    ps.gscale = 1.f;
+    return ps;
+}
+
+// ---- the sequence forms (single, v1, v2)
+template <typename IO>
+ssm_status seq_bwd(int op, int B, int D, int L, int N, const void *u, const void *u_b,
+                   const void *delta, const void *delta_b, const float *A, const float *A_b,
+                   const void *Bm, const void *Cm, const void *Bm_b, const void *Cm_b,
+                   const float *Dskip, const float *D_b, const void *z, const float *bias,
+                   const float *bias_b, int sp, float out_scale, const void *dout, void *du,
+                   void *du_b, void *ddelta, void *ddelta_b, float *dA, float *dA_b, void *dB,
+                   void *dC, void *dB_b, void *dC_b, float *dD, float *dD_b, void *dz,
+                   float *dbias, float *dbias_b, char *ws, const BwdWs &w, cudaStream_t st) {
+    const ssm_dtype dt = sizeof(IO) == 4 ? SSM_F32 : SSM_BF16;
+    const long long n = (long long)B * D * L;
+    float *G = (float *)(ws + w.G);
+    float *acc_du = (float *)(ws + w.du);
+    float *acc_dub = w.du_b ? (float *)(ws + w.du_b) : acc_du;
+    float *acc_ddt = (float *)(ws + w.ddt);
+    float *acc_ddtb = op == 2 ? acc_ddt + n : acc_ddt;
+    // fp32 accumulators start at zero
+    if (cudaMemsetAsync(ws + w.du, 0, (size_t)n * 4, st) != cudaSuccess ||
+        (w.du_b && cudaMemsetAsync(ws + w.du_b, 0, (size_t)n * 4, st) != cudaSuccess) ||
+        cudaMemsetAsync(ws + w.ddt, 0, (size_t)n * 4 * (op == 2 ? 2 : 1), st) != cudaSuccess) {
+        cudaGetLastError();
+        return SSM_ERR_CUDA;
+    }
+    // (1) pre-gate output, only needed for dz
+    void *ypre = ws + w.ypre;
+    void *fws = ws + w.fwd;
+    if (z != nullptr) {
+        ssm_stream_t sst = (ssm_stream_t)st;
+        if (op == 0)
+            TRY(selective_scan_fwd(dt, B, D, L, N, u, delta, A, Bm, Cm, Dskip, nullptr, bias, sp,
+                                   ypre, fws, w.fwd_bytes, sst));
+        else if (op == 1)
+            TRY(bimamba_scan_fwd_v1(dt, B, D, L, N, u, delta, A, A_b, Bm, Cm, Dskip, nullptr,
+                                    bias, sp, out_scale, ypre, fws, w.fwd_bytes, sst));
+        else
+            TRY(bimamba_scan_fwd_v2(dt, B, D, L, N, u, u_b, delta, delta_b, A, A_b, Bm, Cm,
+                                    Bm_b, Cm_b, Dskip, D_b, nullptr, bias, bias_b, sp,
+                                    out_scale, ypre, fws, w.fwd_bytes, sst));
+    }
+    // (2) gy and dz
+    TRY(gate_bwd<IO>(dout, z, ypre, G, dz, n, st));
+    // (3) one pass per direction
+    const long long DL = (long long)D * L, NL = (long long)N * L;
+    Pass p0 = base_pass(ws, w, 0, B, D, L);
+    p0.dt = delta;
+    p0.dt_off = 0;
+    p0.dt_bstride = DL;
+    p0.u = u;
+    p0.Bm = Bm;
+    p0.Cm = Cm;
+    p0.bc_off = 0;
+    p0.bc_bstride = NL;
+    p0.A = A;
+    p0.Dskip = Dskip;
+    p0.bias = bias;
+    p0.gscale = op == 0 ? 1.f : out_scale;
+    p0.rev = 0;
+    p0.stream_rev = 0;
+    p0.du = acc_du;
+    p0.ddt = acc_ddt;
+    TRY(launch_pass<IO>(p0, B, D, L, N, sp, st));
+    if (op != 0) {
+        Pass p1 = p0;
+        Pass q = base_pass(ws, w, 1, B, D, L);
+        p1.pdB = q.pdB;
+        p1.pdC = q.pdC;
+        p1.pdA = q.pdA;
+        p1.pdD = q.pdD;
+        p1.pdbias = q.pdbias;
+        p1.dt = op == 2 ? delta_b : delta;
+        p1.u = (op == 2 && u_b) ? u_b : u;
+        p1.Bm = op == 2 ? Bm_b : Bm;
+        p1.Cm = op == 2 ? Cm_b : Cm;
+        p1.A = A_b;
+        p1.Dskip = op == 2 ? D_b : Dskip;
+        p1.bias = op == 2 ? bias_b : bias;
+        p1.rev = 1;
+        p1.du = acc_dub;
+        p1.ddt = acc_ddtb;
+        TRY(launch_pass<IO>(p1, B, D, L, N, sp, st));
+    }
+    // (4) outputs
+    TRY(convert<IO>(acc_du, nullptr, du, n, st));
+    if (w.du_b) TRY(convert<IO>(acc_dub, nullptr, du_b, n, st));
+    TRY(convert<IO>(acc_ddt, nullptr, ddelta, n, st));
+    if (op == 2) TRY(convert<IO>(acc_ddtb, nullptr, ddelta_b, n, st));
+    const Parts q = parts_of(ws, w, B, D, L, N);
+    const int shared_bc = op == 1 ? 2 : 1;      // v1: both passes add into dB, dC
+    TRY(reduce_bc<IO>(q.dB_slot(0), shared_bc * q.ncg, B, L, N, dB, NL, st));
+    TRY(reduce_bc<IO>(q.dC_slot(0), shared_bc * q.ncg, B, L, N, dC, NL, st));
+    if (op == 2) {
+        TRY(reduce_bc<IO>(q.dB_slot(1), q.ncg, B, L, N, dB_b, NL, st));
+        TRY(reduce_bc<IO>(q.dC_slot(1), q.ncg, B, L, N, dC_b, NL, st));
+    }
+    TRY(reduce_param(q.dA_slot(0), 1, B, D, N, true, dA, st));
+    if (op != 0) TRY(reduce_param(q.dA_slot(1), 1, B, D, N, true, dA_b, st));
+    const int shared_par = op == 1 ? 2 : 1;     // v1: D and bias shared
+    if (Dskip) TRY(reduce_param(q.dD_slot(0), shared_par, B, D, N, false, dD, st));
+    TRY(reduce_param(q.db_slot(0), shared_par, B, D, N, false, dbias, st));
+    if (op == 2) {
+        if (D_b) TRY(reduce_param(q.dD_slot(1), 1, B, D, N, false, dD_b, st));
+        TRY(reduce_param(q.db_slot(1), 1, B, D, N, false, dbias_b, st));
+    }
+    return SSM_OK;
+}
+
+// ---- SS2D: directions 0/2 walk x row-major (forward / reversed), 1/3 walk
+// x^T (column-major of x); each direction's delta, B and C are in its scan
+// order, so the reversed directions read them by walk step.
+template <typename IO>
+ssm_status ss2d_bwd_run(int B, int D, int H, int W, int N, const void *x, const void *delta,
+                        const float *A, const void *Bm, const void *Cm, const float *Dskip,
+                        const void *z, const float *bias, int sp, const void *dout, void *dx,
+                        void *ddelta, float *dA, void *dB, void *dC, float *dD, void *dz,
+                        float *dbias, char *ws, const BwdWs &w, cudaStream_t st) {
+    const ssm_dtype dt = sizeof(IO) == 4 ? SSM_F32 : SSM_BF16;
+    const int L = H * W, K = 4;
+    const long long n = (long long)B * D * L;
+    if (cudaMemsetAsync(ws + w.du, 0, (size_t)n * 4, st) != cudaSuccess ||
+        cudaMemsetAsync(ws + w.dxT, 0, (size_t)n * 4, st) != cudaSuccess ||
+        cudaMemsetAsync(ws + w.ddt, 0, (size_t)n * 4 * K, st) != cudaSuccess) {
+        cudaGetLastError();
+        return SSM_ERR_CUDA;
+    }
+    void *ypre = ws + w.ypre;
+    if (z != nullptr)
+        TRY(ss2d_scan_fwd(dt, B, D, H, W, N, K, x, delta, A, Bm, Cm, Dskip, nullptr, bias, sp,
+                          ypre, ws + w.fwd, w.fwd_bytes, (ssm_stream_t)st));
+    float *G = (float *)(ws + w.G), *GT = (float *)(ws + w.GT);
+    IO *xT = (IO *)(ws + w.xT);
+    TRY(gate_bwd<IO>(dout, z, ypre, G, dz, n, st));
+    TRY(transpose<float>(G, GT, B * D, H, W, st));
+    TRY(transpose<IO>((const IO *)x, xT, B * D, H, W, st));
+    const long long DL = (long long)D * L, NL = (long long)N * L;
+    for (int k = 0; k < K; ++k) {
+        Pass ps = base_pass(ws, w, k, B, D, L);
+        const bool col = k == 1 || k == 3;
+        ps.dt = delta;
+        ps.dt_off = k * DL;
+        ps.dt_bstride = K * DL;
+        ps.Bm = Bm;
+        ps.Cm = Cm;
+        ps.bc_off = k * NL;
+        ps.bc_bstride = K * NL;
+        ps.A = A + (long long)k * D * N;
+        ps.Dskip = Dskip ? Dskip + (long long)k * D : nullptr;
+        ps.bias = bias ? bias + (long long)k * D : nullptr;
+        ps.u = col ? (const void *)xT : x;
+        ps.G = col ? GT : G;
+        ps.rev = k >= 2;
+        ps.stream_rev = k >= 2;
+        ps.du = col ? (float *)(ws + w.dxT) : (float *)(ws + w.du);
+        ps.ddt = (float *)(ws + w.ddt);
+        TRY(launch_pass<IO>(ps, B, D, L, N, sp, st));
+    }
+    // dx = (row pair) + transpose back (column pair); G^T's space is free now
+    TRY(transpose<float>((const float *)(ws + w.dxT), GT, B * D, W, H, st));
+    TRY(convert<IO>((const float *)(ws + w.du), GT, dx, n, st));
+    TRY(convert<IO>((const float *)(ws + w.ddt), nullptr, ddelta, n * K, st));
+    const Parts q = parts_of(ws, w, B, D, L, N);
+    for (int k = 0; k < K; ++k) {
+        TRY(reduce_bc<IO>(q.dB_slot(k), q.ncg, B, L, N, (IO *)dB + k * NL, K * NL, st));
+        TRY(reduce_bc<IO>(q.dC_slot(k), q.ncg, B, L, N, (IO *)dC + k * NL, K * NL, st));
+        TRY(reduce_param(q.dA_slot(k), 1, B, D, N, true, dA + (long long)k * D * N, st));
+        if (Dskip) TRY(reduce_param(q.dD_slot(k), 1, B, D, N, false, dD ? dD + k * D : nullptr,
+                                    st));
+        TRY(reduce_param(q.db_slot(k), 1, B, D, N, false, dbias ? dbias + k * D : nullptr, st));
+    }
+    return SSM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ssm_bwd_workspace_bytes(ssm_op op, ssm_dtype dt, int B, int D, int L_or_HW, int N, int K,
+                               int separate_u_b) {
+    if (dt != SSM_F32 && dt != SSM_BF16) return (size_t)-1;
+    if (B < 0 || D < 0 || L_or_HW < 0 || N <= 0 || N > ssm::kMaxN) return (size_t)-1;
+    int o;
+    switch (op) {
+    case SSM_OP_SELECTIVE_SCAN: o = 0; break;
+    case SSM_OP_BIMAMBA_V1: o = 1; break;
+    case SSM_OP_BIMAMBA_V2: o = 2; break;
+    case SSM_OP_SS2D:
+        if (K != 4) return (size_t)-1;
+        o = 3;
+        break;
+    default: return (size_t)-1;
+    }
+    if ((long long)B * D * L_or_HW == 0) return 0;
+    return bwd_ws(o, dt, B, D, L_or_HW, N, separate_u_b != 0).total;
+}
+
+ssm_status selective_scan_bwd(ssm_dtype dt, int B, int D, int L, int N, const void *u,
+                              const void *delta, const float *A, const void *Bm, const void *Cm,
+                              const float *Dskip, const void *z, const float *delta_bias,
+                              int delta_softplus, const void *dout, void *du, void *ddelta,
+                              float *dA, void *dB, void *dC, float *dD, void *dz,
+                              float *ddelta_bias, void *workspace, size_t ws_bytes,
+                              ssm_stream_t stream) {
+    TRY(check_sizes(dt, B, D, L, N));
+    if (!io_ok(dt, u) || !io_ok(dt, delta) || !io_ok(dt, Bm) || !io_ok(dt, Cm) ||
+        !opt_io(dt, z) || !io_ok(dt, dout) || !io_ok(dt, du) || !io_ok(dt, ddelta) ||
+        !io_ok(dt, dB) || !io_ok(dt, dC) || !opt_io(dt, dz) || !f32_ok(A) || !f32_ok(dA) ||
+        !opt_f32(Dskip) || !opt_f32(dD) || !opt_f32(delta_bias) || !opt_f32(ddelta_bias) ||
+        (z != nullptr && dz == nullptr))
+        return SSM_ERR_INVALID_ARG;
+    if ((long long)B * D * L == 0) return SSM_OK;
+    const BwdWs w = bwd_ws(0, dt, B, D, L, N, false);
+    if (workspace == nullptr || ws_bytes < w.total || !aligned(workspace, 16))
+        return SSM_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    char *ws = (char *)workspace;
+    auto run = [&](auto tag) {
+        using IO = decltype(tag);
+        return seq_bwd<IO>(0, B, D, L, N, u, nullptr, delta, nullptr, A, nullptr, Bm, Cm,
+                           nullptr, nullptr, Dskip, nullptr, z, delta_bias, nullptr,
+                           delta_softplus, 1.f, dout, du, nullptr, ddelta, nullptr, dA, nullptr,
+                           dB, dC, nullptr, nullptr, dD, nullptr, dz, ddelta_bias, nullptr, ws,
+                           w, st);
+    };
+    return dt == SSM_F32 ? run(float()) : run(__nv_bfloat16());
+}
+
+ssm_status bimamba_scan_bwd_v1(ssm_dtype dt, int B, int D, int L, int N, const void *u,
+                               const void *delta, const float *A, const float *A_b,
+                               const void *Bm, const void *Cm, const float *Dskip,
+                               const void *z, const float *delta_bias, int delta_softplus,
+                               float out_scale, const void *dout, void *du, void *ddelta,
+                               float *dA, float *dA_b, void *dB, void *dC, float *dD, void *dz,
+                               float *ddelta_bias, void *workspace, size_t ws_bytes,
+                               ssm_stream_t stream) {
+    TRY(check_sizes(dt, B, D, L, N));
+    if (!io_ok(dt, u) || !io_ok(dt, delta) || !io_ok(dt, Bm) || !io_ok(dt, Cm) ||
+        !opt_io(dt, z) || !io_ok(dt, dout) || !io_ok(dt, du) || !io_ok(dt, ddelta) ||
+        !io_ok(dt, dB) || !io_ok(dt, dC) || !opt_io(dt, dz) || !f32_ok(A) || !f32_ok(A_b) ||
+        !f32_ok(dA) || !f32_ok(dA_b) || !opt_f32(Dskip) || !opt_f32(dD) ||
+        !opt_f32(delta_bias) || !opt_f32(ddelta_bias) || (z != nullptr && dz == nullptr))
+        return SSM_ERR_INVALID_ARG;
+    if ((long long)B * D * L == 0) return SSM_OK;
+    const BwdWs w = bwd_ws(1, dt, B, D, L, N, false);
+    if (workspace == nullptr || ws_bytes < w.total || !aligned(workspace, 16))
+        return SSM_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    char *ws = (char *)workspace;
+    auto run = [&](auto tag) {
+        using IO = decltype(tag);
+        return seq_bwd<IO>(1, B, D, L, N, u, nullptr, delta, nullptr, A, A_b, Bm, Cm, nullptr,
+                           nullptr, Dskip, nullptr, z, delta_bias, nullptr, delta_softplus,
+                           out_scale, dout, du, nullptr, ddelta, nullptr, dA, dA_b, dB, dC,
+                           nullptr, nullptr, dD, nullptr, dz, ddelta_bias, nullptr, ws, w, st);
+    };
+    return dt == SSM_F32 ? run(float()) : run(__nv_bfloat16());
+}
+
+ssm_status bimamba_scan_bwd_v2(ssm_dtype dt, int B, int D, int L, int N, const void *u,
+                               const void *u_b, const void *delta, const void *delta_b,
+                               const float *A, const float *A_b, const void *Bm,
+                               const void *Cm, const void *Bm_b, const void *Cm_b,
+                               const float *Dskip, const float *D_b, const void *z,
+                               const float *delta_bias, const float *delta_bias_b,
+                               int delta_softplus, float out_scale, const void *dout, void *du,
+                               void *du_b, void *ddelta, void *ddelta_b, float *dA,
+                               float *dA_b, void *dB, void *dC, void *dB_b, void *dC_b,
+                               float *dD, float *dD_b, void *dz, float *ddelta_bias,
+                               float *ddelta_bias_b, void *workspace, size_t ws_bytes,
+                               ssm_stream_t stream) {
+    TRY(check_sizes(dt, B, D, L, N));
+    if (!io_ok(dt, u) || !opt_io(dt, u_b) || !io_ok(dt, delta) || !io_ok(dt, delta_b) ||
+        !io_ok(dt, Bm) || !io_ok(dt, Cm) || !io_ok(dt, Bm_b) || !io_ok(dt, Cm_b) ||
+        !opt_io(dt, z) || !io_ok(dt, dout) || !io_ok(dt, du) || !io_ok(dt, ddelta) ||
+        !io_ok(dt, ddelta_b) || !io_ok(dt, dB) || !io_ok(dt, dC) || !io_ok(dt, dB_b) ||
+        !io_ok(dt, dC_b) || !opt_io(dt, dz) || !f32_ok(A) || !f32_ok(A_b) || !f32_ok(dA) ||
+        !f32_ok(dA_b) || !opt_f32(Dskip) || !opt_f32(D_b) || !opt_f32(dD) || !opt_f32(dD_b) ||
+        !opt_f32(delta_bias) || !opt_f32(delta_bias_b) || !opt_f32(ddelta_bias) ||
+        !opt_f32(ddelta_bias_b) || (z != nullptr && dz == nullptr) ||
+        (u_b != nullptr && !io_ok(dt, du_b)))
+        return SSM_ERR_INVALID_ARG;
+    if ((long long)B * D * L == 0) return SSM_OK;
+    const BwdWs w = bwd_ws(2, dt, B, D, L, N, u_b != nullptr);
+    if (workspace == nullptr || ws_bytes < w.total || !aligned(workspace, 16))
+        return SSM_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    char *ws = (char *)workspace;
+    auto run = [&](auto tag) {
+        using IO = decltype(tag);
+        return seq_bwd<IO>(2, B, D, L, N, u, u_b, delta, delta_b, A, A_b, Bm, Cm, Bm_b, Cm_b,
+                           Dskip, D_b, z, delta_bias, delta_bias_b, delta_softplus, out_scale,
+                           dout, du, du_b, ddelta, ddelta_b, dA, dA_b, dB, dC, dB_b, dC_b, dD,
+                           dD_b, dz, ddelta_bias, ddelta_bias_b, ws, w, st);
+    };
+    return dt == SSM_F32 ? run(float()) : run(__nv_bfloat16());
+}
+
+ssm_status ss2d_scan_bwd(ssm_dtype dt, int B, int D, int H, int W, int N, int K, const void *x,
+                         const void *delta, const float *A, const void *Bm, const void *Cm,
+                         const float *Dskip, const void *z, const float *delta_bias,
+                         int delta_softplus, const void *dout, void *dx, void *ddelta,
+                         float *dA, void *dB, void *dC, float *dD, void *dz,
+                         float *ddelta_bias, void *workspace, size_t ws_bytes,
+                         ssm_stream_t stream) {
+    if (H < 0 || W < 0) return SSM_ERR_INVALID_ARG;
+    if (K != 4) return SSM_ERR_UNSUPPORTED;
+    if (!fits((long long)H * W)) return SSM_ERR_UNSUPPORTED;
+    const int L = H * W;
+    TRY(check_sizes(dt, B, D, L, N));
+    if (!fits((long long)K * D * L) || !fits((long long)K * N * L)) return SSM_ERR_UNSUPPORTED;
+    if (!io_ok(dt, x) || !io_ok(dt, delta) || !io_ok(dt, Bm) || !io_ok(dt, Cm) ||
+        !opt_io(dt, z) || !io_ok(dt, dout) || !io_ok(dt, dx) || !io_ok(dt, ddelta) ||
+        !io_ok(dt, dB) || !io_ok(dt, dC) || !opt_io(dt, dz) || !f32_ok(A) || !f32_ok(dA) ||
+        !opt_f32(Dskip) || !opt_f32(dD) || !opt_f32(delta_bias) || !opt_f32(ddelta_bias) ||
+        (z != nullptr && dz == nullptr))
+        return SSM_ERR_INVALID_ARG;
+    if ((long long)B * D * L == 0) return SSM_OK;
+    const BwdWs w = bwd_ws(3, dt, B, D, L, N, false);
+    if (workspace == nullptr || ws_bytes < w.total || !aligned(workspace, 16))
+        return SSM_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    char *ws = (char *)workspace;
+    auto run = [&](auto tag) {
+        using IO = decltype(tag);
+        return ss2d_bwd_run<IO>(B, D, H, W, N, x, delta, A, Bm, Cm, Dskip, z, delta_bias,
+                                delta_softplus, dout, dx, ddelta, dA, dB, dC, dD, dz,
+                                ddelta_bias, ws, w, st);
+    };
+    return dt == SSM_F32 ? run(float()) : run(__nv_bfloat16());
+}
+
+}  // extern "C"

@@ -95,3 +95,47 @@ def test_ss2d_requires_four_directions(lib):
     st = lib.ss2d_scan_fwd(1, 1, 1, 4, 4, 16, 2, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None,
                            1, FAKE, FAKE, 1 << 20, None)
     assert st == 2
+
+
+# ---------------------------------------------------------------- backward
+def test_header_declares_the_backward_operations():
+    names = set(declared_functions())
+    assert {"selective_scan_bwd", "bimamba_scan_bwd_v1", "bimamba_scan_bwd_v2", "ss2d_scan_bwd",
+            "ssm_bwd_workspace_bytes"} <= names
+
+
+def test_bwd_workspace_bytes(lib):
+    wb = lib.ssm_bwd_workspace_bytes
+    neg = ctypes.c_size_t(-1).value
+    assert wb(0, 1, 0, 8, 100, 16, 4, 0) == 0                   # empty problem
+    assert wb(0, 7, 1, 8, 100, 16, 4, 0) == neg                  # bad dtype
+    assert wb(0, 1, 1, 8, 100, 17, 4, 0) == neg                  # N > 16
+    assert wb(3, 1, 1, 8, 100, 16, 2, 0) == neg                  # SS2D needs K = 4
+    single = wb(0, 1, 2, 40, 300, 16, 4, 0)
+    v1, v2 = wb(1, 1, 2, 40, 300, 16, 4, 0), wb(2, 1, 2, 40, 300, 16, 4, 0)
+    assert 0 < single < v1 < v2 < wb(2, 1, 2, 40, 300, 16, 4, 1)   # more passes, more scratch
+    # at least the fp32 gradient of u, the chunk states and two partial sets
+    n = 2 * 40 * 300
+    assert single >= 4 * n + 2 * 40 * 10 * 16 * 4 + 2 * 3 * 2 * 300 * 16 * 4
+
+
+def bwd_single(lib, *, dt=1, B=1, D=1, L=8, N=16, u=FAKE, z=None, dz=None, du=FAKE,
+               ws=None, ws_bytes=0):
+    return lib.selective_scan_bwd(dt, B, D, L, N, u, FAKE, FAKE, FAKE, FAKE, None, z, None, 1,
+                                  FAKE, du, FAKE, FAKE, FAKE, FAKE, None, dz, None, ws,
+                                  ws_bytes, None)
+
+
+def test_bwd_invalid_arguments_are_rejected_before_launch(lib):
+    assert bwd_single(lib, N=17) == 2
+    assert bwd_single(lib, L=-1) == 1
+    assert bwd_single(lib, u=None) == 1                     # required input
+    assert bwd_single(lib, du=None) == 1                    # required gradient output
+    assert bwd_single(lib, du=FAKE + 1) == 1                # misaligned bf16 output
+    assert bwd_single(lib, z=FAKE) == 1                     # z given but no dz
+    assert bwd_single(lib, z=FAKE, dz=FAKE) == 4            # no workspace
+    assert bwd_single(lib, B=0) == 0                        # empty: nothing to do
+    # SS2D: K != 4 unsupported
+    st = lib.ss2d_scan_bwd(1, 1, 1, 2, 2, 16, 3, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None,
+                           1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, None, 0, None)
+    assert st == 2
