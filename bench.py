@@ -300,6 +300,10 @@ def run_ours(args):
         if not torch.equal(h_out.to(dev), outs[(n_e2e - 1) % nb]):
             raise RuntimeError("e2e: downloaded result differs from the device result")
 
+    bwd = None
+    if not args.no_backward:
+        bwd = measure_backward(ssm, spec, g, t, dev, stream, max(3, min(args.steps, 20)))
+
     if rank == 0:
         ms = total_ms / args.steps
         hbm_peak, sm_max, peak_kind = peaks()
@@ -347,11 +351,70 @@ def run_ours(args):
         }
         if e2e:
             line["e2e"] = e2e
+        if bwd:
+            # ALU roof of the backward: 16 fp32 operations per element update
+            # (3 to recompute the state, 13 for the adjoint step)
+            bpeak = 148 * 128 * sm_max * 1e6 / 16 / 1e9
+            bach = spec.updates() / (bwd["ms"] * 1e-3) / 1e9
+            bwd["value"] = round(spec.backward_bytes() / (bwd["ms"] * 1e-3) / 1e9, 2)
+            bwd["unit"] = "GB/s"
+            bwd["roofline"] = {"bound": "alu", "achieved": round(bach, 2),
+                               "peak": round(bpeak, 1), "unit": "Gupd/s",
+                               "frac": round(bach / bpeak, 4),
+                               "peak_basis": "148 SMs x 128 fp32 lanes x %.0f MHz / 16 fp32 "
+                                             "ops per update" % sm_max}
+            line["backward"] = bwd
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(spec, args.workload, args.cpu_seconds)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def measure_backward(ssm, spec, g, t, dev, stream, steps):
+    """Time the backward call (gradients of sum(dout * out)) on the same
+    inputs: 3 warm-up calls, then `steps` calls between CUDA events."""
+    import torch
+    gen = torch.Generator().manual_seed(12345)
+    shape = t["x" if spec.op == "ss2d" else "u"].shape
+    dout = torch.randn(shape, generator=gen).to(dtype=g["x" if spec.op == "ss2d" else "u"].dtype,
+                                                device=dev)
+    L = spec.seq_len
+    ws = torch.empty(max(1, ssm.bwd_workspace_bytes(spec.op, dout.dtype, spec.B, spec.D, L,
+                                                    spec.N, spec.K,
+                                                    spec.op == "v2" and not spec.shared_u)),
+                     dtype=torch.uint8, device=dev)
+    sp = spec.delta_softplus
+
+    def once():
+        if spec.op == "single":
+            return ssm.selective_scan_bwd(dout, g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"],
+                                          g["z"], g["delta_bias"], sp, workspace=ws)
+        if spec.op == "v1":
+            return ssm.bimamba_scan_bwd_v1(dout, g["u"], g["delta"], g["A"], g["A_b"], g["B"],
+                                           g["C"], g["D"], g["z"], g["delta_bias"], sp,
+                                           g["out_scale"], workspace=ws)
+        if spec.op == "v2":
+            return ssm.bimamba_scan_bwd_v2(dout, g["u"], g["delta"], g["delta_b"], g["A"],
+                                           g["A_b"], g["B"], g["C"], g["B_b"], g["C_b"], g["D"],
+                                           g["D_b"], g["z"], g["delta_bias"], g["delta_bias_b"],
+                                           g["u_b"], sp, g["out_scale"], workspace=ws)
+        return ssm.ss2d_scan_bwd(dout, g["x"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"],
+                                 g["delta_bias"], sp, workspace=ws)
+
+    for _ in range(3):
+        once()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        once()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"ms_per_call": round(ms, 4), "ms": ms, "steps": steps,
+            "bytes_per_call": spec.backward_bytes(),
+            "elem_updates_per_s": float("%.4g" % (spec.updates() / (ms * 1e-3)))}
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -441,6 +504,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-backward", action="store_true",
+                    help="skip the backward-pass timing (reported under 'backward')")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture")

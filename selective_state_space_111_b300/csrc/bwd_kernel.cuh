@@ -19,8 +19,10 @@
 //                     (chunks of T = 32 steps).  Pass 2 walks the chunks
 //                     backwards: it recomputes the chunk's states in
 //                     registers from the stored start, then runs the adjoint
-//                     recurrence step by step.  Per-position gradients (du,
-//                     ddelta) are summed over the 16 states by shuffles; dB
+//                     recurrence step by step.  Every direction of a call
+//                     runs in the same launch (blockIdx.z) and writes its own
+//                     per-position gradients (du, ddelta: summed over the 16
+//                     states by shuffles); dB
 //                     and dC (summed over channels) go through shared memory
 //                     into one fp32 partial per CTA, reduced afterwards in a
 //                     fixed order, so results are deterministic.
@@ -53,16 +55,17 @@ struct Pass {
     const float *G;            // dLoss/dy (fp32 [B, D, L], position order)
     float gscale;              // this direction's share of G (out_scale)
     int rev, stream_rev;
-    float *du;                 // fp32 [B, D, L], position order, accumulated
-    float *ddt;                // fp32, indexed like dt, accumulated
+    float *du;                 // fp32 [B, D, L], position order (this pass's own)
+    float *ddt;                // fp32, indexed like dt (this pass's own)
     float *pdB, *pdC;          // this pass's partials [ncg][B][L][16] (stream index)
     float *pdA;                // [B][D][16]
     float *pdD, *pdbias;       // [B][D]
-    float *hc;                 // chunk-start states [B][D][nch][16]
+    float *hc;                 // chunk-start states [B][D][nch][16] (this pass's own)
 };
 
+constexpr int kMaxPass = 4;
 struct Params {
-    Pass ps;
+    Pass ps[kMaxPass];         // one per direction; blockIdx.z selects it
     int B, D, L, N, nch;
     int delta_softplus;
 };
@@ -73,7 +76,7 @@ __device__ __forceinline__ float sigmoid_f(float x) {
 constexpr int kDynBytes = 2 * NWARP * T * kMaxN * (int)sizeof(float);
 
 template <typename IO>
-__global__ void __launch_bounds__(NT)
+__global__ void __launch_bounds__(NT, 3)
 scan_bwd_kernel(const Params P) {
     __shared__ float sD[CH][T + 1], sS[CH][T + 1], sU[CH][T + 1], sG[CH][T + 1];
     __shared__ float sB[T][kMaxN + 1], sC[T][kMaxN + 1];
@@ -83,7 +86,7 @@ scan_bwd_kernel(const Params P) {
     float (*sPB)[T][kMaxN] = reinterpret_cast<float (*)[T][kMaxN]>(dyn);
     float (*sPC)[T][kMaxN] = reinterpret_cast<float (*)[T][kMaxN]>(dyn + NWARP * T * kMaxN);
 
-    const Pass &ps = P.ps;
+    const Pass &ps = P.ps[blockIdx.z];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int ch = tid / kMaxN, n = tid % kMaxN;
     const int b = blockIdx.y, d0 = blockIdx.x * CH, d = d0 + ch;
@@ -200,14 +203,14 @@ scan_bwd_kernel(const Params P) {
             }
         }
         __syncthreads();
-        // per-position gradients, accumulated (several directions may add)
+        // per-position gradients of this direction
         for (int i = tid; i < CH * T; i += NT) {
             const int cc = i / T, j = i % T, w = c * T + j, dd = d0 + cc;
             if (w < L && dd < D) {
                 const long long prow = ((long long)b * D + dd) * L;
-                ps.du[prow + pos(w)] += sDu[cc][j];
+                ps.du[prow + pos(w)] = sDu[cc][j];
                 const float gx = P.delta_softplus ? sDd[cc][j] * sS[cc][j] : sDd[cc][j];
-                ps.ddt[ps.dt_off + b * ps.dt_bstride + (long long)dd * L + sidx(w)] += gx;
+                ps.ddt[ps.dt_off + b * ps.dt_bstride + (long long)dd * L + sidx(w)] = gx;
             }
         }
         // dB, dC partial of this CTA: sum over its warps
@@ -278,13 +281,17 @@ __global__ void transpose_kernel(const E *__restrict__ in, E *__restrict__ out, 
     }
 }
 
-// out (I/O) = a [+ b] elementwise, fp32 inputs
-template <typename IO>
+// out (I/O or fp32) = a [+ b] [+ c] elementwise, fp32 inputs
+template <typename E>
 __global__ void convert_kernel(const float *__restrict__ a, const float *__restrict__ b,
-                               IO *__restrict__ out, long long n) {
+                               const float *__restrict__ c, E *__restrict__ out, long long n) {
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
-         i += (long long)gridDim.x * blockDim.x)
-        out[i] = from_f32<IO>(b ? a[i] + b[i] : a[i]);
+         i += (long long)gridDim.x * blockDim.x) {
+        float v = a[i];
+        if (b) v += b[i];
+        if (c) v += c[i];
+        out[i] = from_f32<E>(v);
+    }
 }
 
 // dB[b][n][s] (I/O, at out + b * out_bstride) = sum over the nslot partials

@@ -2,10 +2,10 @@
 //
 // Each call: (1) recomputes the pre-gate output y with the forward entry
 // point (only when z is given), (2) gy = dout * silu(z) and dz, (3) one
-// scan_bwd_kernel launch per direction, which accumulates the per-position
-// gradients in fp32 and leaves per-CTA partial sums of the parameter
-// gradients, (4) fixed-order reductions of the partials and conversion to
-// the output dtypes.  Nothing is allocated; everything lives in the
+// scan_bwd_kernel launch for all directions, each writing its own fp32
+// per-position gradients and per-CTA partial sums of the parameter
+// gradients, (4) fixed-order sums and reductions, and conversion to the
+// output dtypes.  Nothing is allocated; everything lives in the
 // caller's workspace (ssm_bwd_workspace_bytes).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -40,11 +40,13 @@ size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 // Workspace of one backward call; every region starts on 256 bytes.
 struct BwdWs {
-    size_t fwd, ypre, G, GT, xT, dxT, du, du_b, ddt, hc, pdB, pdC, pdA, pdD, pdbias, total;
+    size_t fwd, ypre, G, GT, xT, du, ddt, hc, pdB, pdC, pdA, pdD, pdbias, total;
     size_t fwd_bytes;
 };
-// op: 0 single, 1 v1, 2 v2 (u_b given: separate du_b), 3 SS2D
+// op: 0 single, 1 v1, 2 v2, 3 SS2D.  du and ddt hold one fp32 map per
+// direction (SS2D's ddt is [B][4][D][L], like delta).
 BwdWs bwd_ws(int op, ssm_dtype dt, int B, int D, int L, int N, bool sep_ub) {
+    (void)sep_ub;
     const size_t n = (size_t)B * D * L;
     const int npass = op == 0 ? 1 : op == 3 ? 4 : 2;
     const int ncg = (D + ssm::bwd::CH - 1) / ssm::bwd::CH;
@@ -66,11 +68,10 @@ BwdWs bwd_ws(int op, ssm_dtype dt, int B, int D, int L, int N, bool sep_ub) {
     w.G = take(n * 4);
     w.GT = op == 3 ? take(n * 4) : 0;
     w.xT = op == 3 ? take(n * esz(dt)) : 0;
-    w.dxT = op == 3 ? take(n * 4) : 0;
-    w.du = take(n * 4);
-    w.du_b = (op == 2 && sep_ub) ? take(n * 4) : 0;
-    w.ddt = take(n * 4 * (op == 2 ? 2 : op == 3 ? 4 : 1));
-    w.hc = take((size_t)B * D * nch * ssm::kMaxN * 4);
+    w.du = take(n * 4 * npass);
+    w.ddt = take(n * 4 * npass);
+    // chunk-start states: one region per direction (they run concurrently)
+    w.hc = take((size_t)npass * B * D * nch * ssm::kMaxN * 4);
     const size_t part = (size_t)npass * ncg * B * L * ssm::kMaxN * 4;
     w.pdB = take(part);
     w.pdC = take(part);
@@ -90,18 +91,20 @@ ssm_status last_error() {
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
-// One scan_bwd_kernel launch (grid: channel groups x batch).
+// One scan_bwd_kernel launch for all directions (grid: channel groups x
+// batch x directions).
 template <typename IO>
-ssm_status launch_pass(const Pass &ps, int B, int D, int L, int N, int sp, cudaStream_t st) {
-    ssm::bwd::Params P;
-    P.ps = ps;
+ssm_status launch_passes(const Pass *ps, int npass, int B, int D, int L, int N, int sp,
+                         cudaStream_t st) {
+    ssm::bwd::Params P{};
+    for (int k = 0; k < npass; ++k) P.ps[k] = ps[k];
     P.B = B;
     P.D = D;
     P.L = L;
     P.N = N;
     P.nch = (L + ssm::bwd::T - 1) / ssm::bwd::T;
     P.delta_softplus = sp ? 1 : 0;
-    dim3 grid((D + ssm::bwd::CH - 1) / ssm::bwd::CH, B);
+    dim3 grid((D + ssm::bwd::CH - 1) / ssm::bwd::CH, B, npass);
     auto *kern = &ssm::bwd::scan_bwd_kernel<IO>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              ssm::bwd::kDynBytes) != cudaSuccess) {
@@ -127,9 +130,10 @@ ssm_status transpose(const E *in, E *out, int maps, int R, int C, cudaStream_t s
     return last_error();
 }
 
-template <typename IO>
-ssm_status convert(const float *a, const float *b, void *out, long long n, cudaStream_t st) {
-    ssm::bwd::convert_kernel<IO><<<grid1d(n), 256, 0, st>>>(a, b, (IO *)out, n);
+template <typename E>
+ssm_status convert(const float *a, const float *b, const float *c, void *out, long long n,
+                   cudaStream_t st) {
+    ssm::bwd::convert_kernel<E><<<grid1d(n), 256, 0, st>>>(a, b, c, (E *)out, n);
     return last_error();
 }
 
@@ -191,7 +195,8 @@ Pass base_pass(char *ws, const BwdWs &w, int p, int B, int D, int L) {
     ps.pdA = (float *)(ws + w.pdA) + (size_t)p * B * D * ssm::kMaxN;
     ps.pdD = (float *)(ws + w.pdD) + (size_t)p * B * D;
     ps.pdbias = (float *)(ws + w.pdbias) + (size_t)p * B * D;
-    ps.hc = (float *)(ws + w.hc);
+    const int nch = (L + ssm::bwd::T - 1) / ssm::bwd::T;
+    ps.hc = (float *)(ws + w.hc) + (size_t)p * B * D * nch * ssm::kMaxN;
     ps.G = (const float *)(ws + w.G);
     ps.gscale = 1.f;
     return ps;
@@ -210,17 +215,8 @@ ssm_status seq_bwd(int op, int B, int D, int L, int N, const void *u, const void
     const ssm_dtype dt = sizeof(IO) == 4 ? SSM_F32 : SSM_BF16;
     const long long n = (long long)B * D * L;
     float *G = (float *)(ws + w.G);
-    float *acc_du = (float *)(ws + w.du);
-    float *acc_dub = w.du_b ? (float *)(ws + w.du_b) : acc_du;
-    float *acc_ddt = (float *)(ws + w.ddt);
-    float *acc_ddtb = op == 2 ? acc_ddt + n : acc_ddt;
-    // fp32 accumulators start at zero
-    if (cudaMemsetAsync(ws + w.du, 0, (size_t)n * 4, st) != cudaSuccess ||
-        (w.du_b && cudaMemsetAsync(ws + w.du_b, 0, (size_t)n * 4, st) != cudaSuccess) ||
-        cudaMemsetAsync(ws + w.ddt, 0, (size_t)n * 4 * (op == 2 ? 2 : 1), st) != cudaSuccess) {
-        cudaGetLastError();
-        return SSM_ERR_CUDA;
-    }
+    float *du0 = (float *)(ws + w.du), *du1 = du0 + n;      // per direction
+    float *dt0 = (float *)(ws + w.ddt), *dt1 = dt0 + n;
     // (1) pre-gate output, only needed for dz
     void *ypre = ws + w.ypre;
     void *fws = ws + w.fwd;
@@ -256,9 +252,9 @@ ssm_status seq_bwd(int op, int B, int D, int L, int N, const void *u, const void
     p0.gscale = op == 0 ? 1.f : out_scale;
     p0.rev = 0;
     p0.stream_rev = 0;
-    p0.du = acc_du;
-    p0.ddt = acc_ddt;
-    TRY(launch_pass<IO>(p0, B, D, L, N, sp, st));
+    p0.du = du0;
+    p0.ddt = dt0;
+    Pass pp[2] = {p0, p0};
     if (op != 0) {
         Pass p1 = p0;
         Pass q = base_pass(ws, w, 1, B, D, L);
@@ -267,6 +263,7 @@ ssm_status seq_bwd(int op, int B, int D, int L, int N, const void *u, const void
         p1.pdA = q.pdA;
         p1.pdD = q.pdD;
         p1.pdbias = q.pdbias;
+        p1.hc = q.hc;
         p1.dt = op == 2 ? delta_b : delta;
         p1.u = (op == 2 && u_b) ? u_b : u;
         p1.Bm = op == 2 ? Bm_b : Bm;
@@ -275,15 +272,17 @@ ssm_status seq_bwd(int op, int B, int D, int L, int N, const void *u, const void
         p1.Dskip = op == 2 ? D_b : Dskip;
         p1.bias = op == 2 ? bias_b : bias;
         p1.rev = 1;
-        p1.du = acc_dub;
-        p1.ddt = acc_ddtb;
-        TRY(launch_pass<IO>(p1, B, D, L, N, sp, st));
+        p1.du = du1;
+        p1.ddt = dt1;
+        pp[1] = p1;
     }
-    // (4) outputs
-    TRY(convert<IO>(acc_du, nullptr, du, n, st));
-    if (w.du_b) TRY(convert<IO>(acc_dub, nullptr, du_b, n, st));
-    TRY(convert<IO>(acc_ddt, nullptr, ddelta, n, st));
-    if (op == 2) TRY(convert<IO>(acc_ddtb, nullptr, ddelta_b, n, st));
+    TRY(launch_passes<IO>(pp, op == 0 ? 1 : 2, B, D, L, N, sp, st));
+    // (4) outputs: shared tensors sum both branches' gradients
+    const bool shared_u = op == 1 || (op == 2 && u_b == nullptr);
+    TRY(convert<IO>(du0, shared_u ? du1 : nullptr, nullptr, du, n, st));
+    if (op == 2 && u_b != nullptr) TRY(convert<IO>(du1, nullptr, nullptr, du_b, n, st));
+    TRY(convert<IO>(dt0, op == 1 ? dt1 : nullptr, nullptr, ddelta, n, st));
+    if (op == 2) TRY(convert<IO>(dt1, nullptr, nullptr, ddelta_b, n, st));
     const Parts q = parts_of(ws, w, B, D, L, N);
     const int shared_bc = op == 1 ? 2 : 1;      // v1: both passes add into dB, dC
     TRY(reduce_bc<IO>(q.dB_slot(0), shared_bc * q.ncg, B, L, N, dB, NL, st));
@@ -316,12 +315,6 @@ ssm_status ss2d_bwd_run(int B, int D, int H, int W, int N, const void *x, const 
     const ssm_dtype dt = sizeof(IO) == 4 ? SSM_F32 : SSM_BF16;
     const int L = H * W, K = 4;
     const long long n = (long long)B * D * L;
-    if (cudaMemsetAsync(ws + w.du, 0, (size_t)n * 4, st) != cudaSuccess ||
-        cudaMemsetAsync(ws + w.dxT, 0, (size_t)n * 4, st) != cudaSuccess ||
-        cudaMemsetAsync(ws + w.ddt, 0, (size_t)n * 4 * K, st) != cudaSuccess) {
-        cudaGetLastError();
-        return SSM_ERR_CUDA;
-    }
     void *ypre = ws + w.ypre;
     if (z != nullptr)
         TRY(ss2d_scan_fwd(dt, B, D, H, W, N, K, x, delta, A, Bm, Cm, Dskip, nullptr, bias, sp,
@@ -332,6 +325,8 @@ ssm_status ss2d_bwd_run(int B, int D, int H, int W, int N, const void *x, const 
     TRY(transpose<float>(G, GT, B * D, H, W, st));
     TRY(transpose<IO>((const IO *)x, xT, B * D, H, W, st));
     const long long DL = (long long)D * L, NL = (long long)N * L;
+    float *du = (float *)(ws + w.du);                 // [4][B][D][L], one map per direction
+    Pass pp[4];
     for (int k = 0; k < K; ++k) {
         Pass ps = base_pass(ws, w, k, B, D, L);
         const bool col = k == 1 || k == 3;
@@ -349,14 +344,17 @@ ssm_status ss2d_bwd_run(int B, int D, int H, int W, int N, const void *x, const 
         ps.G = col ? GT : G;
         ps.rev = k >= 2;
         ps.stream_rev = k >= 2;
-        ps.du = col ? (float *)(ws + w.dxT) : (float *)(ws + w.du);
+        ps.du = du + k * n;
         ps.ddt = (float *)(ws + w.ddt);
-        TRY(launch_pass<IO>(ps, B, D, L, N, sp, st));
+        pp[k] = ps;
     }
-    // dx = (row pair) + transpose back (column pair); G^T's space is free now
-    TRY(transpose<float>((const float *)(ws + w.dxT), GT, B * D, W, H, st));
-    TRY(convert<IO>((const float *)(ws + w.du), GT, dx, n, st));
-    TRY(convert<IO>((const float *)(ws + w.ddt), nullptr, ddelta, n * K, st));
+    TRY(launch_passes<IO>(pp, K, B, D, L, N, sp, st));
+    // dx = row pair (0, 2) + the column pair (1, 3) transposed back; G^T's
+    // space is free now
+    TRY(convert<float>(du + n, du + 3 * n, nullptr, du + n, n, st));
+    TRY(transpose<float>(du + n, GT, B * D, W, H, st));
+    TRY(convert<IO>(du, du + 2 * n, GT, dx, n, st));
+    TRY(convert<IO>((const float *)(ws + w.ddt), nullptr, nullptr, ddelta, n * K, st));
     const Parts q = parts_of(ws, w, B, D, L, N);
     for (int k = 0; k < K; ++k) {
         TRY(reduce_bc<IO>(q.dB_slot(k), q.ncg, B, L, N, (IO *)dB + k * NL, K * NL, st));

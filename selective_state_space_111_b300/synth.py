@@ -62,6 +62,21 @@ class Spec:
         """Element updates: one (b, d, n, t, direction) recurrence step each."""
         return self.directions * self.B * self.D * self.seq_len * self.N
 
+    def backward_bytes(self) -> int:
+        """The backward pass's algorithmic bytes: every forward input and the
+        output gradient read once, every input's gradient written once (the
+        fp32 parameter gradients A, D, bias are ignored)."""
+        e = 4 if self.io == "f32" else 2
+        BD, L, N = self.B * self.D, self.seq_len, self.N
+        z = 1 if self.gate else 0
+        if self.op in ("single", "v1"):
+            rows, bc = 2 + z, 2          # u, delta (+ z); B, C
+        elif self.op == "v2":
+            rows, bc = 3 + z + (0 if self.shared_u else 1), 4
+        else:
+            rows, bc = 1 + z + self.K, 2 * self.K
+        return e * (BD * L * (2 * rows + 1) + self.B * L * N * 2 * bc)
+
     def algorithmic_bytes(self) -> int:
         """Each I/O tensor read once and y written once (A, D, bias ignored)."""
         e = 4 if self.io == "f32" else 2
