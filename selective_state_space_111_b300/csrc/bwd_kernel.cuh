@@ -27,7 +27,8 @@
 //                     into one fp32 partial per CTA, reduced afterwards in a
 //                     fixed order, so results are deterministic.
 //   gate_bwd_kernel   gy = g * silu(z), dz = g * y * silu'(z).
-//   reduce kernels    partial sums -> dA, dD, dbias (fp32), dB, dC (I/O dtype).
+//   reduce kernels    partial sums -> dA (fp32), dB, dC (I/O dtype); dD and
+//                     dbias as channel sums of the fp32 maps (G * u, ddt).
 #pragma once
 
 #include "scan_ops.cuh"
@@ -59,7 +60,6 @@ struct Pass {
     float *ddt;                // fp32, indexed like dt (this pass's own)
     float *pdB, *pdC;          // this pass's partials [ncg][B][L][16] (stream index)
     float *pdA;                // [B][D][16]
-    float *pdD, *pdbias;       // [B][D]
     float *hc;                 // chunk-start states [B][D][nch][16] (this pass's own)
 };
 
@@ -73,18 +73,45 @@ struct Params {
 __device__ __forceinline__ float sigmoid_f(float x) {
     return 1.f / (1.f + expf(-x));
 }
-constexpr int kDynBytes = 2 * NWARP * T * kMaxN * (int)sizeof(float);
+// dynamic shared memory: dB, dC partials per warp, then the chunk's
+// recomputed states (step-major: thread-contiguous rows, no bank conflicts)
+constexpr int kPartFloats = NWARP * kMaxN * (T + 4);
+constexpr int kDynBytes = (2 * kPartFloats + T * NT) * (int)sizeof(float);
+
+// Sum of 8 values over the 16 lanes of a half-warp, by halving exchanges:
+// after the three halving levels lane l holds value (l>>3&1)*4 + (l>>2&1)*2
+// + (l>>1&1) summed over 8 lanes, and the last exchange completes the sum
+// (lanes l and l^1 then hold the same total).
+__device__ __forceinline__ float half_warp_sum8(const float (&v)[8], int lane) {
+    const bool b8 = lane & 8, b4 = lane & 4, b2 = lane & 2;
+    float w[4], x[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float send = b8 ? v[i] : v[i + 4];
+        w[i] = (b8 ? v[i + 4] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float send = b4 ? w[i] : w[i + 2];
+        x[i] = (b4 ? w[i + 2] : w[i]) + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+    const float send = b2 ? x[0] : x[1];
+    const float y = (b2 ? x[1] : x[0]) + __shfl_xor_sync(0xffffffffu, send, 2);
+    return y + __shfl_xor_sync(0xffffffffu, y, 1);
+}
 
 template <typename IO>
-__global__ void __launch_bounds__(NT, 3)
+__global__ void __launch_bounds__(NT, 2)
 scan_bwd_kernel(const Params P) {
-    __shared__ float sD[CH][T + 1], sS[CH][T + 1], sU[CH][T + 1], sG[CH][T + 1];
-    __shared__ float sB[T][kMaxN + 1], sC[T][kMaxN + 1];
+    constexpr int TP = T + 4;                  // padded rows: 16-byte aligned, banks spread
+    __shared__ __align__(16) float sD[CH][TP], sU[CH][TP], sG[CH][TP], sS[CH][TP];
+    __shared__ __align__(16) float sBt[kMaxN][TP], sCt[kMaxN][TP];
     __shared__ float sDu[CH][T + 1], sDd[CH][T + 1];
-    // per-warp dB, dC partials of a chunk (dynamic: kDynBytes)
-    extern __shared__ float dyn[];
-    float (*sPB)[T][kMaxN] = reinterpret_cast<float (*)[T][kMaxN]>(dyn);
-    float (*sPC)[T][kMaxN] = reinterpret_cast<float (*)[T][kMaxN]>(dyn + NWARP * T * kMaxN);
+    // per-warp dB, dC partials of a chunk, [warp][state][step] (dynamic: kDynBytes)
+    extern __shared__ __align__(16) float dyn[];
+    float (*sPB)[kMaxN][TP] = reinterpret_cast<float (*)[kMaxN][TP]>(dyn);
+    float (*sPC)[kMaxN][TP] = reinterpret_cast<float (*)[kMaxN][TP]>(dyn + kPartFloats);
+    float (*sH)[NT] = reinterpret_cast<float (*)[NT]>(dyn + 2 * kPartFloats);
 
     const Pass &ps = P.ps[blockIdx.z];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -94,7 +121,6 @@ scan_bwd_kernel(const Params P) {
     const bool cvalid = d < D, valid = cvalid && n < N;
     const float A2 = valid ? ps.A[(long long)d * N + n] * kLog2e : 0.f;
     const float Av = valid ? ps.A[(long long)d * N + n] : 0.f;
-    const float Dd = (cvalid && ps.Dskip) ? ps.Dskip[d] : 0.f;
     const IO *dtp = (const IO *)ps.dt + ps.dt_off + b * ps.dt_bstride;
     const IO *bp = (const IO *)ps.Bm + ps.bc_off + b * ps.bc_bstride;
     const IO *cp = (const IO *)ps.Cm + ps.bc_off + b * ps.bc_bstride;
@@ -103,112 +129,164 @@ scan_bwd_kernel(const Params P) {
 
     auto pos = [&](int w) { return ps.rev ? L - 1 - w : w; };
     auto sidx = [&](int w) { return ps.stream_rev ? w : pos(w); };
-    // chunk c of every input into shared memory (zeros beyond L and D)
-    auto stage = [&](int c, bool full) {
-        for (int i = tid; i < CH * T; i += NT) {
-            const int cc = i / T, j = i % T, w = c * T + j, dd = d0 + cc;
-            float dl = 0.f, sg = 1.f, uu = 0.f, gg = 0.f;
+    // Chunk staging, software-pipelined: fetch() loads this thread's share
+    // of chunk c (2 of the CH x T per-channel values, 2 of the 16 x T B/C
+    // values) into registers; commit() transforms and stores it.  The next
+    // chunk is fetched before the current one is computed.
+    constexpr int PER = CH * T / NT;              // per-channel values per thread
+    static_assert(PER * NT == CH * T && kMaxN * T == CH * T, "staging split");
+    float rdt[PER], ru[PER], rg[PER], rb[PER], rc[PER];
+    auto fetch = [&](int c, bool full) {
+#pragma unroll
+        for (int r = 0; r < PER; ++r) {
+            const int i = tid + r * NT, cc = i / T, j = i % T, w = c * T + j, dd = d0 + cc;
+            const bool ok = w < L && dd < D;
+            rdt[r] = ok ? to_f32(dtp[(long long)dd * L + sidx(w)]) : 0.f;
+            ru[r] = ok ? to_f32(up[((long long)b * D + dd) * L + pos(w)]) : 0.f;
+            rg[r] = (ok && full) ? ps.G[((long long)b * D + dd) * L + pos(w)] : 0.f;
+            const int nn = i / T;
+            const bool okb = w < L && nn < N;
+            const long long o = (long long)nn * L + (okb ? sidx(w) : 0);
+            rb[r] = okb ? to_f32(bp[o]) : 0.f;
+            rc[r] = (okb && full) ? to_f32(cp[o]) : 0.f;
+        }
+    };
+    auto commit = [&](int c) {
+#pragma unroll
+        for (int r = 0; r < PER; ++r) {
+            const int i = tid + r * NT, cc = i / T, j = i % T, w = c * T + j, dd = d0 + cc;
+            float dl = 0.f, sg = 1.f;
             if (w < L && dd < D) {
-                const float x = to_f32(dtp[(long long)dd * L + sidx(w)]) +
-                                (ps.bias ? ps.bias[dd] : 0.f);
+                const float x = rdt[r] + (ps.bias ? ps.bias[dd] : 0.f);
                 if (P.delta_softplus) {
                     dl = x > 20.f ? x : log1pf(expf(x));
                     sg = sigmoid_f(x);
                 } else {
                     dl = x;
                 }
-                uu = to_f32(up[((long long)b * D + dd) * L + pos(w)]);
-                if (full) gg = ps.gscale * ps.G[((long long)b * D + dd) * L + pos(w)];
             }
             sD[cc][j] = dl;
             sS[cc][j] = sg;
-            sU[cc][j] = uu;
-            sG[cc][j] = gg;
-        }
-        for (int i = tid; i < kMaxN * T; i += NT) {
-            const int nn = i / T, j = i % T, w = c * T + j;
-            const bool ok = w < L && nn < N;
-            const long long o = (long long)nn * L + (ok ? sidx(w) : 0);
-            sB[j][nn] = ok ? to_f32(bp[o]) : 0.f;
-            if (full) sC[j][nn] = ok ? to_f32(cp[o]) : 0.f;
+            sU[cc][j] = ru[r];
+            sG[cc][j] = ps.gscale * rg[r];
+            sBt[cc][j] = rb[r];                   // i / T is the state index here
+            sCt[cc][j] = rc[r];
         }
     };
 
     // ---- pass 1: states at the chunk starts
     float h = 0.f;
+    fetch(0, false);
     for (int c = 0; c < nch; ++c) {
         if (cvalid) hcp[(long long)c * kMaxN] = h;
-        stage(c, false);
+        commit(c);
         __syncthreads();
+        if (c + 1 < nch) fetch(c + 1, false);
         const int len = min(T, L - c * T);
         for (int j = 0; j < len; ++j) {
             const float dl = sD[ch][j];
-            h = fmaf(ex2_approx(dl * A2), h, dl * sB[j][n] * sU[ch][j]);
+            h = fmaf(ex2_approx(dl * A2), h, dl * sBt[n][j] * sU[ch][j]);
         }
         __syncthreads();
     }
 
-    // ---- pass 2: adjoint, chunks in reverse
-    float Gc = 0.f, dA = 0.f, dDs = 0.f, dbs = 0.f;
-    for (int c = nch - 1; c >= 0; --c) {
-        stage(c, true);
-        __syncthreads();
-        const int len = min(T, L - c * T);
-        const float h0 = cvalid ? hcp[(long long)c * kMaxN] : 0.f;
-        float hr[T];
+    // ---- pass 2: adjoint, chunks in reverse; steps in groups of 4
+    float Gc = 0.f, dA = 0.f;
+    // FULL: a whole chunk (no step beyond L)
+    auto chunk = [&](auto FULL, int len, float h0) {
+        constexpr bool F = decltype(FULL)::value;
         {
             float hh = h0;
+#pragma unroll 1
+            for (int j4 = 0; j4 < T / 4; ++j4) {
+                const float4 d4 = *(const float4 *)&sD[ch][4 * j4];
+                const float4 u4 = *(const float4 *)&sU[ch][4 * j4];
+                const float4 b4 = *(const float4 *)&sBt[n][4 * j4];
+                const float dv[4] = {d4.x, d4.y, d4.z, d4.w}, uv[4] = {u4.x, u4.y, u4.z, u4.w};
+                const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-            for (int j = 0; j < T; ++j) {
-                if (j < len) {
-                    const float dl = sD[ch][j];
-                    hh = fmaf(ex2_approx(dl * A2), hh, dl * sB[j][n] * sU[ch][j]);
+                for (int k = 0; k < 4; ++k) {
+                    if (F || 4 * j4 + k < len)
+                        hh = fmaf(ex2_approx(dv[k] * A2), hh, dv[k] * bv[k] * uv[k]);
+                    sH[4 * j4 + k][tid] = hh;
                 }
-                hr[j] = hh;
             }
         }
+        // h_j of the step being undone; the reverse sweep loads h_{j-1} once,
+        // as the previous state of step j and the state of step j - 1
+        float hcur = F ? sH[T - 1][tid] : 0.f;
+        if (!F) {
+            for (int j = T - 1; j >= 0; --j)
+                if (j == len - 1) hcur = sH[j][tid];
+        }
+#pragma unroll 1
+        for (int j4 = T / 4 - 1; j4 >= 0; --j4) {
+            const int j0 = 4 * j4;
+            if (!F && j0 >= len) continue;             // uniform over the CTA
+            const float4 d4 = *(const float4 *)&sD[ch][j0];
+            const float4 u4 = *(const float4 *)&sU[ch][j0];
+            const float4 g4 = *(const float4 *)&sG[ch][j0];
+            const float4 b4 = *(const float4 *)&sBt[n][j0];
+            const float4 c4 = *(const float4 *)&sCt[n][j0];
+            const float dv[4] = {d4.x, d4.y, d4.z, d4.w}, uv[4] = {u4.x, u4.y, u4.z, u4.w};
+            const float gv[4] = {g4.x, g4.y, g4.z, g4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w};
+            const float cv[4] = {c4.x, c4.y, c4.z, c4.w};
+            float red[8], dBp[4], dCp[4];     // red: du of the 4 steps, then ddelta
 #pragma unroll
-        for (int j = T - 1; j >= 0; --j) {
-            if (j < len) {
-                const float dl = sD[ch][j], uu = sU[ch][j], gy = sG[ch][j];
-                const float bb = sB[j][n], cc = sC[j][n];
+            for (int k = 3; k >= 0; --k) {
+                const int j = j0 + k;
+                if (!F && j >= len) {
+                    red[k] = red[4 + k] = dBp[k] = dCp[k] = 0.f;
+                    continue;
+                }
+                const float dl = dv[k], uu = uv[k], gy = gv[k], bb = bv[k];
                 const float a = ex2_approx(dl * A2);
-                const float hp = j > 0 ? hr[j - 1] : h0;
-                const float g = fmaf(gy, cc, Gc);
-                float dCp = gy * hr[j];
-                float dBp = g * dl * uu;
-                float dup = g * dl * bb;
-                float ddp = g * fmaf(hp * a, Av, bb * uu);
+                const float hp = j > 0 ? sH[j - 1][tid] : h0;
+                const float g = fmaf(gy, cv[k], Gc);
+                dCp[k] = gy * hcur;
+                hcur = hp;
+                dBp[k] = g * dl * uu;
+                red[k] = g * dl * bb;
+                red[4 + k] = g * fmaf(hp * a, Av, bb * uu);
                 dA = fmaf(g * hp * a, dl, dA);
                 Gc = a * g;
-                // sums over the 16 states of the channel
-#pragma unroll
-                for (int o = kMaxN / 2; o >= 1; o >>= 1) {
-                    dup += __shfl_xor_sync(0xffffffffu, dup, o);
-                    ddp += __shfl_xor_sync(0xffffffffu, ddp, o);
-                }
-                // sums over the warp's two channels
-                dBp += __shfl_xor_sync(0xffffffffu, dBp, 16);
-                dCp += __shfl_xor_sync(0xffffffffu, dCp, 16);
-                if (n == 0) {
-                    sDu[ch][j] = fmaf(gy, Dd, dup);
-                    sDd[ch][j] = ddp;
-                    dDs = fmaf(gy, uu, dDs);
-                    dbs += P.delta_softplus ? ddp * sS[ch][j] : ddp;
-                }
-                if (lane < 16) {
-                    sPB[warp][j][n] = dBp;
-                    sPC[warp][j][n] = dCp;
-                }
             }
+            // du, ddelta of the 4 steps: sums over the channel's 16 states
+            const float tot = half_warp_sum8(red, lane);
+            if ((lane & 1) == 0) {
+                const int idx = ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+                if (idx < 4) sDu[ch][j0 + idx] = tot;
+                else sDd[ch][j0 + idx - 4] = tot;
+            }
+            // dB, dC: sums over the warp's two channels (lanes < 16 keep dB)
+            const bool hi = lane >= 16;
+            float qv[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float send = hi ? dBp[k] : dCp[k];
+                qv[k] = (hi ? dCp[k] : dBp[k]) + __shfl_xor_sync(0xffffffffu, send, 16);
+            }
+            *(float4 *)(hi ? &sPC[warp][n][j0] : &sPB[warp][n][j0]) =
+                make_float4(qv[0], qv[1], qv[2], qv[3]);
         }
+    };
+    fetch(nch - 1, true);
+    for (int c = nch - 1; c >= 0; --c) {
+        commit(c);
         __syncthreads();
-        // per-position gradients of this direction
+        if (c > 0) fetch(c - 1, true);
+        const int len = min(T, L - c * T);
+        const float h0 = cvalid ? hcp[(long long)c * kMaxN] : 0.f;
+        if (len == T) chunk(BoolC<true>(), len, h0);
+        else chunk(BoolC<false>(), len, h0);
+        __syncthreads();
+        // per-position gradients of this direction (du with the skip term)
         for (int i = tid; i < CH * T; i += NT) {
             const int cc = i / T, j = i % T, w = c * T + j, dd = d0 + cc;
             if (w < L && dd < D) {
                 const long long prow = ((long long)b * D + dd) * L;
-                ps.du[prow + pos(w)] = sDu[cc][j];
+                const float Dd = ps.Dskip ? ps.Dskip[dd] : 0.f;
+                ps.du[prow + pos(w)] = fmaf(sG[cc][j], Dd, sDu[cc][j]);
                 const float gx = P.delta_softplus ? sDd[cc][j] * sS[cc][j] : sDd[cc][j];
                 ps.ddt[ps.dt_off + b * ps.dt_bstride + (long long)dd * L + sidx(w)] = gx;
             }
@@ -220,8 +298,8 @@ scan_bwd_kernel(const Params P) {
                 float sb = 0.f, sc = 0.f;
 #pragma unroll
                 for (int k = 0; k < NWARP; ++k) {
-                    sb += sPB[k][j][nn];
-                    sc += sPC[k][j][nn];
+                    sb += sPB[k][nn][j];
+                    sc += sPC[k][nn][j];
                 }
                 const long long o = (((long long)blockIdx.x * P.B + b) * L + sidx(w)) * kMaxN + nn;
                 ps.pdB[o] = sb;
@@ -230,13 +308,37 @@ scan_bwd_kernel(const Params P) {
         }
         __syncthreads();
     }
-    if (cvalid) {
-        ps.pdA[((long long)b * D + d) * kMaxN + n] = dA;
-        if (n == 0) {
-            ps.pdD[(long long)b * D + d] = dDs;
-            ps.pdbias[(long long)b * D + d] = dbs;
+    if (cvalid) ps.pdA[((long long)b * D + d) * kMaxN + n] = dA;
+}
+
+// out[d] = scale * sum over (b, t) of (a + a2)[b][d][t] (* u[b][d][t] when u
+// is given); a, a2 at + b * a_bstride + d * L, u [B][D][L].  One CTA per channel, a
+// fixed-order tree: deterministic.  dbias (a = ddelta-dt map) and dD
+// (a = G, u = the scanned input).
+template <typename IO>
+__global__ void __launch_bounds__(256)
+channel_sum_kernel(const float *__restrict__ a, const float *__restrict__ a2, long long a_bstride,
+                   const IO *__restrict__ u, int B, int D, int L, float scale,
+                   float *__restrict__ out) {
+    __shared__ float red[256];
+    const int dch = blockIdx.x;
+    float acc = 0.f;
+    for (int b = 0; b < B; ++b) {
+        const long long o = b * a_bstride + (long long)dch * L;
+        const IO *ur = u ? u + ((long long)b * D + dch) * L : nullptr;
+        for (int t = threadIdx.x; t < L; t += 256) {
+            float v = a[o + t];
+            if (a2) v += a2[o + t];
+            acc += u ? v * to_f32(ur[t]) : v;
         }
     }
+    red[threadIdx.x] = acc;
+    __syncthreads();
+    for (int s2 = 128; s2 > 0; s2 >>= 1) {
+        if (threadIdx.x < s2) red[threadIdx.x] += red[threadIdx.x + s2];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) out[dch] = scale * red[0];
 }
 
 // gy = g * silu(z) (fp32), dz = g * y * silu'(z) (I/O dtype); z == null: gy = g

@@ -40,7 +40,7 @@ size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 // Workspace of one backward call; every region starts on 256 bytes.
 struct BwdWs {
-    size_t fwd, ypre, G, GT, xT, du, ddt, hc, pdB, pdC, pdA, pdD, pdbias, total;
+    size_t fwd, ypre, G, GT, xT, du, ddt, hc, pdB, pdC, pdA, total;
     size_t fwd_bytes;
 };
 // op: 0 single, 1 v1, 2 v2, 3 SS2D.  du and ddt hold one fp32 map per
@@ -76,8 +76,6 @@ BwdWs bwd_ws(int op, ssm_dtype dt, int B, int D, int L, int N, bool sep_ub) {
     w.pdB = take(part);
     w.pdC = take(part);
     w.pdA = take((size_t)npass * B * D * ssm::kMaxN * 4);
-    w.pdD = take((size_t)npass * B * D * 4);
-    w.pdbias = take((size_t)npass * B * D * 4);
     w.total = off;
     return w;
 }
@@ -145,6 +143,16 @@ ssm_status reduce_bc(const float *part, int nslot, int B, int L, int N, void *ou
     return last_error();
 }
 
+// out[d] = scale * sum over (b, t) of (a [+ a2]) [* u], see channel_sum_kernel
+template <typename IO>
+ssm_status channel_sum(const float *a, const float *a2, long long a_bstride, const void *u,
+                       int B, int D, int L, float scale, float *out, cudaStream_t st) {
+    if (out == nullptr) return SSM_OK;
+    ssm::bwd::channel_sum_kernel<IO><<<D, 256, 0, st>>>(a, a2, a_bstride, (const IO *)u, B, D, L,
+                                                         scale, out);
+    return last_error();
+}
+
 ssm_status reduce_param(const float *part, int nslot, int B, int D, int N, bool per_state,
                         float *out, cudaStream_t st) {
     if (out == nullptr) return SSM_OK;
@@ -162,13 +170,11 @@ ssm_status reduce_param(const float *part, int nslot, int B, int D, int N, bool 
 
 // The common tail: partials of pass p live at slot offset p * ncg.
 struct Parts {
-    const float *pdB, *pdC, *pdA, *pdD, *pdbias;
+    const float *pdB, *pdC, *pdA;
     int ncg, B, D, L, N;
     const float *dB_slot(int p) const { return pdB + (size_t)p * ncg * B * L * ssm::kMaxN; }
     const float *dC_slot(int p) const { return pdC + (size_t)p * ncg * B * L * ssm::kMaxN; }
     const float *dA_slot(int p) const { return pdA + (size_t)p * B * D * ssm::kMaxN; }
-    const float *dD_slot(int p) const { return pdD + (size_t)p * B * D; }
-    const float *db_slot(int p) const { return pdbias + (size_t)p * B * D; }
 };
 
 Parts parts_of(char *ws, const BwdWs &w, int B, int D, int L, int N) {
@@ -176,8 +182,6 @@ Parts parts_of(char *ws, const BwdWs &w, int B, int D, int L, int N) {
     q.pdB = (const float *)(ws + w.pdB);
     q.pdC = (const float *)(ws + w.pdC);
     q.pdA = (const float *)(ws + w.pdA);
-    q.pdD = (const float *)(ws + w.pdD);
-    q.pdbias = (const float *)(ws + w.pdbias);
     q.ncg = (D + ssm::bwd::CH - 1) / ssm::bwd::CH;
     q.B = B;
     q.D = D;
@@ -193,8 +197,6 @@ Pass base_pass(char *ws, const BwdWs &w, int p, int B, int D, int L) {
     ps.pdB = (float *)(ws + w.pdB) + (size_t)p * ncg * B * L * ssm::kMaxN;
     ps.pdC = (float *)(ws + w.pdC) + (size_t)p * ncg * B * L * ssm::kMaxN;
     ps.pdA = (float *)(ws + w.pdA) + (size_t)p * B * D * ssm::kMaxN;
-    ps.pdD = (float *)(ws + w.pdD) + (size_t)p * B * D;
-    ps.pdbias = (float *)(ws + w.pdbias) + (size_t)p * B * D;
     const int nch = (L + ssm::bwd::T - 1) / ssm::bwd::T;
     ps.hc = (float *)(ws + w.hc) + (size_t)p * B * D * nch * ssm::kMaxN;
     ps.G = (const float *)(ws + w.G);
@@ -261,8 +263,6 @@ ssm_status seq_bwd(int op, int B, int D, int L, int N, const void *u, const void
         p1.pdB = q.pdB;
         p1.pdC = q.pdC;
         p1.pdA = q.pdA;
-        p1.pdD = q.pdD;
-        p1.pdbias = q.pdbias;
         p1.hc = q.hc;
         p1.dt = op == 2 ? delta_b : delta;
         p1.u = (op == 2 && u_b) ? u_b : u;
@@ -293,12 +293,14 @@ ssm_status seq_bwd(int op, int B, int D, int L, int N, const void *u, const void
     }
     TRY(reduce_param(q.dA_slot(0), 1, B, D, N, true, dA, st));
     if (op != 0) TRY(reduce_param(q.dA_slot(1), 1, B, D, N, true, dA_b, st));
-    const int shared_par = op == 1 ? 2 : 1;     // v1: D and bias shared
-    if (Dskip) TRY(reduce_param(q.dD_slot(0), shared_par, B, D, N, false, dD, st));
-    TRY(reduce_param(q.db_slot(0), shared_par, B, D, N, false, dbias, st));
+    // dD: each branch's skip term is D * u_t at every position, so
+    // dD = gscale * sum G u (v1: both branches, shared D); dbias = sum ddt
+    const float gs = op == 0 ? 1.f : out_scale;
+    if (Dskip) TRY(channel_sum<IO>(G, nullptr, DL, u, B, D, L, op == 1 ? 2.f * gs : gs, dD, st));
+    TRY(channel_sum<IO>(dt0, op == 1 ? dt1 : nullptr, DL, nullptr, B, D, L, 1.f, dbias, st));
     if (op == 2) {
-        if (D_b) TRY(reduce_param(q.dD_slot(1), 1, B, D, N, false, dD_b, st));
-        TRY(reduce_param(q.db_slot(1), 1, B, D, N, false, dbias_b, st));
+        if (D_b) TRY(channel_sum<IO>(G, nullptr, DL, u_b ? u_b : u, B, D, L, gs, dD_b, st));
+        TRY(channel_sum<IO>(dt1, nullptr, DL, nullptr, B, D, L, 1.f, dbias_b, st));
     }
     return SSM_OK;
 }
@@ -360,9 +362,11 @@ ssm_status ss2d_bwd_run(int B, int D, int H, int W, int N, const void *x, const 
         TRY(reduce_bc<IO>(q.dB_slot(k), q.ncg, B, L, N, (IO *)dB + k * NL, K * NL, st));
         TRY(reduce_bc<IO>(q.dC_slot(k), q.ncg, B, L, N, (IO *)dC + k * NL, K * NL, st));
         TRY(reduce_param(q.dA_slot(k), 1, B, D, N, true, dA + (long long)k * D * N, st));
-        if (Dskip) TRY(reduce_param(q.dD_slot(k), 1, B, D, N, false, dD ? dD + k * D : nullptr,
-                                    st));
-        TRY(reduce_param(q.db_slot(k), 1, B, D, N, false, dbias ? dbias + k * D : nullptr, st));
+        // every direction visits every position once: dD_k = sum G x
+        if (Dskip)
+            TRY(channel_sum<IO>(G, nullptr, DL, x, B, D, L, 1.f, dD ? dD + k * D : nullptr, st));
+        TRY(channel_sum<IO>((const float *)(ws + w.ddt) + k * DL, nullptr, K * DL, nullptr, B, D,
+                            L, 1.f, dbias ? dbias + k * D : nullptr, st));
     }
     return SSM_OK;
 }
