@@ -107,6 +107,7 @@ scan_bwd_kernel(const Params P) {
     __shared__ __align__(16) float sD[CH][TP], sU[CH][TP], sG[CH][TP], sS[CH][TP];
     __shared__ __align__(16) float sBt[kMaxN][TP], sCt[kMaxN][TP];
     __shared__ float sDu[CH][T + 1], sDd[CH][T + 1];
+    __shared__ float sBias[CH], sDsk[CH];           // per-channel constants
     // per-warp dB, dC partials of a chunk, [warp][state][step] (dynamic: kDynBytes)
     extern __shared__ __align__(16) float dyn[];
     float (*sPB)[kMaxN][TP] = reinterpret_cast<float (*)[kMaxN][TP]>(dyn);
@@ -126,6 +127,12 @@ scan_bwd_kernel(const Params P) {
     const IO *cp = (const IO *)ps.Cm + ps.bc_off + b * ps.bc_bstride;
     const IO *up = (const IO *)ps.u;
     float *hcp = ps.hc + (((long long)b * D + d) * nch) * kMaxN + n;
+    if (tid < CH) {
+        const int dd = d0 + tid;
+        sBias[tid] = (dd < D && ps.bias) ? ps.bias[dd] : 0.f;
+        sDsk[tid] = (dd < D && ps.Dskip) ? ps.Dskip[dd] : 0.f;
+    }
+    __syncthreads();
 
     auto pos = [&](int w) { return ps.rev ? L - 1 - w : w; };
     auto sidx = [&](int w) { return ps.stream_rev ? w : pos(w); };
@@ -157,7 +164,7 @@ scan_bwd_kernel(const Params P) {
             const int i = tid + r * NT, cc = i / T, j = i % T, w = c * T + j, dd = d0 + cc;
             float dl = 0.f, sg = 1.f;
             if (w < L && dd < D) {
-                const float x = rdt[r] + (ps.bias ? ps.bias[dd] : 0.f);
+                const float x = rdt[r] + sBias[cc];
                 if (P.delta_softplus) {
                     dl = x > 20.f ? x : log1pf(expf(x));
                     sg = sigmoid_f(x);
@@ -271,12 +278,16 @@ scan_bwd_kernel(const Params P) {
         }
     };
     fetch(nch - 1, true);
+    float hnext = cvalid ? hcp[(long long)(nch - 1) * kMaxN] : 0.f;
     for (int c = nch - 1; c >= 0; --c) {
         commit(c);
         __syncthreads();
-        if (c > 0) fetch(c - 1, true);
+        const float h0 = hnext;
+        if (c > 0) {
+            fetch(c - 1, true);
+            hnext = cvalid ? hcp[(long long)(c - 1) * kMaxN] : 0.f;
+        }
         const int len = min(T, L - c * T);
-        const float h0 = cvalid ? hcp[(long long)c * kMaxN] : 0.f;
         if (len == T) chunk(BoolC<true>(), len, h0);
         else chunk(BoolC<false>(), len, h0);
         __syncthreads();
@@ -285,8 +296,7 @@ scan_bwd_kernel(const Params P) {
             const int cc = i / T, j = i % T, w = c * T + j, dd = d0 + cc;
             if (w < L && dd < D) {
                 const long long prow = ((long long)b * D + dd) * L;
-                const float Dd = ps.Dskip ? ps.Dskip[dd] : 0.f;
-                ps.du[prow + pos(w)] = fmaf(sG[cc][j], Dd, sDu[cc][j]);
+                ps.du[prow + pos(w)] = fmaf(sG[cc][j], sDsk[cc], sDu[cc][j]);
                 const float gx = P.delta_softplus ? sDd[cc][j] * sS[cc][j] : sDd[cc][j];
                 ps.ddt[ps.dt_off + b * ps.dt_bstride + (long long)dd * L + sidx(w)] = gx;
             }
