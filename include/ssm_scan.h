@@ -21,14 +21,15 @@
  * Common conventions
  *  - All tensor pointers are DEVICE pointers to contiguous, caller-owned
  *    memory.  I/O tensors (u, delta, B, C, z, y and the per-branch copies)
- *    use the dtype `dt` (fp32 or bf16); A, Dskip and delta_bias are fp32.
- *  - Every pointer must be aligned to its element type (2 bytes for bf16,
- *    4 for fp32); I/O tensors may start anywhere else, e.g. at an offset
+ *    use the dtype `dt` (fp32, bf16 or fp16); A, Dskip and delta_bias are
+ *    fp32.
+ *  - Every pointer must be aligned to its element type (2 bytes for bf16
+ *    and fp16, 4 for fp32); I/O tensors may start anywhere else, e.g. at an offset
  *    into a larger buffer.  Only the workspace needs 16 bytes.
  *  - Optional pointers may be NULL: Dskip -> 0, z -> no gate,
  *    delta_bias -> 0 (and u_b -> u for v2).
  *  - `y` must not alias any input.  State and arithmetic are fp32; bf16
- *    outputs are rounded to nearest even.
+ *    and fp16 outputs are rounded to nearest even.
  *  - `workspace` is device memory of at least ssm_workspace_bytes(...)
  *    bytes for the same arguments, 16-byte aligned (NULL is fine when that
  *    is 0).  It holds a status word, the B and C tensors repacked per
@@ -69,7 +70,7 @@ extern "C" {
 
 typedef struct CUstream_st *ssm_stream_t; /* same type as cudaStream_t */
 
-typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
+typedef enum { SSM_F32 = 0, SSM_BF16 = 1, SSM_F16 = 2 } ssm_dtype;
 
 typedef enum {
     SSM_OK = 0,

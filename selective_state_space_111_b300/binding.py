@@ -24,7 +24,8 @@ if not os.path.exists(_LIB_PATH):
 
 _lib = ctypes.CDLL(_LIB_PATH)
 
-SSM_F32, SSM_BF16 = 0, 1
+SSM_F32, SSM_BF16, SSM_F16 = 0, 1, 2
+_CODES = {torch.float32: SSM_F32, torch.bfloat16: SSM_BF16, torch.float16: SSM_F16}
 OPS = {"single": 0, "v1": 1, "v2": 2, "ss2d": 3}
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA launch error",
            4: "workspace", 5: "scratch limit", 6: "timeout"}
@@ -83,11 +84,9 @@ def version() -> str:
 
 
 def _dtype_code(t: torch.Tensor) -> int:
-    if t.dtype == torch.float32:
-        return SSM_F32
-    if t.dtype == torch.bfloat16:
-        return SSM_BF16
-    raise TypeError("I/O tensors must be float32 or bfloat16, got %s" % t.dtype)
+    if t.dtype not in _CODES:
+        raise TypeError("I/O tensors must be float32, bfloat16 or float16, got %s" % t.dtype)
+    return _CODES[t.dtype]
 
 
 def _io(t, io_dtype, name, shape=None, optional=False):
@@ -112,7 +111,7 @@ def _stream(stream):
 
 
 def workspace_bytes(op: str, dtype: torch.dtype, B: int, D: int, L: int, N: int, K: int = 4) -> int:
-    code = SSM_F32 if dtype == torch.float32 else SSM_BF16
+    code = _CODES[dtype]
     n = _lib.ssm_workspace_bytes(OPS[op], code, B, D, L, N, K)
     if n == ctypes.c_size_t(-1).value:
         raise ValueError("invalid sizes")
@@ -269,7 +268,7 @@ def bimamba_scan_fwd_v2_noalloc(u, delta, delta_b, A, A_b, B, C, B_b, C_b, D=Non
 # ---------------------------------------------------------------- backward
 def bwd_workspace_bytes(op: str, dtype: torch.dtype, B: int, D: int, L: int, N: int,
                         K: int = 4, separate_u_b: bool = False) -> int:
-    code = SSM_F32 if dtype == torch.float32 else SSM_BF16
+    code = _CODES[dtype]
     n = _lib.ssm_bwd_workspace_bytes(OPS[op], code, B, D, L, N, K, int(bool(separate_u_b)))
     if n == ctypes.c_size_t(-1).value:
         raise ValueError("invalid sizes")

@@ -6,6 +6,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -80,16 +81,20 @@ __device__ __forceinline__ void cp_async_wait() {
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
 template <typename IO> __device__ __forceinline__ IO from_f32(float x);
 template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
     return __float2bfloat16_rn(x);
 }
+template <> __device__ __forceinline__ __half from_f32<__half>(float x) {
+    return __float2half_rn(x);
+}
 
 // softplus and the SiLU gate.  fp32 I/O uses the accurate library functions;
-// bf16 I/O uses the MUFU forms (ex2 / lg2 / rcp), whose relative error
-// (about 2e-4 on delta for delta near 1e-3, far less elsewhere) is two orders
-// of magnitude below the bf16 output rounding.
+// bf16 and fp16 I/O use the MUFU forms (ex2 / lg2 / rcp), whose relative
+// error (about 2e-4 on delta for delta near 1e-3, far less elsewhere) is
+// below the 16-bit output rounding.
 template <typename IO> __device__ __forceinline__ float softplus_f(float x);
 template <> __device__ __forceinline__ float softplus_f<float>(float x) {
     return x > 0.f ? x + log1pf(expf(-x)) : log1pf(expf(x));
@@ -105,6 +110,12 @@ template <> __device__ __forceinline__ float silu_f<float>(float z) {
 }
 template <> __device__ __forceinline__ float silu_f<__nv_bfloat16>(float z) {
     return z * rcp_approx(1.f + ex2_approx(-z * kLog2e));
+}
+template <> __device__ __forceinline__ float softplus_f<__half>(float x) {
+    return softplus_f<__nv_bfloat16>(x);
+}
+template <> __device__ __forceinline__ float silu_f<__half>(float z) {
+    return silu_f<__nv_bfloat16>(z);
 }
 
 

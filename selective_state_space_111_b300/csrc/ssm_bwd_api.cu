@@ -8,6 +8,7 @@
 // output dtypes.  Nothing is allocated; everything lives in the
 // caller's workspace (ssm_bwd_workspace_bytes).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -28,7 +29,7 @@ bool f32_ok(const float *p) { return p != nullptr && aligned(p, 4); }
 bool opt_f32(const float *p) { return p == nullptr || aligned(p, 4); }
 
 ssm_status check_sizes(ssm_dtype dt, int B, int D, int L, int N) {
-    if (dt != SSM_F32 && dt != SSM_BF16) return SSM_ERR_INVALID_ARG;
+    if (dt != SSM_F32 && dt != SSM_BF16 && dt != SSM_F16) return SSM_ERR_INVALID_ARG;
     if (B < 0 || D < 0 || L < 0 || N <= 0) return SSM_ERR_INVALID_ARG;
     if (N > ssm::kMaxN) return SSM_ERR_UNSUPPORTED;
     if (B > 65535) return SSM_ERR_UNSUPPORTED;
@@ -37,6 +38,10 @@ ssm_status check_sizes(ssm_dtype dt, int B, int D, int L, int N) {
 }
 
 size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+template <typename IO> constexpr ssm_dtype dtype_of() { return SSM_BF16; }
+template <> constexpr ssm_dtype dtype_of<float>() { return SSM_F32; }
+template <> constexpr ssm_dtype dtype_of<__half>() { return SSM_F16; }
 
 // Workspace of one backward call; every region starts on 256 bytes.
 struct BwdWs {
@@ -214,7 +219,7 @@ ssm_status seq_bwd(int op, int B, int D, int L, int N, const void *u, const void
                    void *du_b, void *ddelta, void *ddelta_b, float *dA, float *dA_b, void *dB,
                    void *dC, void *dB_b, void *dC_b, float *dD, float *dD_b, void *dz,
                    float *dbias, float *dbias_b, char *ws, const BwdWs &w, cudaStream_t st) {
-    const ssm_dtype dt = sizeof(IO) == 4 ? SSM_F32 : SSM_BF16;
+    const ssm_dtype dt = dtype_of<IO>();
     const long long n = (long long)B * D * L;
     float *G = (float *)(ws + w.G);
     float *du0 = (float *)(ws + w.du), *du1 = du0 + n;      // per direction
@@ -314,7 +319,7 @@ ssm_status ss2d_bwd_run(int B, int D, int H, int W, int N, const void *x, const 
                         const void *z, const float *bias, int sp, const void *dout, void *dx,
                         void *ddelta, float *dA, void *dB, void *dC, float *dD, void *dz,
                         float *dbias, char *ws, const BwdWs &w, cudaStream_t st) {
-    const ssm_dtype dt = sizeof(IO) == 4 ? SSM_F32 : SSM_BF16;
+    const ssm_dtype dt = dtype_of<IO>();
     const int L = H * W, K = 4;
     const long long n = (long long)B * D * L;
     void *ypre = ws + w.ypre;
@@ -377,7 +382,7 @@ extern "C" {
 
 size_t ssm_bwd_workspace_bytes(ssm_op op, ssm_dtype dt, int B, int D, int L_or_HW, int N, int K,
                                int separate_u_b) {
-    if (dt != SSM_F32 && dt != SSM_BF16) return (size_t)-1;
+    if (dt != SSM_F32 && dt != SSM_BF16 && dt != SSM_F16) return (size_t)-1;
     if (B < 0 || D < 0 || L_or_HW < 0 || N <= 0 || N > ssm::kMaxN) return (size_t)-1;
     int o;
     switch (op) {
@@ -422,7 +427,7 @@ ssm_status selective_scan_bwd(ssm_dtype dt, int B, int D, int L, int N, const vo
                            dB, dC, nullptr, nullptr, dD, nullptr, dz, ddelta_bias, nullptr, ws,
                            w, st);
     };
-    return dt == SSM_F32 ? run(float()) : run(__nv_bfloat16());
+    return dt == SSM_F32 ? run(float()) : dt == SSM_F16 ? run(__half()) : run(__nv_bfloat16());
 }
 
 ssm_status bimamba_scan_bwd_v1(ssm_dtype dt, int B, int D, int L, int N, const void *u,
@@ -453,7 +458,7 @@ ssm_status bimamba_scan_bwd_v1(ssm_dtype dt, int B, int D, int L, int N, const v
                            out_scale, dout, du, nullptr, ddelta, nullptr, dA, dA_b, dB, dC,
                            nullptr, nullptr, dD, nullptr, dz, ddelta_bias, nullptr, ws, w, st);
     };
-    return dt == SSM_F32 ? run(float()) : run(__nv_bfloat16());
+    return dt == SSM_F32 ? run(float()) : dt == SSM_F16 ? run(__half()) : run(__nv_bfloat16());
 }
 
 ssm_status bimamba_scan_bwd_v2(ssm_dtype dt, int B, int D, int L, int N, const void *u,
@@ -492,7 +497,7 @@ ssm_status bimamba_scan_bwd_v2(ssm_dtype dt, int B, int D, int L, int N, const v
                            dout, du, du_b, ddelta, ddelta_b, dA, dA_b, dB, dC, dB_b, dC_b, dD,
                            dD_b, dz, ddelta_bias, ddelta_bias_b, ws, w, st);
     };
-    return dt == SSM_F32 ? run(float()) : run(__nv_bfloat16());
+    return dt == SSM_F32 ? run(float()) : dt == SSM_F16 ? run(__half()) : run(__nv_bfloat16());
 }
 
 ssm_status ss2d_scan_bwd(ssm_dtype dt, int B, int D, int H, int W, int N, int K, const void *x,
@@ -526,7 +531,7 @@ ssm_status ss2d_scan_bwd(ssm_dtype dt, int B, int D, int H, int W, int N, int K,
                                 delta_softplus, dout, dx, ddelta, dA, dB, dC, dD, dz,
                                 ddelta_bias, ws, w, st);
     };
-    return dt == SSM_F32 ? run(float()) : run(__nv_bfloat16());
+    return dt == SSM_F32 ? run(float()) : dt == SSM_F16 ? run(__half()) : run(__nv_bfloat16());
 }
 
 }  // extern "C"

@@ -6,6 +6,7 @@
 // fixed scratch array of the allocation-free entry point and its per-device
 // address.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -22,7 +23,7 @@ bool aligned(const void *p, unsigned a) { return ((uintptr_t)p % a) == 0; }
 bool fits(long long v) { return v >= 0 && v <= 0x7fffffffLL; }
 
 ssm_status check_common(ssm_dtype dt, int B, int D, int L, int N) {
-    if (dt != SSM_F32 && dt != SSM_BF16) return SSM_ERR_INVALID_ARG;
+    if (dt != SSM_F32 && dt != SSM_BF16 && dt != SSM_F16) return SSM_ERR_INVALID_ARG;
     if (B < 0 || D < 0 || L < 0 || N <= 0) return SSM_ERR_INVALID_ARG;
     if (N > ssm::kMaxN) return SSM_ERR_UNSUPPORTED;
     if (B > 65535) return SSM_ERR_UNSUPPORTED;                 // grid.y
@@ -224,6 +225,7 @@ ssm_status bidirectional(ssm_dtype dt, int B, int D, int L, int N, const void *u
     P.delta_softplus = delta_softplus ? 1 : 0;
     P.out_scale = out_scale;
     if (dt == SSM_F32) return run_bidir<float, 2>(P, Bm, Cm, Bm_b, Cm_b, two_sets, stream);
+    if (dt == SSM_F16) return run_bidir<__half, 2>(P, Bm, Cm, Bm_b, Cm_b, two_sets, stream);
     return run_bidir<__nv_bfloat16, 2>(P, Bm, Cm, Bm_b, Cm_b, two_sets, stream);
 }
 
@@ -387,6 +389,7 @@ ssm_status selective_scan_fwd(ssm_dtype dt, int B, int D, int L, int N, const vo
     P.out_scale = 1.f;
     cudaStream_t st = (cudaStream_t)stream;
     if (dt == SSM_F32) return run_bidir<float, 1>(P, Bm, Cm, Bm, Cm, false, st);
+    if (dt == SSM_F16) return run_bidir<__half, 1>(P, Bm, Cm, Bm, Cm, false, st);
     return run_bidir<__nv_bfloat16, 1>(P, Bm, Cm, Bm, Cm, false, st);
 }
 
@@ -454,17 +457,19 @@ ssm_status ss2d_scan_fwd(ssm_dtype dt, int B, int D, int H, int W, int N, int K,
     if (workspace == nullptr || ws_bytes < lay.total || !aligned(workspace, 16))
         return SSM_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
-    return dt == SSM_F32 ? ss2d_run<float>(B, D, H, W, N, x, delta, A, Bm, Cm, Dskip, z,
-                                           delta_bias, delta_softplus, y, (char *)workspace,
-                                           lay, st)
-                         : ss2d_run<__nv_bfloat16>(B, D, H, W, N, x, delta, A, Bm, Cm, Dskip, z,
-                                                   delta_bias, delta_softplus, y,
-                                                   (char *)workspace, lay, st);
+    if (dt == SSM_F32)
+        return ss2d_run<float>(B, D, H, W, N, x, delta, A, Bm, Cm, Dskip, z, delta_bias,
+                               delta_softplus, y, (char *)workspace, lay, st);
+    if (dt == SSM_F16)
+        return ss2d_run<__half>(B, D, H, W, N, x, delta, A, Bm, Cm, Dskip, z, delta_bias,
+                                delta_softplus, y, (char *)workspace, lay, st);
+    return ss2d_run<__nv_bfloat16>(B, D, H, W, N, x, delta, A, Bm, Cm, Dskip, z, delta_bias,
+                                   delta_softplus, y, (char *)workspace, lay, st);
 }
 
 size_t ssm_workspace_bytes(ssm_op op, ssm_dtype dt, int B, int D, int L_or_HW, int N, int K) {
     (void)N;
-    if (dt != SSM_F32 && dt != SSM_BF16) return (size_t)-1;
+    if (dt != SSM_F32 && dt != SSM_BF16 && dt != SSM_F16) return (size_t)-1;
     if (B < 0 || D < 0 || L_or_HW < 0) return (size_t)-1;
     switch (op) {
     case SSM_OP_SELECTIVE_SCAN:

@@ -14,7 +14,7 @@ Recipe (shapes from the Vision Mamba / VMamba pages' workloads):
     whose softplus is delta_d, i.e. log(expm1(delta_d)).
   * dt ~ N(0, 0.5^2); u (x), z, B, C ~ N(0, 1); D = 1 (``perturb``: U(0.5, 1.5)).
   * Every activation is drawn in fp32 and rounded to the I/O dtype (round to
-    nearest even for bf16); A, D and delta_bias stay fp32.
+    nearest even for bf16 and fp16); A, D and delta_bias stay fp32.
 Tensors are drawn on the CPU from ``torch.Generator().manual_seed(seed)`` in a
 fixed order, so a (spec, seed) pair always gives the same values.
 """
@@ -25,7 +25,7 @@ from dataclasses import dataclass, field
 
 import torch
 
-IO_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
+IO_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
 
 
 @dataclass(frozen=True)
@@ -33,7 +33,7 @@ class Spec:
     """One workload: operation, I/O dtype and sizes."""
 
     op: str            # "single" | "v1" | "v2" | "ss2d"
-    io: str            # "f32" | "bf16"
+    io: str            # "f32" | "bf16" | "f16"
     B: int
     D: int
     N: int = 16

@@ -8,8 +8,9 @@ and positions (dA, dD, ddelta_bias, and dB, dC, summed over channels) are
 compared against their own scale: max|gpu - ref| <= tol * (1 + max|ref|),
 because fp32 summation of thousands of terms of both signs leaves an
 absolute error proportional to the terms' size, not to the (possibly
-cancelling) result.  tol = 2e-4 for fp32 I/O, 2e-2 for bf16 I/O (outputs
-rounded to bf16, inputs and the recomputed pre-gate output in bf16).
+cancelling) result.  tol = 2e-4 for fp32 I/O, 2e-2 for bf16 I/O and 1e-2
+for fp16 I/O (outputs rounded to the 16-bit type, inputs and the recomputed
+pre-gate output in it).
 """
 import numpy as np
 import pytest
@@ -21,7 +22,7 @@ from selective_state_space_111_b300.synth import WORKLOADS, Spec, make_inputs, s
 
 pytestmark = pytest.mark.gpu
 
-TOL = {"f32": 2e-4, "bf16": 2e-2}
+TOL = {"f32": 2e-4, "bf16": 2e-2, "f16": 1e-2}
 SEQ = {"du", "du_b", "ddelta", "ddelta_b", "dz", "dx"}
 
 
@@ -105,14 +106,14 @@ SHAPES = [(1, 1, 1, 16), (2, 3, 33, 16), (1, 17, 64, 16), (2, 20, 97, 16), (1, 9
           (2, 4, 129, 1)]
 
 
-@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("io", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("shape", SHAPES)
 def test_single_bwd(io, shape):
     B, D, L, N = shape
     check(Spec("single", io, B=B, D=D, L=L, N=N, perturb=True), 5000 + L)
 
 
-@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("io", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("shape", SHAPES)
 def test_v1_bwd(io, shape):
     B, D, L, N = shape
@@ -120,7 +121,7 @@ def test_v1_bwd(io, shape):
           6000 + L)
 
 
-@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("io", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("shape", SHAPES)
 @pytest.mark.parametrize("shared_u", [True, False])
 def test_v2_bwd(io, shape, shared_u):
@@ -129,7 +130,7 @@ def test_v2_bwd(io, shape, shared_u):
           7000 + L)
 
 
-@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("io", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("shape", [(1, 1, 1, 1), (1, 2, 2, 3), (2, 3, 5, 7), (1, 17, 8, 8),
                                    (1, 4, 11, 3)])
 def test_ss2d_bwd(io, shape):
