@@ -42,7 +42,7 @@
  *    The library allocates nothing and keeps no global state, except the
  *    fixed scratch array that bimamba_scan_fwd_v2_noalloc uses.
  *  - Errors: SSM_ERR_INVALID_ARG for a bad size, NULL required pointer or
- *    misaligned pointer; SSM_ERR_UNSUPPORTED for N > 16, K != 4 or sizes
+ *    misaligned pointer; SSM_ERR_UNSUPPORTED for N > 32, K != 4 or sizes
  *    beyond the 32-bit index range; SSM_ERR_WORKSPACE when ws_bytes is too
  *    small; SSM_ERR_CUDA when a launch fails (cudaGetLastError is consumed);
  *    SSM_ERR_SCRATCH_LIMIT when a problem is too large for the fixed scratch

@@ -19,10 +19,11 @@
 // spend its issue slots there:
 //
 //   pack_bc_kernel  B and C ([B, N, L], I/O dtype) are converted once per
-//                   batch element into a packed fp32 stream BC[b][t][32] =
-//                   (B_0..B_15, C_0..C_15) -- 128 bytes per position, so one
-//                   chunk of positions is one contiguous, aligned range that
-//                   a single bulk copy (cp.async.bulk) moves to shared memory.
+//                   batch element into a packed fp32 stream BC[b][t][2NM] =
+//                   (B_0..B_{NM-1}, C_0..C_{NM-1}) for a state capacity NM of
+//                   16 or 32 (128 or 256 bytes per position), so one chunk of
+//                   positions is one contiguous, aligned range that a single
+//                   bulk copy (cp.async.bulk) moves to shared memory.
 //   bidir_scan_kernel
 //     CTA  = R channels of one batch element x NDIR branches, T = 32
 //            positions per chunk, in three warp roles linked by full/empty
@@ -54,7 +55,8 @@
 
 namespace ssm {
 
-constexpr int kBC = 2 * kMaxN;   // floats per position in the packed B/C stream
+// State capacity NM (16 or 32, a template parameter): the packed B/C stream
+// holds 2 * NM floats per position (B_0..B_{NM-1}, C_0..C_{NM-1}).
 
 #ifndef SSM_SCAN_BLOCK
 #define SSM_SCAN_BLOCK 4         // scan steps per block (loads, then ex2, then recurrences)
@@ -99,30 +101,31 @@ struct BiParams {
 
 // ------------------------------------------------------------------ pack
 // B, C: [Bt, K, N, L] (K = 1 for the sequence forms).  For direction k,
-// batch b and position t: out[((k * Bt + b) * L + t) * 32 + j] = B[b,k,j,t]
-// (j < 16), C[b,k,j-16,t] (j >= 16); 0 for state indices >= N.
+// batch b and position t: out[((k * Bt + b) * L + t) * 2NM + j] = B[b,k,j,t]
+// (j < NM), C[b,k,j-NM,t] (j >= NM); 0 for state indices >= N.
 // Block: 64 positions of one (b, k), 256 threads; block (0,0,0) also clears
 // the status word so that the scan kernel of the same call can set it.
-template <typename IO>
+template <typename IO, int NM>
 __global__ void __launch_bounds__(256)
 pack_bc_kernel(const IO *__restrict__ Bm, const IO *__restrict__ Cm, float *__restrict__ out,
                int N, int L, unsigned *status) {
+    constexpr int kBC = 2 * NM;
     __shared__ float tile[kBC][65];
     const int b = blockIdx.y, k = blockIdx.z, t0 = blockIdx.x * 64;
     const int Bt = gridDim.y, K = gridDim.z;
     if (status != nullptr && blockIdx.x == 0 && b == 0 && k == 0 && threadIdx.x == 0) *status = 0;
     for (int i = threadIdx.x; i < kBC * 64; i += 256) {
-        const int j = i >> 6, tt = i & 63, t = t0 + tt, n = j & (kMaxN - 1);
+        const int j = i >> 6, tt = i & 63, t = t0 + tt, n = j & (NM - 1);
         float v = 0.f;
         if (t < L && n < N) {
-            const IO *src = j < kMaxN ? Bm : Cm;
+            const IO *src = j < NM ? Bm : Cm;
             v = to_f32(src[(((long long)b * K + k) * N + n) * L + t]);
         }
         tile[j][tt] = v;
     }
     __syncthreads();
     for (int i = threadIdx.x; i < 64 * kBC; i += 256) {
-        const int tt = i >> 5, j = i & 31, t = t0 + tt;
+        const int tt = i / kBC, j = i % kBC, t = t0 + tt;
         if (t < L) out[(((long long)k * Bt + b) * L + t) * kBC + j] = tile[j][tt];
     }
 }
@@ -160,10 +163,11 @@ transpose_maps_kernel(const E *__restrict__ in, E *__restrict__ out, int maps, i
 //   epi warps   (NEW)  16 rows each (both branches of 16/NDIR channels):
 //                      readout sums, D*u, fusion, gate, stores; lane 0 of
 //                      the first epilogue warp also issues the B/C copies
-template <typename IO, int S, int NDIR, int R>
+template <typename IO, int S, int NDIR, int R, int NM = kMaxN>
 struct WsLayout {
     static constexpr int T = 32;
-    static constexpr int LPR = kMaxN / S;
+    static constexpr int kBC = 2 * NM;                      // floats per packed position
+    static constexpr int LPR = NM / S;
     static constexpr int ROWS = NDIR * R;                   // (branch, channel) rows
     static constexpr int NSW = ROWS * LPR / 32;
     static constexpr int NPW = ROWS / 16;
@@ -175,7 +179,10 @@ struct WsLayout {
     static constexpr int BC_STAGE = NDIR * BC_DIR;
     static constexpr int DW_ROW = T * 16 + 16;              // float4 per step, padded
     static constexpr int DW_STAGE = ROWS * DW_ROW;
-    static constexpr int YP_ROW = (T * LPR + LPR) * 4;      // padded: banks spread
+    // partial readouts stored per (row, step): lanes of more than two per
+    // channel sum pairs with a shuffle first, so the stage stays small
+    static constexpr int YP = LPR > 2 ? 2 : LPR;
+    static constexpr int YP_ROW = (T * YP + YP) * 4;        // padded: banks spread
     static constexpr int YP_STAGE = ROWS * YP_ROW;
     static constexpr int U_STAGE = ROWS * T * (int)sizeof(IO);   // u in walk order
     static constexpr int off_bc = 0;                        // 128-byte aligned
@@ -191,6 +198,7 @@ struct WsLayout {
     static constexpr int bytes = off_tab + 2 * ROWS * 4;     // D, then bias
 
     static_assert(S == 4 || S == 8 || S == 16, "S must be 4, 8 or 16");
+    static_assert(NM == 16 || NM == 32, "state capacity 16 or 32");
     static_assert((ROWS * LPR) % 32 == 0 && ROWS % 16 == 0, "whole warps per role");
     static_assert(R % 16 == 0 || (R == 8 && NDIR == 2),
                   "a prep warp takes 16 channels of one branch, or 8 of each");
@@ -218,10 +226,11 @@ __device__ __forceinline__ void chunk_geom(int c, int d, int L, int T, int &lo, 
 }
 
 // ------------------------------------------------------------------ kernel
-template <typename IO, int S, int NDIR, int R, int OUT>
-__global__ void __maxnreg__((WsLayout<IO, S, NDIR, R>::MAX_REGS))
+template <typename IO, int S, int NDIR, int R, int OUT, int NM = kMaxN>
+__global__ void __maxnreg__((WsLayout<IO, S, NDIR, R, NM>::MAX_REGS))
 bidir_scan_kernel(const BiParams P) {
-    using LY = WsLayout<IO, S, NDIR, R>;
+    using LY = WsLayout<IO, S, NDIR, R, NM>;
+    constexpr int kBC = LY::kBC;
     constexpr int T = LY::T;
     constexpr int LPR = LY::LPR;
     constexpr int NSW = LY::NSW, NPW = LY::NPW;
@@ -311,7 +320,17 @@ bidir_scan_kernel(const BiParams P) {
                 bstep = -kBC;
             }
             float *ypp = (float *)(sm + LY::off_yp + s2 * LY::YP_STAGE +
-                                   (s_dir * R + s_row) * LY::YP_ROW) + s_sg;
+                                   (s_dir * R + s_row) * LY::YP_ROW) + s_sg / (LPR / LY::YP);
+            // partial readout of one step to shared memory (more than two
+            // lanes per channel: pair sums, stored by the even lanes)
+            auto put = [&](int j, float yv) {
+                if constexpr (LPR > LY::YP) {
+                    yv += __shfl_xor_sync(0xffffffffu, yv, 1);
+                    if ((s_sg & 1) == 0) ypp[j * LY::YP] = yv;
+                } else {
+                    ypp[j * LY::YP] = yv;
+                }
+            };
             // UB steps at a time, in three passes so that independent work
             // is adjacent for the scheduler: (1) every shared-memory load of
             // the block; (2) every decay e = 2^(delta*A*log2e) (MUFU) and
@@ -326,7 +345,7 @@ bidir_scan_kernel(const BiParams P) {
 #pragma unroll
                     for (int k = 0; k < S / 4; ++k) {
                         bv[jj][k] = *(const float4 *)(bj + 4 * k);
-                        cv[jj][k] = *(const float4 *)(bj + kMaxN + 4 * k);
+                        cv[jj][k] = *(const float4 *)(bj + NM + 4 * k);
                     }
                 }
                 f2 e[UB][NP], bw[UB][NP];
@@ -371,7 +390,7 @@ bidir_scan_kernel(const BiParams P) {
                     ys[jj] = ylo + yhi;
                 }
 #pragma unroll
-                for (int jj = 0; jj < UB; ++jj) ypp[(j0 + jj) * LPR] = ys[jj];
+                for (int jj = 0; jj < UB; ++jj) put(j0 + jj, ys[jj]);
             };
             // one step (the chunk's tail)
             auto step = [&](int j) {
@@ -382,7 +401,7 @@ bidir_scan_kernel(const BiParams P) {
 #pragma unroll
                 for (int q = 0; q < NP; ++q) {
                     const float2 vb = *(const float2 *)(bj + 2 * q);
-                    const float2 vc = *(const float2 *)(bj + kMaxN + 2 * q);
+                    const float2 vc = *(const float2 *)(bj + NM + 2 * q);
                     float a0, a1;
                     upk(mul2(dd, A2[q]), a0, a1);
                     const f2 ee = pk(ex2_approx(a0), ex2_approx(a1));
@@ -391,7 +410,7 @@ bidir_scan_kernel(const BiParams P) {
                 }
                 float ylo, yhi;
                 upk(y2, ylo, yhi);
-                ypp[j * LPR] = ylo + yhi;
+                put(j, ylo + yhi);
             };
             int j = 0;
             for (; j + UB <= len; j += UB) block(j);
@@ -622,11 +641,11 @@ bidir_scan_kernel(const BiParams P) {
             const float *yp = (const float *)(sm + LY::off_yp + s2 * LY::YP_STAGE);
             const IO *us = (const IO *)(sm + LY::off_u + (c % LY::NU) * LY::U_STAGE);
             auto ypsum = [&](int row, int jj) -> float {
-                const float *ps = yp + row * (LY::YP_ROW / 4) + jj * LPR;
-                if constexpr (LPR == 4) {
+                const float *ps = yp + row * (LY::YP_ROW / 4) + jj * LY::YP;
+                if constexpr (LY::YP == 4) {
                     const float4 v = *(const float4 *)ps;
                     return (v.x + v.y) + (v.z + v.w);
-                } else if constexpr (LPR == 2) {
+                } else if constexpr (LY::YP == 2) {
                     const float2 v = *(const float2 *)ps;
                     return v.x + v.y;
                 } else {

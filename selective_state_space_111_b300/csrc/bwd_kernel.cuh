@@ -37,9 +37,11 @@ namespace ssm {
 namespace bwd {
 
 constexpr int T = 32;            // steps per chunk
-constexpr int CH = 16;           // channels per CTA
-constexpr int NT = CH * kMaxN;   // threads: lane = (channel, state)
+constexpr int NT = 256;          // threads: lane = (channel, state)
 constexpr int NWARP = NT / 32;
+// channels per CTA for a state capacity NM (16: two channels per warp,
+// 32: one channel per warp)
+template <int NM> __host__ __device__ constexpr int channels() { return NT / NM; }
 
 // One direction of one form.  Walk step w (0..L-1) is position
 // p = rev ? L-1-w : w of the position-ordered tensors (u, G, du); dt and
@@ -58,9 +60,9 @@ struct Pass {
     int rev, stream_rev;
     float *du;                 // fp32 [B, D, L], position order (this pass's own)
     float *ddt;                // fp32, indexed like dt (this pass's own)
-    float *pdB, *pdC;          // this pass's partials [ncg][B][L][16] (stream index)
-    float *pdA;                // [B][D][16]
-    float *hc;                 // chunk-start states [B][D][nch][16] (this pass's own)
+    float *pdB, *pdC;          // this pass's partials [ncg][B][L][NM] (stream index)
+    float *pdA;                // [B][D][NM]
+    float *hc;                 // chunk-start states [B][D][nch][NM] (this pass's own)
 };
 
 constexpr int kMaxPass = 4;
@@ -75,8 +77,10 @@ __device__ __forceinline__ float sigmoid_f(float x) {
 }
 // dynamic shared memory: dB, dC partials per warp, then the chunk's
 // recomputed states (step-major: thread-contiguous rows, no bank conflicts)
-constexpr int kPartFloats = NWARP * kMaxN * (T + 4);
-constexpr int kDynBytes = (2 * kPartFloats + T * NT) * (int)sizeof(float);
+template <int NM> __host__ __device__ constexpr int part_floats() { return NWARP * NM * (T + 4); }
+template <int NM> __host__ __device__ constexpr int dyn_bytes() {
+    return (2 * part_floats<NM>() + T * NT) * (int)sizeof(float);
+}
 
 // Sum of 8 values over the 16 lanes of a half-warp, by halving exchanges:
 // after the three halving levels lane l holds value (l>>3&1)*4 + (l>>2&1)*2
@@ -100,23 +104,46 @@ __device__ __forceinline__ float half_warp_sum8(const float (&v)[8], int lane) {
     return y + __shfl_xor_sync(0xffffffffu, y, 1);
 }
 
-template <typename IO>
+// The same over all 32 lanes (one channel per warp): after three halving
+// levels lane l holds value (l>>4&1)*4 + (l>>3&1)*2 + (l>>2&1) summed over 8
+// lanes; two more exchanges complete it (lanes l, l^1, l^2, l^3 agree).
+__device__ __forceinline__ float warp_sum8(const float (&v)[8], int lane) {
+    const bool b16 = lane & 16, b8 = lane & 8, b4 = lane & 4;
+    float w[4], x[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float send = b16 ? v[i] : v[i + 4];
+        w[i] = (b16 ? v[i + 4] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float send = b8 ? w[i] : w[i + 2];
+        x[i] = (b8 ? w[i + 2] : w[i]) + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    const float send = b4 ? x[0] : x[1];
+    float y = (b4 ? x[1] : x[0]) + __shfl_xor_sync(0xffffffffu, send, 4);
+    y += __shfl_xor_sync(0xffffffffu, y, 2);
+    return y + __shfl_xor_sync(0xffffffffu, y, 1);
+}
+
+template <typename IO, int NM>
 __global__ void __launch_bounds__(NT, 2)
 scan_bwd_kernel(const Params P) {
+    constexpr int CH = channels<NM>();
     constexpr int TP = T + 4;                  // padded rows: 16-byte aligned, banks spread
     __shared__ __align__(16) float sD[CH][TP], sU[CH][TP], sG[CH][TP], sS[CH][TP];
-    __shared__ __align__(16) float sBt[kMaxN][TP], sCt[kMaxN][TP];
+    __shared__ __align__(16) float sBt[NM][TP], sCt[NM][TP];
     __shared__ float sDu[CH][T + 1], sDd[CH][T + 1];
     __shared__ float sBias[CH], sDsk[CH];           // per-channel constants
-    // per-warp dB, dC partials of a chunk, [warp][state][step] (dynamic: kDynBytes)
+    // per-warp dB, dC partials of a chunk, [warp][state][step] (dynamic)
     extern __shared__ __align__(16) float dyn[];
-    float (*sPB)[kMaxN][TP] = reinterpret_cast<float (*)[kMaxN][TP]>(dyn);
-    float (*sPC)[kMaxN][TP] = reinterpret_cast<float (*)[kMaxN][TP]>(dyn + kPartFloats);
-    float (*sH)[NT] = reinterpret_cast<float (*)[NT]>(dyn + 2 * kPartFloats);
+    float (*sPB)[NM][TP] = reinterpret_cast<float (*)[NM][TP]>(dyn);
+    float (*sPC)[NM][TP] = reinterpret_cast<float (*)[NM][TP]>(dyn + part_floats<NM>());
+    float (*sH)[NT] = reinterpret_cast<float (*)[NT]>(dyn + 2 * part_floats<NM>());
 
     const Pass &ps = P.ps[blockIdx.z];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int ch = tid / kMaxN, n = tid % kMaxN;
+    const int ch = tid / NM, n = tid % NM;
     const int b = blockIdx.y, d0 = blockIdx.x * CH, d = d0 + ch;
     const int L = P.L, D = P.D, N = P.N, nch = P.nch;
     const bool cvalid = d < D, valid = cvalid && n < N;
@@ -126,7 +153,7 @@ scan_bwd_kernel(const Params P) {
     const IO *bp = (const IO *)ps.Bm + ps.bc_off + b * ps.bc_bstride;
     const IO *cp = (const IO *)ps.Cm + ps.bc_off + b * ps.bc_bstride;
     const IO *up = (const IO *)ps.u;
-    float *hcp = ps.hc + (((long long)b * D + d) * nch) * kMaxN + n;
+    float *hcp = ps.hc + (((long long)b * D + d) * nch) * NM + n;
     if (tid < CH) {
         const int dd = d0 + tid;
         sBias[tid] = (dd < D && ps.bias) ? ps.bias[dd] : 0.f;
@@ -137,21 +164,24 @@ scan_bwd_kernel(const Params P) {
     auto pos = [&](int w) { return ps.rev ? L - 1 - w : w; };
     auto sidx = [&](int w) { return ps.stream_rev ? w : pos(w); };
     // Chunk staging, software-pipelined: fetch() loads this thread's share
-    // of chunk c (2 of the CH x T per-channel values, 2 of the 16 x T B/C
+    // of chunk c (PC of the CH x T per-channel values, PB of the NM x T B/C
     // values) into registers; commit() transforms and stores it.  The next
     // chunk is fetched before the current one is computed.
-    constexpr int PER = CH * T / NT;              // per-channel values per thread
-    static_assert(PER * NT == CH * T && kMaxN * T == CH * T, "staging split");
-    float rdt[PER], ru[PER], rg[PER], rb[PER], rc[PER];
+    constexpr int PC = CH * T / NT, PB = NM * T / NT;
+    static_assert(PC * NT == CH * T && PB * NT == NM * T, "staging split");
+    float rdt[PC], ru[PC], rg[PC], rb[PB], rc[PB];
     auto fetch = [&](int c, bool full) {
 #pragma unroll
-        for (int r = 0; r < PER; ++r) {
+        for (int r = 0; r < PC; ++r) {
             const int i = tid + r * NT, cc = i / T, j = i % T, w = c * T + j, dd = d0 + cc;
             const bool ok = w < L && dd < D;
             rdt[r] = ok ? to_f32(dtp[(long long)dd * L + sidx(w)]) : 0.f;
             ru[r] = ok ? to_f32(up[((long long)b * D + dd) * L + pos(w)]) : 0.f;
             rg[r] = (ok && full) ? ps.G[((long long)b * D + dd) * L + pos(w)] : 0.f;
-            const int nn = i / T;
+        }
+#pragma unroll
+        for (int r = 0; r < PB; ++r) {
+            const int i = tid + r * NT, nn = i / T, j = i % T, w = c * T + j;
             const bool okb = w < L && nn < N;
             const long long o = (long long)nn * L + (okb ? sidx(w) : 0);
             rb[r] = okb ? to_f32(bp[o]) : 0.f;
@@ -160,7 +190,7 @@ scan_bwd_kernel(const Params P) {
     };
     auto commit = [&](int c) {
 #pragma unroll
-        for (int r = 0; r < PER; ++r) {
+        for (int r = 0; r < PC; ++r) {
             const int i = tid + r * NT, cc = i / T, j = i % T, w = c * T + j, dd = d0 + cc;
             float dl = 0.f, sg = 1.f;
             if (w < L && dd < D) {
@@ -176,8 +206,12 @@ scan_bwd_kernel(const Params P) {
             sS[cc][j] = sg;
             sU[cc][j] = ru[r];
             sG[cc][j] = ps.gscale * rg[r];
-            sBt[cc][j] = rb[r];                   // i / T is the state index here
-            sCt[cc][j] = rc[r];
+        }
+#pragma unroll
+        for (int r = 0; r < PB; ++r) {
+            const int i = tid + r * NT, nn = i / T, j = i % T;
+            sBt[nn][j] = rb[r];
+            sCt[nn][j] = rc[r];
         }
     };
 
@@ -185,7 +219,7 @@ scan_bwd_kernel(const Params P) {
     float h = 0.f;
     fetch(0, false);
     for (int c = 0; c < nch; ++c) {
-        if (cvalid) hcp[(long long)c * kMaxN] = h;
+        if (cvalid) hcp[(long long)c * NM] = h;
         commit(c);
         __syncthreads();
         if (c + 1 < nch) fetch(c + 1, false);
@@ -258,34 +292,46 @@ scan_bwd_kernel(const Params P) {
                 dA = fmaf(g * hp * a, dl, dA);
                 Gc = a * g;
             }
-            // du, ddelta of the 4 steps: sums over the channel's 16 states
-            const float tot = half_warp_sum8(red, lane);
-            if ((lane & 1) == 0) {
-                const int idx = ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
-                if (idx < 4) sDu[ch][j0 + idx] = tot;
-                else sDd[ch][j0 + idx - 4] = tot;
-            }
-            // dB, dC: sums over the warp's two channels (lanes < 16 keep dB)
-            const bool hi = lane >= 16;
-            float qv[4];
+            // du, ddelta of the 4 steps: sums over the channel's NM states
+            if constexpr (NM == 16) {
+                const float tot = half_warp_sum8(red, lane);
+                if ((lane & 1) == 0) {
+                    const int idx = ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+                    if (idx < 4) sDu[ch][j0 + idx] = tot;
+                    else sDd[ch][j0 + idx - 4] = tot;
+                }
+                // dB, dC: sums over the warp's two channels (lanes < 16 keep dB)
+                const bool hi = lane >= 16;
+                float qv[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float send = hi ? dBp[k] : dCp[k];
-                qv[k] = (hi ? dCp[k] : dBp[k]) + __shfl_xor_sync(0xffffffffu, send, 16);
+                for (int k = 0; k < 4; ++k) {
+                    const float send = hi ? dBp[k] : dCp[k];
+                    qv[k] = (hi ? dCp[k] : dBp[k]) + __shfl_xor_sync(0xffffffffu, send, 16);
+                }
+                *(float4 *)(hi ? &sPC[warp][n][j0] : &sPB[warp][n][j0]) =
+                    make_float4(qv[0], qv[1], qv[2], qv[3]);
+            } else {
+                const float tot = warp_sum8(red, lane);
+                if ((lane & 3) == 0) {
+                    const int idx = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+                    if (idx < 4) sDu[ch][j0 + idx] = tot;
+                    else sDd[ch][j0 + idx - 4] = tot;
+                }
+                // one channel per warp: its dB, dC go straight to the partials
+                *(float4 *)&sPB[warp][n][j0] = make_float4(dBp[0], dBp[1], dBp[2], dBp[3]);
+                *(float4 *)&sPC[warp][n][j0] = make_float4(dCp[0], dCp[1], dCp[2], dCp[3]);
             }
-            *(float4 *)(hi ? &sPC[warp][n][j0] : &sPB[warp][n][j0]) =
-                make_float4(qv[0], qv[1], qv[2], qv[3]);
         }
     };
     fetch(nch - 1, true);
-    float hnext = cvalid ? hcp[(long long)(nch - 1) * kMaxN] : 0.f;
+    float hnext = cvalid ? hcp[(long long)(nch - 1) * NM] : 0.f;
     for (int c = nch - 1; c >= 0; --c) {
         commit(c);
         __syncthreads();
         const float h0 = hnext;
         if (c > 0) {
             fetch(c - 1, true);
-            hnext = cvalid ? hcp[(long long)(c - 1) * kMaxN] : 0.f;
+            hnext = cvalid ? hcp[(long long)(c - 1) * NM] : 0.f;
         }
         const int len = min(T, L - c * T);
         if (len == T) chunk(BoolC<true>(), len, h0);
@@ -302,8 +348,8 @@ scan_bwd_kernel(const Params P) {
             }
         }
         // dB, dC partial of this CTA: sum over its warps
-        for (int i = tid; i < T * kMaxN; i += NT) {
-            const int j = i / kMaxN, nn = i % kMaxN, w = c * T + j;
+        for (int i = tid; i < T * NM; i += NT) {
+            const int j = i / NM, nn = i % NM, w = c * T + j;
             if (w < L) {
                 float sb = 0.f, sc = 0.f;
 #pragma unroll
@@ -311,14 +357,14 @@ scan_bwd_kernel(const Params P) {
                     sb += sPB[k][nn][j];
                     sc += sPC[k][nn][j];
                 }
-                const long long o = (((long long)blockIdx.x * P.B + b) * L + sidx(w)) * kMaxN + nn;
+                const long long o = (((long long)blockIdx.x * P.B + b) * L + sidx(w)) * NM + nn;
                 ps.pdB[o] = sb;
                 ps.pdC[o] = sc;
             }
         }
         __syncthreads();
     }
-    if (cvalid) ps.pdA[((long long)b * D + d) * kMaxN + n] = dA;
+    if (cvalid) ps.pdA[((long long)b * D + d) * NM + n] = dA;
 }
 
 // out[d] = scale * sum over (b, t) of (a + a2)[b][d][t] (* u[b][d][t] when u
@@ -410,7 +456,7 @@ __global__ void convert_kernel(const float *__restrict__ a, const float *__restr
 // [slot][B][L][16] (slot-major, fixed order)
 template <typename IO>
 __global__ void reduce_bc_kernel(const float *__restrict__ part, int nslot, int B, int L, int N,
-                                 IO *__restrict__ out, long long out_bstride) {
+                                 int nm, IO *__restrict__ out, long long out_bstride) {
     const long long total = (long long)B * L * N;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
          i += (long long)gridDim.x * blockDim.x) {
@@ -418,7 +464,7 @@ __global__ void reduce_bc_kernel(const float *__restrict__ part, int nslot, int 
         const long long bs = i / N;                  // b * L + s
         const int s = (int)(bs % L), b = (int)(bs / L);
         float acc = 0.f;
-        for (int k = 0; k < nslot; ++k) acc += part[((long long)k * B * L + bs) * kMaxN + nn];
+        for (int k = 0; k < nslot; ++k) acc += part[((long long)k * B * L + bs) * nm + nn];
         out[b * out_bstride + (long long)nn * L + s] = from_f32<IO>(acc);
     }
 }
@@ -426,14 +472,14 @@ __global__ void reduce_bc_kernel(const float *__restrict__ part, int nslot, int 
 // out[i] = sum over the nslot partials [slot][B][cols] of column i (fixed
 // order): dA (cols = D * 16, written [D][N]), dD and dbias (cols = D)
 __global__ void reduce_param_kernel(const float *__restrict__ part, int nslot, int B, int D,
-                                    int N, int per_state, float *__restrict__ out) {
-    const int cols = per_state ? D * kMaxN : D;
+                                    int N, int nm, int per_state, float *__restrict__ out) {
+    const int cols = per_state ? D * nm : D;
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < cols; i += gridDim.x * blockDim.x) {
-        if (per_state && i % kMaxN >= N) continue;
+        if (per_state && i % nm >= N) continue;
         float acc = 0.f;
         for (int k = 0; k < nslot; ++k)
             for (int b = 0; b < B; ++b) acc += part[((long long)k * B + b) * cols + i];
-        out[per_state ? (i / kMaxN) * N + i % kMaxN : i] = acc;
+        out[per_state ? (i / nm) * N + i % nm : i] = acc;
     }
 }
 

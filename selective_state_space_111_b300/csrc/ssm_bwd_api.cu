@@ -31,13 +31,17 @@ bool opt_f32(const float *p) { return p == nullptr || aligned(p, 4); }
 ssm_status check_sizes(ssm_dtype dt, int B, int D, int L, int N) {
     if (dt != SSM_F32 && dt != SSM_BF16 && dt != SSM_F16) return SSM_ERR_INVALID_ARG;
     if (B < 0 || D < 0 || L < 0 || N <= 0) return SSM_ERR_INVALID_ARG;
-    if (N > ssm::kMaxN) return SSM_ERR_UNSUPPORTED;
+    if (N > 2 * ssm::kMaxN) return SSM_ERR_UNSUPPORTED;      // up to 32 states
     if (B > 65535) return SSM_ERR_UNSUPPORTED;
     if (!fits((long long)D * L) || !fits((long long)N * L)) return SSM_ERR_UNSUPPORTED;
     return SSM_OK;
 }
 
 size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+// state capacity (16 or 32) and channels per backward CTA for N states
+int nm_of(int N) { return N <= ssm::kMaxN ? ssm::kMaxN : 2 * ssm::kMaxN; }
+int ch_of(int N) { return ssm::bwd::NT / nm_of(N); }
 
 template <typename IO> constexpr ssm_dtype dtype_of() { return SSM_BF16; }
 template <> constexpr ssm_dtype dtype_of<float>() { return SSM_F32; }
@@ -54,7 +58,7 @@ BwdWs bwd_ws(int op, ssm_dtype dt, int B, int D, int L, int N, bool sep_ub) {
     (void)sep_ub;
     const size_t n = (size_t)B * D * L;
     const int npass = op == 0 ? 1 : op == 3 ? 4 : 2;
-    const int ncg = (D + ssm::bwd::CH - 1) / ssm::bwd::CH;
+    const int nm = nm_of(N), ncg = (D + ch_of(N) - 1) / ch_of(N);
     const int nch = (L + ssm::bwd::T - 1) / ssm::bwd::T;
     BwdWs w{};
     size_t off = 256;
@@ -76,11 +80,11 @@ BwdWs bwd_ws(int op, ssm_dtype dt, int B, int D, int L, int N, bool sep_ub) {
     w.du = take(n * 4 * npass);
     w.ddt = take(n * 4 * npass);
     // chunk-start states: one region per direction (they run concurrently)
-    w.hc = take((size_t)npass * B * D * nch * ssm::kMaxN * 4);
-    const size_t part = (size_t)npass * ncg * B * L * ssm::kMaxN * 4;
+    w.hc = take((size_t)npass * B * D * nch * nm * 4);
+    const size_t part = (size_t)npass * ncg * B * L * nm * 4;
     w.pdB = take(part);
     w.pdC = take(part);
-    w.pdA = take((size_t)npass * B * D * ssm::kMaxN * 4);
+    w.pdA = take((size_t)npass * B * D * nm * 4);
     w.total = off;
     return w;
 }
@@ -96,9 +100,9 @@ ssm_status last_error() {
 
 // One scan_bwd_kernel launch for all directions (grid: channel groups x
 // batch x directions).
-template <typename IO>
-ssm_status launch_passes(const Pass *ps, int npass, int B, int D, int L, int N, int sp,
-                         cudaStream_t st) {
+template <typename IO, int NM>
+ssm_status launch_passes_nm(const Pass *ps, int npass, int B, int D, int L, int N, int sp,
+                            cudaStream_t st) {
     ssm::bwd::Params P{};
     for (int k = 0; k < npass; ++k) P.ps[k] = ps[k];
     P.B = B;
@@ -107,15 +111,23 @@ ssm_status launch_passes(const Pass *ps, int npass, int B, int D, int L, int N, 
     P.N = N;
     P.nch = (L + ssm::bwd::T - 1) / ssm::bwd::T;
     P.delta_softplus = sp ? 1 : 0;
-    dim3 grid((D + ssm::bwd::CH - 1) / ssm::bwd::CH, B, npass);
-    auto *kern = &ssm::bwd::scan_bwd_kernel<IO>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             ssm::bwd::kDynBytes) != cudaSuccess) {
+    constexpr int CH = ssm::bwd::channels<NM>();
+    constexpr int dyn = ssm::bwd::dyn_bytes<NM>();
+    dim3 grid((D + CH - 1) / CH, B, npass);
+    auto *kern = &ssm::bwd::scan_bwd_kernel<IO, NM>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn) !=
+        cudaSuccess) {
         cudaGetLastError();
         return SSM_ERR_CUDA;
     }
-    kern<<<grid, ssm::bwd::NT, ssm::bwd::kDynBytes, st>>>(P);
+    kern<<<grid, ssm::bwd::NT, dyn, st>>>(P);
     return last_error();
+}
+template <typename IO>
+ssm_status launch_passes(const Pass *ps, int npass, int B, int D, int L, int N, int sp,
+                         cudaStream_t st) {
+    if (N <= ssm::kMaxN) return launch_passes_nm<IO, ssm::kMaxN>(ps, npass, B, D, L, N, sp, st);
+    return launch_passes_nm<IO, 2 * ssm::kMaxN>(ps, npass, B, D, L, N, sp, st);
 }
 
 template <typename IO>
@@ -144,7 +156,7 @@ template <typename IO>
 ssm_status reduce_bc(const float *part, int nslot, int B, int L, int N, void *out,
                      long long out_bstride, cudaStream_t st) {
     ssm::bwd::reduce_bc_kernel<IO><<<grid1d((long long)B * L * N), 256, 0, st>>>(
-        part, nslot, B, L, N, (IO *)out, out_bstride);
+        part, nslot, B, L, N, nm_of(N), (IO *)out, out_bstride);
     return last_error();
 }
 
@@ -161,8 +173,8 @@ ssm_status channel_sum(const float *a, const float *a2, long long a_bstride, con
 ssm_status reduce_param(const float *part, int nslot, int B, int D, int N, bool per_state,
                         float *out, cudaStream_t st) {
     if (out == nullptr) return SSM_OK;
-    const int cols = per_state ? D * ssm::kMaxN : D;
-    ssm::bwd::reduce_param_kernel<<<grid1d(cols), 256, 0, st>>>(part, nslot, B, D, N,
+    const int cols = per_state ? D * nm_of(N) : D;
+    ssm::bwd::reduce_param_kernel<<<grid1d(cols), 256, 0, st>>>(part, nslot, B, D, N, nm_of(N),
                                                                 per_state ? 1 : 0, out);
     return last_error();
 }
@@ -177,9 +189,9 @@ ssm_status reduce_param(const float *part, int nslot, int B, int D, int N, bool 
 struct Parts {
     const float *pdB, *pdC, *pdA;
     int ncg, B, D, L, N;
-    const float *dB_slot(int p) const { return pdB + (size_t)p * ncg * B * L * ssm::kMaxN; }
-    const float *dC_slot(int p) const { return pdC + (size_t)p * ncg * B * L * ssm::kMaxN; }
-    const float *dA_slot(int p) const { return pdA + (size_t)p * B * D * ssm::kMaxN; }
+    const float *dB_slot(int p) const { return pdB + (size_t)p * ncg * B * L * nm_of(N); }
+    const float *dC_slot(int p) const { return pdC + (size_t)p * ncg * B * L * nm_of(N); }
+    const float *dA_slot(int p) const { return pdA + (size_t)p * B * D * nm_of(N); }
 };
 
 Parts parts_of(char *ws, const BwdWs &w, int B, int D, int L, int N) {
@@ -187,7 +199,7 @@ Parts parts_of(char *ws, const BwdWs &w, int B, int D, int L, int N) {
     q.pdB = (const float *)(ws + w.pdB);
     q.pdC = (const float *)(ws + w.pdC);
     q.pdA = (const float *)(ws + w.pdA);
-    q.ncg = (D + ssm::bwd::CH - 1) / ssm::bwd::CH;
+    q.ncg = (D + ch_of(N) - 1) / ch_of(N);
     q.B = B;
     q.D = D;
     q.L = L;
@@ -196,14 +208,14 @@ Parts parts_of(char *ws, const BwdWs &w, int B, int D, int L, int N) {
 }
 
 // Pass p's parameter and scratch pointers into the workspace.
-Pass base_pass(char *ws, const BwdWs &w, int p, int B, int D, int L) {
+Pass base_pass(char *ws, const BwdWs &w, int p, int B, int D, int L, int N) {
     Pass ps{};
-    const int ncg = (D + ssm::bwd::CH - 1) / ssm::bwd::CH;
-    ps.pdB = (float *)(ws + w.pdB) + (size_t)p * ncg * B * L * ssm::kMaxN;
-    ps.pdC = (float *)(ws + w.pdC) + (size_t)p * ncg * B * L * ssm::kMaxN;
-    ps.pdA = (float *)(ws + w.pdA) + (size_t)p * B * D * ssm::kMaxN;
+    const int nm = nm_of(N), ncg = (D + ch_of(N) - 1) / ch_of(N);
+    ps.pdB = (float *)(ws + w.pdB) + (size_t)p * ncg * B * L * nm;
+    ps.pdC = (float *)(ws + w.pdC) + (size_t)p * ncg * B * L * nm;
+    ps.pdA = (float *)(ws + w.pdA) + (size_t)p * B * D * nm;
     const int nch = (L + ssm::bwd::T - 1) / ssm::bwd::T;
-    ps.hc = (float *)(ws + w.hc) + (size_t)p * B * D * nch * ssm::kMaxN;
+    ps.hc = (float *)(ws + w.hc) + (size_t)p * B * D * nch * nm;
     ps.G = (const float *)(ws + w.G);
     ps.gscale = 1.f;
     return ps;
@@ -244,7 +256,7 @@ ssm_status seq_bwd(int op, int B, int D, int L, int N, const void *u, const void
     TRY(gate_bwd<IO>(dout, z, ypre, G, dz, n, st));
     // (3) one pass per direction
     const long long DL = (long long)D * L, NL = (long long)N * L;
-    Pass p0 = base_pass(ws, w, 0, B, D, L);
+    Pass p0 = base_pass(ws, w, 0, B, D, L, N);
     p0.dt = delta;
     p0.dt_off = 0;
     p0.dt_bstride = DL;
@@ -264,7 +276,7 @@ ssm_status seq_bwd(int op, int B, int D, int L, int N, const void *u, const void
     Pass pp[2] = {p0, p0};
     if (op != 0) {
         Pass p1 = p0;
-        Pass q = base_pass(ws, w, 1, B, D, L);
+        Pass q = base_pass(ws, w, 1, B, D, L, N);
         p1.pdB = q.pdB;
         p1.pdC = q.pdC;
         p1.pdA = q.pdA;
@@ -335,7 +347,7 @@ ssm_status ss2d_bwd_run(int B, int D, int H, int W, int N, const void *x, const 
     float *du = (float *)(ws + w.du);                 // [4][B][D][L], one map per direction
     Pass pp[4];
     for (int k = 0; k < K; ++k) {
-        Pass ps = base_pass(ws, w, k, B, D, L);
+        Pass ps = base_pass(ws, w, k, B, D, L, N);
         const bool col = k == 1 || k == 3;
         ps.dt = delta;
         ps.dt_off = k * DL;
@@ -383,7 +395,7 @@ extern "C" {
 size_t ssm_bwd_workspace_bytes(ssm_op op, ssm_dtype dt, int B, int D, int L_or_HW, int N, int K,
                                int separate_u_b) {
     if (dt != SSM_F32 && dt != SSM_BF16 && dt != SSM_F16) return (size_t)-1;
-    if (B < 0 || D < 0 || L_or_HW < 0 || N <= 0 || N > ssm::kMaxN) return (size_t)-1;
+    if (B < 0 || D < 0 || L_or_HW < 0 || N <= 0 || N > 2 * ssm::kMaxN) return (size_t)-1;
     int o;
     switch (op) {
     case SSM_OP_SELECTIVE_SCAN: o = 0; break;

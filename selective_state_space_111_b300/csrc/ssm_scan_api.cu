@@ -25,7 +25,7 @@ bool fits(long long v) { return v >= 0 && v <= 0x7fffffffLL; }
 ssm_status check_common(ssm_dtype dt, int B, int D, int L, int N) {
     if (dt != SSM_F32 && dt != SSM_BF16 && dt != SSM_F16) return SSM_ERR_INVALID_ARG;
     if (B < 0 || D < 0 || L < 0 || N <= 0) return SSM_ERR_INVALID_ARG;
-    if (N > ssm::kMaxN) return SSM_ERR_UNSUPPORTED;
+    if (N > 2 * ssm::kMaxN) return SSM_ERR_UNSUPPORTED;      // up to 32 states
     if (B > 65535) return SSM_ERR_UNSUPPORTED;                 // grid.y
     if (!fits((long long)D * L) || !fits((long long)N * L)) return SSM_ERR_UNSUPPORTED;
     return SSM_OK;
@@ -59,21 +59,23 @@ constexpr int kBiG2 = SSM_BI_G2;           // channels per CTA, two branches
 constexpr int kBiG1 = SSM_BI_G1;           // channels per CTA, one branch
 
 int bi_chunks(int L) { return (L + kBiT - 1) / kBiT; }
-size_t bc_bytes(int B, int L) { return (size_t)B * L * ssm::kBC * sizeof(float); }
+// state capacity of the kernels that handle N states (16 or 32)
+int nm_of(int N) { return N <= ssm::kMaxN ? ssm::kMaxN : 2 * ssm::kMaxN; }
+size_t bc_bytes(int B, int L, int nm) { return (size_t)B * L * 2 * nm * sizeof(float); }
 
 struct BiWs {
     size_t bc0, bc1, w, total;
 };
 // bc_sets: 1 (single, v1) or 2 (v2); stash only with two branches.
-BiWs bi_ws(int bc_sets, int ndir, int B, int D, int L) {
+BiWs bi_ws(int bc_sets, int ndir, int B, int D, int L, int nm) {
     BiWs w;
     size_t off = kHeaderBytes;
     w.bc0 = off;
-    off += bc_bytes(B, L);
+    off += bc_bytes(B, L, nm);
     w.bc1 = w.bc0;
     if (bc_sets == 2) {
         w.bc1 = off;
-        off += bc_bytes(B, L);
+        off += bc_bytes(B, L, nm);
     }
     w.w = 0;
     if (ndir == 2 && bi_chunks(L) > 1) {
@@ -84,11 +86,11 @@ BiWs bi_ws(int bc_sets, int ndir, int B, int D, int L) {
     return w;
 }
 
-template <typename IO>
+template <typename IO, int NM>
 ssm_status launch_pack(const void *Bm, const void *Cm, float *out, int B, int N, int L,
                        unsigned *status, cudaStream_t st, int K = 1) {
     dim3 grid((L + 63) / 64, B, K);
-    ssm::pack_bc_kernel<IO><<<grid, 256, 0, st>>>((const IO *)Bm, (const IO *)Cm, out, N, L,
+    ssm::pack_bc_kernel<IO, NM><<<grid, 256, 0, st>>>((const IO *)Bm, (const IO *)Cm, out, N, L,
                                                   status);
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
@@ -102,10 +104,10 @@ thread_local int t_cta_channels = 0;
 // this host thread withholds, to exercise the bounded waits.
 thread_local int t_withhold = -1;
 
-template <typename IO, int S, int NDIR, int G, int OUT = ssm::OUT_Y>
+template <typename IO, int S, int NDIR, int G, int OUT, int NM>
 ssm_status launch_bidir(const ssm::BiParams &P, cudaStream_t st, bool last = true) {
-    using LY = ssm::WsLayout<IO, S, NDIR, G>;
-    auto *kern = &ssm::bidir_scan_kernel<IO, S, NDIR, G, OUT>;
+    using LY = ssm::WsLayout<IO, S, NDIR, G, NM>;
+    auto *kern = &ssm::bidir_scan_kernel<IO, S, NDIR, G, OUT, NM>;
     // Raising the dynamic shared-memory limit and asking for the largest
     // shared-memory carveout are cheap and idempotent; without the carveout
     // the driver may pick one that fits fewer CTAs per SM.
@@ -143,15 +145,15 @@ ssm_status launch_bidir(const ssm::BiParams &P, cudaStream_t st, bool last = tru
 // fewer (branch, channel) rows on the busiest SM -- small B * D, where CTAs
 // of 16 channels leave SMs idle.  An SM holds LY::CPS CTAs at a time; a
 // busier SM runs them in waves.
-template <typename IO, int G>
+template <typename IO, int G, int NM>
 long long busiest_sm_rows(int B, int D, int nsm) {
-    constexpr int cps = ssm::WsLayout<IO, kBiS, 2, G>::CPS;
+    constexpr int cps = ssm::WsLayout<IO, kBiS, 2, G, NM>::CPS;
     const long long ctas = (long long)((D + G - 1) / G) * B;
     const long long per = (ctas + nsm - 1) / nsm;
     const long long slots = per <= cps ? per : (per + cps - 1) / cps * cps;
     return slots * G;
 }
-template <typename IO>
+template <typename IO, int NM>
 bool narrow_ctas(int B, int D) {
     int dev = 0, nsm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -160,31 +162,38 @@ bool narrow_ctas(int B, int D) {
         cudaGetLastError();
         return false;
     }
-    return busiest_sm_rows<IO, 8>(B, D, nsm) < busiest_sm_rows<IO, kBiG2>(B, D, nsm);
+    return busiest_sm_rows<IO, 8, NM>(B, D, nsm) < busiest_sm_rows<IO, kBiG2, NM>(B, D, nsm);
 }
-template <typename IO, int OUT = ssm::OUT_Y>
+template <typename IO, int OUT, int NM>
 ssm_status launch_two_branch(const ssm::BiParams &P, cudaStream_t st, bool last = true) {
     const bool narrow = t_cta_channels == 8 ? true
                         : t_cta_channels == 16 ? false
-                                               : narrow_ctas<IO>(P.B, P.D);
-    if (narrow) return launch_bidir<IO, kBiS, 2, 8, OUT>(P, st, last);
-    return launch_bidir<IO, kBiS, 2, kBiG2, OUT>(P, st, last);
+                                               : narrow_ctas<IO, NM>(P.B, P.D);
+    if (narrow) return launch_bidir<IO, kBiS, 2, 8, OUT, NM>(P, st, last);
+    return launch_bidir<IO, kBiS, 2, kBiG2, OUT, NM>(P, st, last);
 }
 
 // Packs B/C (one or two sets), then runs the scan kernel.
-template <typename IO, int NDIR>
-ssm_status run_bidir(ssm::BiParams P, const void *Bm, const void *Cm, const void *Bm_b,
-                     const void *Cm_b, bool two_sets, cudaStream_t st) {
-    ssm_status s = launch_pack<IO>(Bm, Cm, const_cast<float *>(P.br[0].bc), P.B, P.N, P.L,
+template <typename IO, int NDIR, int NM>
+ssm_status run_bidir_nm(ssm::BiParams P, const void *Bm, const void *Cm, const void *Bm_b,
+                        const void *Cm_b, bool two_sets, cudaStream_t st) {
+    ssm_status s = launch_pack<IO, NM>(Bm, Cm, const_cast<float *>(P.br[0].bc), P.B, P.N, P.L,
                                    P.status, st);
     if (s != SSM_OK) return s;
     if (two_sets) {
-        s = launch_pack<IO>(Bm_b, Cm_b, const_cast<float *>(P.br[1].bc), P.B, P.N, P.L,
+        s = launch_pack<IO, NM>(Bm_b, Cm_b, const_cast<float *>(P.br[1].bc), P.B, P.N, P.L,
                             nullptr, st);
         if (s != SSM_OK) return s;
     }
-    if (NDIR == 2) return launch_two_branch<IO>(P, st);
-    return launch_bidir<IO, kBiS, 1, kBiG1>(P, st);
+    if (NDIR == 2) return launch_two_branch<IO, ssm::OUT_Y, NM>(P, st);
+    return launch_bidir<IO, kBiS, 1, kBiG1, ssm::OUT_Y, NM>(P, st);
+}
+template <typename IO, int NDIR>
+ssm_status run_bidir(ssm::BiParams P, const void *Bm, const void *Cm, const void *Bm_b,
+                     const void *Cm_b, bool two_sets, cudaStream_t st) {
+    if (P.N <= ssm::kMaxN)
+        return run_bidir_nm<IO, NDIR, ssm::kMaxN>(P, Bm, Cm, Bm_b, Cm_b, two_sets, st);
+    return run_bidir_nm<IO, NDIR, 2 * ssm::kMaxN>(P, Bm, Cm, Bm_b, Cm_b, two_sets, st);
 }
 
 // Shared body of v1 / v2 (v1 passes the forward tensors for both branches
@@ -205,7 +214,7 @@ ssm_status bidirectional(ssm_dtype dt, int B, int D, int L, int N, const void *u
         !opt_f32_ok(bias) || !opt_f32_ok(bias_b))
         return SSM_ERR_INVALID_ARG;
     if ((long long)B * D * L == 0) return SSM_OK;
-    const BiWs lay = bi_ws(two_sets ? 2 : 1, 2, B, D, L);
+    const BiWs lay = bi_ws(two_sets ? 2 : 1, 2, B, D, L, nm_of(N));
     if (ws == nullptr || ws_bytes < lay.total || !aligned(ws, 16)) return SSM_ERR_WORKSPACE;
     char *wsb = (char *)ws;
     ssm::BiParams P{};
@@ -245,12 +254,12 @@ struct SsWs {
     size_t bc, xt, r1, r2, total;
 };
 size_t round128(size_t v) { return (v + 127) & ~(size_t)127; }
-SsWs ss2d_ws(ssm_dtype dt, int B, int D, int L) {
+SsWs ss2d_ws(ssm_dtype dt, int B, int D, int L, int nm) {
     const size_t es = dt == SSM_F32 ? 4 : 2;
     const size_t n = (size_t)B * D * L;
     SsWs w;
     w.bc = kHeaderBytes;
-    w.xt = w.bc + 4 * bc_bytes(B, L);
+    w.xt = w.bc + 4 * bc_bytes(B, L, nm);
     w.r1 = w.xt + round128(n * es);
     w.r2 = w.r1 + round128(n * 4);
     w.total = w.r2 + round128(n * 4);
@@ -264,8 +273,8 @@ ssm_status launch_transpose(const E *in, E *out, int maps, int R, int C, cudaStr
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
-template <typename IO>
-ssm_status ss2d_run(int B, int D, int H, int W, int N, const void *x, const void *delta,
+template <typename IO, int NM>
+ssm_status ss2d_run_nm(int B, int D, int H, int W, int N, const void *x, const void *delta,
                     const float *A, const void *Bm, const void *Cm, const float *Dskip,
                     const void *z, const float *bias, int delta_softplus, void *y, char *wsb,
                     const SsWs &lay, cudaStream_t st) {
@@ -275,7 +284,7 @@ ssm_status ss2d_run(int B, int D, int H, int W, int N, const void *x, const void
     IO *xt = (IO *)(wsb + lay.xt);
     float *r1 = (float *)(wsb + lay.r1), *r2 = (float *)(wsb + lay.r2);
     unsigned *status = (unsigned *)wsb;
-    ssm_status s = launch_pack<IO>(Bm, Cm, bcK, B, N, L, status, st, 4);
+    ssm_status s = launch_pack<IO, NM>(Bm, Cm, bcK, B, N, L, status, st, 4);
     if (s != SSM_OK) return s;
     s = launch_transpose<IO>((const IO *)x, xt, B * D, H, W, st);
     if (s != SSM_OK) return s;
@@ -284,7 +293,7 @@ ssm_status ss2d_run(int B, int D, int H, int W, int N, const void *x, const void
         br.dt = delta;
         br.dt_off = k * DL;
         br.u = u;
-        br.bc = bcK + (long long)k * B * L * ssm::kBC;
+        br.bc = bcK + (long long)k * B * L * 2 * NM;
         br.A = A + (long long)k * D * N;
         br.Dskip = Dskip ? Dskip + (long long)k * D : nullptr;
         br.bias = bias ? bias + (long long)k * D : nullptr;
@@ -306,7 +315,7 @@ ssm_status ss2d_run(int B, int D, int H, int W, int N, const void *x, const void
     P.br[1] = branch(3, xt, 1);
     P.W = r1;
     P.acc_out = r2;
-    s = launch_two_branch<IO, ssm::OUT_ACC>(P, st, false);
+    s = launch_two_branch<IO, ssm::OUT_ACC, NM>(P, st, false);
     if (s != SSM_OK) return s;
     // Wa (R1) = Wt (R2) transposed back to H x W
     s = launch_transpose<float>(r2, r1, B * D, W, H, st);
@@ -319,7 +328,18 @@ ssm_status ss2d_run(int B, int D, int H, int W, int N, const void *x, const void
     P.W = r2;
     P.acc_in = r1;
     P.acc_out = nullptr;
-    return launch_two_branch<IO, ssm::OUT_ADD_Y>(P, st);
+    return launch_two_branch<IO, ssm::OUT_ADD_Y, NM>(P, st);
+}
+template <typename IO>
+ssm_status ss2d_run(int B, int D, int H, int W, int N, const void *x, const void *delta,
+                    const float *A, const void *Bm, const void *Cm, const float *Dskip,
+                    const void *z, const float *bias, int delta_softplus, void *y, char *wsb,
+                    const SsWs &lay, cudaStream_t st) {
+    if (N <= ssm::kMaxN)
+        return ss2d_run_nm<IO, ssm::kMaxN>(B, D, H, W, N, x, delta, A, Bm, Cm, Dskip, z, bias,
+                                           delta_softplus, y, wsb, lay, st);
+    return ss2d_run_nm<IO, 2 * ssm::kMaxN>(B, D, H, W, N, x, delta, A, Bm, Cm, Dskip, z, bias,
+                                           delta_softplus, y, wsb, lay, st);
 }
 
 // ---- fixed scratch of the allocation-free entry point
@@ -368,7 +388,7 @@ ssm_status selective_scan_fwd(ssm_dtype dt, int B, int D, int L, int N, const vo
         !opt_f32_ok(delta_bias))
         return SSM_ERR_INVALID_ARG;
     if ((long long)B * D * L == 0) return SSM_OK;
-    const BiWs lay = bi_ws(1, 1, B, D, L);
+    const BiWs lay = bi_ws(1, 1, B, D, L, nm_of(N));
     if (workspace == nullptr || ws_bytes < lay.total || !aligned(workspace, 16))
         return SSM_ERR_WORKSPACE;
     char *wsb = (char *)workspace;
@@ -427,7 +447,8 @@ ssm_status bimamba_scan_fwd_v2_noalloc(ssm_dtype dt, int B, int D, int L, int N,
                                        float out_scale, void *y, ssm_stream_t stream) {
     ssm_status s = check_common(dt, B, D, L, N);
     if (s != SSM_OK) return s;
-    if (bi_ws(2, 2, B, D, L).total > SSM_STATIC_SCRATCH_BYTES) return SSM_ERR_SCRATCH_LIMIT;
+    if (bi_ws(2, 2, B, D, L, nm_of(N)).total > SSM_STATIC_SCRATCH_BYTES)
+        return SSM_ERR_SCRATCH_LIMIT;
     void *scratch = nullptr;
     s = static_scratch(&scratch);
     if (s != SSM_OK) return s;
@@ -453,7 +474,7 @@ ssm_status ss2d_scan_fwd(ssm_dtype dt, int B, int D, int H, int W, int N, int K,
         !opt_f32_ok(delta_bias))
         return SSM_ERR_INVALID_ARG;
     if ((long long)B * D * L == 0) return SSM_OK;
-    const SsWs lay = ss2d_ws(dt, B, D, L);
+    const SsWs lay = ss2d_ws(dt, B, D, L, nm_of(N));
     if (workspace == nullptr || ws_bytes < lay.total || !aligned(workspace, 16))
         return SSM_ERR_WORKSPACE;
     cudaStream_t st = (cudaStream_t)stream;
@@ -468,19 +489,19 @@ ssm_status ss2d_scan_fwd(ssm_dtype dt, int B, int D, int H, int W, int N, int K,
 }
 
 size_t ssm_workspace_bytes(ssm_op op, ssm_dtype dt, int B, int D, int L_or_HW, int N, int K) {
-    (void)N;
     if (dt != SSM_F32 && dt != SSM_BF16 && dt != SSM_F16) return (size_t)-1;
-    if (B < 0 || D < 0 || L_or_HW < 0) return (size_t)-1;
+    if (B < 0 || D < 0 || L_or_HW < 0 || N <= 0 || N > 2 * ssm::kMaxN) return (size_t)-1;
+    const int nm = nm_of(N);
     switch (op) {
     case SSM_OP_SELECTIVE_SCAN:
-        return bi_ws(1, 1, B, D, L_or_HW).total;
+        return bi_ws(1, 1, B, D, L_or_HW, nm).total;
     case SSM_OP_BIMAMBA_V1:
-        return bi_ws(1, 2, B, D, L_or_HW).total;
+        return bi_ws(1, 2, B, D, L_or_HW, nm).total;
     case SSM_OP_BIMAMBA_V2:
-        return bi_ws(2, 2, B, D, L_or_HW).total;
+        return bi_ws(2, 2, B, D, L_or_HW, nm).total;
     case SSM_OP_SS2D:
         if (K != 4) return (size_t)-1;
-        return ss2d_ws(dt, B, D, L_or_HW).total;
+        return ss2d_ws(dt, B, D, L_or_HW, nm).total;
     }
     return (size_t)-1;
 }

@@ -64,7 +64,8 @@ def single(lib, *, dt=1, B=1, D=1, L=8, N=16, u=FAKE, delta=FAKE, A=FAKE, Bm=FAK
 
 
 def test_invalid_arguments_are_rejected_before_launch(lib):
-    assert single(lib, N=17) == 2                   # N > 16: unsupported
+    assert single(lib, N=33) == 2                   # N > 32: unsupported
+    assert single(lib, N=32, y=None) == 1           # 32 states are supported: only y is missing
     assert single(lib, N=0) == 1
     assert single(lib, L=-1) == 1
     assert single(lib, dt=5) == 1
@@ -109,7 +110,7 @@ def test_bwd_workspace_bytes(lib):
     neg = ctypes.c_size_t(-1).value
     assert wb(0, 1, 0, 8, 100, 16, 4, 0) == 0                   # empty problem
     assert wb(0, 7, 1, 8, 100, 16, 4, 0) == neg                  # bad dtype
-    assert wb(0, 1, 1, 8, 100, 17, 4, 0) == neg                  # N > 16
+    assert wb(0, 1, 1, 8, 100, 33, 4, 0) == neg                  # N > 32
     assert wb(3, 1, 1, 8, 100, 16, 2, 0) == neg                  # SS2D needs K = 4
     single = wb(0, 1, 2, 40, 300, 16, 4, 0)
     v1, v2 = wb(1, 1, 2, 40, 300, 16, 4, 0), wb(2, 1, 2, 40, 300, 16, 4, 0)
@@ -127,7 +128,7 @@ def bwd_single(lib, *, dt=1, B=1, D=1, L=8, N=16, u=FAKE, z=None, dz=None, du=FA
 
 
 def test_bwd_invalid_arguments_are_rejected_before_launch(lib):
-    assert bwd_single(lib, N=17) == 2
+    assert bwd_single(lib, N=33) == 2
     assert bwd_single(lib, L=-1) == 1
     assert bwd_single(lib, u=None) == 1                     # required input
     assert bwd_single(lib, du=None) == 1                    # required gradient output

@@ -103,7 +103,7 @@ def check(spec, seed):
 
 
 SHAPES = [(1, 1, 1, 16), (2, 3, 33, 16), (1, 17, 64, 16), (2, 20, 97, 16), (1, 9, 40, 7),
-          (2, 4, 129, 1)]
+          (2, 4, 129, 1), (2, 11, 70, 32), (1, 9, 40, 24)]   # d_state 32 and 17..32
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16", "f16"])
@@ -136,6 +136,10 @@ def test_v2_bwd(io, shape, shared_u):
 def test_ss2d_bwd(io, shape):
     B, D, H, W = shape
     check(Spec("ss2d", io, B=B, D=D, H=H, W=W, perturb=True), 8000 + H * W)
+
+
+def test_ss2d_bwd_d_state_32():
+    check(Spec("ss2d", "f32", B=1, D=10, H=5, W=7, N=32, perturb=True), 8600)
 
 
 @pytest.mark.parametrize("op", ["single", "v1", "v2", "ss2d"])

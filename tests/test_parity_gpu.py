@@ -34,7 +34,8 @@ def check(spec, seed, ref=None):
 # L spans: shorter than a chunk, one chunk, chunk +- 1, several chunks with a
 # ragged tail; D spans partial CTAs; N < 16 exercises the state mask.
 SHAPES = [(1, 1, 1, 16), (2, 3, 5, 16), (1, 17, 31, 16), (2, 16, 32, 16), (1, 5, 33, 16),
-          (3, 20, 97, 16), (2, 40, 197, 16), (1, 9, 64, 7), (2, 4, 129, 1), (1, 33, 300, 16)]
+          (3, 20, 97, 16), (2, 40, 197, 16), (1, 9, 64, 7), (2, 4, 129, 1), (1, 33, 300, 16),
+          (2, 19, 77, 32), (1, 9, 40, 24)]   # d_state 32 and a 17..32 size
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16", "f16"])
@@ -78,6 +79,14 @@ SS2D_SHAPES = [(1, 1, 1, 1), (1, 2, 2, 3), (2, 3, 5, 7), (1, 17, 8, 8), (2, 5, 3
 def test_ss2d(io, shape, cta):
     B, D, H, W = shape
     check(Spec("ss2d", io, B=B, D=D, H=H, W=W, perturb=True), 4000 + H * W)
+
+
+@pytest.mark.parametrize("op", ["single", "v1", "v2", "ss2d"])
+def test_d_state_32(op, cta):
+    # 32 states (the pages recommend 16-32): the 32-state kernels
+    kw = dict(H=7, W=9) if op == "ss2d" else dict(L=150)
+    check(Spec(op, "bf16", B=2, D=24, N=32, perturb=True,
+               out_scale=0.5 if op == "v2" else 1.0, **kw), 4500)
 
 
 # ------------------------------------------------------------ options
