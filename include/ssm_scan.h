@@ -164,6 +164,47 @@ SSM_API ssm_status ss2d_scan_fwd(ssm_dtype dt, int B, int D, int H, int W, int N
                          ssm_stream_t stream);
 
 /*
+ * The same four operations, also returning the final state of every
+ * direction: last_state (fp32, device, required) receives h after the
+ * direction's last step -- position L-1 for a forward walk, position 0 for
+ * the backward branch of v1/v2, the last position of each SS2D direction's
+ * scan order -- laid out [directions][B][D][N] (1, 2 or 4 directions).
+ * It is the state a caller would carry into the next segment of a longer
+ * sequence (chunked inference; the pages' recurrence, "状态空间模型如何重塑
+ * 视觉序列处理", section "选择性扫描机制的计算效率优势", run to its end).
+ * Everything else as for the calls above.
+ */
+SSM_API ssm_status selective_scan_fwd_ls(ssm_dtype dt, int B, int D, int L, int N,
+                         const void *u, const void *delta, const float *A,
+                         const void *Bm, const void *Cm, const float *Dskip,
+                         const void *z, const float *delta_bias,
+                         int delta_softplus, void *y, float *last_state,
+                         void *workspace, size_t ws_bytes, ssm_stream_t stream);
+SSM_API ssm_status bimamba_scan_fwd_v1_ls(ssm_dtype dt, int B, int D, int L, int N,
+                         const void *u, const void *delta, const float *A,
+                         const float *A_b, const void *Bm, const void *Cm,
+                         const float *Dskip, const void *z,
+                         const float *delta_bias, int delta_softplus,
+                         float out_scale, void *y, float *last_state,
+                         void *workspace, size_t ws_bytes, ssm_stream_t stream);
+SSM_API ssm_status bimamba_scan_fwd_v2_ls(ssm_dtype dt, int B, int D, int L, int N,
+                         const void *u, const void *u_b, const void *delta,
+                         const void *delta_b, const float *A, const float *A_b,
+                         const void *Bm, const void *Cm, const void *Bm_b,
+                         const void *Cm_b, const float *Dskip, const float *D_b,
+                         const void *z, const float *delta_bias,
+                         const float *delta_bias_b, int delta_softplus,
+                         float out_scale, void *y, float *last_state,
+                         void *workspace, size_t ws_bytes, ssm_stream_t stream);
+SSM_API ssm_status ss2d_scan_fwd_ls(ssm_dtype dt, int B, int D, int H, int W, int N,
+                         int K, const void *x, const void *delta,
+                         const float *A, const void *Bm, const void *Cm,
+                         const float *Dskip, const void *z,
+                         const float *delta_bias, int delta_softplus, void *y,
+                         float *last_state, void *workspace, size_t ws_bytes,
+                         ssm_stream_t stream);
+
+/*
  * Status of the last call that used `workspace`, once the work queued on
  * `stream` before this call has finished (the call synchronises `stream`):
  * *out = SSM_OK, or SSM_ERR_TIMEOUT when a kernel gave up a bounded wait.

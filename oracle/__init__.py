@@ -29,6 +29,9 @@ incoming output gradient g), returning a dict of gradient arrays:
                                                  ddelta_bias, ddelta_bias_b
   ss2d_bwd(g, ...)                            -> dx, ddelta, dA, dB, dC, dD, dz,
                                                  ddelta_bias
+and the final state of every direction ([directions, B, D, N]):
+  selective_scan_last_state, bimamba_v1_last_state, bimamba_v2_last_state,
+  ss2d_last_state (same inputs as the forward calls; C, D and z play no part)
 Shapes are the ones documented in ``ssm_oracle.c``; a gradient has its
 input's shape.
 """
@@ -76,6 +79,8 @@ def _load():
             lib.oracle_bimamba_v2_bwd.argtypes = ([i, i, i, i] + [_dp] * 15 + [i, d] +
                                                   [_dp] * 16)
             lib.oracle_ss2d_bwd.argtypes = [i, i, i, i, i, i] + [_dp] * 8 + [i] + [_dp] * 9
+            lib.oracle_last_state.argtypes = [i, i, i, i] + [_dp] * 5 + [i, _dp]
+            lib.oracle_last_state.restype = ctypes.c_int
             lib.oracle_cross_scan_index.argtypes = [i, i, i, ctypes.c_long]
             lib.oracle_cross_scan_index.restype = ctypes.c_long
             for f in (lib.oracle_selective_scan, lib.oracle_bimamba_v1,
@@ -269,3 +274,55 @@ def ss2d_bwd(g, x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softpl
         Bn, Dn, H, W, N, K, *map(_ptr, a), int(bool(delta_softplus)),
         _ptr(_f64(g, (Bn, Dn, H, W))), *[_ptr(r[k]) for k in keys]), "ss2d_bwd")
     return {k: v for k, v in r.items() if v is not None}
+
+
+# ---------------------------------------------------------------- final states
+def _last_state(u, delta, A, B, delta_bias, delta_softplus):
+    """Final state of one direction over the rows as given: [B, D, N]."""
+    u = _f64(u)
+    Bn, Dn, L = u.shape
+    N = np.shape(A)[1]
+    out = np.empty((Bn, Dn, N), np.float64)
+    a = [u, _f64(delta, (Bn, Dn, L)), _f64(A, (Dn, N)), _f64(B, (Bn, N, L)),
+         _f64(delta_bias, (Dn,))]
+    _check(_load().oracle_last_state(Bn, Dn, L, N, *map(_ptr, a), int(bool(delta_softplus)),
+                                     _ptr(out)), "last_state")
+    return out
+
+
+def selective_scan_last_state(u, delta, A, B, C=None, D=None, z=None, delta_bias=None,
+                              delta_softplus=True):
+    return _last_state(u, delta, A, B, delta_bias, delta_softplus)[None]
+
+
+def bimamba_v2_last_state(u, delta, delta_b, A, A_b, B, C, B_b, C_b, D=None, D_b=None, z=None,
+                          delta_bias=None, delta_bias_b=None, u_b=None, delta_softplus=True,
+                          out_scale=0.5):
+    """[2, B, D, N]: the forward branch after position L-1, the backward
+    branch (run on the time-reversed copies) after position 0."""
+    ub = _f64(u if u_b is None else u_b)
+    f = _last_state(u, delta, A, B, delta_bias, delta_softplus)
+    b = _last_state(np.flip(ub, -1), np.flip(_f64(delta_b), -1), A_b, np.flip(_f64(B_b), -1),
+                    delta_bias_b, delta_softplus)
+    return np.stack([f, b])
+
+
+def bimamba_v1_last_state(u, delta, A, A_b, B, C, D=None, z=None, delta_bias=None,
+                          delta_softplus=True, out_scale=1.0):
+    return bimamba_v2_last_state(u, delta, delta, A, A_b, B, C, B, C, delta_bias=delta_bias,
+                                 delta_bias_b=delta_bias, delta_softplus=delta_softplus)
+
+
+def ss2d_last_state(x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True):
+    """[4, B, D, N]: direction k run over the image read in its scan order."""
+    x = _f64(x)
+    Bn, Dn, H, W = x.shape
+    L = H * W
+    flat = x.reshape(Bn, Dn, L)
+    out = []
+    for k in range(4):
+        xs = flat[:, :, cross_scan_index(H, W, k)]
+        out.append(_last_state(xs, _f64(delta)[:, k], _f64(A)[k], _f64(B)[:, k],
+                               None if delta_bias is None else _f64(delta_bias)[k],
+                               delta_softplus))
+    return np.stack(out)

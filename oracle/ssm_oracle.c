@@ -807,3 +807,38 @@ done:
     free(dxs);
     return rc;
 }
+
+/* ======================================================================
+ * Final states.  For every row, the state h after the last step of the
+ * recurrence above, over the row as given (callers pass flipped or
+ * cross-scanned copies for the other directions):
+ *   h_t[n] = exp(delta_t * A[n]) * h_{t-1}[n] + delta_t * B[n][t] * u_t
+ * with h_{-1} = 0; out[b][d][n] = h_{L-1}[n].
+ * ====================================================================== */
+int oracle_last_state(int B, int D, int L, int N, const double *u, const double *delta,
+                      const double *A, const double *Bm, const double *delta_bias,
+                      int delta_softplus, double *out)
+{
+    if (B < 0 || D < 0 || L < 0 || N <= 0 || !u || !delta || !A || !Bm || !out)
+        return -1;
+    for (int b = 0; b < B; ++b) {
+        for (int d = 0; d < D; ++d) {
+            const double *ur = u + ((size_t)b * D + d) * (size_t)L;
+            const double *dr = delta + ((size_t)b * D + d) * (size_t)L;
+            const double *bm = Bm + (size_t)b * N * L;
+            double *h = out + ((size_t)b * D + d) * (size_t)N;
+            double bias = delta_bias ? delta_bias[d] : 0.0;
+            for (int n = 0; n < N; ++n)
+                h[n] = 0.0;
+            for (int t = 0; t < L; ++t) {
+                double dl = dr[t] + bias;
+                if (delta_softplus)
+                    dl = softplus(dl);
+                for (int n = 0; n < N; ++n)
+                    h[n] = exp(dl * A[(size_t)d * N + n]) * h[n] +
+                           dl * bm[(size_t)n * L + t] * ur[t];
+            }
+        }
+    }
+    return 0;
+}

@@ -36,6 +36,11 @@ _lib.bimamba_scan_fwd_v1.argtypes = [_i] * 5 + [_vp] * 9 + [_i, _f, _vp, _vp, _s
 _lib.bimamba_scan_fwd_v2.argtypes = [_i] * 5 + [_vp] * 15 + [_i, _f, _vp, _vp, _sz, _vp]
 _lib.ss2d_scan_fwd.argtypes = [_i] * 7 + [_vp] * 8 + [_i, _vp, _vp, _sz, _vp]
 _lib.bimamba_scan_fwd_v2_noalloc.argtypes = [_i] * 5 + [_vp] * 15 + [_i, _f, _vp, _vp]
+_lib.selective_scan_fwd_ls.argtypes = [_i] * 5 + [_vp] * 8 + [_i, _vp, _vp, _vp, _sz, _vp]
+_lib.bimamba_scan_fwd_v1_ls.argtypes = [_i] * 5 + [_vp] * 9 + [_i, _f, _vp, _vp, _vp, _sz, _vp]
+_lib.bimamba_scan_fwd_v2_ls.argtypes = [_i] * 5 + [_vp] * 15 + [_i, _f, _vp, _vp, _vp, _sz,
+                                                                 _vp]
+_lib.ss2d_scan_fwd_ls.argtypes = [_i] * 7 + [_vp] * 8 + [_i, _vp, _vp, _vp, _sz, _vp]
 _lib.ssm_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
 _lib.ssm_workspace_bytes.restype = _sz
 _lib.ssm_get_status.argtypes = [_vp, _vp, ctypes.POINTER(_i)]
@@ -58,7 +63,9 @@ _lib.ss2d_scan_bwd.argtypes = [_i] * 7 + [_vp] * 8 + [_i] + [_vp] * 10 + [_sz, _
 _lib.ssm_bwd_workspace_bytes.argtypes = [_i] * 8
 _lib.ssm_bwd_workspace_bytes.restype = _sz
 for _fn in (_lib.selective_scan_fwd, _lib.bimamba_scan_fwd_v1, _lib.bimamba_scan_fwd_v2,
-            _lib.ss2d_scan_fwd, _lib.bimamba_scan_fwd_v2_noalloc, _lib.selective_scan_bwd,
+            _lib.ss2d_scan_fwd, _lib.bimamba_scan_fwd_v2_noalloc, _lib.selective_scan_fwd_ls,
+            _lib.bimamba_scan_fwd_v1_ls, _lib.bimamba_scan_fwd_v2_ls, _lib.ss2d_scan_fwd_ls,
+            _lib.selective_scan_bwd,
             _lib.bimamba_scan_bwd_v1, _lib.bimamba_scan_bwd_v2, _lib.ss2d_scan_bwd):
     _fn.restype = _i
 
@@ -160,9 +167,11 @@ def _check(status, where):
 
 
 def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None,
-                       delta_softplus=True, out=None, workspace=None, stream=None):
+                       delta_softplus=True, out=None, workspace=None, stream=None,
+                       last_state=None):
     """One direction.  u, delta, z: [Bt, Dc, L]; A: [Dc, N] fp32; B, C: [Bt, N, L];
-    D, delta_bias: [Dc] fp32.  Returns y [Bt, Dc, L]."""
+    D, delta_bias: [Dc] fp32.  Returns y [Bt, Dc, L].  last_state: optional fp32
+    [1, Bt, Dc, N] tensor that receives the final state."""
     io = u.dtype
     Bt, Dc, L = u.shape
     N = A.shape[1]
@@ -172,16 +181,23 @@ def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None,
             _par(D, "D", (Dc,), True), _io(z, io, "z", (Bt, Dc, L), True),
             _par(delta_bias, "delta_bias", (Dc,), True)]
     wp, wn = _workspace("single", io, Bt, Dc, L, N, u.device, workspace)
-    _check(_lib.selective_scan_fwd(_dtype_code(u), Bt, Dc, L, N, *args, int(bool(delta_softplus)),
-                                   _io(y, io, "out", (Bt, Dc, L)), wp, wn, _stream(stream)),
-           "selective_scan_fwd")
+    if last_state is None:
+        _check(_lib.selective_scan_fwd(_dtype_code(u), Bt, Dc, L, N, *args,
+                                       int(bool(delta_softplus)), _io(y, io, "out", (Bt, Dc, L)),
+                                       wp, wn, _stream(stream)), "selective_scan_fwd")
+        return y
+    _check(_lib.selective_scan_fwd_ls(_dtype_code(u), Bt, Dc, L, N, *args,
+                                      int(bool(delta_softplus)), _io(y, io, "out", (Bt, Dc, L)),
+                                      _par(last_state, "last_state", (1, Bt, Dc, N)), wp, wn,
+                                      _stream(stream)), "selective_scan_fwd_ls")
     return y
 
 
 def bimamba_scan_fwd_v1(u, delta, A, A_b, B, C, D=None, z=None, delta_bias=None,
                         delta_softplus=True, out_scale=1.0, out=None, workspace=None,
-                        stream=None):
-    """BiMamba v1: shared delta/B/C/D/bias, separate A and A_b.  Original order."""
+                        stream=None, last_state=None):
+    """BiMamba v1: shared delta/B/C/D/bias, separate A and A_b.  Original order.
+    last_state: optional fp32 [2, Bt, Dc, N] (forward, backward branch)."""
     io = u.dtype
     Bt, Dc, L = u.shape
     N = A.shape[1]
@@ -191,16 +207,26 @@ def bimamba_scan_fwd_v1(u, delta, A, A_b, B, C, D=None, z=None, delta_bias=None,
             _par(D, "D", (Dc,), True), _io(z, io, "z", (Bt, Dc, L), True),
             _par(delta_bias, "delta_bias", (Dc,), True)]
     wp, wn = _workspace("v1", io, Bt, Dc, L, N, u.device, workspace)
-    _check(_lib.bimamba_scan_fwd_v1(_dtype_code(u), Bt, Dc, L, N, *args, int(bool(delta_softplus)),
-                                    float(out_scale), _io(y, io, "out", (Bt, Dc, L)), wp, wn,
-                                    _stream(stream)), "bimamba_scan_fwd_v1")
+    if last_state is None:
+        _check(_lib.bimamba_scan_fwd_v1(_dtype_code(u), Bt, Dc, L, N, *args,
+                                        int(bool(delta_softplus)), float(out_scale),
+                                        _io(y, io, "out", (Bt, Dc, L)), wp, wn, _stream(stream)),
+               "bimamba_scan_fwd_v1")
+        return y
+    _check(_lib.bimamba_scan_fwd_v1_ls(_dtype_code(u), Bt, Dc, L, N, *args,
+                                       int(bool(delta_softplus)), float(out_scale),
+                                       _io(y, io, "out", (Bt, Dc, L)),
+                                       _par(last_state, "last_state", (2, Bt, Dc, N)), wp, wn,
+                                       _stream(stream)), "bimamba_scan_fwd_v1_ls")
     return y
 
 
 def bimamba_scan_fwd_v2(u, delta, delta_b, A, A_b, B, C, B_b, C_b, D=None, D_b=None, z=None,
                         delta_bias=None, delta_bias_b=None, u_b=None, delta_softplus=True,
-                        out_scale=0.5, out=None, workspace=None, stream=None):
-    """BiMamba v2: independent backward set.  Original token order."""
+                        out_scale=0.5, out=None, workspace=None, stream=None,
+                        last_state=None):
+    """BiMamba v2: independent backward set.  Original token order.
+    last_state: optional fp32 [2, Bt, Dc, N] (forward, backward branch)."""
     io = u.dtype
     Bt, Dc, L = u.shape
     N = A.shape[1]
@@ -213,14 +239,22 @@ def bimamba_scan_fwd_v2(u, delta, delta_b, A, A_b, B, C, B_b, C_b, D=None, D_b=N
             _io(z, io, "z", sh, True), _par(delta_bias, "delta_bias", (Dc,), True),
             _par(delta_bias_b, "delta_bias_b", (Dc,), True)]
     wp, wn = _workspace("v2", io, Bt, Dc, L, N, u.device, workspace)
-    _check(_lib.bimamba_scan_fwd_v2(_dtype_code(u), Bt, Dc, L, N, *args, int(bool(delta_softplus)),
-                                    float(out_scale), _io(y, io, "out", sh), wp, wn,
-                                    _stream(stream)), "bimamba_scan_fwd_v2")
+    if last_state is None:
+        _check(_lib.bimamba_scan_fwd_v2(_dtype_code(u), Bt, Dc, L, N, *args,
+                                        int(bool(delta_softplus)), float(out_scale),
+                                        _io(y, io, "out", sh), wp, wn, _stream(stream)),
+               "bimamba_scan_fwd_v2")
+        return y
+    _check(_lib.bimamba_scan_fwd_v2_ls(_dtype_code(u), Bt, Dc, L, N, *args,
+                                       int(bool(delta_softplus)), float(out_scale),
+                                       _io(y, io, "out", sh),
+                                       _par(last_state, "last_state", (2, Bt, Dc, N)), wp, wn,
+                                       _stream(stream)), "bimamba_scan_fwd_v2_ls")
     return y
 
 
 def ss2d_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
-                  out=None, workspace=None, stream=None):
+                  out=None, workspace=None, stream=None, last_state=None):
     """SS2D, K=4.  x, z: [Bt, Dc, H, W]; delta: [Bt, 4, Dc, H*W] and B, C: [Bt, 4, N, H*W]
     in each direction's scan order; A: [4, Dc, N]; D, delta_bias: [4, Dc]."""
     io = x.dtype
@@ -234,9 +268,15 @@ def ss2d_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_soft
             _par(D, "D", (K, Dc), True), _io(z, io, "z", (Bt, Dc, H, W), True),
             _par(delta_bias, "delta_bias", (K, Dc), True)]
     wp, wn = _workspace("ss2d", io, Bt, Dc, L, N, x.device, workspace, K)
-    _check(_lib.ss2d_scan_fwd(_dtype_code(x), Bt, Dc, H, W, N, K, *args, int(bool(delta_softplus)),
-                              _io(y, io, "out", (Bt, Dc, H, W)), wp, wn, _stream(stream)),
-           "ss2d_scan_fwd")
+    if last_state is None:
+        _check(_lib.ss2d_scan_fwd(_dtype_code(x), Bt, Dc, H, W, N, K, *args,
+                                  int(bool(delta_softplus)), _io(y, io, "out", (Bt, Dc, H, W)),
+                                  wp, wn, _stream(stream)), "ss2d_scan_fwd")
+        return y
+    _check(_lib.ss2d_scan_fwd_ls(_dtype_code(x), Bt, Dc, H, W, N, K, *args,
+                                 int(bool(delta_softplus)), _io(y, io, "out", (Bt, Dc, H, W)),
+                                 _par(last_state, "last_state", (4, Bt, Dc, N)), wp, wn,
+                                 _stream(stream)), "ss2d_scan_fwd_ls")
     return y
 
 

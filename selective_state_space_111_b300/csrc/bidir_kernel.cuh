@@ -91,6 +91,7 @@ struct BiParams {
     const float *acc_in;   // [B, D, L] fp32 (OUT_ADD_Y)
     float *acc_out;        // [B, D, L] fp32 (OUT_ACC)
     float *W;              // [B, D, L] fp32 stash (two branches, several chunks)
+    float *last_state[2];  // per branch: final state [B, D, N] fp32, or null
     unsigned *status;      // device status word, or null
     int B, D, L, N;
     int nchunks;
@@ -417,6 +418,20 @@ bidir_scan_kernel(const BiParams P) {
             for (; j < len; ++j) step(j);
             mbar_arrive(&dw_empty[s2]);
             mbar_arrive(&yp_full[s2]);
+        }
+        // the state after the branch's last step (position L-1 forward,
+        // position 0 for the backward walk)
+        float *ls = P.last_state[s_dir];
+        if (ls != nullptr && s_ch < D) {
+            ls += ((long long)b * D + s_ch) * N;
+#pragma unroll
+            for (int q = 0; q < NP; ++q) {
+                const int n0 = s_sg * S + 2 * q;
+                float a0, a1;
+                upk(h[q], a0, a1);
+                if (n0 < N) ls[n0] = a0;
+                if (n0 + 1 < N) ls[n0 + 1] = a1;
+            }
         }
     } else if (warp < NSW + NPW) {
         // ================================================================ prep

@@ -204,9 +204,11 @@ ssm_status bidirectional(ssm_dtype dt, int B, int D, int L, int N, const void *u
                          const void *Bm_b, const void *Cm_b, const float *Dskip,
                          const float *D_b, const void *z, const float *bias,
                          const float *bias_b, int delta_softplus, float out_scale, void *y,
-                         void *ws, size_t ws_bytes, bool two_sets, cudaStream_t stream) {
+                         void *ws, size_t ws_bytes, bool two_sets, cudaStream_t stream,
+                         float *ls = nullptr) {
     ssm_status s = check_common(dt, B, D, L, N);
     if (s != SSM_OK) return s;
+    if (!opt_f32_ok(ls)) return SSM_ERR_INVALID_ARG;
     if (!io_ok(dt, u) || !opt_io_ok(dt, u_b) || !io_ok(dt, delta) || !io_ok(dt, delta_b) ||
         !io_ok(dt, Bm) || !io_ok(dt, Cm) || !io_ok(dt, Bm_b) || !io_ok(dt, Cm_b) ||
         !opt_io_ok(dt, z) || !io_ok(dt, y) ||
@@ -225,6 +227,9 @@ ssm_status bidirectional(ssm_dtype dt, int B, int D, int L, int N, const void *u
     P.z = z;
     P.y = y;
     P.W = lay.w ? (float *)(wsb + lay.w) : nullptr;
+    const long long BDN = (long long)B * D * N;
+    P.last_state[0] = ls;                               // [2][B][D][N]
+    P.last_state[1] = ls ? ls + BDN : nullptr;
     P.status = (unsigned *)wsb;
     P.B = B;
     P.D = D;
@@ -277,7 +282,9 @@ template <typename IO, int NM>
 ssm_status ss2d_run_nm(int B, int D, int H, int W, int N, const void *x, const void *delta,
                     const float *A, const void *Bm, const void *Cm, const float *Dskip,
                     const void *z, const float *bias, int delta_softplus, void *y, char *wsb,
-                    const SsWs &lay, cudaStream_t st) {
+                    const SsWs &lay, cudaStream_t st, float *ls) {
+    const long long BDN = (long long)B * D * N;          // last_state: [4][B][D][N]
+    auto lsk = [&](int k) { return ls ? ls + k * BDN : nullptr; };
     const int L = H * W;
     const long long DL = (long long)D * L;
     float *bcK = (float *)(wsb + lay.bc);
@@ -315,6 +322,8 @@ ssm_status ss2d_run_nm(int B, int D, int H, int W, int N, const void *x, const v
     P.br[1] = branch(3, xt, 1);
     P.W = r1;
     P.acc_out = r2;
+    P.last_state[0] = lsk(1);
+    P.last_state[1] = lsk(3);
     s = launch_two_branch<IO, ssm::OUT_ACC, NM>(P, st, false);
     if (s != SSM_OK) return s;
     // Wa (R1) = Wt (R2) transposed back to H x W
@@ -328,18 +337,20 @@ ssm_status ss2d_run_nm(int B, int D, int H, int W, int N, const void *x, const v
     P.W = r2;
     P.acc_in = r1;
     P.acc_out = nullptr;
+    P.last_state[0] = lsk(0);
+    P.last_state[1] = lsk(2);
     return launch_two_branch<IO, ssm::OUT_ADD_Y, NM>(P, st);
 }
 template <typename IO>
 ssm_status ss2d_run(int B, int D, int H, int W, int N, const void *x, const void *delta,
                     const float *A, const void *Bm, const void *Cm, const float *Dskip,
                     const void *z, const float *bias, int delta_softplus, void *y, char *wsb,
-                    const SsWs &lay, cudaStream_t st) {
+                    const SsWs &lay, cudaStream_t st, float *ls) {
     if (N <= ssm::kMaxN)
         return ss2d_run_nm<IO, ssm::kMaxN>(B, D, H, W, N, x, delta, A, Bm, Cm, Dskip, z, bias,
-                                           delta_softplus, y, wsb, lay, st);
+                                           delta_softplus, y, wsb, lay, st, ls);
     return ss2d_run_nm<IO, 2 * ssm::kMaxN>(B, D, H, W, N, x, delta, A, Bm, Cm, Dskip, z, bias,
-                                           delta_softplus, y, wsb, lay, st);
+                                           delta_softplus, y, wsb, lay, st, ls);
 }
 
 // ---- fixed scratch of the allocation-free entry point
@@ -372,17 +383,14 @@ ssm_status static_scratch(void **out) {
     return SSM_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-ssm_status selective_scan_fwd(ssm_dtype dt, int B, int D, int L, int N, const void *u,
-                              const void *delta, const float *A, const void *Bm,
-                              const void *Cm, const float *Dskip, const void *z,
-                              const float *delta_bias, int delta_softplus, void *y,
-                              void *workspace, size_t ws_bytes, ssm_stream_t stream) {
+ssm_status single_impl(ssm_dtype dt, int B, int D, int L, int N, const void *u,
+                       const void *delta, const float *A, const void *Bm, const void *Cm,
+                       const float *Dskip, const void *z, const float *delta_bias,
+                       int delta_softplus, void *y, void *workspace, size_t ws_bytes,
+                       ssm_stream_t stream, float *ls) {
     ssm_status s = check_common(dt, B, D, L, N);
     if (s != SSM_OK) return s;
+    if (!opt_f32_ok(ls)) return SSM_ERR_INVALID_ARG;
     if (!io_ok(dt, u) || !io_ok(dt, delta) || !io_ok(dt, Bm) || !io_ok(dt, Cm) ||
         !opt_io_ok(dt, z) || !io_ok(dt, y) || !f32_ok(A) || !opt_f32_ok(Dskip) ||
         !opt_f32_ok(delta_bias))
@@ -399,6 +407,8 @@ ssm_status selective_scan_fwd(ssm_dtype dt, int B, int D, int L, int N, const vo
     P.z = z;
     P.y = y;
     P.W = nullptr;
+    P.last_state[0] = ls;
+    P.last_state[1] = nullptr;
     P.status = (unsigned *)wsb;
     P.B = B;
     P.D = D;
@@ -411,6 +421,61 @@ ssm_status selective_scan_fwd(ssm_dtype dt, int B, int D, int L, int N, const vo
     if (dt == SSM_F32) return run_bidir<float, 1>(P, Bm, Cm, Bm, Cm, false, st);
     if (dt == SSM_F16) return run_bidir<__half, 1>(P, Bm, Cm, Bm, Cm, false, st);
     return run_bidir<__nv_bfloat16, 1>(P, Bm, Cm, Bm, Cm, false, st);
+}
+
+ssm_status ss2d_impl(ssm_dtype dt, int B, int D, int H, int W, int N, int K, const void *x,
+                     const void *delta, const float *A, const void *Bm, const void *Cm,
+                     const float *Dskip, const void *z, const float *delta_bias,
+                     int delta_softplus, void *y, void *workspace, size_t ws_bytes,
+                     ssm_stream_t stream, float *ls) {
+    if (H < 0 || W < 0 || !opt_f32_ok(ls)) return SSM_ERR_INVALID_ARG;
+    if (K != 4) return SSM_ERR_UNSUPPORTED;
+    if (!fits((long long)H * W)) return SSM_ERR_UNSUPPORTED;
+    const int L = H * W;
+    ssm_status s = check_common(dt, B, D, L, N);
+    if (s != SSM_OK) return s;
+    if (!fits((long long)K * D * L) || !fits((long long)K * N * L)) return SSM_ERR_UNSUPPORTED;
+    if (!io_ok(dt, x) || !io_ok(dt, delta) || !io_ok(dt, Bm) || !io_ok(dt, Cm) ||
+        !opt_io_ok(dt, z) || !io_ok(dt, y) || !f32_ok(A) || !opt_f32_ok(Dskip) ||
+        !opt_f32_ok(delta_bias))
+        return SSM_ERR_INVALID_ARG;
+    if ((long long)B * D * L == 0) return SSM_OK;
+    const SsWs lay = ss2d_ws(dt, B, D, L, nm_of(N));
+    if (workspace == nullptr || ws_bytes < lay.total || !aligned(workspace, 16))
+        return SSM_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (dt == SSM_F32)
+        return ss2d_run<float>(B, D, H, W, N, x, delta, A, Bm, Cm, Dskip, z, delta_bias,
+                               delta_softplus, y, (char *)workspace, lay, st, ls);
+    if (dt == SSM_F16)
+        return ss2d_run<__half>(B, D, H, W, N, x, delta, A, Bm, Cm, Dskip, z, delta_bias,
+                                delta_softplus, y, (char *)workspace, lay, st, ls);
+    return ss2d_run<__nv_bfloat16>(B, D, H, W, N, x, delta, A, Bm, Cm, Dskip, z, delta_bias,
+                                   delta_softplus, y, (char *)workspace, lay, st, ls);
+}
+
+}  // namespace
+
+extern "C" {
+
+ssm_status selective_scan_fwd(ssm_dtype dt, int B, int D, int L, int N, const void *u,
+                              const void *delta, const float *A, const void *Bm,
+                              const void *Cm, const float *Dskip, const void *z,
+                              const float *delta_bias, int delta_softplus, void *y,
+                              void *workspace, size_t ws_bytes, ssm_stream_t stream) {
+    return single_impl(dt, B, D, L, N, u, delta, A, Bm, Cm, Dskip, z, delta_bias,
+                       delta_softplus, y, workspace, ws_bytes, stream, nullptr);
+}
+
+ssm_status selective_scan_fwd_ls(ssm_dtype dt, int B, int D, int L, int N, const void *u,
+                                 const void *delta, const float *A, const void *Bm,
+                                 const void *Cm, const float *Dskip, const void *z,
+                                 const float *delta_bias, int delta_softplus, void *y,
+                                 float *last_state, void *workspace, size_t ws_bytes,
+                                 ssm_stream_t stream) {
+    if (last_state == nullptr) return SSM_ERR_INVALID_ARG;
+    return single_impl(dt, B, D, L, N, u, delta, A, Bm, Cm, Dskip, z, delta_bias,
+                       delta_softplus, y, workspace, ws_bytes, stream, last_state);
 }
 
 ssm_status bimamba_scan_fwd_v1(ssm_dtype dt, int B, int D, int L, int N, const void *u,
@@ -435,6 +500,33 @@ ssm_status bimamba_scan_fwd_v2(ssm_dtype dt, int B, int D, int L, int N, const v
     return bidirectional(dt, B, D, L, N, u, u_b, delta, delta_b, A, A_b, Bm, Cm, Bm_b, Cm_b,
                          Dskip, D_b, z, delta_bias, delta_bias_b, delta_softplus, out_scale, y,
                          workspace, ws_bytes, true, (cudaStream_t)stream);
+}
+
+ssm_status bimamba_scan_fwd_v1_ls(ssm_dtype dt, int B, int D, int L, int N, const void *u,
+                                  const void *delta, const float *A, const float *A_b,
+                                  const void *Bm, const void *Cm, const float *Dskip,
+                                  const void *z, const float *delta_bias, int delta_softplus,
+                                  float out_scale, void *y, float *last_state, void *workspace,
+                                  size_t ws_bytes, ssm_stream_t stream) {
+    if (last_state == nullptr) return SSM_ERR_INVALID_ARG;
+    return bidirectional(dt, B, D, L, N, u, nullptr, delta, delta, A, A_b, Bm, Cm, Bm, Cm,
+                         Dskip, Dskip, z, delta_bias, delta_bias, delta_softplus, out_scale, y,
+                         workspace, ws_bytes, false, (cudaStream_t)stream, last_state);
+}
+
+ssm_status bimamba_scan_fwd_v2_ls(ssm_dtype dt, int B, int D, int L, int N, const void *u,
+                                  const void *u_b, const void *delta, const void *delta_b,
+                                  const float *A, const float *A_b, const void *Bm,
+                                  const void *Cm, const void *Bm_b, const void *Cm_b,
+                                  const float *Dskip, const float *D_b, const void *z,
+                                  const float *delta_bias, const float *delta_bias_b,
+                                  int delta_softplus, float out_scale, void *y,
+                                  float *last_state, void *workspace, size_t ws_bytes,
+                                  ssm_stream_t stream) {
+    if (last_state == nullptr) return SSM_ERR_INVALID_ARG;
+    return bidirectional(dt, B, D, L, N, u, u_b, delta, delta_b, A, A_b, Bm, Cm, Bm_b, Cm_b,
+                         Dskip, D_b, z, delta_bias, delta_bias_b, delta_softplus, out_scale, y,
+                         workspace, ws_bytes, true, (cudaStream_t)stream, last_state);
 }
 
 ssm_status bimamba_scan_fwd_v2_noalloc(ssm_dtype dt, int B, int D, int L, int N,
@@ -462,30 +554,19 @@ ssm_status ss2d_scan_fwd(ssm_dtype dt, int B, int D, int H, int W, int N, int K,
                          const void *Cm, const float *Dskip, const void *z,
                          const float *delta_bias, int delta_softplus, void *y,
                          void *workspace, size_t ws_bytes, ssm_stream_t stream) {
-    if (H < 0 || W < 0) return SSM_ERR_INVALID_ARG;
-    if (K != 4) return SSM_ERR_UNSUPPORTED;
-    if (!fits((long long)H * W)) return SSM_ERR_UNSUPPORTED;
-    const int L = H * W;
-    ssm_status s = check_common(dt, B, D, L, N);
-    if (s != SSM_OK) return s;
-    if (!fits((long long)K * D * L) || !fits((long long)K * N * L)) return SSM_ERR_UNSUPPORTED;
-    if (!io_ok(dt, x) || !io_ok(dt, delta) || !io_ok(dt, Bm) || !io_ok(dt, Cm) ||
-        !opt_io_ok(dt, z) || !io_ok(dt, y) || !f32_ok(A) || !opt_f32_ok(Dskip) ||
-        !opt_f32_ok(delta_bias))
-        return SSM_ERR_INVALID_ARG;
-    if ((long long)B * D * L == 0) return SSM_OK;
-    const SsWs lay = ss2d_ws(dt, B, D, L, nm_of(N));
-    if (workspace == nullptr || ws_bytes < lay.total || !aligned(workspace, 16))
-        return SSM_ERR_WORKSPACE;
-    cudaStream_t st = (cudaStream_t)stream;
-    if (dt == SSM_F32)
-        return ss2d_run<float>(B, D, H, W, N, x, delta, A, Bm, Cm, Dskip, z, delta_bias,
-                               delta_softplus, y, (char *)workspace, lay, st);
-    if (dt == SSM_F16)
-        return ss2d_run<__half>(B, D, H, W, N, x, delta, A, Bm, Cm, Dskip, z, delta_bias,
-                                delta_softplus, y, (char *)workspace, lay, st);
-    return ss2d_run<__nv_bfloat16>(B, D, H, W, N, x, delta, A, Bm, Cm, Dskip, z, delta_bias,
-                                   delta_softplus, y, (char *)workspace, lay, st);
+    return ss2d_impl(dt, B, D, H, W, N, K, x, delta, A, Bm, Cm, Dskip, z, delta_bias,
+                     delta_softplus, y, workspace, ws_bytes, stream, nullptr);
+}
+
+ssm_status ss2d_scan_fwd_ls(ssm_dtype dt, int B, int D, int H, int W, int N, int K,
+                            const void *x, const void *delta, const float *A, const void *Bm,
+                            const void *Cm, const float *Dskip, const void *z,
+                            const float *delta_bias, int delta_softplus, void *y,
+                            float *last_state, void *workspace, size_t ws_bytes,
+                            ssm_stream_t stream) {
+    if (last_state == nullptr) return SSM_ERR_INVALID_ARG;
+    return ss2d_impl(dt, B, D, H, W, N, K, x, delta, A, Bm, Cm, Dskip, z, delta_bias,
+                     delta_softplus, y, workspace, ws_bytes, stream, last_state);
 }
 
 size_t ssm_workspace_bytes(ssm_op op, ssm_dtype dt, int B, int D, int L_or_HW, int N, int K) {

@@ -41,3 +41,18 @@ def closed_form_sequence(u, dt, A, B, C, D=0.0, bias=0.0, delta_softplus=True):
 def silu_gate(y, z):
     z = np.asarray(z, np.float64)
     return y * z / (1.0 + np.exp(-z))
+
+
+def closed_form_last_state(u, dt, A, B, bias=0.0, delta_softplus=True):
+    """State after the last step, unrolled (no recurrence):
+    h_{L-1}[n] = sum_s exp(A[n] * sum_{r=s+1..L-1} delta_r) * delta_s * B[n,s] * u_s."""
+    u = np.asarray(u, np.float64)
+    x = np.asarray(dt, np.float64) + bias
+    delta = softplus(x) if delta_softplus else x
+    A = np.asarray(A, np.float64)
+    B = np.asarray(B, np.float64)
+    L = u.shape[0]
+    h = np.zeros(A.shape[0])
+    for s in range(L):
+        h += np.exp(A * np.sum(delta[s + 1:])) * delta[s] * B[:, s] * u[s]
+    return h

@@ -136,6 +136,48 @@ def test_cta_shape_does_not_change_results(op):
     assert torch.equal(y8, y16)
 
 
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("op", ["single", "v1", "v2", "ss2d"])
+def test_last_state(op, io, cta):
+    # the final state of every direction against the oracle's; y unchanged
+    import oracle
+    import selective_state_space_111_b300 as ssm
+    kw = dict(H=6, W=9) if op == "ss2d" else dict(L=133)
+    spec = Spec(op, io, B=2, D=21, perturb=True, out_scale=0.5 if op == "v2" else 1.0, **kw)
+    t = make_inputs(spec, 21)
+    g = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in t.items()}
+    ndir = {"single": 1, "v1": 2, "v2": 2, "ss2d": 4}[op]
+    ls = torch.full((ndir, 2, 21, 16), float("nan"), device="cuda")
+    sp = spec.delta_softplus
+    if op == "single":
+        y = ssm.selective_scan_fwd(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"],
+                                   g["delta_bias"], sp, last_state=ls)
+        ref = oracle.selective_scan_last_state(t["u"], t["delta"], t["A"], t["B"],
+                                               delta_bias=t["delta_bias"])
+    elif op == "v1":
+        y = ssm.bimamba_scan_fwd_v1(g["u"], g["delta"], g["A"], g["A_b"], g["B"], g["C"], g["D"],
+                                    g["z"], g["delta_bias"], sp, 1.0, last_state=ls)
+        ref = oracle.bimamba_v1_last_state(t["u"], t["delta"], t["A"], t["A_b"], t["B"], t["C"],
+                                           delta_bias=t["delta_bias"])
+    elif op == "v2":
+        y = ssm.bimamba_scan_fwd_v2(g["u"], g["delta"], g["delta_b"], g["A"], g["A_b"], g["B"],
+                                    g["C"], g["B_b"], g["C_b"], g["D"], g["D_b"], g["z"],
+                                    g["delta_bias"], g["delta_bias_b"], g["u_b"], sp, 0.5,
+                                    last_state=ls)
+        ref = oracle.bimamba_v2_last_state(t["u"], t["delta"], t["delta_b"], t["A"], t["A_b"],
+                                           t["B"], t["C"], t["B_b"], t["C_b"],
+                                           delta_bias=t["delta_bias"],
+                                           delta_bias_b=t["delta_bias_b"], u_b=t["u_b"])
+    else:
+        y = ssm.ss2d_scan_fwd(g["x"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"],
+                              g["delta_bias"], sp, last_state=ls)
+        ref = oracle.ss2d_last_state(t["x"], t["delta"], t["A"], t["B"], t["C"],
+                                     delta_bias=t["delta_bias"])
+    torch.cuda.synchronize()
+    assert max_scaled_err(ls, ref) <= TOL["f32"] * 10    # fp32 state, inputs as rounded
+    assert max_scaled_err(y, run_oracle(spec, t)) <= TOL[io]
+
+
 def test_length_one_branches_agree():
     # With L = 1 and identical parameter sets the two branches coincide, so
     # v2 with out_scale 0.5 equals the single-direction scan.
