@@ -205,6 +205,25 @@ SSM_API ssm_status ss2d_scan_fwd_ls(ssm_dtype dt, int B, int D, int H, int W, in
                          ssm_stream_t stream);
 
 /*
+ * v2 with the backward set in its own scan order: delta_b, Bm_b, Cm_b (and
+ * u_b when given) are time-reversed -- element t of a row is position L-1-t
+ * -- as produced when the backward branch's projections run on the flipped
+ * sequence ("Vision Mamba实战", section 2.2, flips the input before the
+ * backward scan).  u (shared, u_b == NULL), z and y stay in original order;
+ * the result equals bimamba_scan_fwd_v2 on the un-reversed tensors, without
+ * materialising the flips.  last_state may be NULL (else as *_fwd_ls).
+ */
+SSM_API ssm_status bimamba_scan_fwd_v2_so(ssm_dtype dt, int B, int D, int L, int N,
+                         const void *u, const void *u_b, const void *delta,
+                         const void *delta_b, const float *A, const float *A_b,
+                         const void *Bm, const void *Cm, const void *Bm_b,
+                         const void *Cm_b, const float *Dskip, const float *D_b,
+                         const void *z, const float *delta_bias,
+                         const float *delta_bias_b, int delta_softplus,
+                         float out_scale, void *y, float *last_state,
+                         void *workspace, size_t ws_bytes, ssm_stream_t stream);
+
+/*
  * Status of the last call that used `workspace`, once the work queued on
  * `stream` before this call has finished (the call synchronises `stream`):
  * *out = SSM_OK, or SSM_ERR_TIMEOUT when a kernel gave up a bounded wait.

@@ -41,6 +41,8 @@ _lib.bimamba_scan_fwd_v1_ls.argtypes = [_i] * 5 + [_vp] * 9 + [_i, _f, _vp, _vp,
 _lib.bimamba_scan_fwd_v2_ls.argtypes = [_i] * 5 + [_vp] * 15 + [_i, _f, _vp, _vp, _vp, _sz,
                                                                  _vp]
 _lib.ss2d_scan_fwd_ls.argtypes = [_i] * 7 + [_vp] * 8 + [_i, _vp, _vp, _vp, _sz, _vp]
+_lib.bimamba_scan_fwd_v2_so.argtypes = [_i] * 5 + [_vp] * 15 + [_i, _f, _vp, _vp, _vp, _sz,
+                                                                 _vp]
 _lib.ssm_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
 _lib.ssm_workspace_bytes.restype = _sz
 _lib.ssm_get_status.argtypes = [_vp, _vp, ctypes.POINTER(_i)]
@@ -65,6 +67,7 @@ _lib.ssm_bwd_workspace_bytes.restype = _sz
 for _fn in (_lib.selective_scan_fwd, _lib.bimamba_scan_fwd_v1, _lib.bimamba_scan_fwd_v2,
             _lib.ss2d_scan_fwd, _lib.bimamba_scan_fwd_v2_noalloc, _lib.selective_scan_fwd_ls,
             _lib.bimamba_scan_fwd_v1_ls, _lib.bimamba_scan_fwd_v2_ls, _lib.ss2d_scan_fwd_ls,
+            _lib.bimamba_scan_fwd_v2_so,
             _lib.selective_scan_bwd,
             _lib.bimamba_scan_bwd_v1, _lib.bimamba_scan_bwd_v2, _lib.ss2d_scan_bwd):
     _fn.restype = _i
@@ -224,8 +227,9 @@ def bimamba_scan_fwd_v1(u, delta, A, A_b, B, C, D=None, z=None, delta_bias=None,
 def bimamba_scan_fwd_v2(u, delta, delta_b, A, A_b, B, C, B_b, C_b, D=None, D_b=None, z=None,
                         delta_bias=None, delta_bias_b=None, u_b=None, delta_softplus=True,
                         out_scale=0.5, out=None, workspace=None, stream=None,
-                        last_state=None):
-    """BiMamba v2: independent backward set.  Original token order.
+                        last_state=None, scan_order=False):
+    """BiMamba v2: independent backward set.  Original token order, or with
+    scan_order=True the backward set (delta_b, B_b, C_b, u_b) time-reversed.
     last_state: optional fp32 [2, Bt, Dc, N] (forward, backward branch)."""
     io = u.dtype
     Bt, Dc, L = u.shape
@@ -239,6 +243,13 @@ def bimamba_scan_fwd_v2(u, delta, delta_b, A, A_b, B, C, B_b, C_b, D=None, D_b=N
             _io(z, io, "z", sh, True), _par(delta_bias, "delta_bias", (Dc,), True),
             _par(delta_bias_b, "delta_bias_b", (Dc,), True)]
     wp, wn = _workspace("v2", io, Bt, Dc, L, N, u.device, workspace)
+    if scan_order:
+        ls = None if last_state is None else _par(last_state, "last_state", (2, Bt, Dc, N))
+        _check(_lib.bimamba_scan_fwd_v2_so(_dtype_code(u), Bt, Dc, L, N, *args,
+                                           int(bool(delta_softplus)), float(out_scale),
+                                           _io(y, io, "out", sh), ls, wp, wn, _stream(stream)),
+               "bimamba_scan_fwd_v2_so")
+        return y
     if last_state is None:
         _check(_lib.bimamba_scan_fwd_v2(_dtype_code(u), Bt, Dc, L, N, *args,
                                         int(bool(delta_softplus)), float(out_scale),

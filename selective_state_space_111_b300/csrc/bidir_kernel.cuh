@@ -75,6 +75,7 @@ struct BiBranch {
     long long dt_bstride;  // elements between batch elements of dt
     int stream_rev;        // backward branch only: dt and B/C are stored in
                            // walk order (index L-1-p for position p)
+    int u_stream_rev;      // backward branch only: u is stored in walk order too
 };
 
 // What the finalising branch does with the fused value v = out_scale *
@@ -442,7 +443,7 @@ bidir_scan_kernel(const BiParams P) {
         constexpr int NG = 16 / GR;
         const int pw = warp - NSW;
         int gd[NG], gn[NG];
-        bool gsrev[NG];
+        bool gsrev[NG], gusr[NG];
         const IO *gdt[NG], *gu[NG];
 #pragma unroll
         for (int g = 0; g < NG; ++g) {
@@ -451,6 +452,7 @@ bidir_scan_kernel(const BiParams P) {
             const BiBranch &br = P.br[d];
             gd[g] = d;
             gsrev[g] = br.stream_rev != 0;
+            gusr[g] = br.u_stream_rev != 0;
             gn[g] = min(GR, D - (d0 + r0));                  // valid channels
             // first row of the group in dt and u; row i is i * L further on
             // (offsets within the rows stay below D * L < 2^31)
@@ -479,8 +481,9 @@ bidir_scan_kernel(const BiParams P) {
             for (int g = 0; g < NG; ++g) {
                 int lo;
                 chunk_geom(c, gd[g], L, T, lo, len);
-                p[g] = gd[g] ? lo + len - 1 - j : lo + j;        // position of walk step j
-                si[g] = gsrev[g] ? c * T + j : p[g];              // dt stream index
+                const int pos = gd[g] ? lo + len - 1 - j : lo + j;   // position of walk step j
+                si[g] = gsrev[g] ? c * T + j : pos;                  // dt stream index
+                p[g] = gusr[g] ? c * T + j : pos;                    // u index
             }
             if (len == T && all_rows) {
 #pragma unroll

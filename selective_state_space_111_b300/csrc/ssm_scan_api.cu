@@ -205,7 +205,7 @@ ssm_status bidirectional(ssm_dtype dt, int B, int D, int L, int N, const void *u
                          const float *D_b, const void *z, const float *bias,
                          const float *bias_b, int delta_softplus, float out_scale, void *y,
                          void *ws, size_t ws_bytes, bool two_sets, cudaStream_t stream,
-                         float *ls = nullptr) {
+                         float *ls = nullptr, bool scan_order = false) {
     ssm_status s = check_common(dt, B, D, L, N);
     if (s != SSM_OK) return s;
     if (!opt_f32_ok(ls)) return SSM_ERR_INVALID_ARG;
@@ -224,6 +224,11 @@ ssm_status bidirectional(ssm_dtype dt, int B, int D, int L, int N, const void *u
     P.br[0] = {delta, u, (const float *)(wsb + lay.bc0), A, Dskip, bias, 0, DL, 0};
     P.br[1] = {delta_b, u_b ? u_b : u, (const float *)(wsb + lay.bc1), A_b, D_b, bias_b,
                0, DL, 0};
+    if (scan_order) {
+        // the backward set is given in its own walk order (reversed time)
+        P.br[1].stream_rev = 1;
+        P.br[1].u_stream_rev = u_b != nullptr;
+    }
     P.z = z;
     P.y = y;
     P.W = lay.w ? (float *)(wsb + lay.w) : nullptr;
@@ -527,6 +532,20 @@ ssm_status bimamba_scan_fwd_v2_ls(ssm_dtype dt, int B, int D, int L, int N, cons
     return bidirectional(dt, B, D, L, N, u, u_b, delta, delta_b, A, A_b, Bm, Cm, Bm_b, Cm_b,
                          Dskip, D_b, z, delta_bias, delta_bias_b, delta_softplus, out_scale, y,
                          workspace, ws_bytes, true, (cudaStream_t)stream, last_state);
+}
+
+ssm_status bimamba_scan_fwd_v2_so(ssm_dtype dt, int B, int D, int L, int N, const void *u,
+                                  const void *u_b, const void *delta, const void *delta_b,
+                                  const float *A, const float *A_b, const void *Bm,
+                                  const void *Cm, const void *Bm_b, const void *Cm_b,
+                                  const float *Dskip, const float *D_b, const void *z,
+                                  const float *delta_bias, const float *delta_bias_b,
+                                  int delta_softplus, float out_scale, void *y,
+                                  float *last_state, void *workspace, size_t ws_bytes,
+                                  ssm_stream_t stream) {
+    return bidirectional(dt, B, D, L, N, u, u_b, delta, delta_b, A, A_b, Bm, Cm, Bm_b, Cm_b,
+                         Dskip, D_b, z, delta_bias, delta_bias_b, delta_softplus, out_scale, y,
+                         workspace, ws_bytes, true, (cudaStream_t)stream, last_state, true);
 }
 
 ssm_status bimamba_scan_fwd_v2_noalloc(ssm_dtype dt, int B, int D, int L, int N,

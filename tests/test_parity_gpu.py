@@ -178,6 +178,31 @@ def test_last_state(op, io, cta):
     assert max_scaled_err(y, run_oracle(spec, t)) <= TOL[io]
 
 
+@pytest.mark.parametrize("shared_u", [True, False])
+def test_v2_scan_order_inputs(shared_u, cta):
+    # the backward set given time-reversed gives the same y (and states)
+    import selective_state_space_111_b300 as ssm
+    spec = Spec("v2", "bf16", B=2, D=21, L=133, perturb=True, shared_u=shared_u, out_scale=0.5)
+    t = make_inputs(spec, 31)
+    g = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in t.items()}
+    fl = {k: (torch.flip(g[k], dims=[-1]) if g[k] is not None else None)
+          for k in ("delta_b", "B_b", "C_b", "u_b")}
+    ls1 = torch.empty(2, 2, 21, 16, device="cuda")
+    ls2 = torch.empty_like(ls1)
+    y1 = ssm.bimamba_scan_fwd_v2(g["u"], g["delta"], g["delta_b"], g["A"], g["A_b"], g["B"],
+                                 g["C"], g["B_b"], g["C_b"], g["D"], g["D_b"], g["z"],
+                                 g["delta_bias"], g["delta_bias_b"], g["u_b"], True, 0.5,
+                                 last_state=ls1)
+    y2 = ssm.bimamba_scan_fwd_v2(g["u"], g["delta"], fl["delta_b"], g["A"], g["A_b"], g["B"],
+                                 g["C"], fl["B_b"], fl["C_b"], g["D"], g["D_b"], g["z"],
+                                 g["delta_bias"], g["delta_bias_b"], fl["u_b"], True, 0.5,
+                                 last_state=ls2, scan_order=True)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)          # same arithmetic in the same order
+    assert torch.equal(ls1, ls2)
+    assert max_scaled_err(y2, run_oracle(spec, t)) <= TOL["bf16"]
+
+
 def test_length_one_branches_agree():
     # With L = 1 and identical parameter sets the two branches coincide, so
     # v2 with out_scale 0.5 equals the single-direction scan.
