@@ -365,6 +365,34 @@ SSM_API size_t ssm_bwd_workspace_bytes(ssm_op op, ssm_dtype dt, int B, int D,
                                        int L_or_HW, int N, int K,
                                        int separate_u_b);
 
+/* ---------------------------------------------------------------------------
+ * Prologue: the steps that turn a block's input x into the scan's inputs,
+ * for one direction ("Vision Mamba实战" section 2.1, "从Transformer到Mamba"
+ * section 2.1: conv1d, x_proj, dt_proj; "VMamba的SS2D模块详解" section 3.1:
+ * dt, B, C = split(x_proj(.), [dt_rank, d_state, d_state])):
+ *   u[t]  = silu(conv_b[d] + sum_k conv_w[d][k] * xs[t - (K-1) + k])
+ *           (depthwise, causal: xs before the start is 0)
+ *   [dt_low; B; C] = W_x u        (W_x [R + 2N, D] fp32, rows in that order)
+ *   delta = W_dt dt_low           (W_dt [D, R] fp32; dt_proj's bias is the
+ *                                  scan's delta_bias, applied there with the
+ *                                  softplus)
+ * xs = x [B, D, L], or x reversed in time when reverse != 0 -- v2's backward
+ * branch runs its own weights on the flipped sequence, and its outputs then
+ * come out in that branch's scan order, ready for bimamba_scan_fwd_v2_so.
+ * Outputs (I/O dtype, device, caller-owned): u, delta [B, D, L]; Bm, Cm
+ * [B, N, L] -- the layouts the scan calls take.  N <= 32, 1 <= K <= 8.
+ * workspace: ssm_prologue_workspace_bytes(B, L, R) bytes, 16-byte aligned
+ * (the fp32 dt_low).  State of the art for the projections would be tensor
+ * cores; these kernels use fp32 FMA (outputs rounded to the I/O dtype).
+ * ------------------------------------------------------------------------- */
+SSM_API ssm_status mamba_prologue_fwd(ssm_dtype dt, int B, int D, int L, int N,
+                         int R, int K, const void *x, const float *conv_w,
+                         const float *conv_b, const float *W_x,
+                         const float *W_dt, int reverse, void *u, void *delta,
+                         void *Bm, void *Cm, void *workspace, size_t ws_bytes,
+                         ssm_stream_t stream);
+SSM_API size_t ssm_prologue_workspace_bytes(int B, int L, int R);
+
 /*
  * Tuning override for the two-branch kernels (v1, v2 and both SS2D passes).
  * A CTA takes `channels` channels of one batch element, both branches:

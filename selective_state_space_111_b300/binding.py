@@ -62,6 +62,10 @@ _lib.bimamba_scan_bwd_v1.argtypes = ([_i] * 5 + [_vp] * 9 + [_i, _f] + [_vp] * 1
 _lib.bimamba_scan_bwd_v2.argtypes = ([_i] * 5 + [_vp] * 15 + [_i, _f] + [_vp] * 17 +
                                      [_sz, _vp])
 _lib.ss2d_scan_bwd.argtypes = [_i] * 7 + [_vp] * 8 + [_i] + [_vp] * 10 + [_sz, _vp]
+_lib.mamba_prologue_fwd.argtypes = [_i] * 7 + [_vp] * 5 + [_i] + [_vp] * 5 + [_sz, _vp]
+_lib.mamba_prologue_fwd.restype = _i
+_lib.ssm_prologue_workspace_bytes.argtypes = [_i, _i, _i]
+_lib.ssm_prologue_workspace_bytes.restype = _sz
 _lib.ssm_bwd_workspace_bytes.argtypes = [_i] * 8
 _lib.ssm_bwd_workspace_bytes.restype = _sz
 for _fn in (_lib.selective_scan_fwd, _lib.bimamba_scan_fwd_v1, _lib.bimamba_scan_fwd_v2,
@@ -478,3 +482,33 @@ def ss2d_scan_bwd(dout, x, delta, A, B, C, D=None, z=None, delta_bias=None,
                               *map(_ptr_or_none, outs), wp, wn, _stream(stream)),
            "ss2d_scan_bwd")
     return g
+
+
+# ---------------------------------------------------------------- prologue
+def mamba_prologue_fwd(x, conv_w, conv_b, W_x, W_dt, dt_rank, d_state, reverse=False,
+                       workspace=None, stream=None):
+    """One direction's conv1d + SiLU, x_proj split and dt_proj.  x: [Bt, Dc, L]
+    (I/O dtype); conv_w [Dc, K], conv_b [Dc] (or None), W_x [R + 2N, Dc],
+    W_dt [Dc, R] fp32.  Returns (u, delta, B, C): [Bt, Dc, L] x2, [Bt, N, L] x2,
+    in scan order of the reversed sequence when reverse=True."""
+    io = x.dtype
+    Bt, Dc, L = x.shape
+    R, N = int(dt_rank), int(d_state)
+    K = conv_w.shape[1]
+    u = torch.empty_like(x)
+    delta = torch.empty_like(x)
+    Bm = torch.empty((Bt, N, L), dtype=io, device=x.device)
+    Cm = torch.empty((Bt, N, L), dtype=io, device=x.device)
+    need = int(_lib.ssm_prologue_workspace_bytes(Bt, L, R))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    _check(_lib.mamba_prologue_fwd(_dtype_code(x), Bt, Dc, L, N, R, K, _io(x, io, "x"),
+                                   _par(conv_w, "conv_w", (Dc, K)),
+                                   _par(conv_b, "conv_b", (Dc,), True),
+                                   _par(W_x, "W_x", (R + 2 * N, Dc)),
+                                   _par(W_dt, "W_dt", (Dc, R)), int(bool(reverse)),
+                                   u.data_ptr(), delta.data_ptr(), Bm.data_ptr(), Cm.data_ptr(),
+                                   workspace.data_ptr(),
+                                   workspace.numel() * workspace.element_size(),
+                                   _stream(stream)), "mamba_prologue_fwd")
+    return u, delta, Bm, Cm

@@ -2,8 +2,9 @@
 
     python -m selective_state_space_111_b300.build
 
-nvcc compiles csrc/ssm_scan_api.cu (forward) and csrc/ssm_bwd_api.cu
-(backward), which include their kernel headers, into one shared library with the CUDA runtime linked statically, so the .so loads on a
+nvcc compiles csrc/ssm_scan_api.cu (forward), csrc/ssm_bwd_api.cu (backward)
+and csrc/ssm_prologue_api.cu (prologue), which include their kernel headers,
+into one shared library with the CUDA runtime linked statically, so the .so loads on a
 machine without a GPU as well (for symbol checks) and needs nothing from the
 environment at run time beyond the NVIDIA driver.
 """
@@ -14,9 +15,11 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libssm_scan.so")
-SOURCES = [os.path.join(HERE, "csrc", f) for f in ("ssm_scan_api.cu", "ssm_bwd_api.cu")]
+SOURCES = [os.path.join(HERE, "csrc", f) for f in ("ssm_scan_api.cu", "ssm_bwd_api.cu",
+                                                   "ssm_prologue_api.cu")]
 DEPS = SOURCES + [os.path.join(HERE, "csrc", f) for f in
-                  ("bidir_kernel.cuh", "bwd_kernel.cuh", "scan_ops.cuh")] + [
+                  ("bidir_kernel.cuh", "bwd_kernel.cuh", "prologue_kernel.cuh",
+                   "scan_ops.cuh")] + [
                   os.path.join(ROOT, "include", "ssm_scan.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
