@@ -303,6 +303,9 @@ def run_ours(args):
     bwd = None
     if not args.no_backward:
         bwd = measure_backward(ssm, spec, g, t, dev, stream, max(3, min(args.steps, 20)))
+    pro = None
+    if not args.no_prologue and spec.op != "ss2d":
+        pro = measure_prologue(ssm, spec, dev, stream, max(3, min(args.steps, 20)))
 
     if rank == 0:
         ms = total_ms / args.steps
@@ -364,6 +367,13 @@ def run_ours(args):
                                "peak_basis": "148 SMs x 128 fp32 lanes x %.0f MHz / 16 fp32 "
                                              "ops per update" % sm_max}
             line["backward"] = bwd
+        if pro:
+            # the projections run on fp32 FMA: 128 lanes x 2 flops per SM and clock
+            fpeak = 148 * 128 * 2 * sm_max * 1e6 / 1e12
+            pro["roofline"] = {"bound": "fp32", "achieved": round(pro.pop("tflops"), 2),
+                               "peak": round(fpeak, 1), "unit": "TFLOP/s"}
+            pro["roofline"]["frac"] = round(pro["roofline"]["achieved"] / fpeak, 4)
+            line["prologue"] = pro
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(spec, args.workload, args.cpu_seconds)
         print(json.dumps(line), flush=True)
@@ -415,6 +425,48 @@ def measure_backward(ssm, spec, g, t, dev, stream, steps):
     return {"ms_per_call": round(ms, 4), "ms": ms, "steps": steps,
             "bytes_per_call": spec.backward_bytes(),
             "elem_updates_per_s": float("%.4g" % (spec.updates() / (ms * 1e-3)))}
+
+
+def measure_prologue(ssm, spec, dev, stream, steps):
+    """Time the prologue that feeds the scan (conv1d + SiLU, x_proj, dt_proj)
+    on an input of the workload's shape: both branches for v2 (the backward
+    one on the flipped input), one for v1 (shared weights) and single.
+    dt_rank = ceil(d_model / 16) with d_model = D / 2; weights synthetic."""
+    import torch
+    B, D, L, N = spec.B, spec.D, spec.seq_len, spec.N
+    R, K = -(-D // 32), 4
+    dirs = 2 if spec.op == "v2" else 1
+    gen = torch.Generator().manual_seed(4321)
+    io = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[spec.io]
+    x = torch.randn(B, D, L, generator=gen).to(dtype=io, device=dev)
+    w = [dict(conv_w=(torch.rand(D, K, generator=gen) - 0.5).to(dev),
+              conv_b=(torch.rand(D, generator=gen) - 0.5).to(dev),
+              W_x=(torch.randn(R + 2 * N, D, generator=gen) * D ** -0.5).to(dev),
+              W_dt=(torch.randn(D, R, generator=gen) * R ** -0.5).to(dev)) for _ in range(dirs)]
+    ws = torch.empty(B * R * L * 4, dtype=torch.uint8, device=dev)
+
+    def once():
+        for k in range(dirs):
+            ssm.mamba_prologue_fwd(x, w[k]["conv_w"], w[k]["conv_b"], w[k]["W_x"], w[k]["W_dt"],
+                                   R, N, reverse=k == 1, workspace=ws)
+
+    for _ in range(3):
+        once()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        once()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    e = x.element_size()
+    # per direction: x read; u, dt written [B,D,L]; B, C written [B,N,L]
+    nbytes = dirs * e * (3 * B * D * L + 2 * B * N * L)
+    flops = dirs * 2.0 * B * L * ((R + 2 * N) * D + D * R)
+    return {"ms_per_call": round(ms, 4), "directions": dirs, "dt_rank": R, "d_conv": K,
+            "value": round(nbytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "tflops": flops / (ms * 1e-3) / 1e12}
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -506,6 +558,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-backward", action="store_true",
                     help="skip the backward-pass timing (reported under 'backward')")
+    ap.add_argument("--no-prologue", action="store_true",
+                    help="skip the prologue timing (reported under 'prologue')")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture")

@@ -1,6 +1,7 @@
 // prologue_kernel.cuh -- the steps that feed the scan (sm_103a), one direction:
 //   u  = silu(causal depthwise conv1d(x) + bias)      (conv_silu_kernel)
-//   [dt_low; B; C] = W_x @ u,  dt = W_dt @ dt_low     (proj_kernel, twice)
+//   [dt_low; B; C] = W_x @ u                          (xproj_mma_kernel / proj_*)
+//   dt = W_dt @ dt_low                                (dtproj_kernel / proj_*)
 // as in "Vision Mamba实战" section 2.1 and "从Transformer到Mamba" section 2.1
 // (conv1d, x_proj = Linear(d_inner -> dt_rank + 2 d_state), dt_proj =
 // Linear(dt_rank -> d_inner)) and "VMamba的SS2D模块详解" section 3.1 (the
@@ -17,22 +18,49 @@ namespace ssm {
 namespace pro {
 
 // u[b][d][t] = silu(bias[d] + sum_k w[d][k] * xs[t - (K-1) + k]), xs = x or
-// x reversed in time, zero before the start.  One thread per output.
-template <typename IO>
+// x reversed in time, zero before the start.  A CTA covers CONV_T positions
+// of one row: it stages xs over them plus the K - 1 halo in shared memory
+// (coalesced reads, in reverse order for reverse = 1), then each thread
+// makes CONV_T / 256 outputs, consecutive threads on consecutive positions.
+// KT = K fixed at compile time (the usual 4 taps), or 0 for any K <= 8.
+constexpr int CONV_T = 2048;
+template <typename IO, int KT>
 __global__ void __launch_bounds__(256)
 conv_silu_kernel(const IO *__restrict__ x, const float *__restrict__ w,
                  const float *__restrict__ bias, IO *__restrict__ u, int D, int L, int K,
                  int reverse) {
-    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    __shared__ float sx[CONV_T + 8];            // sx[i] = xs[t0 - (K-1) + i], K <= 8
+    const int t0 = blockIdx.x * CONV_T;
     const int d = blockIdx.y, b = blockIdx.z;
-    if (t >= L) return;
     const long long row = ((long long)b * D + d) * L;
-    float acc = bias ? bias[d] : 0.f;
-    for (int k = 0; k < K; ++k) {
-        const int ts = t - (K - 1) + k;
-        if (ts >= 0) acc = fmaf(w[d * K + k], to_f32(x[row + (reverse ? L - 1 - ts : ts)]), acc);
+    const int n_in = min(CONV_T, L - t0) + K - 1;
+    float v[(CONV_T + 8 + 255) / 256];          // every load in flight before the stores
+#pragma unroll
+    for (int j = 0; j < (CONV_T + 8 + 255) / 256; ++j) {
+        const int i = j * 256 + threadIdx.x, ts = t0 - (K - 1) + i;
+        v[j] = (i < n_in && ts >= 0) ? to_f32(x[row + (reverse ? L - 1 - ts : ts)]) : 0.f;
     }
-    u[row + t] = from_f32<IO>(acc / (1.f + expf(-acc)));
+#pragma unroll
+    for (int j = 0; j < (CONV_T + 8 + 255) / 256; ++j) {
+        const int i = j * 256 + threadIdx.x;
+        if (i < CONV_T + 8) sx[i] = v[j];
+    }
+    constexpr int KM = KT > 0 ? KT : 8;
+    float wk[KM];
+#pragma unroll
+    for (int k = 0; k < KM; ++k) wk[k] = (KT > 0 || k < K) ? w[d * K + k] : 0.f;
+    const float bv = bias ? bias[d] : 0.f;
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < CONV_T / 256; ++j) {
+        const int tt = j * 256 + threadIdx.x, t = t0 + tt;
+        if (t >= L) break;
+        float acc = bv;
+#pragma unroll
+        for (int k = 0; k < KM; ++k)
+            if (KT > 0 || k < K) acc = fmaf(wk[k], sx[tt + k], acc);
+        u[row + t] = from_f32<IO>(silu_f<IO>(acc));
+    }
 }
 
 // Output rows [0, M) of one projection go to up to three destinations:
@@ -105,6 +133,288 @@ proj_kernel(const float *__restrict__ W, const IN *__restrict__ in, int M, int K
             if (out.f32[s]) ((float *)out.dst[s])[o + t] = acc[i][j];
             else ((IO *)out.dst[s])[o + t] = from_f32<IO>(acc[i][j]);
         }
+    }
+}
+
+// ---- tensor-core projection (bf16 / fp16 I/O): mma.sync m16n8k16, fp32
+// accumulation.  CTA tile 64 (rows) x 64 (positions), K in slices of 32;
+// 8 warps, warp w computes rows 16 (w % 4) .. +16 of positions 32 (w / 4)
+// .. +32 (four 16 x 8 tiles).  Operands are staged in shared memory in the
+// I/O type (weights converted from fp32): W as [row][k], the input
+// transposed as [position][k], so every fragment register is one aligned
+// 32-bit load (fragment layouts of the PTX ISA's mma.m16n8k16).
+constexpr int TK = 32, TKP = TK + 8;         // K slice, padded row (bank spread)
+
+template <typename IO> __device__ __forceinline__ void mma16816(float (&c)[4], const unsigned (&a)[4],
+                                                                 const unsigned (&b)[2]);
+template <> __device__ __forceinline__ void mma16816<__nv_bfloat16>(float (&c)[4],
+                                                                    const unsigned (&a)[4],
+                                                                    const unsigned (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+template <> __device__ __forceinline__ void mma16816<__half>(float (&c)[4], const unsigned (&a)[4],
+                                                             const unsigned (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+template <typename IN, typename IO>
+__global__ void __launch_bounds__(256)
+proj_mma_kernel(const float *__restrict__ W, const IN *__restrict__ in, int M, int K, int L,
+                ProjOut out) {
+    __shared__ __align__(16) IO sW[BM][TKP];        // [row][k]
+    __shared__ __align__(16) IO sI[BN][TKP];        // [position][k]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, tg = lane & 3;
+    const int wm = (warp % 4) * 16, wn = (warp / 4) * 32;
+    const int t0 = blockIdx.x * BN, m0 = blockIdx.y * BM, b = blockIdx.z;
+    const IN *inb = in + (long long)b * K * L;
+    float acc[4][4] = {};
+    for (int k0 = 0; k0 < K; k0 += TK) {
+        // W slice: 64 x 32 (k fastest: coalesced fp32 reads)
+#pragma unroll
+        for (int r = 0; r < (BM * TK) / 256; ++r) {
+            const int i = tid + r * 256, mm = i / TK, kk = i % TK;
+            const int m = m0 + mm, k = k0 + kk;
+            sW[mm][kk] = from_f32<IO>((m < M && k < K) ? W[(long long)m * K + k] : 0.f);
+        }
+        // input slice: 32 x 64 (positions fastest: coalesced), stored transposed
+#pragma unroll
+        for (int r = 0; r < (TK * BN) / 256; ++r) {
+            const int i = tid + r * 256, kk = i / BN, tt = i % BN;
+            const int k = k0 + kk, t = t0 + tt;
+            sI[tt][kk] = from_f32<IO>((k < K && t < L) ? to_f32(inb[(long long)k * L + t]) : 0.f);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int ks = 0; ks < TK; ks += 16) {
+            unsigned a[4];
+            a[0] = *(const unsigned *)&sW[wm + g][ks + 2 * tg];
+            a[1] = *(const unsigned *)&sW[wm + g + 8][ks + 2 * tg];
+            a[2] = *(const unsigned *)&sW[wm + g][ks + 2 * tg + 8];
+            a[3] = *(const unsigned *)&sW[wm + g + 8][ks + 2 * tg + 8];
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                unsigned bf[2];
+                bf[0] = *(const unsigned *)&sI[wn + nt * 8 + g][ks + 2 * tg];
+                bf[1] = *(const unsigned *)&sI[wn + nt * 8 + g][ks + 2 * tg + 8];
+                mma16816<IO>(acc[nt], a, bf);
+            }
+        }
+        __syncthreads();
+    }
+    // c0, c1: row g, positions 2tg, 2tg+1; c2, c3: row g + 8
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int m = m0 + wm + g + 8 * half;
+        if (m >= M) continue;
+        int s = 0;
+        while (m >= out.r[s + 1]) ++s;
+        const int rows = out.r[s + 1] - out.r[s], mr = m - out.r[s];
+        const long long o = ((long long)b * rows + mr) * L;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int t = t0 + wn + nt * 8 + 2 * tg + j;
+                if (t >= L) continue;
+                const float v = acc[nt][2 * half + j];
+                if (out.f32[s]) ((float *)out.dst[s])[o + t] = v;
+                else ((IO *)out.dst[s])[o + t] = from_f32<IO>(v);
+            }
+    }
+}
+
+// dt_proj with a short inner dimension (R = dt_rank <= RP, RP in {8, 16, 24,
+// 32}): out[b][m][t] = sum_r W[m][r] in[b][r][t].  A CTA takes DTP_T
+// positions (two per thread, DTP_T / 2 apart, their R inputs in registers)
+// and rows [m_lo, m_hi) in chunks of 128 staged in shared memory (zero-
+// padded to RP, read back as broadcast float4); stores are coalesced along
+// positions.  grid.y splits the rows so that short batches still fill the
+// GPU.
+constexpr int DTP_T = 512, DTP_MC = 128;
+template <typename IO, int RP>
+__global__ void __launch_bounds__(256, 2)
+dtproj_kernel(const float *__restrict__ W, const float *__restrict__ in, int M, int R, int L,
+              IO *__restrict__ out) {
+    __shared__ __align__(16) float sW[DTP_MC * RP];
+    const int b = blockIdx.z;
+    const int t_a = blockIdx.x * DTP_T + threadIdx.x, t_b = t_a + DTP_T / 2;
+    const int per = (M + gridDim.y - 1) / gridDim.y;
+    const int m_lo = blockIdx.y * per, m_hi = min(M, m_lo + per);
+    float va[RP], vb[RP];
+#pragma unroll
+    for (int r = 0; r < RP; ++r) {
+        const float *src = in + ((long long)b * R + r) * L;
+        va[r] = (r < R && t_a < L) ? src[t_a] : 0.f;
+        vb[r] = (r < R && t_b < L) ? src[t_b] : 0.f;
+    }
+    for (int m0 = m_lo; m0 < m_hi; m0 += DTP_MC) {
+        const int mc = min(DTP_MC, m_hi - m0);
+        __syncthreads();
+        float wv[DTP_MC * RP / 256];                     // all in flight, then stored
+#pragma unroll
+        for (int j = 0; j < DTP_MC * RP / 256; ++j) {
+            const int i = j * 256 + threadIdx.x, mm = i / RP, r = i % RP;
+            wv[j] = (mm < mc && r < R) ? W[(long long)(m0 + mm) * R + r] : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < DTP_MC * RP / 256; ++j) sW[j * 256 + threadIdx.x] = wv[j];
+        __syncthreads();
+        for (int mm = 0; mm < mc; ++mm) {
+            const float4 *wr = (const float4 *)&sW[mm * RP];
+            float acc_a = 0.f, acc_b = 0.f;
+#pragma unroll
+            for (int q = 0; q < RP / 4; ++q) {
+                const float4 w4 = wr[q];
+                acc_a = fmaf(w4.x, va[4 * q], acc_a);
+                acc_b = fmaf(w4.x, vb[4 * q], acc_b);
+                acc_a = fmaf(w4.y, va[4 * q + 1], acc_a);
+                acc_b = fmaf(w4.y, vb[4 * q + 1], acc_b);
+                acc_a = fmaf(w4.z, va[4 * q + 2], acc_a);
+                acc_b = fmaf(w4.z, vb[4 * q + 2], acc_b);
+                acc_a = fmaf(w4.w, va[4 * q + 3], acc_a);
+                acc_b = fmaf(w4.w, vb[4 * q + 3], acc_b);
+            }
+            IO *o = out + ((long long)b * M + m0 + mm) * L;
+            if (t_a < L) o[t_a] = from_f32<IO>(acc_a);
+            if (t_b < L) o[t_b] = from_f32<IO>(acc_b);
+        }
+    }
+}
+
+// x_proj on tensor cores, weights stationary (16-bit I/O, M <= 64 rows).  A
+// persistent CTA converts the whole W [M][K] to the I/O type once into
+// shared memory ([row][k], padded to KP), then loops over tiles of XP_T
+// positions of one of the nb batch elements, streaming the input in K slices of XP_K:
+// the next slice is loaded into registers while the current one feeds the
+// mma (8 warps; warp w owns rows 16 (w % 4) .. +16 and positions 64 (w / 4)
+// .. +64).  Slices are stored transposed, [position][k], two k per 32-bit
+// word, so every fragment register is one aligned 32-bit shared load (the
+// PTX ISA's m16n8k16 fragment layouts).  The accumulators leave through a
+// shared [row][position] fp32 tile so that the global stores run along
+// positions.
+constexpr int XP_T = 128, XP_K = 128, XP_KP = XP_K + 8, XP_OP = XP_T + 8;
+__host__ __device__ constexpr int xproj_kp(int K) { return ((K + XP_K - 1) / XP_K) * XP_K + 8; }
+inline size_t xproj_smem_bytes(int K, size_t esize) {
+    return (64 * (size_t)xproj_kp(K) + 2 * (size_t)XP_T * XP_KP) * esize;
+}
+template <typename IO>
+__global__ void __launch_bounds__(256, 1)
+xproj_mma_kernel(const float *__restrict__ W, const IO *__restrict__ in, int M, int K, int L,
+                 int nb, ProjOut out) {
+    extern __shared__ __align__(16) unsigned char xp_smem[];
+    const int KP = xproj_kp(K);
+    IO *sW = (IO *)xp_smem;                                    // [64][KP]
+    IO *sI = sW + 64 * KP;                                     // [2][XP_T][XP_KP]
+    float *sO = (float *)sI;                                   // [64][XP_OP], after the slices
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, tg = lane & 3;
+    const int wm = (warp % 4) * 16, wn = (warp / 4) * 64;
+    // slice loader: unit q = j * 8 + warp covers 16 positions x 2 k-pairs;
+    // a lane loads the k-pair (2 kp, 2 kp + 1) of one position
+    const int ld_tt = lane & 15, ld_kp = lane >> 4;
+    // W row by row (warp w takes rows w, w + 8, ...; lanes along k, four
+    // loads in flight each), zero past column K and past row M
+    for (int m = warp; m < 64; m += 8) {
+        IO *dst = sW + m * KP;
+        const float *src = W + (long long)m * K;
+        for (int k0 = 0; k0 < KP; k0 += 128) {
+            float wv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int k = k0 + u * 32 + lane;
+                wv[u] = (m < M && k < K) ? src[k] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int k = k0 + u * 32 + lane;
+                if (k < KP) dst[k] = from_f32<IO>(wv[u]);
+            }
+        }
+    }
+    const int tpb = (L + XP_T - 1) / XP_T, ntiles = tpb * nb;
+    const int nk = (K + XP_K - 1) / XP_K;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        const int b = tile / tpb, t0 = (tile % tpb) * XP_T;
+        const IO *inb = in + (long long)b * K * L;
+        unsigned short reg[2 * (XP_T * XP_K / 2) / 256];       // 64 halves per thread
+        auto load = [&](int k0) {
+#pragma unroll
+            for (int j = 0; j < (XP_T * XP_K / 2) / (16 * 2 * 8); ++j) {
+                const int q = j * 8 + warp, tt = (q % 8) * 16 + ld_tt;
+                const int k = k0 + 2 * ((q / 8) * 2 + ld_kp), t = t0 + tt;
+                const bool tin = t < L;
+                const IO z = from_f32<IO>(0.f);
+                const IO v0 = (tin && k < K) ? inb[(long long)k * L + t] : z;
+                const IO v1 = (tin && k + 1 < K) ? inb[(long long)(k + 1) * L + t] : z;
+                reg[2 * j] = *(const unsigned short *)&v0;
+                reg[2 * j + 1] = *(const unsigned short *)&v1;
+            }
+        };
+        auto store = [&](int buf) {
+            unsigned *dst = (unsigned *)(sI + buf * XP_T * XP_KP);
+#pragma unroll
+            for (int j = 0; j < (XP_T * XP_K / 2) / (16 * 2 * 8); ++j) {
+                const int q = j * 8 + warp, tt = (q % 8) * 16 + ld_tt;
+                const int kp = (q / 8) * 2 + ld_kp;
+                dst[tt * (XP_KP / 2) + kp] = (unsigned)reg[2 * j] | ((unsigned)reg[2 * j + 1] << 16);
+            }
+        };
+        float acc[8][4] = {};
+        load(0);
+        for (int ki = 0; ki < nk; ++ki) {
+            const int buf = ki & 1;
+            store(buf);
+            __syncthreads();
+            if (ki + 1 < nk) load((ki + 1) * XP_K);               // in flight during the mma
+            const IO *bI = sI + buf * XP_T * XP_KP;
+#pragma unroll
+            for (int ks = 0; ks < XP_K; ks += 16) {
+                const int kw = ki * XP_K + ks;
+                unsigned a[4];
+                a[0] = *(const unsigned *)&sW[(wm + g) * KP + kw + 2 * tg];
+                a[1] = *(const unsigned *)&sW[(wm + g + 8) * KP + kw + 2 * tg];
+                a[2] = *(const unsigned *)&sW[(wm + g) * KP + kw + 2 * tg + 8];
+                a[3] = *(const unsigned *)&sW[(wm + g + 8) * KP + kw + 2 * tg + 8];
+#pragma unroll
+                for (int nt = 0; nt < 8; ++nt) {
+                    unsigned bf[2];
+                    const IO *col = bI + (wn + nt * 8 + g) * XP_KP + ks + 2 * tg;
+                    bf[0] = *(const unsigned *)col;
+                    bf[1] = *(const unsigned *)(col + 8);
+                    mma16816<IO>(acc[nt], a, bf);
+                }
+            }
+        }
+        __syncthreads();                                        // slices dead: reuse as sO
+        // c0, c1: row g, positions 2tg, 2tg+1; c2, c3: row g + 8
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int half = 0; half < 2; ++half)
+                *(float2 *)&sO[(wm + g + 8 * half) * XP_OP + wn + nt * 8 + 2 * tg] =
+                    make_float2(acc[nt][2 * half], acc[nt][2 * half + 1]);
+        __syncthreads();
+        for (int i = tid; i < M * XP_T; i += 256) {
+            const int m = i / XP_T, tt = i % XP_T, t = t0 + tt;
+            if (t >= L) continue;
+            int s = 0;
+            while (m >= out.r[s + 1]) ++s;
+            const int rows = out.r[s + 1] - out.r[s], mr = m - out.r[s];
+            const long long o = ((long long)b * rows + mr) * L + t;
+            const float v = sO[m * XP_OP + tt];
+            if (out.f32[s]) ((float *)out.dst[s])[o] = v;
+            else ((IO *)out.dst[s])[o] = from_f32<IO>(v);
+        }
+        __syncthreads();                                        // sO dead before the next slices
     }
 }
 

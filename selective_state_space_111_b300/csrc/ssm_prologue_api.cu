@@ -5,6 +5,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "prologue_kernel.cuh"
@@ -22,13 +23,94 @@ ssm_status last_error() {
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return 148;
+    return n;
+}
+
+// generic tiled projection: fp32 FMA for fp32 I/O, mma.sync for 16-bit I/O
+template <typename IN, typename IO>
+void launch_proj(dim3 grid, const float *W, const IN *in, int M, int K, int L,
+                 ssm::pro::ProjOut o, cudaStream_t st) {
+    if constexpr (sizeof(IO) == 4)
+        ssm::pro::proj_kernel<IN, IO><<<grid, 256, 0, st>>>(W, in, M, K, L, o);
+    else
+        ssm::pro::proj_mma_kernel<IN, IO><<<grid, 256, 0, st>>>(W, in, M, K, L, o);
+}
+
+// x_proj: the weights-stationary tensor-core kernel when its rows (<= 64)
+// and W (in shared memory) fit, else the generic tiled one
+template <typename IO>
+ssm_status x_proj(int B, int M, int K, int L, const float *W, const IO *u, ssm::pro::ProjOut o,
+                  cudaStream_t st) {
+    using namespace ssm::pro;
+    if constexpr (sizeof(IO) == 2) {
+        const size_t smem = xproj_smem_bytes(K, sizeof(IO));
+        if (M <= 64 && smem <= 227 * 1024) {
+            if (cudaFuncSetAttribute(xproj_mma_kernel<IO>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem) != cudaSuccess)
+                return SSM_ERR_CUDA;
+            const long long tiles = (long long)B * ((L + XP_T - 1) / XP_T);
+            const int grid = (int)std::min<long long>(tiles, sm_count());
+            xproj_mma_kernel<IO><<<grid, 256, smem, st>>>(W, u, M, K, L, B, o);
+            return last_error();
+        }
+    }
+    launch_proj<IO, IO>(dim3((L + BN - 1) / BN, (M + BM - 1) / BM, B), W, u, M, K, L, o, st);
+    return last_error();
+}
+
+// dt_proj: the register-blocked FMA kernel for dt_rank <= 32, else the
+// generic tiled one
+template <typename IO, int RP>
+void launch_dtproj(int B, int D, int R, int L, const float *W, const float *dt_low, IO *dt,
+                   cudaStream_t st) {
+    using namespace ssm::pro;
+    const int tiles = (L + DTP_T - 1) / DTP_T;
+    const long long want = 4LL * sm_count();
+    int split = (int)std::min<long long>((want + (long long)tiles * B - 1) / ((long long)tiles * B),
+                                         (D + DTP_MC - 1) / DTP_MC);
+    split = std::max(split, 1);
+    dtproj_kernel<IO, RP><<<dim3(tiles, split, B), 256, 0, st>>>(W, dt_low, D, R, L, dt);
+}
+
+template <typename IO>
+ssm_status dt_proj(int B, int D, int R, int L, const float *W, const float *dt_low, IO *dt,
+                   cudaStream_t st) {
+    using namespace ssm::pro;
+    if (R <= 8) launch_dtproj<IO, 8>(B, D, R, L, W, dt_low, dt, st);
+    else if (R <= 16) launch_dtproj<IO, 16>(B, D, R, L, W, dt_low, dt, st);
+    else if (R <= 24) launch_dtproj<IO, 24>(B, D, R, L, W, dt_low, dt, st);
+    else if (R <= 32) launch_dtproj<IO, 32>(B, D, R, L, W, dt_low, dt, st);
+    else {
+        ProjOut o{};
+        o.dst[0] = dt;
+        o.r[0] = 0;
+        o.r[1] = D;
+        o.r[2] = D;
+        o.r[3] = D;
+        launch_proj<float, IO>(dim3((L + BN - 1) / BN, (D + BM - 1) / BM, B), W, dt_low, D, R, L,
+                               o, st);
+    }
+    return last_error();
+}
+
 template <typename IO>
 ssm_status run(int B, int D, int L, int N, int R, int K, const void *x, const float *conv_w,
                const float *conv_b, const float *W_x, const float *W_dt, int reverse, void *u,
                void *dt, void *Bm, void *Cm, float *dt_low, cudaStream_t st) {
     using namespace ssm::pro;
-    conv_silu_kernel<IO><<<dim3((L + 255) / 256, D, B), 256, 0, st>>>(
-        (const IO *)x, conv_w, conv_b, (IO *)u, D, L, K, reverse ? 1 : 0);
+    const dim3 cgrid((L + CONV_T - 1) / CONV_T, D, B);
+    if (K == 4)
+        conv_silu_kernel<IO, 4><<<cgrid, 256, 0, st>>>((const IO *)x, conv_w, conv_b, (IO *)u, D,
+                                                       L, K, reverse ? 1 : 0);
+    else
+        conv_silu_kernel<IO, 0><<<cgrid, 256, 0, st>>>((const IO *)x, conv_w, conv_b, (IO *)u, D,
+                                                       L, K, reverse ? 1 : 0);
     if (last_error() != SSM_OK) return SSM_ERR_CUDA;
     // x_proj: rows [0, R) -> dt_low (fp32), [R, R+N) -> B, [R+N, R+2N) -> C
     const int M = R + 2 * N;
@@ -41,19 +123,9 @@ ssm_status run(int B, int D, int L, int N, int R, int K, const void *x, const fl
     o1.r[1] = R;
     o1.r[2] = R + N;
     o1.r[3] = M;
-    proj_kernel<IO, IO><<<dim3((L + BN - 1) / BN, (M + BM - 1) / BM, B), 256, 0, st>>>(
-        W_x, (const IO *)u, M, D, L, o1);
-    if (last_error() != SSM_OK) return SSM_ERR_CUDA;
+    if (x_proj<IO>(B, M, D, L, W_x, (const IO *)u, o1, st) != SSM_OK) return SSM_ERR_CUDA;
     // dt_proj: all D rows -> dt
-    ProjOut o2{};
-    o2.dst[0] = dt;
-    o2.r[0] = 0;
-    o2.r[1] = D;
-    o2.r[2] = D;
-    o2.r[3] = D;
-    proj_kernel<float, IO><<<dim3((L + BN - 1) / BN, (D + BM - 1) / BM, B), 256, 0, st>>>(
-        W_dt, dt_low, D, R, L, o2);
-    return last_error();
+    return dt_proj<IO>(B, D, R, L, W_dt, dt_low, (IO *)dt, st);
 }
 
 }  // namespace
