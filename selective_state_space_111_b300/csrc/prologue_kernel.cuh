@@ -268,62 +268,76 @@ dtproj_kernel(const float *__restrict__ W, const float *__restrict__ in, int M, 
 #pragma unroll
         for (int j = 0; j < DTP_MC * RP / 256; ++j) sW[j * 256 + threadIdx.x] = wv[j];
         __syncthreads();
-        for (int mm = 0; mm < mc; ++mm) {
-            const float4 *wr = (const float4 *)&sW[mm * RP];
-            float acc_a = 0.f, acc_b = 0.f;
+        // two rows at a time: four independent accumulation chains
+        for (int mm = 0; mm < mc; mm += 2) {
+            const bool two = mm + 1 < mc;
+            const float4 *w0 = (const float4 *)&sW[mm * RP];
+            const float4 *w1 = (const float4 *)&sW[(two ? mm + 1 : mm) * RP];
+            float a0 = 0.f, b0 = 0.f, a1 = 0.f, b1 = 0.f;
 #pragma unroll
             for (int q = 0; q < RP / 4; ++q) {
-                const float4 w4 = wr[q];
-                acc_a = fmaf(w4.x, va[4 * q], acc_a);
-                acc_b = fmaf(w4.x, vb[4 * q], acc_b);
-                acc_a = fmaf(w4.y, va[4 * q + 1], acc_a);
-                acc_b = fmaf(w4.y, vb[4 * q + 1], acc_b);
-                acc_a = fmaf(w4.z, va[4 * q + 2], acc_a);
-                acc_b = fmaf(w4.z, vb[4 * q + 2], acc_b);
-                acc_a = fmaf(w4.w, va[4 * q + 3], acc_a);
-                acc_b = fmaf(w4.w, vb[4 * q + 3], acc_b);
+                const float4 x0 = w0[q], x1 = w1[q];
+                a0 = fmaf(x0.x, va[4 * q], a0);
+                b0 = fmaf(x0.x, vb[4 * q], b0);
+                a1 = fmaf(x1.x, va[4 * q], a1);
+                b1 = fmaf(x1.x, vb[4 * q], b1);
+                a0 = fmaf(x0.y, va[4 * q + 1], a0);
+                b0 = fmaf(x0.y, vb[4 * q + 1], b0);
+                a1 = fmaf(x1.y, va[4 * q + 1], a1);
+                b1 = fmaf(x1.y, vb[4 * q + 1], b1);
+                a0 = fmaf(x0.z, va[4 * q + 2], a0);
+                b0 = fmaf(x0.z, vb[4 * q + 2], b0);
+                a1 = fmaf(x1.z, va[4 * q + 2], a1);
+                b1 = fmaf(x1.z, vb[4 * q + 2], b1);
+                a0 = fmaf(x0.w, va[4 * q + 3], a0);
+                b0 = fmaf(x0.w, vb[4 * q + 3], b0);
+                a1 = fmaf(x1.w, va[4 * q + 3], a1);
+                b1 = fmaf(x1.w, vb[4 * q + 3], b1);
             }
             IO *o = out + ((long long)b * M + m0 + mm) * L;
-            if (t_a < L) o[t_a] = from_f32<IO>(acc_a);
-            if (t_b < L) o[t_b] = from_f32<IO>(acc_b);
+            if (t_a < L) o[t_a] = from_f32<IO>(a0);
+            if (t_b < L) o[t_b] = from_f32<IO>(b0);
+            if (two) {
+                if (t_a < L) o[L + t_a] = from_f32<IO>(a1);
+                if (t_b < L) o[L + t_b] = from_f32<IO>(b1);
+            }
         }
     }
 }
 
 // x_proj on tensor cores, weights stationary (16-bit I/O, M <= 64 rows).  A
-// persistent CTA converts the whole W [M][K] to the I/O type once into
-// shared memory ([row][k], padded to KP), then loops over tiles of XP_T
-// positions of one of the nb batch elements, streaming the input in K slices of XP_K:
-// the next slice is loaded into registers while the current one feeds the
-// mma (8 warps; warp w owns rows 16 (w % 4) .. +16 and positions 64 (w / 4)
-// .. +64).  Slices are stored transposed, [position][k], two k per 32-bit
-// word, so every fragment register is one aligned 32-bit shared load (the
-// PTX ISA's m16n8k16 fragment layouts).  The accumulators leave through a
-// shared [row][position] fp32 tile so that the global stores run along
-// positions.
-constexpr int XP_T = 128, XP_K = 128, XP_KP = XP_K + 8, XP_OP = XP_T + 8;
+// persistent CTA of 16 warps converts the whole W [M][K] to the I/O type
+// once into shared memory ([row][k], padded to KP), then loops over tiles
+// of XP_T positions of one of the nb batch elements, streaming the input
+// in K slices of XP_K: the next slice is loaded into registers (64 KB in
+// flight per CTA) while the current one feeds the mma (warp w owns rows
+// 16 (w % 4) .. +16 and positions 32 (w / 4) .. +32).  Slices are stored
+// transposed, [position][k], two k per 32-bit word, so every fragment
+// register is one aligned 32-bit shared load (the PTX ISA's m16n8k16
+// fragment layouts).  The accumulators leave through a shared [row]
+// [position] fp32 tile so that the global stores run along positions.
+constexpr int XP_T = 128, XP_K = 256, XP_KP = XP_K + 8, XP_OP = XP_T + 8, XP_NT = 512;
 __host__ __device__ constexpr int xproj_kp(int K) { return ((K + XP_K - 1) / XP_K) * XP_K + 8; }
 inline size_t xproj_smem_bytes(int K, size_t esize) {
-    return (64 * (size_t)xproj_kp(K) + 2 * (size_t)XP_T * XP_KP) * esize;
+    return (64 * (size_t)xproj_kp(K) + (size_t)XP_T * XP_KP) * esize;
 }
 template <typename IO>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(XP_NT, 1)
 xproj_mma_kernel(const float *__restrict__ W, const IO *__restrict__ in, int M, int K, int L,
                  int nb, ProjOut out) {
     extern __shared__ __align__(16) unsigned char xp_smem[];
+    constexpr int NW = XP_NT / 32;                              // 16 warps
+    constexpr int PAIRS = XP_T * XP_K / 2 / XP_NT;              // k-pairs per thread per slice
     const int KP = xproj_kp(K);
     IO *sW = (IO *)xp_smem;                                    // [64][KP]
-    IO *sI = sW + 64 * KP;                                     // [2][XP_T][XP_KP]
-    float *sO = (float *)sI;                                   // [64][XP_OP], after the slices
+    IO *sI = sW + 64 * KP;                                     // [XP_T][XP_KP]
+    float *sO = (float *)sI;                                   // [64][XP_OP], after a tile
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, tg = lane & 3;
-    const int wm = (warp % 4) * 16, wn = (warp / 4) * 64;
-    // slice loader: unit q = j * 8 + warp covers 16 positions x 2 k-pairs;
-    // a lane loads the k-pair (2 kp, 2 kp + 1) of one position
-    const int ld_tt = lane & 15, ld_kp = lane >> 4;
-    // W row by row (warp w takes rows w, w + 8, ...; lanes along k, four
+    const int wm = (warp % 4) * 16, wn = (warp / 4) * 32;
+    // W row by row (warp w takes rows w, w + NW, ...; lanes along k, four
     // loads in flight each), zero past column K and past row M
-    for (int m = warp; m < 64; m += 8) {
+    for (int m = warp; m < 64; m += NW) {
         IO *dst = sW + m * KP;
         const float *src = W + (long long)m * K;
         for (int k0 = 0; k0 < KP; k0 += 128) {
@@ -340,42 +354,37 @@ xproj_mma_kernel(const float *__restrict__ W, const IO *__restrict__ in, int M, 
             }
         }
     }
+    // slice loader: unit q = j * NW + warp covers 16 positions x 2 k-pairs;
+    // a lane loads the k-pair (2 kp, 2 kp + 1) of one position
+    const int ld_tt = (warp % 8) * 16 + (lane & 15);
+    const int ld_kp0 = (warp / 8) * 2 + (lane >> 4);            // + 4 j
     const int tpb = (L + XP_T - 1) / XP_T, ntiles = tpb * nb;
     const int nk = (K + XP_K - 1) / XP_K;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
         const int b = tile / tpb, t0 = (tile % tpb) * XP_T;
-        const IO *inb = in + (long long)b * K * L;
-        unsigned short reg[2 * (XP_T * XP_K / 2) / 256];       // 64 halves per thread
+        const int t = t0 + ld_tt;
+        const IO *src = in + (long long)b * K * L + t;
+        unsigned reg[PAIRS];
         auto load = [&](int k0) {
 #pragma unroll
-            for (int j = 0; j < (XP_T * XP_K / 2) / (16 * 2 * 8); ++j) {
-                const int q = j * 8 + warp, tt = (q % 8) * 16 + ld_tt;
-                const int k = k0 + 2 * ((q / 8) * 2 + ld_kp), t = t0 + tt;
-                const bool tin = t < L;
+            for (int j = 0; j < PAIRS; ++j) {
+                const int k = k0 + 2 * (ld_kp0 + 4 * j);
                 const IO z = from_f32<IO>(0.f);
-                const IO v0 = (tin && k < K) ? inb[(long long)k * L + t] : z;
-                const IO v1 = (tin && k + 1 < K) ? inb[(long long)(k + 1) * L + t] : z;
-                reg[2 * j] = *(const unsigned short *)&v0;
-                reg[2 * j + 1] = *(const unsigned short *)&v1;
+                const IO v0 = (t < L && k < K) ? src[(long long)k * L] : z;
+                const IO v1 = (t < L && k + 1 < K) ? src[(long long)(k + 1) * L] : z;
+                reg[j] = (unsigned)*(const unsigned short *)&v0 |
+                         ((unsigned)*(const unsigned short *)&v1 << 16);
             }
         };
-        auto store = [&](int buf) {
-            unsigned *dst = (unsigned *)(sI + buf * XP_T * XP_KP);
-#pragma unroll
-            for (int j = 0; j < (XP_T * XP_K / 2) / (16 * 2 * 8); ++j) {
-                const int q = j * 8 + warp, tt = (q % 8) * 16 + ld_tt;
-                const int kp = (q / 8) * 2 + ld_kp;
-                dst[tt * (XP_KP / 2) + kp] = (unsigned)reg[2 * j] | ((unsigned)reg[2 * j + 1] << 16);
-            }
-        };
-        float acc[8][4] = {};
+        float acc[4][4] = {};
         load(0);
         for (int ki = 0; ki < nk; ++ki) {
-            const int buf = ki & 1;
-            store(buf);
+            if (ki > 0) __syncthreads();                        // slice ki-1 fully read
+            unsigned *dst = (unsigned *)sI;
+#pragma unroll
+            for (int j = 0; j < PAIRS; ++j) dst[ld_tt * (XP_KP / 2) + ld_kp0 + 4 * j] = reg[j];
             __syncthreads();
             if (ki + 1 < nk) load((ki + 1) * XP_K);               // in flight during the mma
-            const IO *bI = sI + buf * XP_T * XP_KP;
 #pragma unroll
             for (int ks = 0; ks < XP_K; ks += 16) {
                 const int kw = ki * XP_K + ks;
@@ -385,36 +394,36 @@ xproj_mma_kernel(const float *__restrict__ W, const IO *__restrict__ in, int M, 
                 a[2] = *(const unsigned *)&sW[(wm + g) * KP + kw + 2 * tg + 8];
                 a[3] = *(const unsigned *)&sW[(wm + g + 8) * KP + kw + 2 * tg + 8];
 #pragma unroll
-                for (int nt = 0; nt < 8; ++nt) {
+                for (int nt = 0; nt < 4; ++nt) {
                     unsigned bf[2];
-                    const IO *col = bI + (wn + nt * 8 + g) * XP_KP + ks + 2 * tg;
+                    const IO *col = sI + (wn + nt * 8 + g) * XP_KP + ks + 2 * tg;
                     bf[0] = *(const unsigned *)col;
                     bf[1] = *(const unsigned *)(col + 8);
                     mma16816<IO>(acc[nt], a, bf);
                 }
             }
         }
-        __syncthreads();                                        // slices dead: reuse as sO
+        __syncthreads();                                        // slice dead: reuse as sO
         // c0, c1: row g, positions 2tg, 2tg+1; c2, c3: row g + 8
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
             for (int half = 0; half < 2; ++half)
                 *(float2 *)&sO[(wm + g + 8 * half) * XP_OP + wn + nt * 8 + 2 * tg] =
                     make_float2(acc[nt][2 * half], acc[nt][2 * half + 1]);
         __syncthreads();
-        for (int i = tid; i < M * XP_T; i += 256) {
-            const int m = i / XP_T, tt = i % XP_T, t = t0 + tt;
-            if (t >= L) continue;
+        for (int i = tid; i < M * XP_T; i += XP_NT) {
+            const int m = i / XP_T, tt = i % XP_T, tp = t0 + tt;
+            if (tp >= L) continue;
             int s = 0;
             while (m >= out.r[s + 1]) ++s;
             const int rows = out.r[s + 1] - out.r[s], mr = m - out.r[s];
-            const long long o = ((long long)b * rows + mr) * L + t;
+            const long long o = ((long long)b * rows + mr) * L + tp;
             const float v = sO[m * XP_OP + tt];
             if (out.f32[s]) ((float *)out.dst[s])[o] = v;
             else ((IO *)out.dst[s])[o] = from_f32<IO>(v);
         }
-        __syncthreads();                                        // sO dead before the next slices
+        __syncthreads();                                        // sO dead before the next slice
     }
 }
 

@@ -56,7 +56,7 @@ ssm_status x_proj(int B, int M, int K, int L, const float *W, const IO *u, ssm::
                 return SSM_ERR_CUDA;
             const long long tiles = (long long)B * ((L + XP_T - 1) / XP_T);
             const int grid = (int)std::min<long long>(tiles, sm_count());
-            xproj_mma_kernel<IO><<<grid, 256, smem, st>>>(W, u, M, K, L, B, o);
+            xproj_mma_kernel<IO><<<grid, XP_NT, smem, st>>>(W, u, M, K, L, B, o);
             return last_error();
         }
     }
