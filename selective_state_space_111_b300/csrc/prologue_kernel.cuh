@@ -1,7 +1,7 @@
 // prologue_kernel.cuh -- the steps that feed the scan (sm_103a), one direction:
 //   u  = silu(causal depthwise conv1d(x) + bias)      (conv_silu_kernel)
 //   [dt_low; B; C] = W_x @ u                          (xproj_mma_kernel / proj_*)
-//   dt = W_dt @ dt_low                                (dtproj_kernel / proj_*)
+//   dt = W_dt @ dt_low                     (dtproj_tc_kernel / dtproj_kernel / proj_*)
 // as in "Vision Mamba实战" section 2.1 and "从Transformer到Mamba" section 2.1
 // (conv1d, x_proj = Linear(d_inner -> dt_rank + 2 d_state), dt_proj =
 // Linear(dt_rank -> d_inner)) and "VMamba的SS2D模块详解" section 3.1 (the
@@ -19,31 +19,32 @@ namespace pro {
 
 // u[b][d][t] = silu(bias[d] + sum_k w[d][k] * xs[t - (K-1) + k]), xs = x or
 // x reversed in time, zero before the start.  A CTA covers CONV_T positions
-// of one row: it stages xs over them plus the K - 1 halo in shared memory
-// (coalesced reads, in reverse order for reverse = 1), then each thread
-// makes CONV_T / 256 outputs, consecutive threads on consecutive positions.
-// KT = K fixed at compile time (the usual 4 taps), or 0 for any K <= 8.
-constexpr int CONV_T = 2048;
+// of one channel: it stages xs over them plus the K - 1 halo in shared
+// memory (coalesced reads, in reverse order for reverse = 1, every load in
+// flight before the stores), then each thread makes CONV_T / 256 outputs,
+// consecutive threads on consecutive positions.  KT = K fixed at compile
+// time (the usual 4 taps), or 0 for any K <= 8.
+constexpr int CONV_T = 2048, CONV_S = CONV_T + 8, CONV_V = (CONV_S + 255) / 256;
 template <typename IO, int KT>
 __global__ void __launch_bounds__(256)
 conv_silu_kernel(const IO *__restrict__ x, const float *__restrict__ w,
                  const float *__restrict__ bias, IO *__restrict__ u, int D, int L, int K,
                  int reverse) {
-    __shared__ float sx[CONV_T + 8];            // sx[i] = xs[t0 - (K-1) + i], K <= 8
+    __shared__ float sx[CONV_S];                // sx[i] = xs[t0 - (K-1) + i], K <= 8
     const int t0 = blockIdx.x * CONV_T;
     const int d = blockIdx.y, b = blockIdx.z;
     const long long row = ((long long)b * D + d) * L;
     const int n_in = min(CONV_T, L - t0) + K - 1;
-    float v[(CONV_T + 8 + 255) / 256];          // every load in flight before the stores
+    float v[CONV_V];
 #pragma unroll
-    for (int j = 0; j < (CONV_T + 8 + 255) / 256; ++j) {
+    for (int j = 0; j < CONV_V; ++j) {
         const int i = j * 256 + threadIdx.x, ts = t0 - (K - 1) + i;
         v[j] = (i < n_in && ts >= 0) ? to_f32(x[row + (reverse ? L - 1 - ts : ts)]) : 0.f;
     }
 #pragma unroll
-    for (int j = 0; j < (CONV_T + 8 + 255) / 256; ++j) {
+    for (int j = 0; j < CONV_V; ++j) {
         const int i = j * 256 + threadIdx.x;
-        if (i < CONV_T + 8) sx[i] = v[j];
+        if (i < CONV_S) sx[i] = v[j];
     }
     constexpr int KM = KT > 0 ? KT : 8;
     float wk[KM];
@@ -302,6 +303,103 @@ dtproj_kernel(const float *__restrict__ W, const float *__restrict__ in, int M, 
                 if (t_b < L) o[L + t_b] = from_f32<IO>(b1);
             }
         }
+    }
+}
+
+// dt_proj on tensor cores for 16-bit I/O: out[b][m][t] = sum_r W[m][r]
+// in[b][r][t] with W and the fp32 dt_low rounded to tf32 (10-bit mantissa,
+// below the 16-bit output's own rounding) and fp32 accumulation, mma.sync
+// m16n8k8.  A CTA takes DTC_T positions and DTC_RB rows: it stages the
+// input tile [RP][DTC_T] and its W rows [DTC_RB][RP] (zero-padded to RP)
+// once, then for each block of 64 rows runs the mma (warp w: rows
+// 16 (w % 4) .. +16, positions 64 (w / 4) .. +64) and writes the block
+// through a shared fp32 tile so that the global stores run along
+// positions.
+constexpr int DTC_T = 128, DTC_RB = 128, DTC_OS = DTC_T + 8;
+__device__ __forceinline__ unsigned to_tf32(float f) {
+    unsigned r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(f));
+    return r;
+}
+__device__ __forceinline__ void mma1688_tf32(float (&c)[4], const unsigned (&a)[4],
+                                             const unsigned (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+template <int RP> constexpr size_t dtproj_tc_smem_bytes() {
+    return ((size_t)DTC_RB * (RP + 4) + (size_t)RP * DTC_OS + 64 * (size_t)DTC_OS) * 4;
+}
+template <typename IO, int RP>
+__global__ void __launch_bounds__(256)
+dtproj_tc_kernel(const float *__restrict__ W, const float *__restrict__ in, int M, int R, int L,
+                 IO *__restrict__ out) {
+    constexpr int WS = RP + 4, IS = DTC_OS;     // word strides: conflict-free fragment loads
+    extern __shared__ __align__(16) unsigned char dtc_smem[];
+    unsigned *sW = (unsigned *)dtc_smem;        // [DTC_RB][WS]
+    unsigned *sI = sW + DTC_RB * WS;            // [RP][IS]
+    float *sO = (float *)(sI + RP * IS);        // [64][DTC_OS]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, tg = lane & 3;
+    const int wm = (warp % 4) * 16, wn = (warp / 4) * 64;
+    const int t0 = blockIdx.x * DTC_T, b = blockIdx.z;
+    const int m_lo = blockIdx.y * DTC_RB, mc = min(DTC_RB, M - m_lo);
+    {
+        float iv[RP * DTC_T / 256], wv[RP * DTC_RB / 256];
+#pragma unroll
+        for (int j = 0; j < RP * DTC_T / 256; ++j) {
+            const int i = j * 256 + tid, r = i / DTC_T, tt = i % DTC_T, t = t0 + tt;
+            iv[j] = (r < R && t < L) ? in[((long long)b * R + r) * L + t] : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < RP * DTC_RB / 256; ++j) {
+            const int i = j * 256 + tid, mm = i / RP, r = i % RP;
+            wv[j] = (mm < mc && r < R) ? W[(long long)(m_lo + mm) * R + r] : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < RP * DTC_T / 256; ++j) {
+            const int i = j * 256 + tid;
+            sI[(i / DTC_T) * IS + i % DTC_T] = to_tf32(iv[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < RP * DTC_RB / 256; ++j) {
+            const int i = j * 256 + tid;
+            sW[(i / RP) * WS + i % RP] = to_tf32(wv[j]);
+        }
+    }
+    __syncthreads();
+    for (int mb = 0; mb < mc; mb += 64) {
+        float acc[8][4] = {};
+#pragma unroll
+        for (int ks = 0; ks < RP; ks += 8) {
+            // A (row): a0 (g, tg), a1 (g + 8, tg), a2 (g, tg + 4), a3 (g + 8, tg + 4)
+            const unsigned *wr = sW + (mb + wm + g) * WS + ks + tg;
+            const unsigned a[4] = {wr[0], wr[8 * WS], wr[4], wr[8 * WS + 4]};
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+                // B (col): b0 (k = tg, n = g), b1 (k = tg + 4, n = g)
+                const unsigned *col = sI + (ks + tg) * IS + wn + nt * 8 + g;
+                const unsigned bf[2] = {col[0], col[4 * IS]};
+                mma1688_tf32(acc[nt], a, bf);
+            }
+        }
+        // c0, c1: row g, positions 2tg, 2tg+1; c2, c3: row g + 8
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int half = 0; half < 2; ++half)
+                *(float2 *)&sO[(wm + g + 8 * half) * DTC_OS + wn + nt * 8 + 2 * tg] =
+                    make_float2(acc[nt][2 * half], acc[nt][2 * half + 1]);
+        __syncthreads();
+        const int rows = min(64, mc - mb);
+        for (int i = tid; i < rows * DTC_T; i += 256) {
+            const int m = i / DTC_T, tt = i % DTC_T, t = t0 + tt;
+            if (t < L)
+                out[((long long)b * M + m_lo + mb + m) * L + t] = from_f32<IO>(sO[m * DTC_OS + tt]);
+        }
+        __syncthreads();
     }
 }
 

@@ -67,35 +67,48 @@ ssm_status x_proj(int B, int M, int K, int L, const float *W, const IO *u, ssm::
 // dt_proj: the register-blocked FMA kernel for dt_rank <= 32, else the
 // generic tiled one
 template <typename IO, int RP>
-void launch_dtproj(int B, int D, int R, int L, const float *W, const float *dt_low, IO *dt,
-                   cudaStream_t st) {
+ssm_status launch_dtproj(int B, int D, int R, int L, const float *W, const float *dt_low, IO *dt,
+                         cudaStream_t st) {
     using namespace ssm::pro;
-    const int tiles = (L + DTP_T - 1) / DTP_T;
-    const long long want = 4LL * sm_count();
-    int split = (int)std::min<long long>((want + (long long)tiles * B - 1) / ((long long)tiles * B),
-                                         (D + DTP_MC - 1) / DTP_MC);
-    split = std::max(split, 1);
-    dtproj_kernel<IO, RP><<<dim3(tiles, split, B), 256, 0, st>>>(W, dt_low, D, R, L, dt);
+    if constexpr (sizeof(IO) == 2) {
+        // tensor cores (tf32 operands, fp32 accumulation)
+        constexpr size_t smem = dtproj_tc_smem_bytes<RP>();
+        if (cudaFuncSetAttribute(dtproj_tc_kernel<IO, RP>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess)
+            return SSM_ERR_CUDA;
+        dtproj_tc_kernel<IO, RP><<<dim3((L + DTC_T - 1) / DTC_T, (D + DTC_RB - 1) / DTC_RB, B),
+                                   256, smem, st>>>(W, dt_low, D, R, L, dt);
+    } else {
+        // fp32 I/O: fp32 FMA
+        const int tiles = (L + DTP_T - 1) / DTP_T;
+        const long long want = 4LL * sm_count();
+        int split = (int)std::min<long long>(
+            (want + (long long)tiles * B - 1) / ((long long)tiles * B), (D + DTP_MC - 1) / DTP_MC);
+        split = std::max(split, 1);
+        dtproj_kernel<IO, RP><<<dim3(tiles, split, B), 256, 0, st>>>(W, dt_low, D, R, L, dt);
+    }
+    return last_error();
 }
 
+// dt_proj: the register-blocked kernels for dt_rank <= 32, else the generic
+// tiled one
 template <typename IO>
 ssm_status dt_proj(int B, int D, int R, int L, const float *W, const float *dt_low, IO *dt,
                    cudaStream_t st) {
     using namespace ssm::pro;
-    if (R <= 8) launch_dtproj<IO, 8>(B, D, R, L, W, dt_low, dt, st);
-    else if (R <= 16) launch_dtproj<IO, 16>(B, D, R, L, W, dt_low, dt, st);
-    else if (R <= 24) launch_dtproj<IO, 24>(B, D, R, L, W, dt_low, dt, st);
-    else if (R <= 32) launch_dtproj<IO, 32>(B, D, R, L, W, dt_low, dt, st);
-    else {
-        ProjOut o{};
-        o.dst[0] = dt;
-        o.r[0] = 0;
-        o.r[1] = D;
-        o.r[2] = D;
-        o.r[3] = D;
-        launch_proj<float, IO>(dim3((L + BN - 1) / BN, (D + BM - 1) / BM, B), W, dt_low, D, R, L,
-                               o, st);
-    }
+    if (R <= 8) return launch_dtproj<IO, 8>(B, D, R, L, W, dt_low, dt, st);
+    if (R <= 16) return launch_dtproj<IO, 16>(B, D, R, L, W, dt_low, dt, st);
+    if (R <= 24) return launch_dtproj<IO, 24>(B, D, R, L, W, dt_low, dt, st);
+    if (R <= 32) return launch_dtproj<IO, 32>(B, D, R, L, W, dt_low, dt, st);
+    ProjOut o{};
+    o.dst[0] = dt;
+    o.r[0] = 0;
+    o.r[1] = D;
+    o.r[2] = D;
+    o.r[3] = D;
+    launch_proj<float, IO>(dim3((L + BN - 1) / BN, (D + BM - 1) / BM, B), W, dt_low, D, R, L, o,
+                           st);
     return last_error();
 }
 

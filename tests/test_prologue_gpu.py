@@ -6,7 +6,9 @@ scan) against the oracle chain.
 Tolerances: u element by element, |gpu - ref| <= tol * (1 + |ref|); dt, B,
 C (dot products of length D or R over u, which the GPU reads in the I/O
 dtype) against their own scale, max|gpu - ref| <= tol2 * (1 + max|ref|);
-tol = 1e-4 / 1e-2 and tol2 = 5e-4 / 2e-2 for fp32 / bf16 I/O.
+tol = 1e-4 / 1e-2 / 5e-3 and tol2 = 5e-4 / 2e-2 / 1e-2 for fp32 / bf16 / fp16
+I/O (the 16-bit paths round u, dt, B, C to the I/O type and run dt_proj
+on tf32 operands).
 """
 import numpy as np
 import pytest
@@ -17,9 +19,9 @@ from oracle import prologue as pro
 
 pytestmark = pytest.mark.gpu
 
-DT = {"f32": torch.float32, "bf16": torch.bfloat16}
-TOL = {"f32": 1e-4, "bf16": 1e-2}
-TOL2 = {"f32": 5e-4, "bf16": 2e-2}
+DT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+TOL = {"f32": 1e-4, "bf16": 1e-2, "f16": 5e-3}
+TOL2 = {"f32": 5e-4, "bf16": 2e-2, "f16": 1e-2}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -52,7 +54,7 @@ SHAPES = [(1, 5, 7, 4, 2, 4), (2, 70, 130, 16, 5, 4), (1, 33, 65, 32, 3, 3),
           (2, 64, 64, 16, 24, 4), (1, 1, 1, 16, 1, 4)]
 
 
-@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("io", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("reverse", [False, True])
 @pytest.mark.parametrize("shape", SHAPES)
 def test_prologue_matches_oracle(io, reverse, shape):
