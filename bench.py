@@ -473,51 +473,74 @@ def measure_prologue(ssm, spec, dev, stream, steps):
 
 
 # ---------------------------------------------------------------- CPU oracle
+class OracleSampler:
+    """The fp64 oracle, as it stands, over bounded samples of whole rows of
+    the workload, rows spread over the host cores (one oracle call per row).
+    The inputs are built once; each sample() is one timed run.  prefix = P
+    (single / v1 / v2) makes a sample unit the first P positions of a row
+    instead of the whole row, for runs of many short steps."""
+
+    SEQ_KEYS = ("u", "u_b", "delta", "delta_b", "z", "B", "C", "B_b", "C_b")
+
+    def __init__(self, spec, name, prefix=None):
+        import numpy as np
+
+        import oracle
+        from selective_state_space_111_b300.synth import make_inputs, seed_for
+        sys.path.insert(0, os.path.join(ROOT, "tests"))
+        from cases import row_slice, run_oracle
+        self.spec, self.name = spec, name
+        self.prefix = prefix if (prefix and spec.op != "ss2d" and prefix < spec.seq_len) else None
+        self.row_slice, self.run_oracle = row_slice, run_oracle
+        self.cores = len(os.sched_getaffinity(0))
+        self.t = make_inputs(spec, seed_for(name))
+        oracle.build()
+        rng = np.random.default_rng(0)
+        self.rows = [(int(rng.integers(spec.B)), int(rng.integers(spec.D)))
+                     for _ in range(100000)]
+
+    def sample(self, seconds):
+        spec, cores = self.spec, self.cores
+        done = [0]
+        lock = threading.Lock()
+        deadline = time.perf_counter() + seconds
+
+        def worker(k):
+            i = k
+            while i < len(self.rows):
+                b, d = self.rows[i]
+                ts = self.row_slice(spec, self.t, b, d)
+                if self.prefix:
+                    for key in self.SEQ_KEYS:
+                        if ts.get(key) is not None:
+                            ts[key] = ts[key][..., :self.prefix].contiguous()
+                self.run_oracle(spec, ts)
+                with lock:
+                    done[0] += 1
+                i += cores
+                if time.perf_counter() >= deadline:
+                    break
+
+        t0 = time.perf_counter()
+        th = [threading.Thread(target=worker, args=(k,)) for k in range(cores)]
+        for x in th:
+            x.start()
+        for x in th:
+            x.join()
+        el = time.perf_counter() - t0
+        frac = (self.prefix / spec.seq_len) if self.prefix else 1.0
+        per_row_updates = spec.updates() / (spec.B * spec.D) * frac
+        per_row_bytes = spec.algorithmic_bytes() / (spec.B * spec.D) * frac
+        ups = done[0] * per_row_updates / el
+        unit = ("row prefixes of %d positions" % self.prefix) if self.prefix else "whole rows"
+        return {"value": round(done[0] * per_row_bytes / el / 1e9, 6), "unit": "GB/s",
+                "elem_updates_per_s": float("%.4g" % ups), "cores": cores, "kind": "oracle",
+                "sample": "%d %s (all directions, L=%d) of %s in %.2f s, one per oracle call, "
+                          "%d threads" % (done[0], unit, spec.seq_len, self.name, el, cores)}
+
+
 def cpu_baseline(spec, name, seconds):
-    """The fp64 oracle, as it stands, over a bounded sample of whole rows of
-    the workload, rows spread over the host cores (one oracle call per row)."""
-    import numpy as np
-
-    import oracle
-    from selective_state_space_111_b300.synth import make_inputs, seed_for
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from cases import row_slice, run_oracle
-
-    cores = len(os.sched_getaffinity(0))
-    t = make_inputs(spec, seed_for(name))
-    oracle.build()
-    rng = np.random.default_rng(0)
-    rows = [(int(rng.integers(spec.B)), int(rng.integers(spec.D))) for _ in range(100000)]
-    slices = {}
-    done = [0]
-    lock = threading.Lock()
-    deadline = time.perf_counter() + seconds
-
-    def worker(k):
-        i = k
-        while time.perf_counter() < deadline and i < len(rows):
-            b, d = rows[i]
-            run_oracle(spec, row_slice(spec, t, b, d))
-            with lock:
-                done[0] += 1
-            i += cores
-        return
-
-    t0 = time.perf_counter()
-    th = [threading.Thread(target=worker, args=(k,)) for k in range(cores)]
-    for x in th:
-        x.start()
-    for x in th:
-        x.join()
-    el = time.perf_counter() - t0
-    per_row_updates = spec.updates() // (spec.B * spec.D)
-    per_row_bytes = spec.algorithmic_bytes() / (spec.B * spec.D)
-    ups = done[0] * per_row_updates / el
-    del slices
-    return {"value": round(done[0] * per_row_bytes / el / 1e9, 6), "unit": "GB/s",
-            "elem_updates_per_s": float("%.4g" % ups), "cores": cores, "kind": "oracle",
-            "sample": "%d whole rows (both directions, L=%d) of %s in %.1f s, one row per "
-                      "oracle call, %d threads" % (done[0], spec.seq_len, name, el, cores)}
+    return OracleSampler(spec, name).sample(seconds)
 
 
 def run_reference(args):
@@ -526,11 +549,15 @@ def run_reference(args):
         return
     from selective_state_space_111_b300.synth import WORKLOADS
     spec = WORKLOADS[args.workload]
-    vals = []
     t_all = time.perf_counter()
-    per_step = max(2.0, args.cpu_seconds / max(1, args.steps))
+    nsteps = args.warmup + args.steps
+    sampler = OracleSampler(spec, args.workload, prefix=512 if nsteps > 100 else None)
+    # every step is a bounded sample: the whole run stays near a minute of
+    # CPU time whatever --steps and --warmup are (at least one row per core)
+    per_step = max(0.02, min(2.0, 60.0 / max(1, nsteps)))
+    vals = []
     for i in range(args.warmup + args.steps):
-        cb = cpu_baseline(spec, args.workload, per_step if i >= args.warmup else 1.0)
+        cb = sampler.sample(per_step)
         if i >= args.warmup:
             vals.append(cb)
     v = statistics.mean(c["value"] for c in vals)
@@ -544,7 +571,9 @@ def run_reference(args):
             "config": {"workload": args.workload, "op": spec.op, "batch": spec.B,
                        "d_inner": spec.D, "d_state": spec.N, "seq_len": spec.seq_len},
             "cpu_baseline": {"value": v, "unit": "GB/s", "kind": "oracle",
-                             "cores": vals[0]["cores"], "sample": vals[-1]["sample"]},
+                             "cores": vals[0]["cores"],
+                             "sample": "%d steps of ~%.2f s each; last: %s"
+                                       % (args.steps, per_step, vals[-1]["sample"])},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "wall_s": round(time.perf_counter() - t_all, 1)}
     print(json.dumps(line), flush=True)
