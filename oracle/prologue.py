@@ -23,6 +23,22 @@ flipped sequence):
                               scan applies softplus)
 
 Outputs are in scan order for reverse=True (element t is position L-1-t).
+
+SS2D's prologue ("VMamba的SS2D模块详解" section 2.1: conv2d, the depthwise
+convolution on the [B, D, H, W] map, d_conv 3 in its parameter table;
+section 2.2: the four scan orders; section 3.1: one x_proj and one
+dt_proj per scan direction):
+
+  conv2d[h][w] = bias[d] + sum_{i,j} w[d][i][j] * x[h+i-P][w+j-P], P =
+            (Kc-1)/2, zero outside the map (output the size of the input;
+            the pages print conv2d without its arguments -- reading:
+            depthwise, "same" zero padding, odd Kc)
+  u       = silu(conv2d), or conv2d itself with silu=False (the pages'
+            simplified SS2D forward shows no activation after conv2d; the
+            1D path applies SiLU)
+  xs_k    = u flattened in direction k's scan order (k = 0 row-major,
+            1 column-major, 2 and 3 their reversals)
+  proj_k  = W_x[k] @ xs_k, split as in the 1D case; dt_k = W_dt[k] @ dt_low_k
 """
 from __future__ import annotations
 
@@ -69,3 +85,45 @@ def prologue(x, conv_w, conv_b, W_x, W_dt, dt_rank, d_state, reverse=False):
     dt_low, Bm, Cm = proj[:, :R], proj[:, R:R + N], proj[:, R + N:R + 2 * N]
     dt = np.einsum("dr,brl->bdl", _f64(W_dt), dt_low)
     return u, dt, Bm, Cm
+
+
+def depthwise_conv2d(x, w, b=None):
+    """[B, D, H, W] pre-activation of the depthwise 2D convolution with zero
+    padding (Kc-1)/2 on every side: out[h][w] = b + sum_{i,j} w[i][j] *
+    x[h + i - P][w + j - P] (a correlation, as a Conv2d layer computes)."""
+    x = _f64(x)
+    w = _f64(w)
+    Bn, Dn, H, W = x.shape
+    Kc = w.shape[-1]
+    P = (Kc - 1) // 2
+    xp = np.zeros((Bn, Dn, H + 2 * P, W + 2 * P))
+    xp[..., P:P + H, P:P + W] = x
+    out = np.zeros((Bn, Dn, H, W))
+    if b is not None:
+        out += _f64(b)[None, :, None, None]
+    for i in range(Kc):
+        for j in range(Kc):
+            out += w[None, :, i, j, None, None] * xp[..., i:i + H, j:j + W]
+    return out
+
+
+def ss2d_prologue(x, conv_w, conv_b, W_x, W_dt, dt_rank, d_state, silu_act=True):
+    """Returns (u [B,D,H,W], delta [B,4,D,L], Bm [B,4,N,L], Cm [B,4,N,L]),
+    the per-direction tensors in each direction's scan order (L = H W)."""
+    from . import cross_scan_index
+    c = depthwise_conv2d(x, conv_w, conv_b)
+    u = silu(c) if silu_act else c
+    Bn, Dn, H, W = u.shape
+    L = H * W
+    uf = u.reshape(Bn, Dn, L)
+    W_x, W_dt = _f64(W_x), _f64(W_dt)
+    R, N = dt_rank, d_state
+    delta = np.empty((Bn, 4, Dn, L))
+    Bm = np.empty((Bn, 4, N, L))
+    Cm = np.empty((Bn, 4, N, L))
+    for k in range(4):
+        xs = uf[..., cross_scan_index(H, W, k)]
+        proj = np.einsum("md,bdl->bml", W_x[k], xs)
+        Bm[:, k], Cm[:, k] = proj[:, R:R + N], proj[:, R + N:R + 2 * N]
+        delta[:, k] = np.einsum("dr,brl->bdl", W_dt[k], proj[:, :R])
+    return u, delta, Bm, Cm

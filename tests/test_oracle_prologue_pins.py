@@ -1,7 +1,10 @@
 """Pins of the prologue oracle (CPU): the causal convolution against
 numpy's convolve row by row and its impulse response and causality; the
 projections against selection and one-hot inputs (a transposed operand or
-a wrong split row fails them)."""
+a wrong split row fails them).  SS2D: the depthwise conv2d against scipy's
+correlate2d and its impulse response; the four directions' sequences
+against numpy flatten / transpose / flip; the per-direction projections
+with selection weights."""
 import numpy as np
 import pytest
 
@@ -69,3 +72,95 @@ def test_reverse_is_the_prologue_of_the_flipped_input():
     b = pro.prologue(x[..., ::-1].copy(), cw, cb, W_x, W_dt, R, N, reverse=False)
     for p, q in zip(a, b):
         np.testing.assert_allclose(p, q, rtol=1e-14, atol=1e-14)
+
+
+# ---------------------------------------------------------------- SS2D
+
+
+@pytest.mark.parametrize("Kc,H,W", [(3, 5, 7), (5, 6, 4), (1, 3, 3), (3, 1, 6)])
+def test_conv2d_matches_scipy_correlate2d(Kc, H, W):
+    from scipy.signal import correlate2d
+    rng = np.random.default_rng(Kc * 100 + H * 10 + W)
+    x = rng.normal(size=(2, 3, H, W))
+    w = rng.normal(size=(3, Kc, Kc))
+    b = rng.normal(size=(3,))
+    got = pro.depthwise_conv2d(x, w, b)
+    for bb in range(2):
+        for d in range(3):
+            ref = correlate2d(x[bb, d], w[d], mode="same", boundary="fill", fillvalue=0) + b[d]
+            np.testing.assert_allclose(got[bb, d], ref, rtol=1e-13, atol=1e-13)
+
+
+def test_conv2d_impulse_response():
+    # a correlation: an impulse at (h0, w0) leaves the kernel rotated by
+    # 180 degrees around it
+    w = np.arange(1.0, 10.0).reshape(1, 3, 3)
+    x = np.zeros((1, 1, 5, 6))
+    x[0, 0, 2, 3] = 1.0
+    y = pro.depthwise_conv2d(x, w)[0, 0]
+    ref = np.zeros((5, 6))
+    ref[1:4, 2:5] = w[0, ::-1, ::-1]
+    np.testing.assert_array_equal(y, ref)
+
+
+def _ss2d_weights(rng, D, R, N):
+    return (rng.normal(size=(4, R + 2 * N, D)), rng.normal(size=(4, D, R)))
+
+
+def test_ss2d_directions_are_flatten_transpose_flip():
+    # B_k row n selects channel n: B_k must be u's channel n in direction
+    # k's order, written independently with numpy
+    rng = np.random.default_rng(5)
+    Bn, D, H, W, R, N = 2, 4, 3, 5, 2, 3
+    x = rng.normal(size=(Bn, D, H, W))
+    cw = rng.normal(size=(D, 3, 3))
+    W_x = np.zeros((4, R + 2 * N, D))
+    for k in range(4):
+        for n in range(N):
+            W_x[k, R + n, (n + k) % D] = 1.0        # B rows: channel (n + k) mod D
+            W_x[k, R + N + n, n] = 2.0              # C rows: twice channel n
+    W_dt = rng.normal(size=(4, D, R))
+    u, delta, Bm, Cm = pro.ss2d_prologue(x, cw, None, W_x, W_dt, R, N)
+    orders = [lambda m: m.reshape(Bn, -1),
+              lambda m: m.transpose(0, 2, 1).reshape(Bn, -1),
+              lambda m: m.reshape(Bn, -1)[:, ::-1],
+              lambda m: m.transpose(0, 2, 1).reshape(Bn, -1)[:, ::-1]]
+    for k in range(4):
+        for n in range(N):
+            np.testing.assert_array_equal(Bm[:, k, n], orders[k](u[:, (n + k) % D]))
+            np.testing.assert_array_equal(Cm[:, k, n], 2.0 * orders[k](u[:, n]))
+
+
+def test_ss2d_dt_projection_per_direction():
+    # dt_low rows select channels; W_dt[k] one-hot: delta_k[d] = dt_low
+    # row r(d, k), which is channel c(r, k) in direction k's order
+    rng = np.random.default_rng(6)
+    Bn, D, H, W, R, N = 1, 3, 4, 2, 2, 1
+    x = rng.normal(size=(Bn, D, H, W))
+    cw = rng.normal(size=(D, 3, 3))
+    cb = rng.normal(size=(D,))
+    W_x = np.zeros((4, R + 2 * N, D))
+    W_dt = np.zeros((4, D, R))
+    for k in range(4):
+        for r in range(R):
+            W_x[k, r, (r + k) % D] = 1.0
+        for d in range(D):
+            W_dt[k, d, (d + k) % R] = 3.0
+    u, delta, _, _ = pro.ss2d_prologue(x, cw, cb, W_x, W_dt, R, N)
+    orders = [lambda m: m.reshape(-1), lambda m: m.T.reshape(-1),
+              lambda m: m.reshape(-1)[::-1], lambda m: m.T.reshape(-1)[::-1]]
+    for k in range(4):
+        for d in range(D):
+            r = (d + k) % R
+            np.testing.assert_array_equal(delta[0, k, d], 3.0 * orders[k](u[0, (r + k) % D]))
+
+
+def test_ss2d_silu_flag_and_activation():
+    rng = np.random.default_rng(7)
+    x = rng.normal(size=(1, 2, 3, 4))
+    cw = rng.normal(size=(2, 3, 3))
+    W_x, W_dt = _ss2d_weights(rng, 2, 1, 2)
+    u0, *_ = pro.ss2d_prologue(x, cw, None, W_x, W_dt, 1, 2, silu_act=False)
+    u1, *_ = pro.ss2d_prologue(x, cw, None, W_x, W_dt, 1, 2, silu_act=True)
+    np.testing.assert_allclose(u0, pro.depthwise_conv2d(x, cw), rtol=0, atol=0)
+    np.testing.assert_allclose(u1, u0 / (1.0 + np.exp(-u0)), rtol=1e-15, atol=0)
