@@ -304,7 +304,7 @@ def run_ours(args):
     if not args.no_backward:
         bwd = measure_backward(ssm, spec, g, t, dev, stream, max(3, min(args.steps, 20)))
     pro = None
-    if not args.no_prologue and spec.op != "ss2d":
+    if not args.no_prologue:
         pro = measure_prologue(ssm, spec, dev, stream, max(3, min(args.steps, 20)))
 
     if rank == 0:
@@ -433,11 +433,14 @@ def measure_backward(ssm, spec, g, t, dev, stream, steps):
 def measure_prologue(ssm, spec, dev, stream, steps):
     """Time the prologue that feeds the scan (conv1d + SiLU, x_proj, dt_proj)
     on an input of the workload's shape: both branches for v2 (the backward
-    one on the flipped input), one for v1 (shared weights) and single.
+    one on the flipped input), one for v1 (shared weights) and single; for
+    SS2D the 3x3 conv2d + SiLU and the four directions' projections.
     dt_rank = ceil(d_model / 16) with d_model = D / 2; weights synthetic."""
     import torch
     B, D, L, N = spec.B, spec.D, spec.seq_len, spec.N
     R, K = -(-D // 32), 4
+    if spec.op == "ss2d":
+        return measure_ss2d_prologue(ssm, spec, dev, stream, steps, R)
     dirs = 2 if spec.op == "v2" else 1
     gen = torch.Generator().manual_seed(4321)
     io = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[spec.io]
@@ -468,6 +471,42 @@ def measure_prologue(ssm, spec, dev, stream, steps):
     nbytes = dirs * e * (3 * B * D * L + 2 * B * N * L)
     flops = dirs * 2.0 * B * L * ((R + 2 * N) * D + D * R)
     return {"ms_per_call": round(ms, 4), "directions": dirs, "dt_rank": R, "d_conv": K,
+            "value": round(nbytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "tflops": flops / (ms * 1e-3) / 1e12}
+
+
+def measure_ss2d_prologue(ssm, spec, dev, stream, steps, R, Kc=3):
+    import torch
+    B, D, H, W, N = spec.B, spec.D, spec.H, spec.W, spec.N
+    L = H * W
+    gen = torch.Generator().manual_seed(4322)
+    io = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[spec.io]
+    x = torch.randn(B, D, H, W, generator=gen).to(dtype=io, device=dev)
+    w = dict(conv_w=((torch.rand(D, Kc, Kc, generator=gen) - 0.5) / Kc).to(dev),
+             conv_b=(torch.rand(D, generator=gen) - 0.5).to(dev),
+             W_x=(torch.randn(4, R + 2 * N, D, generator=gen) * D ** -0.5).to(dev),
+             W_dt=(torch.randn(4, D, R, generator=gen) * R ** -0.5).to(dev))
+    ws = torch.empty(B * R * L * 4, dtype=torch.uint8, device=dev)
+
+    def once():
+        ssm.ss2d_prologue_fwd(x, w["conv_w"], w["conv_b"], w["W_x"], w["W_dt"], R, N,
+                              workspace=ws)
+
+    for _ in range(3):
+        once()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        once()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    e = x.element_size()
+    # x read; u written [B,D,H,W]; delta [B,4,D,L], B and C [B,4,N,L] written
+    nbytes = e * (2 * B * D * L + 4 * B * D * L + 2 * 4 * B * N * L)
+    flops = 2.0 * B * L * (Kc * Kc * D + 4 * ((R + 2 * N) * D + D * R))
+    return {"ms_per_call": round(ms, 4), "directions": 4, "dt_rank": R, "d_conv": Kc,
             "value": round(nbytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
             "tflops": flops / (ms * 1e-3) / 1e12}
 

@@ -382,8 +382,13 @@ SSM_API size_t ssm_bwd_workspace_bytes(ssm_op op, ssm_dtype dt, int B, int D,
  * Outputs (I/O dtype, device, caller-owned): u, delta [B, D, L]; Bm, Cm
  * [B, N, L] -- the layouts the scan calls take.  N <= 32, 1 <= K <= 8.
  * workspace: ssm_prologue_workspace_bytes(B, L, R) bytes, 16-byte aligned
- * (the fp32 dt_low).  State of the art for the projections would be tensor
- * cores; these kernels use fp32 FMA (outputs rounded to the I/O dtype).
+ * (the fp32 dt_low).  Arithmetic: fp32 accumulation throughout; with
+ * 16-bit I/O x_proj runs on tensor cores with u and W_x in the I/O type and
+ * dt_proj on tf32 operands; with fp32 I/O both are fp32 FMA.  Outputs are
+ * rounded to the I/O dtype.  Errors: SSM_ERR_INVALID_ARG for a bad dtype,
+ * size or pointer; SSM_ERR_UNSUPPORTED for N > 32, K > 8 or sizes past the
+ * 32-bit index range; SSM_ERR_WORKSPACE for a short or misaligned
+ * workspace; SSM_ERR_CUDA for a launch error.  Asynchronous on `stream`.
  * ------------------------------------------------------------------------- */
 SSM_API ssm_status mamba_prologue_fwd(ssm_dtype dt, int B, int D, int L, int N,
                          int R, int K, const void *x, const float *conv_w,
@@ -392,6 +397,36 @@ SSM_API ssm_status mamba_prologue_fwd(ssm_dtype dt, int B, int D, int L, int N,
                          void *Bm, void *Cm, void *workspace, size_t ws_bytes,
                          ssm_stream_t stream);
 SSM_API size_t ssm_prologue_workspace_bytes(int B, int L, int R);
+
+/* ---------------------------------------------------------------------------
+ * SS2D prologue ("VMamba的SS2D模块详解" section 2.1: conv2d on the [B, D, H, W]
+ * map before the core; section 2.2: the four scan orders; section 3.1: one
+ * x_proj and one dt_proj per scan direction):
+ *   u = act(conv_b[d] + sum_{i,j} conv_w[d][i][j] x[h+i-P][w+j-P])
+ *       depthwise, P = (Kc-1)/2, zero outside the map, act = SiLU when
+ *       silu_act != 0, else identity (the pages' simplified SS2D forward
+ *       shows no activation after conv2d; the 1D path applies SiLU)
+ *   for k = 0..3 (row-major, column-major, and their reversals):
+ *     [dt_low; B_k; C_k] = W_x[k] xs_k,  delta_k = W_dt[k] dt_low
+ *   where xs_k is u read in direction k's scan order.
+ * x, u [B, D, H, W]; conv_w [D, Kc, Kc], conv_b [D] or NULL (fp32);
+ * W_x [4, R + 2N, D], W_dt [4, D, R] (fp32).  Outputs, each direction in
+ * its own scan order -- exactly the layouts ss2d_scan_fwd takes (u as its
+ * x): delta [B, 4, D, H*W], Bm, Cm [B, 4, N, H*W].  All tensors contiguous,
+ * device, caller-owned; I/O tensors in `dt`.  Kc odd, <= 7; N <= 32.
+ * workspace: ss2d_prologue_workspace_bytes(B, H, W, R) bytes, 16-byte
+ * aligned (one direction's fp32 dt_low at a time).  Arithmetic and errors
+ * as mamba_prologue_fwd (SSM_ERR_INVALID_ARG also for an even Kc;
+ * SSM_ERR_UNSUPPORTED also when the conv's staging of (rows + Kc - 1) x
+ * (W + Kc - 1) fp32 values passes 200 KB: W above about 17000 for Kc = 3).
+ * ------------------------------------------------------------------------- */
+SSM_API ssm_status ss2d_prologue_fwd(ssm_dtype dt, int B, int D, int H, int W,
+                         int N, int R, int Kc, const void *x,
+                         const float *conv_w, const float *conv_b,
+                         const float *W_x, const float *W_dt, int silu_act,
+                         void *u, void *delta, void *Bm, void *Cm,
+                         void *workspace, size_t ws_bytes, ssm_stream_t stream);
+SSM_API size_t ss2d_prologue_workspace_bytes(int B, int H, int W, int R);
 
 /*
  * Tuning override for the two-branch kernels (v1, v2 and both SS2D passes).

@@ -66,6 +66,10 @@ _lib.mamba_prologue_fwd.argtypes = [_i] * 7 + [_vp] * 5 + [_i] + [_vp] * 5 + [_s
 _lib.mamba_prologue_fwd.restype = _i
 _lib.ssm_prologue_workspace_bytes.argtypes = [_i, _i, _i]
 _lib.ssm_prologue_workspace_bytes.restype = _sz
+_lib.ss2d_prologue_fwd.argtypes = [_i] * 8 + [_vp] * 5 + [_i] + [_vp] * 5 + [_sz, _vp]
+_lib.ss2d_prologue_fwd.restype = _i
+_lib.ss2d_prologue_workspace_bytes.argtypes = [_i, _i, _i, _i]
+_lib.ss2d_prologue_workspace_bytes.restype = _sz
 _lib.ssm_bwd_workspace_bytes.argtypes = [_i] * 8
 _lib.ssm_bwd_workspace_bytes.restype = _sz
 for _fn in (_lib.selective_scan_fwd, _lib.bimamba_scan_fwd_v1, _lib.bimamba_scan_fwd_v2,
@@ -511,4 +515,35 @@ def mamba_prologue_fwd(x, conv_w, conv_b, W_x, W_dt, dt_rank, d_state, reverse=F
                                    workspace.data_ptr(),
                                    workspace.numel() * workspace.element_size(),
                                    _stream(stream)), "mamba_prologue_fwd")
+    return u, delta, Bm, Cm
+
+
+def ss2d_prologue_fwd(x, conv_w, conv_b, W_x, W_dt, dt_rank, d_state, silu_act=True,
+                      workspace=None, stream=None):
+    """SS2D's conv2d (+ SiLU) and its four directions' x_proj and dt_proj.
+    x: [Bt, Dc, H, W] (I/O dtype); conv_w [Dc, Kc, Kc], conv_b [Dc] (or
+    None), W_x [4, R + 2N, Dc], W_dt [4, Dc, R] fp32.  Returns (u, delta, B,
+    C): u [Bt, Dc, H, W]; delta [Bt, 4, Dc, H*W], B, C [Bt, 4, N, H*W], each
+    direction in its own scan order (what ss2d_scan_fwd takes, u as its x)."""
+    io = x.dtype
+    Bt, Dc, H, W = x.shape
+    R, N = int(dt_rank), int(d_state)
+    Kc = conv_w.shape[-1]
+    L = H * W
+    u = torch.empty_like(x)
+    delta = torch.empty((Bt, 4, Dc, L), dtype=io, device=x.device)
+    Bm = torch.empty((Bt, 4, N, L), dtype=io, device=x.device)
+    Cm = torch.empty((Bt, 4, N, L), dtype=io, device=x.device)
+    need = int(_lib.ss2d_prologue_workspace_bytes(Bt, H, W, R))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    _check(_lib.ss2d_prologue_fwd(_dtype_code(x), Bt, Dc, H, W, N, R, Kc, _io(x, io, "x"),
+                                  _par(conv_w, "conv_w", (Dc, Kc, Kc)),
+                                  _par(conv_b, "conv_b", (Dc,), True),
+                                  _par(W_x, "W_x", (4, R + 2 * N, Dc)),
+                                  _par(W_dt, "W_dt", (4, Dc, R)), int(bool(silu_act)),
+                                  u.data_ptr(), delta.data_ptr(), Bm.data_ptr(), Cm.data_ptr(),
+                                  workspace.data_ptr(),
+                                  workspace.numel() * workspace.element_size(),
+                                  _stream(stream)), "ss2d_prologue_fwd")
     return u, delta, Bm, Cm

@@ -64,14 +64,100 @@ conv_silu_kernel(const IO *__restrict__ x, const float *__restrict__ w,
     }
 }
 
+// SS2D's conv2d ("VMamba的SS2D模块详解" section 2.1): u[b][d][h][w] =
+// act(bias[d] + sum_{i,j} w[d][i][j] x[b][d][h+i-P][w+j-P]), P = (Kc-1)/2,
+// zero outside the map, act = SiLU or identity.  A CTA covers RB rows of
+// one channel's map: it stages rows h0-P .. h0+RB+P-1 (zero-padded by P
+// columns on each side) in shared memory, warp by warp along the rows
+// (coalesced), then warp r makes output rows r, r + 8, ... lane by lane
+// along w.  KC = Kc fixed at compile time (3), or 0 for any odd Kc <= 7.
+template <typename IO, int KC>
+__global__ void __launch_bounds__(256)
+conv2d_act_kernel(const IO *__restrict__ x, const float *__restrict__ w,
+                  const float *__restrict__ bias, IO *__restrict__ u, int D, int H, int W,
+                  int Kc, int RB, int act) {
+    extern __shared__ __align__(16) float c2_smem[];        // [RB + 2P][W + 2P]
+    const int P = (Kc - 1) / 2, WP = W + 2 * P;
+    const int h0 = blockIdx.x * RB, d = blockIdx.y, b = blockIdx.z;
+    const int rb = min(RB, H - h0);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const IO *xm = x + ((long long)b * D + d) * H * W;
+    for (int r = warp; r < rb + 2 * P; r += 8) {
+        const int h = h0 - P + r;
+        const bool hin = h >= 0 && h < H;
+        float *dst = c2_smem + r * WP;
+        for (int c0 = lane; c0 < WP; c0 += 128) {
+            float v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int c = c0 + 32 * q, ww = c - P;
+                v[q] = (hin && c < WP && ww >= 0 && ww < W) ? to_f32(xm[(long long)h * W + ww])
+                                                            : 0.f;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (c0 + 32 * q < WP) dst[c0 + 32 * q] = v[q];
+        }
+    }
+    constexpr int KM = KC > 0 ? KC : 7;
+    float wk[KM * KM];
+#pragma unroll
+    for (int i = 0; i < KM; ++i)
+#pragma unroll
+        for (int j = 0; j < KM; ++j)
+            wk[i * KM + j] = (KC > 0 || (i < Kc && j < Kc)) ? w[(d * Kc + i) * Kc + j] : 0.f;
+    const float bv = bias ? bias[d] : 0.f;
+    __syncthreads();
+    IO *um = u + ((long long)b * D + d) * H * W;
+    for (int r = warp; r < rb; r += 8) {
+        for (int c = lane; c < W; c += 32) {
+            float acc = bv;
+#pragma unroll
+            for (int i = 0; i < KM; ++i)
+#pragma unroll
+                for (int j = 0; j < KM; ++j)
+                    if (KC > 0 || (i < Kc && j < Kc))
+                        acc = fmaf(wk[i * KM + j], c2_smem[(r + i) * WP + c + j], acc);
+            um[(long long)(h0 + r) * W + c] = from_f32<IO>(act ? silu_f<IO>(acc) : acc);
+        }
+    }
+}
+
 // Output rows [0, M) of one projection go to up to three destinations:
-// rows [r0, r1) -> dst0, [r1, r2) -> dst1, [r2, M) -> dst2, each [B][rows][L]
-// in its own dtype (fp32 for the internal dt_low, the I/O dtype otherwise).
+// rows [r0, r1) -> dst0, [r1, r2) -> dst1, [r2, M) -> dst2, each
+// [B][rows][L] with batch stride bstride[s] elements, in its own dtype (fp32
+// for the internal dt_low, the I/O dtype otherwise).  order >= 0 (SS2D):
+// the input positions are an H x W map in row-major order and each output
+// goes to its position in scan direction `order` ("VMamba的SS2D模块详解"
+// section 2.2: 0 row-major, 1 column-major, 2 and 3 their reversals).
 struct ProjOut {
     void *dst[3];
     int f32[3];        // 1: fp32 destination
     int r[4];          // row boundaries: r[0] = 0 <= r[1] <= r[2] <= r[3] = M
+    long long bstride[3];
+    int order, H, W;   // order < 0: positions are stored as they are
 };
+
+// scan position of map position p (row-major) in direction k
+__device__ __forceinline__ int scan_pos(int k, int p, int H, int W) {
+    if (k <= 0) return p;
+    const int L = H * W;
+    if (k == 2) return L - 1 - p;
+    const int h = p / W, w = p - h * W, t = w * H + h;    // column-major
+    return k == 1 ? t : L - 1 - t;
+}
+
+// stores output row m, position t of batch element b
+template <typename IO>
+__device__ __forceinline__ void proj_store(const ProjOut &out, int b, int m, int t, int L,
+                                           float v) {
+    int s = 0;
+    while (m >= out.r[s + 1]) ++s;
+    const long long o = (long long)b * out.bstride[s] + (long long)(m - out.r[s]) * L +
+                        scan_pos(out.order, t, out.H, out.W);
+    if (out.f32[s]) ((float *)out.dst[s])[o] = v;
+    else ((IO *)out.dst[s])[o] = from_f32<IO>(v);
+}
 
 constexpr int BM = 64, BN = 64, BK = 16;
 
@@ -123,16 +209,10 @@ proj_kernel(const float *__restrict__ W, const IN *__restrict__ in, int M, int K
     for (int i = 0; i < 4; ++i) {
         const int m = m0 + ty * 4 + i;
         if (m >= M) continue;
-        int s = 0;
-        while (m >= out.r[s + 1]) ++s;
-        const int rows = out.r[s + 1] - out.r[s], mr = m - out.r[s];
-        const long long o = ((long long)b * rows + mr) * L;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int t = t0 + tx * 4 + j;
-            if (t >= L) continue;
-            if (out.f32[s]) ((float *)out.dst[s])[o + t] = acc[i][j];
-            else ((IO *)out.dst[s])[o + t] = from_f32<IO>(acc[i][j]);
+            if (t < L) proj_store<IO>(out, b, m, t, L, acc[i][j]);
         }
     }
 }
@@ -216,25 +296,18 @@ proj_mma_kernel(const float *__restrict__ W, const IN *__restrict__ in, int M, i
     for (int half = 0; half < 2; ++half) {
         const int m = m0 + wm + g + 8 * half;
         if (m >= M) continue;
-        int s = 0;
-        while (m >= out.r[s + 1]) ++s;
-        const int rows = out.r[s + 1] - out.r[s], mr = m - out.r[s];
-        const long long o = ((long long)b * rows + mr) * L;
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const int t = t0 + wn + nt * 8 + 2 * tg + j;
-                if (t >= L) continue;
-                const float v = acc[nt][2 * half + j];
-                if (out.f32[s]) ((float *)out.dst[s])[o + t] = v;
-                else ((IO *)out.dst[s])[o + t] = from_f32<IO>(v);
+                if (t < L) proj_store<IO>(out, b, m, t, L, acc[nt][2 * half + j]);
             }
     }
 }
 
 // dt_proj with a short inner dimension (R = dt_rank <= RP, RP in {8, 16, 24,
-// 32}): out[b][m][t] = sum_r W[m][r] in[b][r][t].  A CTA takes DTP_T
+// 32}): out[b][m][t] = sum_r W[m][r] in[b][r][t] (out's batch stride ob).  A CTA takes DTP_T
 // positions (two per thread, DTP_T / 2 apart, their R inputs in registers)
 // and rows [m_lo, m_hi) in chunks of 128 staged in shared memory (zero-
 // padded to RP, read back as broadcast float4); stores are coalesced along
@@ -244,7 +317,7 @@ constexpr int DTP_T = 512, DTP_MC = 128;
 template <typename IO, int RP>
 __global__ void __launch_bounds__(256, 2)
 dtproj_kernel(const float *__restrict__ W, const float *__restrict__ in, int M, int R, int L,
-              IO *__restrict__ out) {
+              IO *__restrict__ out, long long ob) {
     __shared__ __align__(16) float sW[DTP_MC * RP];
     const int b = blockIdx.z;
     const int t_a = blockIdx.x * DTP_T + threadIdx.x, t_b = t_a + DTP_T / 2;
@@ -295,7 +368,7 @@ dtproj_kernel(const float *__restrict__ W, const float *__restrict__ in, int M, 
                 a1 = fmaf(x1.w, va[4 * q + 3], a1);
                 b1 = fmaf(x1.w, vb[4 * q + 3], b1);
             }
-            IO *o = out + ((long long)b * M + m0 + mm) * L;
+            IO *o = out + (long long)b * ob + (long long)(m0 + mm) * L;
             if (t_a < L) o[t_a] = from_f32<IO>(a0);
             if (t_b < L) o[t_b] = from_f32<IO>(b0);
             if (two) {
@@ -307,7 +380,7 @@ dtproj_kernel(const float *__restrict__ W, const float *__restrict__ in, int M, 
 }
 
 // dt_proj on tensor cores for 16-bit I/O: out[b][m][t] = sum_r W[m][r]
-// in[b][r][t] with W and the fp32 dt_low rounded to tf32 (10-bit mantissa,
+// in[b][r][t] (out's batch stride ob) with W and the fp32 dt_low rounded to tf32 (10-bit mantissa,
 // below the 16-bit output's own rounding) and fp32 accumulation, mma.sync
 // m16n8k8.  A CTA takes DTC_T positions and DTC_RB rows: it stages the
 // input tile [RP][DTC_T] and its W rows [DTC_RB][RP] (zero-padded to RP)
@@ -335,7 +408,7 @@ template <int RP> constexpr size_t dtproj_tc_smem_bytes() {
 template <typename IO, int RP>
 __global__ void __launch_bounds__(256)
 dtproj_tc_kernel(const float *__restrict__ W, const float *__restrict__ in, int M, int R, int L,
-                 IO *__restrict__ out) {
+                 IO *__restrict__ out, long long ob) {
     constexpr int WS = RP + 4, IS = DTC_OS;     // word strides: conflict-free fragment loads
     extern __shared__ __align__(16) unsigned char dtc_smem[];
     unsigned *sW = (unsigned *)dtc_smem;        // [DTC_RB][WS]
@@ -397,7 +470,8 @@ dtproj_tc_kernel(const float *__restrict__ W, const float *__restrict__ in, int 
         for (int i = tid; i < rows * DTC_T; i += 256) {
             const int m = i / DTC_T, tt = i % DTC_T, t = t0 + tt;
             if (t < L)
-                out[((long long)b * M + m_lo + mb + m) * L + t] = from_f32<IO>(sO[m * DTC_OS + tt]);
+                out[(long long)b * ob + (long long)(m_lo + mb + m) * L + t] =
+                    from_f32<IO>(sO[m * DTC_OS + tt]);
         }
         __syncthreads();
     }
@@ -512,14 +586,7 @@ xproj_mma_kernel(const float *__restrict__ W, const IO *__restrict__ in, int M, 
         __syncthreads();
         for (int i = tid; i < M * XP_T; i += XP_NT) {
             const int m = i / XP_T, tt = i % XP_T, tp = t0 + tt;
-            if (tp >= L) continue;
-            int s = 0;
-            while (m >= out.r[s + 1]) ++s;
-            const int rows = out.r[s + 1] - out.r[s], mr = m - out.r[s];
-            const long long o = ((long long)b * rows + mr) * L + tp;
-            const float v = sO[m * XP_OP + tt];
-            if (out.f32[s]) ((float *)out.dst[s])[o] = v;
-            else ((IO *)out.dst[s])[o] = from_f32<IO>(v);
+            if (tp < L) proj_store<IO>(out, b, m, tp, L, sO[m * XP_OP + tt]);
         }
         __syncthreads();                                        // sO dead before the next slice
     }

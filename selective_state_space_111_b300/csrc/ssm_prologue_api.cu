@@ -1,6 +1,7 @@
-// ssm_prologue_api.cu -- mamba_prologue_fwd (include/ssm_scan.h): one
-// direction's conv1d + SiLU, x_proj split and dt_proj, producing the
-// scan's inputs u, dt, B, C in the scan's own layouts.
+// ssm_prologue_api.cu -- mamba_prologue_fwd and ss2d_prologue_fwd
+// (include/ssm_scan.h): one direction's conv1d + SiLU, x_proj split and
+// dt_proj, or SS2D's conv2d (+ SiLU) and its four directions' x_proj and
+// dt_proj, producing the scan's inputs in the scan's own layouts.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -68,7 +69,7 @@ ssm_status x_proj(int B, int M, int K, int L, const float *W, const IO *u, ssm::
 // generic tiled one
 template <typename IO, int RP>
 ssm_status launch_dtproj(int B, int D, int R, int L, const float *W, const float *dt_low, IO *dt,
-                         cudaStream_t st) {
+                         long long ob, cudaStream_t st) {
     using namespace ssm::pro;
     if constexpr (sizeof(IO) == 2) {
         // tensor cores (tf32 operands, fp32 accumulation)
@@ -78,7 +79,7 @@ ssm_status launch_dtproj(int B, int D, int R, int L, const float *W, const float
                                  (int)smem) != cudaSuccess)
             return SSM_ERR_CUDA;
         dtproj_tc_kernel<IO, RP><<<dim3((L + DTC_T - 1) / DTC_T, (D + DTC_RB - 1) / DTC_RB, B),
-                                   256, smem, st>>>(W, dt_low, D, R, L, dt);
+                                   256, smem, st>>>(W, dt_low, D, R, L, dt, ob);
     } else {
         // fp32 I/O: fp32 FMA
         const int tiles = (L + DTP_T - 1) / DTP_T;
@@ -86,27 +87,29 @@ ssm_status launch_dtproj(int B, int D, int R, int L, const float *W, const float
         int split = (int)std::min<long long>(
             (want + (long long)tiles * B - 1) / ((long long)tiles * B), (D + DTP_MC - 1) / DTP_MC);
         split = std::max(split, 1);
-        dtproj_kernel<IO, RP><<<dim3(tiles, split, B), 256, 0, st>>>(W, dt_low, D, R, L, dt);
+        dtproj_kernel<IO, RP><<<dim3(tiles, split, B), 256, 0, st>>>(W, dt_low, D, R, L, dt, ob);
     }
     return last_error();
 }
 
 // dt_proj: the register-blocked kernels for dt_rank <= 32, else the generic
-// tiled one
+// tiled one; ob = batch stride of dt in elements
 template <typename IO>
 ssm_status dt_proj(int B, int D, int R, int L, const float *W, const float *dt_low, IO *dt,
-                   cudaStream_t st) {
+                   long long ob, cudaStream_t st) {
     using namespace ssm::pro;
-    if (R <= 8) return launch_dtproj<IO, 8>(B, D, R, L, W, dt_low, dt, st);
-    if (R <= 16) return launch_dtproj<IO, 16>(B, D, R, L, W, dt_low, dt, st);
-    if (R <= 24) return launch_dtproj<IO, 24>(B, D, R, L, W, dt_low, dt, st);
-    if (R <= 32) return launch_dtproj<IO, 32>(B, D, R, L, W, dt_low, dt, st);
+    if (R <= 8) return launch_dtproj<IO, 8>(B, D, R, L, W, dt_low, dt, ob, st);
+    if (R <= 16) return launch_dtproj<IO, 16>(B, D, R, L, W, dt_low, dt, ob, st);
+    if (R <= 24) return launch_dtproj<IO, 24>(B, D, R, L, W, dt_low, dt, ob, st);
+    if (R <= 32) return launch_dtproj<IO, 32>(B, D, R, L, W, dt_low, dt, ob, st);
     ProjOut o{};
     o.dst[0] = dt;
     o.r[0] = 0;
     o.r[1] = D;
     o.r[2] = D;
     o.r[3] = D;
+    o.bstride[0] = ob;
+    o.order = -1;
     launch_proj<float, IO>(dim3((L + BN - 1) / BN, (D + BM - 1) / BM, B), W, dt_low, D, R, L, o,
                            st);
     return last_error();
@@ -136,9 +139,71 @@ ssm_status run(int B, int D, int L, int N, int R, int K, const void *x, const fl
     o1.r[1] = R;
     o1.r[2] = R + N;
     o1.r[3] = M;
+    o1.bstride[0] = (long long)R * L;
+    o1.bstride[1] = o1.bstride[2] = (long long)N * L;
+    o1.order = -1;
     if (x_proj<IO>(B, M, D, L, W_x, (const IO *)u, o1, st) != SSM_OK) return SSM_ERR_CUDA;
     // dt_proj: all D rows -> dt
-    return dt_proj<IO>(B, D, R, L, W_dt, dt_low, (IO *)dt, st);
+    return dt_proj<IO>(B, D, R, L, W_dt, dt_low, (IO *)dt, (long long)D * L, st);
+}
+
+// rows of the map per conv2d CTA (about 2048 outputs) and its shared bytes
+int c2_rows(int H, int W) { return std::max(1, std::min(H, 2048 / std::max(W, 1))); }
+size_t c2_smem(int H, int W, int Kc) {
+    const int P = (Kc - 1) / 2;
+    return (size_t)(c2_rows(H, W) + 2 * P) * (W + 2 * P) * sizeof(float);
+}
+
+// SS2D: conv2d (+ SiLU), then for each of the four directions x_proj
+// (outputs scattered to that direction's scan order) and dt_proj
+template <typename IO>
+ssm_status run_ss2d(int B, int D, int H, int W, int N, int R, int Kc, const void *x,
+                    const float *conv_w, const float *conv_b, const float *W_x,
+                    const float *W_dt, int act, void *u, void *delta, void *Bm, void *Cm,
+                    float *dt_low, cudaStream_t st) {
+    using namespace ssm::pro;
+    const int L = H * W, RB = c2_rows(H, W);
+    const size_t smem = c2_smem(H, W, Kc);
+    const dim3 cgrid((H + RB - 1) / RB, D, B);
+    if (Kc == 3) {
+        if (cudaFuncSetAttribute(conv2d_act_kernel<IO, 3>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess)
+            return SSM_ERR_CUDA;
+        conv2d_act_kernel<IO, 3><<<cgrid, 256, smem, st>>>((const IO *)x, conv_w, conv_b, (IO *)u,
+                                                          D, H, W, Kc, RB, act);
+    } else {
+        if (cudaFuncSetAttribute(conv2d_act_kernel<IO, 0>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess)
+            return SSM_ERR_CUDA;
+        conv2d_act_kernel<IO, 0><<<cgrid, 256, smem, st>>>((const IO *)x, conv_w, conv_b, (IO *)u,
+                                                          D, H, W, Kc, RB, act);
+    }
+    if (last_error() != SSM_OK) return SSM_ERR_CUDA;
+    const int M = R + 2 * N;
+    for (int k = 0; k < 4; ++k) {
+        ProjOut o{};
+        o.dst[0] = dt_low;
+        o.dst[1] = (IO *)Bm + (long long)k * N * L;
+        o.dst[2] = (IO *)Cm + (long long)k * N * L;
+        o.f32[0] = 1;
+        o.r[0] = 0;
+        o.r[1] = R;
+        o.r[2] = R + N;
+        o.r[3] = M;
+        o.bstride[0] = (long long)R * L;
+        o.bstride[1] = o.bstride[2] = 4LL * N * L;
+        o.order = k;
+        o.H = H;
+        o.W = W;
+        if (x_proj<IO>(B, M, D, L, W_x + (long long)k * M * D, (const IO *)u, o, st) != SSM_OK)
+            return SSM_ERR_CUDA;
+        if (dt_proj<IO>(B, D, R, L, W_dt + (long long)k * D * R, dt_low,
+                        (IO *)delta + (long long)k * D * L, 4LL * D * L, st) != SSM_OK)
+            return SSM_ERR_CUDA;
+    }
+    return SSM_OK;
 }
 
 }  // namespace
@@ -177,6 +242,44 @@ ssm_status mamba_prologue_fwd(ssm_dtype dt, int B, int D, int L, int N, int R, i
                            Cm, dt_low, st);
     return run<__nv_bfloat16>(B, D, L, N, R, K, x, conv_w, conv_b, W_x, W_dt, reverse, u, delta,
                               Bm, Cm, dt_low, st);
+}
+
+size_t ss2d_prologue_workspace_bytes(int B, int H, int W, int R) {
+    if (B < 0 || H < 0 || W < 0 || R <= 0) return (size_t)-1;
+    return (size_t)B * R * H * W * sizeof(float);
+}
+
+ssm_status ss2d_prologue_fwd(ssm_dtype dt, int B, int D, int H, int W, int N, int R, int Kc,
+                             const void *x, const float *conv_w, const float *conv_b,
+                             const float *W_x, const float *W_dt, int silu_act, void *u,
+                             void *delta, void *Bm, void *Cm, void *workspace, size_t ws_bytes,
+                             ssm_stream_t stream) {
+    if (dt != SSM_F32 && dt != SSM_BF16 && dt != SSM_F16) return SSM_ERR_INVALID_ARG;
+    if (B < 0 || D < 0 || H < 0 || W < 0 || N <= 0 || R <= 0 || Kc <= 0 || Kc % 2 == 0)
+        return SSM_ERR_INVALID_ARG;
+    if (N > 32 || Kc > 7 || B > 65535 || D > 65535) return SSM_ERR_UNSUPPORTED;
+    const long long L = (long long)H * W;
+    if ((long long)D * L > 0x7fffffffLL || (long long)(R + 2 * N) * L > 0x7fffffffLL ||
+        4LL * D * L > 0x7fffffffLL || c2_smem(H, W, Kc) > 200 * 1024)
+        return SSM_ERR_UNSUPPORTED;
+    if (!io_ok(dt, x) || !f32_ok(conv_w) || !opt_f32(conv_b) || !f32_ok(W_x) || !f32_ok(W_dt) ||
+        !io_ok(dt, u) || !io_ok(dt, delta) || !io_ok(dt, Bm) || !io_ok(dt, Cm))
+        return SSM_ERR_INVALID_ARG;
+    if ((long long)B * D * L == 0) return SSM_OK;
+    if (workspace == nullptr || ws_bytes < ss2d_prologue_workspace_bytes(B, H, W, R) ||
+        !aligned(workspace, 16))
+        return SSM_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    float *dt_low = (float *)workspace;
+    const int act = silu_act ? 1 : 0;
+    if (dt == SSM_F32)
+        return run_ss2d<float>(B, D, H, W, N, R, Kc, x, conv_w, conv_b, W_x, W_dt, act, u, delta,
+                               Bm, Cm, dt_low, st);
+    if (dt == SSM_F16)
+        return run_ss2d<__half>(B, D, H, W, N, R, Kc, x, conv_w, conv_b, W_x, W_dt, act, u, delta,
+                                Bm, Cm, dt_low, st);
+    return run_ss2d<__nv_bfloat16>(B, D, H, W, N, R, Kc, x, conv_w, conv_b, W_x, W_dt, act, u,
+                                   delta, Bm, Cm, dt_low, st);
 }
 
 }  // extern "C"

@@ -140,3 +140,39 @@ def test_bwd_invalid_arguments_are_rejected_before_launch(lib):
     st = lib.ss2d_scan_bwd(1, 1, 1, 2, 2, 16, 3, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None,
                            1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, None, 0, None)
     assert st == 2
+
+
+def prologue(lib, *, dt=1, B=1, D=2, L=8, N=16, R=2, K=4, x=FAKE, ws=None, wsb=0):
+    return lib.mamba_prologue_fwd(dt, B, D, L, N, R, K, x, FAKE, None, FAKE, FAKE, 0, FAKE,
+                                  FAKE, FAKE, FAKE, ws, wsb, None)
+
+
+def ss2d_prologue(lib, *, dt=1, B=1, D=2, H=3, W=4, N=16, R=2, Kc=3, x=FAKE, ws=None, wsb=0):
+    return lib.ss2d_prologue_fwd(dt, B, D, H, W, N, R, Kc, x, FAKE, None, FAKE, FAKE, 1, FAKE,
+                                 FAKE, FAKE, FAKE, ws, wsb, None)
+
+
+def test_prologue_arguments_are_rejected_before_launch(lib):
+    assert prologue(lib, K=9) == 2                  # more than 8 taps
+    assert prologue(lib, N=33) == 2
+    assert prologue(lib, R=0) == 1
+    assert prologue(lib, x=None) == 1
+    assert prologue(lib, x=FAKE + 1) == 1
+    assert prologue(lib) == 4                       # no workspace
+    assert prologue(lib, ws=FAKE, wsb=2 * 8 * 4 - 1) == 4
+    assert prologue(lib, B=0) == 0                  # empty: nothing to launch
+    assert lib.ssm_prologue_workspace_bytes(3, 10, 5) == 3 * 5 * 10 * 4
+
+
+def test_ss2d_prologue_arguments_are_rejected_before_launch(lib):
+    assert ss2d_prologue(lib, Kc=4) == 1            # even kernel: no centred padding
+    assert ss2d_prologue(lib, Kc=9) == 2            # larger than 7
+    assert ss2d_prologue(lib, N=33) == 2
+    assert ss2d_prologue(lib, W=-1) == 1
+    assert ss2d_prologue(lib, x=None) == 1
+    assert ss2d_prologue(lib, x=FAKE + 1) == 1
+    assert ss2d_prologue(lib, W=40000) == 2         # conv staging over its shared-memory bound
+    assert ss2d_prologue(lib) == 4                  # no workspace
+    assert ss2d_prologue(lib, ws=FAKE, wsb=2 * 12 * 4 - 1) == 4
+    assert ss2d_prologue(lib, H=0) == 0
+    assert lib.ss2d_prologue_workspace_bytes(2, 3, 4, 5) == 2 * 5 * 12 * 4

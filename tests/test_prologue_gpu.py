@@ -113,3 +113,84 @@ def test_v2_inner_path_from_x(io):
                                  bias_b, torch.flip(ub, [-1]), True, 0.5)
     assert seq_err(y, ref_scan) <= TOL[io]              # the scan on what it was given
     assert scale_err(y, ref_chain) <= 2 * TOL2[io]      # the whole path from x
+
+
+# ---------------------------------------------------------------- SS2D
+
+def ss2d_weights(g, D, R, N, Kc):
+    """Seeded SS2D prologue weights (fp32): one x_proj and dt_proj per
+    direction, PyTorch-like init scales."""
+    u = lambda *s, a: (torch.rand(*s, generator=g) * 2 - 1) * a
+    return dict(conv_w=u(D, Kc, Kc, a=1.0 / Kc), conv_b=u(D, a=1.0 / Kc),
+                W_x=torch.randn(4, R + 2 * N, D, generator=g) * D ** -0.5,
+                W_dt=torch.randn(4, D, R, generator=g) * R ** -0.5)
+
+
+# (B, D, H, W, N, R, Kc): non-square maps, one-row and one-column maps,
+# d_state 32 (x_proj past 64 rows: the generic tiled kernel), Kc 1..7
+SS2D_SHAPES = [(1, 5, 4, 6, 16, 2, 3), (2, 70, 9, 13, 16, 5, 3), (1, 33, 7, 5, 32, 3, 5),
+               (2, 64, 16, 16, 16, 6, 3), (1, 1, 1, 1, 16, 1, 3), (1, 8, 3, 40, 16, 4, 7),
+               (1, 9, 50, 1, 16, 2, 1), (1, 16, 130, 3, 16, 24, 3)]
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("shape", SS2D_SHAPES)
+def test_ss2d_prologue_matches_oracle(io, shape):
+    import selective_state_space_111_b300 as ssm
+    B, D, H, W, N, R, Kc = shape
+    act = (H + W) % 2 == 0 or io == "bf16"
+    g = torch.Generator().manual_seed(B * 1000 + D + H * W + Kc)
+    x = torch.randn(B, D, H, W, generator=g).to(DT[io])
+    w = ss2d_weights(g, D, R, N, Kc)
+    wg = {k: v.cuda() for k, v in w.items()}
+    u, delta, Bm, Cm = ssm.ss2d_prologue_fwd(x.cuda(), wg["conv_w"], wg["conv_b"], wg["W_x"],
+                                             wg["W_dt"], R, N, silu_act=act)
+    torch.cuda.synchronize()
+    ru, rdelta, rB, rC = pro.ss2d_prologue(x, w["conv_w"], w["conv_b"], w["W_x"], w["W_dt"], R,
+                                           N, silu_act=act)
+    assert seq_err(u, ru) <= TOL[io]
+    for a, r in ((delta, rdelta), (Bm, rB), (Cm, rC)):
+        assert scale_err(a, r) <= TOL2[io], scale_err(a, r)
+
+
+def test_ss2d_prologue_without_activation_and_bias():
+    import selective_state_space_111_b300 as ssm
+    B, D, H, W, N, R, Kc = 2, 20, 11, 7, 16, 4, 3
+    g = torch.Generator().manual_seed(91)
+    x = torch.randn(B, D, H, W, generator=g)
+    w = ss2d_weights(g, D, R, N, Kc)
+    wg = {k: v.cuda() for k, v in w.items()}
+    u, delta, Bm, Cm = ssm.ss2d_prologue_fwd(x.cuda(), wg["conv_w"], None, wg["W_x"], wg["W_dt"],
+                                             R, N, silu_act=False)
+    torch.cuda.synchronize()
+    ru, rdelta, rB, rC = pro.ss2d_prologue(x, w["conv_w"], None, w["W_x"], w["W_dt"], R, N,
+                                           silu_act=False)
+    assert seq_err(u, ru) <= TOL["f32"]
+    for a, r in ((delta, rdelta), (Bm, rB), (Cm, rC)):
+        assert scale_err(a, r) <= TOL2["f32"]
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_ss2d_inner_path_from_x(io):
+    # conv2d + the four directions' projections -> ss2d_scan_fwd, against
+    # the oracle chain
+    import selective_state_space_111_b300 as ssm
+    B, D, H, W, N, R, Kc = 2, 24, 9, 11, 16, 3, 3
+    g = torch.Generator().manual_seed(123)
+    x = torch.randn(B, D, H, W, generator=g).to(DT[io])
+    z = torch.randn(B, D, H, W, generator=g).to(DT[io])
+    w = ss2d_weights(g, D, R, N, Kc)
+    A = -torch.arange(1, N + 1, dtype=torch.float32).repeat(4, D, 1)
+    A = A * (1 + 0.1 * torch.rand(4, D, N, generator=g))
+    Dk = torch.rand(4, D, generator=g) + 0.5
+    bias = torch.rand(4, D, generator=g) - 2.0
+    wg = {k: v.cuda() for k, v in w.items()}
+    u, delta, Bm, Cm = ssm.ss2d_prologue_fwd(x.cuda(), wg["conv_w"], wg["conv_b"], wg["W_x"],
+                                             wg["W_dt"], R, N)
+    y = ssm.ss2d_scan_fwd(u, delta, A.cuda(), Bm, Cm, Dk.cuda(), z.cuda(), bias.cuda(), True)
+    torch.cuda.synchronize()
+    ru, rdelta, rB, rC = pro.ss2d_prologue(x, w["conv_w"], w["conv_b"], w["W_x"], w["W_dt"], R, N)
+    ref_chain = oracle.ss2d(ru, rdelta, A, rB, rC, Dk, z, bias, True)
+    ref_scan = oracle.ss2d(u, delta, A, Bm, Cm, Dk, z, bias, True)
+    assert seq_err(y, ref_scan) <= TOL[io]              # the scan on what it was given
+    assert scale_err(y, ref_chain) <= 2 * TOL2[io]      # the whole path from x
