@@ -67,17 +67,22 @@ conv_silu_kernel(const IO *__restrict__ x, const float *__restrict__ w,
 // SS2D's conv2d ("VMamba的SS2D模块详解" section 2.1): u[b][d][h][w] =
 // act(bias[d] + sum_{i,j} w[d][i][j] x[b][d][h+i-P][w+j-P]), P = (Kc-1)/2,
 // zero outside the map, act = SiLU or identity.  A CTA covers RB rows of
-// one channel's map: it stages rows h0-P .. h0+RB+P-1 (zero-padded by P
-// columns on each side) in shared memory, warp by warp along the rows
-// (coalesced), then warp r makes output rows r, r + 8, ... lane by lane
-// along w.  KC = Kc fixed at compile time (3), or 0 for any odd Kc <= 7.
+// one channel's map: it stages rows h0-P .. h0+RB+P-1, zero-padded by P
+// columns on the left and to the row stride WS on the right, in shared
+// memory (warp by warp along the rows: coalesced).  KC = 3 (compile time):
+// a thread makes 4 consecutive outputs of a row from a 3 x 8 window read
+// with six 16-byte shared loads (WS is a multiple of 4 floats); KC = 0
+// (any odd Kc <= 7): warp r makes rows r, r + 8, ... one output per lane.
+__host__ __device__ constexpr int conv2d_ws(int W, int Kc) {
+    return ((W + 3) / 4) * 4 + ((Kc - 1) / 2) * 2 + 4 - (((Kc - 1) / 2) * 2) % 4;
+}
 template <typename IO, int KC>
 __global__ void __launch_bounds__(256)
 conv2d_act_kernel(const IO *__restrict__ x, const float *__restrict__ w,
                   const float *__restrict__ bias, IO *__restrict__ u, int D, int H, int W,
                   int Kc, int RB, int act) {
-    extern __shared__ __align__(16) float c2_smem[];        // [RB + 2P][W + 2P]
-    const int P = (Kc - 1) / 2, WP = W + 2 * P;
+    extern __shared__ __align__(16) float c2_smem[];        // [RB + 2P][WS]
+    const int P = (Kc - 1) / 2, WS = conv2d_ws(W, Kc);
     const int h0 = blockIdx.x * RB, d = blockIdx.y, b = blockIdx.z;
     const int rb = min(RB, H - h0);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -85,18 +90,18 @@ conv2d_act_kernel(const IO *__restrict__ x, const float *__restrict__ w,
     for (int r = warp; r < rb + 2 * P; r += 8) {
         const int h = h0 - P + r;
         const bool hin = h >= 0 && h < H;
-        float *dst = c2_smem + r * WP;
-        for (int c0 = lane; c0 < WP; c0 += 128) {
-            float v[4];
+        const IO *xr = xm + (long long)(hin ? h : 0) * W;
+        float *dst = c2_smem + r * WS;
+        for (int c0 = lane; c0 < WS; c0 += 64) {
+            float v[2];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int c = c0 + 32 * q, ww = c - P;
-                v[q] = (hin && c < WP && ww >= 0 && ww < W) ? to_f32(xm[(long long)h * W + ww])
-                                                            : 0.f;
+            for (int q = 0; q < 2; ++q) {
+                const int ww = c0 + 32 * q - P;
+                v[q] = (hin && ww >= 0 && ww < W) ? to_f32(xr[ww]) : 0.f;
             }
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                if (c0 + 32 * q < WP) dst[c0 + 32 * q] = v[q];
+            for (int q = 0; q < 2; ++q)
+                if (c0 + 32 * q < WS) dst[c0 + 32 * q] = v[q];
         }
     }
     constexpr int KM = KC > 0 ? KC : 7;
@@ -109,16 +114,47 @@ conv2d_act_kernel(const IO *__restrict__ x, const float *__restrict__ w,
     const float bv = bias ? bias[d] : 0.f;
     __syncthreads();
     IO *um = u + ((long long)b * D + d) * H * W;
-    for (int r = warp; r < rb; r += 8) {
-        for (int c = lane; c < W; c += 32) {
-            float acc = bv;
+    if constexpr (KC == 3) {
+        const int U = (W + 3) / 4;                              // 4-output units per row
+        for (int q = threadIdx.x; q < rb * U; q += 256) {
+            const int r = q / U, c = (q - r * U) * 4;
+            float win[3][8];
 #pragma unroll
-            for (int i = 0; i < KM; ++i)
+            for (int i = 0; i < 3; ++i) {
+                const float4 lo = *(const float4 *)&c2_smem[(r + i) * WS + c];
+                const float4 hi = *(const float4 *)&c2_smem[(r + i) * WS + c + 4];
+                win[i][0] = lo.x;
+                win[i][1] = lo.y;
+                win[i][2] = lo.z;
+                win[i][3] = lo.w;
+                win[i][4] = hi.x;
+                win[i][5] = hi.y;
+                win[i][6] = hi.z;
+                win[i][7] = hi.w;
+            }
+            IO *orow = um + (long long)(h0 + r) * W;
 #pragma unroll
-                for (int j = 0; j < KM; ++j)
-                    if (KC > 0 || (i < Kc && j < Kc))
-                        acc = fmaf(wk[i * KM + j], c2_smem[(r + i) * WP + c + j], acc);
-            um[(long long)(h0 + r) * W + c] = from_f32<IO>(act ? silu_f<IO>(acc) : acc);
+            for (int o = 0; o < 4; ++o) {
+                float acc = bv;
+#pragma unroll
+                for (int i = 0; i < 3; ++i)
+#pragma unroll
+                    for (int j = 0; j < 3; ++j) acc = fmaf(wk[i * 3 + j], win[i][o + j], acc);
+                if (c + o < W) orow[c + o] = from_f32<IO>(act ? silu_f<IO>(acc) : acc);
+            }
+        }
+    } else {
+        for (int r = warp; r < rb; r += 8) {
+            for (int c = lane; c < W; c += 32) {
+                float acc = bv;
+#pragma unroll
+                for (int i = 0; i < KM; ++i)
+#pragma unroll
+                    for (int j = 0; j < KM; ++j)
+                        if (i < Kc && j < Kc)
+                            acc = fmaf(wk[i * KM + j], c2_smem[(r + i) * WS + c + j], acc);
+                um[(long long)(h0 + r) * W + c] = from_f32<IO>(act ? silu_f<IO>(acc) : acc);
+            }
         }
     }
 }

@@ -151,7 +151,7 @@ ssm_status run(int B, int D, int L, int N, int R, int K, const void *x, const fl
 int c2_rows(int H, int W) { return std::max(1, std::min(H, 2048 / std::max(W, 1))); }
 size_t c2_smem(int H, int W, int Kc) {
     const int P = (Kc - 1) / 2;
-    return (size_t)(c2_rows(H, W) + 2 * P) * (W + 2 * P) * sizeof(float);
+    return (size_t)(c2_rows(H, W) + 2 * P) * ssm::pro::conv2d_ws(W, Kc) * sizeof(float);
 }
 
 // SS2D: conv2d (+ SiLU), then for each of the four directions x_proj
