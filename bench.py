@@ -486,7 +486,7 @@ def measure_ss2d_prologue(ssm, spec, dev, stream, steps, R, Kc=3):
              conv_b=(torch.rand(D, generator=gen) - 0.5).to(dev),
              W_x=(torch.randn(4, R + 2 * N, D, generator=gen) * D ** -0.5).to(dev),
              W_dt=(torch.randn(4, D, R, generator=gen) * R ** -0.5).to(dev))
-    ws = torch.empty(B * R * L * 4, dtype=torch.uint8, device=dev)
+    ws = torch.empty(B * 4 * R * L * 4, dtype=torch.uint8, device=dev)   # four dt_low sets
 
     def once():
         ssm.ss2d_prologue_fwd(x, w["conv_w"], w["conv_b"], w["W_x"], w["W_dt"], R, N,

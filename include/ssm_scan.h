@@ -415,7 +415,7 @@ SSM_API size_t ssm_prologue_workspace_bytes(int B, int L, int R);
  * x): delta [B, 4, D, H*W], Bm, Cm [B, 4, N, H*W].  All tensors contiguous,
  * device, caller-owned; I/O tensors in `dt`.  Kc odd, <= 7; N <= 32.
  * workspace: ss2d_prologue_workspace_bytes(B, H, W, R) bytes, 16-byte
- * aligned (one direction's fp32 dt_low at a time).  Arithmetic and errors
+ * aligned (the four directions' fp32 dt_low, [B, 4, R, H*W]).  B <= 16383.  Arithmetic and errors
  * as mamba_prologue_fwd (SSM_ERR_INVALID_ARG also for an even Kc;
  * SSM_ERR_UNSUPPORTED also when the conv's staging of (rows + Kc - 1) x
  * (W + Kc - 1) fp32 values passes 200 KB: W above about 17000 for Kc = 3).

@@ -198,17 +198,17 @@ __device__ __forceinline__ void proj_store(const ProjOut &out, int b, int m, int
 constexpr int BM = 64, BN = 64, BK = 16;
 
 // out[b][m][t] = sum_k W[m][k] * in[b][k][t]: W fp32 [M][K], in [B][K][L]
-// (I/O dtype or fp32).  Tile 64 x 64 per CTA, 16-deep K slices through
+// with batch stride ib (I/O dtype or fp32).  Tile 64 x 64 per CTA, 16-deep K slices through
 // shared memory, 4 x 4 outputs per thread (fp32 FMA).
 template <typename IN, typename IO>
 __global__ void __launch_bounds__(256)
 proj_kernel(const float *__restrict__ W, const IN *__restrict__ in, int M, int K, int L,
-            ProjOut out) {
+            long long ib, ProjOut out) {
     __shared__ float sW[BK][BM + 4];
     __shared__ __align__(16) float sI[BK][BN + 4];
     const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
     const int t0 = blockIdx.x * BN, m0 = blockIdx.y * BM, b = blockIdx.z;
-    const IN *inb = in + (long long)b * K * L;
+    const IN *inb = in + (long long)b * ib;
     float acc[4][4] = {};
     for (int k0 = 0; k0 < K; k0 += BK) {
 #pragma unroll
@@ -285,14 +285,14 @@ template <> __device__ __forceinline__ void mma16816<__half>(float (&c)[4], cons
 template <typename IN, typename IO>
 __global__ void __launch_bounds__(256)
 proj_mma_kernel(const float *__restrict__ W, const IN *__restrict__ in, int M, int K, int L,
-                ProjOut out) {
+                long long ib, ProjOut out) {
     __shared__ __align__(16) IO sW[BM][TKP];        // [row][k]
     __shared__ __align__(16) IO sI[BN][TKP];        // [position][k]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, tg = lane & 3;
     const int wm = (warp % 4) * 16, wn = (warp / 4) * 32;
     const int t0 = blockIdx.x * BN, m0 = blockIdx.y * BM, b = blockIdx.z;
-    const IN *inb = in + (long long)b * K * L;
+    const IN *inb = in + (long long)b * ib;
     float acc[4][4] = {};
     for (int k0 = 0; k0 < K; k0 += TK) {
         // W slice: 64 x 32 (k fastest: coalesced fp32 reads)
@@ -343,7 +343,8 @@ proj_mma_kernel(const float *__restrict__ W, const IN *__restrict__ in, int M, i
 }
 
 // dt_proj with a short inner dimension (R = dt_rank <= RP, RP in {8, 16, 24,
-// 32}): out[b][m][t] = sum_r W[m][r] in[b][r][t] (out's batch stride ob).  A CTA takes DTP_T
+// 32}): out[b][m][t] = sum_r W[m][r] in[b][r][t] (out's batch stride ob;
+// batch element b uses weight set b mod nw, sets [M][R] one after another).  A CTA takes DTP_T
 // positions (two per thread, DTP_T / 2 apart, their R inputs in registers)
 // and rows [m_lo, m_hi) in chunks of 128 staged in shared memory (zero-
 // padded to RP, read back as broadcast float4); stores are coalesced along
@@ -353,9 +354,10 @@ constexpr int DTP_T = 512, DTP_MC = 128;
 template <typename IO, int RP>
 __global__ void __launch_bounds__(256, 2)
 dtproj_kernel(const float *__restrict__ W, const float *__restrict__ in, int M, int R, int L,
-              IO *__restrict__ out, long long ob) {
+              IO *__restrict__ out, long long ob, int nw) {
     __shared__ __align__(16) float sW[DTP_MC * RP];
     const int b = blockIdx.z;
+    W += (long long)(b % nw) * M * R;                        // this z group's weight set
     const int t_a = blockIdx.x * DTP_T + threadIdx.x, t_b = t_a + DTP_T / 2;
     const int per = (M + gridDim.y - 1) / gridDim.y;
     const int m_lo = blockIdx.y * per, m_hi = min(M, m_lo + per);
@@ -416,7 +418,7 @@ dtproj_kernel(const float *__restrict__ W, const float *__restrict__ in, int M, 
 }
 
 // dt_proj on tensor cores for 16-bit I/O: out[b][m][t] = sum_r W[m][r]
-// in[b][r][t] (out's batch stride ob) with W and the fp32 dt_low rounded to tf32 (10-bit mantissa,
+// in[b][r][t] (out's batch stride ob; weight set b mod nw) with W and the fp32 dt_low rounded to tf32 (10-bit mantissa,
 // below the 16-bit output's own rounding) and fp32 accumulation, mma.sync
 // m16n8k8.  A CTA takes DTC_T positions and DTC_RB rows: it stages the
 // input tile [RP][DTC_T] and its W rows [DTC_RB][RP] (zero-padded to RP)
@@ -444,7 +446,7 @@ template <int RP> constexpr size_t dtproj_tc_smem_bytes() {
 template <typename IO, int RP>
 __global__ void __launch_bounds__(256)
 dtproj_tc_kernel(const float *__restrict__ W, const float *__restrict__ in, int M, int R, int L,
-                 IO *__restrict__ out, long long ob) {
+                 IO *__restrict__ out, long long ob, int nw) {
     constexpr int WS = RP + 4, IS = DTC_OS;     // word strides: conflict-free fragment loads
     extern __shared__ __align__(16) unsigned char dtc_smem[];
     unsigned *sW = (unsigned *)dtc_smem;        // [DTC_RB][WS]
@@ -455,6 +457,7 @@ dtproj_tc_kernel(const float *__restrict__ W, const float *__restrict__ in, int 
     const int wm = (warp % 4) * 16, wn = (warp / 4) * 64;
     const int t0 = blockIdx.x * DTC_T, b = blockIdx.z;
     const int m_lo = blockIdx.y * DTC_RB, mc = min(DTC_RB, M - m_lo);
+    W += (long long)(b % nw) * M * R;                        // this z group's weight set
     {
         float iv[RP * DTC_T / 256], wv[RP * DTC_RB / 256];
 #pragma unroll
@@ -625,6 +628,113 @@ xproj_mma_kernel(const float *__restrict__ W, const IO *__restrict__ in, int M, 
             if (tp < L) proj_store<IO>(out, b, m, tp, L, sO[m * XP_OP + tt]);
         }
         __syncthreads();                                        // sO dead before the next slice
+    }
+}
+
+// SS2D x_proj for all four scan directions in one pass over u (16-bit I/O,
+// K <= 256 so that one slice holds the whole inner dimension, M <= 64 rows
+// per direction).  A persistent CTA of 16 warps keeps the four weight sets
+// [4][64][KQ] in shared memory (the I/O type, zero-padded), stages each
+// tile's u [XP_T][KQ] once, then for each direction runs the mma against
+// that direction's weights (warp w: rows 16 (w % 4) .. +16, positions
+// 32 (w / 4) .. +32) and stores through a shared fp32 tile to that
+// direction's destinations and scan order (outs.o[k]).
+struct ProjOut4 {
+    ProjOut o[4];
+};
+__host__ __device__ constexpr int xproj4_kq(int K) { return ((K + 15) / 16) * 16 + 8; }
+inline size_t xproj4_smem_bytes(int K, size_t esize) {
+    return (4 * 64 * (size_t)xproj4_kq(K) + (size_t)XP_T * xproj4_kq(K)) * esize +
+           64 * (size_t)XP_OP * sizeof(float);
+}
+template <typename IO>
+__global__ void __launch_bounds__(XP_NT, 1)
+xproj4_mma_kernel(const float *__restrict__ W, const IO *__restrict__ in, int M, int K, int L,
+                  int nb, ProjOut4 outs) {
+    extern __shared__ __align__(16) unsigned char xq_smem[];
+    constexpr int NW = XP_NT / 32;                              // 16 warps
+    constexpr int PAIRS = XP_T * XP_K / 2 / XP_NT;              // covers K <= XP_K
+    const int KQ = xproj4_kq(K), KR = KQ - 8;                  // KR: K rounded up to 16
+    IO *sW = (IO *)xq_smem;                                    // [4][64][KQ]
+    IO *sI = sW + 4 * 64 * KQ;                                 // [XP_T][KQ]
+    float *sO = (float *)(sI + XP_T * KQ);                     // [64][XP_OP]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, tg = lane & 3;
+    const int wm = (warp % 4) * 16, wn = (warp / 4) * 32;
+    for (int m = warp; m < 4 * 64; m += NW) {
+        const int k4 = m / 64, mr = m % 64;
+        IO *dst = sW + m * KQ;
+        const float *src = W + ((long long)k4 * M + mr) * K;
+        for (int k0 = 0; k0 < KQ; k0 += 128) {
+            float wv[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int k = k0 + q * 32 + lane;
+                wv[q] = (mr < M && k < K) ? src[k] : 0.f;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int k = k0 + q * 32 + lane;
+                if (k < KQ) dst[k] = from_f32<IO>(wv[q]);
+            }
+        }
+    }
+    const int ld_tt = (warp % 8) * 16 + (lane & 15);
+    const int ld_kp0 = (warp / 8) * 2 + (lane >> 4);            // + 4 j
+    const int tpb = (L + XP_T - 1) / XP_T, ntiles = tpb * nb;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        const int b = tile / tpb, t0 = (tile % tpb) * XP_T;
+        const int t = t0 + ld_tt;
+        const IO *src = in + (long long)b * K * L + t;
+        unsigned reg[PAIRS];
+#pragma unroll
+        for (int j = 0; j < PAIRS; ++j) {
+            const int k = 2 * (ld_kp0 + 4 * j);
+            const IO z = from_f32<IO>(0.f);
+            const IO v0 = (t < L && k < K) ? src[(long long)k * L] : z;
+            const IO v1 = (t < L && k + 1 < K) ? src[(long long)(k + 1) * L] : z;
+            reg[j] = (unsigned)*(const unsigned short *)&v0 |
+                     ((unsigned)*(const unsigned short *)&v1 << 16);
+        }
+        __syncthreads();                                        // previous tile's sI reads done
+        unsigned *dsti = (unsigned *)sI;
+#pragma unroll
+        for (int j = 0; j < PAIRS; ++j) {
+            const int kp = ld_kp0 + 4 * j;
+            if (2 * kp < KR) dsti[ld_tt * (KQ / 2) + kp] = reg[j];
+        }
+        __syncthreads();
+        for (int k4 = 0; k4 < 4; ++k4) {
+            const IO *wk = sW + k4 * 64 * KQ;
+            float acc[4][4] = {};
+            for (int ks = 0; ks < KR; ks += 16) {
+                unsigned a[4];
+                a[0] = *(const unsigned *)&wk[(wm + g) * KQ + ks + 2 * tg];
+                a[1] = *(const unsigned *)&wk[(wm + g + 8) * KQ + ks + 2 * tg];
+                a[2] = *(const unsigned *)&wk[(wm + g) * KQ + ks + 2 * tg + 8];
+                a[3] = *(const unsigned *)&wk[(wm + g + 8) * KQ + ks + 2 * tg + 8];
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    unsigned bf[2];
+                    const IO *col = sI + (wn + nt * 8 + g) * KQ + ks + 2 * tg;
+                    bf[0] = *(const unsigned *)col;
+                    bf[1] = *(const unsigned *)(col + 8);
+                    mma16816<IO>(acc[nt], a, bf);
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int half = 0; half < 2; ++half)
+                    *(float2 *)&sO[(wm + g + 8 * half) * XP_OP + wn + nt * 8 + 2 * tg] =
+                        make_float2(acc[nt][2 * half], acc[nt][2 * half + 1]);
+            __syncthreads();
+            for (int i = tid; i < M * XP_T; i += XP_NT) {
+                const int m = i / XP_T, tt = i % XP_T, tp = t0 + tt;
+                if (tp < L) proj_store<IO>(outs.o[k4], b, m, tp, L, sO[m * XP_OP + tt]);
+            }
+            __syncthreads();                                    // sO read before the next block
+        }
     }
 }
 

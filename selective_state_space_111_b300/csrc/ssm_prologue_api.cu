@@ -34,12 +34,12 @@ int sm_count() {
 
 // generic tiled projection: fp32 FMA for fp32 I/O, mma.sync for 16-bit I/O
 template <typename IN, typename IO>
-void launch_proj(dim3 grid, const float *W, const IN *in, int M, int K, int L,
+void launch_proj(dim3 grid, const float *W, const IN *in, int M, int K, int L, long long ib,
                  ssm::pro::ProjOut o, cudaStream_t st) {
     if constexpr (sizeof(IO) == 4)
-        ssm::pro::proj_kernel<IN, IO><<<grid, 256, 0, st>>>(W, in, M, K, L, o);
+        ssm::pro::proj_kernel<IN, IO><<<grid, 256, 0, st>>>(W, in, M, K, L, ib, o);
     else
-        ssm::pro::proj_mma_kernel<IN, IO><<<grid, 256, 0, st>>>(W, in, M, K, L, o);
+        ssm::pro::proj_mma_kernel<IN, IO><<<grid, 256, 0, st>>>(W, in, M, K, L, ib, o);
 }
 
 // x_proj: the weights-stationary tensor-core kernel when its rows (<= 64)
@@ -61,7 +61,8 @@ ssm_status x_proj(int B, int M, int K, int L, const float *W, const IO *u, ssm::
             return last_error();
         }
     }
-    launch_proj<IO, IO>(dim3((L + BN - 1) / BN, (M + BM - 1) / BM, B), W, u, M, K, L, o, st);
+    launch_proj<IO, IO>(dim3((L + BN - 1) / BN, (M + BM - 1) / BM, B), W, u, M, K, L,
+                        (long long)K * L, o, st);
     return last_error();
 }
 
@@ -69,7 +70,7 @@ ssm_status x_proj(int B, int M, int K, int L, const float *W, const IO *u, ssm::
 // generic tiled one
 template <typename IO, int RP>
 ssm_status launch_dtproj(int B, int D, int R, int L, const float *W, const float *dt_low, IO *dt,
-                         long long ob, cudaStream_t st) {
+                         long long ob, int nw, cudaStream_t st) {
     using namespace ssm::pro;
     if constexpr (sizeof(IO) == 2) {
         // tensor cores (tf32 operands, fp32 accumulation)
@@ -79,7 +80,7 @@ ssm_status launch_dtproj(int B, int D, int R, int L, const float *W, const float
                                  (int)smem) != cudaSuccess)
             return SSM_ERR_CUDA;
         dtproj_tc_kernel<IO, RP><<<dim3((L + DTC_T - 1) / DTC_T, (D + DTC_RB - 1) / DTC_RB, B),
-                                   256, smem, st>>>(W, dt_low, D, R, L, dt, ob);
+                                   256, smem, st>>>(W, dt_low, D, R, L, dt, ob, nw);
     } else {
         // fp32 I/O: fp32 FMA
         const int tiles = (L + DTP_T - 1) / DTP_T;
@@ -87,32 +88,41 @@ ssm_status launch_dtproj(int B, int D, int R, int L, const float *W, const float
         int split = (int)std::min<long long>(
             (want + (long long)tiles * B - 1) / ((long long)tiles * B), (D + DTP_MC - 1) / DTP_MC);
         split = std::max(split, 1);
-        dtproj_kernel<IO, RP><<<dim3(tiles, split, B), 256, 0, st>>>(W, dt_low, D, R, L, dt, ob);
+        dtproj_kernel<IO, RP><<<dim3(tiles, split, B), 256, 0, st>>>(W, dt_low, D, R, L, dt, ob,
+                                                                     nw);
     }
     return last_error();
 }
 
-// dt_proj: the register-blocked kernels for dt_rank <= 32, else the generic
-// tiled one; ob = batch stride of dt in elements
+// dt_proj of nw weight sets (scan directions): dt_low [B][nw][R][L] ->
+// dt [B][nw][D][L] with W [nw][D][R]; the register-blocked kernels for
+// dt_rank <= 32 (one launch, the (batch, set) pairs along grid z), else the
+// generic tiled one per set
 template <typename IO>
-ssm_status dt_proj(int B, int D, int R, int L, const float *W, const float *dt_low, IO *dt,
-                   long long ob, cudaStream_t st) {
+ssm_status dt_proj(int B, int nw, int D, int R, int L, const float *W, const float *dt_low,
+                   IO *dt, cudaStream_t st) {
     using namespace ssm::pro;
-    if (R <= 8) return launch_dtproj<IO, 8>(B, D, R, L, W, dt_low, dt, ob, st);
-    if (R <= 16) return launch_dtproj<IO, 16>(B, D, R, L, W, dt_low, dt, ob, st);
-    if (R <= 24) return launch_dtproj<IO, 24>(B, D, R, L, W, dt_low, dt, ob, st);
-    if (R <= 32) return launch_dtproj<IO, 32>(B, D, R, L, W, dt_low, dt, ob, st);
-    ProjOut o{};
-    o.dst[0] = dt;
-    o.r[0] = 0;
-    o.r[1] = D;
-    o.r[2] = D;
-    o.r[3] = D;
-    o.bstride[0] = ob;
-    o.order = -1;
-    launch_proj<float, IO>(dim3((L + BN - 1) / BN, (D + BM - 1) / BM, B), W, dt_low, D, R, L, o,
-                           st);
-    return last_error();
+    const long long ob = (long long)D * L;
+    const int Bz = B * nw;
+    if (R <= 8) return launch_dtproj<IO, 8>(Bz, D, R, L, W, dt_low, dt, ob, nw, st);
+    if (R <= 16) return launch_dtproj<IO, 16>(Bz, D, R, L, W, dt_low, dt, ob, nw, st);
+    if (R <= 24) return launch_dtproj<IO, 24>(Bz, D, R, L, W, dt_low, dt, ob, nw, st);
+    if (R <= 32) return launch_dtproj<IO, 32>(Bz, D, R, L, W, dt_low, dt, ob, nw, st);
+    for (int k = 0; k < nw; ++k) {
+        ProjOut o{};
+        o.dst[0] = dt + (long long)k * D * L;
+        o.r[0] = 0;
+        o.r[1] = D;
+        o.r[2] = D;
+        o.r[3] = D;
+        o.bstride[0] = (long long)nw * D * L;
+        o.order = -1;
+        launch_proj<float, IO>(dim3((L + BN - 1) / BN, (D + BM - 1) / BM, B),
+                               W + (long long)k * D * R, dt_low + (long long)k * R * L, D, R, L,
+                               (long long)nw * R * L, o, st);
+        if (last_error() != SSM_OK) return SSM_ERR_CUDA;
+    }
+    return SSM_OK;
 }
 
 template <typename IO>
@@ -144,7 +154,7 @@ ssm_status run(int B, int D, int L, int N, int R, int K, const void *x, const fl
     o1.order = -1;
     if (x_proj<IO>(B, M, D, L, W_x, (const IO *)u, o1, st) != SSM_OK) return SSM_ERR_CUDA;
     // dt_proj: all D rows -> dt
-    return dt_proj<IO>(B, D, R, L, W_dt, dt_low, (IO *)dt, (long long)D * L, st);
+    return dt_proj<IO>(B, 1, D, R, L, W_dt, dt_low, (IO *)dt, st);
 }
 
 // rows of the map per conv2d CTA (about 2048 outputs) and its shared bytes
@@ -181,10 +191,13 @@ ssm_status run_ss2d(int B, int D, int H, int W, int N, int R, int Kc, const void
                                                           D, H, W, Kc, RB, act);
     }
     if (last_error() != SSM_OK) return SSM_ERR_CUDA;
+    // x_proj of the four directions: dt_low [B][4][R][L] (workspace), B, C
+    // [B][4][N][L], each output at its position in that direction's order
     const int M = R + 2 * N;
+    ProjOut4 outs{};
     for (int k = 0; k < 4; ++k) {
-        ProjOut o{};
-        o.dst[0] = dt_low;
+        ProjOut &o = outs.o[k];
+        o.dst[0] = dt_low + (long long)k * R * L;
         o.dst[1] = (IO *)Bm + (long long)k * N * L;
         o.dst[2] = (IO *)Cm + (long long)k * N * L;
         o.f32[0] = 1;
@@ -192,18 +205,35 @@ ssm_status run_ss2d(int B, int D, int H, int W, int N, int R, int Kc, const void
         o.r[1] = R;
         o.r[2] = R + N;
         o.r[3] = M;
-        o.bstride[0] = (long long)R * L;
+        o.bstride[0] = 4LL * R * L;
         o.bstride[1] = o.bstride[2] = 4LL * N * L;
         o.order = k;
         o.H = H;
         o.W = W;
-        if (x_proj<IO>(B, M, D, L, W_x + (long long)k * M * D, (const IO *)u, o, st) != SSM_OK)
-            return SSM_ERR_CUDA;
-        if (dt_proj<IO>(B, D, R, L, W_dt + (long long)k * D * R, dt_low,
-                        (IO *)delta + (long long)k * D * L, 4LL * D * L, st) != SSM_OK)
-            return SSM_ERR_CUDA;
     }
-    return SSM_OK;
+    bool done = false;
+    if constexpr (sizeof(IO) == 2) {
+        // one pass over u for all four directions
+        const size_t xs = xproj4_smem_bytes(D, sizeof(IO));
+        if (M <= 64 && D <= XP_K && xs <= 227 * 1024) {
+            if (cudaFuncSetAttribute(xproj4_mma_kernel<IO>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)xs) != cudaSuccess)
+                return SSM_ERR_CUDA;
+            const long long tiles = (long long)B * ((L + XP_T - 1) / XP_T);
+            const int grid = (int)std::min<long long>(tiles, sm_count());
+            xproj4_mma_kernel<IO><<<grid, XP_NT, xs, st>>>(W_x, (const IO *)u, M, D, L, B, outs);
+            if (last_error() != SSM_OK) return SSM_ERR_CUDA;
+            done = true;
+        }
+    }
+    if (!done)
+        for (int k = 0; k < 4; ++k)
+            if (x_proj<IO>(B, M, D, L, W_x + (long long)k * M * D, (const IO *)u, outs.o[k], st) !=
+                SSM_OK)
+                return SSM_ERR_CUDA;
+    // dt_proj of the four directions in one launch
+    return dt_proj<IO>(B, 4, D, R, L, W_dt, dt_low, (IO *)delta, st);
 }
 
 }  // namespace
@@ -246,7 +276,7 @@ ssm_status mamba_prologue_fwd(ssm_dtype dt, int B, int D, int L, int N, int R, i
 
 size_t ss2d_prologue_workspace_bytes(int B, int H, int W, int R) {
     if (B < 0 || H < 0 || W < 0 || R <= 0) return (size_t)-1;
-    return (size_t)B * R * H * W * sizeof(float);
+    return (size_t)B * 4 * R * H * W * sizeof(float);
 }
 
 ssm_status ss2d_prologue_fwd(ssm_dtype dt, int B, int D, int H, int W, int N, int R, int Kc,
@@ -257,7 +287,7 @@ ssm_status ss2d_prologue_fwd(ssm_dtype dt, int B, int D, int H, int W, int N, in
     if (dt != SSM_F32 && dt != SSM_BF16 && dt != SSM_F16) return SSM_ERR_INVALID_ARG;
     if (B < 0 || D < 0 || H < 0 || W < 0 || N <= 0 || R <= 0 || Kc <= 0 || Kc % 2 == 0)
         return SSM_ERR_INVALID_ARG;
-    if (N > 32 || Kc > 7 || B > 65535 || D > 65535) return SSM_ERR_UNSUPPORTED;
+    if (N > 32 || Kc > 7 || B > 16383 || D > 65535) return SSM_ERR_UNSUPPORTED;
     const long long L = (long long)H * W;
     if ((long long)D * L > 0x7fffffffLL || (long long)(R + 2 * N) * L > 0x7fffffffLL ||
         4LL * D * L > 0x7fffffffLL || c2_smem(H, W, Kc) > 200 * 1024)

@@ -173,6 +173,7 @@ def test_ss2d_prologue_arguments_are_rejected_before_launch(lib):
     assert ss2d_prologue(lib, x=FAKE + 1) == 1
     assert ss2d_prologue(lib, W=40000) == 2         # conv staging over its shared-memory bound
     assert ss2d_prologue(lib) == 4                  # no workspace
-    assert ss2d_prologue(lib, ws=FAKE, wsb=2 * 12 * 4 - 1) == 4
+    assert ss2d_prologue(lib, ws=FAKE, wsb=4 * 2 * 12 * 4 - 1) == 4
+    assert ss2d_prologue(lib, B=16384) == 2          # the (batch, direction) grid's z bound
     assert ss2d_prologue(lib, H=0) == 0
-    assert lib.ss2d_prologue_workspace_bytes(2, 3, 4, 5) == 2 * 5 * 12 * 4
+    assert lib.ss2d_prologue_workspace_bytes(2, 3, 4, 5) == 2 * 4 * 5 * 12 * 4   # four dt_low sets
