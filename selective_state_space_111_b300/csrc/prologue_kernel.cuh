@@ -21,16 +21,18 @@ namespace pro {
 // x reversed in time, zero before the start.  A CTA covers CONV_T positions
 // of one channel: it stages xs over them plus the K - 1 halo in shared
 // memory (coalesced reads, in reverse order for reverse = 1, every load in
-// flight before the stores), then each thread makes CONV_T / 256 outputs,
-// consecutive threads on consecutive positions.  KT = K fixed at compile
-// time (the usual 4 taps), or 0 for any K <= 8.
+// flight before the stores).  KT = 4 (compile time, the usual taps): each
+// thread makes 4 consecutive outputs from the 8 values two 16-byte shared
+// loads give, puts them back in shared memory, and the CTA stores along
+// positions (coalesced); KT = 0 (any K <= 8): CONV_T / 256 outputs per
+// thread, consecutive threads on consecutive positions.
 constexpr int CONV_T = 2048, CONV_S = CONV_T + 8, CONV_V = (CONV_S + 255) / 256;
 template <typename IO, int KT>
 __global__ void __launch_bounds__(256)
 conv_silu_kernel(const IO *__restrict__ x, const float *__restrict__ w,
                  const float *__restrict__ bias, IO *__restrict__ u, int D, int L, int K,
                  int reverse) {
-    __shared__ float sx[CONV_S];                // sx[i] = xs[t0 - (K-1) + i], K <= 8
+    __shared__ __align__(16) float sx[CONV_S];  // sx[i] = xs[t0 - (K-1) + i], K <= 8
     const int t0 = blockIdx.x * CONV_T;
     const int d = blockIdx.y, b = blockIdx.z;
     const long long row = ((long long)b * D + d) * L;
@@ -52,15 +54,46 @@ conv_silu_kernel(const IO *__restrict__ x, const float *__restrict__ w,
     for (int k = 0; k < KM; ++k) wk[k] = (KT > 0 || k < K) ? w[d * K + k] : 0.f;
     const float bv = bias ? bias[d] : 0.f;
     __syncthreads();
+    if constexpr (KT == 4) {
+        // outputs go back to shared memory (after everyone has read sx),
+        // then out along positions: coalesced stores
+        float res[CONV_T / 1024][4];
 #pragma unroll
-    for (int j = 0; j < CONV_T / 256; ++j) {
-        const int tt = j * 256 + threadIdx.x, t = t0 + tt;
-        if (t >= L) break;
-        float acc = bv;
+        for (int j = 0; j < CONV_T / 1024; ++j) {
+            const int tt = (j * 256 + threadIdx.x) * 4;
+            const float4 lo = *(const float4 *)&sx[tt];
+            const float4 hi = *(const float4 *)&sx[tt + 4];
+            const float win[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
-        for (int k = 0; k < KM; ++k)
-            if (KT > 0 || k < K) acc = fmaf(wk[k], sx[tt + k], acc);
-        u[row + t] = from_f32<IO>(silu_f<IO>(acc));
+            for (int o = 0; o < 4; ++o) {
+                float acc = bv;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) acc = fmaf(wk[k], win[o + k], acc);
+                res[j][o] = silu_f<IO>(acc);
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < CONV_T / 1024; ++j)
+            *(float4 *)&sx[(j * 256 + threadIdx.x) * 4] =
+                make_float4(res[j][0], res[j][1], res[j][2], res[j][3]);
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < CONV_T / 256; ++j) {
+            const int tt = j * 256 + threadIdx.x, t = t0 + tt;
+            if (t < L) u[row + t] = from_f32<IO>(sx[tt]);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < CONV_T / 256; ++j) {
+            const int tt = j * 256 + threadIdx.x, t = t0 + tt;
+            if (t >= L) break;
+            float acc = bv;
+#pragma unroll
+            for (int k = 0; k < KM; ++k)
+                if (k < K) acc = fmaf(wk[k], sx[tt + k], acc);
+            u[row + t] = from_f32<IO>(silu_f<IO>(acc));
+        }
     }
 }
 

@@ -50,8 +50,11 @@ def scale_err(a, r):
     return float(np.max(np.abs(a - r)) / (1 + np.max(np.abs(r)))) if r.size else 0.0
 
 
+# (B, D, L, N, R, K); D = 1400: W_x past shared memory, the generic tiled
+# x_proj; R = 40: dt_proj past 32, the generic tiled dt_proj
 SHAPES = [(1, 5, 7, 4, 2, 4), (2, 70, 130, 16, 5, 4), (1, 33, 65, 32, 3, 3),
-          (2, 64, 64, 16, 24, 4), (1, 1, 1, 16, 1, 4)]
+          (2, 64, 64, 16, 24, 4), (1, 1, 1, 16, 1, 4), (1, 1400, 37, 16, 6, 4),
+          (1, 48, 2100, 16, 40, 4)]
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16", "f16"])
@@ -127,10 +130,13 @@ def ss2d_weights(g, D, R, N, Kc):
 
 
 # (B, D, H, W, N, R, Kc): non-square maps, one-row and one-column maps,
-# d_state 32 (x_proj past 64 rows: the generic tiled kernel), Kc 1..7
+# d_state 32 (x_proj past 64 rows: the generic tiled kernel), Kc 1..7,
+# and the fallbacks below
 SS2D_SHAPES = [(1, 5, 4, 6, 16, 2, 3), (2, 70, 9, 13, 16, 5, 3), (1, 33, 7, 5, 32, 3, 5),
                (2, 64, 16, 16, 16, 6, 3), (1, 1, 1, 1, 16, 1, 3), (1, 8, 3, 40, 16, 4, 7),
-               (1, 9, 50, 1, 16, 2, 1), (1, 16, 130, 3, 16, 24, 3)]
+               (1, 9, 50, 1, 16, 2, 1), (1, 16, 130, 3, 16, 24, 3),
+               (1, 300, 5, 6, 16, 4, 3),     # d_inner > 256: x_proj per direction, 2 slices
+               (2, 12, 6, 7, 16, 36, 3)]     # dt_rank > 32: the generic dt_proj per direction
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16", "f16"])
