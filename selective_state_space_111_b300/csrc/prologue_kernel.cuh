@@ -216,6 +216,18 @@ __device__ __forceinline__ int scan_pos(int k, int p, int H, int W) {
     return k == 1 ? t : L - 1 - t;
 }
 
+// stores output row m of batch element b at position t of its row, t
+// already in the destination's order
+template <typename IO>
+__device__ __forceinline__ void proj_store_at(const ProjOut &out, int b, int m, int t, int L,
+                                              float v) {
+    int s = 0;
+    while (m >= out.r[s + 1]) ++s;
+    const long long o = (long long)b * out.bstride[s] + (long long)(m - out.r[s]) * L + t;
+    if (out.f32[s]) ((float *)out.dst[s])[o] = v;
+    else ((IO *)out.dst[s])[o] = from_f32<IO>(v);
+}
+
 // stores output row m, position t of batch element b
 template <typename IO>
 __device__ __forceinline__ void proj_store(const ProjOut &out, int b, int m, int t, int L,
@@ -671,7 +683,10 @@ xproj_mma_kernel(const float *__restrict__ W, const IO *__restrict__ in, int M, 
 // tile's u [XP_T][KQ] once, then for each direction runs the mma against
 // that direction's weights (warp w: rows 16 (w % 4) .. +16, positions
 // 32 (w / 4) .. +32) and stores through a shared fp32 tile to that
-// direction's destinations and scan order (outs.o[k]).
+// direction's destinations (outs.o[k]).  A tile is a block of 8 map rows x
+// 16 columns: the row-major directions store runs of 16 positions, and the
+// column-major ones, walking h fastest, runs of 8 (a tile of 128
+// consecutive row-major positions would scatter them one by one, H apart).
 struct ProjOut4 {
     ProjOut o[4];
 };
@@ -712,20 +727,23 @@ xproj4_mma_kernel(const float *__restrict__ W, const IO *__restrict__ in, int M,
             }
         }
     }
-    const int ld_tt = (warp % 8) * 16 + (lane & 15);
+    const int ld_tt = (warp % 8) * 16 + (lane & 15);            // = 16 (row in block) + column
     const int ld_kp0 = (warp / 8) * 2 + (lane >> 4);            // + 4 j
-    const int tpb = (L + XP_T - 1) / XP_T, ntiles = tpb * nb;
+    const int H = outs.o[0].H, Wd = outs.o[0].W;
+    const int tW = (Wd + 15) / 16, tpb = ((H + 7) / 8) * tW, ntiles = tpb * nb;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-        const int b = tile / tpb, t0 = (tile % tpb) * XP_T;
-        const int t = t0 + ld_tt;
-        const IO *src = in + (long long)b * K * L + t;
+        const int b = tile / tpb, blk = tile % tpb;
+        const int h0 = (blk / tW) * 8, w0 = (blk % tW) * 16;
+        const int lh = h0 + ld_tt / 16, lw = w0 + ld_tt % 16;
+        const bool pin = lh < H && lw < Wd;
+        const IO *src = in + (long long)b * K * L + (pin ? lh * Wd + lw : 0);
         unsigned reg[PAIRS];
 #pragma unroll
         for (int j = 0; j < PAIRS; ++j) {
             const int k = 2 * (ld_kp0 + 4 * j);
             const IO z = from_f32<IO>(0.f);
-            const IO v0 = (t < L && k < K) ? src[(long long)k * L] : z;
-            const IO v1 = (t < L && k + 1 < K) ? src[(long long)(k + 1) * L] : z;
+            const IO v0 = (pin && k < K) ? src[(long long)k * L] : z;
+            const IO v1 = (pin && k + 1 < K) ? src[(long long)(k + 1) * L] : z;
             reg[j] = (unsigned)*(const unsigned short *)&v0 |
                      ((unsigned)*(const unsigned short *)&v1 << 16);
         }
@@ -762,9 +780,16 @@ xproj4_mma_kernel(const float *__restrict__ W, const IO *__restrict__ in, int M,
                     *(float2 *)&sO[(wm + g + 8 * half) * XP_OP + wn + nt * 8 + 2 * tg] =
                         make_float2(acc[nt][2 * half], acc[nt][2 * half + 1]);
             __syncthreads();
+            const bool colmajor = k4 == 1 || k4 == 3;
             for (int i = tid; i < M * XP_T; i += XP_NT) {
-                const int m = i / XP_T, tt = i % XP_T, tp = t0 + tt;
-                if (tp < L) proj_store<IO>(outs.o[k4], b, m, tp, L, sO[m * XP_OP + tt]);
+                const int m = i / XP_T, e = i % XP_T;
+                const int tt = colmajor ? (e % 8) * 16 + e / 8 : e;    // h fastest: runs in t
+                const int h = h0 + tt / 16, w = w0 + tt % 16;
+                if (h < H && w < Wd) {
+                    const int p = h * Wd + w, c = w * H + h;
+                    const int ts = k4 == 0 ? p : k4 == 1 ? c : k4 == 2 ? L - 1 - p : L - 1 - c;
+                    proj_store_at<IO>(outs.o[k4], b, m, ts, L, sO[m * XP_OP + tt]);
+                }
             }
             __syncthreads();                                    // sO read before the next block
         }

@@ -220,7 +220,8 @@ ssm_status run_ss2d(int B, int D, int H, int W, int N, int R, int Kc, const void
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)xs) != cudaSuccess)
                 return SSM_ERR_CUDA;
-            const long long tiles = (long long)B * ((L + XP_T - 1) / XP_T);
+            // tiles of 8 map rows x 16 columns
+            const long long tiles = (long long)B * ((H + 7) / 8) * ((W + 15) / 16);
             const int grid = (int)std::min<long long>(tiles, sm_count());
             xproj4_mma_kernel<IO><<<grid, XP_NT, xs, st>>>(W_x, (const IO *)u, M, D, L, B, outs);
             if (last_error() != SSM_OK) return SSM_ERR_CUDA;
