@@ -200,3 +200,36 @@ def test_ss2d_inner_path_from_x(io):
     ref_scan = oracle.ss2d(u, delta, A, Bm, Cm, Dk, z, bias, True)
     assert seq_err(y, ref_scan) <= TOL[io]              # the scan on what it was given
     assert scale_err(y, ref_chain) <= 2 * TOL2[io]      # the whole path from x
+
+
+def test_prologue_outputs_off_the_4_byte_grid():
+    # outputs one element into larger buffers (2-byte aligned only): the
+    # pair stores must fall back to 2-byte stores; straight through the C ABI
+    from selective_state_space_111_b300 import binding
+    lib = binding.lib()
+    B, D, L, N, R, K = 2, 40, 301, 16, 5, 4
+    g = torch.Generator().manual_seed(303)
+    x = torch.randn(B, D, L, generator=g).to(torch.bfloat16)
+    w = weights(g, D, R, N, K)
+    wg = {k: v.cuda() for k, v in w.items()}
+    xc = x.cuda()
+
+    def shifted(*shape):
+        n = int(np.prod(shape))
+        return torch.zeros(n + 1, dtype=torch.bfloat16, device="cuda")[1:].view(*shape)
+
+    u, delta, Bm, Cm = shifted(B, D, L), shifted(B, D, L), shifted(B, N, L), shifted(B, N, L)
+    assert u.data_ptr() % 4 == 2
+    nws = int(lib.ssm_prologue_workspace_bytes(B, L, R))
+    ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+    st = lib.mamba_prologue_fwd(1, B, D, L, N, R, K, xc.data_ptr(), wg["conv_w"].data_ptr(),
+                                wg["conv_b"].data_ptr(), wg["W_x"].data_ptr(),
+                                wg["W_dt"].data_ptr(), 0, u.data_ptr(), delta.data_ptr(),
+                                Bm.data_ptr(), Cm.data_ptr(), ws.data_ptr(), nws,
+                                torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    ru, rdt, rB, rC = pro.prologue(x, w["conv_w"], w["conv_b"], w["W_x"], w["W_dt"], R, N)
+    assert seq_err(u, ru) <= TOL["bf16"]
+    for a, r in ((delta, rdt), (Bm, rB), (Cm, rC)):
+        assert scale_err(a, r) <= TOL2["bf16"]
