@@ -50,9 +50,9 @@ def peaks():
 
 # ---------------------------------------------------------------- GPU arm
 def launches_per_step(op):
-    """Kernels one call launches: B/C packing (one per B/C set), the
-    transposes of SS2D, and the scan kernel(s)."""
-    return {"single": 2, "v1": 2, "v2": 3, "ss2d": 5}[op]
+    """Kernels one call launches: B/C packing (one launch for every B/C
+    set), the transposes of SS2D, and the scan kernel(s)."""
+    return {"single": 2, "v1": 2, "v2": 2, "ss2d": 5}[op]
 
 
 def scan_sources_sha():

@@ -107,15 +107,30 @@ struct BiParams {
 // (j < NM), C[b,k,j-NM,t] (j >= NM); 0 for state indices >= N.
 // Block: 64 positions of one (b, k), 256 threads; block (0,0,0) also clears
 // the status word so that the scan kernel of the same call can set it.
+// With Bm1 given, grid z = 2 packs two separate sets (v2's two branches) in
+// one launch: z = 0 the first (Bm, Cm -> out), z = 1 the second (Bm1, Cm1 ->
+// out1), each with K = 1.
 template <typename IO, int NM>
 __global__ void __launch_bounds__(256)
 pack_bc_kernel(const IO *__restrict__ Bm, const IO *__restrict__ Cm, float *__restrict__ out,
-               int N, int L, unsigned *status) {
+               int N, int L, unsigned *status, const IO *__restrict__ Bm1 = nullptr,
+               const IO *__restrict__ Cm1 = nullptr, float *__restrict__ out1 = nullptr) {
     constexpr int kBC = 2 * NM;
     __shared__ float tile[kBC][65];
-    const int b = blockIdx.y, k = blockIdx.z, t0 = blockIdx.x * 64;
-    const int Bt = gridDim.y, K = gridDim.z;
-    if (status != nullptr && blockIdx.x == 0 && b == 0 && k == 0 && threadIdx.x == 0) *status = 0;
+    const int b = blockIdx.y, t0 = blockIdx.x * 64;
+    int k = blockIdx.z, K = gridDim.z;
+    const int Bt = gridDim.y;
+    if (status != nullptr && blockIdx.x == 0 && b == 0 && blockIdx.z == 0 && threadIdx.x == 0)
+        *status = 0;
+    if (Bm1 != nullptr) {
+        if (k == 1) {
+            Bm = Bm1;
+            Cm = Cm1;
+            out = out1;
+        }
+        k = 0;
+        K = 1;
+    }
     for (int i = threadIdx.x; i < kBC * 64; i += 256) {
         const int j = i >> 6, tt = i & 63, t = t0 + tt, n = j & (NM - 1);
         float v = 0.f;

@@ -177,14 +177,18 @@ ssm_status launch_two_branch(const ssm::BiParams &P, cudaStream_t st, bool last 
 template <typename IO, int NDIR, int NM>
 ssm_status run_bidir_nm(ssm::BiParams P, const void *Bm, const void *Cm, const void *Bm_b,
                         const void *Cm_b, bool two_sets, cudaStream_t st) {
-    ssm_status s = launch_pack<IO, NM>(Bm, Cm, const_cast<float *>(P.br[0].bc), P.B, P.N, P.L,
-                                   P.status, st);
-    if (s != SSM_OK) return s;
+    ssm_status s;
     if (two_sets) {
-        s = launch_pack<IO, NM>(Bm_b, Cm_b, const_cast<float *>(P.br[1].bc), P.B, P.N, P.L,
-                            nullptr, st);
-        if (s != SSM_OK) return s;
+        // both branches' B/C sets in one launch (grid z = 2)
+        ssm::pack_bc_kernel<IO, NM><<<dim3((P.L + 63) / 64, P.B, 2), 256, 0, st>>>(
+            (const IO *)Bm, (const IO *)Cm, const_cast<float *>(P.br[0].bc), P.N, P.L, P.status,
+            (const IO *)Bm_b, (const IO *)Cm_b, const_cast<float *>(P.br[1].bc));
+        s = cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+    } else {
+        s = launch_pack<IO, NM>(Bm, Cm, const_cast<float *>(P.br[0].bc), P.B, P.N, P.L,
+                                P.status, st);
     }
+    if (s != SSM_OK) return s;
     if (NDIR == 2) return launch_two_branch<IO, ssm::OUT_Y, NM>(P, st);
     return launch_bidir<IO, kBiS, 1, kBiG1, ssm::OUT_Y, NM>(P, st);
 }
