@@ -171,6 +171,30 @@ transpose_maps_kernel(const E *__restrict__ in, E *__restrict__ out, int maps, i
     }
 }
 
+// out[m][c][r] = in[m][r][c] for maps small enough to sit whole in shared
+// memory (R x (C + 1) elements, at most 48 KB): a CTA takes whole maps, so a
+// map is read and written as one contiguous run (warp w, lane l: rows
+// w, w + 8, ... in, columns w, w + 8, ... out; the padded row keeps the
+// column reads free of bank conflicts).
+template <typename E>
+__global__ void __launch_bounds__(256)
+transpose_whole_maps_kernel(const E *__restrict__ in, E *__restrict__ out, int maps, int R,
+                            int C) {
+    extern __shared__ __align__(16) unsigned char tw_smem[];
+    E *tile = (E *)tw_smem;                                  // [R][C + 1]
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int m = blockIdx.x; m < maps; m += gridDim.x) {
+        const E *src = in + (long long)m * R * C;
+        E *dst = out + (long long)m * R * C;
+        for (int r = warp; r < R; r += 8)
+            for (int c = lane; c < C; c += 32) tile[r * (C + 1) + c] = src[(long long)r * C + c];
+        __syncthreads();
+        for (int c = warp; c < C; c += 8)
+            for (int r = lane; r < R; r += 32) dst[(long long)c * R + r] = tile[r * (C + 1) + c];
+        __syncthreads();
+    }
+}
+
 // ------------------------------------------------------------------ layout
 // One CTA = R channels of one batch element x NDIR branches, in warps with
 // three roles linked by full/empty mbarrier rings (T = 32 positions per

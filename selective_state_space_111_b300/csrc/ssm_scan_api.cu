@@ -282,8 +282,15 @@ SsWs ss2d_ws(ssm_dtype dt, int B, int D, int L, int nm) {
 
 template <typename E>
 ssm_status launch_transpose(const E *in, E *out, int maps, int R, int C, cudaStream_t st) {
-    dim3 grid((C + 31) / 32, (R + 31) / 32, maps < 65535 ? maps : 65535);
-    ssm::transpose_maps_kernel<E><<<grid, 256, 0, st>>>(in, out, maps, R, C);
+    const size_t whole = (size_t)R * (C + 1) * sizeof(E);
+    if (whole <= 48 * 1024) {
+        // whole maps per CTA: each map one contiguous read and write
+        const int grid = maps < 65535 ? maps : 65535;
+        ssm::transpose_whole_maps_kernel<E><<<grid, 256, whole, st>>>(in, out, maps, R, C);
+    } else {
+        dim3 grid((C + 31) / 32, (R + 31) / 32, maps < 65535 ? maps : 65535);
+        ssm::transpose_maps_kernel<E><<<grid, 256, 0, st>>>(in, out, maps, R, C);
+    }
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
