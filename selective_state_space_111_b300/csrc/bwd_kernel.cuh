@@ -378,17 +378,29 @@ channel_sum_kernel(const float *__restrict__ a, const float *__restrict__ a2, lo
                    float *__restrict__ out) {
     __shared__ float red[256];
     const int dch = blockIdx.x;
-    float acc = 0.f;
+    // four independent accumulators (positions t, t + 256, t + 512, t + 768
+    // of every 1024), so four loads are in flight; combined in a fixed order
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int b = 0; b < B; ++b) {
         const long long o = b * a_bstride + (long long)dch * L;
         const IO *ur = u ? u + ((long long)b * D + dch) * L : nullptr;
-        for (int t = threadIdx.x; t < L; t += 256) {
-            float v = a[o + t];
-            if (a2) v += a2[o + t];
-            acc += u ? v * to_f32(ur[t]) : v;
+        for (int t0 = threadIdx.x; t0 < L; t0 += 1024) {
+            float v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int t = t0 + 256 * q;
+                v[q] = 0.f;
+                if (t < L) {
+                    v[q] = a[o + t];
+                    if (a2) v[q] += a2[o + t];
+                    if (u) v[q] *= to_f32(ur[t]);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[q] += v[q];
         }
     }
-    red[threadIdx.x] = acc;
+    red[threadIdx.x] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
     __syncthreads();
     for (int s2 = 128; s2 > 0; s2 >>= 1) {
         if (threadIdx.x < s2) red[threadIdx.x] += red[threadIdx.x + s2];
@@ -453,7 +465,8 @@ __global__ void convert_kernel(const float *__restrict__ a, const float *__restr
 }
 
 // dB[b][n][s] (I/O, at out + b * out_bstride) = sum over the nslot partials
-// [slot][B][L][16] (slot-major, fixed order)
+// [slot][B][L][nm] (slot-major; a fixed summation order, so the result is
+// the same on every run)
 template <typename IO>
 __global__ void reduce_bc_kernel(const float *__restrict__ part, int nslot, int B, int L, int N,
                                  int nm, IO *__restrict__ out, long long out_bstride) {
