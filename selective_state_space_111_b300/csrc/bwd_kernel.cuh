@@ -75,6 +75,12 @@ struct Params {
 __device__ __forceinline__ float sigmoid_f(float x) {
     return 1.f / (1.f + expf(-x));
 }
+// sigmoid for the softplus derivative: the accurate form for fp32 I/O, the
+// MUFU form (ex2, rcp) for 16-bit I/O, as the forward pass's gate uses
+template <typename IO> __device__ __forceinline__ float sigmoid_io(float x) {
+    if constexpr (sizeof(IO) == 4) return sigmoid_f(x);
+    else return rcp_approx(1.f + ex2_approx(-x * kLog2e));
+}
 // dynamic shared memory: dB, dC partials per warp, then the chunk's
 // recomputed states (step-major: thread-contiguous rows, no bank conflicts)
 template <int NM> __host__ __device__ constexpr int part_floats() { return NWARP * NM * (T + 4); }
@@ -196,8 +202,10 @@ scan_bwd_kernel(const Params P) {
             if (w < L && dd < D) {
                 const float x = rdt[r] + sBias[cc];
                 if (P.delta_softplus) {
-                    dl = x > 20.f ? x : log1pf(expf(x));
-                    sg = sigmoid_f(x);
+                    // the forward pass's own softplus (MUFU forms for 16-bit
+                    // I/O), so the recomputed states match the forward's
+                    dl = softplus_f<IO>(x);
+                    sg = sigmoid_io<IO>(x);
                 } else {
                     dl = x;
                 }
