@@ -232,9 +232,24 @@ scan_bwd_kernel(const Params P) {
         __syncthreads();
         if (c + 1 < nch) fetch(c + 1, false);
         const int len = min(T, L - c * T);
-        for (int j = 0; j < len; ++j) {
-            const float dl = sD[ch][j];
-            h = fmaf(ex2_approx(dl * A2), h, dl * sBt[n][j] * sU[ch][j]);
+        if (len == T) {
+            // full chunk: 4 steps per group from 16-byte shared loads
+#pragma unroll 2
+            for (int j4 = 0; j4 < T / 4; ++j4) {
+                const float4 d4 = *(const float4 *)&sD[ch][4 * j4];
+                const float4 u4 = *(const float4 *)&sU[ch][4 * j4];
+                const float4 b4 = *(const float4 *)&sBt[n][4 * j4];
+                const float dv[4] = {d4.x, d4.y, d4.z, d4.w}, uv[4] = {u4.x, u4.y, u4.z, u4.w};
+                const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    h = fmaf(ex2_approx(dv[k] * A2), h, dv[k] * bv[k] * uv[k]);
+            }
+        } else {
+            for (int j = 0; j < len; ++j) {
+                const float dl = sD[ch][j];
+                h = fmaf(ex2_approx(dl * A2), h, dl * sBt[n][j] * sU[ch][j]);
+            }
         }
         __syncthreads();
     }
