@@ -105,19 +105,22 @@ struct BiParams {
 // B, C: [Bt, K, N, L] (K = 1 for the sequence forms).  For direction k,
 // batch b and position t: out[((k * Bt + b) * L + t) * 2NM + j] = B[b,k,j,t]
 // (j < NM), C[b,k,j-NM,t] (j >= NM); 0 for state indices >= N.
-// Block: 64 positions of one (b, k), 256 threads; block (0,0,0) also clears
-// the status word so that the scan kernel of the same call can set it.
+// Block: pack_pt<NM>() positions of one (b, k) (256 for 16 states, 128 for
+// 32: 8192 values, 32 loads per thread in flight), 256 threads; block
+// (0,0,0) also clears the status word so that the scan kernel of the same
+// call can set it.
 // With Bm1 given, grid z = 2 packs two separate sets (v2's two branches) in
 // one launch: z = 0 the first (Bm, Cm -> out), z = 1 the second (Bm1, Cm1 ->
 // out1), each with K = 1.
+template <int NM> __host__ __device__ constexpr int pack_pt() { return 8192 / (2 * NM); }
 template <typename IO, int NM>
 __global__ void __launch_bounds__(256)
 pack_bc_kernel(const IO *__restrict__ Bm, const IO *__restrict__ Cm, float *__restrict__ out,
                int N, int L, unsigned *status, const IO *__restrict__ Bm1 = nullptr,
                const IO *__restrict__ Cm1 = nullptr, float *__restrict__ out1 = nullptr) {
-    constexpr int kBC = 2 * NM;
-    __shared__ float tile[kBC][65];
-    const int b = blockIdx.y, t0 = blockIdx.x * 64;
+    constexpr int kBC = 2 * NM, PT = pack_pt<NM>();
+    __shared__ float tile[kBC][PT + 1];
+    const int b = blockIdx.y, t0 = blockIdx.x * PT;
     int k = blockIdx.z, K = gridDim.z;
     const int Bt = gridDim.y;
     if (status != nullptr && blockIdx.x == 0 && b == 0 && blockIdx.z == 0 && threadIdx.x == 0)
@@ -131,17 +134,24 @@ pack_bc_kernel(const IO *__restrict__ Bm, const IO *__restrict__ Cm, float *__re
         k = 0;
         K = 1;
     }
-    for (int i = threadIdx.x; i < kBC * 64; i += 256) {
-        const int j = i >> 6, tt = i & 63, t = t0 + tt, n = j & (NM - 1);
-        float v = 0.f;
+    float v[kBC * PT / 256];
+#pragma unroll
+    for (int r = 0; r < kBC * PT / 256; ++r) {
+        const int i = threadIdx.x + r * 256, j = i / PT, tt = i % PT, t = t0 + tt;
+        const int n = j & (NM - 1);
+        v[r] = 0.f;
         if (t < L && n < N) {
             const IO *src = j < NM ? Bm : Cm;
-            v = to_f32(src[(((long long)b * K + k) * N + n) * L + t]);
+            v[r] = to_f32(src[(((long long)b * K + k) * N + n) * L + t]);
         }
-        tile[j][tt] = v;
+    }
+#pragma unroll
+    for (int r = 0; r < kBC * PT / 256; ++r) {
+        const int i = threadIdx.x + r * 256;
+        tile[i / PT][i % PT] = v[r];
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < 64 * kBC; i += 256) {
+    for (int i = threadIdx.x; i < PT * kBC; i += 256) {
         const int tt = i / kBC, j = i % kBC, t = t0 + tt;
         if (t < L) out[(((long long)k * Bt + b) * L + t) * kBC + j] = tile[j][tt];
     }

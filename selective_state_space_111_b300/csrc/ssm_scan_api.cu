@@ -89,7 +89,8 @@ BiWs bi_ws(int bc_sets, int ndir, int B, int D, int L, int nm) {
 template <typename IO, int NM>
 ssm_status launch_pack(const void *Bm, const void *Cm, float *out, int B, int N, int L,
                        unsigned *status, cudaStream_t st, int K = 1) {
-    dim3 grid((L + 63) / 64, B, K);
+    constexpr int PT = ssm::pack_pt<NM>();
+    dim3 grid((L + PT - 1) / PT, B, K);
     ssm::pack_bc_kernel<IO, NM><<<grid, 256, 0, st>>>((const IO *)Bm, (const IO *)Cm, out, N, L,
                                                   status);
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
@@ -180,7 +181,8 @@ ssm_status run_bidir_nm(ssm::BiParams P, const void *Bm, const void *Cm, const v
     ssm_status s;
     if (two_sets) {
         // both branches' B/C sets in one launch (grid z = 2)
-        ssm::pack_bc_kernel<IO, NM><<<dim3((P.L + 63) / 64, P.B, 2), 256, 0, st>>>(
+        constexpr int PT = ssm::pack_pt<NM>();
+        ssm::pack_bc_kernel<IO, NM><<<dim3((P.L + PT - 1) / PT, P.B, 2), 256, 0, st>>>(
             (const IO *)Bm, (const IO *)Cm, const_cast<float *>(P.br[0].bc), P.N, P.L, P.status,
             (const IO *)Bm_b, (const IO *)Cm_b, const_cast<float *>(P.br[1].bc));
         s = cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
