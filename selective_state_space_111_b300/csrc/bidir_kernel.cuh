@@ -185,8 +185,9 @@ transpose_maps_kernel(const E *__restrict__ in, E *__restrict__ out, int maps, i
 // memory (R x (C + 1) elements, at most 48 KB): a CTA takes whole maps, so a
 // map is read and written as one contiguous run (warp w, lane l: rows
 // w, w + 8, ... in, columns w, w + 8, ... out; the padded row keeps the
-// column reads free of bank conflicts).
-template <typename E>
+// column reads free of bank conflicts).  SMALL (R, C <= 64): the loads are
+// unrolled so that all of a thread's are in flight at once.
+template <typename E, bool SMALL>
 __global__ void __launch_bounds__(256)
 transpose_whole_maps_kernel(const E *__restrict__ in, E *__restrict__ out, int maps, int R,
                             int C) {
@@ -196,8 +197,29 @@ transpose_whole_maps_kernel(const E *__restrict__ in, E *__restrict__ out, int m
     for (int m = blockIdx.x; m < maps; m += gridDim.x) {
         const E *src = in + (long long)m * R * C;
         E *dst = out + (long long)m * R * C;
-        for (int r = warp; r < R; r += 8)
-            for (int c = lane; c < C; c += 32) tile[r * (C + 1) + c] = src[(long long)r * C + c];
+        if constexpr (SMALL) {
+            // R, C <= 64: a thread's 16 elements, every load in flight
+            // before the shared stores
+            E v[8][2];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int r = warp + 8 * k, c = lane + 32 * q;
+                    if (r < R && c < C) v[k][q] = src[r * C + c];
+                }
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int r = warp + 8 * k, c = lane + 32 * q;
+                    if (r < R && c < C) tile[r * (C + 1) + c] = v[k][q];
+                }
+        } else {
+            for (int r = warp; r < R; r += 8)
+                for (int c = lane; c < C; c += 32)
+                    tile[r * (C + 1) + c] = src[(long long)r * C + c];
+        }
         __syncthreads();
         for (int c = warp; c < C; c += 8)
             for (int r = lane; r < R; r += 32) dst[(long long)c * R + r] = tile[r * (C + 1) + c];

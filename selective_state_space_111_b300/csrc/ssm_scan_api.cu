@@ -288,7 +288,12 @@ ssm_status launch_transpose(const E *in, E *out, int maps, int R, int C, cudaStr
     if (whole <= 48 * 1024) {
         // whole maps per CTA: each map one contiguous read and write
         const int grid = maps < 65535 ? maps : 65535;
-        ssm::transpose_whole_maps_kernel<E><<<grid, 256, whole, st>>>(in, out, maps, R, C);
+        if (R <= 64 && C <= 64)
+            ssm::transpose_whole_maps_kernel<E, true><<<grid, 256, whole, st>>>(in, out, maps, R,
+                                                                                C);
+        else
+            ssm::transpose_whole_maps_kernel<E, false><<<grid, 256, whole, st>>>(in, out, maps, R,
+                                                                                 C);
     } else {
         dim3 grid((C + 31) / 32, (R + 31) / 32, maps < 65535 ? maps : 65535);
         ssm::transpose_maps_kernel<E><<<grid, 256, 0, st>>>(in, out, maps, R, C);
