@@ -102,7 +102,9 @@ conv_silu_kernel(const IO *__restrict__ x, const float *__restrict__ w,
 // zero outside the map, act = SiLU or identity.  A CTA covers RB rows of
 // one channel's map: it stages rows h0-P .. h0+RB+P-1, zero-padded by P
 // columns on the left and to the row stride WS on the right, in shared
-// memory (warp by warp along the rows: coalesced).  KC = 3 (compile time):
+// memory (warp by warp along the rows: coalesced; for rows of at most 64
+// values eight rows per warp at a time, every load in flight).  KC = 3
+// (compile time):
 // a thread makes 4 consecutive outputs of a row from a 3 x 8 window read
 // with six 16-byte shared loads (WS is a multiple of 4 floats); KC = 0
 // (any odd Kc <= 7): warp r makes rows r, r + 8, ... one output per lane.
@@ -120,21 +122,46 @@ conv2d_act_kernel(const IO *__restrict__ x, const float *__restrict__ w,
     const int rb = min(RB, H - h0);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const IO *xm = x + ((long long)b * D + d) * H * W;
-    for (int r = warp; r < rb + 2 * P; r += 8) {
-        const int h = h0 - P + r;
-        const bool hin = h >= 0 && h < H;
-        const IO *xr = xm + (long long)(hin ? h : 0) * W;
-        float *dst = c2_smem + r * WS;
-        for (int c0 = lane; c0 < WS; c0 += 64) {
-            float v[2];
+    if (WS <= 64) {
+        // rows of at most 64: eight rows per warp at a time, all 16 loads of
+        // a lane in flight before the shared stores
+        for (int r0 = warp; r0 < rb + 2 * P; r0 += 64) {
+            float v[8][2];
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const int ww = c0 + 32 * q - P;
-                v[q] = (hin && ww >= 0 && ww < W) ? to_f32(xr[ww]) : 0.f;
+            for (int k = 0; k < 8; ++k) {
+                const int r = r0 + 8 * k, h = h0 - P + r;
+                const bool hin = r < rb + 2 * P && h >= 0 && h < H;
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int ww = lane + 32 * q - P;
+                    v[k][q] = (hin && ww >= 0 && ww < W) ? to_f32(xm[(long long)h * W + ww]) : 0.f;
+                }
             }
 #pragma unroll
-            for (int q = 0; q < 2; ++q)
-                if (c0 + 32 * q < WS) dst[c0 + 32 * q] = v[q];
+            for (int k = 0; k < 8; ++k) {
+                const int r = r0 + 8 * k;
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+                    if (r < rb + 2 * P && lane + 32 * q < WS) c2_smem[r * WS + lane + 32 * q] = v[k][q];
+            }
+        }
+    } else {
+        for (int r = warp; r < rb + 2 * P; r += 8) {
+            const int h = h0 - P + r;
+            const bool hin = h >= 0 && h < H;
+            const IO *xr = xm + (long long)(hin ? h : 0) * W;
+            float *dst = c2_smem + r * WS;
+            for (int c0 = lane; c0 < WS; c0 += 64) {
+                float v[2];
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int ww = c0 + 32 * q - P;
+                    v[q] = (hin && ww >= 0 && ww < W) ? to_f32(xr[ww]) : 0.f;
+                }
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+                    if (c0 + 32 * q < WS) dst[c0 + 32 * q] = v[q];
+            }
         }
     }
     constexpr int KM = KC > 0 ? KC : 7;
