@@ -39,8 +39,13 @@
  *    by ssm_get_status.  Two calls in flight at once must not share a
  *    workspace.
  *  - Calls are asynchronous on `stream` (0 = the legacy default stream).
- *    The library allocates nothing and keeps no global state, except the
- *    fixed scratch array that bimamba_scan_fwd_v2_noalloc uses.
+ *    The library allocates nothing.  Its only state outside the caller's
+ *    buffers is the fixed scratch array that bimamba_scan_fwd_v2_noalloc
+ *    uses and three per-host-thread settings, each changed only by its own
+ *    setter and applying to later calls made on that host thread: the
+ *    profiling events (ssm_set_profile_events), the CTA-shape override
+ *    (ssm_set_cta_channels) and the one-launch failure-test hook
+ *    (ssm_test_withhold_copy).
  *  - Errors: SSM_ERR_INVALID_ARG for a bad size, NULL required pointer or
  *    misaligned pointer; SSM_ERR_UNSUPPORTED for N > 32, K != 4 or sizes
  *    beyond the 32-bit index range; SSM_ERR_WORKSPACE when ws_bytes is too
@@ -252,11 +257,18 @@ SSM_API size_t ssm_workspace_bytes(ssm_op op, ssm_dtype dt, int B, int D,
  * Arguments, layouts, results and errors are those of bimamba_scan_fwd_v2,
  * without `workspace` / `ws_bytes`.  Instead of a caller workspace, the call
  * uses a scratch array of SSM_STATIC_SCRATCH_BYTES bytes that the library
- * declares as a file-scope __device__ array, so every GPU that loads the
- * library holds those bytes until the process exits.
- *  - Problems whose workspace (ssm_workspace_bytes(SSM_OP_BIMAMBA_V2, ...))
- *    exceeds SSM_STATIC_SCRATCH_BYTES return SSM_ERR_SCRATCH_LIMIT before
- *    anything runs.
+ * declares as a file-scope static __device__ array, so every GPU that loads
+ * the library holds those bytes until the process exits.
+ *  - Argument errors (SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED) are checked
+ *    first; then problems whose workspace (ssm_workspace_bytes(
+ *    SSM_OP_BIMAMBA_V2, ...)) exceeds SSM_STATIC_SCRATCH_BYTES return
+ *    SSM_ERR_SCRATCH_LIMIT before anything runs.
+ *  - The status word that ssm_get_status reads for the other calls lives in
+ *    the scratch array here, which the caller cannot address: a bounded wait
+ *    that runs out inside this call (SSM_ERR_TIMEOUT for the other calls)
+ *    is not observable through this entry point.  The call still returns,
+ *    the device stays usable and the next call runs normally, but the
+ *    output of the timed-out call is incomplete.
  *  - The first call on a device (the one current on the calling thread,
  *    which must be the device `stream` belongs to) looks up the array's
  *    device address, once; make that first call before any stream capture.

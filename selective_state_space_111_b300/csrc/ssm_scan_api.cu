@@ -15,6 +15,11 @@
 #include "bidir_kernel.cuh"
 #include "ssm_scan.h"
 
+// Scratch of bimamba_scan_fwd_v2_noalloc: a fixed device array of the
+// library's image (internal linkage), held by every GPU that loads the
+// library until the process exits.
+static __device__ __align__(256) unsigned char g_static_scratch[SSM_STATIC_SCRATCH_BYTES];
+
 namespace {
 
 bool aligned(const void *p, unsigned a) { return ((uintptr_t)p % a) == 0; }
@@ -377,12 +382,12 @@ ssm_status ss2d_run(int B, int D, int H, int W, int N, const void *x, const void
 }
 
 // ---- fixed scratch of the allocation-free entry point
-// The array lives in the library's device image; in host code its name is
-// only a host-side stand-in, so the kernel is given the device address that
-// cudaGetSymbolAddress reports for the current device (looked up once per
-// device, on that device's first call).
+// The array itself (g_static_scratch) is declared at file scope above this
+// namespace; in host code its name is only a host-side stand-in, so the
+// kernel is given the device address that cudaGetSymbolAddress reports for
+// the current device (looked up once per device, on that device's first
+// call).
 constexpr int kMaxDevices = 256;
-__device__ __align__(256) unsigned char g_static_scratch[SSM_STATIC_SCRATCH_BYTES];
 std::mutex g_scratch_mutex;
 void *g_scratch_addr[kMaxDevices];
 
@@ -576,6 +581,13 @@ ssm_status bimamba_scan_fwd_v2_noalloc(ssm_dtype dt, int B, int D, int L, int N,
                                        float out_scale, void *y, ssm_stream_t stream) {
     ssm_status s = check_common(dt, B, D, L, N);
     if (s != SSM_OK) return s;
+    // argument errors are reported before the scratch limit
+    if (!io_ok(dt, u) || !opt_io_ok(dt, u_b) || !io_ok(dt, delta) || !io_ok(dt, delta_b) ||
+        !io_ok(dt, Bm) || !io_ok(dt, Cm) || !io_ok(dt, Bm_b) || !io_ok(dt, Cm_b) ||
+        !opt_io_ok(dt, z) || !io_ok(dt, y) || !f32_ok(A) || !f32_ok(A_b) ||
+        !opt_f32_ok(Dskip) || !opt_f32_ok(D_b) || !opt_f32_ok(delta_bias) ||
+        !opt_f32_ok(delta_bias_b))
+        return SSM_ERR_INVALID_ARG;
     if (bi_ws(2, 2, B, D, L, nm_of(N)).total > SSM_STATIC_SCRATCH_BYTES)
         return SSM_ERR_SCRATCH_LIMIT;
     void *scratch = nullptr;

@@ -190,3 +190,52 @@ def test_bwd_workload_sampled_rows(name, nrows):
         ref = run_bwd_oracle(spec, ts, dout[b:b + 1, d:d + 1])
         sub = {k: gpu[k][b:b + 1, d:d + 1] for k in ("du", "ddelta", "ddelta_b", "dz")}
         compare(sub, {k: ref[k] for k in sub}, spec.io)
+
+
+def _channel_rows(spec, t, d):
+    """Inputs of every batch element's rows of channel d (B x 1 rows, B/C
+    whole): the parameter gradients of channel d sum over exactly these."""
+    s = {}
+    for k, v in t.items():
+        if not isinstance(v, torch.Tensor):
+            s[k] = v
+        elif k in ("u", "u_b", "delta", "delta_b", "z"):
+            s[k] = v[:, d:d + 1]
+        elif k in ("A", "A_b", "D", "D_b", "delta_bias", "delta_bias_b"):
+            s[k] = v[d:d + 1]
+        else:
+            s[k] = v
+    return s
+
+
+def _batch_rows(spec, t, b):
+    """Inputs of batch element b (all channels): dB and dC of b sum over
+    exactly these rows."""
+    return {k: (v[b:b + 1] if isinstance(v, torch.Tensor) and
+                k in ("u", "u_b", "delta", "delta_b", "z", "B", "C", "B_b", "C_b") else v)
+            for k, v in t.items()}
+
+
+@pytest.mark.slow
+def test_bwd_workload_parameter_gradients():
+    # Vim-S 1248^2 v2 at full size: dA, dD and ddelta_bias of sampled
+    # channels (each a sum over that channel's rows of every batch element)
+    # and dB, dC of the last batch element (a sum over its 768 channels),
+    # each against the oracle run on exactly the rows it sums over
+    name = "vim_s_1248_bimamba_v2"
+    spec = WORKLOADS[name]
+    seed = seed_for(name)
+    t = make_inputs(spec, seed)
+    dout = _dout(spec, t, seed + 1)
+    gpu = run_bwd_gpu(spec, t, dout)
+    rng = np.random.default_rng(seed + 2)
+    chans = sorted({0, spec.D - 1, *[int(c) for c in rng.integers(spec.D, size=4)]})
+    per_channel = ("dA", "dA_b", "dD", "dD_b", "ddelta_bias", "ddelta_bias_b")
+    for d in chans:
+        ref = run_bwd_oracle(spec, _channel_rows(spec, t, d), dout[:, d:d + 1])
+        compare({k: gpu[k][d:d + 1] for k in per_channel}, {k: ref[k] for k in per_channel},
+                spec.io)
+    b = spec.B - 1
+    ref = run_bwd_oracle(spec, _batch_rows(spec, t, b), dout[b:b + 1])
+    per_batch = ("dB", "dC", "dB_b", "dC_b")
+    compare({k: gpu[k][b:b + 1] for k in per_batch}, {k: ref[k] for k in per_batch}, spec.io)

@@ -1,7 +1,10 @@
 """Failure detection without a GPU fault: every wait in the scan kernel is
 bounded.  The test hook ssm_test_withhold_copy makes the kernel skip one
 chunk's B/C bulk copy, so the scan's wait for it runs out; the kernel must
-stop, set the workspace status word, and leave the context usable."""
+stop, set the workspace status word, and leave the context usable.  The
+allocation-free entry point runs the same kernel on its fixed scratch: its
+status word is not observable, but the call must return and the next call
+must run normally."""
 import numpy as np
 import pytest
 import torch
@@ -45,3 +48,30 @@ def test_withheld_copy_times_out_and_context_stays_usable(ssm):
     ref = run_oracle(spec, t)
     assert max_scaled_err(y, ref) <= TOL["bf16"]
     assert torch.cuda.is_available() and np.isfinite(y.float().sum().item())
+
+
+def test_withheld_copy_in_allocation_free_call_returns(ssm):
+    import ctypes
+    from selective_state_space_111_b300 import binding
+    lib = binding.lib()
+    spec = Spec("v2", "bf16", B=1, D=16, L=300, perturb=True, out_scale=0.5)
+    t = make_inputs(spec, 32)
+    g = to_dev(t)
+    stream = torch.cuda.current_stream().cuda_stream
+
+    def call(y):
+        p = lambda v: None if v is None else v.data_ptr()
+        return lib.bimamba_scan_fwd_v2_noalloc(
+            1, 1, 16, 300, 16, p(g["u"]), p(g["u_b"]), p(g["delta"]), p(g["delta_b"]),
+            p(g["A"]), p(g["A_b"]), p(g["B"]), p(g["C"]), p(g["B_b"]), p(g["C_b"]), p(g["D"]),
+            p(g["D_b"]), p(g["z"]), p(g["delta_bias"]), p(g["delta_bias_b"]), 1,
+            ctypes.c_float(0.5), y.data_ptr(), stream)
+
+    lib.ssm_test_withhold_copy(3)                       # chunk 3 of 10 never arrives
+    y = torch.empty_like(g["u"])
+    assert call(y) == 0
+    torch.cuda.synchronize()                            # returns: the waits are bounded
+    y = torch.empty_like(g["u"])
+    assert call(y) == 0                                 # hook cleared: a normal call
+    torch.cuda.synchronize()
+    assert max_scaled_err(y, run_oracle(spec, t)) <= TOL["bf16"]

@@ -1,14 +1,23 @@
 """GPU parity of the prologue (conv1d + SiLU, x_proj split, dt_proj) against
 the fp64 prologue oracle, and of the whole v2 inner path (prologue of each
 branch, the backward one on the flipped input, then the scan-order v2
-scan) against the oracle chain.
+scan), link by link.
 
-Tolerances: u element by element, |gpu - ref| <= tol * (1 + |ref|); dt, B,
-C (dot products of length D or R over u, which the GPU reads in the I/O
-dtype) against their own scale, max|gpu - ref| <= tol2 * (1 + max|ref|);
-tol = 1e-4 / 1e-2 / 5e-3 and tol2 = 5e-4 / 2e-2 / 1e-2 for fp32 / bf16 / fp16
-I/O (the 16-bit paths round u, dt, B, C to the I/O type and run dt_proj
-on tf32 operands).
+Tolerances, element by element.  u: |gpu - ref| <= tol * (1 + |ref|), tol
+= 1e-4 / 1e-2 / 5e-3 for fp32 / bf16 / fp16 I/O.  dt, B and C are dot
+products of rounded operands, so their rounding error scales with the sum
+of the terms' magnitudes, not with the (possibly cancelling) result: each
+element is held to |gpu - ref| <= tol_el * (1 + S), where S = sum_k
+|W[m,k] * u[k,t]| for the rows of B and C, and S = sum_r |W_dt[d,r]| *
+sum_k |W_x[r,k] * u[k,t]| for dt (the bound of its two-stage sum).  tol_el
+= 1e-4 / 1e-2 / 5e-3: bf16 operands carry 2^-9 relative rounding each (W
+and u: 2^-8 per product), the tf32 dt_proj 2^-11 per operand and the bf16
+output 2^-9, which sum to below 7e-3 * S; fp16 to below 2.5e-3 * S; fp32
+accumulation over K <= 1400 terms to below 1e-4 * S.
+
+Full-size cases run the persistent x_proj kernels with several tiles per
+CTA (Vim-S 1248^2 and a longer sequence for the 1D prologue, VMamba 56x56
+for SS2D), checked over every element.
 """
 import numpy as np
 import pytest
@@ -21,7 +30,7 @@ pytestmark = pytest.mark.gpu
 
 DT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
 TOL = {"f32": 1e-4, "bf16": 1e-2, "f16": 5e-3}
-TOL2 = {"f32": 5e-4, "bf16": 2e-2, "f16": 1e-2}
+TOL_EL = {"f32": 1e-4, "bf16": 1e-2, "f16": 5e-3}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -45,9 +54,52 @@ def seq_err(a, r):
     return float(np.max(np.abs(a - r) / (1 + np.abs(r)))) if r.size else 0.0
 
 
-def scale_err(a, r):
-    a = a.double().cpu().numpy() if hasattr(a, "cpu") else a
-    return float(np.max(np.abs(a - r)) / (1 + np.max(np.abs(r)))) if r.size else 0.0
+def _np(a):
+    return a.double().cpu().numpy() if hasattr(a, "cpu") else np.asarray(a, dtype=np.float64)
+
+
+def proj_bounds(W_x, W_dt, u, R, N):
+    """(S_dt, S_B, S_C): per-element sums of the terms' magnitudes of the
+    two projections, from the oracle's u [B, D, L] (fp64)."""
+    Wx, Wdt = np.abs(_np(W_x)), np.abs(_np(W_dt))
+    S = np.einsum("mk,bkl->bml", Wx, np.abs(u))
+    return np.einsum("dr,brl->bdl", Wdt, S[:, :R]), S[:, R:R + N], S[:, R + N:R + 2 * N]
+
+
+def elem_err(a, r, S):
+    """max over elements of |a - r| / (1 + S)."""
+    a = _np(a)
+    assert a.shape == r.shape == S.shape, (a.shape, r.shape, S.shape)
+    return float(np.max(np.abs(a - r) / (1.0 + S))) if r.size else 0.0
+
+
+def check_prologue(io, got, ref, w, R, N):
+    """u element by element; dt, B, C against their per-element bounds."""
+    u, dt, Bm, Cm = got
+    ru, rdt, rB, rC = ref
+    assert seq_err(u, ru) <= TOL[io], seq_err(u, ru)
+    Sdt, SB, SC = proj_bounds(w["W_x"], w["W_dt"], ru, R, N)
+    for name, a, r, S in (("dt", dt, rdt, Sdt), ("B", Bm, rB, SB), ("C", Cm, rC, SC)):
+        e = elem_err(a, r, S)
+        assert np.isfinite(e) and e <= TOL_EL[io], "%s: %.3g" % (name, e)
+
+
+def check_ss2d_prologue(io, got, ref, w, R, N, H, W):
+    """The four directions' projections against their per-element bounds
+    (each direction's sequence is u in its own scan order)."""
+    u, delta, Bm, Cm = got
+    ru, rdelta, rB, rC = ref
+    assert seq_err(u, ru) <= TOL[io], seq_err(u, ru)
+    Bn, Dn = ru.shape[:2]
+    uf = ru.reshape(Bn, Dn, H * W)
+    dl, Bg, Cg = _np(delta), _np(Bm), _np(Cm)
+    for k in range(4):
+        xs = uf[..., oracle.cross_scan_index(H, W, k)]
+        Sdt, SB, SC = proj_bounds(w["W_x"][k], w["W_dt"][k], xs, R, N)
+        for name, a, r, S in (("delta", dl[:, k], rdelta[:, k], Sdt), ("B", Bg[:, k], rB[:, k], SB),
+                              ("C", Cg[:, k], rC[:, k], SC)):
+            e = elem_err(a, r, S)
+            assert np.isfinite(e) and e <= TOL_EL[io], "direction %d %s: %.3g" % (k, name, e)
 
 
 # (B, D, L, N, R, K); D = 1400: W_x past shared memory, the generic tiled
@@ -70,18 +122,38 @@ def test_prologue_matches_oracle(io, reverse, shape):
     u, dt, Bm, Cm = ssm.mamba_prologue_fwd(x.cuda(), wg["conv_w"], wg["conv_b"], wg["W_x"],
                                            wg["W_dt"], R, N, reverse=reverse)
     torch.cuda.synchronize()
-    ru, rdt, rB, rC = pro.prologue(x, w["conv_w"], w["conv_b"], w["W_x"], w["W_dt"], R, N,
-                                   reverse=reverse)
-    assert seq_err(u, ru) <= TOL[io]
-    for a, r in ((dt, rdt), (Bm, rB), (Cm, rC)):
-        assert scale_err(a, r) <= TOL2[io], scale_err(a, r)
+    ref = pro.prologue(x, w["conv_w"], w["conv_b"], w["W_x"], w["W_dt"], R, N, reverse=reverse)
+    check_prologue(io, (u, dt, Bm, Cm), ref, w, R, N)
+
+
+# Full size: B * ceil(L / 128) tiles of 128 positions on one persistent CTA
+# per SM -- Vim-S 1248^2 (384 tiles: two or three per CTA, a 69-position
+# tail) and a longer sequence (504 tiles: three or four per CTA, a
+# 1-position tail)
+FULL = [(8, 768, 6085, 16, 24, 4), (4, 128, 16001, 16, 8, 4)]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("reverse", [False, True])
+@pytest.mark.parametrize("shape", FULL)
+def test_prologue_full_size_multi_tile(shape, reverse):
+    import selective_state_space_111_b300 as ssm
+    B, D, L, N, R, K = shape
+    g = torch.Generator().manual_seed(L + 3 * reverse)
+    x = torch.randn(B, D, L, generator=g).to(torch.bfloat16)
+    w = weights(g, D, R, N, K)
+    wg = {k: v.cuda() for k, v in w.items()}
+    got = ssm.mamba_prologue_fwd(x.cuda(), wg["conv_w"], wg["conv_b"], wg["W_x"], wg["W_dt"], R,
+                                 N, reverse=reverse)
+    torch.cuda.synchronize()
+    ref = pro.prologue(x, w["conv_w"], w["conv_b"], w["W_x"], w["W_dt"], R, N, reverse=reverse)
+    check_prologue("bf16", got, ref, w, R, N)
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
 def test_v2_inner_path_from_x(io):
     # prologue of each branch (the backward one on the flipped input, its
-    # outputs in scan order) -> bimamba_scan_fwd_v2 with scan_order=True,
-    # against the oracle chain in position order
+    # outputs in scan order) -> bimamba_scan_fwd_v2 with scan_order=True
     import selective_state_space_111_b300 as ssm
     B, D, L, N, R, K = 2, 40, 150, 16, 6, 4
     g = torch.Generator().manual_seed(77)
@@ -103,19 +175,22 @@ def test_v2_inner_path_from_x(io):
                                 Db.cuda(), z.cuda(), bias.cuda(), bias_b.cuda(), ub, True, 0.5,
                                 scan_order=True)
     torch.cuda.synchronize()
-    # oracle chain: the GPU prologue outputs are what the scan consumed, so
-    # the scan is checked on them (position order) and the prologue above
-    ru, rdt, rB, rC = pro.prologue(x, wf["conv_w"], wf["conv_b"], wf["W_x"], wf["W_dt"], R, N)
-    rub, rdtb, rBb, rCb = pro.prologue(x, wb["conv_w"], wb["conv_b"], wb["W_x"], wb["W_dt"], R,
-                                       N, reverse=True)
-    flip = lambda a: a[..., ::-1]
-    ref_chain = oracle.bimamba_v2(ru, rdt, flip(rdtb), A, A_b, rB, rC, flip(rBb), flip(rCb), Dk,
-                                  Db, z, bias, bias_b, flip(rub), True, 0.5)
+    # link by link: each branch's prologue against the oracle prologue
+    # (per-element bounds), then the scan on the very tensors the prologues
+    # produced against the oracle scan on them.  The chain from x is the
+    # composition of these links; a direct comparison of y with the oracle
+    # chain has no per-element bound short of one that amplifies the
+    # prologue's accumulated rounding by the scan's sensitivity.
+    check_prologue(io, (u, dt, Bm, Cm),
+                   pro.prologue(x, wf["conv_w"], wf["conv_b"], wf["W_x"], wf["W_dt"], R, N),
+                   wf, R, N)
+    check_prologue(io, (ub, dtb, Bb, Cb),
+                   pro.prologue(x, wb["conv_w"], wb["conv_b"], wb["W_x"], wb["W_dt"], R, N,
+                                reverse=True), wb, R, N)
     ref_scan = oracle.bimamba_v2(u, dt, torch.flip(dtb, [-1]), A, A_b, Bm, Cm,
                                  torch.flip(Bb, [-1]), torch.flip(Cb, [-1]), Dk, Db, z, bias,
                                  bias_b, torch.flip(ub, [-1]), True, 0.5)
     assert seq_err(y, ref_scan) <= TOL[io]              # the scan on what it was given
-    assert scale_err(y, ref_chain) <= 2 * TOL2[io]      # the whole path from x
 
 
 # ---------------------------------------------------------------- SS2D
@@ -152,11 +227,25 @@ def test_ss2d_prologue_matches_oracle(io, shape):
     u, delta, Bm, Cm = ssm.ss2d_prologue_fwd(x.cuda(), wg["conv_w"], wg["conv_b"], wg["W_x"],
                                              wg["W_dt"], R, N, silu_act=act)
     torch.cuda.synchronize()
-    ru, rdelta, rB, rC = pro.ss2d_prologue(x, w["conv_w"], w["conv_b"], w["W_x"], w["W_dt"], R,
-                                           N, silu_act=act)
-    assert seq_err(u, ru) <= TOL[io]
-    for a, r in ((delta, rdelta), (Bm, rB), (Cm, rC)):
-        assert scale_err(a, r) <= TOL2[io], scale_err(a, r)
+    ref = pro.ss2d_prologue(x, w["conv_w"], w["conv_b"], w["W_x"], w["W_dt"], R, N,
+                            silu_act=act)
+    check_ss2d_prologue(io, (u, delta, Bm, Cm), ref, w, R, N, H, W)
+
+
+@pytest.mark.slow
+def test_ss2d_prologue_full_size_multi_tile():
+    # VMamba 56x56 (B 32, d_inner 192, dt_rank 6): 896 map tiles of 8 x 16
+    # on one persistent CTA per SM, six or seven per CTA, ragged in W
+    import selective_state_space_111_b300 as ssm
+    B, D, H, W, N, R, Kc = 32, 192, 56, 56, 16, 6, 3
+    g = torch.Generator().manual_seed(5656)
+    x = torch.randn(B, D, H, W, generator=g).to(torch.bfloat16)
+    w = ss2d_weights(g, D, R, N, Kc)
+    wg = {k: v.cuda() for k, v in w.items()}
+    got = ssm.ss2d_prologue_fwd(x.cuda(), wg["conv_w"], wg["conv_b"], wg["W_x"], wg["W_dt"], R, N)
+    torch.cuda.synchronize()
+    ref = pro.ss2d_prologue(x, w["conv_w"], w["conv_b"], w["W_x"], w["W_dt"], R, N)
+    check_ss2d_prologue("bf16", got, ref, w, R, N, H, W)
 
 
 def test_ss2d_prologue_without_activation_and_bias():
@@ -169,11 +258,8 @@ def test_ss2d_prologue_without_activation_and_bias():
     u, delta, Bm, Cm = ssm.ss2d_prologue_fwd(x.cuda(), wg["conv_w"], None, wg["W_x"], wg["W_dt"],
                                              R, N, silu_act=False)
     torch.cuda.synchronize()
-    ru, rdelta, rB, rC = pro.ss2d_prologue(x, w["conv_w"], None, w["W_x"], w["W_dt"], R, N,
-                                           silu_act=False)
-    assert seq_err(u, ru) <= TOL["f32"]
-    for a, r in ((delta, rdelta), (Bm, rB), (Cm, rC)):
-        assert scale_err(a, r) <= TOL2["f32"]
+    ref = pro.ss2d_prologue(x, w["conv_w"], None, w["W_x"], w["W_dt"], R, N, silu_act=False)
+    check_ss2d_prologue("f32", (u, delta, Bm, Cm), ref, w, R, N, H, W)
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
@@ -195,11 +281,12 @@ def test_ss2d_inner_path_from_x(io):
                                              wg["W_dt"], R, N)
     y = ssm.ss2d_scan_fwd(u, delta, A.cuda(), Bm, Cm, Dk.cuda(), z.cuda(), bias.cuda(), True)
     torch.cuda.synchronize()
-    ru, rdelta, rB, rC = pro.ss2d_prologue(x, w["conv_w"], w["conv_b"], w["W_x"], w["W_dt"], R, N)
-    ref_chain = oracle.ss2d(ru, rdelta, A, rB, rC, Dk, z, bias, True)
+    # link by link, as for the v2 path
+    check_ss2d_prologue(io, (u, delta, Bm, Cm),
+                        pro.ss2d_prologue(x, w["conv_w"], w["conv_b"], w["W_x"], w["W_dt"], R, N),
+                        w, R, N, H, W)
     ref_scan = oracle.ss2d(u, delta, A, Bm, Cm, Dk, z, bias, True)
     assert seq_err(y, ref_scan) <= TOL[io]              # the scan on what it was given
-    assert scale_err(y, ref_chain) <= 2 * TOL2[io]      # the whole path from x
 
 
 def test_prologue_outputs_off_the_4_byte_grid():
@@ -229,7 +316,5 @@ def test_prologue_outputs_off_the_4_byte_grid():
                                 torch.cuda.current_stream().cuda_stream)
     assert st == 0
     torch.cuda.synchronize()
-    ru, rdt, rB, rC = pro.prologue(x, w["conv_w"], w["conv_b"], w["W_x"], w["W_dt"], R, N)
-    assert seq_err(u, ru) <= TOL["bf16"]
-    for a, r in ((delta, rdt), (Bm, rB), (Cm, rC)):
-        assert scale_err(a, r) <= TOL2["bf16"]
+    ref = pro.prologue(x, w["conv_w"], w["conv_b"], w["W_x"], w["W_dt"], R, N)
+    check_prologue("bf16", (u, delta, Bm, Cm), ref, w, R, N)
