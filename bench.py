@@ -78,6 +78,25 @@ def measured_traffic(workload):
     return ent.get("dram_bytes_per_launch")
 
 
+def alu_rates():
+    """Lane operations per SM per clock of scalar FMA, packed FMA and MUFU
+    2^x on this GPU (the microbenchmark in csrc/alu_rates.cu), or None."""
+    import ctypes
+    try:
+        from selective_state_space_111_b300 import build
+        lib = ctypes.CDLL(build.build_alu())
+        out = (ctypes.c_double * 3)()
+        if lib.ssm_alu_rates(out) != 0:
+            return None
+    except (OSError, subprocess.CalledProcessError):
+        return None
+    r = {"ffma": round(out[0], 1), "ffma2": round(out[1], 1), "mufu_ex2": round(out[2], 1)}
+    # element updates per SM per clock each pipe allows: 4 FMA-pipe operations
+    # and one MUFU ex2 per update
+    r["updates_per_sm_clock"] = round(min(max(out[0], out[1]) / 4, out[2]), 2)
+    return r
+
+
 # ---------------------------------------------------------------- ranks
 def rank_env():
     """(world, rank, local_rank) from the torchrun environment (1, 0, 0 alone)."""
@@ -140,7 +159,7 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -215,32 +234,49 @@ def run_ours(args):
         if world > 1:
             dist.barrier()
 
-    sampler = ClockSampler(local)
-    sampler.start()
     for _ in range(args.warmup):
         call(ssm, spec, g, ws, out)
     torch.cuda.synchronize()
-    barrier()
-    torch.cuda.synchronize()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-    # the scan kernel's own launches, bracketed by the library's profiling hook
+
+    # The timed region: windows of exactly K steps, each bracketed by a
+    # barrier and a synchronize on both sides, repeated until the windows
+    # add up to at least --min-seconds of device time, with the SM clock and
+    # throttle reasons sampled throughout.  ms_per_step is the median
+    # window's; the scan kernel's own time comes from the library's
+    # profiling hook around each of its launches.
     kb = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ke = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     for e in kb + ke:
         e.record(stream)                  # creates the CUDA events
     torch.cuda.synchronize()
-    ev[0].record(stream)
-    for i in range(args.steps):
-        ssm.set_profile_events(kb[i], ke[i])
-        call(ssm, spec, g, ws, out)
-        ev[i + 1].record(stream)
-    ssm.set_profile_events(None, None)
-    torch.cuda.synchronize()
-    barrier()
-    torch.cuda.synchronize()
+
+    def window():
+        barrier()
+        torch.cuda.synchronize()
+        ev[0].record(stream)
+        for i in range(args.steps):
+            ssm.set_profile_events(kb[i], ke[i])
+            call(ssm, spec, g, ws, out)
+            ev[i + 1].record(stream)
+        ssm.set_profile_events(None, None)
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        return ev[0].elapsed_time(ev[-1]), [kb[i].elapsed_time(ke[i]) for i in range(args.steps)]
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.15)                      # the sampler's first reading
+    wins, kern = [], []
+    spent = 0.0
+    while not wins or (spent < args.min_seconds * 1e3 and len(wins) < 10000):
+        w_ms, k_ms = window()
+        wins.append(w_ms)
+        kern.extend(k_ms)
+        spent += w_ms
     clocks = sampler.stop()
-    kern = [kb[i].elapsed_time(ke[i]) for i in range(args.steps)]
-    total_ms = ev[0].elapsed_time(ev[-1])
+    total_ms = statistics.median(wins)
     total_ms = max_over_ranks(total_ms, world, dev)
 
     # e2e: host (pinned) inputs -> device -> the public API -> result to host,
@@ -320,6 +356,9 @@ def run_ours(args):
         # update (equal to the MUFU ex2 roof: 32 per SM per clock, one each)
         alu_peak = 148 * 32 * sm_max * 1e6 / 1e9          # Gupd/s
         alu_ach = upd_launch / (kern_ms * 1e-3) / 1e9
+        sm_run = clocks.get("sm_mhz") or sm_max           # the clock the kernel ran at
+        alu_peak_run = 148 * 32 * sm_run * 1e6 / 1e9
+        rates = alu_rates()
         line = {
             "metric": METRIC,
             "value": round(gbps, 2),
@@ -330,6 +369,10 @@ def run_ours(args):
             "steps": args.steps,
             "warmup": args.warmup,
             "ms_per_step": round(ms, 5),
+            "timed_windows": {"windows": len(wins), "steps_each": args.steps,
+                              "device_s": round(spent / 1e3, 3),
+                              "ms_per_step_min": round(min(wins) / args.steps, 5),
+                              "ms_per_step_max": round(max(wins) / args.steps, 5)},
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
@@ -346,6 +389,9 @@ def run_ours(args):
                          "kernel": "bidir_scan_kernel", "kernel_ms": round(kern_ms, 5),
                          "peak_basis": "148 SMs x 128 fp32 lanes x %.0f MHz / 4 fp32 ops per "
                                        "update (recipe unit counts and max clock)" % sm_max,
+                         "frac_at_sampled_clock": round(alu_ach / alu_peak_run, 4),
+                         "sampled_sm_mhz": sm_run,
+                         "alu_rates_per_sm_clock": rates,
                          "hbm_gbs_kernel": round(spec.algorithmic_bytes() / scans
                                                  / (kern_ms * 1e-3) / 1e9, 1),
                          "hbm_peak_gbs": hbm_peak, "hbm_peak_kind": peak_kind},
@@ -379,6 +425,8 @@ def run_ours(args):
             line["prologue"] = pro
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(spec, args.workload, args.cpu_seconds)
+            line["cpu_baseline_single_thread"] = cpu_baseline(spec, args.workload,
+                                                              args.cpu_seconds / 2, threads=1)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -521,7 +569,7 @@ class OracleSampler:
 
     SEQ_KEYS = ("u", "u_b", "delta", "delta_b", "z", "B", "C", "B_b", "C_b")
 
-    def __init__(self, spec, name, prefix=None):
+    def __init__(self, spec, name, prefix=None, threads=None):
         import numpy as np
 
         import oracle
@@ -531,7 +579,7 @@ class OracleSampler:
         self.spec, self.name = spec, name
         self.prefix = prefix if (prefix and spec.op != "ss2d" and prefix < spec.seq_len) else None
         self.row_slice, self.run_oracle = row_slice, run_oracle
-        self.cores = len(os.sched_getaffinity(0))
+        self.cores = threads or len(os.sched_getaffinity(0))
         self.t = make_inputs(spec, seed_for(name))
         oracle.build()
         rng = np.random.default_rng(0)
@@ -574,12 +622,13 @@ class OracleSampler:
         unit = ("row prefixes of %d positions" % self.prefix) if self.prefix else "whole rows"
         return {"value": round(done[0] * per_row_bytes / el / 1e9, 6), "unit": "GB/s",
                 "elem_updates_per_s": float("%.4g" % ups), "cores": cores, "kind": "oracle",
+                "seconds": round(el, 3),
                 "sample": "%d %s (all directions, L=%d) of %s in %.2f s, one per oracle call, "
                           "%d threads" % (done[0], unit, spec.seq_len, self.name, el, cores)}
 
 
-def cpu_baseline(spec, name, seconds):
-    return OracleSampler(spec, name).sample(seconds)
+def cpu_baseline(spec, name, seconds, threads=None):
+    return OracleSampler(spec, name, threads=threads).sample(seconds)
 
 
 def run_reference(args):
@@ -601,11 +650,17 @@ def run_reference(args):
             vals.append(cb)
     v = statistics.mean(c["value"] for c in vals)
     ups = statistics.mean(c["elem_updates_per_s"] for c in vals)
-    ms = spec.algorithmic_bytes() / (v * 1e9) * 1e3 if v > 0 else None
+    # each step is a bounded sample of the workload: its measured wall time
+    # is ms_per_step; the time the oracle would take for the whole workload
+    # is extrapolated from the sample's throughput and reported beside it
+    ms = statistics.mean(c["seconds"] for c in vals) * 1e3
+    ms_full = spec.algorithmic_bytes() / (v * 1e9) * 1e3 if v > 0 else None
     line = {"metric": METRIC, "value": v, "unit": "GB/s", "impl": "reference",
             "elem_updates_per_s": ups, "n_gpus": args.gpus, "host_only": True,
             "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "ms_per_step": round(ms, 3), "step_is": "a bounded sample of the workload",
+            "ms_whole_workload_extrapolated": round(ms_full, 1) if ms_full else None,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic (seeded)",
             "config": {"workload": args.workload, "op": spec.op, "batch": spec.B,
                        "d_inner": spec.D, "d_state": spec.N, "seq_len": spec.seq_len},
@@ -632,11 +687,22 @@ def main():
     ap.add_argument("--no-prologue", action="store_true",
                     help="skip the prologue timing (reported under 'prologue')")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--min-seconds", type=float, default=1.5,
+                    help="repeat the K-step timed window until this much device time "
+                         "has passed, sampling the clocks throughout")
+    ap.add_argument("--alu-rates", action="store_true",
+                    help="print the FMA / packed FMA / MUFU ex2 rates per SM per clock and exit")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.alu_rates:
+        import torch
+        torch.cuda.init()
+        print(json.dumps({"alu_rates_per_sm_clock": alu_rates(),
+                          "gpu": torch.cuda.get_device_name(0)}), flush=True)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -7,6 +7,10 @@ and csrc/ssm_prologue_api.cu (prologue), which include their kernel headers,
 into one shared library with the CUDA runtime linked statically, so the .so loads on a
 machine without a GPU as well (for symbol checks) and needs nothing from the
 environment at run time beyond the NVIDIA driver.
+
+build_alu() compiles csrc/alu_rates.cu, the benchmark's throughput
+microbenchmark of the update's instruction kinds, into its own small
+libssm_alu.so (never loaded by the library or the tests).
 """
 import os
 import subprocess
@@ -22,6 +26,8 @@ DEPS = SOURCES + [os.path.join(HERE, "csrc", f) for f in
                    "scan_ops.cuh")] + [
                   os.path.join(ROOT, "include", "ssm_scan.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+ALU_LIB = os.path.join(HERE, "libssm_alu.so")
+ALU_SRC = os.path.join(HERE, "csrc", "alu_rates.cu")
 
 
 def nvcc():
@@ -51,6 +57,18 @@ def build(force=False, verbose=False, extra=()):
     return LIB
 
 
+def build_alu(force=False):
+    if not force and os.path.exists(ALU_LIB) and os.path.getmtime(ALU_LIB) >= os.path.getmtime(ALU_SRC):
+        return ALU_LIB
+    tmp = ALU_LIB + ".tmp%d" % os.getpid()
+    subprocess.check_call([nvcc(), *ARCH, "-O3", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
+                           "-Xcompiler", "-fvisibility=hidden", "-cudart", "static", "-o", tmp,
+                           ALU_SRC])
+    os.replace(tmp, ALU_LIB)
+    return ALU_LIB
+
+
 if __name__ == "__main__":
     build(force="--force" in sys.argv, verbose="-v" in sys.argv)
+    build_alu(force="--force" in sys.argv)
     print(LIB)

@@ -465,12 +465,14 @@ bidir_scan_kernel(const BiParams P) {
 #pragma unroll
                 for (int jj = 0; jj < UB; ++jj) put(j0 + jj, ys[jj]);
             };
-            // one step (the chunk's tail)
+            // one step (the chunk's tail); the readout is summed in the
+            // block's order (even and odd state pairs apart, then together),
+            // so every step of every path rounds alike
             auto step = [&](int j) {
                 const float4 v = *(const float4 *)(dwp + j * 16);
                 const f2 dd = pk(v.x, v.y), ww = pk(v.z, v.w);
                 const float *bj = bcp + j * bstep;
-                f2 y2;
+                f2 ya = pk(0.f, 0.f), yb = pk(0.f, 0.f);
 #pragma unroll
                 for (int q = 0; q < NP; ++q) {
                     const float2 vb = *(const float2 *)(bj + 2 * q);
@@ -479,10 +481,11 @@ bidir_scan_kernel(const BiParams P) {
                     upk(mul2(dd, A2[q]), a0, a1);
                     const f2 ee = pk(ex2_approx(a0), ex2_approx(a1));
                     h[q] = fma2(ee, h[q], mul2(pk(vb.x, vb.y), ww));
-                    y2 = (q == 0) ? mul2(pk(vc.x, vc.y), h[q]) : fma2(pk(vc.x, vc.y), h[q], y2);
+                    if (q & 1) yb = fma2(pk(vc.x, vc.y), h[q], yb);
+                    else ya = fma2(pk(vc.x, vc.y), h[q], ya);
                 }
                 float ylo, yhi;
-                upk(y2, ylo, yhi);
+                upk(NP > 1 ? add2(ya, yb) : ya, ylo, yhi);
                 put(j, ylo + yhi);
             };
             int j = 0;
