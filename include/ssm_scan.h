@@ -41,11 +41,11 @@
  *  - Calls are asynchronous on `stream` (0 = the legacy default stream).
  *    The library allocates nothing.  Its only state outside the caller's
  *    buffers is the fixed scratch array that bimamba_scan_fwd_v2_noalloc
- *    uses and three per-host-thread settings, each changed only by its own
+ *    uses and four per-host-thread settings, each changed only by its own
  *    setter and applying to later calls made on that host thread: the
  *    profiling events (ssm_set_profile_events), the CTA-shape override
- *    (ssm_set_cta_channels) and the one-launch failure-test hook
- *    (ssm_test_withhold_copy).
+ *    (ssm_set_cta_channels) and the one-launch test hooks
+ *    (ssm_test_withhold_copy, ssm_test_shrink_extents).
  *  - Errors: SSM_ERR_INVALID_ARG for a bad size, NULL required pointer or
  *    misaligned pointer; SSM_ERR_UNSUPPORTED for N > 32, K != 4 or sizes
  *    beyond the 32-bit index range; SSM_ERR_WORKSPACE when ws_bytes is too
@@ -54,7 +54,10 @@
  *    of bimamba_scan_fwd_v2_noalloc;
  *    SSM_ERR_TIMEOUT (through ssm_get_status, after the call's kernels ran)
  *    when a kernel's bounded wait for its own bulk copies ran out; its
- *    output is then incomplete.
+ *    output is then incomplete.  SSM_ERR_BOUNDS (through ssm_get_status)
+ *    only from a build with SSM_DEBUG_BOUNDS defined (libssm_scan_debug.so):
+ *    a forward kernel caught an element offset outside the tensor it
+ *    addresses and skipped that access; the product build never checks.
  *    Every check happens before any launch: an error means nothing ran.
  *  - A call with B == 0, D == 0 or L == 0 is valid and launches nothing.
  */
@@ -84,7 +87,8 @@ typedef enum {
     SSM_ERR_CUDA = 3,
     SSM_ERR_WORKSPACE = 4,
     SSM_ERR_SCRATCH_LIMIT = 5,
-    SSM_ERR_TIMEOUT = 6
+    SSM_ERR_TIMEOUT = 6,
+    SSM_ERR_BOUNDS = 7
 } ssm_status;
 
 typedef enum {
@@ -460,6 +464,17 @@ SSM_API void ssm_set_cta_channels(int channels);
  * hook applies to one launch only; -1 clears it.
  */
 SSM_API void ssm_test_withhold_copy(int chunk);
+
+/*
+ * Test hook of the debug build (SSM_DEBUG_BOUNDS).  The next scan-kernel
+ * launch made on this host thread checks its accesses to the [B, D, L]
+ * tensors against an extent `elems` elements short of the real one, so the
+ * accesses to the last `elems` elements are caught, skipped and reported
+ * (SSM_ERR_BOUNDS through ssm_get_status) -- without any access leaving the
+ * real tensor.  One launch only; the product build, which has no checks,
+ * ignores it.
+ */
+SSM_API void ssm_test_shrink_extents(long long elems);
 
 /* Library version, "major.minor.patch". */
 SSM_API const char *ssm_version(void);

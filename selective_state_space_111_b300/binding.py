@@ -28,57 +28,68 @@ SSM_F32, SSM_BF16, SSM_F16 = 0, 1, 2
 _CODES = {torch.float32: SSM_F32, torch.bfloat16: SSM_BF16, torch.float16: SSM_F16}
 OPS = {"single": 0, "v1": 1, "v2": 2, "ss2d": 3}
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA launch error",
-           4: "workspace", 5: "scratch limit", 6: "timeout"}
+           4: "workspace", 5: "scratch limit", 6: "timeout", 7: "bounds (debug build)"}
 
 _vp, _fp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
-_lib.selective_scan_fwd.argtypes = [_i] * 5 + [_vp] * 8 + [_i, _vp, _vp, _sz, _vp]
-_lib.bimamba_scan_fwd_v1.argtypes = [_i] * 5 + [_vp] * 9 + [_i, _f, _vp, _vp, _sz, _vp]
-_lib.bimamba_scan_fwd_v2.argtypes = [_i] * 5 + [_vp] * 15 + [_i, _f, _vp, _vp, _sz, _vp]
-_lib.ss2d_scan_fwd.argtypes = [_i] * 7 + [_vp] * 8 + [_i, _vp, _vp, _sz, _vp]
-_lib.bimamba_scan_fwd_v2_noalloc.argtypes = [_i] * 5 + [_vp] * 15 + [_i, _f, _vp, _vp]
-_lib.selective_scan_fwd_ls.argtypes = [_i] * 5 + [_vp] * 8 + [_i, _vp, _vp, _vp, _sz, _vp]
-_lib.bimamba_scan_fwd_v1_ls.argtypes = [_i] * 5 + [_vp] * 9 + [_i, _f, _vp, _vp, _vp, _sz, _vp]
-_lib.bimamba_scan_fwd_v2_ls.argtypes = [_i] * 5 + [_vp] * 15 + [_i, _f, _vp, _vp, _vp, _sz,
-                                                                 _vp]
-_lib.ss2d_scan_fwd_ls.argtypes = [_i] * 7 + [_vp] * 8 + [_i, _vp, _vp, _vp, _sz, _vp]
-_lib.bimamba_scan_fwd_v2_so.argtypes = [_i] * 5 + [_vp] * 15 + [_i, _f, _vp, _vp, _vp, _sz,
-                                                                 _vp]
-_lib.ssm_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
-_lib.ssm_workspace_bytes.restype = _sz
-_lib.ssm_get_status.argtypes = [_vp, _vp, ctypes.POINTER(_i)]
-_lib.ssm_get_status.restype = _i
-_lib.ssm_status_string.argtypes = [_i]
-_lib.ssm_status_string.restype = ctypes.c_char_p
-_lib.ssm_version.restype = ctypes.c_char_p
-_lib.ssm_test_withhold_copy.argtypes = [_i]
-_lib.ssm_test_withhold_copy.restype = None
-_lib.ssm_set_cta_channels.argtypes = [_i]
-_lib.ssm_set_cta_channels.restype = None
-_lib.ssm_set_profile_events.argtypes = [_vp, _vp]
-_lib.ssm_set_profile_events.restype = None
-_lib.selective_scan_bwd.argtypes = [_i] * 5 + [_vp] * 8 + [_i] + [_vp] * 10 + [_sz, _vp]
-_lib.bimamba_scan_bwd_v1.argtypes = ([_i] * 5 + [_vp] * 9 + [_i, _f] + [_vp] * 11 +
-                                     [_sz, _vp])
-_lib.bimamba_scan_bwd_v2.argtypes = ([_i] * 5 + [_vp] * 15 + [_i, _f] + [_vp] * 17 +
-                                     [_sz, _vp])
-_lib.ss2d_scan_bwd.argtypes = [_i] * 7 + [_vp] * 8 + [_i] + [_vp] * 10 + [_sz, _vp]
-_lib.mamba_prologue_fwd.argtypes = [_i] * 7 + [_vp] * 5 + [_i] + [_vp] * 5 + [_sz, _vp]
-_lib.mamba_prologue_fwd.restype = _i
-_lib.ssm_prologue_workspace_bytes.argtypes = [_i, _i, _i]
-_lib.ssm_prologue_workspace_bytes.restype = _sz
-_lib.ss2d_prologue_fwd.argtypes = [_i] * 8 + [_vp] * 5 + [_i] + [_vp] * 5 + [_sz, _vp]
-_lib.ss2d_prologue_fwd.restype = _i
-_lib.ss2d_prologue_workspace_bytes.argtypes = [_i, _i, _i, _i]
-_lib.ss2d_prologue_workspace_bytes.restype = _sz
-_lib.ssm_bwd_workspace_bytes.argtypes = [_i] * 8
-_lib.ssm_bwd_workspace_bytes.restype = _sz
-for _fn in (_lib.selective_scan_fwd, _lib.bimamba_scan_fwd_v1, _lib.bimamba_scan_fwd_v2,
-            _lib.ss2d_scan_fwd, _lib.bimamba_scan_fwd_v2_noalloc, _lib.selective_scan_fwd_ls,
-            _lib.bimamba_scan_fwd_v1_ls, _lib.bimamba_scan_fwd_v2_ls, _lib.ss2d_scan_fwd_ls,
-            _lib.bimamba_scan_fwd_v2_so,
-            _lib.selective_scan_bwd,
-            _lib.bimamba_scan_bwd_v1, _lib.bimamba_scan_bwd_v2, _lib.ss2d_scan_bwd):
-    _fn.restype = _i
+
+
+def _declare(lib):
+    """Argument and result types of every entry point of `lib` (this
+    library, or a build of the same sources with other flags)."""
+    lib.selective_scan_fwd.argtypes = [_i] * 5 + [_vp] * 8 + [_i, _vp, _vp, _sz, _vp]
+    lib.bimamba_scan_fwd_v1.argtypes = [_i] * 5 + [_vp] * 9 + [_i, _f, _vp, _vp, _sz, _vp]
+    lib.bimamba_scan_fwd_v2.argtypes = [_i] * 5 + [_vp] * 15 + [_i, _f, _vp, _vp, _sz, _vp]
+    lib.ss2d_scan_fwd.argtypes = [_i] * 7 + [_vp] * 8 + [_i, _vp, _vp, _sz, _vp]
+    lib.bimamba_scan_fwd_v2_noalloc.argtypes = [_i] * 5 + [_vp] * 15 + [_i, _f, _vp, _vp]
+    lib.selective_scan_fwd_ls.argtypes = [_i] * 5 + [_vp] * 8 + [_i, _vp, _vp, _vp, _sz, _vp]
+    lib.bimamba_scan_fwd_v1_ls.argtypes = [_i] * 5 + [_vp] * 9 + [_i, _f, _vp, _vp, _vp, _sz, _vp]
+    lib.bimamba_scan_fwd_v2_ls.argtypes = [_i] * 5 + [_vp] * 15 + [_i, _f, _vp, _vp, _vp, _sz,
+                                                                     _vp]
+    lib.ss2d_scan_fwd_ls.argtypes = [_i] * 7 + [_vp] * 8 + [_i, _vp, _vp, _vp, _sz, _vp]
+    lib.bimamba_scan_fwd_v2_so.argtypes = [_i] * 5 + [_vp] * 15 + [_i, _f, _vp, _vp, _vp, _sz,
+                                                                     _vp]
+    lib.ssm_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
+    lib.ssm_workspace_bytes.restype = _sz
+    lib.ssm_get_status.argtypes = [_vp, _vp, ctypes.POINTER(_i)]
+    lib.ssm_get_status.restype = _i
+    lib.ssm_status_string.argtypes = [_i]
+    lib.ssm_status_string.restype = ctypes.c_char_p
+    lib.ssm_version.restype = ctypes.c_char_p
+    lib.ssm_test_withhold_copy.argtypes = [_i]
+    lib.ssm_test_withhold_copy.restype = None
+    lib.ssm_test_shrink_extents.argtypes = [ctypes.c_longlong]
+    lib.ssm_test_shrink_extents.restype = None
+    lib.ssm_set_cta_channels.argtypes = [_i]
+    lib.ssm_set_cta_channels.restype = None
+    lib.ssm_set_profile_events.argtypes = [_vp, _vp]
+    lib.ssm_set_profile_events.restype = None
+    lib.selective_scan_bwd.argtypes = [_i] * 5 + [_vp] * 8 + [_i] + [_vp] * 10 + [_sz, _vp]
+    lib.bimamba_scan_bwd_v1.argtypes = ([_i] * 5 + [_vp] * 9 + [_i, _f] + [_vp] * 11 +
+                                         [_sz, _vp])
+    lib.bimamba_scan_bwd_v2.argtypes = ([_i] * 5 + [_vp] * 15 + [_i, _f] + [_vp] * 17 +
+                                         [_sz, _vp])
+    lib.ss2d_scan_bwd.argtypes = [_i] * 7 + [_vp] * 8 + [_i] + [_vp] * 10 + [_sz, _vp]
+    lib.mamba_prologue_fwd.argtypes = [_i] * 7 + [_vp] * 5 + [_i] + [_vp] * 5 + [_sz, _vp]
+    lib.mamba_prologue_fwd.restype = _i
+    lib.ssm_prologue_workspace_bytes.argtypes = [_i, _i, _i]
+    lib.ssm_prologue_workspace_bytes.restype = _sz
+    lib.ss2d_prologue_fwd.argtypes = [_i] * 8 + [_vp] * 5 + [_i] + [_vp] * 5 + [_sz, _vp]
+    lib.ss2d_prologue_fwd.restype = _i
+    lib.ss2d_prologue_workspace_bytes.argtypes = [_i, _i, _i, _i]
+    lib.ss2d_prologue_workspace_bytes.restype = _sz
+    lib.ssm_bwd_workspace_bytes.argtypes = [_i] * 8
+    lib.ssm_bwd_workspace_bytes.restype = _sz
+    for _fn in (lib.selective_scan_fwd, lib.bimamba_scan_fwd_v1, lib.bimamba_scan_fwd_v2,
+                lib.ss2d_scan_fwd, lib.bimamba_scan_fwd_v2_noalloc, lib.selective_scan_fwd_ls,
+                lib.bimamba_scan_fwd_v1_ls, lib.bimamba_scan_fwd_v2_ls, lib.ss2d_scan_fwd_ls,
+                lib.bimamba_scan_fwd_v2_so,
+                lib.selective_scan_bwd,
+                lib.bimamba_scan_bwd_v1, lib.bimamba_scan_bwd_v2, lib.ss2d_scan_bwd):
+        _fn.restype = _i
+    return lib
+
+
+_declare(_lib)
 
 
 class SsmError(RuntimeError):

@@ -8,6 +8,11 @@ into one shared library with the CUDA runtime linked statically, so the .so load
 machine without a GPU as well (for symbol checks) and needs nothing from the
 environment at run time beyond the NVIDIA driver.
 
+build_debug() compiles the same sources with SSM_DEBUG_BOUNDS defined into
+libssm_scan_debug.so: the forward kernels check every global access and
+bulk copy against its tensor's extent (a test-only build, loaded by the
+tests that exercise it).
+
 build_alu() compiles csrc/alu_rates.cu, the benchmark's throughput
 microbenchmark of the update's instruction kinds, into its own small
 libssm_alu.so (never loaded by the library or the tests).
@@ -27,6 +32,7 @@ DEPS = SOURCES + [os.path.join(HERE, "csrc", f) for f in
                   os.path.join(ROOT, "include", "ssm_scan.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 ALU_LIB = os.path.join(HERE, "libssm_alu.so")
+DEBUG_LIB = os.path.join(HERE, "libssm_scan_debug.so")
 ALU_SRC = os.path.join(HERE, "csrc", "alu_rates.cu")
 
 
@@ -35,17 +41,17 @@ def nvcc():
     return cand if os.path.exists(cand) else "nvcc"
 
 
-def needs_build():
-    if not os.path.exists(LIB):
+def needs_build(lib=LIB):
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(p) > t for p in DEPS)
 
 
-def build(force=False, verbose=False, extra=()):
-    if not force and not needs_build():
-        return LIB
-    tmp = LIB + ".tmp%d" % os.getpid()
+def build(force=False, verbose=False, extra=(), lib=LIB):
+    if not force and not needs_build(lib):
+        return lib
+    tmp = lib + ".tmp%d" % os.getpid()
     cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
            "-Xcompiler", "-fvisibility=hidden", "-cudart", "static",
            "-I", os.path.join(ROOT, "include"), "-o", tmp, *SOURCES, *extra]
@@ -53,8 +59,12 @@ def build(force=False, verbose=False, extra=()):
         cmd.insert(1, "-Xptxas=-v")
         print(" ".join(cmd))
     subprocess.check_call(cmd)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
+
+
+def build_debug(force=False):
+    return build(force=force, extra=("-DSSM_DEBUG_BOUNDS",), lib=DEBUG_LIB)
 
 
 def build_alu(force=False):
@@ -71,4 +81,5 @@ def build_alu(force=False):
 if __name__ == "__main__":
     build(force="--force" in sys.argv, verbose="-v" in sys.argv)
     build_alu(force="--force" in sys.argv)
+    build_debug(force="--force" in sys.argv)
     print(LIB)

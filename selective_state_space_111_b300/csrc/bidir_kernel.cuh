@@ -99,6 +99,10 @@ struct BiParams {
     int delta_softplus;
     float out_scale;
     int withhold_bc;       // test hook: chunk whose B/C copy is never issued (-1: none)
+    // extents (elements) for the debug build's index checks: each branch's
+    // dt tensor and packed B/C buffer from their base pointers, the [B, D, L]
+    // tensors (u, u_b, z, y, W, acc_in, acc_out), A [D, N]
+    long long dt_elems[2], bc_elems[2], io_elems, a_elems;
 };
 
 // ------------------------------------------------------------------ pack
@@ -118,6 +122,12 @@ __global__ void __launch_bounds__(256)
 pack_bc_kernel(const IO *__restrict__ Bm, const IO *__restrict__ Cm, float *__restrict__ out,
                int N, int L, unsigned *status, const IO *__restrict__ Bm1 = nullptr,
                const IO *__restrict__ Cm1 = nullptr, float *__restrict__ out1 = nullptr) {
+    // extents of B, C (each [Bt, K, N, L]) and of the packed output
+    // [K, Bt, L, 2NM] (per set when two sets are packed), for the debug checks
+    const long long in_elems = (long long)gridDim.y * (Bm1 != nullptr ? 1 : gridDim.z) * N * L;
+    const long long out_elems = (long long)(Bm1 != nullptr ? 1 : gridDim.z) * gridDim.y * L * 2 * NM;
+    (void)in_elems;                  // read by the debug build's checks only
+    (void)out_elems;
     constexpr int kBC = 2 * NM, PT = pack_pt<NM>();
     __shared__ float tile[kBC][PT + 1];
     const int b = blockIdx.y, t0 = blockIdx.x * PT;
@@ -142,7 +152,8 @@ pack_bc_kernel(const IO *__restrict__ Bm, const IO *__restrict__ Cm, float *__re
         v[r] = 0.f;
         if (t < L && n < N) {
             const IO *src = j < NM ? Bm : Cm;
-            v[r] = to_f32(src[(((long long)b * K + k) * N + n) * L + t]);
+            const long long o = (((long long)b * K + k) * N + n) * L + t;
+            if (SSM_IN(o, in_elems, status)) v[r] = to_f32(src[o]);
         }
     }
 #pragma unroll
@@ -153,7 +164,8 @@ pack_bc_kernel(const IO *__restrict__ Bm, const IO *__restrict__ Cm, float *__re
     __syncthreads();
     for (int i = threadIdx.x; i < PT * kBC; i += 256) {
         const int tt = i / kBC, j = i % kBC, t = t0 + tt;
-        if (t < L) out[(((long long)k * Bt + b) * L + t) * kBC + j] = tile[j][tt];
+        const long long o = (((long long)k * Bt + b) * L + t) * kBC + j;
+        if (t < L && SSM_IN(o, out_elems, status)) out[o] = tile[j][tt];
     }
 }
 
@@ -370,8 +382,11 @@ bidir_scan_kernel(const BiParams P) {
             for (int q = 0; q < NP; ++q) {
                 const int n0 = s_sg * S + 2 * q;
                 const bool ok = s_ch < D;
-                const float a0 = (ok && n0 < N) ? A[(long long)s_ch * N + n0] * kLog2e : 0.f;
-                const float a1 = (ok && n0 + 1 < N) ? A[(long long)s_ch * N + n0 + 1] * kLog2e : 0.f;
+                const bool in0 = ok && n0 < N && SSM_IN((long long)s_ch * N + n0, P.a_elems, P.status);
+                const bool in1 =
+                    ok && n0 + 1 < N && SSM_IN((long long)s_ch * N + n0 + 1, P.a_elems, P.status);
+                const float a0 = in0 ? A[(long long)s_ch * N + n0] * kLog2e : 0.f;
+                const float a1 = in1 ? A[(long long)s_ch * N + n0 + 1] * kLog2e : 0.f;
                 A2[q] = pk(a0, a1);
                 h[q] = pk(0.f, 0.f);
             }
@@ -394,6 +409,17 @@ bidir_scan_kernel(const BiParams P) {
             }
             float *ypp = (float *)(sm + LY::off_yp + s2 * LY::YP_STAGE +
                                    (s_dir * R + s_row) * LY::YP_ROW) + s_sg / (LPR / LY::YP);
+            // the chunk's shared-memory reads and writes stay inside their
+            // stages (debug build; a chunk that fails is not scanned)
+            if (!SSM_IN((dwp - sm) - LY::off_dw + (len - 1) * 16 + 15, 2 * LY::DW_STAGE, P.status) ||
+                !SSM_IN((const char *)(bcp + (bstep < 0 ? (len - 1) * bstep : 0)) - sm - LY::off_bc,
+                        LY::NBC * LY::BC_STAGE, P.status) ||
+                !SSM_IN((const char *)(bcp + (bstep > 0 ? (len - 1) * bstep : 0) + NM + S) - sm -
+                            LY::off_bc - 1,
+                        LY::NBC * LY::BC_STAGE, P.status) ||
+                !SSM_IN((const char *)(ypp + (len - 1) * LY::YP) - sm - LY::off_yp + 3,
+                        2 * LY::YP_STAGE, P.status))
+                len = 0;
             // partial readout of one step to shared memory (more than two
             // lanes per channel: pair sums, stored by the even lanes)
             auto put = [&](int j, float yv) {
@@ -498,14 +524,16 @@ bidir_scan_kernel(const BiParams P) {
         // position 0 for the backward walk)
         float *ls = P.last_state[s_dir];
         if (ls != nullptr && s_ch < D) {
-            ls += ((long long)b * D + s_ch) * N;
+            const long long lo = ((long long)b * D + s_ch) * N;
+            ls += lo;
 #pragma unroll
             for (int q = 0; q < NP; ++q) {
                 const int n0 = s_sg * S + 2 * q;
                 float a0, a1;
                 upk(h[q], a0, a1);
-                if (n0 < N) ls[n0] = a0;
-                if (n0 + 1 < N) ls[n0 + 1] = a1;
+                if (n0 < N && SSM_IN(lo + n0, (long long)P.B * D * N, P.status)) ls[n0] = a0;
+                if (n0 + 1 < N && SSM_IN(lo + n0 + 1, (long long)P.B * D * N, P.status))
+                    ls[n0 + 1] = a1;
             }
         }
     } else if (warp < NSW + NPW) {
@@ -559,12 +587,21 @@ bidir_scan_kernel(const BiParams P) {
                 si[g] = gsrev[g] ? c * T + j : pos;                  // dt stream index
                 p[g] = gusr[g] ? c * T + j : pos;                    // u index
             }
+            // element offsets from the tensors' bases (the debug build's checks)
+            auto dt_in = [&](int g, int ii) {
+                return SSM_IN((gdt[g] - (const IO *)P.br[gd[g]].dt) + ii * L + si[g],
+                              P.br[gd[g]].dt ? P.dt_elems[gd[g]] : 0, P.status);
+            };
+            auto u_in = [&](int g, int ii) {
+                return SSM_IN((gu[g] - (const IO *)P.br[gd[g]].u) + ii * L + p[g], P.io_elems,
+                              P.status);
+            };
             if (len == T && all_rows) {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int g = i / GR, ii = i % GR;
-                    xdt[i] = __ldg(gdt[g] + (ii * L + si[g]));
-                    xu[i] = __ldg(gu[g] + (ii * L + p[g]));
+                    xdt[i] = dt_in(g, ii) ? __ldg(gdt[g] + (ii * L + si[g])) : from_f32<IO>(0.f);
+                    xu[i] = u_in(g, ii) ? __ldg(gu[g] + (ii * L + p[g])) : from_f32<IO>(0.f);
                 }
             } else {
                 const bool act = j < len;
@@ -572,8 +609,9 @@ bidir_scan_kernel(const BiParams P) {
                 for (int i = 0; i < 16; ++i) {
                     const int g = i / GR, ii = i % GR;
                     const bool ok = act && ii < gn[g];
-                    xdt[i] = ok ? __ldg(gdt[g] + (ii * L + si[g])) : from_f32<IO>(0.f);
-                    xu[i] = ok ? __ldg(gu[g] + (ii * L + p[g])) : from_f32<IO>(0.f);
+                    xdt[i] = (ok && dt_in(g, ii)) ? __ldg(gdt[g] + (ii * L + si[g]))
+                                                  : from_f32<IO>(0.f);
+                    xu[i] = (ok && u_in(g, ii)) ? __ldg(gu[g] + (ii * L + p[g])) : from_f32<IO>(0.f);
                 }
             }
         };
@@ -651,8 +689,15 @@ bidir_scan_kernel(const BiParams P) {
 #pragma unroll
             for (int d = 0; d < NDIR; ++d) {
                 chunk_geom(c, d, L, T, lo, len);
-                bulk_g2s(sm + LY::off_bc + st * LY::BC_STAGE + d * LY::BC_DIR,
-                         P.br[d].bc + ((long long)b * L + stream_lo(c, d, lo)) * kBC,
+                const long long so = ((long long)b * L + stream_lo(c, d, lo)) * kBC;
+                // source range inside the packed buffer, destination inside
+                // the stage (a copy that fails either is not issued)
+                if (!SSM_IN(so, P.bc_elems[d], P.status) ||
+                    !SSM_IN(so + (long long)len * kBC - 1, P.bc_elems[d], P.status) ||
+                    !SSM_IN(LY::off_bc + st * LY::BC_STAGE + d * LY::BC_DIR + len * kBC * 4 - 1,
+                            LY::off_bc + LY::NBC * LY::BC_STAGE, P.status))
+                    continue;
+                bulk_g2s(sm + LY::off_bc + st * LY::BC_STAGE + d * LY::BC_DIR, P.br[d].bc + so,
                          (unsigned)(len * kBC * 4), &bc_full[st]);
             }
         };
@@ -697,10 +742,11 @@ bidir_scan_kernel(const BiParams P) {
                 for (int i = 0; i < CPE; ++i) {
                     const bool ok = fin && (decltype(FULL)::value || i < nch_ok);
                     const int o = i * L + p;
-                    zr[d][i] = (ok && OUT != OUT_ACC && zrow != nullptr) ? __ldg(zrow + o)
+                    const bool in = ok && SSM_IN(rowb0 + o, P.io_elems, P.status);
+                    zr[d][i] = (in && OUT != OUT_ACC && zrow != nullptr) ? __ldg(zrow + o)
                                                                           : from_f32<IO>(0.f);
-                    wr[d][i] = (ok && stash) ? Wrow[o] : 0.f;
-                    ar[d][i] = (OUT == OUT_ADD_Y && ok) ? __ldg(airow + o) : 0.f;
+                    wr[d][i] = (in && stash) ? Wrow[o] : 0.f;
+                    ar[d][i] = (OUT == OUT_ADD_Y && in) ? __ldg(airow + o) : 0.f;
                 }
             }
         };
@@ -760,7 +806,8 @@ bidir_scan_kernel(const BiParams P) {
                     const int p = (d ? lo1 : lo0) + q;
 #pragma unroll
                     for (int i = 0; i < CPE; ++i)
-                        if (i < nch_ok) Wrow[i * L + p] = own(d, i, d ? T - 1 - q : q);
+                        if (i < nch_ok && SSM_IN(rowb0 + i * L + p, P.io_elems, P.status))
+                            Wrow[i * L + p] = own(d, i, d ? T - 1 - q : q);
                 }
                 mbar_arrive(&u_empty[c % LY::NU]);
             } else if (kd == 1) {
@@ -778,7 +825,8 @@ bidir_scan_kernel(const BiParams P) {
                         if (NDIR == 2) v = P.out_scale * (v + wr[d][i]);
                         if (OUT == OUT_ADD_Y) v += ar[d][i];
                         if (gate) v *= silu_f<IO>(to_f32(zr[d][i]));
-                        if (full || (act && i < nch_ok)) {
+                        if ((full || (act && i < nch_ok)) &&
+                            SSM_IN(rowb0 + i * L + p, P.io_elems, P.status)) {
                             if (OUT == OUT_ACC) aorow[i * L + p] = v;
                             else yrow[i * L + p] = from_f32<IO>(v);
                         }
@@ -826,8 +874,9 @@ bidir_scan_kernel(const BiParams P) {
                     const bool fin = live && (NDIR == 1 || k != 0);
 #pragma unroll
                     for (int i = 0; i < CPE; ++i) {
-                        const bool ok = i < nch_ok;
                         const int o = i * L + p;
+                        const bool ok = i < nch_ok && (!(live || fin) ||
+                                                       SSM_IN(rowb0 + o, P.io_elems, P.status));
                         if (NDIR == 2 && ok && live && k == 0) Wrow[o] = vv[d][i];
                         if (ok && fin) {
                             if (OUT == OUT_ACC) aorow[o] = vv[d][i];

@@ -119,6 +119,23 @@ template <> __device__ __forceinline__ float silu_f<__half>(float z) {
 }
 
 
+// ---- index checks of the debug build
+// Built with SSM_DEBUG_BOUNDS, every global access and bulk copy of the
+// forward path first checks its element offset against the extent of the
+// tensor it addresses; an offset outside it sets bit 1 of the status word
+// (ssm_get_status then reports SSM_ERR_BOUNDS) and the access is skipped (a
+// load gives 0).  The product build compiles the checks away.
+#ifdef SSM_DEBUG_BOUNDS
+__device__ __forceinline__ bool dbg_in(long long i, long long n, unsigned *status) {
+    if (i >= 0 && i < n) return true;
+    if (status != nullptr) atomicOr(status, 2u);
+    return false;
+}
+#define SSM_IN(i, n, status) ::ssm::dbg_in((long long)(i), (long long)(n), (status))
+#else
+#define SSM_IN(i, n, status) true
+#endif
+
 // ---- mbarrier and 1-D bulk copy (TMA) helpers
 __device__ __forceinline__ unsigned smem_addr(const void *p) {
     return (unsigned)__cvta_generic_to_shared(p);

@@ -109,6 +109,10 @@ thread_local int t_cta_channels = 0;
 // Test hook (ssm_test_withhold_copy): chunk whose B/C copy the next call on
 // this host thread withholds, to exercise the bounded waits.
 thread_local int t_withhold = -1;
+// Test hook of the debug build (ssm_test_shrink_extents): elements the next
+// scan-kernel launch on this host thread takes off the [B, D, L] extent its
+// index checks use.
+thread_local long long t_shrink = 0;
 
 template <typename IO, int S, int NDIR, int G, int OUT, int NM>
 ssm_status launch_bidir(const ssm::BiParams &P, cudaStream_t st, bool last = true) {
@@ -134,6 +138,8 @@ ssm_status launch_bidir(const ssm::BiParams &P, cudaStream_t st, bool last = tru
     ssm::BiParams Q = P;
     Q.withhold_bc = t_withhold;
     t_withhold = -1;
+    Q.io_elems = t_shrink < Q.io_elems ? Q.io_elems - t_shrink : 0;
+    t_shrink = 0;
     if (prof && cudaEventRecord(t_prof_begin, st) != cudaSuccess) {
         cudaGetLastError();
         return SSM_ERR_CUDA;
@@ -254,6 +260,9 @@ ssm_status bidirectional(ssm_dtype dt, int B, int D, int L, int N, const void *u
     P.nchunks = bi_chunks(L);
     P.delta_softplus = delta_softplus ? 1 : 0;
     P.out_scale = out_scale;
+    P.dt_elems[0] = P.dt_elems[1] = P.io_elems = (long long)B * D * L;
+    P.bc_elems[0] = P.bc_elems[1] = (long long)B * L * 2 * nm_of(N);
+    P.a_elems = (long long)D * N;
     if (dt == SSM_F32) return run_bidir<float, 2>(P, Bm, Cm, Bm_b, Cm_b, two_sets, stream);
     if (dt == SSM_F16) return run_bidir<__half, 2>(P, Bm, Cm, Bm_b, Cm_b, two_sets, stream);
     return run_bidir<__nv_bfloat16, 2>(P, Bm, Cm, Bm_b, Cm_b, two_sets, stream);
@@ -336,6 +345,16 @@ ssm_status ss2d_run_nm(int B, int D, int H, int W, int N, const void *x, const v
         br.stream_rev = rev;
         return br;
     };
+    // extents from each branch's base pointers (dt, B/C and A are the whole
+    // four-direction tensors, offset per direction)
+    auto extents = [&](ssm::BiParams &Q, int k0, int k1) {
+        Q.dt_elems[0] = (long long)B * 4 * DL;             // offset through dt_off
+        Q.dt_elems[1] = (long long)B * 4 * DL;
+        Q.bc_elems[0] = (long long)(4 - k0) * B * L * 2 * NM;
+        Q.bc_elems[1] = (long long)(4 - k1) * B * L * 2 * NM;
+        Q.io_elems = (long long)B * DL;
+        Q.a_elems = (long long)D * N;
+    };
     ssm::BiParams P{};
     P.status = status;
     P.B = B;
@@ -348,6 +367,7 @@ ssm_status ss2d_run_nm(int B, int D, int H, int W, int N, const void *x, const v
     // column pair on x^T: the fused sum goes to Wt (R2), stash in R1
     P.br[0] = branch(1, xt, 0);
     P.br[1] = branch(3, xt, 1);
+    extents(P, 1, 3);
     P.W = r1;
     P.acc_out = r2;
     P.last_state[0] = lsk(1);
@@ -360,6 +380,7 @@ ssm_status ss2d_run_nm(int B, int D, int H, int W, int N, const void *x, const v
     // row pair on x: y = gate(y0 + y2 + Wa), stash in R2
     P.br[0] = branch(0, x, 0);
     P.br[1] = branch(2, x, 1);
+    extents(P, 0, 2);
     P.z = z;
     P.y = y;
     P.W = r2;
@@ -445,6 +466,9 @@ ssm_status single_impl(ssm_dtype dt, int B, int D, int L, int N, const void *u,
     P.nchunks = bi_chunks(L);
     P.delta_softplus = delta_softplus ? 1 : 0;
     P.out_scale = 1.f;
+    P.dt_elems[0] = P.dt_elems[1] = P.io_elems = (long long)B * D * L;
+    P.bc_elems[0] = P.bc_elems[1] = (long long)B * L * 2 * nm_of(N);
+    P.a_elems = (long long)D * N;
     cudaStream_t st = (cudaStream_t)stream;
     if (dt == SSM_F32) return run_bidir<float, 1>(P, Bm, Cm, Bm, Cm, false, st);
     if (dt == SSM_F16) return run_bidir<__half, 1>(P, Bm, Cm, Bm, Cm, false, st);
@@ -645,7 +669,7 @@ ssm_status ssm_get_status(const void *workspace, ssm_stream_t stream, ssm_status
         cudaGetLastError();
         return SSM_ERR_CUDA;
     }
-    *out = word ? SSM_ERR_TIMEOUT : SSM_OK;
+    *out = (word & 2u) ? SSM_ERR_BOUNDS : word ? SSM_ERR_TIMEOUT : SSM_OK;
     return SSM_OK;
 }
 
@@ -659,11 +683,15 @@ const char *ssm_status_string(ssm_status s) {
     case SSM_ERR_TIMEOUT: return "a kernel's bounded wait for its own copies ran out";
     case SSM_ERR_SCRATCH_LIMIT:
         return "problem needs more scratch than the library's fixed 64 MiB array";
+    case SSM_ERR_BOUNDS:
+        return "an index outside its tensor was caught and skipped (debug build)";
     }
     return "unknown status";
 }
 
 void ssm_test_withhold_copy(int chunk) { t_withhold = chunk; }
+
+void ssm_test_shrink_extents(long long elems) { t_shrink = elems > 0 ? elems : 0; }
 
 void ssm_set_cta_channels(int channels) {
     t_cta_channels = (channels == 8 || channels == 16) ? channels : 0;
