@@ -42,6 +42,10 @@ size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
 // state capacity (16 or 32) and channels per backward CTA for N states
 int nm_of(int N) { return N <= ssm::kMaxN ? ssm::kMaxN : 2 * ssm::kMaxN; }
 int ch_of(int N) { return ssm::bwd::NT / nm_of(N); }
+// steps per chunk of the backward scan (the 16-state kernel's chunks are
+// shorter: its recomputed states take eight floats per thread and step)
+int chunk_of(int N) { return N <= ssm::kMaxN ? ssm::bwd::T16 : ssm::bwd::T; }
+int nch_of(int L, int N) { return (L + chunk_of(N) - 1) / chunk_of(N); }
 
 template <typename IO> constexpr ssm_dtype dtype_of() { return SSM_BF16; }
 template <> constexpr ssm_dtype dtype_of<float>() { return SSM_F32; }
@@ -59,7 +63,7 @@ BwdWs bwd_ws(int op, ssm_dtype dt, int B, int D, int L, int N, bool sep_ub) {
     const size_t n = (size_t)B * D * L;
     const int npass = op == 0 ? 1 : op == 3 ? 4 : 2;
     const int nm = nm_of(N), ncg = (D + ch_of(N) - 1) / ch_of(N);
-    const int nch = (L + ssm::bwd::T - 1) / ssm::bwd::T;
+    const int nch = nch_of(L, N);
     BwdWs w{};
     size_t off = 256;
     auto take = [&](size_t bytes) {
@@ -109,19 +113,33 @@ ssm_status launch_passes_nm(const Pass *ps, int npass, int B, int D, int L, int 
     P.D = D;
     P.L = L;
     P.N = N;
-    P.nch = (L + ssm::bwd::T - 1) / ssm::bwd::T;
+    P.nch = nch_of(L, N);
     P.delta_softplus = sp ? 1 : 0;
-    constexpr int CH = ssm::bwd::channels<NM>();
-    constexpr int dyn = ssm::bwd::dyn_bytes<NM>();
-    dim3 grid((D + CH - 1) / CH, B, npass);
-    auto *kern = &ssm::bwd::scan_bwd_kernel<IO, NM>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn) !=
-        cudaSuccess) {
-        cudaGetLastError();
-        return SSM_ERR_CUDA;
+    if constexpr (NM == ssm::kMaxN) {
+        // 16 states: eight per thread, 32 channels per CTA
+        constexpr int dyn = ssm::bwd::H16_BYTES;
+        dim3 grid((D + ssm::bwd::CH16 - 1) / ssm::bwd::CH16, B, npass);
+        auto *kern = &ssm::bwd::scan_bwd16_kernel<IO>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return SSM_ERR_CUDA;
+        }
+        kern<<<grid, ssm::bwd::NT16, dyn, st>>>(P);
+        return last_error();
+    } else {
+        constexpr int CH = ssm::bwd::channels<NM>();
+        constexpr int dyn = ssm::bwd::dyn_bytes<NM>();
+        dim3 grid((D + CH - 1) / CH, B, npass);
+        auto *kern = &ssm::bwd::scan_bwd_kernel<IO, NM>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return SSM_ERR_CUDA;
+        }
+        kern<<<grid, ssm::bwd::NT, dyn, st>>>(P);
+        return last_error();
     }
-    kern<<<grid, ssm::bwd::NT, dyn, st>>>(P);
-    return last_error();
 }
 template <typename IO>
 ssm_status launch_passes(const Pass *ps, int npass, int B, int D, int L, int N, int sp,
@@ -214,8 +232,7 @@ Pass base_pass(char *ws, const BwdWs &w, int p, int B, int D, int L, int N) {
     ps.pdB = (float *)(ws + w.pdB) + (size_t)p * ncg * B * L * nm;
     ps.pdC = (float *)(ws + w.pdC) + (size_t)p * ncg * B * L * nm;
     ps.pdA = (float *)(ws + w.pdA) + (size_t)p * B * D * nm;
-    const int nch = (L + ssm::bwd::T - 1) / ssm::bwd::T;
-    ps.hc = (float *)(ws + w.hc) + (size_t)p * B * D * nch * nm;
+    ps.hc = (float *)(ws + w.hc) + (size_t)p * B * D * nch_of(L, N) * nm;
     ps.G = (const float *)(ws + w.G);
     ps.gscale = 1.f;
     return ps;
