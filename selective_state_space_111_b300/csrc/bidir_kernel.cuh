@@ -93,6 +93,11 @@ struct BiParams {
     float *acc_out;        // [B, D, L] fp32 (OUT_ACC)
     float *W;              // [B, D, L] fp32 stash (two branches, several chunks)
     float *last_state[2];  // per branch: final state [B, D, N] fp32, or null
+    // per branch: the state before every 16th walk step, [B, D, ceil(L/16),
+    // 16] fp32 (walk chunk k holds the state after walk steps 0 .. 16k-1),
+    // or null; state capacity 16 only.  The backward pass starts its
+    // recomputation from these.
+    float *chunk_state[2];
     unsigned *status;      // device status word, or null
     int B, D, L, N;
     int nchunks;
@@ -392,6 +397,13 @@ bidir_scan_kernel(const BiParams P) {
             }
         }
         const bool walk_down = s_dir == 1 && !P.br[1].stream_rev;
+        // this lane's eight states of the chunk-state output (16 states)
+        float *cs = (NM == kMaxN && s_ch < D) ? P.chunk_state[s_dir] : nullptr;
+        const long long cs_chunks = (L + 15) / 16;
+        const long long cs_off = ((bD + s_ch) * cs_chunks) * NM + s_sg * S;
+        const long long cs_elems = (long long)P.B * D * cs_chunks * NM;
+        (void)cs_elems;
+        if (cs != nullptr) cs += cs_off;
         for (int c = 0; c < nch; ++c) {
             const int s2 = c & 1, sb = c % LY::NBC;
             if (*abort_flag || !wait(&dw_full[s2], (c >> 1) & 1) ||
@@ -514,6 +526,32 @@ bidir_scan_kernel(const BiParams P) {
                 upk(NP > 1 ? add2(ya, yb) : ya, ylo, yhi);
                 put(j, ylo + yhi);
             };
+            if constexpr (NM == kMaxN && T % 16 == 0) {
+                if (cs != nullptr) {
+                    // walk chunks of 16 steps: store the state at the start
+                    // of each, then scan it
+#pragma unroll 1
+                    for (int j0 = 0; j0 < len; j0 += 16) {
+                        const long long k = (long long)c * (T / 16) + j0 / 16;
+                        float v[2 * NP];
+#pragma unroll
+                        for (int q = 0; q < NP; ++q) upk(h[q], v[2 * q], v[2 * q + 1]);
+                        if (SSM_IN(cs_off + k * NM + S - 1, cs_elems, P.status)) {
+#pragma unroll
+                            for (int q = 0; q < NP / 2; ++q)
+                                *(float4 *)(cs + k * NM + 4 * q) =
+                                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                        }
+                        const int j1 = min(len, j0 + 16);
+                        int j = j0;
+                        for (; j + UB <= j1; j += UB) block(j);
+                        for (; j < j1; ++j) step(j);
+                    }
+                    mbar_arrive(&dw_empty[s2]);
+                    mbar_arrive(&yp_full[s2]);
+                    continue;
+                }
+            }
             int j = 0;
             for (; j + UB <= len; j += UB) block(j);
             for (; j < len; ++j) step(j);

@@ -70,6 +70,8 @@ struct Params {
     Pass ps[kMaxPass];         // one per direction; blockIdx.z selects it
     int B, D, L, N, nch;
     int delta_softplus;
+    int hc_given;              // 16-state kernel: hc already holds the chunk-start
+                               // states (stored by the forward pass); no pass 1
 };
 
 __device__ __forceinline__ float sigmoid_f(float x) {
@@ -397,7 +399,8 @@ scan_bwd_kernel(const Params P) {
 // fp32 pairs (f32x2 MUL/FMA).  CTA = 32 channels of one batch element, one
 // direction (64 threads, two warps of 16 channels); chunks of T16 steps.
 //  * pass 1 runs the recurrence forward and stores the state at each chunk
-//    start (hc, [B][D][nch][16]);
+//    start (hc, [B][D][nch][16]) -- skipped when the forward pass of the
+//    same call already stored them there (hc_given);
 //  * pass 2 walks the chunks backwards: it recomputes the chunk's states
 //    from the stored start into shared memory (h_{j-1} at step j), then
 //    undoes the steps in groups of KG16.  Per step a lane forms, over its
@@ -547,8 +550,9 @@ scan_bwd16_kernel(const Params P) {
         sH4[(2 * j + 1) * NT16 + tid] = make_float4(v[4], v[5], v[6], v[7]);
     };
 
-    // ---- pass 1: states at the chunk starts
-    {
+    // ---- pass 1: states at the chunk starts (unless the forward pass
+    // stored them)
+    if (!P.hc_given) {
         f2 h[NP];
 #pragma unroll
         for (int q = 0; q < NP; ++q) h[q] = pk(0.f, 0.f);

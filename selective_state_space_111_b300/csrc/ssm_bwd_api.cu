@@ -14,6 +14,7 @@
 #include <cstdint>
 
 #include "bwd_kernel.cuh"
+#include "internal.h"
 #include "ssm_scan.h"
 
 namespace {
@@ -106,7 +107,7 @@ ssm_status last_error() {
 // batch x directions).
 template <typename IO, int NM>
 ssm_status launch_passes_nm(const Pass *ps, int npass, int B, int D, int L, int N, int sp,
-                            cudaStream_t st) {
+                            bool hc_given, cudaStream_t st) {
     ssm::bwd::Params P{};
     for (int k = 0; k < npass; ++k) P.ps[k] = ps[k];
     P.B = B;
@@ -115,6 +116,7 @@ ssm_status launch_passes_nm(const Pass *ps, int npass, int B, int D, int L, int 
     P.N = N;
     P.nch = nch_of(L, N);
     P.delta_softplus = sp ? 1 : 0;
+    P.hc_given = (NM == ssm::kMaxN && hc_given) ? 1 : 0;
     if constexpr (NM == ssm::kMaxN) {
         // 16 states: eight per thread, 32 channels per CTA
         constexpr int dyn = ssm::bwd::H16_BYTES;
@@ -141,12 +143,24 @@ ssm_status launch_passes_nm(const Pass *ps, int npass, int B, int D, int L, int 
         return last_error();
     }
 }
+// hc_given: the forward pass of this call stored the chunk-start states
+// (16 states only)
 template <typename IO>
 ssm_status launch_passes(const Pass *ps, int npass, int B, int D, int L, int N, int sp,
-                         cudaStream_t st) {
-    if (N <= ssm::kMaxN) return launch_passes_nm<IO, ssm::kMaxN>(ps, npass, B, D, L, N, sp, st);
-    return launch_passes_nm<IO, 2 * ssm::kMaxN>(ps, npass, B, D, L, N, sp, st);
+                         bool hc_given, cudaStream_t st) {
+    if (N <= ssm::kMaxN)
+        return launch_passes_nm<IO, ssm::kMaxN>(ps, npass, B, D, L, N, sp, hc_given, st);
+    return launch_passes_nm<IO, 2 * ssm::kMaxN>(ps, npass, B, D, L, N, sp, false, st);
 }
+
+// Scope in which the forward calls of this host thread also store their
+// chunk-start states for the 16-state backward kernel.
+struct CaptureScope {
+    explicit CaptureScope(float *const *hc) { ssm_internal::set_chunk_state_capture(hc); }
+    ~CaptureScope() { ssm_internal::set_chunk_state_capture(nullptr); }
+    CaptureScope(const CaptureScope &) = delete;
+    CaptureScope &operator=(const CaptureScope &) = delete;
+};
 
 template <typename IO>
 ssm_status gate_bwd(const void *g, const void *z, const void *y, float *G, void *dz, long long n,
@@ -253,10 +267,16 @@ ssm_status seq_bwd(int op, int B, int D, int L, int N, const void *u, const void
     float *G = (float *)(ws + w.G);
     float *du0 = (float *)(ws + w.du), *du1 = du0 + n;      // per direction
     float *dt0 = (float *)(ws + w.ddt), *dt1 = dt0 + n;
-    // (1) pre-gate output, only needed for dz
+    // (1) the forward pass: the pre-gate output (for dz) and, with 16
+    // states, the chunk-start states of every direction (the backward
+    // kernel then skips its own forward sweep)
     void *ypre = ws + w.ypre;
     void *fws = ws + w.fwd;
-    if (z != nullptr) {
+    const bool capture = N <= ssm::kMaxN;
+    if (z != nullptr || capture) {
+        float *hc[4] = {base_pass(ws, w, 0, B, D, L, N).hc,
+                        op == 0 ? nullptr : base_pass(ws, w, 1, B, D, L, N).hc, nullptr, nullptr};
+        CaptureScope scope(capture ? hc : nullptr);
         ssm_stream_t sst = (ssm_stream_t)st;
         if (op == 0)
             TRY(selective_scan_fwd(dt, B, D, L, N, u, delta, A, Bm, Cm, Dskip, nullptr, bias, sp,
@@ -310,7 +330,7 @@ ssm_status seq_bwd(int op, int B, int D, int L, int N, const void *u, const void
         p1.ddt = dt1;
         pp[1] = p1;
     }
-    TRY(launch_passes<IO>(pp, op == 0 ? 1 : 2, B, D, L, N, sp, st));
+    TRY(launch_passes<IO>(pp, op == 0 ? 1 : 2, B, D, L, N, sp, capture, st));
     // (4) outputs: shared tensors sum both branches' gradients
     const bool shared_u = op == 1 || (op == 2 && u_b == nullptr);
     TRY(convert<IO>(du0, shared_u ? du1 : nullptr, nullptr, du, n, st));
@@ -352,9 +372,16 @@ ssm_status ss2d_bwd_run(int B, int D, int H, int W, int N, const void *x, const 
     const int L = H * W, K = 4;
     const long long n = (long long)B * D * L;
     void *ypre = ws + w.ypre;
-    if (z != nullptr)
+    // the forward pass: the pre-gate output (for dz) and, with 16 states,
+    // the chunk-start states of the four directions
+    const bool capture = N <= ssm::kMaxN;
+    if (z != nullptr || capture) {
+        float *hc[4];
+        for (int k = 0; k < K; ++k) hc[k] = base_pass(ws, w, k, B, D, L, N).hc;
+        CaptureScope scope(capture ? hc : nullptr);
         TRY(ss2d_scan_fwd(dt, B, D, H, W, N, K, x, delta, A, Bm, Cm, Dskip, nullptr, bias, sp,
                           ypre, ws + w.fwd, w.fwd_bytes, (ssm_stream_t)st));
+    }
     float *G = (float *)(ws + w.G), *GT = (float *)(ws + w.GT);
     IO *xT = (IO *)(ws + w.xT);
     TRY(gate_bwd<IO>(dout, z, ypre, G, dz, n, st));
@@ -384,7 +411,7 @@ ssm_status ss2d_bwd_run(int B, int D, int H, int W, int N, const void *x, const 
         ps.ddt = (float *)(ws + w.ddt);
         pp[k] = ps;
     }
-    TRY(launch_passes<IO>(pp, K, B, D, L, N, sp, st));
+    TRY(launch_passes<IO>(pp, K, B, D, L, N, sp, capture, st));
     // dx = row pair (0, 2) + the column pair (1, 3) transposed back; G^T's
     // space is free now
     TRY(convert<float>(du + n, du + 3 * n, nullptr, du + n, n, st));

@@ -13,6 +13,7 @@
 #include <mutex>
 
 #include "bidir_kernel.cuh"
+#include "internal.h"
 #include "ssm_scan.h"
 
 // Scratch of bimamba_scan_fwd_v2_noalloc: a fixed device array of the
@@ -113,6 +114,8 @@ thread_local int t_withhold = -1;
 // scan-kernel launch on this host thread takes off the [B, D, L] extent its
 // index checks use.
 thread_local long long t_shrink = 0;
+// Chunk-state capture (ssm_internal::set_chunk_state_capture), per direction.
+thread_local float *t_capture[4] = {nullptr, nullptr, nullptr, nullptr};
 
 template <typename IO, int S, int NDIR, int G, int OUT, int NM>
 ssm_status launch_bidir(const ssm::BiParams &P, cudaStream_t st, bool last = true) {
@@ -252,6 +255,8 @@ ssm_status bidirectional(ssm_dtype dt, int B, int D, int L, int N, const void *u
     const long long BDN = (long long)B * D * N;
     P.last_state[0] = ls;                               // [2][B][D][N]
     P.last_state[1] = ls ? ls + BDN : nullptr;
+    P.chunk_state[0] = t_capture[0];
+    P.chunk_state[1] = t_capture[1];
     P.status = (unsigned *)wsb;
     P.B = B;
     P.D = D;
@@ -372,6 +377,8 @@ ssm_status ss2d_run_nm(int B, int D, int H, int W, int N, const void *x, const v
     P.acc_out = r2;
     P.last_state[0] = lsk(1);
     P.last_state[1] = lsk(3);
+    P.chunk_state[0] = t_capture[1];
+    P.chunk_state[1] = t_capture[3];
     s = launch_two_branch<IO, ssm::OUT_ACC, NM>(P, st, false);
     if (s != SSM_OK) return s;
     // Wa (R1) = Wt (R2) transposed back to H x W
@@ -388,6 +395,8 @@ ssm_status ss2d_run_nm(int B, int D, int H, int W, int N, const void *x, const v
     P.acc_out = nullptr;
     P.last_state[0] = lsk(0);
     P.last_state[1] = lsk(2);
+    P.chunk_state[0] = t_capture[0];
+    P.chunk_state[1] = t_capture[2];
     return launch_two_branch<IO, ssm::OUT_ADD_Y, NM>(P, st);
 }
 template <typename IO>
@@ -458,6 +467,7 @@ ssm_status single_impl(ssm_dtype dt, int B, int D, int L, int N, const void *u,
     P.W = nullptr;
     P.last_state[0] = ls;
     P.last_state[1] = nullptr;
+    P.chunk_state[0] = t_capture[0];
     P.status = (unsigned *)wsb;
     P.B = B;
     P.D = D;
@@ -507,6 +517,10 @@ ssm_status ss2d_impl(ssm_dtype dt, int B, int D, int H, int W, int N, int K, con
 }
 
 }  // namespace
+
+void ssm_internal::set_chunk_state_capture(float *const *hc) {
+    for (int k = 0; k < 4; ++k) t_capture[k] = hc ? hc[k] : nullptr;
+}
 
 extern "C" {
 
