@@ -336,12 +336,18 @@ def run_ours(args):
         if not torch.equal(h_out.to(dev), outs[(n_e2e - 1) % nb]):
             raise RuntimeError("e2e: downloaded result differs from the device result")
 
+    # NVTX ranges name the backward and prologue legs, so a profiler can
+    # select their launches (ncu --nvtx --nvtx-include "backward/")
     bwd = None
     if not args.no_backward:
+        torch.cuda.nvtx.range_push("backward")
         bwd = measure_backward(ssm, spec, g, t, dev, stream, max(3, min(args.steps, 20)))
+        torch.cuda.nvtx.range_pop()
     pro = None
     if not args.no_prologue:
+        torch.cuda.nvtx.range_push("prologue")
         pro = measure_prologue(ssm, spec, dev, stream, max(3, min(args.steps, 20)))
+        torch.cuda.nvtx.range_pop()
 
     if rank == 0:
         ms = total_ms / args.steps

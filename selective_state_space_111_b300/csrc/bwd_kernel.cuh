@@ -60,6 +60,12 @@ struct Pass {
     int rev, stream_rev;
     float *du;                 // fp32 [B, D, L], position order (this pass's own)
     float *ddt;                // fp32, indexed like dt (this pass's own)
+    // 16-state kernel only (null elsewhere): when set, du and ddt are
+    // written in the I/O dtype here instead of the fp32 maps above, and the
+    // per-(batch, channel) sums of ddt and of gscale * G * u (the dbias and
+    // dD terms) are written to pbias and pdD, [B][D] fp32
+    void *du_io, *ddt_io;
+    float *pbias, *pdD;
     float *pdB, *pdC;          // this pass's partials [ncg][B][L][NM] (stream index)
     float *pdA;                // [B][D][NM]
     float *hc;                 // chunk-start states [B][D][nch][NM] (this pass's own)
@@ -606,6 +612,8 @@ scan_bwd16_kernel(const Params P) {
         h[2] = pk(v1.x, v1.y);
         h[3] = pk(v1.z, v1.w);
     };
+    const float dsk = sDsk[ch];                  // this lane's channel's skip weight
+    float sum_bias = 0.f, sum_skip = 0.f;        // its dbias and dD terms (half 1)
     // one adjoint step; hh holds h_j of the step being undone on entry and
     // h_{j-1} on exit
     auto step_bwd = [&](int j, int k, f2 (&hh)[NP]) {
@@ -645,8 +653,15 @@ scan_bwd16_kernel(const Params P) {
         float SU = su0 + su1, SD = sd0 + sd1;
         SU += __shfl_xor_sync(0xffffffffu, SU, 1);
         SD += __shfl_xor_sync(0xffffffffu, SD, 1);
-        if (half == 0) sDu[ch][j] = dv.x * SU;
-        else sDd[ch][j] = fmaf(uu, SU, SD);
+        // du (with the skip term) and the gradient of dt (times softplus'
+        // when the forward applied softplus): both halves hold the same
+        // channel sums; half 0 stores du, half 1 the dt gradient.  Both
+        // accumulate the channel's dbias and dD terms.
+        const float du_j = fmaf(gy, dsk, dv.x * SU);
+        const float gx = fmaf(uu, SU, SD) * sS[ch][j];
+        *(half ? &sDd[ch][j] : &sDu[ch][j]) = half ? gx : du_j;
+        sum_bias += gx;
+        sum_skip = fmaf(gy, uu, sum_skip);
         float vb[S], vc[S];
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
@@ -720,17 +735,26 @@ scan_bwd16_kernel(const Params P) {
         if (len == T) chunk(BoolC<true>(), c, len, hh);
         else chunk(BoolC<false>(), c, len, hh);
         __syncthreads();
-        // per-position gradients of this direction (du with the skip term)
-        for (int i = tid; i < CH16 * T; i += NT16) {
-            const int cc = i / T, j = i % T, w = c * T + j, dd = d0 + cc;
+        // per-position gradients of this direction
+#pragma unroll
+        for (int r = 0; r < PC; ++r) {
+            const int i = tid + r * NT16, cc = i / T, j = i % T, w = c * T + j, dd = d0 + cc;
             if (w < L && dd < D) {
                 const long long prow = ((long long)b * D + dd) * L;
-                ps.du[prow + pos(w)] = fmaf(sG[cc][j], sDsk[cc], sDu[cc][j]);
-                const float gx = P.delta_softplus ? sDd[cc][j] * sS[cc][j] : sDd[cc][j];
-                ps.ddt[ps.dt_off + b * ps.dt_bstride + (long long)dd * L + sidx(w)] = gx;
+                const float du = sDu[cc][j], gx = sDd[cc][j];
+                const long long di = ps.dt_off + b * ps.dt_bstride + (long long)dd * L + sidx(w);
+                if (ps.du_io != nullptr) ((IO *)ps.du_io)[prow + pos(w)] = from_f32<IO>(du);
+                else ps.du[prow + pos(w)] = du;
+                if (ps.ddt_io != nullptr) ((IO *)ps.ddt_io)[di] = from_f32<IO>(gx);
+                else ps.ddt[di] = gx;
             }
         }
         __syncthreads();
+    }
+    // the channel's dbias and dD terms
+    if (ps.pbias != nullptr && half == 1 && cvalid) {
+        ps.pbias[(long long)b * D + d] = sum_bias;
+        ps.pdD[(long long)b * D + d] = sum_skip;
     }
     if (cvalid) {
         float v[S];
@@ -841,24 +865,43 @@ __global__ void convert_kernel(const float *__restrict__ a, const float *__restr
 
 // dB[b][n][s] (I/O, at out + b * out_bstride) = sum over the nslot partials
 // [slot][B][L][nm] (slot-major; a fixed summation order, so the result is
-// the same on every run)
-template <typename IO>
-__global__ void reduce_bc_kernel(const float *__restrict__ part, int nslot, int B, int L, int N,
-                                 int nm, IO *__restrict__ out, long long out_bstride) {
-    const long long total = (long long)B * L * N;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
-        const int nn = (int)(i % N);
-        const long long bs = i / N;                  // b * L + s
-        const int s = (int)(bs % L), b = (int)(bs / L);
-        float acc = 0.f;
-        for (int k = 0; k < nslot; ++k) acc += part[((long long)k * B * L + bs) * nm + nn];
-        out[b * out_bstride + (long long)nn * L + s] = from_f32<IO>(acc);
+// the same on every run).  CTA = 256 / (nm / 4) positions of one batch
+// element: thread = (position, group of four states), 16-byte loads of the
+// partials; the sums are transposed through shared memory so each state's
+// row of positions is stored contiguously.
+template <typename IO, int NM>
+__global__ void __launch_bounds__(256)
+reduce_bc_kernel(const float *__restrict__ part, int nslot, int B, int L, int N,
+                 IO *__restrict__ out, long long out_bstride) {
+    constexpr int QN = NM / 4, PS = 256 / QN;           // quads per position, positions per CTA
+    __shared__ float tile[NM][PS + 1];
+    const int b = blockIdx.y, s0 = blockIdx.x * PS;
+    const int t = threadIdx.x, sl = t / QN, q = t % QN, s = s0 + sl;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (s < L) {
+        const float4 *src = reinterpret_cast<const float4 *>(part) +
+                            (((long long)b * L + s) * NM) / 4 + q;
+        const long long slot_stride = (long long)B * L * NM / 4;
+#pragma unroll 8
+        for (int k = 0; k < nslot; ++k) {
+            const float4 v = src[k * slot_stride];
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+    }
+    tile[4 * q][sl] = acc.x;
+    tile[4 * q + 1][sl] = acc.y;
+    tile[4 * q + 2][sl] = acc.z;
+    tile[4 * q + 3][sl] = acc.w;
+    __syncthreads();
+    for (int i = t; i < N * PS; i += 256) {
+        const int nn = i / PS, j = i % PS;
+        if (s0 + j < L) out[b * out_bstride + (long long)nn * L + s0 + j] = from_f32<IO>(tile[nn][j]);
     }
 }
 
-// out[i] = sum over the nslot partials [slot][B][cols] of column i (fixed
-// order): dA (cols = D * 16, written [D][N]), dD and dbias (cols = D)
 __global__ void reduce_param_kernel(const float *__restrict__ part, int nslot, int B, int D,
                                     int N, int nm, int per_state, float *__restrict__ out) {
     const int cols = per_state ? D * nm : D;

@@ -54,7 +54,7 @@ template <> constexpr ssm_dtype dtype_of<__half>() { return SSM_F16; }
 
 // Workspace of one backward call; every region starts on 256 bytes.
 struct BwdWs {
-    size_t fwd, ypre, G, GT, xT, du, ddt, hc, pdB, pdC, pdA, total;
+    size_t fwd, ypre, G, GT, xT, du, ddt, hc, pdB, pdC, pdA, pbias, pdD, total;
     size_t fwd_bytes;
 };
 // op: 0 single, 1 v1, 2 v2, 3 SS2D.  du and ddt hold one fp32 map per
@@ -90,6 +90,9 @@ BwdWs bwd_ws(int op, ssm_dtype dt, int B, int D, int L, int N, bool sep_ub) {
     w.pdB = take(part);
     w.pdC = take(part);
     w.pdA = take((size_t)npass * B * D * nm * 4);
+    // per-(direction, batch, channel) sums of ddt and G * u (16 states)
+    w.pbias = take((size_t)npass * B * D * 4);
+    w.pdD = take((size_t)npass * B * D * 4);
     w.total = off;
     return w;
 }
@@ -187,8 +190,17 @@ ssm_status convert(const float *a, const float *b, const float *c, void *out, lo
 template <typename IO>
 ssm_status reduce_bc(const float *part, int nslot, int B, int L, int N, void *out,
                      long long out_bstride, cudaStream_t st) {
-    ssm::bwd::reduce_bc_kernel<IO><<<grid1d((long long)B * L * N), 256, 0, st>>>(
-        part, nslot, B, L, N, nm_of(N), (IO *)out, out_bstride);
+    if (B == 0 || L == 0) return SSM_OK;
+    if (N <= ssm::kMaxN) {
+        constexpr int PS = 256 / (ssm::kMaxN / 4);
+        ssm::bwd::reduce_bc_kernel<IO, ssm::kMaxN><<<dim3((L + PS - 1) / PS, B), 256, 0, st>>>(
+            part, nslot, B, L, N, (IO *)out, out_bstride);
+    } else {
+        constexpr int PS = 256 / (2 * ssm::kMaxN / 4);
+        ssm::bwd::reduce_bc_kernel<IO, 2 * ssm::kMaxN>
+            <<<dim3((L + PS - 1) / PS, B), 256, 0, st>>>(part, nslot, B, L, N, (IO *)out,
+                                                         out_bstride);
+    }
     return last_error();
 }
 
@@ -249,6 +261,11 @@ Pass base_pass(char *ws, const BwdWs &w, int p, int B, int D, int L, int N) {
     ps.hc = (float *)(ws + w.hc) + (size_t)p * B * D * nch_of(L, N) * nm;
     ps.G = (const float *)(ws + w.G);
     ps.gscale = 1.f;
+    if (N <= ssm::kMaxN) {
+        // the 16-state kernel sums dbias and dD itself
+        ps.pbias = (float *)(ws + w.pbias) + (size_t)p * B * D;
+        ps.pdD = (float *)(ws + w.pdD) + (size_t)p * B * D;
+    }
     return ps;
 }
 
@@ -310,6 +327,15 @@ ssm_status seq_bwd(int op, int B, int D, int L, int N, const void *u, const void
     p0.stream_rev = 0;
     p0.du = du0;
     p0.ddt = dt0;
+    // 16 states: a direction that owns its du or ddelta writes it in the
+    // I/O dtype directly; tensors the two branches share are summed from
+    // the fp32 maps below
+    const bool fused = N <= ssm::kMaxN;
+    const bool du_own = op == 0 || (op == 2 && u_b != nullptr), ddt_own = op != 1;
+    if (fused) {
+        p0.du_io = du_own ? du : nullptr;
+        p0.ddt_io = ddt_own ? ddelta : nullptr;
+    }
     Pass pp[2] = {p0, p0};
     if (op != 0) {
         Pass p1 = p0;
@@ -318,6 +344,10 @@ ssm_status seq_bwd(int op, int B, int D, int L, int N, const void *u, const void
         p1.pdC = q.pdC;
         p1.pdA = q.pdA;
         p1.hc = q.hc;
+        p1.pbias = q.pbias;
+        p1.pdD = q.pdD;
+        p1.du_io = fused && du_own ? du_b : nullptr;
+        p1.ddt_io = fused && ddt_own ? ddelta_b : nullptr;
         p1.dt = op == 2 ? delta_b : delta;
         p1.u = (op == 2 && u_b) ? u_b : u;
         p1.Bm = op == 2 ? Bm_b : Bm;
@@ -333,10 +363,14 @@ ssm_status seq_bwd(int op, int B, int D, int L, int N, const void *u, const void
     TRY(launch_passes<IO>(pp, op == 0 ? 1 : 2, B, D, L, N, sp, capture, st));
     // (4) outputs: shared tensors sum both branches' gradients
     const bool shared_u = op == 1 || (op == 2 && u_b == nullptr);
-    TRY(convert<IO>(du0, shared_u ? du1 : nullptr, nullptr, du, n, st));
-    if (op == 2 && u_b != nullptr) TRY(convert<IO>(du1, nullptr, nullptr, du_b, n, st));
-    TRY(convert<IO>(dt0, op == 1 ? dt1 : nullptr, nullptr, ddelta, n, st));
-    if (op == 2) TRY(convert<IO>(dt1, nullptr, nullptr, ddelta_b, n, st));
+    if (!(fused && du_own)) {
+        TRY(convert<IO>(du0, shared_u ? du1 : nullptr, nullptr, du, n, st));
+        if (op == 2 && u_b != nullptr) TRY(convert<IO>(du1, nullptr, nullptr, du_b, n, st));
+    }
+    if (!(fused && ddt_own)) {
+        TRY(convert<IO>(dt0, op == 1 ? dt1 : nullptr, nullptr, ddelta, n, st));
+        if (op == 2) TRY(convert<IO>(dt1, nullptr, nullptr, ddelta_b, n, st));
+    }
     const Parts q = parts_of(ws, w, B, D, L, N);
     const int shared_bc = op == 1 ? 2 : 1;      // v1: both passes add into dB, dC
     TRY(reduce_bc<IO>(q.dB_slot(0), shared_bc * q.ncg, B, L, N, dB, NL, st));
@@ -350,6 +384,19 @@ ssm_status seq_bwd(int op, int B, int D, int L, int N, const void *u, const void
     // dD: each branch's skip term is D * u_t at every position, so
     // dD = gscale * sum G u (v1: both branches, shared D); dbias = sum ddt
     const float gs = op == 0 ? 1.f : out_scale;
+    if (fused) {
+        // the kernel's per-(direction, batch) channel sums (G already
+        // carries gscale); v1 adds both directions
+        const float *pb = p0.pbias, *pd = p0.pdD;
+        const int nsum = op == 1 ? 2 : 1;
+        if (Dskip) TRY(reduce_param(pd, nsum, B, D, N, false, dD, st));
+        TRY(reduce_param(pb, nsum, B, D, N, false, dbias, st));
+        if (op == 2) {
+            if (D_b) TRY(reduce_param(pd + (size_t)B * D, 1, B, D, N, false, dD_b, st));
+            TRY(reduce_param(pb + (size_t)B * D, 1, B, D, N, false, dbias_b, st));
+        }
+        return SSM_OK;
+    }
     if (Dskip) TRY(channel_sum<IO>(G, nullptr, DL, u, B, D, L, op == 1 ? 2.f * gs : gs, dD, st));
     TRY(channel_sum<IO>(dt0, op == 1 ? dt1 : nullptr, DL, nullptr, B, D, L, 1.f, dbias, st));
     if (op == 2) {
@@ -409,6 +456,7 @@ ssm_status ss2d_bwd_run(int B, int D, int H, int W, int N, const void *x, const 
         ps.stream_rev = k >= 2;
         ps.du = du + k * n;
         ps.ddt = (float *)(ws + w.ddt);
+        if (capture) ps.ddt_io = ddelta;        // each direction owns its ddelta slice
         pp[k] = ps;
     }
     TRY(launch_passes<IO>(pp, K, B, D, L, N, sp, capture, st));
@@ -417,12 +465,22 @@ ssm_status ss2d_bwd_run(int B, int D, int H, int W, int N, const void *x, const 
     TRY(convert<float>(du + n, du + 3 * n, nullptr, du + n, n, st));
     TRY(transpose<float>(du + n, GT, B * D, W, H, st));
     TRY(convert<IO>(du, du + 2 * n, GT, dx, n, st));
-    TRY(convert<IO>((const float *)(ws + w.ddt), nullptr, nullptr, ddelta, n * K, st));
+    if (!capture)
+        TRY(convert<IO>((const float *)(ws + w.ddt), nullptr, nullptr, ddelta, n * K, st));
     const Parts q = parts_of(ws, w, B, D, L, N);
     for (int k = 0; k < K; ++k) {
         TRY(reduce_bc<IO>(q.dB_slot(k), q.ncg, B, L, N, (IO *)dB + k * NL, K * NL, st));
         TRY(reduce_bc<IO>(q.dC_slot(k), q.ncg, B, L, N, (IO *)dC + k * NL, K * NL, st));
         TRY(reduce_param(q.dA_slot(k), 1, B, D, N, true, dA + (long long)k * D * N, st));
+        if (capture) {
+            // the kernel's channel sums: every direction visits every
+            // position once, so its sum of G * x is dD_k
+            if (Dskip)
+                TRY(reduce_param(pp[k].pdD, 1, B, D, N, false, dD ? dD + k * D : nullptr, st));
+            TRY(reduce_param(pp[k].pbias, 1, B, D, N, false, dbias ? dbias + k * D : nullptr,
+                             st));
+            continue;
+        }
         // every direction visits every position once: dD_k = sum G x
         if (Dskip)
             TRY(channel_sum<IO>(G, nullptr, DL, x, B, D, L, 1.f, dD ? dD + k * D : nullptr, st));
