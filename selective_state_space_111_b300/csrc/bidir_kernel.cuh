@@ -93,10 +93,10 @@ struct BiParams {
     float *acc_out;        // [B, D, L] fp32 (OUT_ACC)
     float *W;              // [B, D, L] fp32 stash (two branches, several chunks)
     float *last_state[2];  // per branch: final state [B, D, N] fp32, or null
-    // per branch: the state before every 16th walk step, [B, D, ceil(L/16),
-    // 16] fp32 (walk chunk k holds the state after walk steps 0 .. 16k-1),
-    // or null; state capacity 16 only.  The backward pass starts its
-    // recomputation from these.
+    // per branch: the state before every kStateChunk-th walk step, [B, D,
+    // ceil(L / kStateChunk), 16] fp32 (walk chunk k holds the state after
+    // walk steps 0 .. k * kStateChunk - 1), or null; state capacity 16
+    // only.  The backward pass starts its recomputation from these.
     float *chunk_state[2];
     unsigned *status;      // device status word, or null
     int B, D, L, N;
@@ -399,7 +399,7 @@ bidir_scan_kernel(const BiParams P) {
         const bool walk_down = s_dir == 1 && !P.br[1].stream_rev;
         // this lane's eight states of the chunk-state output (16 states)
         float *cs = (NM == kMaxN && s_ch < D) ? P.chunk_state[s_dir] : nullptr;
-        const long long cs_chunks = (L + 15) / 16;
+        const long long cs_chunks = (L + kStateChunk - 1) / kStateChunk;
         const long long cs_off = ((bD + s_ch) * cs_chunks) * NM + s_sg * S;
         const long long cs_elems = (long long)P.B * D * cs_chunks * NM;
         (void)cs_elems;
@@ -526,13 +526,13 @@ bidir_scan_kernel(const BiParams P) {
                 upk(NP > 1 ? add2(ya, yb) : ya, ylo, yhi);
                 put(j, ylo + yhi);
             };
-            if constexpr (NM == kMaxN && T % 16 == 0) {
+            if constexpr (NM == kMaxN && T % kStateChunk == 0 && kStateChunk % UB == 0) {
                 if (cs != nullptr) {
-                    // walk chunks of 16 steps: store the state at the start
-                    // of each, then scan it
+                    // walk chunks of kStateChunk steps: store the state at
+                    // the start of each, then scan it
 #pragma unroll 1
-                    for (int j0 = 0; j0 < len; j0 += 16) {
-                        const long long k = (long long)c * (T / 16) + j0 / 16;
+                    for (int j0 = 0; j0 < len; j0 += kStateChunk) {
+                        const long long k = (long long)c * (T / kStateChunk) + j0 / kStateChunk;
                         float v[2 * NP];
 #pragma unroll
                         for (int q = 0; q < NP; ++q) upk(h[q], v[2 * q], v[2 * q + 1]);
@@ -542,7 +542,7 @@ bidir_scan_kernel(const BiParams P) {
                                 *(float4 *)(cs + k * NM + 4 * q) =
                                     make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                         }
-                        const int j1 = min(len, j0 + 16);
+                        const int j1 = min(len, j0 + kStateChunk);
                         int j = j0;
                         for (; j + UB <= j1; j += UB) block(j);
                         for (; j < j1; ++j) step(j);

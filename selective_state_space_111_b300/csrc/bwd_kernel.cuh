@@ -422,17 +422,21 @@ scan_bwd_kernel(const Params P) {
 // memory synchronisation to two __syncwarp per KG16 steps.  Shared-memory
 // rows are padded so that the per-step accesses of a warp (16 channels, two
 // lanes each) hit distinct banks.
-#ifndef SSM_BWD16_T
-#define SSM_BWD16_T 16
+#ifndef SSM_BWD16_KG
+#define SSM_BWD16_KG 2           // adjoint steps per dB/dC tile group (1, 2 or 4)
 #endif
-constexpr int T16 = SSM_BWD16_T, CH16 = 32, NT16 = 64, KG16 = 4;
+#ifndef SSM_BWD16_MINB
+#define SSM_BWD16_MINB 4         // CTAs per SM the register allocation allows for
+#endif
+constexpr int T16 = kStateChunk, CH16 = 32, NT16 = 64, KG16 = SSM_BWD16_KG;
+static_assert(KG16 == 1 || KG16 == 2 || KG16 == 4, "group length");
 constexpr int TILE16 = 36;                                        // tile row stride (floats)
 constexpr int H16_BYTES = T16 * 2 * NT16 * (int)sizeof(float4) +  // recomputed states
                           2 * KG16 * 16 * TILE16 * (int)sizeof(float);   // dB / dC tiles
 static_assert(T16 % KG16 == 0, "chunk length: a multiple of the group length");
 
 template <typename IO>
-__global__ void __launch_bounds__(NT16, 3)
+__global__ void __launch_bounds__(NT16, SSM_BWD16_MINB)
 scan_bwd16_kernel(const Params P) {
     constexpr int NM = 16, S = 8, NP = S / 2, T = T16, TP = T + 1, KG = KG16;
     __shared__ __align__(16) float4 sDW[CH16][TP];   // (delta, delta, w, w), w = delta * u
@@ -596,11 +600,13 @@ scan_bwd16_kernel(const Params P) {
     const int slot = blockIdx.x * 2 + warp;                      // 16-channel group
     const bool slot_ok = d0 + warp * 16 < D;
     float *tile = sT + warp * (KG * 16 * TILE16);
-    // tile reduction: lane -> group step k = lane >> 3, column quad q = lane & 7
-    // (dB for q & 2 clear, else dC; states (q >> 2) * 8 + (q & 1) * 4 .. +3)
-    const int rk = lane >> 3, rq = lane & 7;
-    float *const pdst = ((rq & 2) ? ps.pdC : ps.pdB) +
-                        ((long long)slot * P.B + b) * L * NM + (rq >> 2) * 8 + (rq & 1) * 4;
+    // tile reduction: lane -> group step rk, columns c0 .. c0 + KG - 1 of
+    // the row [dB 0-7 | dC 0-7 | dB 8-15 | dC 8-15] (KG <= 4 columns stay
+    // inside one block of eight): dC when c0 & 8, states (c0 >> 4) * 8 + c0 % 8
+    constexpr int LPS = 32 / KG;                 // lanes per group step
+    const int rk = lane / LPS, c0 = (lane % LPS) * KG;
+    float *const pdst = ((c0 & 8) ? ps.pdC : ps.pdB) +
+                        ((long long)slot * P.B + b) * L * NM + (c0 >> 4) * 8 + (c0 & 7);
     auto load_h = [&](int c, f2 (&h)[NP]) {
         float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
         if (cvalid) {
@@ -677,20 +683,37 @@ scan_bwd16_kernel(const Params P) {
     // the group's dB, dC partials: step g0 + rk, four columns over 16 channels
     auto reduce_group = [&](int c, int g0, int len) {
         __syncwarp();
-        const float *col = tile + rk * 16 * TILE16 + 4 * rq;
-        f2 a0 = pk(0.f, 0.f), a1 = a0;
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const float4 v = *(const float4 *)(col + r * TILE16);
-            a0 = add2(a0, pk(v.x, v.y));
-            a1 = add2(a1, pk(v.z, v.w));
-        }
+        const float *col = tile + rk * 16 * TILE16 + c0;
         const int j = g0 + rk;
-        if (j < len && slot_ok) {
+        float *dst = pdst + (long long)sidx(c * T + min(j, len - 1)) * NM;
+        const bool st = j < len && slot_ok;
+        if constexpr (KG == 4) {
+            f2 a0 = pk(0.f, 0.f), a1 = a0;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                const float4 v = *(const float4 *)(col + r * TILE16);
+                a0 = add2(a0, pk(v.x, v.y));
+                a1 = add2(a1, pk(v.z, v.w));
+            }
             float x0, x1, x2, x3;
             upk(a0, x0, x1);
             upk(a1, x2, x3);
-            *(float4 *)(pdst + (long long)sidx(c * T + j) * NM) = make_float4(x0, x1, x2, x3);
+            if (st) *(float4 *)dst = make_float4(x0, x1, x2, x3);
+        } else if constexpr (KG == 2) {
+            f2 a0 = pk(0.f, 0.f);
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                const float2 v = *(const float2 *)(col + r * TILE16);
+                a0 = add2(a0, pk(v.x, v.y));
+            }
+            float x0, x1;
+            upk(a0, x0, x1);
+            if (st) *(float2 *)dst = make_float2(x0, x1);
+        } else {
+            float a0 = 0.f;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) a0 += col[r * TILE16];
+            if (st) *dst = a0;
         }
         __syncwarp();
     };

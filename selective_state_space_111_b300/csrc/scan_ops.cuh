@@ -13,6 +13,12 @@
 namespace ssm {
 
 constexpr int kMaxN = 16;      // states per channel held by the kernels
+// Walk steps per chunk of the 16-state backward scan: the forward pass
+// stores the state before every kStateChunk-th walk step for it.
+#ifndef SSM_BWD16_T
+#define SSM_BWD16_T 8
+#endif
+constexpr int kStateChunk = SSM_BWD16_T;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
