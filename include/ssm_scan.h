@@ -41,11 +41,14 @@
  *  - Calls are asynchronous on `stream` (0 = the legacy default stream).
  *    The library allocates nothing.  Its only state outside the caller's
  *    buffers is the fixed scratch array that bimamba_scan_fwd_v2_noalloc
- *    uses and four per-host-thread settings, each changed only by its own
+ *    uses and five per-host-thread settings, each changed only by its own
  *    setter and applying to later calls made on that host thread: the
  *    profiling events (ssm_set_profile_events), the CTA-shape override
- *    (ssm_set_cta_channels) and the one-launch test hooks
- *    (ssm_test_withhold_copy, ssm_test_shrink_extents).
+ *    (ssm_set_cta_channels), the prologue's kernel choice
+ *    (ssm_set_prologue_fused) and the one-launch test hooks
+ *    (ssm_test_withhold_copy, ssm_test_shrink_extents).  (The backward
+ *    calls also set, and clear before returning, a per-thread request that
+ *    the forward run inside them store its chunk-start states.)
  *  - Errors: SSM_ERR_INVALID_ARG for a bad size, NULL required pointer or
  *    misaligned pointer; SSM_ERR_UNSUPPORTED for N > 32, K != 4 or sizes
  *    beyond the 32-bit index range; SSM_ERR_WORKSPACE when ws_bytes is too
@@ -398,9 +401,16 @@ SSM_API size_t ssm_bwd_workspace_bytes(ssm_op op, ssm_dtype dt, int B, int D,
  * Outputs (I/O dtype, device, caller-owned): u, delta [B, D, L]; Bm, Cm
  * [B, N, L] -- the layouts the scan calls take.  N <= 32, 1 <= K <= 8.
  * workspace: ssm_prologue_workspace_bytes(B, L, R) bytes, 16-byte aligned
- * (the fp32 dt_low).  Arithmetic: fp32 accumulation throughout; with
- * 16-bit I/O x_proj runs on tensor cores with u and W_x in the I/O type and
- * dt_proj on tf32 operands; with fp32 I/O both are fp32 FMA.  Outputs are
+ * (the fp32 dt_low of the three-kernel path; the fused path below does not
+ * touch it, but the size is required either way).  Kernels: with 16-bit
+ * I/O, K = 4, R + 2N <= 64, R <= 32 and L < 1024 one fused kernel per call
+ * (conv, x_proj and dt_proj per tile of 64 positions: u written once and
+ * not read back, dt_low kept on chip; ssm_set_prologue_fused overrides the
+ * choice), otherwise three launches (conv1d + SiLU, x_proj, dt_proj).
+ * Arithmetic:
+ * fp32 accumulation throughout; with 16-bit I/O x_proj runs on tensor
+ * cores with u and W_x in the I/O type and dt_proj on tf32 operands; with
+ * fp32 I/O both are fp32 FMA.  Outputs are
  * rounded to the I/O dtype.  Errors: SSM_ERR_INVALID_ARG for a bad dtype,
  * size or pointer; SSM_ERR_UNSUPPORTED for N > 32, K > 8 or sizes past the
  * 32-bit index range; SSM_ERR_WORKSPACE for a short or misaligned
@@ -454,6 +464,17 @@ SSM_API size_t ss2d_prologue_workspace_bytes(int B, int H, int W, int R);
  * any other value is treated as 0.  Results do not depend on it.
  */
 SSM_API void ssm_set_cta_channels(int channels);
+
+/*
+ * Kernel choice of mamba_prologue_fwd where the fused kernel applies (16-bit
+ * I/O, K = 4, R + 2N <= 64, R <= 32).  mode 1 (the default, and any value
+ * other than 0 or 2): automatic -- the fused kernel for L < 1024, where it
+ * measured faster, else the three-kernel path; 0: always the three-kernel
+ * path; 2: the fused kernel at every L.  Applies to later calls on this host
+ * thread.  Both paths compute the same sums with the same operand
+ * roundings; results agree to accumulation order, not bit for bit.
+ */
+SSM_API void ssm_set_prologue_fused(int mode);
 
 /*
  * Test hook for the failure path.  The next scan-kernel launch made on this

@@ -61,6 +61,8 @@ def _declare(lib):
     lib.ssm_test_shrink_extents.restype = None
     lib.ssm_set_cta_channels.argtypes = [_i]
     lib.ssm_set_cta_channels.restype = None
+    lib.ssm_set_prologue_fused.argtypes = [_i]
+    lib.ssm_set_prologue_fused.restype = None
     lib.ssm_set_profile_events.argtypes = [_vp, _vp]
     lib.ssm_set_profile_events.restype = None
     lib.selective_scan_bwd.argtypes = [_i] * 5 + [_vp] * 8 + [_i] + [_vp] * 10 + [_sz, _vp]
@@ -172,6 +174,13 @@ def set_cta_channels(channels: int = 0) -> None:
     """Channels per CTA of the two-branch kernels for later calls on this
     thread: 8, 16, or 0 for the automatic choice."""
     _lib.ssm_set_cta_channels(int(channels))
+
+
+def set_prologue_fused(mode: int = 1) -> None:
+    """Kernels of mamba_prologue_fwd for later calls on this thread, where
+    the fused kernel applies: 1 automatic (fused for L < 1024), 0 always
+    the three-kernel path, 2 the fused kernel at every L."""
+    _lib.ssm_set_prologue_fused(int(mode))
 
 
 def get_status(workspace, stream=None) -> int:

@@ -588,6 +588,267 @@ dtproj_tc_kernel(const float *__restrict__ W, const float *__restrict__ in, int 
     }
 }
 
+// ---- the whole 1-D prologue of one direction in one kernel (16-bit I/O,
+// K = 4 conv taps, x_proj rows M = R + 2N <= 64, dt_rank R <= RP <= 32):
+//   u = silu(conv1d(x) + bias), [dt_low; B; C] = W_x u, dt = W_dt dt_low
+// ("从Transformer到Mamba" section 2.1: conv1d, x_proj, dt_proj in that
+// order; "VMamba的SS2D模块详解" section 3.1: the split into dt, B and C).
+// A CTA takes FP_T positions (walk order) of one batch element and every
+// channel, in slices of FP_KS channels:
+//   * the slice's x window (FP_T + 3 positions per channel) and W_x
+//     columns are fetched one slice ahead into registers (raw loads from
+//     clamped in-range addresses; masks and conversion at commit);
+//   * thread = (position, 8 channels): the conv + SiLU of 8 channels at one
+//     position, stored to u (along positions: coalesced) and as one 16-byte
+//     row of the tensor-core operand [position][channel] in shared memory;
+//   * the x_proj contribution of the slice accumulates in registers
+//     (mma.sync m16n8k16, fp32 accumulation; warp w: rows 16 (w % 4) .. +16,
+//     positions 32 (w / 4) .. +32);
+//   * after the last slice B and C leave through a shared fp32 tile along
+//     positions, dt_low stays in shared memory (rounded to tf32), and dt_proj
+//     runs there in blocks of 64 rows (mma.sync m16n8k8 tf32, fp32
+//     accumulation), dt stored along positions.
+// So u is written once and never read back, and dt_low never leaves the
+// CTA (the three-kernel path reads u again and round-trips dt_low).
+#ifndef SSM_FP_MINB
+#define SSM_FP_MINB 2            // CTAs per SM the register allocation allows for
+#endif
+constexpr int FP_T = 64, FP_KS = 32, FP_NT = 256;
+constexpr int FP_XS = FP_T + 4;                  // x window row: positions t0-3 .. t0+63 (+pad)
+constexpr int FP_IP = FP_KS + 8;                 // operand row [position][channel] (bank spread)
+constexpr int FP_OP = FP_T + 8;                  // x_proj result row (fp32)
+constexpr int FP_XV = (FP_KS * FP_XS + FP_NT - 1) / FP_NT;   // x values per thread and slice
+constexpr int FP_WV = 64 * FP_KS / FP_NT;                    // W_x values per thread and slice
+constexpr int FP_OS = FP_T + 4;                  // dt block row (fp32)
+constexpr int FP_IS = FP_T + 8;                  // dt_low (tf32) row
+// one slice's buffers: x window, operand [position][channel], W_x
+// columns, conv taps and bias (two of them: slice s + 1 is staged while
+// the mma of slice s still reads its own)
+__host__ __device__ constexpr int fp_slice_bytes() {
+    return FP_KS * FP_XS * 4 + 2 * 64 * FP_IP * 2 + FP_KS * 5 * 4;
+}
+template <int RP> __host__ __device__ constexpr int fp_region() {
+    // slice buffers, or (after the slices) dt_proj's W block, dt_low and
+    // output block; conv weights and bias at the end of the slice buffers
+    constexpr int a = 2 * fp_slice_bytes();
+    constexpr int c = 64 * (RP + 4) * 4 + RP * FP_IS * 4 + 64 * FP_OS * 4;
+    return ((a > c ? a : c) + 15) / 16 * 16;
+}
+template <int RP> __host__ __device__ constexpr size_t fused_prologue_smem_bytes() {
+    return (size_t)fp_region<RP>() + (size_t)64 * FP_OP * 4;
+}
+
+template <typename IO, int RP>
+__global__ void __launch_bounds__(FP_NT, SSM_FP_MINB)
+fused_prologue_kernel(const IO *__restrict__ x, const float *__restrict__ cw,
+                      const float *__restrict__ cb, const float *__restrict__ Wx,
+                      const float *__restrict__ Wdt, int D, int L, int N, int R, int reverse,
+                      IO *__restrict__ u, IO *__restrict__ dt, IO *__restrict__ Bm,
+                      IO *__restrict__ Cm) {
+    static_assert(sizeof(IO) == 2, "16-bit I/O");
+    extern __shared__ __align__(16) unsigned char fp_smem[];
+    // slice phase: buffer set k of slice s = k (mod 2)
+    auto sx = [&](int k) { return (float *)(fp_smem + k * fp_slice_bytes()); };   // [FP_KS][FP_XS]
+    auto sI = [&](int k) { return (IO *)(sx(k) + FP_KS * FP_XS); };               // [FP_T][FP_IP]
+    auto sW = [&](int k) { return sI(k) + FP_T * FP_IP; };                        // [64][FP_IP]
+    auto sCW = [&](int k) { return (float *)(sW(k) + 64 * FP_IP); };             // [FP_KS][4]
+    auto sCB = [&](int k) { return sCW(k) + FP_KS * 4; };                         // [FP_KS]
+    // dt_proj phase (the same bytes)
+    constexpr int WS = RP + 4;
+    unsigned *sWd = (unsigned *)fp_smem;                       // [64][WS] tf32
+    unsigned *sDL = sWd + 64 * WS;                             // [RP][FP_IS] tf32
+    float *sOut = (float *)(sDL + RP * FP_IS);                 // [64][FP_OS]
+    float *sO = (float *)(fp_smem + fp_region<RP>());          // [64][FP_OP]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, tg = lane & 3;
+    const int wm = (warp % 4) * 16, wn = (warp / 4) * 32;
+    const int t0 = blockIdx.x * FP_T, b = blockIdx.y;
+    const int M = R + 2 * N, nsl = (D + FP_KS - 1) / FP_KS;
+    const long long xb = (long long)b * D * L;
+
+    // this thread's share of a slice: x window element i = tid + j * FP_NT
+    // (channel i / FP_XS, position i % FP_XS of the window), W_x element
+    // i = tid + j * FP_NT (row i / FP_KS, channel i % FP_KS).  Offsets and
+    // masks that do not depend on the slice are formed once.
+    int xo[FP_XV];                    // offset in x of the element, slice 0 (clamped in range)
+    unsigned xok = 0;                 // bit j: position inside the window and the sequence
+    // channel within the slice of element j (>= FP_KS: not an element)
+    auto xcc = [&](int j) {
+        const int i = tid + j * FP_NT;
+        return i < FP_KS * FP_XS ? i / FP_XS : FP_KS;
+    };
+#pragma unroll
+    for (int j = 0; j < FP_XV; ++j) {
+        const int i = tid + j * FP_NT, cc = i / FP_XS, pp = i % FP_XS, ts = t0 - 3 + pp;
+        const int tc = min(max(ts, 0), L - 1);
+        xo[j] = min(cc, FP_KS - 1) * L + (reverse ? L - 1 - tc : tc);
+        if (i < FP_KS * FP_XS && pp < FP_T + 3 && ts >= 0 && ts < L) xok |= 1u << j;
+    }
+    const int wk = tid % FP_KS;       // W_x column within the slice (rows tid / FP_KS + 8 j)
+    const IO *xbp = x + xb;
+    IO rx[FP_XV];
+    float rw[FP_WV], rc = 0.f;
+    auto fetch = [&](int s) {
+        const int c0 = s * FP_KS;
+        const int cmax = D - 1 - c0;              // last channel of the slice inside D
+        const IO *xs = xbp + (long long)c0 * L;
+#pragma unroll
+        for (int j = 0; j < FP_XV; ++j) {
+            // clamp the channel into range (masked at commit)
+            const int o = xcc(j) <= cmax ? xo[j] : xo[j] - (min(xcc(j), FP_KS - 1) - cmax) * L;
+            rx[j] = xs[o];
+        }
+        const int kc = min(c0 + wk, D - 1);
+#pragma unroll
+        for (int j = 0; j < FP_WV; ++j) {
+            const int m = min(tid / FP_KS + j * (FP_NT / FP_KS), M - 1);
+            rw[j] = Wx[(long long)m * D + kc];
+        }
+        if (tid < FP_KS * 5) {                       // 4 taps and the bias of each channel
+            const int c = min(c0 + tid % FP_KS, D - 1), q = tid / FP_KS;
+            rc = q < 4 ? cw[(long long)c * 4 + q] : (cb ? cb[c] : 0.f);
+        }
+    };
+    auto commit = [&](int s) {
+        const int c0 = s * FP_KS, cmax = D - 1 - c0, k = s & 1;
+        float *x_s = sx(k);
+#pragma unroll
+        for (int j = 0; j < FP_XV; ++j) {
+            const int i = tid + j * FP_NT;
+            if (i < FP_KS * FP_XS) x_s[i] = ((xok >> j) & 1u) && xcc(j) <= cmax ? to_f32(rx[j]) : 0.f;
+        }
+        const bool kin = wk <= cmax;
+        IO *w_s = sW(k);
+#pragma unroll
+        for (int j = 0; j < FP_WV; ++j) {
+            const int m = tid / FP_KS + j * (FP_NT / FP_KS);
+            w_s[m * FP_IP + wk] = from_f32<IO>((m < M && kin) ? rw[j] : 0.f);
+        }
+        if (tid < FP_KS * 5) {
+            const int cc = tid % FP_KS, q = tid / FP_KS;
+            const float v = cc <= cmax ? rc : 0.f;
+            if (q < 4) sCW(k)[cc * 4 + q] = v;
+            else sCB(k)[cc] = v;
+        }
+    };
+    // conv + SiLU: position cp of the tile, channels cg * 8 .. cg * 8 + 7 of the slice
+    const int cp = tid % FP_T, cg = tid / FP_T;
+    auto conv = [&](int s) {
+        const int c0 = s * FP_KS, t = t0 + cp, k = s & 1;
+        const float *x_s = sx(k), *cw_s = sCW(k), *cb_s = sCB(k);
+        IO res[8];
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+            const int cc = cg * 8 + c8;
+            const float4 w = *(const float4 *)&cw_s[cc * 4];
+            const float *xr = x_s + cc * FP_XS + cp;
+            float acc = cb_s[cc];
+            acc = fmaf(w.x, xr[0], acc);
+            acc = fmaf(w.y, xr[1], acc);
+            acc = fmaf(w.z, xr[2], acc);
+            acc = fmaf(w.w, xr[3], acc);
+            res[c8] = from_f32<IO>(silu_f<IO>(acc));
+            if (t < L && c0 + cc < D) u[xb + (long long)(c0 + cc) * L + t] = res[c8];
+        }
+        uint4 pk4;
+        pk4.x = (unsigned)*(const unsigned short *)&res[0] |
+                ((unsigned)*(const unsigned short *)&res[1] << 16);
+        pk4.y = (unsigned)*(const unsigned short *)&res[2] |
+                ((unsigned)*(const unsigned short *)&res[3] << 16);
+        pk4.z = (unsigned)*(const unsigned short *)&res[4] |
+                ((unsigned)*(const unsigned short *)&res[5] << 16);
+        pk4.w = (unsigned)*(const unsigned short *)&res[6] |
+                ((unsigned)*(const unsigned short *)&res[7] << 16);
+        *(uint4 *)&sI(k)[cp * FP_IP + cg * 8] = pk4;
+    };
+    float acc[4][4] = {};
+    fetch(0);
+    for (int s = 0; s < nsl; ++s) {
+        // slice s's buffers were last read by the mma of slice s - 2, two
+        // barriers ago
+        commit(s);
+        __syncthreads();
+        if (s + 1 < nsl) fetch(s + 1);              // in flight during this slice
+        conv(s);
+        __syncthreads();
+        const IO *w_s = sW(s & 1), *i_s = sI(s & 1);
+#pragma unroll
+        for (int ks = 0; ks < FP_KS; ks += 16) {
+            unsigned a[4];
+            a[0] = *(const unsigned *)&w_s[(wm + g) * FP_IP + ks + 2 * tg];
+            a[1] = *(const unsigned *)&w_s[(wm + g + 8) * FP_IP + ks + 2 * tg];
+            a[2] = *(const unsigned *)&w_s[(wm + g) * FP_IP + ks + 2 * tg + 8];
+            a[3] = *(const unsigned *)&w_s[(wm + g + 8) * FP_IP + ks + 2 * tg + 8];
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                unsigned bf[2];
+                const IO *col = i_s + (wn + nt * 8 + g) * FP_IP + ks + 2 * tg;
+                bf[0] = *(const unsigned *)col;
+                bf[1] = *(const unsigned *)(col + 8);
+                mma16816<IO>(acc[nt], a, bf);
+            }
+        }
+    }
+    __syncthreads();                                  // every warp past its last mma
+    // x_proj rows to shared memory: c0, c1 row g, positions 2tg, 2tg+1; c2,
+    // c3 row g + 8
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            *(float2 *)&sO[(wm + g + 8 * h) * FP_OP + wn + nt * 8 + 2 * tg] =
+                make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]);
+    __syncthreads();
+    // B and C (rows R .. R + 2N - 1) along positions; dt_low (rows 0 .. R-1,
+    // zero to RP) to tf32
+    for (int i = tid; i < 2 * N * FP_T; i += FP_NT) {
+        const int mm = i / FP_T, tt = i % FP_T, t = t0 + tt;
+        if (t < L) {
+            const IO v = from_f32<IO>(sO[(R + mm) * FP_OP + tt]);
+            if (mm < N) Bm[((long long)b * N + mm) * L + t] = v;
+            else Cm[((long long)b * N + mm - N) * L + t] = v;
+        }
+    }
+    for (int i = tid; i < RP * FP_T; i += FP_NT) {
+        const int r = i / FP_T, tt = i % FP_T;
+        sDL[r * FP_IS + tt] = to_tf32(r < R ? sO[r * FP_OP + tt] : 0.f);
+    }
+    // dt_proj in blocks of 64 rows
+    for (int mb = 0; mb < D; mb += 64) {
+        for (int i = tid; i < 64 * RP; i += FP_NT) {
+            const int mm = i / RP, r = i % RP, m = mb + mm;
+            sWd[mm * WS + r] = to_tf32((m < D && r < R) ? Wdt[(long long)m * R + r] : 0.f);
+        }
+        __syncthreads();
+        float dacc[4][4] = {};
+#pragma unroll
+        for (int ks = 0; ks < RP; ks += 8) {
+            // A (row): a0 (g, tg), a1 (g + 8, tg), a2 (g, tg + 4), a3 (g + 8, tg + 4)
+            const unsigned *wr = sWd + (wm + g) * WS + ks + tg;
+            const unsigned a[4] = {wr[0], wr[8 * WS], wr[4], wr[8 * WS + 4]};
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                // B (col): b0 (k = tg, n = g), b1 (k = tg + 4, n = g)
+                const unsigned *col = sDL + (ks + tg) * FP_IS + wn + nt * 8 + g;
+                const unsigned bf[2] = {col[0], col[4 * FP_IS]};
+                mma1688_tf32(dacc[nt], a, bf);
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                *(float2 *)&sOut[(wm + g + 8 * h) * FP_OS + wn + nt * 8 + 2 * tg] =
+                    make_float2(dacc[nt][2 * h], dacc[nt][2 * h + 1]);
+        __syncthreads();
+        for (int i = tid; i < 64 * FP_T; i += FP_NT) {
+            const int mm = i / FP_T, tt = i % FP_T, m = mb + mm, t = t0 + tt;
+            if (m < D && t < L) dt[xb + (long long)m * L + t] = from_f32<IO>(sOut[mm * FP_OS + tt]);
+        }
+        __syncthreads();
+    }
+}
+
 // x_proj on tensor cores, weights stationary (16-bit I/O, M <= 64 rows).  A
 // persistent CTA of 16 warps converts the whole W [M][K] to the I/O type
 // once into shared memory ([row][k], padded to KP), then loops over tiles

@@ -24,6 +24,17 @@ ssm_status last_error() {
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
+// Per-host-thread choice of the 1-D prologue's kernels
+// (ssm_set_prologue_fused): 1 automatic, 0 always the three-kernel path, 2
+// the fused kernel wherever it applies.
+thread_local int t_fused = 1;
+// Automatic choice: the fused kernel below this sequence length.  Measured on
+// B300 (bf16, 50k positions per call): fused / three-kernel time 0.39-0.44
+// at L = 197, 0.65-0.78 at 512, 0.91-1.13 at 1024, 1.10-1.42 from 2048 up
+// (the three-kernel conv streams long rows with wide CTAs; short rows
+// leave most of its threads idle).
+constexpr int kFusedMaxL = 1024;
+
 int sm_count() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -125,11 +136,44 @@ ssm_status dt_proj(int B, int nw, int D, int R, int L, const float *W, const flo
     return SSM_OK;
 }
 
+// the fused one-kernel prologue (16-bit I/O, 4 taps, x_proj rows <= 64,
+// dt_rank <= RP)
+template <typename IO, int RP>
+ssm_status launch_fused(int B, int D, int L, int N, int R, const void *x, const float *conv_w,
+                        const float *conv_b, const float *W_x, const float *W_dt, int reverse,
+                        void *u, void *dt, void *Bm, void *Cm, cudaStream_t st) {
+    using namespace ssm::pro;
+    constexpr size_t smem = fused_prologue_smem_bytes<RP>();
+    if (cudaFuncSetAttribute(fused_prologue_kernel<IO, RP>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    fused_prologue_kernel<IO, RP><<<dim3((L + FP_T - 1) / FP_T, B), FP_NT, smem, st>>>(
+        (const IO *)x, conv_w, conv_b, W_x, W_dt, D, L, N, R, reverse ? 1 : 0, (IO *)u, (IO *)dt,
+        (IO *)Bm, (IO *)Cm);
+    return last_error();
+}
+
 template <typename IO>
 ssm_status run(int B, int D, int L, int N, int R, int K, const void *x, const float *conv_w,
                const float *conv_b, const float *W_x, const float *W_dt, int reverse, void *u,
                void *dt, void *Bm, void *Cm, float *dt_low, cudaStream_t st) {
     using namespace ssm::pro;
+    if constexpr (sizeof(IO) == 2) {
+        if (K == 4 && R + 2 * N <= 64 && R <= 32 &&
+            (t_fused == 2 || (t_fused == 1 && L < kFusedMaxL))) {
+            if (R <= 8)
+                return launch_fused<IO, 8>(B, D, L, N, R, x, conv_w, conv_b, W_x, W_dt, reverse,
+                                           u, dt, Bm, Cm, st);
+            if (R <= 16)
+                return launch_fused<IO, 16>(B, D, L, N, R, x, conv_w, conv_b, W_x, W_dt, reverse,
+                                            u, dt, Bm, Cm, st);
+            if (R <= 24)
+                return launch_fused<IO, 24>(B, D, L, N, R, x, conv_w, conv_b, W_x, W_dt, reverse,
+                                            u, dt, Bm, Cm, st);
+            return launch_fused<IO, 32>(B, D, L, N, R, x, conv_w, conv_b, W_x, W_dt, reverse, u,
+                                        dt, Bm, Cm, st);
+        }
+    }
     const dim3 cgrid((L + CONV_T - 1) / CONV_T, D, B);
     if (K == 4)
         conv_silu_kernel<IO, 4><<<cgrid, 256, 0, st>>>((const IO *)x, conv_w, conv_b, (IO *)u, D,
@@ -240,6 +284,8 @@ ssm_status run_ss2d(int B, int D, int H, int W, int N, int R, int Kc, const void
 }  // namespace
 
 extern "C" {
+
+void ssm_set_prologue_fused(int mode) { t_fused = (mode == 0 || mode == 2) ? mode : 1; }
 
 size_t ssm_prologue_workspace_bytes(int B, int L, int R) {
     if (B < 0 || L < 0 || R <= 0) return (size_t)-1;

@@ -109,11 +109,24 @@ SHAPES = [(1, 5, 7, 4, 2, 4), (2, 70, 130, 16, 5, 4), (1, 33, 65, 32, 3, 3),
           (1, 48, 2100, 16, 40, 4)]
 
 
+@pytest.fixture(params=["fused", "three_kernel"])
+def path(request):
+    """The 1-D prologue's kernels for 16-bit I/O, forced: the fused
+    one-kernel path (where it applies: K = 4, R + 2N <= 64, R <= 32; at
+    every L) or the three-kernel path."""
+    import selective_state_space_111_b300 as ssm
+    ssm.set_prologue_fused(2 if request.param == "fused" else 0)
+    yield request.param
+    ssm.set_prologue_fused(1)
+
+
 @pytest.mark.parametrize("io", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("reverse", [False, True])
 @pytest.mark.parametrize("shape", SHAPES)
-def test_prologue_matches_oracle(io, reverse, shape):
+def test_prologue_matches_oracle(io, reverse, shape, path):
     import selective_state_space_111_b300 as ssm
+    if io == "f32" and path == "three_kernel":
+        pytest.skip("fp32 I/O has one path")
     B, D, L, N, R, K = shape
     g = torch.Generator().manual_seed(B * 1000 + D + L + 7 * reverse)
     x = torch.randn(B, D, L, generator=g).to(DT[io])
@@ -126,17 +139,18 @@ def test_prologue_matches_oracle(io, reverse, shape):
     check_prologue(io, (u, dt, Bm, Cm), ref, w, R, N)
 
 
-# Full size: B * ceil(L / 128) tiles of 128 positions on one persistent CTA
-# per SM -- Vim-S 1248^2 (384 tiles: two or three per CTA, a 69-position
-# tail) and a longer sequence (504 tiles: three or four per CTA, a
-# 1-position tail)
+# Full size.  Three-kernel path: B * ceil(L / 128) tiles of 128 positions on
+# one persistent x_proj CTA per SM -- Vim-S 1248^2 (384 tiles: two or three
+# per CTA, a 69-position tail) and a longer sequence (504 tiles: three or
+# four per CTA, a 1-position tail).  Fused path: B * ceil(L / 64) CTAs
+# (768: a 5-position tail; 1004: a 1-position tail), 24 and 4 channel slices.
 FULL = [(8, 768, 6085, 16, 24, 4), (4, 128, 16001, 16, 8, 4)]
 
 
 @pytest.mark.slow
 @pytest.mark.parametrize("reverse", [False, True])
 @pytest.mark.parametrize("shape", FULL)
-def test_prologue_full_size_multi_tile(shape, reverse):
+def test_prologue_full_size_multi_tile(shape, reverse, path):
     import selective_state_space_111_b300 as ssm
     B, D, L, N, R, K = shape
     g = torch.Generator().manual_seed(L + 3 * reverse)
@@ -289,7 +303,7 @@ def test_ss2d_inner_path_from_x(io):
     assert seq_err(y, ref_scan) <= TOL[io]              # the scan on what it was given
 
 
-def test_prologue_outputs_off_the_4_byte_grid():
+def test_prologue_outputs_off_the_4_byte_grid(path):
     # outputs one element into larger buffers (2-byte aligned only): the
     # pair stores must fall back to 2-byte stores; straight through the C ABI
     from selective_state_space_111_b300 import binding
