@@ -28,7 +28,7 @@ SOURCES = [os.path.join(HERE, "csrc", f) for f in ("ssm_scan_api.cu", "ssm_bwd_a
                                                    "ssm_prologue_api.cu")]
 DEPS = SOURCES + [os.path.join(HERE, "csrc", f) for f in
                   ("bidir_kernel.cuh", "bwd_kernel.cuh", "prologue_kernel.cuh",
-                   "scan_ops.cuh", "internal.h")] + [
+                   "scan_ops.cuh", "internal.h", "tc_ops.cuh")] + [
                   os.path.join(ROOT, "include", "ssm_scan.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 ALU_LIB = os.path.join(HERE, "libssm_alu.so")

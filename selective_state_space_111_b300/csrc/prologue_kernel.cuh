@@ -13,6 +13,7 @@
 #pragma once
 
 #include "scan_ops.cuh"
+#include "tc_ops.cuh"
 
 namespace ssm {
 namespace pro {
@@ -849,119 +850,150 @@ fused_prologue_kernel(const IO *__restrict__ x, const float *__restrict__ cw,
     }
 }
 
-// x_proj on tensor cores, weights stationary (16-bit I/O, M <= 64 rows).  A
-// persistent CTA of 16 warps converts the whole W [M][K] to the I/O type
-// once into shared memory ([row][k], padded to KP), then loops over tiles
-// of XP_T positions of one of the nb batch elements, streaming the input
-// in K slices of XP_K: the next slice is loaded into registers (64 KB in
-// flight per CTA) while the current one feeds the mma (warp w owns rows
-// 16 (w % 4) .. +16 and positions 32 (w / 4) .. +32).  Slices are stored
-// transposed, [position][k], two k per 32-bit word, so every fragment
-// register is one aligned 32-bit shared load (the PTX ISA's m16n8k16
-// fragment layouts).  The accumulators leave through a shared [row]
-// [position] fp32 tile so that the global stores run along positions.
-constexpr int XP_T = 128, XP_K = 256, XP_KP = XP_K + 8, XP_OP = XP_T + 8, XP_NT = 512;
-__host__ __device__ constexpr int xproj_kp(int K) { return ((K + XP_K - 1) / XP_K) * XP_K + 8; }
-inline size_t xproj_smem_bytes(int K, size_t esize) {
-    return (64 * (size_t)xproj_kp(K) + (size_t)XP_T * XP_KP) * esize;
+// Tiles of the SS2D x_proj below: XP_T positions per tile, XP_K-deep K
+// slices, XP_NT threads, XP_OP the fp32 output tile's row.
+constexpr int XP_T = 128, XP_K = 256, XP_OP = XP_T + 8, XP_NT = 512;
+
+// x_proj on the 5th-generation tensor cores (tcgen05, 16-bit I/O, M <= 64
+// rows): out[b][m][t] = sum_k W[m][k] u[b][k][t] as D[t][m] = U[t][k] W[m][k]
+// with MMA M = 128 positions, N = 64 rows, K = 16 per instruction and an
+// fp32 accumulator of 128 lanes x 64 columns in tensor memory.  A persistent
+// CTA of 16 warps (one per SM) keeps W (I/O type, zero-padded to 64 rows
+// and a multiple of 128 columns) in shared memory as the B operand in the
+// canonical K-major layout without swizzle (8 x 16-byte core matrices,
+// 128 bytes apart along K, 8-row groups KR * 16 bytes apart).  For each
+// tile of 128 positions it streams u in slices of 128 channels: the
+// threads load the next slice into registers (raw values, clamped
+// addresses) while the tensor core works on the current one, then store it
+// transposed into one of two A buffers (core matrices: 8 positions x 8
+// channels, 2048 bytes between 8-position groups); one thread issues the 8
+// MMAs of the slice and commits them to that buffer's mbarrier, which the
+// threads wait on before they overwrite the buffer two slices later.  After
+// a tile's last slice every warp reads its TMEM quarter (32 positions x 16
+// rows, tcgen05.ld) and stores along positions: coalesced, no staging tile.
+constexpr int TCX_T = 128, TCX_K = 128, TCX_NT = 512;
+__host__ __device__ constexpr int tcx_kr(int K) { return ((K + TCX_K - 1) / TCX_K) * TCX_K; }
+inline size_t xproj_tc_smem_bytes(int K) {
+    return (size_t)64 * tcx_kr(K) * 2 + 2 * (size_t)TCX_T * TCX_K * 2 + 64;
 }
 template <typename IO>
-__global__ void __launch_bounds__(XP_NT, 1)
-xproj_mma_kernel(const float *__restrict__ W, const IO *__restrict__ in, int M, int K, int L,
-                 int nb, ProjOut out) {
-    extern __shared__ __align__(16) unsigned char xp_smem[];
-    constexpr int NW = XP_NT / 32;                              // 16 warps
-    constexpr int PAIRS = XP_T * XP_K / 2 / XP_NT;              // k-pairs per thread per slice
-    const int KP = xproj_kp(K);
-    IO *sW = (IO *)xp_smem;                                    // [64][KP]
-    IO *sI = sW + 64 * KP;                                     // [XP_T][XP_KP]
-    float *sO = (float *)sI;                                   // [64][XP_OP], after a tile
+__global__ void __launch_bounds__(TCX_NT, 1)
+xproj_tc_kernel(const float *__restrict__ W, const IO *__restrict__ in, int M, int K, int L,
+                int nb, ProjOut out) {
+    static_assert(sizeof(IO) == 2, "16-bit I/O");
+    extern __shared__ __align__(1024) unsigned char tcx_smem[];
+    constexpr int PAIRS = TCX_T * TCX_K / 2 / TCX_NT;           // k-pairs per thread and slice
+    constexpr unsigned SBO_A = TCX_K / 8 * 128;                 // 2048: next 8 positions
+    constexpr int A_BYTES = TCX_T * TCX_K * 2;
+    const int KR = tcx_kr(K);
+    const unsigned SBO_W = (unsigned)KR / 8 * 128;              // next 8 rows of W
+    unsigned char *sW = tcx_smem;                               // [64 rows][KR], core matrices
+    unsigned char *sA = sW + 64 * KR * 2;                       // [2][128 positions][128]
+    uint64_t *bars = (uint64_t *)(sA + 2 * A_BYTES);            // one per A buffer
+    unsigned *tslot = (unsigned *)(bars + 2);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g = lane >> 2, tg = lane & 3;
-    const int wm = (warp % 4) * 16, wn = (warp / 4) * 32;
-    // W row by row (warp w takes rows w, w + NW, ...; lanes along k, four
-    // loads in flight each), zero past column K and past row M
-    for (int m = warp; m < 64; m += NW) {
-        IO *dst = sW + m * KP;
-        const float *src = W + (long long)m * K;
-        for (int k0 = 0; k0 < KP; k0 += 128) {
-            float wv[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int k = k0 + u * 32 + lane;
-                wv[u] = (m < M && k < K) ? src[k] : 0.f;
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int k = k0 + u * 32 + lane;
-                if (k < KP) dst[k] = from_f32<IO>(wv[u]);
-            }
-        }
+    // byte offset of element (row r, column k) of a K-major tile whose
+    // 8-row groups are sbo bytes apart
+    auto kmaj = [](int r, int k, unsigned sbo) {
+        return (int)((r >> 3) * sbo) + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
+    };
+    if (warp == 0) tc_alloc(tslot, 64);
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        fence_barrier_init();
     }
-    // slice loader: unit q = j * NW + warp covers 16 positions x 2 k-pairs;
-    // a lane loads the k-pair (2 kp, 2 kp + 1) of one position
+    // W: element (m, k), zero past row M and column K
+    for (int i = tid; i < 64 * KR / 2; i += TCX_NT) {
+        const int m = i / (KR / 2), k = 2 * (i % (KR / 2));
+        const float w0 = (m < M && k < K) ? W[(long long)m * K + k] : 0.f;
+        const float w1 = (m < M && k + 1 < K) ? W[(long long)m * K + k + 1] : 0.f;
+        const IO a = from_f32<IO>(w0), c = from_f32<IO>(w1);
+        *(unsigned *)(sW + kmaj(m, k, SBO_W)) =
+            (unsigned)*(const unsigned short *)&a | ((unsigned)*(const unsigned short *)&c << 16);
+    }
+    fence_proxy_async_shared();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const unsigned tmem = *tslot;
+    const unsigned idesc = tc_idesc<IO>(128, 64);
+    // slice loader: position tt, k-pairs kp0 + 4 j of the slice
     const int ld_tt = (warp % 8) * 16 + (lane & 15);
-    const int ld_kp0 = (warp / 8) * 2 + (lane >> 4);            // + 4 j
-    const int tpb = (L + XP_T - 1) / XP_T, ntiles = tpb * nb;
-    const int nk = (K + XP_K - 1) / XP_K;
+    const int ld_kp0 = (warp / 8) * 2 + (lane >> 4);
+    const int tpb = (L + TCX_T - 1) / TCX_T, ntiles = tpb * nb;
+    const int nk = KR / TCX_K;
+    IO r0[PAIRS], r1[PAIRS];
+    int it = 0;                        // slices issued by this CTA (buffer it & 1)
+    bool ok = true;                    // every wait finished in time
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-        const int b = tile / tpb, t0 = (tile % tpb) * XP_T;
-        const int t = t0 + ld_tt;
+        const int b = tile / tpb, t0 = (tile % tpb) * TCX_T;
+        const int t = min(t0 + ld_tt, L - 1);
+        const bool tin = t0 + ld_tt < L;
         const IO *src = in + (long long)b * K * L + t;
-        unsigned reg[PAIRS];
         auto load = [&](int k0) {
 #pragma unroll
             for (int j = 0; j < PAIRS; ++j) {
                 const int k = k0 + 2 * (ld_kp0 + 4 * j);
-                const IO z = from_f32<IO>(0.f);
-                const IO v0 = (t < L && k < K) ? src[(long long)k * L] : z;
-                const IO v1 = (t < L && k + 1 < K) ? src[(long long)(k + 1) * L] : z;
-                reg[j] = (unsigned)*(const unsigned short *)&v0 |
-                         ((unsigned)*(const unsigned short *)&v1 << 16);
+                r0[j] = src[(long long)min(k, K - 1) * L];
+                r1[j] = src[(long long)min(k + 1, K - 1) * L];
             }
         };
-        float acc[4][4] = {};
         load(0);
-        for (int ki = 0; ki < nk; ++ki) {
-            if (ki > 0) __syncthreads();                        // slice ki-1 fully read
-            unsigned *dst = (unsigned *)sI;
+        for (int ki = 0; ki < nk; ++ki, ++it) {
+            const int buf = it & 1;
+            unsigned char *a_s = sA + buf * A_BYTES;
+            // the mma that last read this buffer (two slices ago) is done
+            if (it >= 2) ok &= mbar_wait_bounded(&bars[buf], (unsigned)(((it >> 1) - 1) & 1));
+            const int k0 = ki * TCX_K;
 #pragma unroll
-            for (int j = 0; j < PAIRS; ++j) dst[ld_tt * (XP_KP / 2) + ld_kp0 + 4 * j] = reg[j];
+            for (int j = 0; j < PAIRS; ++j) {
+                const int kk = 2 * (ld_kp0 + 4 * j), k = k0 + kk;
+                const IO z = from_f32<IO>(0.f);
+                const IO v0 = (tin && k < K) ? r0[j] : z, v1 = (tin && k + 1 < K) ? r1[j] : z;
+                *(unsigned *)(a_s + kmaj(ld_tt, kk, SBO_A)) =
+                    (unsigned)*(const unsigned short *)&v0 |
+                    ((unsigned)*(const unsigned short *)&v1 << 16);
+            }
+            fence_proxy_async_shared();
+            tc_fence_before();
             __syncthreads();
-            if (ki + 1 < nk) load((ki + 1) * XP_K);               // in flight during the mma
+            tc_fence_after();
+            if (tid == 0) {
 #pragma unroll
-            for (int ks = 0; ks < XP_K; ks += 16) {
-                const int kw = ki * XP_K + ks;
-                unsigned a[4];
-                a[0] = *(const unsigned *)&sW[(wm + g) * KP + kw + 2 * tg];
-                a[1] = *(const unsigned *)&sW[(wm + g + 8) * KP + kw + 2 * tg];
-                a[2] = *(const unsigned *)&sW[(wm + g) * KP + kw + 2 * tg + 8];
-                a[3] = *(const unsigned *)&sW[(wm + g + 8) * KP + kw + 2 * tg + 8];
-#pragma unroll
-                for (int nt = 0; nt < 4; ++nt) {
-                    unsigned bf[2];
-                    const IO *col = sI + (wn + nt * 8 + g) * XP_KP + ks + 2 * tg;
-                    bf[0] = *(const unsigned *)col;
-                    bf[1] = *(const unsigned *)(col + 8);
-                    mma16816<IO>(acc[nt], a, bf);
+                for (int ks = 0; ks < TCX_K / 16; ++ks) {
+                    const unsigned long long ad = tc_desc(smem_addr(a_s) + ks * 256, 128, SBO_A);
+                    const unsigned long long bd =
+                        tc_desc(smem_addr(sW) + (unsigned)(k0 / 8 * 128) + ks * 256, 128, SBO_W);
+                    tc_mma(tmem, ad, bd, idesc, ki > 0 || ks > 0);
                 }
+                tc_commit(&bars[buf]);
+            }
+            if (ki + 1 < nk) load(k0 + TCX_K);              // in flight during the mma
+        }
+        // the tile's last slice (and so every earlier one) is done
+        ok &= mbar_wait_bounded(&bars[(it - 1) & 1], (unsigned)(((it - 1) >> 1) & 1));
+        tc_fence_after();
+        {
+            // warp w: TMEM lanes (positions) 32 (w % 4) .., columns (rows) 16 (w / 4) ..
+            const int q4 = warp % 4, m0 = 16 * (warp / 4);
+            float v[16];
+            tc_ld16(tmem + ((unsigned)(32 * q4) << 16) + (unsigned)m0, v);
+            const int tp = t0 + 32 * q4 + lane;
+            if (tp < L) {
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    if (m0 + q < M) proj_store<IO>(out, b, m0 + q, tp, L, v[q]);
             }
         }
-        __syncthreads();                                        // slice dead: reuse as sO
-        // c0, c1: row g, positions 2tg, 2tg+1; c2, c3: row g + 8
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-            for (int half = 0; half < 2; ++half)
-                *(float2 *)&sO[(wm + g + 8 * half) * XP_OP + wn + nt * 8 + 2 * tg] =
-                    make_float2(acc[nt][2 * half], acc[nt][2 * half + 1]);
+        // every warp has read TMEM before the next tile's first mma overwrites it
+        tc_fence_before();
         __syncthreads();
-        for (int i = tid; i < M * XP_T; i += XP_NT) {
-            const int m = i / XP_T, tt = i % XP_T, tp = t0 + tt;
-            if (tp < L) proj_store<IO>(out, b, m, tp, L, sO[m * XP_OP + tt]);
-        }
-        __syncthreads();                                        // sO dead before the next slice
+        tc_fence_after();
     }
+    (void)ok;
+    __syncthreads();
+    if (warp == 0) tc_dealloc(tmem, 64);
 }
 
 // SS2D x_proj for all four scan directions in one pass over u (16-bit I/O,

@@ -53,22 +53,22 @@ void launch_proj(dim3 grid, const float *W, const IN *in, int M, int K, int L, l
         ssm::pro::proj_mma_kernel<IN, IO><<<grid, 256, 0, st>>>(W, in, M, K, L, ib, o);
 }
 
-// x_proj: the weights-stationary tensor-core kernel when its rows (<= 64)
-// and W (in shared memory) fit, else the generic tiled one
+// x_proj: the weights-stationary tcgen05 kernel when its rows (<= 64) and W
+// (in shared memory) fit, else the generic tiled one
 template <typename IO>
 ssm_status x_proj(int B, int M, int K, int L, const float *W, const IO *u, ssm::pro::ProjOut o,
                   cudaStream_t st) {
     using namespace ssm::pro;
     if constexpr (sizeof(IO) == 2) {
-        const size_t smem = xproj_smem_bytes(K, sizeof(IO));
+        const size_t smem = xproj_tc_smem_bytes(K);
         if (M <= 64 && smem <= 227 * 1024) {
-            if (cudaFuncSetAttribute(xproj_mma_kernel<IO>,
+            if (cudaFuncSetAttribute(xproj_tc_kernel<IO>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)smem) != cudaSuccess)
                 return SSM_ERR_CUDA;
-            const long long tiles = (long long)B * ((L + XP_T - 1) / XP_T);
+            const long long tiles = (long long)B * ((L + TCX_T - 1) / TCX_T);
             const int grid = (int)std::min<long long>(tiles, sm_count());
-            xproj_mma_kernel<IO><<<grid, XP_NT, smem, st>>>(W, u, M, K, L, B, o);
+            xproj_tc_kernel<IO><<<grid, TCX_NT, smem, st>>>(W, u, M, K, L, B, o);
             return last_error();
         }
     }
