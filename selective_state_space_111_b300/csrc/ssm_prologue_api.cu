@@ -175,7 +175,16 @@ ssm_status run(int B, int D, int L, int N, int R, int K, const void *x, const fl
         }
     }
     const dim3 cgrid((L + CONV_T - 1) / CONV_T, D, B);
-    if (K == 4)
+    bool done = false;
+    if constexpr (sizeof(IO) == 2) {
+        if (K == 4) {
+            conv_silu_vec_kernel<IO><<<cgrid, 256, 0, st>>>((const IO *)x, conv_w, conv_b,
+                                                            (IO *)u, D, L, reverse ? 1 : 0);
+            done = true;
+        }
+    }
+    if (done) {
+    } else if (K == 4)
         conv_silu_kernel<IO, 4><<<cgrid, 256, 0, st>>>((const IO *)x, conv_w, conv_b, (IO *)u, D,
                                                        L, K, reverse ? 1 : 0);
     else
