@@ -39,6 +39,12 @@ dt_proj per scan direction):
   xs_k    = u flattened in direction k's scan order (k = 0 row-major,
             1 column-major, 2 and 3 their reversals)
   proj_k  = W_x[k] @ xs_k, split as in the 1D case; dt_k = W_dt[k] @ dt_low_k
+
+The block's output projection ("VMamba的SS2D模块详解" section 2.1: after the
+gate y * act(z), out_proj = Linear(d_inner -> d_model); the pages show no
+bias -- reading: none, as in Mamba), on the library's [B, D, L] layout:
+
+  out[b][m][t] = sum_k W_out[m][k] * y[b][k][t]
 """
 from __future__ import annotations
 
@@ -127,3 +133,8 @@ def ss2d_prologue(x, conv_w, conv_b, W_x, W_dt, dt_rank, d_state, silu_act=True)
         Bm[:, k], Cm[:, k] = proj[:, R:R + N], proj[:, R + N:R + 2 * N]
         delta[:, k] = np.einsum("dr,brl->bdl", W_dt[k], proj[:, :R])
     return u, delta, Bm, Cm
+
+
+def out_proj(y, W_out):
+    """[B, d_model, L] = W_out [d_model, d_inner] applied to y [B, d_inner, L]."""
+    return np.einsum("mk,bkl->bml", _f64(W_out), _f64(y))

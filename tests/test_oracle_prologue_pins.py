@@ -164,3 +164,33 @@ def test_ss2d_silu_flag_and_activation():
     u1, *_ = pro.ss2d_prologue(x, cw, None, W_x, W_dt, 1, 2, silu_act=True)
     np.testing.assert_allclose(u0, pro.depthwise_conv2d(x, cw), rtol=0, atol=0)
     np.testing.assert_allclose(u1, u0 / (1.0 + np.exp(-u0)), rtol=1e-15, atol=0)
+
+
+def test_out_proj_with_selection_weights():
+    # W_out rows pick and scale channels (a wrong operand order or a
+    # transposed W fails): out[0] = y[2], out[1] = -3 y[0], out[2] = y[1] + y[3]
+    rng = np.random.default_rng(11)
+    y = rng.normal(size=(2, 4, 7))
+    W = np.zeros((3, 4))
+    W[0, 2] = 1.0
+    W[1, 0] = -3.0
+    W[2, 1] = W[2, 3] = 1.0
+    out = pro.out_proj(y, W)
+    assert out.shape == (2, 3, 7)
+    np.testing.assert_array_equal(out[:, 0], y[:, 2])
+    np.testing.assert_array_equal(out[:, 1], -3.0 * y[:, 0])
+    np.testing.assert_array_equal(out[:, 2], y[:, 1] + y[:, 3])
+
+
+def test_out_proj_is_position_independent_and_linear():
+    # each position is W @ y[:, :, t] (brute force per position) and the
+    # map is linear in y
+    rng = np.random.default_rng(12)
+    y1, y2 = rng.normal(size=(1, 5, 6)), rng.normal(size=(1, 5, 6))
+    W = rng.normal(size=(4, 5))
+    out = pro.out_proj(y1, W)
+    for t in range(6):
+        ref = [sum(W[m, k] * y1[0, k, t] for k in range(5)) for m in range(4)]
+        np.testing.assert_allclose(out[0, :, t], ref, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(pro.out_proj(2.0 * y1 + y2, W), 2.0 * out + pro.out_proj(y2, W),
+                               rtol=1e-12, atol=1e-12)
