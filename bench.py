@@ -48,6 +48,15 @@ def peaks():
     return 6400.0, 2032.0, "fallback"
 
 
+def bf16_peak_tflops():
+    """Dense bf16 tensor peak for a kernel timed on its own (burst)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            return float(json.load(fh)["bf16_tflops"]), "measured"
+    return 1800.0, "fallback"
+
+
 # ---------------------------------------------------------------- GPU arm
 def launches_per_step(op):
     """Kernels one call launches: B/C packing (one launch for every B/C
@@ -348,6 +357,11 @@ def run_ours(args):
         torch.cuda.nvtx.range_push("prologue")
         pro = measure_prologue(ssm, spec, dev, stream, max(3, min(args.steps, 20)))
         torch.cuda.nvtx.range_pop()
+    opj = None
+    if not args.no_out_proj:
+        torch.cuda.nvtx.range_push("out_proj")
+        opj = measure_out_proj(ssm, spec, dev, stream, max(3, min(args.steps, 20)))
+        torch.cuda.nvtx.range_pop()
 
     if rank == 0:
         ms = total_ms / args.steps
@@ -429,6 +443,16 @@ def run_ours(args):
                                "peak_kind": peak_kind,
                                "tflops": round(pro.pop("tflops"), 3)}
             line["prologue"] = pro
+        if opj:
+            # a dense contraction (d_inner -> d_model per position): its roof
+            # is the tensor peak of its dtype (fp16 at bf16's rate); the
+            # HBM fraction of its bytes is reported beside it
+            tpk, tkind = bf16_peak_tflops()
+            opj["roofline"] = {"bound": "tensor", "achieved": opj["tflops"], "peak": tpk,
+                               "unit": "TFLOP/s", "frac": round(opj["tflops"] / tpk, 4),
+                               "peak_kind": tkind,
+                               "hbm_frac": round(opj["value"] / hbm_peak, 4)}
+            line["out_proj"] = opj
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(spec, args.workload, args.cpu_seconds)
             line["cpu_baseline_single_thread"] = cpu_baseline(spec, args.workload,
@@ -482,6 +506,35 @@ def measure_backward(ssm, spec, g, t, dev, stream, steps):
     return {"ms_per_call": round(ms, 4), "ms": ms, "steps": steps,
             "bytes_per_call": spec.backward_bytes(),
             "elem_updates_per_s": float("%.4g" % (spec.updates() / (ms * 1e-3)))}
+
+
+def measure_out_proj(ssm, spec, dev, stream, steps):
+    """Time the block's output projection (d_inner -> d_model = d_inner / 2,
+    the pages' ssm_ratio / expand of 2) on a gated output of the workload's
+    shape: out = W_out y, synthetic weights in the I/O dtype."""
+    import torch
+    B, D, L = spec.B, spec.D, spec.seq_len
+    Dm = D // 2
+    gen = torch.Generator().manual_seed(2468)
+    io = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[spec.io]
+    y = torch.randn(B, D, L, generator=gen).to(dtype=io, device=dev)
+    W = (torch.randn(Dm, D, generator=gen) * D ** -0.5).to(dtype=io, device=dev)
+    for _ in range(3):
+        ssm.out_proj_fwd(y, W)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        ssm.out_proj_fwd(y, W)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    e = y.element_size()
+    nbytes = e * (B * D * L + Dm * D + B * Dm * L)        # y and W read, out written
+    flops = 2.0 * B * L * D * Dm
+    return {"ms_per_call": round(ms, 4), "d_inner": D, "d_model": Dm,
+            "value": round(nbytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "tflops": round(flops / (ms * 1e-3) / 1e12, 2)}
 
 
 def measure_prologue(ssm, spec, dev, stream, steps):
@@ -692,6 +745,8 @@ def main():
                     help="skip the backward-pass timing (reported under 'backward')")
     ap.add_argument("--no-prologue", action="store_true",
                     help="skip the prologue timing (reported under 'prologue')")
+    ap.add_argument("--no-out-proj", action="store_true",
+                    help="skip the output-projection timing (reported under 'out_proj')")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--min-seconds", type=float, default=1.5,
                     help="repeat the K-step timed window until this much device time "

@@ -454,6 +454,24 @@ SSM_API ssm_status ss2d_prologue_fwd(ssm_dtype dt, int B, int D, int H, int W,
                          void *workspace, size_t ws_bytes, ssm_stream_t stream);
 SSM_API size_t ss2d_prologue_workspace_bytes(int B, int H, int W, int R);
 
+/* ---------------------------------------------------------------------------
+ * The block's output projection ("VMamba的SS2D模块详解" section 2.1: after the
+ * gate y * act(z), out_proj = Linear(d_inner -> d_model), no bias):
+ *   out[b][m][t] = sum_k W_out[m][k] * y[b][k][t]
+ * y [B, Di, L] (the gated output of a scan call), W_out [Dm, Di] and out
+ * [B, Dm, L], all in the I/O dtype; device pointers, caller-owned.
+ * Arithmetic: fp32 accumulation; with 16-bit I/O, Dm <= 512, Di a multiple
+ * of 8 and W_out 16-byte aligned on the tcgen05 tensor cores (fp32
+ * accumulator in tensor memory), otherwise tiled (mma.sync for 16-bit I/O,
+ * fp32 FMA for fp32 I/O); out is rounded to the I/O dtype.  No workspace.
+ * Errors: SSM_ERR_INVALID_ARG for a bad dtype, size or pointer (NULL or
+ * misaligned); SSM_ERR_UNSUPPORTED for B > 65535 or Di * L, Dm * L or
+ * Dm * Di past the 32-bit index range; SSM_ERR_CUDA for a launch error.  Asynchronous on
+ * `stream`.
+ * ------------------------------------------------------------------------- */
+SSM_API ssm_status out_proj_fwd(ssm_dtype dt, int B, int Di, int Dm, int L, const void *y,
+                                const void *W_out, void *out, ssm_stream_t stream);
+
 /*
  * Tuning override for the two-branch kernels (v1, v2 and both SS2D passes).
  * A CTA takes `channels` channels of one batch element, both branches:

@@ -73,6 +73,8 @@ def _declare(lib):
     lib.ss2d_scan_bwd.argtypes = [_i] * 7 + [_vp] * 8 + [_i] + [_vp] * 10 + [_sz, _vp]
     lib.mamba_prologue_fwd.argtypes = [_i] * 7 + [_vp] * 5 + [_i] + [_vp] * 5 + [_sz, _vp]
     lib.mamba_prologue_fwd.restype = _i
+    lib.out_proj_fwd.argtypes = [_i] * 5 + [_vp] * 4
+    lib.out_proj_fwd.restype = _i
     lib.ssm_prologue_workspace_bytes.argtypes = [_i, _i, _i]
     lib.ssm_prologue_workspace_bytes.restype = _sz
     lib.ss2d_prologue_fwd.argtypes = [_i] * 8 + [_vp] * 5 + [_i] + [_vp] * 5 + [_sz, _vp]
@@ -536,6 +538,22 @@ def mamba_prologue_fwd(x, conv_w, conv_b, W_x, W_dt, dt_rank, d_state, reverse=F
                                    workspace.numel() * workspace.element_size(),
                                    _stream(stream)), "mamba_prologue_fwd")
     return u, delta, Bm, Cm
+
+
+def out_proj_fwd(y, W_out, stream=None):
+    """The block's output projection: out[b, m, t] = sum_k W_out[m, k] y[b, k, t].
+    y: [Bt, Di, L] (I/O dtype, the gated scan output); W_out [Dm, Di] in the
+    same dtype.  Returns out [Bt, Dm, L]."""
+    io = y.dtype
+    Bt, Di, L = y.shape
+    if W_out.dim() != 2 or W_out.shape[1] != Di:
+        raise ValueError("W_out: expected [Dm, %d], got %s" % (Di, tuple(W_out.shape)))
+    Dm = W_out.shape[0]
+    out = torch.empty((Bt, Dm, L), dtype=io, device=y.device)
+    _check(_lib.out_proj_fwd(_dtype_code(y), Bt, Di, Dm, L, _io(y, io, "y"),
+                             _io(W_out, io, "W_out"), out.data_ptr(), _stream(stream)),
+           "out_proj_fwd")
+    return out
 
 
 def ss2d_prologue_fwd(x, conv_w, conv_b, W_x, W_dt, dt_rank, d_state, silu_act=True,

@@ -377,9 +377,9 @@ constexpr int BM = 64, BN = 64, BK = 16;
 // out[b][m][t] = sum_k W[m][k] * in[b][k][t]: W fp32 [M][K], in [B][K][L]
 // with batch stride ib (I/O dtype or fp32).  Tile 64 x 64 per CTA, 16-deep K slices through
 // shared memory, 4 x 4 outputs per thread (fp32 FMA).
-template <typename IN, typename IO>
+template <typename IN, typename IO, typename WT = float>
 __global__ void __launch_bounds__(256)
-proj_kernel(const float *__restrict__ W, const IN *__restrict__ in, int M, int K, int L,
+proj_kernel(const WT *__restrict__ W, const IN *__restrict__ in, int M, int K, int L,
             long long ib, ProjOut out) {
     __shared__ float sW[BK][BM + 4];
     __shared__ __align__(16) float sI[BK][BN + 4];
@@ -392,7 +392,7 @@ proj_kernel(const float *__restrict__ W, const IN *__restrict__ in, int M, int K
         for (int r = 0; r < (BM * BK) / 256; ++r) {
             const int i = tid + r * 256, mm = i / BK, kk = i % BK;
             const int m = m0 + mm, k = k0 + kk;
-            sW[kk][mm] = (m < M && k < K) ? W[(long long)m * K + k] : 0.f;
+            sW[kk][mm] = (m < M && k < K) ? to_f32(W[(long long)m * K + k]) : 0.f;
         }
 #pragma unroll
         for (int r = 0; r < (BK * BN) / 256; ++r) {
@@ -459,9 +459,9 @@ template <> __device__ __forceinline__ void mma16816<__half>(float (&c)[4], cons
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-template <typename IN, typename IO>
+template <typename IN, typename IO, typename WT = float>
 __global__ void __launch_bounds__(256)
-proj_mma_kernel(const float *__restrict__ W, const IN *__restrict__ in, int M, int K, int L,
+proj_mma_kernel(const WT *__restrict__ W, const IN *__restrict__ in, int M, int K, int L,
                 long long ib, ProjOut out) {
     __shared__ __align__(16) IO sW[BM][TKP];        // [row][k]
     __shared__ __align__(16) IO sI[BN][TKP];        // [position][k]
@@ -477,7 +477,7 @@ proj_mma_kernel(const float *__restrict__ W, const IN *__restrict__ in, int M, i
         for (int r = 0; r < (BM * TK) / 256; ++r) {
             const int i = tid + r * 256, mm = i / TK, kk = i % TK;
             const int m = m0 + mm, k = k0 + kk;
-            sW[mm][kk] = from_f32<IO>((m < M && k < K) ? W[(long long)m * K + k] : 0.f);
+            sW[mm][kk] = from_f32<IO>((m < M && k < K) ? to_f32(W[(long long)m * K + k]) : 0.f);
         }
         // input slice: 32 x 64 (positions fastest: coalesced), stored transposed
 #pragma unroll
@@ -1098,6 +1098,178 @@ xproj_tc_kernel(const float *__restrict__ W, const IO *__restrict__ in, int M, i
     (void)ok;
     __syncthreads();
     if (warp == 0) tc_dealloc(tmem, 64);
+}
+
+// The block's output projection on tcgen05 (16-bit I/O, d_model <= 512,
+// d_inner a multiple of 8): out[b][m][t] = sum_k W[m][k] y[b][k][t]
+// ("VMamba的SS2D模块详解" section 2.1: out_proj = Linear(d_inner -> d_model)
+// after the gate), as D[t][m] = Y[t][k] W[m][k]: MMA M = 128 positions, N in
+// chunks of 128 rows (every d_model row of a tile: NCH chunks, 128 * NCH
+// TMEM columns), K = 16 per instruction, fp32 accumulator in tensor memory.
+// A persistent CTA of 16 warps walks one stream of slices (64 channels of
+// one tile of 128 positions) over its tiles.  W (I/O dtype) goes straight
+// from global memory into the K-major no-swizzle layout by 16-byte
+// cp.async (one core-matrix row = 8 consecutive k of one row; zero-filled
+// past d_inner), issued one slice ahead; y goes through registers
+// (transposed, raw values from clamped addresses, one slice ahead).  Two
+// buffer sets: one thread issues a slice's 4 * NCH MMAs and commits them
+// to the set's mbarrier, which gates the set's next refill.  The epilogue
+// reads TMEM (warp w: lanes 32 (w % 4), a quarter of the columns) and
+// stores along positions.
+constexpr int OP_T = 128, OP_K = 64, OP_NT = 512, OP_MAXN = 512;
+template <int NCH> __host__ __device__ constexpr size_t out_proj_smem_bytes() {
+    return 2 * ((size_t)OP_T * OP_K * 2 + (size_t)NCH * 128 * OP_K * 2) + 64;
+}
+__device__ __forceinline__ void cp_async16_zfill(void *smem, const void *gmem, bool full) {
+    unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem),
+                 "r"(full ? 16 : 0)
+                 : "memory");
+}
+template <typename IO, int NCH>
+__global__ void __launch_bounds__(OP_NT, 1)
+out_proj_tc_kernel(const IO *__restrict__ W, const IO *__restrict__ y, int Dm, int Di, int L,
+                   int nb, IO *__restrict__ out) {
+    static_assert(sizeof(IO) == 2, "16-bit I/O");
+    extern __shared__ __align__(1024) unsigned char op_smem[];
+    constexpr int NR = NCH * 128;                               // rows of the MMA's N
+    constexpr int A_BYTES = OP_T * OP_K * 2, W_BYTES = NR * OP_K * 2;
+    constexpr int SET = A_BYTES + W_BYTES;
+    constexpr unsigned SBO = OP_K / 8 * 128;                    // 1024: next 8 rows
+    constexpr int AP = OP_T * OP_K / 2 / OP_NT;                 // y k-pairs per thread: 8
+    constexpr int WC = NR * (OP_K / 8) / OP_NT;                 // W 16-byte chunks per thread
+    uint64_t *bars = (uint64_t *)(op_smem + 2 * SET);
+    unsigned *tslot = (unsigned *)(bars + 2);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    auto kmaj = [](int r, int k) {
+        return (r >> 3) * (int)SBO + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
+    };
+    constexpr unsigned TCOLS = NR <= 128 ? 128 : NR <= 256 ? 256 : 512;
+    if (warp == 0) tc_alloc(tslot, TCOLS);
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        fence_barrier_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const unsigned tmem = *tslot;
+    const unsigned idesc = tc_idesc<IO>(128, 128);
+    const int ld_tt = (warp % 8) * 16 + (lane & 15);
+    const int ld_kp0 = (warp / 8) * 2 + (lane >> 4);
+    const int tpb = (L + OP_T - 1) / OP_T, ntiles = tpb * nb;
+    const int nk = (Di + OP_K - 1) / OP_K;
+    const int my_tiles =
+        (int)blockIdx.x < ntiles ? (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int nslices = my_tiles * nk;
+    IO ry0[AP], ry1[AP];
+    // slice g: tile blockIdx.x + (g / nk) * gridDim.x, channels (g % nk) * OP_K ..
+    auto load_y = [&](int g) {
+        const int tile = blockIdx.x + (g / nk) * gridDim.x, k0 = (g % nk) * OP_K;
+        const int b = tile / tpb, t = min((tile % tpb) * OP_T + ld_tt, L - 1);
+        const IO *src = y + (long long)b * Di * L + t;
+#pragma unroll
+        for (int j = 0; j < AP; ++j) {
+            const int k = k0 + 2 * (ld_kp0 + 4 * j);
+            ry0[j] = src[(long long)min(k, Di - 1) * L];
+            ry1[j] = src[(long long)min(k + 1, Di - 1) * L];
+        }
+    };
+    // W rows 0 .. NR-1, channels k0 .. k0 + 63 of slice g into set `set`
+    auto issue_w = [&](int g, int set) {
+        const int k0 = (g % nk) * OP_K;
+        unsigned char *w_s = op_smem + set * SET + A_BYTES;
+#pragma unroll
+        for (int j = 0; j < WC; ++j) {
+            // a warp instruction: rows 8 q .. 8 q + 7 (lanes % 8) x chunks
+            // kc = 0..3 or 4..7 (lanes / 8): 512 contiguous shared bytes, and
+            // each row's 64 global bytes read by one instruction
+            const int c = tid + j * OP_NT, R = c / 32;
+            const int n = 8 * (R / 2) + c % 8, kc = (c / 8) % 4 + 4 * (R % 2);
+            const int k = k0 + 8 * kc;
+            const bool full = n < Dm && k < Di;
+            const IO *src = W + (long long)min(n, Dm - 1) * Di + min(k, Di - 8);
+            cp_async16_zfill(w_s + kmaj(n, 8 * kc), src, full);
+        }
+        cp_async_commit();
+    };
+    bool ok = true;
+    if (nslices > 0) {
+        issue_w(0, 0);
+        load_y(0);
+    }
+    for (int g = 0; g < nslices; ++g) {
+        const int tile = blockIdx.x + (g / nk) * gridDim.x, ki = g % nk, k0 = ki * OP_K;
+        const int b = tile / tpb, t0 = (tile % tpb) * OP_T;
+        const bool tin = t0 + ld_tt < L;
+        const int set = g & 1;
+        unsigned char *a_s = op_smem + set * SET, *w_s = a_s + A_BYTES;
+        // (this set's previous mma, slice g - 2, was waited for before its W refill)
+        const IO z = from_f32<IO>(0.f);
+#pragma unroll
+        for (int j = 0; j < AP; ++j) {
+            const int kk = 2 * (ld_kp0 + 4 * j), k = k0 + kk;
+            const IO v0 = (tin && k < Di) ? ry0[j] : z, v1 = (tin && k + 1 < Di) ? ry1[j] : z;
+            *(unsigned *)(a_s + kmaj(ld_tt, kk)) =
+                (unsigned)*(const unsigned short *)&v0 |
+                ((unsigned)*(const unsigned short *)&v1 << 16);
+        }
+        cp_async_wait<0>();                                    // W of slice g has landed
+        fence_proxy_async_shared();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {
+#pragma unroll
+            for (int ks = 0; ks < OP_K / 16; ++ks) {
+                const unsigned long long ad = tc_desc(smem_addr(a_s) + ks * 256, 128, SBO);
+#pragma unroll
+                for (int c = 0; c < NCH; ++c) {
+                    const unsigned long long bd =
+                        tc_desc(smem_addr(w_s) + c * 128 * (OP_K * 2) + ks * 256, 128, SBO);
+                    tc_mma(tmem + 128 * c, ad, bd, idesc, ki > 0 || ks > 0);
+                }
+            }
+            tc_commit(&bars[set]);
+        }
+        if (g + 1 < nslices) {
+            // the other set's last mma (slice g - 1) is done before it is refilled
+            const int nset = (g + 1) & 1;
+            if (g >= 1) ok &= mbar_wait_bounded(&bars[nset], (unsigned)(((g - 1) >> 1) & 1));
+            issue_w(g + 1, nset);
+            load_y(g + 1);
+        }
+        if (ki == nk - 1) {
+            // the tile's last slice (and so every earlier one) is done
+            ok &= mbar_wait_bounded(&bars[set], (unsigned)((g >> 1) & 1));
+            tc_fence_after();
+            // warp w: TMEM lanes (positions) 32 (w % 4) .., columns (rows)
+            // (w / 4) * NR / 4 .. + NR / 4
+            const int q4 = warp % 4, tp = t0 + 32 * q4 + lane;
+#pragma unroll 1
+            for (int h = 0; h < NR / 4 / 16; ++h) {
+                const int m0 = (warp / 4) * (NR / 4) + 16 * h;
+                if (m0 >= Dm) break;                               // uniform over the warp
+                float v[16];
+                tc_ld16(tmem + ((unsigned)(32 * q4) << 16) + (unsigned)m0, v);
+                if (tp < L) {
+#pragma unroll
+                    for (int q = 0; q < 16; ++q)
+                        if (m0 + q < Dm)
+                            out[((long long)b * Dm + m0 + q) * L + tp] = from_f32<IO>(v[q]);
+                }
+            }
+            // every warp has read TMEM before the next tile's first mma overwrites it
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+        }
+    }
+    (void)ok;
+    cp_async_wait<0>();
+    __syncthreads();
+    if (warp == 0) tc_dealloc(tmem, TCOLS);
 }
 
 // SS2D x_proj for all four scan directions in one pass over u (16-bit I/O,

@@ -44,13 +44,14 @@ int sm_count() {
 }
 
 // generic tiled projection: fp32 FMA for fp32 I/O, mma.sync for 16-bit I/O
-template <typename IN, typename IO>
-void launch_proj(dim3 grid, const float *W, const IN *in, int M, int K, int L, long long ib,
+// (weights fp32, or WT)
+template <typename IN, typename IO, typename WT = float>
+void launch_proj(dim3 grid, const WT *W, const IN *in, int M, int K, int L, long long ib,
                  ssm::pro::ProjOut o, cudaStream_t st) {
     if constexpr (sizeof(IO) == 4)
-        ssm::pro::proj_kernel<IN, IO><<<grid, 256, 0, st>>>(W, in, M, K, L, ib, o);
+        ssm::pro::proj_kernel<IN, IO, WT><<<grid, 256, 0, st>>>(W, in, M, K, L, ib, o);
     else
-        ssm::pro::proj_mma_kernel<IN, IO><<<grid, 256, 0, st>>>(W, in, M, K, L, ib, o);
+        ssm::pro::proj_mma_kernel<IN, IO, WT><<<grid, 256, 0, st>>>(W, in, M, K, L, ib, o);
 }
 
 // x_proj: the weights-stationary tcgen05 kernel when its rows (<= 64) and W
@@ -290,6 +291,49 @@ ssm_status run_ss2d(int B, int D, int H, int W, int N, int R, int Kc, const void
     return dt_proj<IO>(B, 4, D, R, L, W_dt, dt_low, (IO *)delta, st);
 }
 
+
+// out_proj: the tcgen05 kernel for 16-bit I/O and d_model <= 512 (NCH
+// chunks of 128 rows), else the generic tiled projection
+template <typename IO, int NCH>
+ssm_status launch_out_proj(int B, int Di, int Dm, int L, const void *y, const IO *W,
+                           void *out, cudaStream_t st) {
+    using namespace ssm::pro;
+    constexpr size_t smem = out_proj_smem_bytes<NCH>();
+    if (cudaFuncSetAttribute(out_proj_tc_kernel<IO, NCH>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    const long long tiles = (long long)B * ((L + OP_T - 1) / OP_T);
+    const int grid = (int)std::min<long long>(tiles, sm_count());
+    out_proj_tc_kernel<IO, NCH><<<grid, OP_NT, smem, st>>>(W, (const IO *)y, Dm, Di, L, B,
+                                                           (IO *)out);
+    return last_error();
+}
+template <typename IO>
+ssm_status out_proj_run(int B, int Di, int Dm, int L, const void *y, const void *Wv, void *out,
+                        cudaStream_t st) {
+    using namespace ssm::pro;
+    const IO *W = (const IO *)Wv;
+    if constexpr (sizeof(IO) == 2) {
+        // W rows are copied as 16-byte chunks: Di a multiple of 8 and W
+        // 16-byte aligned, so that every row starts on a 16-byte boundary
+        if (Di % 8 == 0 && aligned(W, 16)) {
+            if (Dm <= 128) return launch_out_proj<IO, 1>(B, Di, Dm, L, y, W, out, st);
+            if (Dm <= 256) return launch_out_proj<IO, 2>(B, Di, Dm, L, y, W, out, st);
+            if (Dm <= 384) return launch_out_proj<IO, 3>(B, Di, Dm, L, y, W, out, st);
+            if (Dm <= OP_MAXN) return launch_out_proj<IO, 4>(B, Di, Dm, L, y, W, out, st);
+        }
+    }
+    ProjOut o{};
+    o.dst[0] = out;
+    o.r[0] = 0;
+    o.r[1] = o.r[2] = o.r[3] = Dm;
+    o.bstride[0] = (long long)Dm * L;
+    o.order = -1;
+    launch_proj<IO, IO, IO>(dim3((L + BN - 1) / BN, (Dm + BM - 1) / BM, B), W, (const IO *)y, Dm,
+                            Di, L, (long long)Di * L, o, st);
+    return last_error();
+}
+
 }  // namespace
 
 extern "C" {
@@ -366,6 +410,21 @@ ssm_status ss2d_prologue_fwd(ssm_dtype dt, int B, int D, int H, int W, int N, in
                                 Bm, Cm, dt_low, st);
     return run_ss2d<__nv_bfloat16>(B, D, H, W, N, R, Kc, x, conv_w, conv_b, W_x, W_dt, act, u,
                                    delta, Bm, Cm, dt_low, st);
+}
+
+ssm_status out_proj_fwd(ssm_dtype dt, int B, int Di, int Dm, int L, const void *y,
+                        const void *W_out, void *out, ssm_stream_t stream) {
+    if (dt != SSM_F32 && dt != SSM_BF16 && dt != SSM_F16) return SSM_ERR_INVALID_ARG;
+    if (B < 0 || Di <= 0 || Dm <= 0 || L < 0) return SSM_ERR_INVALID_ARG;
+    if (B > 65535 || (long long)Di * L > 0x7fffffffLL || (long long)Dm * L > 0x7fffffffLL ||
+        (long long)Dm * Di > 0x7fffffffLL)
+        return SSM_ERR_UNSUPPORTED;
+    if (!io_ok(dt, y) || !io_ok(dt, W_out) || !io_ok(dt, out)) return SSM_ERR_INVALID_ARG;
+    if ((long long)B * L == 0) return SSM_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (dt == SSM_F32) return out_proj_run<float>(B, Di, Dm, L, y, W_out, out, st);
+    if (dt == SSM_F16) return out_proj_run<__half>(B, Di, Dm, L, y, W_out, out, st);
+    return out_proj_run<__nv_bfloat16>(B, Di, Dm, L, y, W_out, out, st);
 }
 
 }  // extern "C"
