@@ -958,6 +958,102 @@ fused_prologue_kernel(const IO *__restrict__ x, const float *__restrict__ cw,
 // slices, XP_NT threads, XP_OP the fp32 output tile's row.
 constexpr int XP_T = 128, XP_K = 256, XP_OP = XP_T + 8, XP_NT = 512;
 
+// ---- position-contiguous 16-bit rows as the MN-major A operand of tcgen05
+// A slice is KS channels (k0 ..) x 128 positions (t0 ..) of a tensor x
+// [nb][K][L] whose rows are contiguous along positions and whose base is
+// 16-byte aligned.  Each row is copied raw by 16-byte cp.async (no
+// registers): the 17 chunks from the 16-byte boundary at or below its first
+// position, zero-filled past the tensor's end and for rows at or past K;
+// every thread then arrives on the stage's mbarrier once its copies have
+// landed (per-row bulk copies of 272 bytes measured slower on B300 at
+// this piece length).  The threads then realign the raw rows in
+// shared memory into the A tile, MN-major without swizzle: element (t, k) at
+//   (k / 8) * MN_KSTR + (t / 8) * MN_MSTR + (k % 8) * 16 + (t % 8) * 2,
+// core matrices of 8 channels x 8 consecutive positions; the descriptor's
+// leading byte offset is MN_KSTR (between channel groups), its stride byte
+// offset MN_MSTR (between position groups; 144 rather than 128 so that the
+// 16-byte stores of 8 lanes along positions fall on distinct banks).
+// Positions past the row's end hold the next row's values (or zeros): they
+// only reach output positions that are not stored.
+constexpr int RAW_CH = 17, RAW_ROW = RAW_CH * 16;     // chunks and bytes per raw row
+constexpr unsigned MN_MSTR = 144, MN_KSTR = 16 * MN_MSTR;
+__host__ __device__ constexpr int mn_tile_bytes(int KS) { return KS / 8 * (int)MN_KSTR; }
+
+__device__ __forceinline__ void cp_async16_zfill(void *smem, const void *gmem, bool full) {
+    unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem),
+                 "r"(full ? 16 : 0)
+                 : "memory");
+}
+// the barrier's pending count drops by one when every cp.async this thread
+// issued before has landed
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+__device__ __forceinline__ void cp_async16_n(void *smem, const void *gmem, int bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(smem)),
+                 "l"(gmem), "r"(bytes)
+                 : "memory");
+}
+// the raw rows of a slice (rows row0 .. row0 + KS - 1 of x, i.e. b * K +
+// k0 + r; rows r >= nrow, k >= K, are zero), positions from t0, by 16-byte
+// cp.async with zero fill past the tensor's end (E elements): NT / KS
+// threads per row, thread tid copies chunks tid % (NT / KS) + (NT / KS) * i
+// of row tid / (NT / KS)
+template <int KS, int NT, typename IO>
+__device__ __forceinline__ void raw_rows_copy(unsigned char *raw, const IO *x, long long E,
+                                              long long row0, int nrow, int L, int t0,
+                                              int tid) {
+    constexpr int TPR = NT / KS;
+    static_assert(KS * TPR == NT && TPR <= RAW_CH, "threads per raw row");
+    const int r = tid / TPR, c0 = tid % TPR;
+    const long long cs = ((row0 + r) * L + t0) & ~7LL;
+    const long long nv0 = r < nrow ? E - cs : 0;                // elements of x from cs on
+    unsigned char *d = raw + r * RAW_ROW;
+#pragma unroll
+    for (int i = 0; i < (RAW_CH + TPR - 1) / TPR; ++i) {
+        const int ch = c0 + TPR * i;
+        if (i * TPR + TPR <= RAW_CH || ch < RAW_CH) {
+            const long long nv = nv0 - 8 * ch;
+            const int bytes = nv >= 8 ? 16 : nv > 0 ? 2 * (int)nv : 0;
+            cp_async16_n(d + ch * 16, bytes > 0 ? (const void *)(x + cs + 8 * ch) : (const void *)x,
+                         bytes);
+        }
+    }
+}
+// raw rows -> A tile, 16 bytes (8 positions of one channel) per step: row r
+// starts s = (its first element's offset) mod 8 elements into its raw copy,
+// so output words 0..3 are element pairs s + 2i of the raw chunks j, j + 1
+template <int KS, int NT>
+__device__ __forceinline__ void raw_rows_realign(const unsigned char *raw, unsigned char *a,
+                                                 long long row0, int L, int t0, int tid) {
+#pragma unroll
+    for (int c = tid; c < KS * 16; c += NT) {
+        const int r = c >> 4, j = c & 15;
+        const unsigned s = ((unsigned)(row0 + r) * (unsigned)L + (unsigned)t0) & 7u;
+        const uint4 p = *(const uint4 *)(raw + r * RAW_ROW + 16 * j);
+        const uint4 q = *(const uint4 *)(raw + r * RAW_ROW + 16 * j + 16);
+        // f_i = word i + s / 2 of p, q (two selects on the bits of s / 2)
+        const bool h2 = s & 4, h1 = s & 2;
+        const unsigned e0 = h2 ? p.z : p.x, e1 = h2 ? p.w : p.y, e2 = h2 ? q.x : p.z,
+                       e3 = h2 ? q.y : p.w, e4 = h2 ? q.z : q.x, e5 = h2 ? q.w : q.y;
+        const unsigned f0 = h1 ? e1 : e0, f1 = h1 ? e2 : e1, f2 = h1 ? e3 : e2,
+                       f3 = h1 ? e4 : e3, f4 = h1 ? e5 : e4;
+        const unsigned sel = (s & 1) ? 0x5432u : 0x3210u;
+        uint4 o;
+        o.x = __byte_perm(f0, f1, sel);
+        o.y = __byte_perm(f1, f2, sel);
+        o.z = __byte_perm(f2, f3, sel);
+        o.w = __byte_perm(f3, f4, sel);
+        *(uint4 *)(a + (r >> 3) * MN_KSTR + j * MN_MSTR + (r & 7) * 16) = o;
+    }
+}
+
 // x_proj on the 5th-generation tensor cores (tcgen05, 16-bit I/O, M <= 64
 // rows): out[b][m][t] = sum_k W[m][k] u[b][k][t] as D[t][m] = U[t][k] W[m][k]
 // with MMA M = 128 positions, N = 64 rows, K = 16 per instruction and an
@@ -1007,14 +1103,27 @@ xproj_tc_kernel(const float *__restrict__ W, const IO *__restrict__ in, int M, i
         mbar_init(&bars[1], 1);
         fence_barrier_init();
     }
-    // W: element (m, k), zero past row M and column K
-    for (int i = tid; i < 64 * KR / 2; i += TCX_NT) {
-        const int m = i / (KR / 2), k = 2 * (i % (KR / 2));
-        const float w0 = (m < M && k < K) ? W[(long long)m * K + k] : 0.f;
-        const float w1 = (m < M && k + 1 < K) ? W[(long long)m * K + k + 1] : 0.f;
-        const IO a = from_f32<IO>(w0), c = from_f32<IO>(w1);
-        *(unsigned *)(sW + kmaj(m, k, SBO_W)) =
-            (unsigned)*(const unsigned short *)&a | ((unsigned)*(const unsigned short *)&c << 16);
+    // W: element (m, k), zero past row M and column K (eight element pairs
+    // per thread and step, every load of a step in flight)
+    for (int i0 = tid; i0 < 64 * KR / 2; i0 += 8 * TCX_NT) {
+        float w0[8], w1[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * TCX_NT, m = i / (KR / 2), k = 2 * (i - m * (KR / 2));
+            const bool in = i < 64 * KR / 2 && m < M;
+            w0[u] = (in && k < K) ? W[(long long)m * K + k] : 0.f;
+            w1[u] = (in && k + 1 < K) ? W[(long long)m * K + k + 1] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * TCX_NT, m = i / (KR / 2), k = 2 * (i - m * (KR / 2));
+            if (i < 64 * KR / 2) {
+                const IO a = from_f32<IO>(w0[u]), c = from_f32<IO>(w1[u]);
+                *(unsigned *)(sW + kmaj(m, k, SBO_W)) =
+                    (unsigned)*(const unsigned short *)&a |
+                    ((unsigned)*(const unsigned short *)&c << 16);
+            }
+        }
     }
     fence_proxy_async_shared();
     tc_fence_before();
@@ -1101,149 +1210,156 @@ xproj_tc_kernel(const float *__restrict__ W, const IO *__restrict__ in, int M, i
 }
 
 // The block's output projection on tcgen05 (16-bit I/O, d_model <= 512,
-// d_inner a multiple of 8): out[b][m][t] = sum_k W[m][k] y[b][k][t]
-// ("VMamba的SS2D模块详解" section 2.1: out_proj = Linear(d_inner -> d_model)
-// after the gate), as D[t][m] = Y[t][k] W[m][k]: MMA M = 128 positions, N in
-// chunks of 128 rows (every d_model row of a tile: NCH chunks, 128 * NCH
-// TMEM columns), K = 16 per instruction, fp32 accumulator in tensor memory.
-// A persistent CTA of 16 warps walks one stream of slices (64 channels of
-// one tile of 128 positions) over its tiles.  W (I/O dtype) goes straight
-// from global memory into the K-major no-swizzle layout by 16-byte
-// cp.async (one core-matrix row = 8 consecutive k of one row; zero-filled
-// past d_inner), issued one slice ahead; y goes through registers
-// (transposed, raw values from clamped addresses, one slice ahead).  Two
-// buffer sets: one thread issues a slice's 4 * NCH MMAs and commits them
-// to the set's mbarrier, which gates the set's next refill.  The epilogue
-// reads TMEM (warp w: lanes 32 (w % 4), a quarter of the columns) and
-// stores along positions.
-constexpr int OP_T = 128, OP_K = 64, OP_NT = 512, OP_MAXN = 512;
-template <int NCH> __host__ __device__ constexpr size_t out_proj_smem_bytes() {
-    return 2 * ((size_t)OP_T * OP_K * 2 + (size_t)NCH * 128 * OP_K * 2) + 64;
+// d_inner a multiple of 8, y and W 16-byte aligned):
+// out[b][m][t] = sum_k W[m][k] y[b][k][t] ("VMamba的SS2D模块详解" section
+// 2.1: out_proj = Linear(d_inner -> d_model) after the gate), as
+// D[t][m] = Y[t][k] W[m][k]: MMA M = 128 positions, N in chunks of 128 rows
+// (every d_model row of a tile: NCH chunks, 128 * NCH TMEM columns), K = 16
+// per instruction, fp32 accumulator in tensor memory.  A persistent CTA of
+// 16 warps walks one stream of slices (OP_K channels of one tile of 128
+// positions) over its tiles through a ring of `ns` stages, each holding a
+// slice's raw y rows (sixteen threads per row) and its W columns (K-major
+// without swizzle, straight from global memory by 16-byte cp.async,
+// zero-filled past d_model and d_inner) and completing on
+// its own mbarrier; ns - 1 slices are in flight.  Per slice: wait for the
+// stage, realign y into one of two A buffers, one thread issues the
+// slice's 2 * NCH MMAs and commits them to the buffer's mbarrier; once the
+// previous slice's MMAs are done its stage takes the slice ns - 1 ahead.
+// The epilogue reads TMEM (warp w: lanes 32 (w % 4), a quarter of the
+// columns) and stores along positions.
+constexpr int OP_T = 128, OP_K = 32, OP_NT = 512, OP_MAXN = 512, OP_MAXNS = 8;
+template <int NCH> __host__ __device__ constexpr size_t out_proj_stage_bytes() {
+    return (size_t)OP_K * RAW_ROW + (size_t)NCH * 128 * OP_K * 2;
 }
-__device__ __forceinline__ void cp_async16_zfill(void *smem, const void *gmem, bool full) {
-    unsigned s = (unsigned)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem),
-                 "r"(full ? 16 : 0)
-                 : "memory");
+template <int NCH> __host__ __device__ constexpr size_t out_proj_fixed_bytes() {
+    return 2 * (size_t)mn_tile_bytes(OP_K) + 8 * (2 + OP_MAXNS) + 16;
+}
+template <int NCH> inline int out_proj_stages(size_t smem_max) {
+    const size_t fixed = out_proj_fixed_bytes<NCH>();
+    if (fixed >= smem_max) return 0;
+    const size_t ns = (smem_max - fixed) / out_proj_stage_bytes<NCH>();
+    return ns < 3 ? 0 : (int)(ns < (size_t)OP_MAXNS ? ns : OP_MAXNS);
+}
+template <int NCH> inline size_t out_proj_smem_bytes(int ns) {
+    return out_proj_fixed_bytes<NCH>() + (size_t)ns * out_proj_stage_bytes<NCH>();
 }
 template <typename IO, int NCH>
 __global__ void __launch_bounds__(OP_NT, 1)
 out_proj_tc_kernel(const IO *__restrict__ W, const IO *__restrict__ y, int Dm, int Di, int L,
-                   int nb, IO *__restrict__ out) {
+                   int nb, int ns, IO *__restrict__ out) {
     static_assert(sizeof(IO) == 2, "16-bit I/O");
     extern __shared__ __align__(1024) unsigned char op_smem[];
     constexpr int NR = NCH * 128;                               // rows of the MMA's N
-    constexpr int A_BYTES = OP_T * OP_K * 2, W_BYTES = NR * OP_K * 2;
-    constexpr int SET = A_BYTES + W_BYTES;
-    constexpr unsigned SBO = OP_K / 8 * 128;                    // 1024: next 8 rows
-    constexpr int AP = OP_T * OP_K / 2 / OP_NT;                 // y k-pairs per thread: 8
+    constexpr int A_BYTES = mn_tile_bytes(OP_K), RAW_BYTES = OP_K * RAW_ROW;
+    constexpr size_t STAGE = out_proj_stage_bytes<NCH>();
+    constexpr unsigned SBO = OP_K / 8 * 128;                    // 512: next 8 rows of W
     constexpr int WC = NR * (OP_K / 8) / OP_NT;                 // W 16-byte chunks per thread
-    uint64_t *bars = (uint64_t *)(op_smem + 2 * SET);
-    unsigned *tslot = (unsigned *)(bars + 2);
+    static_assert(NR * (OP_K / 8) % OP_NT == 0, "W chunks per thread");
+    unsigned char *sA = op_smem;                                // [2] A tiles (MN-major)
+    unsigned char *sS = sA + 2 * A_BYTES;                       // [ns] stages: raw y, W
+    uint64_t *mbars = (uint64_t *)(sS + (size_t)ns * STAGE);    // one per A buffer
+    uint64_t *rbars = mbars + 2;                                // one per stage
+    unsigned *tslot = (unsigned *)(rbars + OP_MAXNS);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    auto kmaj = [](int r, int k) {
-        return (r >> 3) * (int)SBO + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
-    };
     constexpr unsigned TCOLS = NR <= 128 ? 128 : NR <= 256 ? 256 : 512;
     if (warp == 0) tc_alloc(tslot, TCOLS);
     if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
+        mbar_init(&mbars[0], 1);
+        mbar_init(&mbars[1], 1);
+        // per use: one arrival (cp.async tracking) per thread
+        for (int s = 0; s < ns; ++s) mbar_init(&rbars[s], OP_NT);
         fence_barrier_init();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const unsigned tmem = *tslot;
-    const unsigned idesc = tc_idesc<IO>(128, 128);
-    const int ld_tt = (warp % 8) * 16 + (lane & 15);
-    const int ld_kp0 = (warp / 8) * 2 + (lane >> 4);
+    const unsigned idesc = tc_idesc<IO>(128, 128, true);
     const int tpb = (L + OP_T - 1) / OP_T, ntiles = tpb * nb;
     const int nk = (Di + OP_K - 1) / OP_K;
-    const int my_tiles =
-        (int)blockIdx.x < ntiles ? (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-    const int nslices = my_tiles * nk;
-    IO ry0[AP], ry1[AP];
-    // slice g: tile blockIdx.x + (g / nk) * gridDim.x, channels (g % nk) * OP_K ..
-    auto load_y = [&](int g) {
-        const int tile = blockIdx.x + (g / nk) * gridDim.x, k0 = (g % nk) * OP_K;
-        const int b = tile / tpb, t = min((tile % tpb) * OP_T + ld_tt, L - 1);
-        const IO *src = y + (long long)b * Di * L + t;
+    const long long E = (long long)nb * Di * L;
+    // this thread's W chunks: lanes = 8 rows x 4 chunks of 16 bytes (one
+    // row's 64 bytes), 512 contiguous shared bytes per warp instruction
+    const IO *w_row[WC];
+    int w_dst[WC];
+    bool w_in[WC];
 #pragma unroll
-        for (int j = 0; j < AP; ++j) {
-            const int k = k0 + 2 * (ld_kp0 + 4 * j);
-            ry0[j] = src[(long long)min(k, Di - 1) * L];
-            ry1[j] = src[(long long)min(k + 1, Di - 1) * L];
-        }
-    };
-    // W rows 0 .. NR-1, channels k0 .. k0 + 63 of slice g into set `set`
-    auto issue_w = [&](int g, int set) {
-        const int k0 = (g % nk) * OP_K;
-        unsigned char *w_s = op_smem + set * SET + A_BYTES;
+    for (int j = 0; j < WC; ++j) {
+        const int c = tid + j * OP_NT, n = c >> 2, kc = c & 3;
+        w_row[j] = W + (long long)min(n, Dm - 1) * Di + 8 * kc;
+        w_dst[j] = (n >> 3) * SBO + kc * 128 + (n & 7) * 16;
+        w_in[j] = n < Dm;
+    }
+    // the copy side: slice (i_tile, i_ki) into stage i_st
+    int i_tile = blockIdx.x, i_ki = 0, i_st = 0;
+    long long i_row = (long long)(i_tile / tpb) * Di;          // b * Di of i_tile
+    int i_t0 = (i_tile % tpb) * OP_T;
+    auto issue = [&]() {
+        if (i_tile >= ntiles) return;
+        unsigned char *s_p = sS + (size_t)i_st * STAGE;
+        const int k0 = i_ki * OP_K;
+        raw_rows_copy<OP_K, OP_NT>(s_p, y, E, i_row + k0, Di - k0, L, i_t0, tid);
 #pragma unroll
         for (int j = 0; j < WC; ++j) {
-            // a warp instruction: rows 8 q .. 8 q + 7 (lanes % 8) x chunks
-            // kc = 0..3 or 4..7 (lanes / 8): 512 contiguous shared bytes, and
-            // each row's 64 global bytes read by one instruction
-            const int c = tid + j * OP_NT, R = c / 32;
-            const int n = 8 * (R / 2) + c % 8, kc = (c / 8) % 4 + 4 * (R % 2);
-            const int k = k0 + 8 * kc;
-            const bool full = n < Dm && k < Di;
-            const IO *src = W + (long long)min(n, Dm - 1) * Di + min(k, Di - 8);
-            cp_async16_zfill(w_s + kmaj(n, 8 * kc), src, full);
+            const int kc0 = k0 + (tid & 3) * 8;                    // this chunk's first k
+            cp_async16_zfill(s_p + RAW_BYTES + w_dst[j], w_row[j] + min(k0, Di - 8 - (tid & 3) * 8),
+                             w_in[j] && kc0 < Di);
         }
-        cp_async_commit();
+        cp_async_arrive_noinc(&rbars[i_st]);
+        if (++i_st == ns) i_st = 0;
+        if (++i_ki == nk) {
+            i_ki = 0;
+            i_tile += gridDim.x;
+            i_row = (long long)(i_tile / tpb) * Di;
+            i_t0 = (i_tile % tpb) * OP_T;
+        }
     };
+    for (int g = 0; g + 1 < ns; ++g) issue();
     bool ok = true;
-    if (nslices > 0) {
-        issue_w(0, 0);
-        load_y(0);
-    }
-    for (int g = 0; g < nslices; ++g) {
-        const int tile = blockIdx.x + (g / nk) * gridDim.x, ki = g % nk, k0 = ki * OP_K;
+    int g = 0, st = 0;                 // slices consumed, their stage
+    unsigned rpar = 0;                 // phase parity of the stages' current use
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
         const int b = tile / tpb, t0 = (tile % tpb) * OP_T;
-        const bool tin = t0 + ld_tt < L;
-        const int set = g & 1;
-        unsigned char *a_s = op_smem + set * SET, *w_s = a_s + A_BYTES;
-        // (this set's previous mma, slice g - 2, was waited for before its W refill)
-        const IO z = from_f32<IO>(0.f);
-#pragma unroll
-        for (int j = 0; j < AP; ++j) {
-            const int kk = 2 * (ld_kp0 + 4 * j), k = k0 + kk;
-            const IO v0 = (tin && k < Di) ? ry0[j] : z, v1 = (tin && k + 1 < Di) ? ry1[j] : z;
-            *(unsigned *)(a_s + kmaj(ld_tt, kk)) =
-                (unsigned)*(const unsigned short *)&v0 |
-                ((unsigned)*(const unsigned short *)&v1 << 16);
-        }
-        cp_async_wait<0>();                                    // W of slice g has landed
-        fence_proxy_async_shared();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (tid == 0) {
-#pragma unroll
-            for (int ks = 0; ks < OP_K / 16; ++ks) {
-                const unsigned long long ad = tc_desc(smem_addr(a_s) + ks * 256, 128, SBO);
-#pragma unroll
-                for (int c = 0; c < NCH; ++c) {
-                    const unsigned long long bd =
-                        tc_desc(smem_addr(w_s) + c * 128 * (OP_K * 2) + ks * 256, 128, SBO);
-                    tc_mma(tmem + 128 * c, ad, bd, idesc, ki > 0 || ks > 0);
-                }
-            }
-            tc_commit(&bars[set]);
-        }
-        if (g + 1 < nslices) {
-            // the other set's last mma (slice g - 1) is done before it is refilled
-            const int nset = (g + 1) & 1;
-            if (g >= 1) ok &= mbar_wait_bounded(&bars[nset], (unsigned)(((g - 1) >> 1) & 1));
-            issue_w(g + 1, nset);
-            load_y(g + 1);
-        }
-        if (ki == nk - 1) {
-            // the tile's last slice (and so every earlier one) is done
-            ok &= mbar_wait_bounded(&bars[set], (unsigned)((g >> 1) & 1));
+        const long long row_b = (long long)b * Di;
+        for (int ki = 0; ki < nk; ++ki, ++g) {
+            const int buf = g & 1;
+            unsigned char *a_s = sA + buf * A_BYTES;
+            const unsigned char *s_p = sS + (size_t)st * STAGE;
+            // (the mma that last read this A buffer, slice g - 2, was waited
+            // for before the previous slice's stage was refilled)
+            ok &= mbar_wait_bounded(&rbars[st], rpar);
+            raw_rows_realign<OP_K, OP_NT>(s_p, a_s, row_b + ki * OP_K, L, t0, tid);
+            fence_proxy_async_shared();
+            tc_fence_before();
+            __syncthreads();
             tc_fence_after();
+            if (tid == 0) {
+                const unsigned w_a = smem_addr(s_p + RAW_BYTES);
+#pragma unroll
+                for (int ks = 0; ks < OP_K / 16; ++ks) {
+                    const unsigned long long ad =
+                        tc_desc(smem_addr(a_s) + ks * 2 * MN_KSTR, MN_KSTR, MN_MSTR);
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c) {
+                        const unsigned long long bd =
+                            tc_desc(w_a + c * 16 * SBO + ks * 256, 128, SBO);
+                        tc_mma(tmem + 128 * c, ad, bd, idesc, ki > 0 || ks > 0);
+                    }
+                }
+                tc_commit(&mbars[buf]);
+            }
+            // the previous slice's mma is done: its stage takes slice g + ns - 1
+            if (g >= 1) ok &= mbar_wait_bounded(&mbars[buf ^ 1], (unsigned)(((g - 1) >> 1) & 1));
+            issue();
+            if (++st == ns) {
+                st = 0;
+                rpar ^= 1u;
+            }
+        }
+        // the tile's last slice (and so every earlier one) is done
+        ok &= mbar_wait_bounded(&mbars[(g - 1) & 1], (unsigned)(((g - 1) >> 1) & 1));
+        tc_fence_after();
+        {
             // warp w: TMEM lanes (positions) 32 (w % 4) .., columns (rows)
             // (w / 4) * NR / 4 .. + NR / 4
             const int q4 = warp % 4, tp = t0 + 32 * q4 + lane;
@@ -1260,14 +1376,14 @@ out_proj_tc_kernel(const IO *__restrict__ W, const IO *__restrict__ y, int Dm, i
                             out[((long long)b * Dm + m0 + q) * L + tp] = from_f32<IO>(v[q]);
                 }
             }
-            // every warp has read TMEM before the next tile's first mma overwrites it
-            tc_fence_before();
-            __syncthreads();
-            tc_fence_after();
         }
+        // every warp has read TMEM before the next tile's first mma overwrites it
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
     }
     (void)ok;
-    cp_async_wait<0>();
+    cp_async_wait_all();
     __syncthreads();
     if (warp == 0) tc_dealloc(tmem, TCOLS);
 }

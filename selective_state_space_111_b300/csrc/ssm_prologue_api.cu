@@ -34,6 +34,8 @@ thread_local int t_fused = 1;
 // (the three-kernel conv streams long rows with wide CTAs; short rows
 // leave most of its threads idle).
 constexpr int kFusedMaxL = 1024;
+// shared memory a CTA may opt into on sm_100-class GPUs (227 KB)
+constexpr size_t kSmemOptin = 227 * 1024;
 
 int sm_count() {
     int dev = 0, n = 0;
@@ -62,7 +64,7 @@ ssm_status x_proj(int B, int M, int K, int L, const float *W, const IO *u, ssm::
     using namespace ssm::pro;
     if constexpr (sizeof(IO) == 2) {
         const size_t smem = xproj_tc_smem_bytes(K);
-        if (M <= 64 && smem <= 227 * 1024) {
+        if (M <= 64 && smem <= kSmemOptin) {
             if (cudaFuncSetAttribute(xproj_tc_kernel<IO>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)smem) != cudaSuccess)
@@ -298,13 +300,14 @@ template <typename IO, int NCH>
 ssm_status launch_out_proj(int B, int Di, int Dm, int L, const void *y, const IO *W,
                            void *out, cudaStream_t st) {
     using namespace ssm::pro;
-    constexpr size_t smem = out_proj_smem_bytes<NCH>();
+    const int ns = out_proj_stages<NCH>(kSmemOptin);
+    const size_t smem = out_proj_smem_bytes<NCH>(ns);
     if (cudaFuncSetAttribute(out_proj_tc_kernel<IO, NCH>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return SSM_ERR_CUDA;
     const long long tiles = (long long)B * ((L + OP_T - 1) / OP_T);
     const int grid = (int)std::min<long long>(tiles, sm_count());
-    out_proj_tc_kernel<IO, NCH><<<grid, OP_NT, smem, st>>>(W, (const IO *)y, Dm, Di, L, B,
+    out_proj_tc_kernel<IO, NCH><<<grid, OP_NT, smem, st>>>(W, (const IO *)y, Dm, Di, L, B, ns,
                                                            (IO *)out);
     return last_error();
 }
@@ -314,9 +317,10 @@ ssm_status out_proj_run(int B, int Di, int Dm, int L, const void *y, const void 
     using namespace ssm::pro;
     const IO *W = (const IO *)Wv;
     if constexpr (sizeof(IO) == 2) {
-        // W rows are copied as 16-byte chunks: Di a multiple of 8 and W
-        // 16-byte aligned, so that every row starts on a 16-byte boundary
-        if (Di % 8 == 0 && aligned(W, 16)) {
+        // W rows and y are copied as 16-byte chunks: Di a multiple of 8 and
+        // W 16-byte aligned, so that every W row starts on a 16-byte
+        // boundary, and y 16-byte aligned
+        if (Di % 8 == 0 && aligned(W, 16) && aligned(y, 16)) {
             if (Dm <= 128) return launch_out_proj<IO, 1>(B, Di, Dm, L, y, W, out, st);
             if (Dm <= 256) return launch_out_proj<IO, 2>(B, Di, Dm, L, y, W, out, st);
             if (Dm <= 384) return launch_out_proj<IO, 3>(B, Di, Dm, L, y, W, out, st);

@@ -12,22 +12,27 @@
 namespace ssm {
 
 // ---- tcgen05 (5th-generation tensor core) helpers: one CTA (cta_group::1)
-// Shared-memory matrix descriptor for a K-major operand without swizzle:
-// 8-row x 16-byte core matrices, `lbo` bytes between core matrices adjacent
-// along K, `sbo` bytes between 8-row groups (PTX ISA, tcgen05 shared memory
-// descriptor: start address, leading and stride byte offsets in 16-byte
-// units, descriptor version 1, base offset 0, layout type 0 = no swizzle).
+// Shared-memory matrix descriptor of an operand without swizzle, in 8 x
+// 16-byte core matrices (PTX ISA, tcgen05 shared memory descriptor: start
+// address, leading and stride byte offsets in 16-byte units, descriptor
+// version 1, base offset 0, layout type 0 = no swizzle).  K-major: a core
+// matrix is 8 rows x 8 consecutive k; `lbo` bytes between core matrices
+// adjacent along K, `sbo` bytes between 8-row groups.  MN-major: a core
+// matrix is 8 k x 8 consecutive rows; `lbo` bytes between groups of 8 k,
+// `sbo` bytes between groups of 8 rows.
 __device__ __forceinline__ unsigned long long tc_desc(unsigned saddr, unsigned lbo, unsigned sbo) {
     return (unsigned long long)((saddr >> 4) & 0x3FFF) |
            ((unsigned long long)((lbo >> 4) & 0x3FFF) << 16) |
            ((unsigned long long)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46);
 }
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, A and
-// B of the same 16-bit type (bf16: 1, f16: 0), both K-major, M x N.
-template <typename IO> __host__ __device__ constexpr unsigned tc_idesc(int M, int N) {
+// B of the same 16-bit type (bf16: 1, f16: 0), B K-major, A K-major or
+// (a_mn) MN-major, M x N.
+template <typename IO>
+__host__ __device__ constexpr unsigned tc_idesc(int M, int N, bool a_mn = false) {
     return (1u << 4) | ((sizeof(IO) == 2 && !std::is_same<IO, __half>::value ? 1u : 0u) << 7) |
            ((sizeof(IO) == 2 && !std::is_same<IO, __half>::value ? 1u : 0u) << 10) |
-           ((unsigned)(N >> 3) << 17) | ((unsigned)(M >> 4) << 24);
+           ((a_mn ? 1u : 0u) << 15) | ((unsigned)(N >> 3) << 17) | ((unsigned)(M >> 4) << 24);
 }
 // D[tmem] (+)= A * B^T for one K step of 16, issued by one thread
 __device__ __forceinline__ void tc_mma(unsigned tmem, unsigned long long a, unsigned long long b,
