@@ -71,6 +71,20 @@ def test_out_proj_weights_off_the_16_byte_grid():
     _check(got, y, W, "bf16")
 
 
+def test_out_proj_activations_off_the_16_byte_grid():
+    # y one element into a larger buffer: its rows cannot be staged by
+    # 16-byte copies, so the tiled path runs; same results
+    import selective_state_space_111_b300 as ssm
+    B, Di, Dm, L = 2, 64, 96, 50
+    y, W = _inputs(B, Di, Dm, L, "bf16", 8)
+    buf = torch.empty(B * Di * L + 1, dtype=torch.bfloat16, device="cuda")[1:].view(B, Di, L)
+    buf.copy_(y.cuda())
+    assert buf.data_ptr() % 16 != 0
+    got = ssm.out_proj_fwd(buf, W.cuda())
+    torch.cuda.synchronize()
+    _check(got, y, W, "bf16")
+
+
 def test_out_proj_full_size_vim_s():
     # Vim-S 1248^2: d_inner 768 -> d_model 384 over 8 x 6085 positions
     # (384 tiles on the persistent CTAs: two or three each, a 69-position
