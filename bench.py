@@ -432,6 +432,13 @@ def run_ours(args):
                                "frac": round(bach / bpeak, 4),
                                "peak_basis": "148 SMs x 128 fp32 lanes x %.0f MHz / 16 fp32 "
                                              "ops per update" % sm_max}
+            fc = bwd.get("from_context")
+            if fc:
+                cach = spec.updates() / (fc["ms"] * 1e-3) / 1e9
+                fc["roofline"] = {"bound": "alu", "achieved": round(cach, 2),
+                                  "peak": round(bpeak, 1), "unit": "Gupd/s",
+                                  "frac": round(cach / bpeak, 4)}
+                del fc["ms"]
             line["backward"] = bwd
         if pro:
             # the projections are skinny (x_proj d_inner -> dt_rank + 2 d_state,
@@ -503,9 +510,42 @@ def measure_backward(ssm, spec, g, t, dev, stream, steps):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
-    return {"ms_per_call": round(ms, 4), "ms": ms, "steps": steps,
-            "bytes_per_call": spec.backward_bytes(),
-            "elem_updates_per_s": float("%.4g" % (spec.updates() / (ms * 1e-3)))}
+    res = {"ms_per_call": round(ms, 4), "ms": ms, "steps": steps,
+           "bytes_per_call": spec.backward_bytes(),
+           "elem_updates_per_s": float("%.4g" % (spec.updates() / (ms * 1e-3)))}
+    if spec.op in ("single", "v1", "v2") and spec.N <= 16:
+        # the training pairing: the forward call leaves the backward's context
+        # (pre-gate output, chunk-start states) and the backward call reads it
+        # instead of running the forward pass again; both timed
+        n = ssm.bwd_context_bytes(spec.op, dout.dtype, spec.B, spec.D, L, spec.N)
+        ctx = torch.empty(n, dtype=torch.uint8, device=dev)
+        fws = torch.empty(max(16, ssm.workspace_bytes(spec.op, dout.dtype, spec.B, spec.D, L,
+                                                      spec.N, spec.K)),
+                          dtype=torch.uint8, device=dev)
+        out = torch.empty_like(dout)
+        ssm.set_bwd_context(ctx)
+        try:
+            for _ in range(3):
+                call(ssm, spec, g, fws, out)
+                once()
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(steps):
+                call(ssm, spec, g, fws, out)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            f_ms = e0.elapsed_time(e1) / steps
+            e0.record(stream)
+            for _ in range(steps):
+                once()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            b_ms = e0.elapsed_time(e1) / steps
+        finally:
+            ssm.set_bwd_context(None)
+        res["from_context"] = {"ms_per_call": round(b_ms, 4), "ms": b_ms,
+                               "forward_ms_per_call": round(f_ms, 4), "context_bytes": n}
+    return res
 
 
 def measure_out_proj(ssm, spec, dev, stream, steps):

@@ -41,11 +41,12 @@
  *  - Calls are asynchronous on `stream` (0 = the legacy default stream).
  *    The library allocates nothing.  Its only state outside the caller's
  *    buffers is the fixed scratch array that bimamba_scan_fwd_v2_noalloc
- *    uses and five per-host-thread settings, each changed only by its own
+ *    uses and six per-host-thread settings, each changed only by its own
  *    setter and applying to later calls made on that host thread: the
  *    profiling events (ssm_set_profile_events), the CTA-shape override
  *    (ssm_set_cta_channels), the prologue's kernel choice
- *    (ssm_set_prologue_fused) and the one-launch test hooks
+ *    (ssm_set_prologue_fused), the saved backward context
+ *    (ssm_set_bwd_context) and the one-launch test hooks
  *    (ssm_test_withhold_copy, ssm_test_shrink_extents).  (The backward
  *    calls also set, and clear before returning, a per-thread request that
  *    the forward run inside them store its chunk-start states.)
@@ -383,6 +384,43 @@ SSM_API ssm_status ss2d_scan_bwd(ssm_dtype dt, int B, int D, int H, int W, int N
 SSM_API size_t ssm_bwd_workspace_bytes(ssm_op op, ssm_dtype dt, int B, int D,
                                        int L_or_HW, int N, int K,
                                        int separate_u_b);
+
+/* ---------------------------------------------------------------------------
+ * Saved backward context.  Each backward call above first runs the forward
+ * pass again: the gate's derivative needs the pre-gate output y, and with
+ * d_state <= 16 the backward kernel starts from the states the forward
+ * pass had before every eighth step.  That is the recompute side of the
+ * memory / compute trade-off ("Vision Mamba实战" section 4 recomputes
+ * activations under gradient checkpointing to save memory).  A training
+ * loop that can spend the memory keeps both from its own forward call:
+ *
+ *   ssm_set_bwd_context(ctx, ctx_bytes)   on the host thread making the calls
+ *   forward call                          also stores y before the gate and
+ *                                         the chunk-start states in ctx
+ *   ... (other calls, each layer with its own context)
+ *   ssm_set_bwd_context(ctx, ctx_bytes)   the same buffer again
+ *   backward call, same inputs            reads ctx instead of running the
+ *                                         forward pass
+ *   ssm_set_bwd_context(NULL, 0)
+ *
+ * It applies to selective_scan_fwd / _bwd, bimamba_scan_fwd_v1 / _bwd_v1
+ * and bimamba_scan_fwd_v2 (and its _ls, _so and _noalloc variants) /
+ * _bwd_v2 with d_state <= 16; SS2D calls and d_state > 16 ignore it.  The
+ * caller guarantees that the backward call has the same operation, sizes,
+ * dtype, inputs and gate (z given or not) as the forward call that filled
+ * ctx; the library cannot check this.  `ctx`: device memory of at least
+ * ssm_bwd_context_bytes(...) bytes, 16-byte aligned, owned by the caller;
+ * a forward or backward call that finds it smaller or misaligned returns
+ * SSM_ERR_WORKSPACE.  The setting is per host thread (the sixth per-thread
+ * setting) and stays until changed.  Results are bit-identical to the
+ * backward call without a context. */
+SSM_API void ssm_set_bwd_context(void *ctx, size_t ctx_bytes);
+
+/* Bytes of a saved backward context for these sizes: the pre-gate output
+ * (B * D * L elements of dt) and, per direction, fp32 states [B][D][ceil(L
+ * / 8)][16]; 0 when d_state > 16 or B*D*L is 0 (the context is then
+ * ignored); (size_t)-1 for SS2D or invalid sizes. */
+SSM_API size_t ssm_bwd_context_bytes(ssm_op op, ssm_dtype dt, int B, int D, int L, int N);
 
 /* ---------------------------------------------------------------------------
  * Prologue: the steps that turn a block's input x into the scan's inputs,

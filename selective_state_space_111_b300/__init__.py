@@ -11,7 +11,8 @@ _OPS = ("selective_scan_fwd", "bimamba_scan_fwd_v1", "bimamba_scan_fwd_v2",
         "bimamba_scan_fwd_v2_noalloc", "ss2d_scan_fwd", "workspace_bytes", "library_path",
         "SsmError", "version", "set_profile_events", "get_status", "set_cta_channels", "set_prologue_fused",
         "selective_scan_bwd", "bimamba_scan_bwd_v1", "bimamba_scan_bwd_v2", "ss2d_scan_bwd",
-        "bwd_workspace_bytes", "mamba_prologue_fwd", "out_proj_fwd",
+        "bwd_workspace_bytes", "bwd_context_bytes", "set_bwd_context", "mamba_prologue_fwd",
+        "out_proj_fwd",
         "ss2d_prologue_fwd")
 
 

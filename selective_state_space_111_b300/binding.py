@@ -83,6 +83,10 @@ def _declare(lib):
     lib.ss2d_prologue_workspace_bytes.restype = _sz
     lib.ssm_bwd_workspace_bytes.argtypes = [_i] * 8
     lib.ssm_bwd_workspace_bytes.restype = _sz
+    lib.ssm_set_bwd_context.argtypes = [_vp, _sz]
+    lib.ssm_set_bwd_context.restype = None
+    lib.ssm_bwd_context_bytes.argtypes = [_i] * 6
+    lib.ssm_bwd_context_bytes.restype = _sz
     for _fn in (lib.selective_scan_fwd, lib.bimamba_scan_fwd_v1, lib.bimamba_scan_fwd_v2,
                 lib.ss2d_scan_fwd, lib.bimamba_scan_fwd_v2_noalloc, lib.selective_scan_fwd_ls,
                 lib.bimamba_scan_fwd_v1_ls, lib.bimamba_scan_fwd_v2_ls, lib.ss2d_scan_fwd_ls,
@@ -354,6 +358,31 @@ def bwd_workspace_bytes(op: str, dtype: torch.dtype, B: int, D: int, L: int, N: 
     if n == ctypes.c_size_t(-1).value:
         raise ValueError("invalid sizes")
     return int(n)
+
+
+def bwd_context_bytes(op: str, dtype: torch.dtype, B: int, D: int, L: int, N: int) -> int:
+    """Bytes of a saved backward context (0: d_state > 16, none is kept)."""
+    n = _lib.ssm_bwd_context_bytes(OPS[op], _CODES[dtype], B, D, L, N)
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("invalid sizes or operation")
+    return int(n)
+
+
+def set_bwd_context(ctx=None) -> None:
+    """Saved backward context for later calls on this thread: a uint8 CUDA
+    tensor of at least bwd_context_bytes(...) bytes, or None to stop.  While
+    it is set, forward calls (single, v1, v2; d_state <= 16) also store the
+    pre-gate output and chunk-start states there, and backward calls on the
+    same inputs read them instead of running the forward pass again.  The
+    caller keeps the tensor alive and pairs each backward call with the
+    forward call that filled the context."""
+    if ctx is None:
+        _lib.ssm_set_bwd_context(None, 0)
+        return
+    if not (isinstance(ctx, torch.Tensor) and ctx.is_cuda and ctx.dtype == torch.uint8 and
+            ctx.is_contiguous()):
+        raise ValueError("the context is a contiguous uint8 CUDA tensor")
+    _lib.ssm_set_bwd_context(ctypes.c_void_p(ctx.data_ptr()), ctx.numel())
 
 
 def _bwd_workspace(op, dtype, B, D, L, N, device, workspace, K=4, separate_u_b=False):

@@ -82,13 +82,16 @@ struct BiBranch {
 // (y_fwd + y_bwd) of a position:
 //   OUT_Y      gate with z, store y (I/O dtype);
 //   OUT_ACC    store v to acc_out (fp32, no gate);
-//   OUT_ADD_Y  add acc_in (fp32), gate with z, store y.
-enum { OUT_Y = 0, OUT_ACC = 1, OUT_ADD_Y = 2 };
+//   OUT_ADD_Y  add acc_in (fp32), gate with z, store y;
+//   OUT_Y_PRE  as OUT_Y, and also store v itself (before the gate) to ypre
+//              (I/O dtype): the pre-gate output the backward pass needs.
+enum { OUT_Y = 0, OUT_ACC = 1, OUT_ADD_Y = 2, OUT_Y_PRE = 3 };
 
 struct BiParams {
     BiBranch br[2];
     const void *z;         // [B, D, L] or null
     void *y;               // [B, D, L]
+    void *ypre;            // [B, D, L] (OUT_Y_PRE)
     const float *acc_in;   // [B, D, L] fp32 (OUT_ADD_Y)
     float *acc_out;        // [B, D, L] fp32 (OUT_ACC)
     float *W;              // [B, D, L] fp32 stash (two branches, several chunks)
@@ -715,6 +718,7 @@ bidir_scan_kernel(const BiParams P) {
         const IO *zrow = P.z ? (const IO *)P.z + rowb0 : nullptr;
         float *Wrow = P.W ? P.W + rowb0 : nullptr;
         IO *yrow = P.y ? (IO *)P.y + rowb0 : nullptr;
+        IO *yprow = (OUT == OUT_Y_PRE && P.ypre) ? (IO *)P.ypre + rowb0 : nullptr;
         float *aorow = P.acc_out ? P.acc_out + rowb0 : nullptr;
         const float *airow = P.acc_in ? P.acc_in + rowb0 : nullptr;
         const int nch_ok = min(CPE, D - (d0 + c0));           // valid channels
@@ -862,11 +866,13 @@ bidir_scan_kernel(const BiParams P) {
                         float v = own(d, i, jw);
                         if (NDIR == 2) v = P.out_scale * (v + wr[d][i]);
                         if (OUT == OUT_ADD_Y) v += ar[d][i];
+                        const float pre = v;
                         if (gate) v *= silu_f<IO>(to_f32(zr[d][i]));
                         if ((full || (act && i < nch_ok)) &&
                             SSM_IN(rowb0 + i * L + p, P.io_elems, P.status)) {
                             if (OUT == OUT_ACC) aorow[i * L + p] = v;
                             else yrow[i * L + p] = from_f32<IO>(v);
+                            if (OUT == OUT_Y_PRE) yprow[i * L + p] = from_f32<IO>(pre);
                         }
                     }
                 }
@@ -874,6 +880,7 @@ bidir_scan_kernel(const BiParams P) {
             } else {
                 // the middle of the sequence: classes differ between lanes
                 float vv[NDIR][CPE];     // the stash value (first arrival) or the output
+                float pv[NDIR][CPE];     // OUT_Y_PRE: the output before the gate
                 int kk[NDIR];
 #pragma unroll
                 for (int d = 0; d < NDIR; ++d) {
@@ -898,6 +905,7 @@ bidir_scan_kernel(const BiParams P) {
                         float v = ow[i];
                         if (NDIR == 2) v = k == 0 ? v : P.out_scale * (v + wr[d][i]);
                         if (OUT == OUT_ADD_Y) v += ar[d][i];
+                        if (OUT == OUT_Y_PRE) pv[d][i] = v;
                         if (OUT != OUT_ACC && zrow != nullptr && !(NDIR == 2 && k == 0))
                             v *= silu_f<IO>(to_f32(zr[d][i]));
                         vv[d][i] = v;
@@ -919,6 +927,7 @@ bidir_scan_kernel(const BiParams P) {
                         if (ok && fin) {
                             if (OUT == OUT_ACC) aorow[o] = vv[d][i];
                             else yrow[o] = from_f32<IO>(vv[d][i]);
+                            if (OUT == OUT_Y_PRE) yprow[o] = from_f32<IO>(pv[d][i]);
                         }
                     }
                 }

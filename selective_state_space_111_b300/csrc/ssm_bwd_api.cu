@@ -156,6 +156,10 @@ ssm_status launch_passes(const Pass *ps, int npass, int B, int D, int L, int N, 
     return launch_passes_nm<IO, 2 * ssm::kMaxN>(ps, npass, B, D, L, N, sp, false, st);
 }
 
+// Saved backward context of this host thread (ssm_set_bwd_context).
+thread_local void *t_ctx = nullptr;
+thread_local size_t t_ctx_bytes = 0;
+
 // Scope in which the forward calls of this host thread also store their
 // chunk-start states for the 16-state backward kernel.
 struct CaptureScope {
@@ -286,11 +290,19 @@ ssm_status seq_bwd(int op, int B, int D, int L, int N, const void *u, const void
     float *dt0 = (float *)(ws + w.ddt), *dt1 = dt0 + n;
     // (1) the forward pass: the pre-gate output (for dz) and, with 16
     // states, the chunk-start states of every direction (the backward
-    // kernel then skips its own forward sweep)
+    // kernel then skips its own forward sweep) -- or, with a saved context
+    // (16 states), both as the forward call left them
     void *ypre = ws + w.ypre;
     void *fws = ws + w.fwd;
     const bool capture = N <= ssm::kMaxN;
-    if (z != nullptr || capture) {
+    const bool from_ctx = capture && t_ctx != nullptr;
+    ssm_internal::CtxLayout cl{};
+    if (from_ctx) {
+        cl = ssm_internal::ctx_layout(op == 0 ? 1 : 2, esz(dt), B, D, L);
+        if (t_ctx_bytes < cl.total || !aligned(t_ctx, 16)) return SSM_ERR_WORKSPACE;
+        ypre = (char *)t_ctx + cl.ypre;
+    }
+    if (!from_ctx && (z != nullptr || capture)) {
         float *hc[4] = {base_pass(ws, w, 0, B, D, L, N).hc,
                         op == 0 ? nullptr : base_pass(ws, w, 1, B, D, L, N).hc, nullptr, nullptr};
         CaptureScope scope(capture ? hc : nullptr);
@@ -327,6 +339,7 @@ ssm_status seq_bwd(int op, int B, int D, int L, int N, const void *u, const void
     p0.stream_rev = 0;
     p0.du = du0;
     p0.ddt = dt0;
+    if (from_ctx) p0.hc = (float *)((char *)t_ctx + cl.hc[0]);
     // 16 states: a direction that owns its du or ddelta writes it in the
     // I/O dtype directly; tensors the two branches share are summed from
     // the fp32 maps below
@@ -343,7 +356,7 @@ ssm_status seq_bwd(int op, int B, int D, int L, int N, const void *u, const void
         p1.pdB = q.pdB;
         p1.pdC = q.pdC;
         p1.pdA = q.pdA;
-        p1.hc = q.hc;
+        p1.hc = from_ctx ? (float *)((char *)t_ctx + cl.hc[1]) : q.hc;
         p1.pbias = q.pbias;
         p1.pdD = q.pdD;
         p1.du_io = fused && du_own ? du_b : nullptr;
@@ -492,7 +505,47 @@ ssm_status ss2d_bwd_run(int B, int D, int H, int W, int N, const void *x, const 
 
 }  // namespace
 
+void *ssm_internal::bwd_context(size_t *bytes) {
+    if (bytes) *bytes = t_ctx_bytes;
+    return t_ctx;
+}
+
+ssm_internal::CtxLayout ssm_internal::ctx_layout(int ndir, unsigned esize, int B, int D, int L) {
+    CtxLayout c{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += (bytes + 255) / 256 * 256;
+        return at;
+    };
+    const size_t n = (size_t)B * D * L;
+    c.ypre = take(n * esize);
+    for (int k = 0; k < ndir; ++k)
+        c.hc[k] = take((size_t)B * D * nch_of(L, ssm::kMaxN) * ssm::kMaxN * sizeof(float));
+    c.total = off;
+    return c;
+}
+
 extern "C" {
+
+void ssm_set_bwd_context(void *ctx, size_t ctx_bytes) {
+    t_ctx = ctx;
+    t_ctx_bytes = ctx ? ctx_bytes : 0;
+}
+
+size_t ssm_bwd_context_bytes(ssm_op op, ssm_dtype dt, int B, int D, int L, int N) {
+    if (dt != SSM_F32 && dt != SSM_BF16 && dt != SSM_F16) return (size_t)-1;
+    if (B < 0 || D < 0 || L < 0 || N <= 0 || N > 2 * ssm::kMaxN) return (size_t)-1;
+    int ndir;
+    switch (op) {
+    case SSM_OP_SELECTIVE_SCAN: ndir = 1; break;
+    case SSM_OP_BIMAMBA_V1:
+    case SSM_OP_BIMAMBA_V2: ndir = 2; break;
+    default: return (size_t)-1;
+    }
+    if (N > ssm::kMaxN || (long long)B * D * L == 0) return 0;
+    return ssm_internal::ctx_layout(ndir, esz(dt), B, D, L).total;
+}
 
 size_t ssm_bwd_workspace_bytes(ssm_op op, ssm_dtype dt, int B, int D, int L_or_HW, int N, int K,
                                int separate_u_b) {

@@ -117,6 +117,23 @@ thread_local long long t_shrink = 0;
 // Chunk-state capture (ssm_internal::set_chunk_state_capture), per direction.
 thread_local float *t_capture[4] = {nullptr, nullptr, nullptr, nullptr};
 
+// A saved backward context (ssm_set_bwd_context) on this host thread, for
+// a sequence form with d_state <= 16 and no internal capture active: the
+// call also stores its chunk-start states and (with a gate) its pre-gate
+// output there, in the layout the backward calls read.
+ssm_status apply_bwd_context(ssm::BiParams &P, int ndir, ssm_dtype dt) {
+    if (P.N > ssm::kMaxN || t_capture[0] != nullptr || t_capture[1] != nullptr) return SSM_OK;
+    size_t cb = 0;
+    char *ctx = (char *)ssm_internal::bwd_context(&cb);
+    if (ctx == nullptr) return SSM_OK;
+    const ssm_internal::CtxLayout cl =
+        ssm_internal::ctx_layout(ndir, dt == SSM_F32 ? 4u : 2u, P.B, P.D, P.L);
+    if (cb < cl.total || !aligned(ctx, 16)) return SSM_ERR_WORKSPACE;
+    for (int k = 0; k < ndir; ++k) P.chunk_state[k] = (float *)(ctx + cl.hc[k]);
+    P.ypre = P.z ? (void *)(ctx + cl.ypre) : nullptr;
+    return SSM_OK;
+}
+
 template <typename IO, int S, int NDIR, int G, int OUT, int NM>
 ssm_status launch_bidir(const ssm::BiParams &P, cudaStream_t st, bool last = true) {
     using LY = ssm::WsLayout<IO, S, NDIR, G, NM>;
@@ -205,6 +222,12 @@ ssm_status run_bidir_nm(ssm::BiParams P, const void *Bm, const void *Cm, const v
                                 P.status, st);
     }
     if (s != SSM_OK) return s;
+    if constexpr (NM == ssm::kMaxN) {
+        if (P.ypre != nullptr) {
+            if (NDIR == 2) return launch_two_branch<IO, ssm::OUT_Y_PRE, NM>(P, st);
+            return launch_bidir<IO, kBiS, 1, kBiG1, ssm::OUT_Y_PRE, NM>(P, st);
+        }
+    }
     if (NDIR == 2) return launch_two_branch<IO, ssm::OUT_Y, NM>(P, st);
     return launch_bidir<IO, kBiS, 1, kBiG1, ssm::OUT_Y, NM>(P, st);
 }
@@ -268,6 +291,7 @@ ssm_status bidirectional(ssm_dtype dt, int B, int D, int L, int N, const void *u
     P.dt_elems[0] = P.dt_elems[1] = P.io_elems = (long long)B * D * L;
     P.bc_elems[0] = P.bc_elems[1] = (long long)B * L * 2 * nm_of(N);
     P.a_elems = (long long)D * N;
+    if ((s = apply_bwd_context(P, 2, dt)) != SSM_OK) return s;
     if (dt == SSM_F32) return run_bidir<float, 2>(P, Bm, Cm, Bm_b, Cm_b, two_sets, stream);
     if (dt == SSM_F16) return run_bidir<__half, 2>(P, Bm, Cm, Bm_b, Cm_b, two_sets, stream);
     return run_bidir<__nv_bfloat16, 2>(P, Bm, Cm, Bm_b, Cm_b, two_sets, stream);
@@ -479,6 +503,7 @@ ssm_status single_impl(ssm_dtype dt, int B, int D, int L, int N, const void *u,
     P.dt_elems[0] = P.dt_elems[1] = P.io_elems = (long long)B * D * L;
     P.bc_elems[0] = P.bc_elems[1] = (long long)B * L * 2 * nm_of(N);
     P.a_elems = (long long)D * N;
+    if ((s = apply_bwd_context(P, 1, dt)) != SSM_OK) return s;
     cudaStream_t st = (cudaStream_t)stream;
     if (dt == SSM_F32) return run_bidir<float, 1>(P, Bm, Cm, Bm, Cm, false, st);
     if (dt == SSM_F16) return run_bidir<__half, 1>(P, Bm, Cm, Bm, Cm, false, st);
