@@ -12,6 +12,8 @@
 // branch's scan order.
 #pragma once
 
+#include <cuda.h>
+
 #include "scan_ops.cuh"
 #include "tc_ops.cuh"
 
@@ -979,12 +981,6 @@ constexpr int RAW_CH = 17, RAW_ROW = RAW_CH * 16;     // chunks and bytes per ra
 constexpr unsigned MN_MSTR = 144, MN_KSTR = 16 * MN_MSTR;
 __host__ __device__ constexpr int mn_tile_bytes(int KS) { return KS / 8 * (int)MN_KSTR; }
 
-__device__ __forceinline__ void cp_async16_zfill(void *smem, const void *gmem, bool full) {
-    unsigned s = (unsigned)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem),
-                 "r"(full ? 16 : 0)
-                 : "memory");
-}
 // the barrier's pending count drops by one when every cp.async this thread
 // issued before has landed
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
@@ -993,6 +989,17 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
 }
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
+}
+// tiled TMA load of the box at (x, y) (x: innermost coordinate, its byte
+// offset a multiple of 16) of the tensor map into shared memory, completing
+// its bytes on `bar`
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, int x, int y,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_addr(dst)), "l"((unsigned long long)tm), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
 }
 
 __device__ __forceinline__ void cp_async16_n(void *smem, const void *gmem, int bytes) {
@@ -1218,10 +1225,15 @@ xproj_tc_kernel(const float *__restrict__ W, const IO *__restrict__ in, int M, i
 // per instruction, fp32 accumulator in tensor memory.  A persistent CTA of
 // 16 warps walks one stream of slices (OP_K channels of one tile of 128
 // positions) over its tiles through a ring of `ns` stages, each holding a
-// slice's raw y rows (sixteen threads per row) and its W columns (K-major
-// without swizzle, straight from global memory by 16-byte cp.async,
-// zero-filled past d_model and d_inner) and completing on
-// its own mbarrier; ns - 1 slices are in flight.  Per slice: wait for the
+// slice's raw y rows (sixteen threads per row, cp.async) and its W columns,
+// and completing on its own mbarrier; ns - 1 slices are in flight.  W
+// arrives by tiled TMA copies (tensor map `tmW`: W [d_model][d_inner],
+// boxes of 8 channels x 128 rows, zero fill past d_model and d_inner): a
+// box lands as 128 rows x 16 bytes, i.e. 16 core matrices of the K-major
+// operand without swizzle, so the slice's W is K-major with the 8-channel
+// groups NR * 16 bytes apart (leading byte offset) and 8-row groups 128
+// bytes apart (stride byte offset).  One thread announces the W bytes on
+// the stage's mbarrier and issues the 4 * NCH copies.  Per slice: wait for the
 // stage, realign y into one of two A buffers, one thread issues the
 // slice's 2 * NCH MMAs and commits them to the buffer's mbarrier; once the
 // previous slice's MMAs are done its stage takes the slice ns - 1 ahead.
@@ -1245,16 +1257,15 @@ template <int NCH> inline size_t out_proj_smem_bytes(int ns) {
 }
 template <typename IO, int NCH>
 __global__ void __launch_bounds__(OP_NT, 1)
-out_proj_tc_kernel(const IO *__restrict__ W, const IO *__restrict__ y, int Dm, int Di, int L,
-                   int nb, int ns, IO *__restrict__ out) {
+out_proj_tc_kernel(const __grid_constant__ CUtensorMap tmW, const IO *__restrict__ y, int Dm,
+                   int Di, int L, int nb, int ns, IO *__restrict__ out) {
     static_assert(sizeof(IO) == 2, "16-bit I/O");
     extern __shared__ __align__(1024) unsigned char op_smem[];
     constexpr int NR = NCH * 128;                               // rows of the MMA's N
     constexpr int A_BYTES = mn_tile_bytes(OP_K), RAW_BYTES = OP_K * RAW_ROW;
     constexpr size_t STAGE = out_proj_stage_bytes<NCH>();
-    constexpr unsigned SBO = OP_K / 8 * 128;                    // 512: next 8 rows of W
-    constexpr int WC = NR * (OP_K / 8) / OP_NT;                 // W 16-byte chunks per thread
-    static_assert(NR * (OP_K / 8) % OP_NT == 0, "W chunks per thread");
+    constexpr unsigned W_LBO = NR * 16;                          // next 8 channels of W
+    constexpr unsigned W_BYTES = NR * OP_K * 2;
     unsigned char *sA = op_smem;                                // [2] A tiles (MN-major)
     unsigned char *sS = sA + 2 * A_BYTES;                       // [ns] stages: raw y, W
     uint64_t *mbars = (uint64_t *)(sS + (size_t)ns * STAGE);    // one per A buffer
@@ -1278,18 +1289,6 @@ out_proj_tc_kernel(const IO *__restrict__ W, const IO *__restrict__ y, int Dm, i
     const int tpb = (L + OP_T - 1) / OP_T, ntiles = tpb * nb;
     const int nk = (Di + OP_K - 1) / OP_K;
     const long long E = (long long)nb * Di * L;
-    // this thread's W chunks: lanes = 8 rows x 4 chunks of 16 bytes (one
-    // row's 64 bytes), 512 contiguous shared bytes per warp instruction
-    const IO *w_row[WC];
-    int w_dst[WC];
-    bool w_in[WC];
-#pragma unroll
-    for (int j = 0; j < WC; ++j) {
-        const int c = tid + j * OP_NT, n = c >> 2, kc = c & 3;
-        w_row[j] = W + (long long)min(n, Dm - 1) * Di + 8 * kc;
-        w_dst[j] = (n >> 3) * SBO + kc * 128 + (n & 7) * 16;
-        w_in[j] = n < Dm;
-    }
     // the copy side: slice (i_tile, i_ki) into stage i_st
     int i_tile = blockIdx.x, i_ki = 0, i_st = 0;
     long long i_row = (long long)(i_tile / tpb) * Di;          // b * Di of i_tile
@@ -1298,13 +1297,18 @@ out_proj_tc_kernel(const IO *__restrict__ W, const IO *__restrict__ y, int Dm, i
         if (i_tile >= ntiles) return;
         unsigned char *s_p = sS + (size_t)i_st * STAGE;
         const int k0 = i_ki * OP_K;
-        raw_rows_copy<OP_K, OP_NT>(s_p, y, E, i_row + k0, Di - k0, L, i_t0, tid);
+        if (tid == 0) {
+            // W columns k0 .. k0 + OP_K - 1 of every row: box (channel group
+            // kc, rows 128 c ..) to kc * NR * 16 + c * 2048
+            mbar_expect_tx(&rbars[i_st], W_BYTES);
 #pragma unroll
-        for (int j = 0; j < WC; ++j) {
-            const int kc0 = k0 + (tid & 3) * 8;                    // this chunk's first k
-            cp_async16_zfill(s_p + RAW_BYTES + w_dst[j], w_row[j] + min(k0, Di - 8 - (tid & 3) * 8),
-                             w_in[j] && kc0 < Di);
+            for (int kc = 0; kc < OP_K / 8; ++kc)
+#pragma unroll
+                for (int c = 0; c < NCH; ++c)
+                    tma_load_2d(s_p + RAW_BYTES + kc * W_LBO + c * 2048, &tmW, k0 + 8 * kc,
+                                128 * c, &rbars[i_st]);
         }
+        raw_rows_copy<OP_K, OP_NT>(s_p, y, E, i_row + k0, Di - k0, L, i_t0, tid);
         cp_async_arrive_noinc(&rbars[i_st]);
         if (++i_st == ns) i_st = 0;
         if (++i_ki == nk) {
@@ -1342,7 +1346,7 @@ out_proj_tc_kernel(const IO *__restrict__ W, const IO *__restrict__ y, int Dm, i
 #pragma unroll
                     for (int c = 0; c < NCH; ++c) {
                         const unsigned long long bd =
-                            tc_desc(w_a + c * 16 * SBO + ks * 256, 128, SBO);
+                            tc_desc(w_a + ks * 2 * W_LBO + c * 2048, W_LBO, 128);
                         tc_mma(tmem + 128 * c, ad, bd, idesc, ki > 0 || ks > 0);
                     }
                 }

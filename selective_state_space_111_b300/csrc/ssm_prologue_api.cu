@@ -4,6 +4,8 @@
 // dt_proj, producing the scan's inputs in the scan's own layouts.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -296,8 +298,60 @@ ssm_status run_ss2d(int B, int D, int H, int W, int N, int R, int Kc, const void
 
 // out_proj: the tcgen05 kernel for 16-bit I/O and d_model <= 512 (NCH
 // chunks of 128 rows), else the generic tiled projection
+// The driver's tensor-map encoder, looked up once through the runtime (the
+// library does not link the driver library itself).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return (PFN_cuTensorMapEncodeTiled_v12000)p;
+    }();
+    return fn;
+}
+
+// Tensor map of W [Dm][Di] (16-bit, 16-byte aligned, Di a multiple of 8)
+// for boxes of 8 channels x 128 rows, no swizzle, zero fill out of range.
+// A map describes memory by address and sizes only, so the last one made on
+// this host thread is reused for the same W address, sizes and dtype.
+struct WMapCache {
+    const void *W = nullptr;
+    int Dm = 0, Di = 0, f16 = 0;
+    CUtensorMap map;
+};
+thread_local WMapCache t_wmap;
+template <typename IO>
+bool out_proj_w_map(CUtensorMap *m, const IO *W, int Dm, int Di) {
+    const int f16 = std::is_same<IO, __half>::value ? 1 : 0;
+    if (t_wmap.W == (const void *)W && t_wmap.Dm == Dm && t_wmap.Di == Di && t_wmap.f16 == f16) {
+        *m = t_wmap.map;
+        return true;
+    }
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)Di, (cuuint64_t)Dm};
+    const cuuint64_t strides[1] = {(cuuint64_t)Di * sizeof(IO)};
+    const cuuint32_t box[2] = {8, 128}, estr[2] = {1, 1};
+    const CUtensorMapDataType t = std::is_same<IO, __half>::value
+                                      ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (enc(m, t, 2, (void *)W, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    t_wmap.W = W;
+    t_wmap.Dm = Dm;
+    t_wmap.Di = Di;
+    t_wmap.f16 = f16;
+    t_wmap.map = *m;
+    return true;
+}
+
 template <typename IO, int NCH>
-ssm_status launch_out_proj(int B, int Di, int Dm, int L, const void *y, const IO *W,
+ssm_status launch_out_proj(int B, int Di, int Dm, int L, const void *y, const CUtensorMap &tmW,
                            void *out, cudaStream_t st) {
     using namespace ssm::pro;
     const int ns = out_proj_stages<NCH>(kSmemOptin);
@@ -307,8 +361,8 @@ ssm_status launch_out_proj(int B, int Di, int Dm, int L, const void *y, const IO
         return SSM_ERR_CUDA;
     const long long tiles = (long long)B * ((L + OP_T - 1) / OP_T);
     const int grid = (int)std::min<long long>(tiles, sm_count());
-    out_proj_tc_kernel<IO, NCH><<<grid, OP_NT, smem, st>>>(W, (const IO *)y, Dm, Di, L, B, ns,
-                                                           (IO *)out);
+    out_proj_tc_kernel<IO, NCH><<<grid, OP_NT, smem, st>>>(tmW, (const IO *)y, Dm, Di, L, B,
+                                                           ns, (IO *)out);
     return last_error();
 }
 template <typename IO>
@@ -317,14 +371,16 @@ ssm_status out_proj_run(int B, int Di, int Dm, int L, const void *y, const void 
     using namespace ssm::pro;
     const IO *W = (const IO *)Wv;
     if constexpr (sizeof(IO) == 2) {
-        // W rows and y are copied as 16-byte chunks: Di a multiple of 8 and
-        // W 16-byte aligned, so that every W row starts on a 16-byte
-        // boundary, and y 16-byte aligned
-        if (Di % 8 == 0 && aligned(W, 16) && aligned(y, 16)) {
-            if (Dm <= 128) return launch_out_proj<IO, 1>(B, Di, Dm, L, y, W, out, st);
-            if (Dm <= 256) return launch_out_proj<IO, 2>(B, Di, Dm, L, y, W, out, st);
-            if (Dm <= 384) return launch_out_proj<IO, 3>(B, Di, Dm, L, y, W, out, st);
-            if (Dm <= OP_MAXN) return launch_out_proj<IO, 4>(B, Di, Dm, L, y, W, out, st);
+        // W goes through a tensor map (base 16-byte aligned, row pitch Di * 2
+        // bytes a multiple of 16) and y is copied as 16-byte chunks (16-byte
+        // aligned); without a tensor-map encoder the tiled kernel runs
+        CUtensorMap tmW;
+        if (Di % 8 == 0 && aligned(W, 16) && aligned(y, 16) && Dm <= OP_MAXN &&
+            out_proj_w_map<IO>(&tmW, W, Dm, Di)) {
+            if (Dm <= 128) return launch_out_proj<IO, 1>(B, Di, Dm, L, y, tmW, out, st);
+            if (Dm <= 256) return launch_out_proj<IO, 2>(B, Di, Dm, L, y, tmW, out, st);
+            if (Dm <= 384) return launch_out_proj<IO, 3>(B, Di, Dm, L, y, tmW, out, st);
+            return launch_out_proj<IO, 4>(B, Di, Dm, L, y, tmW, out, st);
         }
     }
     ProjOut o{};
