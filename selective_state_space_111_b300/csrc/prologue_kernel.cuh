@@ -1222,29 +1222,37 @@ xproj_tc_kernel(const float *__restrict__ W, const IO *__restrict__ in, int M, i
 // 2.1: out_proj = Linear(d_inner -> d_model) after the gate), as
 // D[t][m] = Y[t][k] W[m][k]: MMA M = 128 positions, N in chunks of 128 rows
 // (every d_model row of a tile: NCH chunks, 128 * NCH TMEM columns), K = 16
-// per instruction, fp32 accumulator in tensor memory.  A persistent CTA of
-// 16 warps walks one stream of slices (OP_K channels of one tile of 128
-// positions) over its tiles through a ring of `ns` stages, each holding a
-// slice's raw y rows (sixteen threads per row, cp.async) and its W columns,
-// and completing on its own mbarrier; ns - 1 slices are in flight.  W
-// arrives by tiled TMA copies (tensor map `tmW`: W [d_model][d_inner],
-// boxes of 8 channels x 128 rows, zero fill past d_model and d_inner): a
-// box lands as 128 rows x 16 bytes, i.e. 16 core matrices of the K-major
-// operand without swizzle, so the slice's W is K-major with the 8-channel
-// groups NR * 16 bytes apart (leading byte offset) and 8-row groups 128
-// bytes apart (stride byte offset).  One thread announces the W bytes on
-// the stage's mbarrier and issues the 4 * NCH copies.  Per slice: wait for the
-// stage, realign y into one of two A buffers, one thread issues the
-// slice's 2 * NCH MMAs and commits them to the buffer's mbarrier; once the
-// previous slice's MMAs are done its stage takes the slice ns - 1 ahead.
-// The epilogue reads TMEM (warp w: lanes 32 (w % 4), a quarter of the
-// columns) and stores along positions.
+// per instruction, fp32 accumulator in tensor memory.  A persistent CTA
+// walks one stream of slices (OP_K channels of one tile of 128 positions)
+// over its tiles through a ring of `ns` stages, each holding a slice's raw
+// y rows and its W columns and completing on its own mbarrier; ns - 1
+// slices are in flight.  Warp roles:
+//   * 16 worker warps: copy the raw y rows of the slice ns - 1 ahead
+//     (sixteen threads per row, cp.async, each thread arriving on the stage
+//     once its copies land), realign a landed slice into one of two A
+//     buffers (MN-major) and signal it on that buffer's "A full" mbarrier
+//     (one arrival per warp), and after a tile's last slice read TMEM
+//     (warp w: lanes 32 (w % 4), a quarter of the columns), store along
+//     positions and signal "TMEM free";
+//   * one MMA warp: per slice, once "A full", issues the slice's 2 * NCH
+//     MMAs and commits them to the A buffer's mbarrier; once the previous
+//     slice's MMAs are done it refills that stage's W by tiled TMA copies
+//     (tensor map `tmW`: W [d_model][d_inner], boxes of 8 channels x 128
+//     rows, zero fill past d_model and d_inner; a box lands as 128 rows x 16
+//     bytes, i.e. 16 core matrices of the K-major operand without swizzle,
+//     so the slice's W is K-major with the 8-channel groups NR * 16 bytes
+//     apart and 8-row groups 128 bytes apart), announcing the bytes with its
+//     own arrival on the stage; before a tile's first MMA it waits for
+//     "TMEM free" of the tile before.
+// No CTA-wide barrier inside the loop: every hand-off is an mbarrier, and
+// every wait is bounded.
 constexpr int OP_T = 128, OP_K = 32, OP_NT = 512, OP_MAXN = 512, OP_MAXNS = 8;
+constexpr int OP_THREADS = OP_NT + 32;                      // workers + the MMA warp
 template <int NCH> __host__ __device__ constexpr size_t out_proj_stage_bytes() {
     return (size_t)OP_K * RAW_ROW + (size_t)NCH * 128 * OP_K * 2;
 }
 template <int NCH> __host__ __device__ constexpr size_t out_proj_fixed_bytes() {
-    return 2 * (size_t)mn_tile_bytes(OP_K) + 8 * (2 + OP_MAXNS) + 16;
+    return 2 * (size_t)mn_tile_bytes(OP_K) + 8 * (5 + OP_MAXNS) + 16;
 }
 template <int NCH> inline int out_proj_stages(size_t smem_max) {
     const size_t fixed = out_proj_fixed_bytes<NCH>();
@@ -1256,7 +1264,7 @@ template <int NCH> inline size_t out_proj_smem_bytes(int ns) {
     return out_proj_fixed_bytes<NCH>() + (size_t)ns * out_proj_stage_bytes<NCH>();
 }
 template <typename IO, int NCH>
-__global__ void __launch_bounds__(OP_NT, 1)
+__global__ void __launch_bounds__(OP_THREADS, 1)
 out_proj_tc_kernel(const __grid_constant__ CUtensorMap tmW, const IO *__restrict__ y, int Dm,
                    int Di, int L, int nb, int ns, IO *__restrict__ out) {
     static_assert(sizeof(IO) == 2, "16-bit I/O");
@@ -1268,102 +1276,135 @@ out_proj_tc_kernel(const __grid_constant__ CUtensorMap tmW, const IO *__restrict
     constexpr unsigned W_BYTES = NR * OP_K * 2;
     unsigned char *sA = op_smem;                                // [2] A tiles (MN-major)
     unsigned char *sS = sA + 2 * A_BYTES;                       // [ns] stages: raw y, W
-    uint64_t *mbars = (uint64_t *)(sS + (size_t)ns * STAGE);    // one per A buffer
-    uint64_t *rbars = mbars + 2;                                // one per stage
+    uint64_t *mbars = (uint64_t *)(sS + (size_t)ns * STAGE);    // MMA done, per A buffer
+    uint64_t *afull = mbars + 2;                                // A written, per A buffer
+    uint64_t *tfree = afull + 2;                                // TMEM read by the epilogue
+    uint64_t *rbars = tfree + 1;                                // stage landed, per stage
     unsigned *tslot = (unsigned *)(rbars + OP_MAXNS);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool mma_warp = warp == OP_NT / 32;
     constexpr unsigned TCOLS = NR <= 128 ? 128 : NR <= 256 ? 256 : 512;
-    if (warp == 0) tc_alloc(tslot, TCOLS);
+    if (mma_warp) tc_alloc(tslot, TCOLS);
     if (tid == 0) {
         mbar_init(&mbars[0], 1);
         mbar_init(&mbars[1], 1);
-        // per use: one arrival (cp.async tracking) per thread
-        for (int s = 0; s < ns; ++s) mbar_init(&rbars[s], OP_NT);
+        mbar_init(&afull[0], OP_NT / 32);
+        mbar_init(&afull[1], OP_NT / 32);
+        mbar_init(tfree, OP_NT / 32);
+        // per use: one arrival (cp.async tracking) per worker thread and the
+        // MMA warp's arrival announcing the W bytes
+        for (int s = 0; s < ns; ++s) mbar_init(&rbars[s], OP_NT + 1);
         fence_barrier_init();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const unsigned tmem = *tslot;
-    const unsigned idesc = tc_idesc<IO>(128, 128, true);
     const int tpb = (L + OP_T - 1) / OP_T, ntiles = tpb * nb;
     const int nk = (Di + OP_K - 1) / OP_K;
     const long long E = (long long)nb * Di * L;
-    // the copy side: slice (i_tile, i_ki) into stage i_st
-    int i_tile = blockIdx.x, i_ki = 0, i_st = 0;
-    long long i_row = (long long)(i_tile / tpb) * Di;          // b * Di of i_tile
-    int i_t0 = (i_tile % tpb) * OP_T;
-    auto issue = [&]() {
-        if (i_tile >= ntiles) return;
-        unsigned char *s_p = sS + (size_t)i_st * STAGE;
-        const int k0 = i_ki * OP_K;
-        if (tid == 0) {
-            // W columns k0 .. k0 + OP_K - 1 of every row: box (channel group
-            // kc, rows 128 c ..) to kc * NR * 16 + c * 2048
-            mbar_expect_tx(&rbars[i_st], W_BYTES);
+    bool ok = true;                    // every wait finished in time
+    if (mma_warp) {
+        if (lane == 0) {
+            const unsigned idesc = tc_idesc<IO>(128, 128, true);
+            // the W side of the copies: slice (i_ki of any tile) into stage i_st
+            int i_tile = blockIdx.x, i_ki = 0, i_st = 0;
+            auto issue_w = [&]() {
+                if (i_tile >= ntiles) return;
+                unsigned char *w_s = sS + (size_t)i_st * STAGE + RAW_BYTES;
+                mbar_arrive_expect_tx(&rbars[i_st], W_BYTES);
 #pragma unroll
-            for (int kc = 0; kc < OP_K / 8; ++kc)
+                for (int kc = 0; kc < OP_K / 8; ++kc)
 #pragma unroll
-                for (int c = 0; c < NCH; ++c)
-                    tma_load_2d(s_p + RAW_BYTES + kc * W_LBO + c * 2048, &tmW, k0 + 8 * kc,
-                                128 * c, &rbars[i_st]);
-        }
-        raw_rows_copy<OP_K, OP_NT>(s_p, y, E, i_row + k0, Di - k0, L, i_t0, tid);
-        cp_async_arrive_noinc(&rbars[i_st]);
-        if (++i_st == ns) i_st = 0;
-        if (++i_ki == nk) {
-            i_ki = 0;
-            i_tile += gridDim.x;
-            i_row = (long long)(i_tile / tpb) * Di;
-            i_t0 = (i_tile % tpb) * OP_T;
-        }
-    };
-    for (int g = 0; g + 1 < ns; ++g) issue();
-    bool ok = true;
-    int g = 0, st = 0;                 // slices consumed, their stage
-    unsigned rpar = 0;                 // phase parity of the stages' current use
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-        const int b = tile / tpb, t0 = (tile % tpb) * OP_T;
-        const long long row_b = (long long)b * Di;
-        for (int ki = 0; ki < nk; ++ki, ++g) {
-            const int buf = g & 1;
-            unsigned char *a_s = sA + buf * A_BYTES;
-            const unsigned char *s_p = sS + (size_t)st * STAGE;
-            // (the mma that last read this A buffer, slice g - 2, was waited
-            // for before the previous slice's stage was refilled)
-            ok &= mbar_wait_bounded(&rbars[st], rpar);
-            raw_rows_realign<OP_K, OP_NT>(s_p, a_s, row_b + ki * OP_K, L, t0, tid);
-            fence_proxy_async_shared();
-            tc_fence_before();
-            __syncthreads();
-            tc_fence_after();
-            if (tid == 0) {
-                const unsigned w_a = smem_addr(s_p + RAW_BYTES);
-#pragma unroll
-                for (int ks = 0; ks < OP_K / 16; ++ks) {
-                    const unsigned long long ad =
-                        tc_desc(smem_addr(a_s) + ks * 2 * MN_KSTR, MN_KSTR, MN_MSTR);
-#pragma unroll
-                    for (int c = 0; c < NCH; ++c) {
-                        const unsigned long long bd =
-                            tc_desc(w_a + ks * 2 * W_LBO + c * 2048, W_LBO, 128);
-                        tc_mma(tmem + 128 * c, ad, bd, idesc, ki > 0 || ks > 0);
-                    }
+                    for (int c = 0; c < NCH; ++c)
+                        tma_load_2d(w_s + kc * W_LBO + c * 2048, &tmW, i_ki * OP_K + 8 * kc,
+                                    128 * c, &rbars[i_st]);
+                if (++i_st == ns) i_st = 0;
+                if (++i_ki == nk) {
+                    i_ki = 0;
+                    i_tile += gridDim.x;
                 }
-                tc_commit(&mbars[buf]);
-            }
-            // the previous slice's mma is done: its stage takes slice g + ns - 1
-            if (g >= 1) ok &= mbar_wait_bounded(&mbars[buf ^ 1], (unsigned)(((g - 1) >> 1) & 1));
-            issue();
-            if (++st == ns) {
-                st = 0;
-                rpar ^= 1u;
+            };
+            for (int g = 0; g + 1 < ns; ++g) issue_w();
+            int g = 0, st = 0, nt = 0;
+            for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++nt) {
+                // the epilogue of the tile before has read TMEM
+                if (nt > 0) ok &= mbar_wait_bounded(tfree, (unsigned)((nt - 1) & 1));
+                for (int ki = 0; ki < nk; ++ki, ++g) {
+                    const int buf = g & 1;
+                    ok &= mbar_wait_bounded(&afull[buf], (unsigned)((g >> 1) & 1));
+                    tc_fence_after();
+                    const unsigned a_a = smem_addr(sA + buf * A_BYTES);
+                    const unsigned w_a = smem_addr(sS + (size_t)st * STAGE + RAW_BYTES);
+#pragma unroll
+                    for (int ks = 0; ks < OP_K / 16; ++ks) {
+                        const unsigned long long ad =
+                            tc_desc(a_a + ks * 2 * MN_KSTR, MN_KSTR, MN_MSTR);
+#pragma unroll
+                        for (int c = 0; c < NCH; ++c) {
+                            const unsigned long long bd =
+                                tc_desc(w_a + ks * 2 * W_LBO + c * 2048, W_LBO, 128);
+                            tc_mma(tmem + 128 * c, ad, bd, idesc, ki > 0 || ks > 0);
+                        }
+                    }
+                    tc_commit(&mbars[buf]);
+                    // the previous slice's MMAs are done: its stage takes the
+                    // W of slice g + ns - 1
+                    if (g >= 1)
+                        ok &= mbar_wait_bounded(&mbars[buf ^ 1], (unsigned)(((g - 1) >> 1) & 1));
+                    issue_w();
+                    if (++st == ns) st = 0;
+                }
             }
         }
-        // the tile's last slice (and so every earlier one) is done
-        ok &= mbar_wait_bounded(&mbars[(g - 1) & 1], (unsigned)(((g - 1) >> 1) & 1));
-        tc_fence_after();
-        {
+        __syncwarp();
+    } else {
+        // the y side of the copies: slice (i_tile, i_ki) into stage i_st
+        int i_tile = blockIdx.x, i_ki = 0, i_st = 0;
+        long long i_row = (long long)(i_tile / tpb) * Di;      // b * Di of i_tile
+        int i_t0 = (i_tile % tpb) * OP_T;
+        auto issue_y = [&]() {
+            if (i_tile >= ntiles) return;
+            const int k0 = i_ki * OP_K;
+            raw_rows_copy<OP_K, OP_NT>(sS + (size_t)i_st * STAGE, y, E, i_row + k0, Di - k0, L,
+                                       i_t0, tid);
+            cp_async_arrive_noinc(&rbars[i_st]);
+            if (++i_st == ns) i_st = 0;
+            if (++i_ki == nk) {
+                i_ki = 0;
+                i_tile += gridDim.x;
+                i_row = (long long)(i_tile / tpb) * Di;
+                i_t0 = (i_tile % tpb) * OP_T;
+            }
+        };
+        for (int g = 0; g + 1 < ns; ++g) issue_y();
+        int g = 0, st = 0;             // slices consumed, their stage
+        unsigned rpar = 0;             // phase parity of the stages' current use
+        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+            const int b = tile / tpb, t0 = (tile % tpb) * OP_T;
+            const long long row_b = (long long)b * Di;
+            for (int ki = 0; ki < nk; ++ki, ++g) {
+                const int buf = g & 1;
+                ok &= mbar_wait_bounded(&rbars[st], rpar);
+                // the MMAs that last read this A buffer (slice g - 2) are done
+                if (g >= 2) ok &= mbar_wait_bounded(&mbars[buf], (unsigned)(((g - 2) >> 1) & 1));
+                raw_rows_realign<OP_K, OP_NT>(sS + (size_t)st * STAGE, sA + buf * A_BYTES,
+                                              row_b + ki * OP_K, L, t0, tid);
+                fence_proxy_async_shared();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&afull[buf]);
+                // the previous slice's MMAs are done (and so every warp has
+                // realigned it): its stage takes the y rows of slice g + ns - 1
+                if (g >= 1) ok &= mbar_wait_bounded(&mbars[buf ^ 1], (unsigned)(((g - 1) >> 1) & 1));
+                issue_y();
+                if (++st == ns) {
+                    st = 0;
+                    rpar ^= 1u;
+                }
+            }
+            // the tile's last slice (and so every earlier one) is done
+            ok &= mbar_wait_bounded(&mbars[(g - 1) & 1], (unsigned)(((g - 1) >> 1) & 1));
+            tc_fence_after();
             // warp w: TMEM lanes (positions) 32 (w % 4) .., columns (rows)
             // (w / 4) * NR / 4 .. + NR / 4
             const int q4 = warp % 4, tp = t0 + 32 * q4 + lane;
@@ -1380,16 +1421,17 @@ out_proj_tc_kernel(const __grid_constant__ CUtensorMap tmW, const IO *__restrict
                             out[((long long)b * Dm + m0 + q) * L + tp] = from_f32<IO>(v[q]);
                 }
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tfree);
         }
-        // every warp has read TMEM before the next tile's first mma overwrites it
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
+        cp_async_wait_all();
     }
     (void)ok;
-    cp_async_wait_all();
+    tc_fence_before();
     __syncthreads();
-    if (warp == 0) tc_dealloc(tmem, TCOLS);
+    tc_fence_after();
+    if (mma_warp) tc_dealloc(tmem, TCOLS);
 }
 
 // SS2D x_proj for all four scan directions in one pass over u (16-bit I/O,

@@ -361,8 +361,8 @@ ssm_status launch_out_proj(int B, int Di, int Dm, int L, const void *y, const CU
         return SSM_ERR_CUDA;
     const long long tiles = (long long)B * ((L + OP_T - 1) / OP_T);
     const int grid = (int)std::min<long long>(tiles, sm_count());
-    out_proj_tc_kernel<IO, NCH><<<grid, OP_NT, smem, st>>>(tmW, (const IO *)y, Dm, Di, L, B,
-                                                           ns, (IO *)out);
+    out_proj_tc_kernel<IO, NCH><<<grid, OP_THREADS, smem, st>>>(tmW, (const IO *)y, Dm, Di, L,
+                                                                B, ns, (IO *)out);
     return last_error();
 }
 template <typename IO>
