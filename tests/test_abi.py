@@ -120,6 +120,26 @@ def test_bwd_workspace_bytes(lib):
     assert single >= 4 * n + 2 * 40 * 10 * 16 * 4 + 2 * 3 * 2 * 300 * 16 * 4
 
 
+def test_bwd_context_bytes(lib):
+    # the saved backward context: the pre-gate output in the I/O dtype, then
+    # per direction the fp32 states [B][D][ceil(L / 8)][16], each region
+    # rounded up to 256 bytes
+    cb = lib.ssm_bwd_context_bytes
+    neg = ctypes.c_size_t(-1).value
+    up = lambda x: (x + 255) // 256 * 256
+    B, D, L = 2, 40, 301
+    hc = up(B * D * ((L + 7) // 8) * 16 * 4)
+    assert cb(0, 1, B, D, L, 16) == up(B * D * L * 2) + hc          # single, bf16
+    assert cb(2, 0, B, D, L, 16) == up(B * D * L * 4) + 2 * hc      # v2, fp32
+    assert cb(1, 2, B, D, L, 8) == up(B * D * L * 2) + 2 * hc       # v1, fp16, N < 16
+    assert cb(2, 1, B, D, L, 24) == 0                                # past 16 states: none
+    assert cb(2, 1, 0, D, L, 16) == 0                                # empty problem
+    assert cb(3, 1, B, D, L, 16) == neg                              # SS2D keeps no context
+    assert cb(2, 7, B, D, L, 16) == neg                              # bad dtype
+    assert cb(2, 1, B, D, L, 33) == neg                              # N > 32
+    lib.ssm_set_bwd_context(None, 0)                                 # clearing is always valid
+
+
 def bwd_single(lib, *, dt=1, B=1, D=1, L=8, N=16, u=FAKE, z=None, dz=None, du=FAKE,
                ws=None, ws_bytes=0):
     return lib.selective_scan_bwd(dt, B, D, L, N, u, FAKE, FAKE, FAKE, FAKE, None, z, None, 1,
