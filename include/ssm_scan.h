@@ -499,9 +499,12 @@ SSM_API size_t ss2d_prologue_workspace_bytes(int B, int H, int W, int R);
  * y [B, Di, L] (the gated output of a scan call), W_out [Dm, Di] and out
  * [B, Dm, L], all in the I/O dtype; device pointers, caller-owned.
  * Arithmetic: fp32 accumulation; with 16-bit I/O, Dm <= 512, Di a multiple
- * of 8 and W_out 16-byte aligned on the tcgen05 tensor cores (fp32
- * accumulator in tensor memory), otherwise tiled (mma.sync for 16-bit I/O,
- * fp32 FMA for fp32 I/O); out is rounded to the I/O dtype.  No workspace.
+ * of 8 and y and W_out 16-byte aligned on the tcgen05 tensor cores (fp32
+ * accumulator in tensor memory; W_out read through a TMA tensor map that
+ * the call encodes and caches per host thread), otherwise tiled (mma.sync
+ * for 16-bit I/O, fp32 FMA for fp32 I/O); out is rounded to the I/O dtype.
+ * The result does not depend on which kernel runs beyond fp32 summation
+ * order.  No workspace.
  * Errors: SSM_ERR_INVALID_ARG for a bad dtype, size or pointer (NULL or
  * misaligned); SSM_ERR_UNSUPPORTED for B > 65535 or Di * L, Dm * L or
  * Dm * Di past the 32-bit index range; SSM_ERR_CUDA for a launch error.  Asynchronous on
