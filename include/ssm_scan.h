@@ -49,7 +49,9 @@
  *    (ssm_set_bwd_context) and the one-launch test hooks
  *    (ssm_test_withhold_copy, ssm_test_shrink_extents).  (The backward
  *    calls also set, and clear before returning, a per-thread request that
- *    the forward run inside them store its chunk-start states.)
+ *    the forward run inside them store its chunk-start states; and
+ *    out_proj_fwd keeps, per host thread, the TMA tensor map it last made,
+ *    reused for the same W_out address, sizes and dtype.)
  *  - Errors: SSM_ERR_INVALID_ARG for a bad size, NULL required pointer or
  *    misaligned pointer; SSM_ERR_UNSUPPORTED for N > 32, K != 4 or sizes
  *    beyond the 32-bit index range; SSM_ERR_WORKSPACE when ws_bytes is too
