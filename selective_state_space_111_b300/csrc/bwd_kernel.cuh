@@ -888,16 +888,26 @@ __global__ void convert_kernel(const float *__restrict__ a, const float *__restr
 
 // dB[b][n][s] (I/O, at out + b * out_bstride) = sum over the nslot partials
 // [slot][B][L][nm] (slot-major; a fixed summation order, so the result is
-// the same on every run).  CTA = 256 / (nm / 4) positions of one batch
-// element: thread = (position, group of four states), 16-byte loads of the
-// partials; the sums are transposed through shared memory so each state's
-// row of positions is stored contiguously.
+// the same on every run).  One launch reduces up to eight tensors (jobs,
+// grid z).  CTA = 256 / (nm / 4) positions of one batch element: thread =
+// (position, group of four states), 16-byte loads of the partials, twelve
+// in flight, added in slot order; the sums are transposed through shared
+// memory so each state's row of positions is stored contiguously.
+struct BcJobs {
+    const float *part[8];
+    void *out[8];
+    int nslot[8];
+    long long out_bstride;
+};
 template <typename IO, int NM>
 __global__ void __launch_bounds__(256)
-reduce_bc_kernel(const float *__restrict__ part, int nslot, int B, int L, int N,
-                 IO *__restrict__ out, long long out_bstride) {
+reduce_bc_kernel(const BcJobs J, int B, int L, int N) {
     constexpr int QN = NM / 4, PS = 256 / QN;           // quads per position, positions per CTA
+    constexpr int KB = 12;                               // partial loads in flight
     __shared__ float tile[NM][PS + 1];
+    const float *part = J.part[blockIdx.z];
+    IO *out = (IO *)J.out[blockIdx.z];
+    const int nslot = J.nslot[blockIdx.z];
     const int b = blockIdx.y, s0 = blockIdx.x * PS;
     const int t = threadIdx.x, sl = t / QN, q = t % QN, s = s0 + sl;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -905,13 +915,20 @@ reduce_bc_kernel(const float *__restrict__ part, int nslot, int B, int L, int N,
         const float4 *src = reinterpret_cast<const float4 *>(part) +
                             (((long long)b * L + s) * NM) / 4 + q;
         const long long slot_stride = (long long)B * L * NM / 4;
-#pragma unroll 8
-        for (int k = 0; k < nslot; ++k) {
-            const float4 v = src[k * slot_stride];
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
+        for (int k0 = 0; k0 < nslot; k0 += KB) {
+            float4 v[KB];
+#pragma unroll
+            for (int k = 0; k < KB; ++k)
+                if (k0 + k < nslot) v[k] = src[(k0 + k) * slot_stride];
+#pragma unroll
+            for (int k = 0; k < KB; ++k) {
+                if (k0 + k < nslot) {
+                    acc.x += v[k].x;
+                    acc.y += v[k].y;
+                    acc.z += v[k].z;
+                    acc.w += v[k].w;
+                }
+            }
         }
     }
     tile[4 * q][sl] = acc.x;
@@ -921,7 +938,8 @@ reduce_bc_kernel(const float *__restrict__ part, int nslot, int B, int L, int N,
     __syncthreads();
     for (int i = t; i < N * PS; i += 256) {
         const int nn = i / PS, j = i % PS;
-        if (s0 + j < L) out[b * out_bstride + (long long)nn * L + s0 + j] = from_f32<IO>(tile[nn][j]);
+        if (s0 + j < L)
+            out[b * J.out_bstride + (long long)nn * L + s0 + j] = from_f32<IO>(tile[nn][j]);
     }
 }
 

@@ -192,18 +192,17 @@ ssm_status convert(const float *a, const float *b, const float *c, void *out, lo
 }
 
 template <typename IO>
-ssm_status reduce_bc(const float *part, int nslot, int B, int L, int N, void *out,
-                     long long out_bstride, cudaStream_t st) {
-    if (B == 0 || L == 0) return SSM_OK;
+ssm_status reduce_bc(const ssm::bwd::BcJobs &J, int njobs, int B, int L, int N,
+                     cudaStream_t st) {
+    if (B == 0 || L == 0 || njobs == 0) return SSM_OK;
     if (N <= ssm::kMaxN) {
         constexpr int PS = 256 / (ssm::kMaxN / 4);
-        ssm::bwd::reduce_bc_kernel<IO, ssm::kMaxN><<<dim3((L + PS - 1) / PS, B), 256, 0, st>>>(
-            part, nslot, B, L, N, (IO *)out, out_bstride);
+        ssm::bwd::reduce_bc_kernel<IO, ssm::kMaxN>
+            <<<dim3((L + PS - 1) / PS, B, njobs), 256, 0, st>>>(J, B, L, N);
     } else {
         constexpr int PS = 256 / (2 * ssm::kMaxN / 4);
         ssm::bwd::reduce_bc_kernel<IO, 2 * ssm::kMaxN>
-            <<<dim3((L + PS - 1) / PS, B), 256, 0, st>>>(part, nslot, B, L, N, (IO *)out,
-                                                         out_bstride);
+            <<<dim3((L + PS - 1) / PS, B, njobs), 256, 0, st>>>(J, B, L, N);
     }
     return last_error();
 }
@@ -386,11 +385,19 @@ ssm_status seq_bwd(int op, int B, int D, int L, int N, const void *u, const void
     }
     const Parts q = parts_of(ws, w, B, D, L, N);
     const int shared_bc = op == 1 ? 2 : 1;      // v1: both passes add into dB, dC
-    TRY(reduce_bc<IO>(q.dB_slot(0), shared_bc * q.ncg, B, L, N, dB, NL, st));
-    TRY(reduce_bc<IO>(q.dC_slot(0), shared_bc * q.ncg, B, L, N, dC, NL, st));
-    if (op == 2) {
-        TRY(reduce_bc<IO>(q.dB_slot(1), q.ncg, B, L, N, dB_b, NL, st));
-        TRY(reduce_bc<IO>(q.dC_slot(1), q.ncg, B, L, N, dC_b, NL, st));
+    {
+        // dB, dC (and for v2 dB_b, dC_b) in one launch
+        ssm::bwd::BcJobs J{};
+        J.out_bstride = NL;
+        const float *parts[4] = {q.dB_slot(0), q.dC_slot(0), op == 2 ? q.dB_slot(1) : nullptr,
+                                 op == 2 ? q.dC_slot(1) : nullptr};
+        void *outs[4] = {dB, dC, dB_b, dC_b};
+        for (int j = 0; j < (op == 2 ? 4 : 2); ++j) {
+            J.part[j] = parts[j];
+            J.out[j] = outs[j];
+            J.nslot[j] = j < 2 ? shared_bc * q.ncg : q.ncg;
+        }
+        TRY(reduce_bc<IO>(J, op == 2 ? 4 : 2, B, L, N, st));
     }
     TRY(reduce_param(q.dA_slot(0), 1, B, D, N, true, dA, st));
     if (op != 0) TRY(reduce_param(q.dA_slot(1), 1, B, D, N, true, dA_b, st));
@@ -481,9 +488,20 @@ ssm_status ss2d_bwd_run(int B, int D, int H, int W, int N, const void *x, const 
     if (!capture)
         TRY(convert<IO>((const float *)(ws + w.ddt), nullptr, nullptr, ddelta, n * K, st));
     const Parts q = parts_of(ws, w, B, D, L, N);
+    {
+        // the four directions' dB and dC in one launch
+        ssm::bwd::BcJobs J{};
+        J.out_bstride = K * NL;
+        for (int k = 0; k < K; ++k) {
+            J.part[2 * k] = q.dB_slot(k);
+            J.out[2 * k] = (IO *)dB + k * NL;
+            J.part[2 * k + 1] = q.dC_slot(k);
+            J.out[2 * k + 1] = (IO *)dC + k * NL;
+            J.nslot[2 * k] = J.nslot[2 * k + 1] = q.ncg;
+        }
+        TRY(reduce_bc<IO>(J, 2 * K, B, L, N, st));
+    }
     for (int k = 0; k < K; ++k) {
-        TRY(reduce_bc<IO>(q.dB_slot(k), q.ncg, B, L, N, (IO *)dB + k * NL, K * NL, st));
-        TRY(reduce_bc<IO>(q.dC_slot(k), q.ncg, B, L, N, (IO *)dC + k * NL, K * NL, st));
         TRY(reduce_param(q.dA_slot(k), 1, B, D, N, true, dA + (long long)k * D * N, st));
         if (capture) {
             // the kernel's channel sums: every direction visits every
