@@ -943,8 +943,20 @@ reduce_bc_kernel(const BcJobs J, int B, int L, int N) {
     }
 }
 
-__global__ void reduce_param_kernel(const float *__restrict__ part, int nslot, int B, int D,
-                                    int N, int nm, int per_state, float *__restrict__ out) {
+// Parameter gradients: out = sum over nslot x B partial rows of cols
+// values (per_state: [D][nm] rows whose columns past N are padding, stored
+// as [D][N]); up to twelve reductions (jobs, grid y) in one launch, each
+// summed in the same fixed order.
+struct ParamJobs {
+    const float *part[12];
+    float *out[12];
+    int nslot[12];
+    int per_state[12];
+};
+__global__ void reduce_param_kernel(const ParamJobs J, int B, int D, int N, int nm) {
+    const float *part = J.part[blockIdx.y];
+    float *out = J.out[blockIdx.y];
+    const int nslot = J.nslot[blockIdx.y], per_state = J.per_state[blockIdx.y];
     const int cols = per_state ? D * nm : D;
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < cols; i += gridDim.x * blockDim.x) {
         if (per_state && i % nm >= N) continue;

@@ -217,12 +217,27 @@ ssm_status channel_sum(const float *a, const float *a2, long long a_bstride, con
     return last_error();
 }
 
-ssm_status reduce_param(const float *part, int nslot, int B, int D, int N, bool per_state,
-                        float *out, cudaStream_t st) {
-    if (out == nullptr) return SSM_OK;
-    const int cols = per_state ? D * nm_of(N) : D;
-    ssm::bwd::reduce_param_kernel<<<grid1d(cols), 256, 0, st>>>(part, nslot, B, D, N, nm_of(N),
-                                                                per_state ? 1 : 0, out);
+// Parameter-gradient reductions gathered for one launch (null outputs are
+// skipped).
+struct ParamList {
+    ssm::bwd::ParamJobs J{};
+    int n = 0;
+    bool per_state_any = false;
+    void add(const float *part, int nslot, bool per_state, float *out) {
+        if (out == nullptr) return;
+        J.part[n] = part;
+        J.out[n] = out;
+        J.nslot[n] = nslot;
+        J.per_state[n] = per_state ? 1 : 0;
+        per_state_any = per_state_any || per_state;
+        ++n;
+    }
+};
+ssm_status reduce_params(const ParamList &pl, int B, int D, int N, cudaStream_t st) {
+    if (pl.n == 0) return SSM_OK;
+    const int cols = pl.per_state_any ? D * nm_of(N) : D;
+    dim3 grid(grid1d(cols), pl.n);
+    ssm::bwd::reduce_param_kernel<<<grid, 256, 0, st>>>(pl.J, B, D, N, nm_of(N));
     return last_error();
 }
 
@@ -399,24 +414,27 @@ ssm_status seq_bwd(int op, int B, int D, int L, int N, const void *u, const void
         }
         TRY(reduce_bc<IO>(J, op == 2 ? 4 : 2, B, L, N, st));
     }
-    TRY(reduce_param(q.dA_slot(0), 1, B, D, N, true, dA, st));
-    if (op != 0) TRY(reduce_param(q.dA_slot(1), 1, B, D, N, true, dA_b, st));
+    // dA of each direction; with 16 states also dD and dbias from the
+    // kernel's per-(direction, batch) channel sums -- one launch
+    ParamList pl;
+    pl.add(q.dA_slot(0), 1, true, dA);
+    if (op != 0) pl.add(q.dA_slot(1), 1, true, dA_b);
     // dD: each branch's skip term is D * u_t at every position, so
     // dD = gscale * sum G u (v1: both branches, shared D); dbias = sum ddt
     const float gs = op == 0 ? 1.f : out_scale;
     if (fused) {
-        // the kernel's per-(direction, batch) channel sums (G already
-        // carries gscale); v1 adds both directions
+        // (G already carries gscale; v1 adds both directions)
         const float *pb = p0.pbias, *pd = p0.pdD;
         const int nsum = op == 1 ? 2 : 1;
-        if (Dskip) TRY(reduce_param(pd, nsum, B, D, N, false, dD, st));
-        TRY(reduce_param(pb, nsum, B, D, N, false, dbias, st));
+        if (Dskip) pl.add(pd, nsum, false, dD);
+        pl.add(pb, nsum, false, dbias);
         if (op == 2) {
-            if (D_b) TRY(reduce_param(pd + (size_t)B * D, 1, B, D, N, false, dD_b, st));
-            TRY(reduce_param(pb + (size_t)B * D, 1, B, D, N, false, dbias_b, st));
+            if (D_b) pl.add(pd + (size_t)B * D, 1, false, dD_b);
+            pl.add(pb + (size_t)B * D, 1, false, dbias_b);
         }
-        return SSM_OK;
+        return reduce_params(pl, B, D, N, st);
     }
+    TRY(reduce_params(pl, B, D, N, st));
     if (Dskip) TRY(channel_sum<IO>(G, nullptr, DL, u, B, D, L, op == 1 ? 2.f * gs : gs, dD, st));
     TRY(channel_sum<IO>(dt0, op == 1 ? dt1 : nullptr, DL, nullptr, B, D, L, 1.f, dbias, st));
     if (op == 2) {
@@ -501,15 +519,14 @@ ssm_status ss2d_bwd_run(int B, int D, int H, int W, int N, const void *x, const 
         }
         TRY(reduce_bc<IO>(J, 2 * K, B, L, N, st));
     }
+    ParamList pl;
     for (int k = 0; k < K; ++k) {
-        TRY(reduce_param(q.dA_slot(k), 1, B, D, N, true, dA + (long long)k * D * N, st));
+        pl.add(q.dA_slot(k), 1, true, dA + (long long)k * D * N);
         if (capture) {
             // the kernel's channel sums: every direction visits every
             // position once, so its sum of G * x is dD_k
-            if (Dskip)
-                TRY(reduce_param(pp[k].pdD, 1, B, D, N, false, dD ? dD + k * D : nullptr, st));
-            TRY(reduce_param(pp[k].pbias, 1, B, D, N, false, dbias ? dbias + k * D : nullptr,
-                             st));
+            if (Dskip) pl.add(pp[k].pdD, 1, false, dD ? dD + k * D : nullptr);
+            pl.add(pp[k].pbias, 1, false, dbias ? dbias + k * D : nullptr);
             continue;
         }
         // every direction visits every position once: dD_k = sum G x
@@ -518,7 +535,7 @@ ssm_status ss2d_bwd_run(int B, int D, int H, int W, int N, const void *x, const 
         TRY(channel_sum<IO>((const float *)(ws + w.ddt) + k * DL, nullptr, K * DL, nullptr, B, D,
                             L, 1.f, dbias ? dbias + k * D : nullptr, st));
     }
-    return SSM_OK;
+    return reduce_params(pl, B, D, N, st);
 }
 
 }  // namespace
