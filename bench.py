@@ -349,9 +349,7 @@ def run_ours(args):
     # select their launches (ncu --nvtx --nvtx-include "backward/")
     bwd = None
     if not args.no_backward:
-        torch.cuda.nvtx.range_push("backward")
         bwd = measure_backward(ssm, spec, g, t, dev, stream, max(3, min(args.steps, 20)))
-        torch.cuda.nvtx.range_pop()
     pro = None
     if not args.no_prologue:
         torch.cuda.nvtx.range_push("prologue")
@@ -500,6 +498,7 @@ def measure_backward(ssm, spec, g, t, dev, stream, steps):
         return ssm.ss2d_scan_bwd(dout, g["x"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"],
                                  g["delta_bias"], sp, workspace=ws)
 
+    torch.cuda.nvtx.range_push("backward")
     for _ in range(3):
         once()
     torch.cuda.synchronize()
@@ -509,6 +508,7 @@ def measure_backward(ssm, spec, g, t, dev, stream, steps):
         once()
     e1.record(stream)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     ms = e0.elapsed_time(e1) / steps
     res = {"ms_per_call": round(ms, 4), "ms": ms, "steps": steps,
            "bytes_per_call": spec.backward_bytes(),
@@ -516,7 +516,9 @@ def measure_backward(ssm, spec, g, t, dev, stream, steps):
     if spec.op in ("single", "v1", "v2") and spec.N <= 16:
         # the training pairing: the forward call leaves the backward's context
         # (pre-gate output, chunk-start states) and the backward call reads it
-        # instead of running the forward pass again; both timed
+        # instead of running the forward pass again; both timed (in an NVTX
+        # range of their own)
+        torch.cuda.nvtx.range_push("backward_from_context")
         n = ssm.bwd_context_bytes(spec.op, dout.dtype, spec.B, spec.D, L, spec.N)
         ctx = torch.empty(n, dtype=torch.uint8, device=dev)
         fws = torch.empty(max(16, ssm.workspace_bytes(spec.op, dout.dtype, spec.B, spec.D, L,
@@ -543,6 +545,7 @@ def measure_backward(ssm, spec, g, t, dev, stream, steps):
             b_ms = e0.elapsed_time(e1) / steps
         finally:
             ssm.set_bwd_context(None)
+            torch.cuda.nvtx.range_pop()
         res["from_context"] = {"ms_per_call": round(b_ms, 4), "ms": b_ms,
                                "forward_ms_per_call": round(f_ms, 4), "context_bytes": n}
     return res
